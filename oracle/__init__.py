@@ -1,0 +1,166 @@
+"""CPU oracle for Conv2d dgrad -- TEST INFRASTRUCTURE ONLY.
+
+A ctypes wrapper around ``oracle.c``: the plain double-precision statement of
+the operation the GPU library computes (the gradient of a cross-correlation
+Conv2d with respect to its input, "Conv2d dgrad" in apache/tvm PR #10110).
+
+Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
+leg may import this package.  The GPU library never touches it; the two share
+no code.  Arrays are numpy: fp16/bf16 tensors are passed as ``uint16`` bit
+patterns, fp32 as ``float32`` and fp64 as ``float64``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = os.path.join(HERE, "oracle.c")
+LIB = os.path.join(HERE, "liboracle.so")
+
+F16, BF16, F32, F64 = 0, 1, 2, 3
+DTYPE_CODES = {"f16": F16, "bf16": BF16, "f32": F32, "f64": F64}
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so (gcc, OpenMP) if missing or stale."""
+    if (not force and os.path.exists(LIB)
+            and os.path.getmtime(LIB) >= os.path.getmtime(SRC)):
+        return LIB
+    tmp = LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11",
+           "-o", tmp, SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, LIB)
+    return LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(LIB)
+            vp, ip, i = ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32), ctypes.c_int
+            lib.oracle_dgrad.argtypes = [vp, vp, vp, i, vp] + [i] * 10
+            lib.oracle_dgrad.restype = i
+            lib.oracle_dgrad_pixels.argtypes = [vp, vp, vp, i, vp, ctypes.c_int64, vp] + [i] * 10
+            lib.oracle_dgrad_pixels.restype = i
+            lib.oracle_conv_fwd.argtypes = [vp, vp, i, vp] + [i] * 10
+            lib.oracle_conv_fwd.restype = i
+            lib.oracle_out_extent.argtypes = [i] * 5
+            lib.oracle_out_extent.restype = i
+            lib.oracle_half_to_double.argtypes = [ctypes.c_uint16]
+            lib.oracle_half_to_double.restype = ctypes.c_double
+            lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+            lib.oracle_bf16_to_double.restype = ctypes.c_double
+            lib.oracle_num_threads.argtypes = []
+            lib.oracle_num_threads.restype = i
+            _lib = lib
+    return _lib
+
+
+def _dtype_of(a: np.ndarray, dtype: str | None) -> int:
+    if dtype is not None:
+        return DTYPE_CODES[dtype]
+    if a.dtype == np.float64:
+        return F64
+    if a.dtype == np.float32:
+        return F32
+    raise ValueError("uint16 arrays need an explicit dtype ('f16' or 'bf16')")
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _check(a, code):
+    want = {F16: np.uint16, BF16: np.uint16, F32: np.float32, F64: np.float64}[code]
+    if a.dtype != want or not a.flags.c_contiguous:
+        raise ValueError(f"expected contiguous {np.dtype(want)} array, got {a.dtype}")
+
+
+def out_extent(size: int, filt: int, stride: int, pad: int, dil: int) -> int:
+    return _load().oracle_out_extent(size, filt, stride, pad, dil)
+
+
+def num_threads() -> int:
+    return _load().oracle_num_threads()
+
+
+def half_to_double(bits: int) -> float:
+    return _load().oracle_half_to_double(bits)
+
+
+def bf16_to_double(bits: int) -> float:
+    return _load().oracle_bf16_to_double(bits)
+
+
+def dgrad(dY, W, H, Wd, stride=1, pad=0, dil=1, x=None, dtype=None):
+    """dX (float64, NHWC [N][H][Wd][C]) from dY [N][P][Q][K] and W [K][R][S][C].
+
+    H and Wd are dX's spatial sizes.  ``x`` (same shape as dX, same element
+    type as dY) enables the ReLU-backward gate.
+    """
+    code = _dtype_of(dY, dtype)
+    N, P, Q, K = dY.shape
+    K2, R, S, C = W.shape
+    if K2 != K:
+        raise ValueError("K mismatch")
+    if (out_extent(H, R, stride, pad, dil), out_extent(Wd, S, stride, pad, dil)) != (P, Q):
+        raise ValueError("dY spatial shape does not match the geometry")
+    for a in (dY, W) + ((x,) if x is not None else ()):
+        _check(a, code)
+    if x is not None and x.shape != (N, H, Wd, C):
+        raise ValueError("x must have dX's shape")
+    out = np.empty((N, H, Wd, C), np.float64)
+    rc = _load().oracle_dgrad(_ptr(dY), _ptr(W), _ptr(x), code, _ptr(out),
+                              N, H, Wd, C, K, R, S, stride, pad, dil)
+    if rc:
+        raise RuntimeError("oracle_dgrad failed")
+    return out
+
+
+def dgrad_pixels(dY, W, H, Wd, pix, stride=1, pad=0, dil=1, x=None, dtype=None):
+    """dgrad at the pixels ``pix`` (int array [npix][3] of (n, h, w)) -> [npix][C]."""
+    code = _dtype_of(dY, dtype)
+    N, P, Q, K = dY.shape
+    _, R, S, C = W.shape
+    for a in (dY, W) + ((x,) if x is not None else ()):
+        _check(a, code)
+    pix = np.ascontiguousarray(pix, dtype=np.int32).reshape(-1, 3)
+    out = np.empty((pix.shape[0], C), np.float64)
+    rc = _load().oracle_dgrad_pixels(_ptr(dY), _ptr(W), _ptr(x), code,
+                                     pix.ctypes.data_as(ctypes.c_void_p),
+                                     pix.shape[0], _ptr(out),
+                                     N, H, Wd, C, K, R, S, stride, pad, dil)
+    if rc:
+        raise RuntimeError("oracle_dgrad_pixels failed")
+    return out
+
+
+def conv_fwd(x, W, stride=1, pad=0, dil=1, dtype=None):
+    """Forward cross-correlation y [N][P][Q][K] (float64) of x [N][H][W][C]."""
+    code = _dtype_of(x, dtype)
+    N, H, Wd, C = x.shape
+    K, R, S, C2 = W.shape
+    if C2 != C:
+        raise ValueError("C mismatch")
+    _check(x, code)
+    _check(W, code)
+    P, Q = out_extent(H, R, stride, pad, dil), out_extent(Wd, S, stride, pad, dil)
+    if P <= 0 or Q <= 0:
+        raise ValueError("empty output")
+    y = np.empty((N, P, Q, K), np.float64)
+    rc = _load().oracle_conv_fwd(_ptr(x), _ptr(W), code, _ptr(y),
+                                 N, H, Wd, C, K, R, S, stride, pad, dil)
+    if rc:
+        raise RuntimeError("oracle_conv_fwd failed")
+    return y

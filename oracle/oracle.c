@@ -1,0 +1,294 @@
+/*
+ * CPU oracle for Conv2d backward-data (dgrad).  TEST INFRASTRUCTURE ONLY.
+ *
+ * This file is the plain, slow, obviously correct statement of what the GPU
+ * library computes.  Only the test suite, the smoke check and the CPU-baseline
+ * leg of the benchmark load it; the library itself never links, loads or calls
+ * it, and it shares no code, header, table or helper with the CUDA sources.
+ *
+ * What it computes (the definition, written out):
+ *
+ *   dX[n,h,w,c] = sum over k, r, s and every (p, q) with
+ *                 h = p*stride - pad + r*dil  and  w = q*stride - pad + s*dil,
+ *                 0 <= p < P, 0 <= q < Q, of dY[n,p,q,k] * W[k,r,s,c]
+ *
+ * i.e. the gradient of a cross-correlation Conv2d with respect to its input,
+ * the operation named "Conv2d dgrad" on apache/tvm PR #10110 ("[CUTLASS]
+ * Conv2d dgrad", opening description).  For a fixed output pixel h and filter
+ * row r there is at most one p solving h = p*stride - pad + r*dil, so the sum
+ * over (p, q) is taken by solving for them; nothing is reordered beyond that.
+ *
+ * P and Q are the forward convolution's output extents,
+ *     P = floor((H + 2*pad - dil*(R-1) - 1) / stride) + 1,
+ * the usual floor convention; H and W are the sizes of dX.
+ *
+ * Optional ReLU-backward epilogue (the "activation fusion" for dgrad that the
+ * same page says is not enabled yet, last comments): the saved activation x
+ * gates each output, out = (x > 0) ? dX : +0.0.  x <= 0, -0.0 and NaN give +0.0.
+ *
+ * Precision: every product and sum is taken in IEEE double.  fp16 and bf16
+ * inputs are decoded from their bit patterns (IEEE-754 binary16; bfloat16 =
+ * the upper half of a binary32) by the decoders below.
+ *
+ * Tensor layouts: dY is NHWC [N][P][Q][K], W is KRSC [K][R][S][C], dX and x
+ * are NHWC [N][H][W][C].  All contiguous.
+ *
+ * Pins: the tests check this file against a materialised forward-convolution
+ * matrix (brute force), the adjoint identity with the forward convolution
+ * below, closed forms (1x1 GEMM, impulse response, identity filter), a
+ * hand-worked case, integer-exact results and an independent library routine.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { ORACLE_F16 = 0, ORACLE_BF16 = 1, ORACLE_F32 = 2, ORACLE_F64 = 3 };
+
+/* IEEE-754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+double oracle_half_to_double(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int expo = (h >> 10) & 0x1f;
+    int frac = h & 0x3ff;
+    double v;
+    if (expo == 0)
+        v = ldexp((double)frac, -24); /* subnormal: frac * 2^-14 * 2^-10 */
+    else if (expo == 31)
+        v = frac ? NAN : INFINITY;
+    else
+        v = ldexp((double)(frac | 0x400), expo - 25); /* (1 + frac/1024) * 2^(e-15) */
+    return sign ? -v : v;
+}
+
+/* bfloat16: the upper 16 bits of an IEEE binary32. */
+double oracle_bf16_to_double(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* Forward output extent along one axis; -1 when the geometry is empty. */
+int oracle_out_extent(int in, int filt, int stride, int pad, int dil)
+{
+    if (in <= 0 || filt <= 0 || stride <= 0 || dil <= 0 || pad < 0) return -1;
+    int span = in + 2 * pad - dil * (filt - 1) - 1;
+    if (span < 0) return -1;
+    return span / stride + 1;
+}
+
+/* Decode a whole buffer of the given element type into doubles. */
+static double *decode_all(const void *src, size_t n, int dtype)
+{
+    double *out = (double *)malloc(n ? n * sizeof(double) : sizeof(double));
+    if (!out) return NULL;
+    if (dtype == ORACLE_F64) {
+        memcpy(out, src, n * sizeof(double));
+    } else if (dtype == ORACLE_F32) {
+        const float *s = (const float *)src;
+        for (size_t i = 0; i < n; ++i) out[i] = s[i];
+    } else if (dtype == ORACLE_BF16) {
+        const uint16_t *s = (const uint16_t *)src;
+        for (size_t i = 0; i < n; ++i) out[i] = oracle_bf16_to_double(s[i]);
+    } else {
+        const uint16_t *s = (const uint16_t *)src;
+        for (size_t i = 0; i < n; ++i) out[i] = oracle_half_to_double(s[i]);
+    }
+    return out;
+}
+
+/* One element of a buffer of the given type, as a double. */
+static double load_one(const void *src, size_t i, int dtype)
+{
+    switch (dtype) {
+    case ORACLE_F64: return ((const double *)src)[i];
+    case ORACLE_F32: return (double)((const float *)src)[i];
+    case ORACLE_BF16: return oracle_bf16_to_double(((const uint16_t *)src)[i]);
+    default: return oracle_half_to_double(((const uint16_t *)src)[i]);
+    }
+}
+
+static int floor_mod(int a, int m)
+{
+    int r = a % m;
+    return r < 0 ? r + m : r;
+}
+
+/*
+ * The sum for one dX pixel (n, h, w), all C channels, into acc[0..C).
+ * Wd is W decoded to double.  For each filter tap (r, s) the unique (p, q)
+ * with h = p*stride - pad + r*dil (and likewise for w) is found; taps with no
+ * integer or in-range solution contribute nothing.
+ */
+static void pixel_sum(const void *dY, int dtype, const double *Wd, double *acc,
+                      int n, int h, int w, int C, int K, int R, int S,
+                      int stride, int pad, int dil, int P, int Q)
+{
+    for (int c = 0; c < C; ++c) acc[c] = 0.0;
+    for (int r = 0; r < R; ++r) {
+        int th = h + pad - r * dil; /* = p * stride */
+        if (floor_mod(th, stride) != 0) continue;
+        int p = th / stride; /* exact */
+        if (p < 0 || p >= P) continue;
+        for (int s = 0; s < S; ++s) {
+            int tw = w + pad - s * dil; /* = q * stride */
+            if (floor_mod(tw, stride) != 0) continue;
+            int q = tw / stride;
+            if (q < 0 || q >= Q) continue;
+            size_t dy_base = (((size_t)n * P + p) * Q + q) * (size_t)K;
+            for (int k = 0; k < K; ++k) {
+                double dy = load_one(dY, dy_base + k, dtype);
+                const double *wrow = Wd + (((size_t)k * R + r) * S + s) * (size_t)C;
+                for (int c = 0; c < C; ++c) acc[c] += dy * wrow[c];
+            }
+        }
+    }
+}
+
+/* ReLU-backward gate: keep where x > 0 (NaN, -0.0 and negatives give +0.0). */
+static void apply_gate(double *acc, const void *x, int dtype, size_t base, int C)
+{
+    for (int c = 0; c < C; ++c) {
+        double xv = load_one(x, base + c, dtype);
+        if (!(xv > 0.0)) acc[c] = 0.0;
+    }
+}
+
+static int check_geometry(int N, int H, int W, int C, int K, int R, int S,
+                          int stride, int pad, int dil, int *P, int *Q)
+{
+    if (N <= 0 || C <= 0 || K <= 0) return -1;
+    *P = oracle_out_extent(H, R, stride, pad, dil);
+    *Q = oracle_out_extent(W, S, stride, pad, dil);
+    if (*P <= 0 || *Q <= 0) return -1;
+    return 0;
+}
+
+/*
+ * Full dgrad.  dY, W and x (x may be NULL: no gate) are of element type
+ * `dtype`; dX is written as doubles, NHWC.  Returns 0, or -1 on bad geometry
+ * or allocation failure.  OpenMP-parallel over (n, h).
+ */
+int oracle_dgrad(const void *dY, const void *Wt, const void *x, int dtype, double *dX,
+                 int N, int H, int W, int C, int K, int R, int S,
+                 int stride, int pad, int dil)
+{
+    int P, Q;
+    if (check_geometry(N, H, W, C, K, R, S, stride, pad, dil, &P, &Q)) return -1;
+    double *Wd = decode_all(Wt, (size_t)K * R * S * C, dtype);
+    if (!Wd) return -1;
+    int failed = 0;
+#pragma omp parallel
+    {
+        double *acc = (double *)malloc((size_t)C * sizeof(double));
+        if (!acc) {
+#pragma omp atomic write
+            failed = 1;
+        } else {
+#pragma omp for collapse(2) schedule(dynamic, 1)
+            for (int n = 0; n < N; ++n)
+                for (int h = 0; h < H; ++h)
+                    for (int w = 0; w < W; ++w) {
+                        pixel_sum(dY, dtype, Wd, acc, n, h, w, C, K, R, S, stride, pad, dil, P, Q);
+                        size_t base = (((size_t)n * H + h) * W + w) * (size_t)C;
+                        if (x) apply_gate(acc, x, dtype, base, C);
+                        memcpy(dX + base, acc, (size_t)C * sizeof(double));
+                    }
+            free(acc);
+        }
+    }
+    free(Wd);
+    return failed ? -1 : 0;
+}
+
+/*
+ * dgrad at selected pixels only: pix holds npix triples (n, h, w); out gets
+ * npix rows of C doubles.  Same arithmetic as oracle_dgrad, for checking
+ * sampled outputs of problems too large to evaluate in full.
+ */
+int oracle_dgrad_pixels(const void *dY, const void *Wt, const void *x, int dtype,
+                        const int32_t *pix, int64_t npix, double *out,
+                        int N, int H, int W, int C, int K, int R, int S,
+                        int stride, int pad, int dil)
+{
+    int P, Q;
+    if (check_geometry(N, H, W, C, K, R, S, stride, pad, dil, &P, &Q)) return -1;
+    for (int64_t i = 0; i < npix; ++i) {
+        const int32_t *t = pix + 3 * i;
+        if (t[0] < 0 || t[0] >= N || t[1] < 0 || t[1] >= H || t[2] < 0 || t[2] >= W) return -1;
+    }
+    double *Wd = decode_all(Wt, (size_t)K * R * S * C, dtype);
+    if (!Wd) return -1;
+    int failed = 0;
+#pragma omp parallel
+    {
+        double *acc = (double *)malloc((size_t)C * sizeof(double));
+        if (!acc) {
+#pragma omp atomic write
+            failed = 1;
+        } else {
+#pragma omp for schedule(dynamic, 4)
+            for (int64_t i = 0; i < npix; ++i) {
+                int n = pix[3 * i], h = pix[3 * i + 1], w = pix[3 * i + 2];
+                pixel_sum(dY, dtype, Wd, acc, n, h, w, C, K, R, S, stride, pad, dil, P, Q);
+                if (x) apply_gate(acc, x, dtype, (((size_t)n * H + h) * W + w) * (size_t)C, C);
+                memcpy(out + (size_t)i * C, acc, (size_t)C * sizeof(double));
+            }
+            free(acc);
+        }
+    }
+    free(Wd);
+    return failed ? -1 : 0;
+}
+
+/*
+ * Forward cross-correlation, the operation whose input gradient dgrad is:
+ *   y[n,p,q,k] = sum_{r,s,c} x[n, p*stride - pad + r*dil, q*stride - pad + s*dil, c] * W[k,r,s,c]
+ * with out-of-range input positions reading zero.  x is NHWC of `dtype`,
+ * y is written as doubles, NHWC [N][P][Q][K].  Used by the adjoint-identity pin.
+ */
+int oracle_conv_fwd(const void *x, const void *Wt, int dtype, double *y,
+                    int N, int H, int W, int C, int K, int R, int S,
+                    int stride, int pad, int dil)
+{
+    int P, Q;
+    if (check_geometry(N, H, W, C, K, R, S, stride, pad, dil, &P, &Q)) return -1;
+    double *Wd = decode_all(Wt, (size_t)K * R * S * C, dtype);
+    if (!Wd) return -1;
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (int n = 0; n < N; ++n)
+        for (int p = 0; p < P; ++p)
+            for (int q = 0; q < Q; ++q)
+                for (int k = 0; k < K; ++k) {
+                    double acc = 0.0;
+                    for (int r = 0; r < R; ++r) {
+                        int h = p * stride - pad + r * dil;
+                        if (h < 0 || h >= H) continue;
+                        for (int s = 0; s < S; ++s) {
+                            int w = q * stride - pad + s * dil;
+                            if (w < 0 || w >= W) continue;
+                            size_t xb = (((size_t)n * H + h) * W + w) * (size_t)C;
+                            const double *wrow = Wd + (((size_t)k * R + r) * S + s) * (size_t)C;
+                            for (int c = 0; c < C; ++c) acc += load_one(x, xb + c, dtype) * wrow[c];
+                        }
+                    }
+                    y[(((size_t)n * P + p) * Q + q) * (size_t)K + k] = acc;
+                }
+    free(Wd);
+    return 0;
+}
+
+/* Threads an OpenMP region of this library would use. */
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
