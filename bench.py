@@ -1,0 +1,341 @@
+"""Benchmark: Conv2d dgrad over the ResNet-50 v1.5 bottleneck convolutions
+(all but conv1) at batch 256, NHWC bf16, fp32 accumulation, on one GB300.
+
+One step = one dgrad of each of the 22 layers (one launch each), inputs
+resident in HBM.  Prints one JSON line:
+  value        aggregate useful TFLOP/s (sum of 2*N*P*Q*K*C*R*S over the 22
+               layers / device time of the step), whole job over all ranks
+  per_layer    each layer's TFLOP/s and its fraction of the slower-of
+               (tensor, HBM) roofline
+  roofline     for the launch with the largest share of the step
+  e2e          the same metric with dY uploaded from pinned host memory and
+               dX read back every step, through the same C-ABI calls
+  cpu_baseline the CPU oracle on a bounded sample (first images of each layer)
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 (torchrun, one rank per GPU): every rank runs the full workload on its
+own GPU (replicas; dgrad has no exchange step), barrier + max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from implicit_gemm_dgrad_gb300 import synth  # noqa: E402
+from implicit_gemm_dgrad_gb300.workloads import RESNET50_B256  # noqa: E402
+
+METRIC = "dgrad TFLOP/s per ResNet-50 layer (1 GB300) and % of slower-of roofline"
+WORKLOAD = "resnet50_v1.5_bottleneck_dgrad_b256_bf16_22_layers"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return dict(FALLBACK_PEAKS, source="fallback")
+
+
+def roofline_time_s(layer, peaks):
+    t_tc = layer.flops / (peaks["bf16_tflops_sustained"] * 1e12)
+    t_hbm = layer.bytes / (peaks["hbm_gbs"] * 1e9)
+    return max(t_tc, t_hbm), ("tensor" if t_tc >= t_hbm else "hbm")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"cdg_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.out.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax = float(parts[2])
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_oracle_sample(layers, arrays, images: int):
+    """Time the CPU oracle on the first `images` images of every layer."""
+    import oracle
+    t0 = time.perf_counter()
+    flops = 0
+    for L, (dY, W, x) in zip(layers, arrays):
+        oracle.dgrad(dY[:images], W, L.H, L.W, L.stride, L.pad, L.dil, x=None, dtype=L.dtype)
+        flops += L.flops * images // L.N
+    dt = time.perf_counter() - t0
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"first {images} image(s) of each of the {len(layers)} layers "
+                      f"({flops / 1e9:.1f} GFLOP, {dt:.1f} s, double precision)",
+            "seconds": dt}
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the CPU oracle, as it stands, on a bounded sample."""
+    if rank != 0:
+        return
+    layers = RESNET50_B256
+    n = args.ref_images
+    arrays = [synth.make_inputs(L.shape(), L.dtype, L.dist, L.workload, L.index, batch=n) for L in layers]
+    for _ in range(args.warmup):
+        cpu_oracle_sample(layers[:1], arrays[:1], 1)
+    times, res = [], None
+    for _ in range(args.steps):
+        res = cpu_oracle_sample(layers, arrays, n)
+        times.append(res["seconds"])
+    value = res["value"]
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * float(np.mean(times)),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "images_per_layer_per_step": n, "layers": len(layers)},
+            "cpu_baseline": {k: res[k] for k in ("value", "unit", "cores", "kind", "sample")},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--cpu-images", type=int, default=48)
+    ap.add_argument("--ref-images", type=int, default=8, help="images per layer per reference-arm step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", default="", help="comma-separated layer names (default: all 22)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    import implicit_gemm_dgrad_gb300 as cdg
+
+    if world > 1:
+        dist.init_process_group("gloo")  # control path only: barrier and max-over-ranks
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.Stream(device=dev)
+    peaks = load_peaks()
+
+    layers = RESNET50_B256
+    if args.layers:
+        keep = set(args.layers.split(","))
+        layers = [L for L in layers if L.name in keep]
+
+    # ---- inputs (seeded, host), upload, plan, prepack
+    host, state = [], []
+    with torch.cuda.stream(stream):
+        for L in layers:
+            dY, W, _ = synth.make_inputs(L.shape(), L.dtype, L.dist, L.workload, L.index)
+            host.append((dY, W, None))
+            p = cdg.plan(L.N, L.H, L.W, L.C, L.K, L.R, L.S, L.stride, L.pad, L.dil, L.dtype)
+            d_dY = torch.from_numpy(dY.view(np.int16)).to(dev)
+            d_W = torch.from_numpy(W.view(np.int16)).to(dev)
+            d_Wp = torch.empty(p.packed_weight_bytes // 2, dtype=torch.int16, device=dev)
+            d_dX = torch.empty(L.N * L.H * L.W * L.C, dtype=torch.int16, device=dev)
+            p.prepack_weights(d_W, d_Wp, stream)
+            state.append((L, p, d_dY, d_Wp, d_dX))
+    torch.cuda.synchronize()
+
+    def step():
+        for (_, p, d_dY, d_Wp, d_dX) in state:
+            p.dgrad(d_dY, d_Wp, d_dX, None, stream)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    # ---- warm-up, then the timed region with per-launch events
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    for (_, p, *_rest) in state:
+        st = p.device_status(stream)
+        if st != 0:
+            raise RuntimeError(f"device status {st} after warm-up")
+
+    nL = len(state)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nL + 1)] for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clocks:
+        t_host0 = time.perf_counter()
+        for k in range(args.steps):
+            ev[k][0].record(stream)
+            for i, (_, p, d_dY, d_Wp, d_dX) in enumerate(state):
+                p.dgrad(d_dY, d_Wp, d_dX, None, stream)
+                ev[k][i + 1].record(stream)
+        torch.cuda.synchronize()
+        t_host1 = time.perf_counter()
+    barrier()
+    per_layer_ms = np.zeros(nL)
+    step_ms = []
+    for k in range(args.steps):
+        step_ms.append(ev[k][0].elapsed_time(ev[k][nL]))
+        for i in range(nL):
+            per_layer_ms[i] += ev[k][i].elapsed_time(ev[k][i + 1])
+    per_layer_ms /= args.steps
+    total_ms = float(np.sum(step_ms))
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    flops_step = sum(L.flops for (L, *_r) in state)
+    value = world * flops_step * args.steps / (total_ms * 1e-3) / 1e12
+
+    per_layer = []
+    for i, (L, p, *_r) in enumerate(state):
+        t = per_layer_ms[i] * 1e-3
+        t_roof, bound = roofline_time_s(L, peaks)
+        per_layer.append({"layer": L.name, "ms": round(per_layer_ms[i], 5),
+                          "tflops": round(L.flops / t / 1e12, 2),
+                          "gbs": round(L.bytes / t / 1e9, 1), "bound": bound,
+                          "roofline_frac": round(t_roof / t, 4),
+                          "tensor_peak_frac": round(L.flops / t / 1e12 / peaks["bf16_tflops_sustained"], 4)})
+
+    # dominant launch: the layer with the largest share of the step
+    dom = int(np.argmax(per_layer_ms))
+    Ld = state[dom][0]
+    td = per_layer_ms[dom] * 1e-3
+    _, bound = roofline_time_s(Ld, peaks)
+    if bound == "tensor":
+        achieved, peak, unit = Ld.flops / td / 1e12, peaks["bf16_tflops_sustained"], "TFLOP/s"
+    else:
+        achieved, peak, unit = Ld.bytes / td / 1e9, peaks["hbm_gbs"], "GB/s"
+    roofline = {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+                "frac": round(achieved / peak, 4), "traffic": None, "kernel": f"dgrad_kernel ({Ld.name})",
+                "peak_source": peaks["source"] + (" sustained bf16" if bound == "tensor" else " copy bandwidth"),
+                "share_of_step": round(per_layer_ms[dom] / float(np.sum(per_layer_ms)), 4),
+                "step_roofline_frac": round(sum(roofline_time_s(L, peaks)[0] for (L, *_r) in state)
+                                            / (ms_per_step * 1e-3), 4)}
+
+    # ---- end to end: dY from pinned host memory, dX back to pinned host memory, every step
+    h_dY = [torch.from_numpy(h[0].view(np.int16)).pin_memory() for h in host]
+    h_dX = [torch.empty(L.N * L.H * L.W * L.C, dtype=torch.int16).pin_memory() for (L, *_r) in state]
+    h2d = sum(t.numel() * 2 for t in h_dY)
+    d2h = sum(t.numel() * 2 for t in h_dX)
+
+    def e2e_step():
+        for i, (_, p, d_dY, d_Wp, d_dX) in enumerate(state):
+            d_dY.copy_(h_dY[i], non_blocking=True)
+            p.dgrad(d_dY, d_Wp, d_dX, None, stream)
+            h_dX[i].copy_(d_dX, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * flops_step * args.e2e_steps / (e2e_ms * 1e-3) / 1e12
+    for (_, p, *_rest) in state:
+        st = p.device_status(stream)
+        if st != 0:
+            raise RuntimeError(f"device status {st} after timed runs")
+
+    if rank != 0:
+        return
+    cpu = None
+    if not args.no_cpu_baseline:
+        c = cpu_oracle_sample([s[0] for s in state], host, args.cpu_images)
+        cpu = {k: c[k] for k in ("value", "unit", "cores", "kind", "sample")}
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "global_batch": 256 * world, "layers": nL,
+                   "l2": "inputs larger than L2: the step cycles ~5 GB of operands, so each layer's data is "
+                         "evicted before its next use",
+                   "flops_per_step": flops_step, "parallelism": f"replicas x{world}"},
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": args.e2e_steps},
+        "gpu_launches": nL * args.steps,
+        "clocks": clocks.summary(),
+        "host_wall_s_timed": round(t_host1 - t_host0, 4),
+        "per_layer": per_layer,
+        "peaks": peaks,
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

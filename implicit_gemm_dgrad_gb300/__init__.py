@@ -1,0 +1,201 @@
+"""GB300 (sm_103a) Conv2d backward-data engine: Python binding of libcdg.so.
+
+Argument marshalling only: every step of dgrad runs in the library's CUDA
+kernels.  Tensors may be torch CUDA tensors or raw device addresses (ints);
+streams may be torch streams, raw ``cudaStream_t`` values (ints) or None (the
+current torch stream when torch is loaded, else the legacy default stream).
+
+The operation (apache/tvm PR #10110, "[CUTLASS] Conv2d dgrad"):
+    dX[n,h,w,c] = sum_{k,r,s} dY[n,p,q,k] * W[k,r,s,c]
+over every (p, q) with h = p*stride - pad + r*dil, w = q*stride - pad + s*dil.
+NHWC dX/dY, KRSC W, fp16/bf16 inputs, fp32 accumulation.
+
+There is no CPU fallback: if the library is missing, importing the functions
+that need it raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libcdg.so")
+
+OK = 0
+STATUS_NAMES = {0: "CDG_OK", 1: "CDG_ERR_INVALID_ARG", 2: "CDG_ERR_UNSUPPORTED", 3: "CDG_ERR_ALIGNMENT",
+                4: "CDG_ERR_ALIAS", 5: "CDG_ERR_CUDA", 6: "CDG_ERR_TIMEOUT", 7: "CDG_ERR_NO_DEVICE"}
+F16, BF16 = 0, 1
+EPI_RELU_BWD, EPI_OUT_F32 = 1, 2
+DTYPES = {"f16": F16, "bf16": BF16}
+
+EXPORTS = ("cdg_plan", "cdg_plan_host", "cdg_destroy", "cdg_get_output_dims", "cdg_packed_weight_bytes",
+           "cdg_plan_get_info", "cdg_prepack_weights", "cdg_dgrad", "cdg_device_status", "cdg_status_string")
+
+
+class CdgError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)} ({status_string(status)})")
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("P", ctypes.c_int), ("Q", ctypes.c_int), ("num_phases", ctypes.c_int),
+                ("phase_taps", ctypes.c_int * 16), ("tile_m", ctypes.c_int), ("tile_n", ctypes.c_int),
+                ("tile_k", ctypes.c_int), ("a_mode", ctypes.c_int), ("box_w", ctypes.c_int),
+                ("box_h", ctypes.c_int), ("box_n", ctypes.c_int), ("stages", ctypes.c_int),
+                ("work_items", ctypes.c_int), ("grid", ctypes.c_int), ("smem_bytes", ctypes.c_int),
+                ("tmem_cols", ctypes.c_int)]
+
+    def as_dict(self) -> dict:
+        d = {name: getattr(self, name) for name, _ in self._fields_}
+        d["phase_taps"] = list(self.phase_taps)[: self.num_phases]
+        return d
+
+
+_lib = None
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Load libcdg.so (building it first if the sources are newer)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    path = path or LIB_PATH
+    if path == LIB_PATH:
+        from . import build as _build
+        if not _build.up_to_date():
+            _build.build()
+    if not os.path.exists(path):
+        raise ImportError(f"libcdg.so not found at {path}; run `python -m implicit_gemm_dgrad_gb300.build`")
+    lib = ctypes.CDLL(path)
+    i, vp, hp = ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p
+    lib.cdg_plan.argtypes = [i] * 12 + [ctypes.POINTER(hp)]
+    lib.cdg_plan.restype = i
+    lib.cdg_plan_host.argtypes = [i] * 13 + [ctypes.POINTER(hp)]
+    lib.cdg_plan_host.restype = i
+    lib.cdg_destroy.argtypes = [hp]
+    lib.cdg_destroy.restype = None
+    lib.cdg_get_output_dims.argtypes = [hp, ctypes.POINTER(i), ctypes.POINTER(i)]
+    lib.cdg_get_output_dims.restype = i
+    lib.cdg_packed_weight_bytes.argtypes = [hp]
+    lib.cdg_packed_weight_bytes.restype = ctypes.c_size_t
+    lib.cdg_plan_get_info.argtypes = [hp, ctypes.POINTER(PlanInfo)]
+    lib.cdg_plan_get_info.restype = i
+    lib.cdg_prepack_weights.argtypes = [hp, vp, vp, vp]
+    lib.cdg_prepack_weights.restype = i
+    lib.cdg_dgrad.argtypes = [hp, vp, vp, vp, vp, vp]
+    lib.cdg_dgrad.restype = i
+    lib.cdg_device_status.argtypes = [hp, vp]
+    lib.cdg_device_status.restype = i
+    lib.cdg_status_string.argtypes = [i]
+    lib.cdg_status_string.restype = ctypes.c_char_p
+    if path == LIB_PATH:
+        _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return load_library().cdg_status_string(status).decode()
+    except Exception:  # noqa: BLE001 - message formatting must not raise
+        return "?"
+
+
+def _addr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(s) -> int | None:
+    if s is None:
+        try:
+            import torch
+            if torch.cuda.is_available() and torch.cuda.is_initialized():
+                return torch.cuda.current_stream().cuda_stream
+        except ImportError:
+            pass
+        return None
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+class Plan:
+    """One planned dgrad shape (a ``cdg_handle_t``)."""
+
+    def __init__(self, N, H, W, C, K, R, S, stride=1, pad=0, dil=1, dtype="bf16", relu=False,
+                 out_f32=False, host_sms: int | None = None):
+        self.lib = load_library()
+        self.shape = dict(N=N, H=H, W=W, C=C, K=K, R=R, S=S, stride=stride, pad=pad, dil=dil)
+        self.dtype = dtype
+        self.relu = relu
+        self.out_f32 = out_f32
+        epi = (EPI_RELU_BWD if relu else 0) | (EPI_OUT_F32 if out_f32 else 0)
+        h = ctypes.c_void_p()
+        dt = DTYPES[dtype] if isinstance(dtype, str) else int(dtype)
+        if host_sms is None:
+            rc = self.lib.cdg_plan(N, H, W, C, K, R, S, stride, pad, dil, dt, epi, ctypes.byref(h))
+        else:
+            rc = self.lib.cdg_plan_host(N, H, W, C, K, R, S, stride, pad, dil, dt, epi, host_sms, ctypes.byref(h))
+        if rc != OK:
+            raise CdgError(rc, "cdg_plan")
+        self.handle = h
+
+    def close(self):
+        if getattr(self, "handle", None) is not None and self.handle.value:
+            self.lib.cdg_destroy(self.handle)
+        self.handle = None
+
+    def __del__(self):
+        self.close()
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    @property
+    def output_dims(self) -> tuple[int, int]:
+        P, Q = ctypes.c_int(), ctypes.c_int()
+        rc = self.lib.cdg_get_output_dims(self.handle, ctypes.byref(P), ctypes.byref(Q))
+        if rc != OK:
+            raise CdgError(rc, "cdg_get_output_dims")
+        return P.value, Q.value
+
+    @property
+    def packed_weight_bytes(self) -> int:
+        return int(self.lib.cdg_packed_weight_bytes(self.handle))
+
+    def info(self) -> dict:
+        inf = PlanInfo()
+        rc = self.lib.cdg_plan_get_info(self.handle, ctypes.byref(inf))
+        if rc != OK:
+            raise CdgError(rc, "cdg_plan_get_info")
+        return inf.as_dict()
+
+    def prepack_weights(self, W_krsc, W_packed, stream=None) -> None:
+        rc = self.lib.cdg_prepack_weights(self.handle, _addr(W_krsc), _addr(W_packed), _stream(stream))
+        if rc != OK:
+            raise CdgError(rc, "cdg_prepack_weights")
+
+    def dgrad(self, dY, W_packed, dX, relu_mask=None, stream=None) -> None:
+        rc = self.lib.cdg_dgrad(self.handle, _addr(dY), _addr(W_packed), _addr(dX), _addr(relu_mask),
+                                _stream(stream))
+        if rc != OK:
+            raise CdgError(rc, "cdg_dgrad")
+
+    def device_status(self, stream=None) -> int:
+        return int(self.lib.cdg_device_status(self.handle, _stream(stream)))
+
+
+def plan(N, H, W, C, K, R, S, stride=1, pad=0, dil=1, dtype="bf16", relu=False, out_f32=False) -> Plan:
+    return Plan(N, H, W, C, K, R, S, stride, pad, dil, dtype, relu, out_f32)
+
+
+def plan_host(N, H, W, C, K, R, S, stride=1, pad=0, dil=1, dtype="bf16", relu=False, out_f32=False,
+              num_sms=148) -> Plan:
+    return Plan(N, H, W, C, K, R, S, stride, pad, dil, dtype, relu, out_f32, host_sms=num_sms)

@@ -1,0 +1,455 @@
+// C-ABI of the dgrad library: validation, planning, TMA descriptors, launches.
+//
+// The plan turns one Conv2d dgrad shape into the parameter block of a single
+// persistent kernel launch:
+//   * P, Q from the floor convention of the forward convolution;
+//   * the stride^2 phase sub-convolutions of a strided dgrad (apache/tvm PR
+//     #10110, "[CUTLASS] Conv2d dgrad", benchmark comment: the "strided dgrad"
+//     case): dX pixel (h, w) with h = stride*i + ph, w = stride*j + pw receives
+//     exactly the taps (r, s) with ph + pad - r*dil = 0 (mod stride) and
+//     likewise for s, reading dY at p = i + (ph + pad - r*dil)/stride;
+//   * the operand mode: 1x1 pad-0 filters read dY rows as a plain 2-D matrix,
+//     everything else reads 4-D (channel, column, row, image) halo boxes whose
+//     out-of-range part the TMA unit fills with zeros;
+//   * the tile shape, pipeline depth and work list (phases ordered by tap
+//     count, longest first, then M tiles, then N tiles).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "../../include/cdg.h"
+#include "cdg_params.h"
+
+namespace {
+
+constexpr int kMaxSmem = CDG_MAX_DYN_SMEM;
+constexpr int kMaxStages = 8;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled()
+{
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+
+int floor_mod(int a, int m)
+{
+    int r = a % m;
+    return r < 0 ? r + m : r;
+}
+
+}  // namespace
+
+struct cdg_plan_st {
+    int N, H, W, C, K, R, S, stride, pad, dil, dtype, epi;
+    int P, Q;
+    bool host_only;
+    int device;
+    int num_sms;
+    int out_type, in_type;
+    bool mask;
+    size_t smem;
+    int grid;
+    int *d_status;
+    CdgParams prm;  // tensor maps and pointers are filled per call
+    const void *cached_dY, *cached_Wp;
+    cdg_plan_info_t info;
+};
+
+namespace {
+
+// Choose the 4-D halo box (box_w x box_h x box_n dX pixels of one phase
+// sub-grid, at most 128) that covers the phases' sub-grids with the fewest
+// tiles; ties prefer wider boxes (longer contiguous rows in dY and dX).
+void choose_box(const std::vector<CdgPhase> &phases, int N, int &bw, int &bh, int &bn)
+{
+    int hmax = 0, wmax = 0;
+    for (const CdgPhase &ph : phases)
+        if (ph.tap_count > 0) {
+            hmax = std::max(hmax, ph.hph);
+            wmax = std::max(wmax, ph.wph);
+        }
+    long long best = -1;
+    bw = bh = bn = 1;
+    for (int w = 1; w <= std::min(wmax, CDG_BM); ++w)
+        for (int h = 1; h <= std::min(hmax, CDG_BM / w); ++h) {
+            int n = 1;
+            if (w >= wmax && h >= hmax) n = std::max(1, std::min(N, CDG_BM / (w * h)));
+            long long tiles = 0;
+            for (const CdgPhase &ph : phases)
+                if (ph.tap_count > 0)
+                    tiles += 1LL * ceil_div(ph.wph, w) * ceil_div(ph.hph, h) * ceil_div(N, n);
+            const bool better = best < 0 || tiles < best || (tiles == best && w > bw) ||
+                                (tiles == best && w == bw && h > bh);
+            if (better) {
+                best = tiles;
+                bw = w;
+                bh = h;
+                bn = n;
+            }
+        }
+}
+
+int choose_bn(int C)
+{
+    if (C <= 256) return ((C + 15) / 16) * 16;
+    int best = 256;
+    long long best_waste = -1;
+    for (int bn = 256; bn >= 64; bn -= 16) {
+        const long long waste = 1LL * ceil_div(C, bn) * bn - C;
+        if (best_waste < 0 || waste < best_waste) {
+            best_waste = waste;
+            best = bn;
+        }
+    }
+    return best;
+}
+
+int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int pad, int dil, int dtype, int epilogue,
+              int num_sms, bool host_only, cdg_handle_t *out)
+{
+    if (!out) return CDG_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (N < 1 || H < 1 || W < 1 || C < 1 || K < 1 || R < 1 || S < 1 || stride < 1 || pad < 0 || dil < 1)
+        return CDG_ERR_INVALID_ARG;
+    if (dtype != CDG_F16 && dtype != CDG_BF16) return CDG_ERR_INVALID_ARG;
+    if (epilogue & ~(CDG_EPI_RELU_BWD | CDG_EPI_OUT_F32)) return CDG_ERR_INVALID_ARG;
+    const long long spanH = 1LL * H + 2LL * pad - 1LL * dil * (R - 1) - 1;
+    const long long spanW = 1LL * W + 2LL * pad - 1LL * dil * (S - 1) - 1;
+    if (spanH < 0 || spanW < 0) return CDG_ERR_INVALID_ARG;
+    const int P = static_cast<int>(spanH / stride + 1), Q = static_cast<int>(spanW / stride + 1);
+    if (C % 8 || K % 8) return CDG_ERR_UNSUPPORTED;
+    if (stride > 4 || R * S > CDG_MAX_TAPS) return CDG_ERR_UNSUPPORTED;
+    // TMA: dimensions < 2^32, strides < 2^40 bytes; keep every index in int32
+    if (1LL * N * P * Q * K >= (1LL << 31) || 1LL * N * H * W * C >= (1LL << 31) ||
+        1LL * R * S * C * K >= (1LL << 31) || P > 65535 || Q > 65535)
+        return CDG_ERR_UNSUPPORTED;
+    // tap offsets (pad - r*dil)/stride are kept as int16
+    if (pad + 1LL * dil * (std::max(R, S) - 1) > 32767) return CDG_ERR_UNSUPPORTED;
+
+    cdg_plan_st *h = new (std::nothrow) cdg_plan_st();
+    if (!h) return CDG_ERR_INVALID_ARG;
+    h->N = N; h->H = H; h->W = W; h->C = C; h->K = K; h->R = R; h->S = S;
+    h->stride = stride; h->pad = pad; h->dil = dil; h->dtype = dtype; h->epi = epilogue;
+    h->P = P; h->Q = Q;
+    h->host_only = host_only;
+    h->num_sms = num_sms;
+    h->in_type = dtype == CDG_F16 ? CDG_T_F16 : CDG_T_BF16;
+    h->out_type = (epilogue & CDG_EPI_OUT_F32) ? CDG_T_F32 : h->in_type;
+    h->mask = (epilogue & CDG_EPI_RELU_BWD) != 0;
+
+    // ---- phases and their taps
+    std::vector<CdgPhase> phases;
+    std::vector<CdgTap> taps;
+    int phase_taps_by_index[16] = {0};
+    for (int ph = 0; ph < stride; ++ph)
+        for (int pw = 0; pw < stride; ++pw) {
+            CdgPhase f;
+            std::memset(&f, 0, sizeof f);
+            f.ph = ph;
+            f.pw = pw;
+            f.hph = ph < H ? (H - ph + stride - 1) / stride : 0;
+            f.wph = pw < W ? (W - pw + stride - 1) / stride : 0;
+            std::vector<CdgTap> mine;
+            for (int r = 0; r < R; ++r) {
+                const int th = ph + pad - r * dil;
+                if (floor_mod(th, stride)) continue;
+                for (int s = 0; s < S; ++s) {
+                    const int tw = pw + pad - s * dil;
+                    if (floor_mod(tw, stride)) continue;
+                    CdgTap t;
+                    t.dr = static_cast<int16_t>(th / stride);  // exact: th is a multiple of stride
+                    t.ds = static_cast<int16_t>(tw / stride);
+                    t.t = static_cast<int16_t>(r * S + s);
+                    t.unused = 0;
+                    mine.push_back(t);
+                }
+            }
+            f.tap_count = static_cast<int>(mine.size());
+            phase_taps_by_index[ph * stride + pw] = f.tap_count;
+            if (f.hph == 0 || f.wph == 0) continue;  // no dX pixel in this residue class
+            f.tap_begin = static_cast<int>(taps.size());
+            taps.insert(taps.end(), mine.begin(), mine.end());
+            phases.push_back(f);
+        }
+    // longest phases first (static schedule, largest work items in the first wave)
+    std::stable_sort(phases.begin(), phases.end(),
+                     [](const CdgPhase &a, const CdgPhase &b) { return a.tap_count > b.tap_count; });
+
+    // ---- operand mode and tiles
+    const bool flat = (R == 1 && S == 1 && pad == 0);
+    int bw = 0, bh = 0, bnb = 0;
+    if (!flat) choose_box(phases, N, bw, bh, bnb);
+    const int BN = choose_bn(C);
+    const int tiles_n = ceil_div(C, BN);
+    int items = 0;
+    for (CdgPhase &f : phases) {
+        f.linear = (flat || f.tap_count == 0) ? 1 : 0;
+        if (f.linear) {
+            f.tiles_w = f.tiles_h = 1;
+            f.tiles_m = ceil_div(1LL * N * f.hph * f.wph, CDG_BM);
+        } else {
+            f.tiles_w = ceil_div(f.wph, bw);
+            f.tiles_h = ceil_div(f.hph, bh);
+            f.tiles_m = f.tiles_w * f.tiles_h * ceil_div(N, bnb);
+        }
+        f.item_begin = items;
+        items += f.tiles_m * tiles_n;
+    }
+    const int stage_bytes = CDG_BM * 128 + BN * 128;
+    const int stages = std::min(kMaxStages, (kMaxSmem - 1024 - 256) / stage_bytes);
+    int tmem_cols = 32;
+    while (tmem_cols < 2 * BN) tmem_cols *= 2;
+
+    CdgParams &p = h->prm;
+    std::memset(&p, 0, sizeof p);
+    p.N = N; p.H = H; p.W = W; p.C = C; p.K = K; p.P = P; p.Q = Q; p.stride = stride;
+    p.BN = BN;
+    p.KB = ceil_div(K, CDG_BK);
+    p.stages = stages;
+    p.tiles_n = tiles_n;
+    p.nphases = static_cast<int>(phases.size());
+    p.total_items = items;
+    p.a_flat = flat ? 1 : 0;
+    p.box_w = bw; p.box_h = bh; p.box_n = bnb;
+    const uint32_t ab = dtype == CDG_BF16 ? 1u : 0u;
+    p.idesc = (1u << 4) | (ab << 7) | (ab << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
+              (static_cast<uint32_t>(CDG_BM >> 4) << 24);
+    p.tx_bytes = static_cast<uint32_t>((flat ? CDG_BM : bw * bh * bnb) * 128 + BN * 128);
+    p.tmem_cols = static_cast<uint32_t>(tmem_cols);
+    p.acc_stride = static_cast<uint32_t>(tmem_cols / 2);
+    for (size_t i = 0; i < phases.size(); ++i) p.phase[i] = phases[i];
+    for (size_t i = 0; i < taps.size(); ++i) p.tap[i] = taps[i];
+
+    h->smem = static_cast<size_t>(1024 + stages * stage_bytes + 256);
+    h->grid = std::max(1, std::min(num_sms, items));
+
+    cdg_plan_info_t &inf = h->info;
+    std::memset(&inf, 0, sizeof inf);
+    inf.P = P; inf.Q = Q;
+    inf.num_phases = stride * stride;
+    for (int i = 0; i < stride * stride; ++i) inf.phase_taps[i] = phase_taps_by_index[i];
+    inf.tile_m = CDG_BM; inf.tile_n = BN; inf.tile_k = CDG_BK;
+    inf.a_mode = flat ? 1 : 0;
+    inf.box_w = bw; inf.box_h = bh; inf.box_n = bnb;
+    inf.stages = stages;
+    inf.work_items = items;
+    inf.grid = h->grid;
+    inf.smem_bytes = static_cast<int>(h->smem);
+    inf.tmem_cols = tmem_cols;
+
+    if (!host_only) {
+        if (cudaGetDevice(&h->device) != cudaSuccess ||
+            cdg_prepare_dgrad(h->out_type, h->in_type, h->mask, h->smem) != cudaSuccess ||
+            cudaMalloc(&h->d_status, sizeof(int)) != cudaSuccess ||
+            cudaMemset(h->d_status, 0, sizeof(int)) != cudaSuccess) {
+            if (h->d_status) cudaFree(h->d_status);
+            delete h;
+            return CDG_ERR_CUDA;
+        }
+    }
+    *out = h;
+    return CDG_OK;
+}
+
+bool overlaps(const void *a, size_t na, const void *b, size_t nb)
+{
+    const char *pa = static_cast<const char *>(a), *pb = static_cast<const char *>(b);
+    return pa < pb + nb && pb < pa + na;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+CUtensorMapDataType tmap_type(int dtype)
+{
+    return dtype == CDG_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+}
+
+int encode_maps(cdg_plan_st *h, const void *dY, const void *Wp)
+{
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return CDG_ERR_CUDA;
+    CdgParams &p = h->prm;
+    const cuuint32_t ones[4] = {1, 1, 1, 1};
+    const CUtensorMapDataType dt = tmap_type(h->dtype);
+    CUresult r;
+    if (p.a_flat) {
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(h->K), static_cast<cuuint64_t>(1LL * h->N * h->P * h->Q)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(h->K) * 2};
+        const cuuint32_t box[2] = {CDG_BK, CDG_BM};
+        r = enc(&p.tmA, dt, 2, const_cast<void *>(dY), dims, strides, box, ones, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        const cuuint64_t dims[4] = {static_cast<cuuint64_t>(h->K), static_cast<cuuint64_t>(h->Q),
+                                    static_cast<cuuint64_t>(h->P), static_cast<cuuint64_t>(h->N)};
+        const cuuint64_t strides[3] = {static_cast<cuuint64_t>(h->K) * 2, static_cast<cuuint64_t>(h->Q) * h->K * 2,
+                                       static_cast<cuuint64_t>(h->P) * h->Q * h->K * 2};
+        const cuuint32_t box[4] = {CDG_BK, static_cast<cuuint32_t>(p.box_w), static_cast<cuuint32_t>(p.box_h),
+                                   static_cast<cuuint32_t>(p.box_n)};
+        r = enc(&p.tmA, dt, 4, const_cast<void *>(dY), dims, strides, box, ones, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
+    if (r != CUDA_SUCCESS) return CDG_ERR_CUDA;
+    const cuuint64_t bdims[3] = {static_cast<cuuint64_t>(h->K), static_cast<cuuint64_t>(h->C),
+                                 static_cast<cuuint64_t>(h->R) * h->S};
+    const cuuint64_t bstrides[2] = {static_cast<cuuint64_t>(h->K) * 2, static_cast<cuuint64_t>(h->C) * h->K * 2};
+    const cuuint32_t bbox[3] = {CDG_BK, static_cast<cuuint32_t>(p.BN), 1};
+    r = enc(&p.tmB, dt, 3, const_cast<void *>(Wp), bdims, bstrides, bbox, ones, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return CDG_ERR_CUDA;
+    h->cached_dY = dY;
+    h->cached_Wp = Wp;
+    return CDG_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int cdg_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int pad, int dil, int dtype, int epilogue,
+             cdg_handle_t *out)
+{
+    if (out) *out = nullptr;
+    int dev = 0, sms = 0;
+    // validate first so that argument errors never depend on a device
+    cdg_handle_t probe = nullptr;
+    int rc = make_plan(N, H, W, C, K, R, S, stride, pad, dil, dtype, epilogue, 1, true, &probe);
+    if (rc != CDG_OK) return rc;
+    cdg_destroy(probe);
+    if (cudaGetDevice(&dev) != cudaSuccess) return CDG_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+        return CDG_ERR_CUDA;
+    return make_plan(N, H, W, C, K, R, S, stride, pad, dil, dtype, epilogue, sms, false, out);
+}
+
+int cdg_plan_host(int N, int H, int W, int C, int K, int R, int S, int stride, int pad, int dil, int dtype,
+                  int epilogue, int num_sms, cdg_handle_t *out)
+{
+    if (num_sms < 1) {
+        if (out) *out = nullptr;
+        return CDG_ERR_INVALID_ARG;
+    }
+    return make_plan(N, H, W, C, K, R, S, stride, pad, dil, dtype, epilogue, num_sms, true, out);
+}
+
+void cdg_destroy(cdg_handle_t h)
+{
+    if (!h) return;
+    if (h->d_status) cudaFree(h->d_status);
+    delete h;
+}
+
+int cdg_get_output_dims(cdg_handle_t h, int *P, int *Q)
+{
+    if (!h || !P || !Q) return CDG_ERR_INVALID_ARG;
+    *P = h->P;
+    *Q = h->Q;
+    return CDG_OK;
+}
+
+size_t cdg_packed_weight_bytes(cdg_handle_t h)
+{
+    if (!h) return 0;
+    return static_cast<size_t>(h->R) * h->S * h->C * h->K * 2;
+}
+
+int cdg_plan_get_info(cdg_handle_t h, cdg_plan_info_t *info)
+{
+    if (!h || !info) return CDG_ERR_INVALID_ARG;
+    *info = h->info;
+    return CDG_OK;
+}
+
+int cdg_prepack_weights(cdg_handle_t h, const void *W_krsc, void *Wpacked, cdg_stream_t stream)
+{
+    if (!h || !W_krsc || !Wpacked) return CDG_ERR_INVALID_ARG;
+    if (h->host_only) return CDG_ERR_NO_DEVICE;
+    if (!aligned16(W_krsc) || !aligned16(Wpacked)) return CDG_ERR_ALIGNMENT;
+    const size_t nb = cdg_packed_weight_bytes(h);
+    if (overlaps(W_krsc, nb, Wpacked, nb)) return CDG_ERR_ALIAS;
+    if (cdg_launch_prepack(W_krsc, Wpacked, h->K, h->R * h->S, h->C, static_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
+        return CDG_ERR_CUDA;
+    return CDG_OK;
+}
+
+int cdg_dgrad(cdg_handle_t h, const void *dY, const void *Wpacked, void *dX, const void *relu_mask,
+              cdg_stream_t stream)
+{
+    if (!h || !dY || !Wpacked || !dX) return CDG_ERR_INVALID_ARG;
+    if (h->mask != (relu_mask != nullptr)) return CDG_ERR_INVALID_ARG;
+    if (h->host_only) return CDG_ERR_NO_DEVICE;
+    if (!aligned16(dY) || !aligned16(Wpacked) || !aligned16(dX) || (relu_mask && !aligned16(relu_mask)))
+        return CDG_ERR_ALIGNMENT;
+    const size_t dx_bytes = static_cast<size_t>(h->N) * h->H * h->W * h->C * (h->out_type == CDG_T_F32 ? 4 : 2);
+    const size_t dy_bytes = static_cast<size_t>(h->N) * h->P * h->Q * h->K * 2;
+    const size_t x_bytes = static_cast<size_t>(h->N) * h->H * h->W * h->C * 2;
+    if (overlaps(dX, dx_bytes, dY, dy_bytes) || overlaps(dX, dx_bytes, Wpacked, cdg_packed_weight_bytes(h)) ||
+        (relu_mask && overlaps(dX, dx_bytes, relu_mask, x_bytes)))
+        return CDG_ERR_ALIAS;
+    if (dY != h->cached_dY || Wpacked != h->cached_Wp) {
+        const int rc = encode_maps(h, dY, Wpacked);
+        if (rc != CDG_OK) return rc;
+    }
+    CdgParams &p = h->prm;
+    p.dX = dX;
+    p.mask = relu_mask;
+    p.status = h->d_status;
+    if (cdg_launch_dgrad(p, h->out_type, h->in_type, h->mask, h->grid, h->smem, static_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
+        return CDG_ERR_CUDA;
+    return CDG_OK;
+}
+
+int cdg_device_status(cdg_handle_t h, cdg_stream_t stream)
+{
+    if (!h) return CDG_ERR_INVALID_ARG;
+    if (h->host_only) return CDG_ERR_NO_DEVICE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int v = 0;
+    if (cudaMemcpyAsync(&v, h->d_status, sizeof v, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return CDG_ERR_CUDA;
+    if (v != 0) {
+        if (cudaMemsetAsync(h->d_status, 0, sizeof(int), s) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess)
+            return CDG_ERR_CUDA;
+    }
+    return v;
+}
+
+const char *cdg_status_string(int status)
+{
+    switch (status) {
+    case CDG_OK: return "ok";
+    case CDG_ERR_INVALID_ARG: return "invalid argument";
+    case CDG_ERR_UNSUPPORTED: return "unsupported shape (C and K must be multiples of 8, stride <= 4, R*S <= 128)";
+    case CDG_ERR_ALIGNMENT: return "tensor pointer not 16-byte aligned";
+    case CDG_ERR_ALIAS: return "dX overlaps an input tensor";
+    case CDG_ERR_CUDA: return "CUDA runtime or launch error";
+    case CDG_ERR_TIMEOUT: return "device pipeline wait timed out";
+    case CDG_ERR_NO_DEVICE: return "handle was planned without a device";
+    default: return "unknown status";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,62 @@
+// Launch parameters shared by the host planner (cdg_api.cu) and the sm_103a
+// dgrad kernel (dgrad_sm103.cu).  Passed by value as one __grid_constant__
+// kernel argument, so the TMA descriptors live in parameter space.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#define CDG_MAX_PHASES 16   // stride <= 4
+#define CDG_MAX_TAPS 128    // R * S <= 128
+#define CDG_BM 128          // dX pixels per tile = TMEM lanes = UMMA M
+#define CDG_BK 64           // dY channels per pipeline stage (128 B of fp16/bf16)
+#define CDG_MAX_DYN_SMEM 232448  // sm_103 opt-in dynamic shared memory per CTA (227 KB)
+#define CDG_THREADS 192     // warp 0 TMA producer, warp 1 MMA issuer, warps 2-5 epilogue
+#define CDG_WAIT_LIMIT_NS 4000000000ull  // a pipeline wait gives up after 4 s
+
+// One phase sub-convolution of a (possibly strided) dgrad.  The dX pixels with
+// h = stride*i + ph, w = stride*j + pw (0 <= i < hph, 0 <= j < wph) form the
+// phase sub-grid; the filter taps whose contributions land on it are
+// tap[tap_begin .. tap_begin + tap_count), each reading dY at (i + dr, j + ds).
+struct CdgPhase {
+    int ph, pw;
+    int hph, wph;
+    int tap_begin, tap_count;
+    int linear;            // tile rows = a linear range of (n, i, j); else 4-D boxes
+    int tiles_w, tiles_h;  // 4-D box tiles along j and i
+    int tiles_m;           // M tiles of this phase
+    int item_begin;        // first work item of this phase in the launch
+};
+
+struct CdgTap {
+    int16_t dr, ds;  // dY row/column offset relative to the phase sub-grid position
+    int16_t t;       // tap index r*S + s into the packed weights
+    int16_t unused;
+};
+
+struct __align__(64) CdgParams {
+    CUtensorMap tmA;  // dY: 4-D {K, Q, P, N} halo boxes, or 2-D {K, N*P*Q} rows
+    CUtensorMap tmB;  // packed weights: 3-D {K, C, R*S}
+    void *dX;
+    const void *mask;
+    int *status;
+    int N, H, W, C, K, P, Q, stride;
+    int BN, KB, stages, tiles_n, nphases, total_items;
+    int a_flat, box_w, box_h, box_n;
+    uint32_t idesc;       // tcgen05 instruction descriptor (kind::f16, M=128, N=BN)
+    uint32_t tx_bytes;    // bytes one pipeline stage receives (A box + B box)
+    uint32_t tmem_cols;   // allocated TMEM columns (two accumulators)
+    uint32_t acc_stride;  // column offset of the second accumulator
+    CdgPhase phase[CDG_MAX_PHASES];
+    CdgTap tap[CDG_MAX_TAPS];
+};
+
+// Element types of dX and of the gate input, as kernel template arguments.
+enum { CDG_T_F16 = 0, CDG_T_BF16 = 1, CDG_T_F32 = 2 };
+
+// Launchers implemented in dgrad_sm103.cu.
+cudaError_t cdg_launch_dgrad(const CdgParams &p, int out_type, int in_type, bool mask,
+                             int grid, size_t smem, cudaStream_t stream);
+cudaError_t cdg_prepare_dgrad(int out_type, int in_type, bool mask, size_t smem);
+cudaError_t cdg_launch_prepack(const void *W, void *Wp, int K, int T, int C, cudaStream_t stream);

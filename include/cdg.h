@@ -1,0 +1,163 @@
+/*
+ * cdg.h -- Conv2d backward-data (dgrad) on one NVIDIA GB300 (sm_103a).
+ *
+ * The operation (apache/tvm PR #10110, "[CUTLASS] Conv2d dgrad", opening
+ * description: "Conv2d dgrad"; the stride-2 case is the "strided dgrad" of the
+ * benchmark comment on the same page):
+ *
+ *     dX[n,h,w,c] = sum over k, r, s and every (p, q) with
+ *                   h = p*stride - pad + r*dil,  w = q*stride - pad + s*dil,
+ *                   0 <= p < P, 0 <= q < Q,   of  dY[n,p,q,k] * W[k,r,s,c]
+ *
+ * the gradient of a cross-correlation Conv2d with respect to its input.
+ * P = floor((H + 2*pad - dil*(R-1) - 1)/stride) + 1, Q likewise with W and S.
+ * Inputs are fp16 or bf16; every product is accumulated in fp32 (the page's
+ * closing remark that training needs fp32 accumulation).  Optionally the
+ * result is gated by a saved activation x, out = (x > 0) ? dX : +0.0 (the
+ * dgrad "activation fusion" of the page's last comments).
+ *
+ * Layouts: dY  NHWC  [N][P][Q][K]
+ *          W   KRSC  [K][R][S][C]      (the forward filter, as stored)
+ *          dX  NHWC  [N][H][W][C]      (fp16/bf16 like dY, or fp32)
+ *          x   NHWC  [N][H][W][C]      (same type as dY)
+ * All tensors are dense and contiguous.  Every pointer passed to prepack or
+ * dgrad is a DEVICE pointer, 16-byte aligned.
+ *
+ * Ownership: the caller owns all tensors and streams; the library never
+ * allocates, frees or retains caller memory.  A handle owns its host plan
+ * and a 4-byte device status word.  Calls are asynchronous on the given stream.
+ *
+ * Errors: every function returns a cdg_status_t; nothing aborts or throws
+ * across this interface.  On any error other than CDG_ERR_CUDA nothing has
+ * been launched.
+ *
+ * Thread safety: a handle may be used from one thread at a time; calls on one
+ * handle from different streams must not overlap on the GPU (they share the
+ * handle's status word and its cached descriptors).
+ */
+#ifndef CDG_H
+#define CDG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct cdg_plan_st *cdg_handle_t;
+/* A cudaStream_t, passed as an opaque pointer (NULL = the legacy default stream). */
+typedef void *cdg_stream_t;
+
+typedef enum {
+    CDG_OK = 0,
+    CDG_ERR_INVALID_ARG = 1,  /* bad size, NULL pointer, unknown flag            */
+    CDG_ERR_UNSUPPORTED = 2,  /* valid but outside what the kernels handle:       */
+                              /* C or K not a multiple of 8, stride > 4,          */
+                              /* R*S > 128, tensor dims beyond TMA limits         */
+    CDG_ERR_ALIGNMENT = 3,    /* a tensor pointer is not 16-byte aligned          */
+    CDG_ERR_ALIAS = 4,        /* dX overlaps dY, the packed weights or x          */
+    CDG_ERR_CUDA = 5,         /* a CUDA runtime/driver call or launch failed      */
+    CDG_ERR_TIMEOUT = 6,      /* a kernel gave up a bounded pipeline wait         */
+    CDG_ERR_NO_DEVICE = 7     /* the handle was planned without a device          */
+} cdg_status_t;
+
+typedef enum { CDG_F16 = 0, CDG_BF16 = 1 } cdg_dtype_t;
+
+/* Epilogue flags (bit set). */
+enum {
+    CDG_EPI_RELU_BWD = 1, /* gate by the saved activation: out = (x > 0) ? v : +0.0 */
+    CDG_EPI_OUT_F32 = 2   /* write dX as fp32 instead of the input type             */
+};
+
+/*
+ * Plan one dgrad shape on the current CUDA device.
+ *   N, H, W    batch and dX spatial size (the forward input size)
+ *   C, K       dX channels and dY channels (forward in / out channels)
+ *   R, S       filter size; stride, pad, dil apply to both axes, pad symmetric
+ *   dtype      CDG_F16 or CDG_BF16 for dY, W and x
+ *   epilogue   CDG_EPI_* bit set
+ * On success *out receives a handle (free it with cdg_destroy).  Validation:
+ * all sizes >= 1 (pad >= 0), P and Q >= 1, C % 8 == 0, K % 8 == 0, stride <= 4,
+ * R*S <= 128.  The plan derives P and Q, splits a strided problem into its
+ * stride^2 phase sub-convolutions (each dX pixel residue class (h mod stride,
+ * w mod stride) receives a fixed subset of the filter taps), chooses tiles and
+ * allocates the 4-byte device status word.
+ */
+int cdg_plan(int N, int H, int W, int C, int K, int R, int S,
+             int stride, int pad, int dil, int dtype, int epilogue, cdg_handle_t *out);
+
+/*
+ * The same planning without touching any GPU: num_sms stands in for the
+ * device's SM count.  The handle answers the query functions below; prepack
+ * and dgrad on it return CDG_ERR_NO_DEVICE.  For inspecting the planner.
+ */
+int cdg_plan_host(int N, int H, int W, int C, int K, int R, int S,
+                  int stride, int pad, int dil, int dtype, int epilogue,
+                  int num_sms, cdg_handle_t *out);
+
+/* Release a handle (NULL is ignored).  Synchronises nothing. */
+void cdg_destroy(cdg_handle_t h);
+
+/* dY's spatial extents P and Q. */
+int cdg_get_output_dims(cdg_handle_t h, int *P, int *Q);
+
+/* Bytes the packed-weight buffer must have (R*S*C*K elements of dtype). */
+size_t cdg_packed_weight_bytes(cdg_handle_t h);
+
+/*
+ * Planner description, for logs and tests.
+ */
+typedef struct {
+    int P, Q;
+    int num_phases;       /* stride^2                                            */
+    int phase_taps[16];   /* taps of phase (ph, pw) at index ph*stride + pw       */
+    int tile_m;           /* dX pixels per tile (GEMM M tile)                      */
+    int tile_n;           /* channels per tile (GEMM N tile)                       */
+    int tile_k;           /* dY channels per pipeline stage (GEMM K block)         */
+    int a_mode;           /* 0: 4-D halo boxes over dY, 1: dY rows as a 2-D matrix */
+    int box_w, box_h, box_n; /* 4-D box (a_mode 0)                                 */
+    int stages;           /* shared-memory pipeline depth                          */
+    int work_items;       /* (phase, m-tile, n-tile) items in one launch           */
+    int grid;             /* persistent CTAs                                       */
+    int smem_bytes;       /* dynamic shared memory per CTA                         */
+    int tmem_cols;        /* tensor-memory columns per CTA                         */
+} cdg_plan_info_t;
+
+int cdg_plan_get_info(cdg_handle_t h, cdg_plan_info_t *info);
+
+/*
+ * Re-lay the forward filter W (KRSC, dtype, device) into the packed operand
+ * the dgrad kernel reads: Wpacked[r*S + s][c][k] = W[k][r][s][c], i.e. for
+ * every tap a C x K matrix with K contiguous.  Wpacked must hold
+ * cdg_packed_weight_bytes(h) bytes and not overlap W.  Asynchronous on stream.
+ */
+int cdg_prepack_weights(cdg_handle_t h, const void *W_krsc, void *Wpacked, cdg_stream_t stream);
+
+/*
+ * dX = dgrad(dY, W) for the planned shape, one kernel launch, asynchronous
+ * on stream.  relu_mask is the saved activation x (NULL unless the plan has
+ * CDG_EPI_RELU_BWD).  Every element of dX is written, including pixels no
+ * filter tap reaches (+0.0); dX is never read, so its prior contents do not
+ * matter.  dY, Wpacked and x are only read.  No workspace, no allocation.
+ * A device-side pipeline timeout (which a correct launch never hits) is
+ * reported by cdg_device_status, not here.
+ */
+int cdg_dgrad(cdg_handle_t h, const void *dY, const void *Wpacked, void *dX,
+              const void *relu_mask, cdg_stream_t stream);
+
+/*
+ * Synchronise stream, then read and clear the handle's device status word:
+ * CDG_OK, or CDG_ERR_TIMEOUT if a launch since the last call gave up a
+ * bounded wait (its dX is then incomplete).
+ */
+int cdg_device_status(cdg_handle_t h, cdg_stream_t stream);
+
+/* Static text for a status code. */
+const char *cdg_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CDG_H */

@@ -1,0 +1,142 @@
+"""Host-only checks of the C-ABI library: it loads, exports what include/cdg.h
+declares, validates arguments without a device, and plans the phase
+decomposition of strided dgrad as the definition requires."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import implicit_gemm_dgrad_gb300 as cdg
+from implicit_gemm_dgrad_gb300.workloads import ALL
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "cdg.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(cdg_[a-z_0-9]+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = cdg.load_library()
+    names = declared_functions()
+    assert len(names) >= 10, names
+    for name in names:
+        assert hasattr(lib, name), f"{name} declared in cdg.h but not exported"
+    assert set(names) == set(cdg.EXPORTS)
+
+
+def test_status_strings():
+    for code in range(0, 8):
+        s = cdg.status_string(code)
+        assert s and s != "unknown status"
+    assert cdg.status_string(99) == "unknown status"
+
+
+def _plan_rc(*args, host=True):
+    lib = cdg.load_library()
+    h = ctypes.c_void_p()
+    if host:
+        rc = lib.cdg_plan_host(*args, 148, ctypes.byref(h))
+    else:
+        rc = lib.cdg_plan(*args, ctypes.byref(h))
+    if h.value:
+        lib.cdg_destroy(h)
+    return rc
+
+
+GOOD = (2, 8, 8, 16, 16, 3, 3, 1, 1, 1, cdg.BF16, 0)
+
+
+@pytest.mark.parametrize("host", [True, False])
+@pytest.mark.parametrize("field,value,expect", [
+    (0, 0, 1), (1, 0, 1), (3, 0, 1), (5, 0, 1), (7, 0, 1), (8, -1, 1), (9, 0, 1),
+    (10, 2, 1), (11, 4, 1),
+    (3, 12, 2), (4, 20, 2), (7, 5, 2),
+])
+def test_argument_validation_needs_no_device(host, field, value, expect):
+    args = list(GOOD)
+    args[field] = value
+    assert _plan_rc(*args, host=host) == expect
+
+
+def test_geometry_too_small_is_invalid():
+    # H + 2*pad - dil*(R-1) - 1 < 0: empty forward output
+    assert _plan_rc(1, 2, 2, 8, 8, 5, 5, 1, 0, 1, cdg.F16, 0) == 1
+
+
+def test_filter_too_large_is_unsupported():
+    assert _plan_rc(1, 40, 40, 8, 8, 12, 12, 1, 5, 1, cdg.F16, 0) == 2
+
+
+def test_host_plan_refuses_device_work():
+    p = cdg.plan_host(1, 8, 8, 16, 16, 3, 3, 1, 1, 1, "f16")
+    with pytest.raises(cdg.CdgError) as e:
+        p.dgrad(16, 16, 1024 * 1024)
+    assert e.value.status == 7
+    with pytest.raises(cdg.CdgError) as e:
+        p.prepack_weights(16, 1024 * 1024)
+    assert e.value.status == 7
+
+
+def test_misaligned_and_aliased_pointers_rejected_before_launch():
+    p = cdg.plan_host(1, 8, 8, 16, 16, 3, 3, 1, 1, 1, "f16")
+    # host-only handles report NO_DEVICE after argument checks of NULLs
+    with pytest.raises(cdg.CdgError) as e:
+        p.dgrad(0, 16, 32)
+    assert e.value.status == 1
+    q = cdg.plan_host(1, 8, 8, 16, 16, 3, 3, 1, 1, 1, "f16", relu=True)
+    with pytest.raises(cdg.CdgError) as e:  # gated plan without a gate tensor
+        q.dgrad(16, 16, 4096, None)
+    assert e.value.status == 1
+
+
+@pytest.mark.parametrize("R,stride,pad,expect", [
+    (3, 2, 1, [1, 2, 2, 4]),   # 3x3 stride 2, pad 1: even h = 2p-1+r needs r = 1; odd h takes r in {0, 2}
+    (1, 2, 0, [1, 0, 0, 0]),   # 1x1 stride 2: three of four phases receive no tap
+    (3, 1, 1, [9]),
+    (3, 3, 1, [1, 1, 1, 1, 1, 1, 1, 1, 1]),
+    (5, 2, 2, [9, 6, 6, 4]),
+])
+def test_phase_tap_counts(R, stride, pad, expect):
+    p = cdg.plan_host(2, 16, 16, 32, 32, R, R, stride, pad, 1, "bf16")
+    info = p.info()
+    assert info["num_phases"] == stride * stride
+    assert info["phase_taps"] == expect
+    assert sum(info["phase_taps"]) == R * R
+
+
+def test_phase_taps_match_definition_bruteforce():
+    """Each tap lands in exactly the phase (h mod s, w mod s) the definition puts it in."""
+    for R, S, stride, pad, dil in [(3, 3, 2, 1, 1), (3, 2, 3, 2, 2), (5, 5, 4, 2, 1), (2, 3, 2, 0, 3)]:
+        H = W = 24
+        p = cdg.plan_host(1, H, W, 8, 8, R, S, stride, pad, dil, "f16")
+        counts = [0] * (stride * stride)
+        for r in range(R):
+            for s in range(S):
+                # any p, q: h = p*stride - pad + r*dil -> residue of h
+                ph = (-pad + r * dil) % stride
+                pw = (-pad + s * dil) % stride
+                counts[ph * stride + pw] += 1
+        assert p.info()["phase_taps"] == counts
+
+
+def test_workload_plans():
+    for L in ALL:
+        p = cdg.plan_host(L.N, L.H, L.W, L.C, L.K, L.R, L.S, L.stride, L.pad, L.dil, L.dtype,
+                          relu=L.relu, out_f32=(L.out == "f32"), num_sms=148)
+        info = p.info()
+        assert (info["P"], info["Q"]) == (L.P, L.Q), L.name
+        assert info["smem_bytes"] <= 232448
+        assert info["stages"] >= 3
+        assert info["tmem_cols"] <= 512 and info["tmem_cols"] >= 2 * info["tile_n"]
+        assert info["grid"] <= 148
+        if L.R == 1 and L.pad == 0:
+            assert info["a_mode"] == 1
+        else:
+            assert info["box_w"] * info["box_h"] * info["box_n"] <= 128
+        assert p.packed_weight_bytes == 2 * L.K * L.R * L.S * L.C

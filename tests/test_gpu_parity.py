@@ -1,0 +1,162 @@
+"""GPU parity: the sm_103a library against the CPU oracle, element by element.
+
+Bar (per element): |gpu - oracle| <= 2e-3*max(1,|oracle|) for fp32 dX and
+1e-2*max(1,|oracle|) for fp16/bf16 dX; integer inputs must give the oracle's
+value rounded once to the output type, bit for bit; the ReLU-backward gate
+must leave +0.0 at exactly the gated-off positions.  dX is pre-filled with NaN
+(or garbage) and surrounded by sentinel guard bands for every call.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from implicit_gemm_dgrad_gb300 import synth
+from implicit_gemm_dgrad_gb300.workloads import BATCH8, TINY, Layer
+
+from gpu_util import GpuRun, assert_close, check_gate_zero_pattern, decode_out
+
+pytestmark = pytest.mark.gpu
+
+
+def oracle_full(run: GpuRun) -> np.ndarray:
+    L = run.layer
+    return oracle.dgrad(run.dY, run.W, L.H, L.W, L.stride, L.pad, L.dil, x=run.x, dtype=L.dtype)
+
+
+def check_layer(L, prefill="nan", dist=None):
+    run = GpuRun(L, dist=dist, prefill=prefill)
+    run.run()
+    got = run.result()
+    assert run.out.guards_intact(), "write outside dX"
+    assert run.status() == 0
+    ref = oracle_full(run)
+    assert_close(got, ref, run.odt, L.name)
+    if L.relu:
+        check_gate_zero_pattern(run.result_bytes(), run.x, run.odt, L.dtype)
+    return run, got, ref
+
+
+def test_tiny_config():
+    check_layer(TINY)
+
+
+@pytest.mark.parametrize("L", BATCH8, ids=lambda L: L.name)
+def test_batch8_configs(L):
+    check_layer(L)
+
+
+def _case(N, H, W, C, K, R, S, stride, pad, dil, dtype, out="same", relu=False, idx=0):
+    return Layer(f"N{N}H{H}W{W}C{C}K{K}R{R}S{S}s{stride}p{pad}d{dil}{dtype}{out}{'relu' if relu else ''}",
+                 N, H, W, C, K, R, S, stride, pad, dil, dtype=dtype, out=out, relu=relu,
+                 dist="normal", workload=9, index=idx)
+
+
+SWEEP = [
+    _case(2, 9, 7, 24, 40, 3, 3, 1, 1, 1, "bf16"),
+    _case(2, 11, 13, 72, 136, 3, 3, 2, 1, 1, "f16", relu=True),
+    _case(3, 10, 9, 8, 8, 1, 1, 2, 0, 1, "bf16", out="f32"),
+    _case(2, 7, 7, 136, 72, 1, 1, 1, 0, 1, "bf16"),
+    _case(1, 12, 10, 16, 24, 5, 3, 3, 2, 2, "f16", out="f32"),
+    _case(2, 9, 9, 40, 24, 2, 3, 2, 2, 1, "bf16", relu=True),
+    _case(4, 6, 5, 264, 80, 3, 3, 1, 1, 2, "bf16"),
+    _case(1, 1, 3, 8, 8, 1, 1, 2, 0, 1, "f16"),            # phase with no dX row (H < stride)
+    _case(2, 13, 11, 32, 16, 3, 3, 4, 1, 1, "bf16"),       # 16 phases
+    _case(3, 5, 17, 48, 200, 1, 1, 1, 1, 1, "f16", out="f32"),  # 1x1 with padding: box path
+    _case(1, 30, 30, 520, 64, 3, 3, 1, 1, 1, "bf16"),       # C > 256: several N tiles
+    _case(2, 14, 14, 64, 520, 3, 3, 2, 1, 1, "f16", relu=True),
+    _case(5, 3, 4, 16, 8, 3, 3, 1, 2, 1, "bf16"),           # dX smaller than the halo
+    _case(1, 57, 3, 16, 16, 3, 1, 1, 1, 1, "f16"),          # tall and narrow
+    _case(2, 16, 16, 8, 8, 7, 7, 2, 3, 1, "bf16", out="f32"),
+]
+
+
+@pytest.mark.parametrize("L", SWEEP, ids=lambda L: L.name)
+def test_shape_sweep(L):
+    check_layer(L)
+
+
+@pytest.mark.parametrize("prefill", ["nan", "garbage"])
+def test_prior_contents_do_not_matter(prefill):
+    L = _case(2, 9, 9, 40, 24, 3, 3, 2, 1, 1, "bf16", relu=True)
+    _, got, _ = check_layer(L, prefill=prefill)
+
+
+@pytest.mark.parametrize("L", [
+    _case(2, 9, 7, 24, 40, 3, 3, 1, 1, 1, "bf16"),
+    _case(2, 11, 13, 72, 136, 3, 3, 2, 1, 1, "f16"),
+    _case(2, 10, 12, 16, 32, 3, 3, 3, 1, 2, "f16", out="f32"),
+    _case(3, 8, 8, 24, 16, 1, 1, 2, 0, 1, "bf16"),
+    _case(2, 14, 14, 264, 72, 3, 3, 1, 1, 1, "bf16"),
+], ids=lambda L: L.name)
+def test_integer_inputs_bit_exact(L):
+    """Inputs in {-2..2}: fp32 accumulation is exact, so dX = RNE(oracle) bit for bit."""
+    inputs = synth.make_inputs(L.shape(), L.dtype, "int", L.workload, L.index, with_x=L.relu)
+    run = GpuRun(L, inputs=inputs)
+    run.run()
+    raw = run.result_bytes()
+    ref = oracle_full(run)
+    if run.odt == "f32":
+        expect = ref.astype(np.float32).view(np.uint32).reshape(-1)
+        got = raw.view(np.uint32)
+    elif run.odt == "f16":
+        expect = ref.astype(np.float16).view(np.uint16).reshape(-1)
+        got = raw.view(np.uint16)
+    else:
+        expect = synth.f32_to_bf16_bits(ref.astype(np.float32)).reshape(-1)
+        got = raw.view(np.uint16)
+    mism = np.flatnonzero(got != expect)
+    assert mism.size == 0, f"{mism.size} mismatches, first at {mism[:5]}: {got[mism[:5]]} vs {expect[mism[:5]]}"
+
+
+def test_deterministic():
+    L = _case(2, 11, 13, 72, 136, 3, 3, 2, 1, 1, "bf16", relu=True)
+    run = GpuRun(L)
+    run.run()
+    a = run.result_bytes().copy()
+    run.run()
+    b = run.result_bytes()
+    assert np.array_equal(a, b)
+
+
+def test_gate_special_values():
+    """x = +0, -0, NaN, negative, subnormal, +Inf: only x > 0 passes the value through."""
+    L = _case(1, 4, 4, 16, 16, 1, 1, 1, 0, 1, "f16", relu=True)
+    dY, W, _ = synth.make_inputs(L.shape(), L.dtype, "uniform", L.workload, L.index)
+    specials = np.array([0x3C00, 0x0000, 0x8000, 0x7E00, 0xBC00, 0x0001, 0x7C00, 0xFE00], np.uint16)
+    x = np.resize(specials, (1, 4, 4, 16)).astype(np.uint16)
+    run = GpuRun(L, inputs=(dY, W, x))
+    run.run()
+    raw = run.result_bytes()
+    check_gate_zero_pattern(raw, x, run.odt, "f16")
+    got = decode_out(raw, run.odt).reshape(1, 4, 4, 16)
+    ref = oracle.dgrad(dY, W, 4, 4, 1, 0, 1, x=x, dtype="f16")
+    assert_close(got, ref, run.odt, "specials")
+
+
+def test_empty_phases_written_zero_and_linear_in_dY():
+    """1x1 stride 2: odd rows/columns of dX are +0.0 exactly; dgrad(2*dY) = 2*dgrad(dY)."""
+    L = _case(2, 12, 10, 32, 48, 1, 1, 2, 0, 1, "bf16", out="f32")
+    run = GpuRun(L)
+    run.run()
+    got = run.result()
+    bits = run.result_bytes().view(np.uint32).reshape(got.shape)
+    assert np.all(bits[:, 1::2] == 0) and np.all(bits[:, :, 1::2] == 0)
+    dY2 = synth.to_bits(2 * synth.bits_to_f32(run.dY, "bf16"), "bf16")
+    run2 = GpuRun(L, inputs=(dY2, run.W, None))
+    run2.run()
+    np.testing.assert_array_equal(run2.result(), 2 * got)
+
+
+def test_interleaved_plans():
+    """Plans of different shapes (different shared-memory sizes, same kernel
+    instantiation) stay valid when used after one another in any order."""
+    cases = [_case(2, 9, 7, 256, 64, 3, 3, 1, 1, 1, "bf16"), _case(2, 9, 7, 16, 64, 3, 3, 1, 1, 1, "bf16"),
+             _case(2, 8, 8, 64, 64, 1, 1, 2, 0, 1, "bf16")]
+    runs = [GpuRun(L) for L in cases]
+    for run in reversed(runs):
+        run.run()
+    for run in runs:
+        got = run.result()
+        assert run.status() == 0
+        ref = oracle_full(run)
+        assert_close(got, ref, run.odt, run.layer.name)
