@@ -73,6 +73,7 @@ struct cdg_plan_st {
     int *d_status;
     CdgParams prm;  // tensor maps and pointers are filled per call
     const void *cached_dY, *cached_Wp;
+    void *cached_dX;
     cdg_plan_info_t info;
 };
 
@@ -110,12 +111,16 @@ void choose_box(const std::vector<CdgPhase> &phases, int N, int &bw, int &bh, in
         }
 }
 
+// GEMM N tile.  C <= 256: one tile covering C (a multiple of 16, the UMMA N
+// granule).  C > 256: several tiles, each a multiple of 64 so that the
+// epilogue's 64-channel store boxes never reach into the neighbouring tile;
+// least padding wins, larger tiles on ties.
 int choose_bn(int C)
 {
     if (C <= 256) return ((C + 15) / 16) * 16;
     int best = 256;
     long long best_waste = -1;
-    for (int bn = 256; bn >= 64; bn -= 16) {
+    for (int bn = 256; bn >= 64; bn -= 64) {
         const long long waste = 1LL * ceil_div(C, bn) * bn - C;
         if (best_waste < 0 || waste < best_waste) {
             best_waste = waste;
@@ -196,8 +201,23 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     std::stable_sort(phases.begin(), phases.end(),
                      [](const CdgPhase &a, const CdgPhase &b) { return a.tap_count > b.tap_count; });
 
-    // ---- operand mode and tiles
-    const bool flat = (R == 1 && S == 1 && pad == 0);
+    // ---- operand and store modes, tiles
+    // 1x1 pad-0 filters read dY as a plain matrix of rows.  At stride 1 a tile
+    // is 128 consecutive dX pixels; at stride s > 1 (only phase (0,0) has a
+    // tap) a tile is whole rows of the phase sub-grid, which the store map can
+    // address as one box when H is a multiple of s.  Everything else uses 4-D
+    // halo boxes over the phase sub-grids.
+    int d_mode = CDG_D_BOX4, rpt = 0, m_step = CDG_BM;
+    if (R == 1 && S == 1 && pad == 0) {
+        if (stride == 1) {
+            d_mode = CDG_D_LINEAR;
+        } else if (H % stride == 0 && Q <= CDG_BM) {
+            d_mode = CDG_D_ROWS;
+            rpt = CDG_BM / Q;
+            m_step = rpt * Q;
+        }
+    }
+    const bool flat = d_mode != CDG_D_BOX4;
     int bw = 0, bh = 0, bnb = 0;
     if (!flat) choose_box(phases, N, bw, bh, bnb);
     const int BN = choose_bn(C);
@@ -205,21 +225,27 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     int items = 0;
     for (CdgPhase &f : phases) {
         f.linear = (flat || f.tap_count == 0) ? 1 : 0;
-        if (f.linear) {
+        if (f.tap_count == 0) {
             f.tiles_w = f.tiles_h = 1;
             f.tiles_m = ceil_div(1LL * N * f.hph * f.wph, CDG_BM);
+        } else if (flat) {
+            f.tiles_w = f.tiles_h = 1;
+            f.tiles_m = ceil_div(1LL * N * P * Q, m_step);
         } else {
             f.tiles_w = ceil_div(f.wph, bw);
             f.tiles_h = ceil_div(f.hph, bh);
             f.tiles_m = f.tiles_w * f.tiles_h * ceil_div(N, bnb);
         }
         f.item_begin = items;
-        items += f.tiles_m * tiles_n;
+        f.items = f.tiles_m * tiles_n;
+        items += f.items;
     }
     const int stage_bytes = CDG_BM * 128 + BN * 128;
-    const int stages = std::min(kMaxStages, (kMaxSmem - 1024 - 256) / stage_bytes);
+    const int stages =
+        std::min(kMaxStages, (kMaxSmem - 1024 - CDG_SMEM_STAGING - CDG_SMEM_TAIL) / stage_bytes);
+    // two accumulators, each at least as wide as the 64-column chunks the epilogue reads
     int tmem_cols = 32;
-    while (tmem_cols < 2 * BN) tmem_cols *= 2;
+    while (tmem_cols < 2 * (((BN + 63) / 64) * 64)) tmem_cols *= 2;
 
     CdgParams &p = h->prm;
     std::memset(&p, 0, sizeof p);
@@ -229,9 +255,13 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     p.stages = stages;
     p.tiles_n = tiles_n;
     p.nphases = static_cast<int>(phases.size());
+    p.ntaps = static_cast<int>(taps.size());
     p.total_items = items;
     p.a_flat = flat ? 1 : 0;
     p.box_w = bw; p.box_h = bh; p.box_n = bnb;
+    p.d_mode = d_mode;
+    p.m_step = m_step;
+    p.rows_per_tile = rpt;
     const uint32_t ab = dtype == CDG_BF16 ? 1u : 0u;
     p.idesc = (1u << 4) | (ab << 7) | (ab << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
               (static_cast<uint32_t>(CDG_BM >> 4) << 24);
@@ -241,7 +271,7 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     for (size_t i = 0; i < phases.size(); ++i) p.phase[i] = phases[i];
     for (size_t i = 0; i < taps.size(); ++i) p.tap[i] = taps[i];
 
-    h->smem = static_cast<size_t>(1024 + stages * stage_bytes + 256);
+    h->smem = static_cast<size_t>(1024 + stages * stage_bytes + CDG_SMEM_STAGING + CDG_SMEM_TAIL);
     h->grid = std::max(1, std::min(num_sms, items));
 
     cdg_plan_info_t &inf = h->info;
@@ -285,12 +315,12 @@ CUtensorMapDataType tmap_type(int dtype)
     return dtype == CDG_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
 }
 
-int encode_maps(cdg_plan_st *h, const void *dY, const void *Wp)
+int encode_operand_maps(cdg_plan_st *h, const void *dY, const void *Wp)
 {
     EncodeTiledFn enc = encode_tiled();
     if (!enc) return CDG_ERR_CUDA;
     CdgParams &p = h->prm;
-    const cuuint32_t ones[4] = {1, 1, 1, 1};
+    const cuuint32_t ones[5] = {1, 1, 1, 1, 1};
     const CUtensorMapDataType dt = tmap_type(h->dtype);
     CUresult r;
     if (p.a_flat) {
@@ -319,6 +349,54 @@ int encode_maps(cdg_plan_st *h, const void *dY, const void *Wp)
     if (r != CUDA_SUCCESS) return CDG_ERR_CUDA;
     h->cached_dY = dY;
     h->cached_Wp = Wp;
+    return CDG_OK;
+}
+
+// Store maps for dX: one per phase slot that has taps (zero phases are
+// written with plain stores).  Each covers 128-byte rows (64 fp16/bf16 or 32
+// fp32 channels) with the 128-byte swizzle the epilogue's staging uses.
+int encode_store_maps(cdg_plan_st *h, void *dX)
+{
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return CDG_ERR_CUDA;
+    CdgParams &p = h->prm;
+    const cuuint32_t ones[4] = {1, 1, 1, 1};
+    const bool f32 = h->out_type == CDG_T_F32;
+    const cuuint64_t osz = f32 ? 4 : 2;
+    const cuuint32_t ch = static_cast<cuuint32_t>(128 / osz);
+    const CUtensorMapDataType dt = f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : tmap_type(h->dtype);
+    const cuuint64_t C = h->C, W = h->W, H = h->H, s = h->stride;
+    for (int i = 0; i < p.nphases; ++i) {
+        const CdgPhase &f = p.phase[i];
+        if (f.tap_count == 0) continue;
+        CUresult r;
+        if (p.d_mode == CDG_D_LINEAR) {
+            const cuuint64_t dims[2] = {C, static_cast<cuuint64_t>(h->N) * H * W};
+            const cuuint64_t strides[1] = {C * osz};
+            const cuuint32_t box[2] = {ch, CDG_BM};
+            r = enc(&p.tmD[i], dt, 2, dX, dims, strides, box, ones, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        } else if (p.d_mode == CDG_D_ROWS) {
+            // phase (0,0): rows n*hph + i are s*W*C elements apart because H = s*hph
+            const cuuint64_t dims[3] = {C, static_cast<cuuint64_t>(f.wph),
+                                        static_cast<cuuint64_t>(h->N) * static_cast<cuuint64_t>(f.hph)};
+            const cuuint64_t strides[2] = {s * C * osz, s * W * C * osz};
+            const cuuint32_t box[3] = {ch, static_cast<cuuint32_t>(f.wph), static_cast<cuuint32_t>(p.rows_per_tile)};
+            r = enc(&p.tmD[i], dt, 3, dX, dims, strides, box, ones, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        } else {
+            char *base = static_cast<char *>(dX) + (static_cast<cuuint64_t>(f.ph) * W + f.pw) * C * osz;
+            const cuuint64_t dims[4] = {C, static_cast<cuuint64_t>(f.wph), static_cast<cuuint64_t>(f.hph),
+                                        static_cast<cuuint64_t>(h->N)};
+            const cuuint64_t strides[3] = {s * C * osz, s * W * C * osz, H * W * C * osz};
+            const cuuint32_t box[4] = {ch, static_cast<cuuint32_t>(p.box_w), static_cast<cuuint32_t>(p.box_h),
+                                       static_cast<cuuint32_t>(p.box_n)};
+            r = enc(&p.tmD[i], dt, 4, base, dims, strides, box, ones, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        }
+        if (r != CUDA_SUCCESS) return CDG_ERR_CUDA;
+    }
+    h->cached_dX = dX;
     return CDG_OK;
 }
 
@@ -408,7 +486,11 @@ int cdg_dgrad(cdg_handle_t h, const void *dY, const void *Wpacked, void *dX, con
         (relu_mask && overlaps(dX, dx_bytes, relu_mask, x_bytes)))
         return CDG_ERR_ALIAS;
     if (dY != h->cached_dY || Wpacked != h->cached_Wp) {
-        const int rc = encode_maps(h, dY, Wpacked);
+        const int rc = encode_operand_maps(h, dY, Wpacked);
+        if (rc != CDG_OK) return rc;
+    }
+    if (dX != h->cached_dX) {
+        const int rc = encode_store_maps(h, dX);
         if (rc != CDG_OK) return rc;
     }
     CdgParams &p = h->prm;

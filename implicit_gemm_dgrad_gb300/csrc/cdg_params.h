@@ -14,6 +14,12 @@
 #define CDG_MAX_DYN_SMEM 232448  // sm_103 opt-in dynamic shared memory per CTA (227 KB)
 #define CDG_THREADS 192     // warp 0 TMA producer, warp 1 MMA issuer, warps 2-5 epilogue
 #define CDG_WAIT_LIMIT_NS 4000000000ull  // a pipeline wait gives up after 4 s
+// Shared memory after the operand ring: two 16 KB output staging buffers
+// (128 rows x 128 B, the box a TMA store writes), then mbarriers and flags
+// (256 B), then the phase and tap tables copied out of the parameter block.
+#define CDG_SMEM_STAGING (2 * 128 * 128)
+#define CDG_SMEM_TAIL 2048
+#define CDG_SMEM_TABLES 256
 
 // One phase sub-convolution of a (possibly strided) dgrad.  The dX pixels with
 // h = stride*i + ph, w = stride*j + pw (0 <= i < hph, 0 <= j < wph) form the
@@ -26,6 +32,7 @@ struct CdgPhase {
     int linear;            // tile rows = a linear range of (n, i, j); else 4-D boxes
     int tiles_w, tiles_h;  // 4-D box tiles along j and i
     int tiles_m;           // M tiles of this phase
+    int items;             // tiles_m * (N tiles): work items of this phase
     int item_begin;        // first work item of this phase in the launch
 };
 
@@ -35,15 +42,26 @@ struct CdgTap {
     int16_t unused;
 };
 
-struct __align__(64) CdgParams {
+// How a tile's rows map onto dX and how the epilogue's TMA store addresses them.
+enum {
+    CDG_D_BOX4 = 0,   // per-phase 4-D map {C, wph, hph, N} over the phase sub-grid; tile = box
+    CDG_D_LINEAR = 1, // 2-D map {C, N*H*W}; tile = 128 consecutive pixels (stride 1, 1x1, pad 0)
+    CDG_D_ROWS = 2    // 3-D map {C, wph, N*hph} over phase (0,0); tile = whole sub-grid rows
+};
+
+struct CdgParams {  // CUtensorMap members carry their own (128-byte) alignment
     CUtensorMap tmA;  // dY: 4-D {K, Q, P, N} halo boxes, or 2-D {K, N*P*Q} rows
     CUtensorMap tmB;  // packed weights: 3-D {K, C, R*S}
+    CUtensorMap tmD[CDG_MAX_PHASES];  // dX stores, one map per phase with taps (index = phase slot)
     void *dX;
     const void *mask;
     int *status;
     int N, H, W, C, K, P, Q, stride;
-    int BN, KB, stages, tiles_n, nphases, total_items;
+    int BN, KB, stages, tiles_n, nphases, ntaps, total_items;
     int a_flat, box_w, box_h, box_n;
+    int d_mode;           // CDG_D_*
+    int m_step;           // linear operand modes: dY rows per M tile (128, or whole sub-grid rows)
+    int rows_per_tile;    // CDG_D_ROWS: sub-grid rows per tile
     uint32_t idesc;       // tcgen05 instruction descriptor (kind::f16, M=128, N=BN)
     uint32_t tx_bytes;    // bytes one pipeline stage receives (A box + B box)
     uint32_t tmem_cols;   // allocated TMEM columns (two accumulators)

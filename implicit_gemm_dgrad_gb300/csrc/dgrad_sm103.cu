@@ -30,30 +30,16 @@ namespace cdg {
 
 constexpr int kTimeoutStatus = 6;  // CDG_ERR_TIMEOUT
 
-struct SmemLayout {
-    uint32_t base;        // 1024-aligned shared address of stage 0
-    uint32_t stage_bytes;
-    uint32_t bars;        // first mbarrier
-    int stages;
-    __device__ uint32_t a(int s) const { return base + s * stage_bytes; }
-    __device__ uint32_t b(int s) const { return base + s * stage_bytes + CDG_BM * 128; }
-    __device__ uint32_t full(int s) const { return bars + 8u * s; }
-    __device__ uint32_t empty(int s) const { return bars + 8u * (stages + s); }
-    __device__ uint32_t acc_full(int a) const { return bars + 8u * (2 * stages + a); }
-    __device__ uint32_t acc_empty(int a) const { return bars + 8u * (2 * stages + 2 + a); }
-    __device__ uint32_t drain() const { return bars + 8u * (2 * stages + 4); }
-};
-
 struct Ctl {
     volatile uint32_t *abort;
     int *status;
 };
 
-// Wait for phase `parity` of barrier `bar` to complete; false if this CTA is
-// aborting (another role gave up, or this wait ran past the limit).
-__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const Ctl &ctl)
+// Slow path of a pipeline wait: spin on try_wait (which itself suspends the
+// thread for a while) until the phase completes, the CTA aborts, or the wait
+// runs past CDG_WAIT_LIMIT_NS, in which case it records the timeout.
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, Ctl ctl)
 {
-    if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t n = 1;; ++n) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -68,119 +54,183 @@ __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const C
     }
 }
 
-struct Item {
-    int phase, mt, nt;
-};
-
-__device__ __forceinline__ Item decode_item(const CdgParams &p, int g)
+// Wait for phase `parity` of barrier `bar`; false if the CTA is aborting.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Ctl ctl)
 {
-    int ph = 0;
-    while (ph + 1 < p.nphases && g >= p.phase[ph + 1].item_begin) ++ph;
-    const int local = g - p.phase[ph].item_begin;
-    return {ph, local / p.tiles_n, local % p.tiles_n};
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_slow(bar, parity, ctl);
 }
 
+// Walk over this CTA's work items g = blockIdx.x, blockIdx.x + gridDim.x, ...
+// as (phase, index within the phase), phases read from the shared-memory copy.
+struct ItemWalk {
+    const CdgPhase *tab;
+    int nph;
+    int phase, local;
+    __device__ __forceinline__ ItemWalk(const CdgPhase *t, int n) : tab(t), nph(n), phase(0), local(blockIdx.x)
+    {
+        settle();
+    }
+    __device__ __forceinline__ void settle()
+    {
+        while (phase < nph && local >= tab[phase].items) {
+            local -= tab[phase].items;
+            ++phase;
+        }
+    }
+    __device__ __forceinline__ bool valid() const { return phase < nph; }
+    __device__ __forceinline__ void next()
+    {
+        local += gridDim.x;
+        settle();
+    }
+};
+
 // Origin (j0, i0, n0) of 4-D box tile mt of a phase.
-__device__ __forceinline__ void box_origin(const CdgParams &p, const CdgPhase &ph, int mt, int &j0, int &i0,
+__device__ __forceinline__ void box_origin(const CdgPhase &ph, int mt, int bw, int bh, int bn, int &j0, int &i0,
                                            int &n0)
 {
     const int tj = mt % ph.tiles_w;
     const int rest = mt / ph.tiles_w;
     const int ti = rest % ph.tiles_h;
     const int tn = rest / ph.tiles_h;
-    j0 = tj * p.box_w;
-    i0 = ti * p.box_h;
-    n0 = tn * p.box_n;
+    j0 = tj * bw;
+    i0 = ti * bh;
+    n0 = tn * bn;
 }
 
+struct Ring {
+    uint32_t a0;           // shared address of stage 0's A tile (1024-aligned)
+    uint32_t stage_bytes;  // A tile + B tile
+    uint32_t out0;         // first of the two 16 KB output staging buffers
+    uint32_t full0, empty0;
+    uint32_t acc_full0, acc_empty0, drain;
+};
+
 // ------------------------------------------------------------------ producer
-__device__ void run_producer(const CdgParams &p, const SmemLayout &L, const Ctl &ctl)
+// Whole warp runs the loop (converged control flow); lane 0 issues.
+__device__ __forceinline__ void run_producer(const CdgParams &p, const Ring &R, const CdgPhase *tab,
+                                             const CdgTap *taps, Ctl ctl, bool leader)
 {
+    const uint64_t mapA = reinterpret_cast<uint64_t>(&p.tmA);
+    const uint64_t mapB = reinterpret_cast<uint64_t>(&p.tmB);
+    if (leader) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(mapA) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(mapB) : "memory");
+    }
+    const int KB = p.KB, stages = p.stages, tiles_n = p.tiles_n, BN = p.BN, m_step = p.m_step;
+    const int bw = p.box_w, bh = p.box_h, bn = p.box_n;
+    const bool flat = p.a_flat != 0;
+    const uint32_t tx = p.tx_bytes;
+    const uint32_t a0 = R.a0, sbytes = R.stage_bytes, full0 = R.full0, empty0 = R.empty0;
+
     int stage = 0;
     uint32_t parity = 0;
     uint32_t used_mask = 0, last_parity = 0;  // for the final drain
     bool ok = true;
-    for (int g = blockIdx.x; ok && g < p.total_items; g += gridDim.x) {
-        const Item it = decode_item(p, g);
-        const CdgPhase &ph = p.phase[it.phase];
-        if (ph.tap_count == 0) continue;
+    for (ItemWalk w(tab, p.nphases); ok && w.valid(); w.next()) {
+        const CdgPhase &ph = tab[w.phase];
+        const int ntap = ph.tap_count;
+        if (ntap == 0) continue;
+        const int mt = tiles_n == 1 ? w.local : w.local / tiles_n;
+        const int nt = w.local - mt * tiles_n;
         int j0 = 0, i0 = 0, n0 = 0;
-        if (!p.a_flat) box_origin(p, ph, it.mt, j0, i0, n0);
-        const int c0 = it.nt * p.BN;
-        for (int tt = 0; ok && tt < ph.tap_count; ++tt) {
-            const CdgTap tap = p.tap[ph.tap_begin + tt];
-            for (int kb = 0; kb < p.KB; ++kb) {
-                if (!wait_bounded(L.empty(stage), parity ^ 1u, ctl)) {
+        if (!flat) box_origin(ph, mt, bw, bh, bn, j0, i0, n0);
+        const int c0 = nt * BN;
+        const int m0 = mt * m_step;
+        for (int tt = 0; ok && tt < ntap; ++tt) {
+            const CdgTap tap = taps[ph.tap_begin + tt];
+            const int y = j0 + tap.ds, z = i0 + tap.dr, t = tap.t;
+            for (int kb = 0; kb < KB; ++kb) {
+                const uint32_t full = full0 + 8u * stage;
+                if (!wait_bar(empty0 + 8u * stage, parity ^ 1u, ctl)) {
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(L.full(stage), p.tx_bytes);
-                if (p.a_flat)
-                    tma_load_2d(L.a(stage), &p.tmA, L.full(stage), kb * CDG_BK, it.mt * CDG_BM);
-                else
-                    tma_load_4d(L.a(stage), &p.tmA, L.full(stage), kb * CDG_BK, j0 + tap.ds, i0 + tap.dr, n0);
-                tma_load_3d(L.b(stage), &p.tmB, L.full(stage), kb * CDG_BK, c0, tap.t);
+                if (leader) {
+                    mbar_arrive_expect_tx(full, tx);
+                    const uint32_t sa = a0 + stage * sbytes;
+                    if (flat)
+                        tma_load_2d(sa, mapA, full, kb * CDG_BK, m0);
+                    else
+                        tma_load_4d(sa, mapA, full, kb * CDG_BK, y, z, n0);
+                    tma_load_3d(sa + CDG_BM * 128, mapB, full, kb * CDG_BK, c0, t);
+                }
+                __syncwarp();
                 used_mask |= 1u << stage;
                 last_parity = (last_parity & ~(1u << stage)) | (parity << stage);
-                if (++stage == p.stages) {
+                if (++stage == stages) {
                     stage = 0;
                     parity ^= 1u;
                 }
             }
         }
     }
-    // Every copy this thread started must land before the CTA may exit.  On
-    // the normal path they all have (the MMA warp waited for each) and this
+    // Every copy this warp started must land before the CTA may exit.  On the
+    // normal path they all have (the MMA warp waited for each) and this
     // returns at once; after an abort it waits, bounded, for copies in flight.
     volatile uint32_t no_abort = 0;
     const Ctl drain_ctl{&no_abort, ctl.status};
-    for (int s = 0; s < p.stages; ++s)
-        if (used_mask & (1u << s)) wait_bounded(L.full(s), (last_parity >> s) & 1u, drain_ctl);
+    for (int s = 0; s < stages; ++s)
+        if (used_mask & (1u << s)) wait_bar(full0 + 8u * s, (last_parity >> s) & 1u, drain_ctl);
 }
 
 // ------------------------------------------------------------------ MMA issuer
-__device__ void run_mma(const CdgParams &p, const SmemLayout &L, const Ctl &ctl, uint32_t tmem_base)
+// Whole warp runs the loop; lane 0 issues tcgen05.mma / tcgen05.commit.
+__device__ __forceinline__ void run_mma(const CdgParams &p, const Ring &R, const CdgPhase *tab, Ctl ctl,
+                                        uint32_t tmem_base, bool leader)
 {
+    const int KB = p.KB, stages = p.stages;
+    const uint32_t idesc = p.idesc, acc_stride = p.acc_stride;
+    const uint64_t adesc0 = sdesc_k128_sw128(R.a0);
+    const uint64_t bdesc0 = sdesc_k128_sw128(R.a0 + CDG_BM * 128);
+    const uint32_t dstep = R.stage_bytes >> 4;  // descriptor units per stage
+    const uint32_t full0 = R.full0, empty0 = R.empty0;
+
     int stage = 0;
     uint32_t parity = 0;
     uint32_t acc_count = 0;
     bool ok = true;
-    for (int g = blockIdx.x; ok && g < p.total_items; g += gridDim.x) {
-        const Item it = decode_item(p, g);
-        const CdgPhase &ph = p.phase[it.phase];
-        if (ph.tap_count == 0) continue;
+    for (ItemWalk w(tab, p.nphases); ok && w.valid(); w.next()) {
+        const int ntap = tab[w.phase].tap_count;
+        if (ntap == 0) continue;
         const uint32_t acc = acc_count & 1u;
         const uint32_t acc_parity = (acc_count >> 1) & 1u;
-        if (!wait_bounded(L.acc_empty(acc), acc_parity ^ 1u, ctl)) break;
+        if (!wait_bar(R.acc_empty0 + 8u * acc, acc_parity ^ 1u, ctl)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * p.acc_stride;
-        const int nk = ph.tap_count * p.KB;
+        const uint32_t d_tmem = tmem_base + acc * acc_stride;
+        const int nk = ntap * KB;
         for (int kk = 0; kk < nk; ++kk) {
-            if (!wait_bounded(L.full(stage), parity, ctl)) {
+            if (!wait_bar(full0 + 8u * stage, parity, ctl)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const uint64_t adesc = sdesc_k128_sw128(L.a(stage));
-            const uint64_t bdesc = sdesc_k128_sw128(L.b(stage));
+            if (leader) {
+                const uint64_t adesc = adesc0 + static_cast<uint64_t>(stage * dstep);
+                const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(stage * dstep);
 #pragma unroll
-            for (int k = 0; k < CDG_BK / 16; ++k)  // 16 elements = 32 bytes = 2 descriptor units
-                umma_f16(d_tmem, adesc + 2u * k, bdesc + 2u * k, p.idesc, (kk | k) != 0);
-            umma_commit(L.empty(stage));
-            if (++stage == p.stages) {
+                for (int k = 0; k < CDG_BK / 16; ++k)  // 16 elements = 32 bytes = 2 descriptor units
+                    umma_f16(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, (kk | k) != 0);
+                umma_commit(empty0 + 8u * stage);
+            }
+            __syncwarp();
+            if (++stage == stages) {
                 stage = 0;
                 parity ^= 1u;
             }
         }
         if (!ok) break;
-        umma_commit(L.acc_full(acc));
+        if (leader) umma_commit(R.acc_full0 + 8u * acc);
+        __syncwarp();
         ++acc_count;
     }
-    // All MMAs issued by this thread complete before TMEM is released.
-    umma_commit(L.drain());
+    // All MMAs issued by this warp complete before TMEM is released.
+    if (leader) umma_commit(R.drain);
+    __syncwarp();
     volatile uint32_t no_abort = 0;
-    Ctl drain_ctl{&no_abort, ctl.status};
-    wait_bounded(L.drain(), 0, drain_ctl);
+    const Ctl drain_ctl{&no_abort, ctl.status};
+    wait_bar(R.drain, 0, drain_ctl);
 }
 
 // ------------------------------------------------------------------ epilogue
@@ -191,121 +241,177 @@ __device__ __forceinline__ float gate_value(uint16_t bits)
     return __half2float(__ushort_as_half(bits));
 }
 
-// Store n (8 or 16) consecutive channel values of one pixel.
-template <int OUT_T>
-__device__ __forceinline__ void store_chunk(void *dst, const float *v, int n)
+__device__ __forceinline__ uint32_t pack2(float a, float b, int out_t)
 {
-    if (OUT_T == CDG_T_F32) {
-        float4 *d = reinterpret_cast<float4 *>(dst);
-        for (int i = 0; i < n / 4; ++i) d[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+    if (out_t == CDG_T_BF16) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// ReLU-backward gate on PER (8 or 4) consecutive channels: v = (x > 0) ? v : +0.0.
+template <int IN_T, int PER>
+__device__ __forceinline__ void gate(float *v, const uint16_t *x)
+{
+    uint32_t w[PER / 2];
+    if constexpr (PER == 8) {
+        const uint4 u = __ldg(reinterpret_cast<const uint4 *>(x));
+        w[0] = u.x;
+        w[1] = u.y;
+        w[2] = u.z;
+        w[3] = u.w;
     } else {
-        uint4 *d = reinterpret_cast<uint4 *>(dst);
-        for (int i = 0; i < n / 8; ++i) {
-            uint32_t w[4];
+        const uint2 u = __ldg(reinterpret_cast<const uint2 *>(x));
+        w[0] = u.x;
+        w[1] = u.y;
+    }
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float a = v[8 * i + 2 * j], b = v[8 * i + 2 * j + 1];
-                if (OUT_T == CDG_T_BF16) {
-                    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-                    w[j] = *reinterpret_cast<uint32_t *>(&h);
-                } else {
-                    __half2 h = __floats2half2_rn(a, b);
-                    w[j] = *reinterpret_cast<uint32_t *>(&h);
-                }
-            }
-            d[i] = make_uint4(w[0], w[1], w[2], w[3]);
-        }
+    for (int e = 0; e < PER / 2; ++e) {
+        if (!(gate_value<IN_T>(static_cast<uint16_t>(w[e] & 0xFFFFu)) > 0.0f)) v[2 * e] = 0.0f;
+        if (!(gate_value<IN_T>(static_cast<uint16_t>(w[e] >> 16)) > 0.0f)) v[2 * e + 1] = 0.0f;
     }
 }
 
+// dX pixel index (n*H + h)*W + w of a sub-grid position of a phase, or -1.
+__device__ __forceinline__ long long phase_pixel(const CdgPhase &ph, int n, int i, int j, int N, int H, int W,
+                                                 int stride)
+{
+    if (n >= N || i >= ph.hph || j >= ph.wph) return -1;
+    return (static_cast<long long>(n) * H + (stride * i + ph.ph)) * W + (stride * j + ph.pw);
+}
+
 template <int OUT_T, bool MASK, int IN_T>
-__device__ void run_epilogue(const CdgParams &p, const SmemLayout &L, const Ctl &ctl, uint32_t tmem_base)
+__device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, const CdgPhase *tab, Ctl ctl,
+                                             uint32_t tmem_base)
 {
     constexpr int OSZ = OUT_T == CDG_T_F32 ? 4 : 2;
+    constexpr int CH = 128 / OSZ;  // channels per 128-byte staging row
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int quad = warp & 3;  // this warp may read TMEM lanes [32*quad, 32*quad + 32)
     const int row = quad * 32 + lane;
-    uint32_t acc_count = 0;
-    for (int g = blockIdx.x; g < p.total_items; g += gridDim.x) {
-        const Item it = decode_item(p, g);
-        const CdgPhase &ph = p.phase[it.phase];
-        // dX pixel of this tile row
-        int n, i, j;
-        bool valid;
-        if (ph.linear) {
-            const long long m = static_cast<long long>(it.mt) * CDG_BM + row;
-            const long long plane = static_cast<long long>(ph.hph) * ph.wph;
-            valid = m < plane * p.N;
-            n = static_cast<int>(m / plane);
-            const int rem = static_cast<int>(m - static_cast<long long>(n) * plane);
-            i = rem / ph.wph;
-            j = rem - i * ph.wph;
-        } else {
-            int j0, i0, n0;
-            box_origin(p, ph, it.mt, j0, i0, n0);
-            const int jl = row % p.box_w;
-            const int il = (row / p.box_w) % p.box_h;
-            const int nl = row / (p.box_w * p.box_h);
-            n = n0 + nl;
-            i = i0 + il;
-            j = j0 + jl;
-            valid = nl < p.box_n && n < p.N && i < ph.hph && j < ph.wph;
-        }
-        const long long pix =
-            valid ? (static_cast<long long>(n) * p.H + (p.stride * i + ph.ph)) * p.W + (p.stride * j + ph.pw) : 0;
-        char *out_row = static_cast<char *>(p.dX) + pix * p.C * OSZ;
-        const uint16_t *x_row = MASK ? static_cast<const uint16_t *>(p.mask) + pix * p.C : nullptr;
-        const int c_begin = it.nt * p.BN;
-        const int c_end = min(p.C, c_begin + p.BN);
+    const int et = threadIdx.x - 64;  // 0..127 over the epilogue warps
+    const bool leader = et == 0;
+    const int tiles_n = p.tiles_n, BN = p.BN, C = p.C, N = p.N, H = p.H, W = p.W, stride = p.stride;
+    // box dims are 0 in the linear operand modes; keep the divisions defined
+    const int bw = max(p.box_w, 1), bh = max(p.box_h, 1), bn = max(p.box_n, 1);
+    const int d_mode = p.d_mode, m_step = p.m_step, rpt = max(p.rows_per_tile, 1);
+    const uint32_t acc_stride = p.acc_stride;
+    char *const dX = static_cast<char *>(p.dX);
+    const uint16_t *const xg = static_cast<const uint16_t *>(p.mask);
+    const int jl = row % bw, il = (row / bw) % bh, nl = row / (bw * bh);  // tile row -> box position
+    const uint32_t srow_off = static_cast<uint32_t>(row) * 128u;
+    const uint32_t sw = static_cast<uint32_t>(row & 7);
 
-        if (ph.tap_count == 0) {  // no tap reaches this phase: dX = +0.0
-            if (valid) {
-                uint4 *d = reinterpret_cast<uint4 *>(out_row + static_cast<long long>(c_begin) * OSZ);
-                const int n16 = (c_end - c_begin) * OSZ / 16;
-                for (int q = 0; q < n16; ++q) d[q] = make_uint4(0, 0, 0, 0);
+    uint32_t acc_count = 0, chunk_count = 0;
+    for (ItemWalk w(tab, p.nphases); w.valid(); w.next()) {
+        const CdgPhase &ph = tab[w.phase];
+        const int mt = tiles_n == 1 ? w.local : w.local / tiles_n;
+        const int nt = w.local - mt * tiles_n;
+        const int c_begin = nt * BN;
+        const int c_end = min(C, c_begin + BN);
+
+        if (ph.tap_count == 0) {
+            // No tap reaches this phase: dX = +0.0 over 128 consecutive sub-grid
+            // positions.  Each epilogue warp takes every fourth row; its lanes
+            // cover the row's channels with coalesced 16-byte stores.
+            const int n16 = (c_end - c_begin) * OSZ / 16;
+            const int plane = ph.hph * ph.wph;  // N * plane < 2^31 (checked by the planner)
+            int m = mt * CDG_BM + et / 32;
+            int n = m / plane;
+            int i = (m - n * plane) / ph.wph;
+            int j = m - n * plane - i * ph.wph;
+            for (int r = et / 32; r < CDG_BM && n < N; r += 4) {
+                const long long pix = (static_cast<long long>(n) * H + (stride * i + ph.ph)) * W + (stride * j + ph.pw);
+                uint4 *dst = reinterpret_cast<uint4 *>(dX + (pix * C + c_begin) * OSZ);
+                for (int q = lane; q < n16; q += 32) dst[q] = make_uint4(0, 0, 0, 0);
+                j += 4;  // next row of this warp: four positions on
+                while (j >= ph.wph) {
+                    j -= ph.wph;
+                    if (++i == ph.hph) {
+                        i = 0;
+                        ++n;
+                    }
+                }
             }
             continue;
         }
 
-        const uint32_t acc = acc_count & 1u;
-        const uint32_t acc_parity = (acc_count >> 1) & 1u;
-        if (!wait_bounded(L.acc_full(acc), acc_parity, ctl)) break;
-        tc_fence_after();
-        const uint32_t taddr = tmem_base + acc * p.acc_stride + (static_cast<uint32_t>(quad * 32) << 16);
-        for (int cc = 0; cc < p.BN; cc += 16) {
-            uint32_t r[16];
-            tmem_ld_32x32b_x16(taddr + cc, r);
-            tmem_ld_wait();
-            const int c = c_begin + cc;
-            if (valid && c < c_end) {
-                const int nc = min(16, c_end - c);  // 16 or 8 (C is a multiple of 8)
-                float v[16];
-#pragma unroll
-                for (int q = 0; q < 16; ++q) v[q] = __uint_as_float(r[q]);
-                if (MASK) {
-                    uint16_t xb[16];
-                    const uint4 *xs = reinterpret_cast<const uint4 *>(x_row + c);
-                    for (int q = 0; q < nc / 8; ++q) {
-                        const uint4 u = __ldg(xs + q);
-                        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            xb[8 * q + 2 * e] = static_cast<uint16_t>(w4[e] & 0xFFFFu);
-                            xb[8 * q + 2 * e + 1] = static_cast<uint16_t>(w4[e] >> 16);
-                        }
-                    }
-#pragma unroll
-                    for (int q = 0; q < 16; ++q)
-                        if (q < nc && !(gate_value<IN_T>(xb[q]) > 0.0f)) v[q] = 0.0f;
-                }
-                store_chunk<OUT_T>(out_row + static_cast<long long>(c) * OSZ, v, nc);
+        // tile origin in the store map's coordinates, and (for the gate) this row's pixel
+        int j0 = 0, i0 = 0, n0 = 0;
+        long long pix = -1;
+        if (d_mode == CDG_D_BOX4) {
+            box_origin(ph, mt, bw, bh, bn, j0, i0, n0);
+            if (MASK && nl < bn) pix = phase_pixel(ph, n0 + nl, i0 + il, j0 + jl, N, H, W, stride);
+        } else if (MASK) {
+            const long long m = static_cast<long long>(mt) * m_step + row;
+            const long long plane = static_cast<long long>(ph.hph) * ph.wph;
+            if (row < m_step && m < plane * N) {
+                const int n = static_cast<int>(m / plane);
+                const int rem = static_cast<int>(m - plane * n);
+                pix = phase_pixel(ph, n, rem / ph.wph, rem % ph.wph, N, H, W, stride);
             }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(L.acc_empty(acc));
+        const uint64_t mapD = reinterpret_cast<uint64_t>(&p.tmD[w.phase]);
+
+        const uint32_t acc = acc_count & 1u;
+        const uint32_t acc_parity = (acc_count >> 1) & 1u;
+        if (!wait_bar(R.acc_full0 + 8u * acc, acc_parity, ctl)) break;
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + acc * acc_stride + (static_cast<uint32_t>(quad * 32) << 16);
+        for (int cc = 0; cc < BN; cc += CH) {
+            const uint32_t buf = R.out0 + (chunk_count & 1u) * (128u * 128u);
+            ++chunk_count;
+            // the TMA store that last read this staging buffer must be done with it
+            if (leader) bulk_wait_group_read<1>();
+            named_bar_sync(1, 128);
+            uint32_t r[CH];
+#pragma unroll
+            for (int q = 0; q < CH / 16; ++q)
+                tmem_ld_32x32b_x16(taddr + cc + 16 * q, *reinterpret_cast<uint32_t(*)[16]>(&r[16 * q]));
+            tmem_ld_wait();
+            if (cc + CH >= BN) {  // last read of this accumulator: hand it back to the MMA warp
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(R.acc_empty0 + 8u * acc);
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {  // 16-byte pieces of this row
+                constexpr int PER = 16 / OSZ;  // values per piece
+                float v[PER];
+#pragma unroll
+                for (int e = 0; e < PER; ++e) v[e] = __uint_as_float(r[PER * q + e]);
+                if (MASK) {
+                    const int c = c_begin + cc + PER * q;
+                    if (pix >= 0 && c < c_end) gate<IN_T, PER>(v, xg + pix * C + c);
+                }
+                uint32_t wv[4];
+                if (OUT_T == CDG_T_F32) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) wv[e] = __float_as_uint(v[e]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) wv[e] = pack2(v[2 * e], v[2 * e + 1], OUT_T);
+                }
+                st_shared_v4(buf + srow_off + ((static_cast<uint32_t>(q) ^ sw) << 4), wv[0], wv[1], wv[2], wv[3]);
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(1, 128);
+            if (leader) {
+                const int c = c_begin + cc;
+                if (d_mode == CDG_D_BOX4)
+                    tma_store_4d(mapD, buf, c, j0, i0, n0);
+                else if (d_mode == CDG_D_LINEAR)
+                    tma_store_2d(mapD, buf, c, mt * m_step);
+                else
+                    tma_store_3d(mapD, buf, c, 0, mt * rpt);
+                bulk_commit_group();
+            }
+        }
         ++acc_count;
     }
+    if (leader) bulk_wait_group_all();
 }
 
 // ------------------------------------------------------------------ kernel
@@ -314,26 +420,37 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_cons
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
-    SmemLayout L;
-    L.base = (raw + 1023u) & ~1023u;
-    L.stage_bytes = CDG_BM * 128 + p.BN * 128;
-    L.stages = p.stages;
-    L.bars = L.base + p.stages * L.stage_bytes;
-    uint8_t *bars_generic = smem_raw + (L.bars - raw);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars_generic + 8 * (2 * p.stages + 5));
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const int stages = p.stages;
+    Ring R;
+    R.a0 = base;
+    R.stage_bytes = CDG_BM * 128 + p.BN * 128;
+    R.out0 = base + stages * R.stage_bytes;
+    const uint32_t bars = R.out0 + CDG_SMEM_STAGING;
+    R.full0 = bars;
+    R.empty0 = bars + 8u * stages;
+    R.acc_full0 = bars + 16u * stages;
+    R.acc_empty0 = bars + 16u * stages + 16u;
+    R.drain = bars + 16u * stages + 32u;
+    uint8_t *const tail = smem_raw + (bars - raw);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tail + 8 * (2 * stages + 5));
     volatile uint32_t *abort_flag = tmem_slot + 1;
+    CdgPhase *tab = reinterpret_cast<CdgPhase *>(tail + CDG_SMEM_TABLES);
+    CdgTap *taps = reinterpret_cast<CdgTap *>(tab + CDG_MAX_PHASES);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    for (int i = threadIdx.x; i < p.nphases; i += blockDim.x) tab[i] = p.phase[i];
+    for (int i = threadIdx.x; i < p.ntaps; i += blockDim.x) taps[i] = p.tap[i];
     if (threadIdx.x == 0) {
-        for (int s = 0; s < p.stages; ++s) {
-            mbar_init(L.full(s), 1);
-            mbar_init(L.empty(s), 1);
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(R.full0 + 8u * s, 1);
+            mbar_init(R.empty0 + 8u * s, 1);
         }
         for (int a = 0; a < 2; ++a) {
-            mbar_init(L.acc_full(a), 1);
-            mbar_init(L.acc_empty(a), 4);  // one arrival per epilogue warp
+            mbar_init(R.acc_full0 + 8u * a, 1);
+            mbar_init(R.acc_empty0 + 8u * a, 4);  // one arrival per epilogue warp
         }
-        mbar_init(L.drain(), 1);
+        mbar_init(R.drain, 1);
         *abort_flag = 0u;
         fence_mbar_init();
     }
@@ -347,15 +464,12 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_cons
     const uint32_t tmem_base = *tmem_slot;
     const Ctl ctl{abort_flag, p.status};
 
-    if (warp == 0) {
-        if (lane == 0) run_producer(p, L, ctl);
-        __syncwarp();
-    } else if (warp == 1) {
-        if (lane == 0) run_mma(p, L, ctl, tmem_base);
-        __syncwarp();
-    } else {
-        run_epilogue<OUT_T, MASK, IN_T>(p, L, ctl, tmem_base);
-    }
+    if (warp == 0)
+        run_producer(p, R, tab, taps, ctl, lane == 0);
+    else if (warp == 1)
+        run_mma(p, R, tab, ctl, tmem_base, lane == 0);
+    else
+        run_epilogue<OUT_T, MASK, IN_T>(p, R, tab, ctl, tmem_base);
 
     tc_fence_before();
     __syncthreads();
