@@ -224,10 +224,14 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     const int tiles_n = ceil_div(C, BN);
     int items = 0;
     for (CdgPhase &f : phases) {
-        f.linear = (flat || f.tap_count == 0) ? 1 : 0;
         if (f.tap_count == 0) {
-            f.tiles_w = f.tiles_h = 1;
-            f.tiles_m = ceil_div(1LL * N * f.hph * f.wph, CDG_BM);
+            // zero-filled with TMA stores of a zeroed 128-row staging buffer:
+            // boxes of up to 128 sub-grid positions, whole rows where possible
+            f.zbw = std::min(f.wph, CDG_BM);
+            f.zbh = std::min(f.hph, std::max(1, CDG_BM / f.zbw));
+            f.tiles_w = ceil_div(f.wph, f.zbw);
+            f.tiles_h = ceil_div(f.hph, f.zbh);
+            f.tiles_m = f.tiles_w * f.tiles_h * N;
         } else if (flat) {
             f.tiles_w = f.tiles_h = 1;
             f.tiles_m = ceil_div(1LL * N * P * Q, m_step);
@@ -236,7 +240,6 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
             f.tiles_h = ceil_div(f.hph, bh);
             f.tiles_m = f.tiles_w * f.tiles_h * ceil_div(N, bnb);
         }
-        f.item_begin = items;
         f.items = f.tiles_m * tiles_n;
         items += f.items;
     }
@@ -368,30 +371,32 @@ int encode_store_maps(cdg_plan_st *h, void *dX)
     const cuuint64_t C = h->C, W = h->W, H = h->H, s = h->stride;
     for (int i = 0; i < p.nphases; ++i) {
         const CdgPhase &f = p.phase[i];
-        if (f.tap_count == 0) continue;
         CUresult r;
-        if (p.d_mode == CDG_D_LINEAR) {
+        if (f.tap_count == 0 || p.d_mode == CDG_D_BOX4) {
+            // phase sub-grid {C, wph, hph, N} of dX, starting at pixel (ph, pw)
+            char *base = static_cast<char *>(dX) + (static_cast<cuuint64_t>(f.ph) * W + f.pw) * C * osz;
+            const cuuint64_t dims[4] = {C, static_cast<cuuint64_t>(f.wph), static_cast<cuuint64_t>(f.hph),
+                                        static_cast<cuuint64_t>(h->N)};
+            const cuuint64_t strides[3] = {s * C * osz, s * W * C * osz, H * W * C * osz};
+            const bool zero = f.tap_count == 0;
+            const cuuint32_t box[4] = {ch, static_cast<cuuint32_t>(zero ? f.zbw : p.box_w),
+                                       static_cast<cuuint32_t>(zero ? f.zbh : p.box_h),
+                                       static_cast<cuuint32_t>(zero ? 1 : p.box_n)};
+            r = enc(&p.tmD[i], dt, 4, base, dims, strides, box, ones, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        } else if (p.d_mode == CDG_D_LINEAR) {
             const cuuint64_t dims[2] = {C, static_cast<cuuint64_t>(h->N) * H * W};
             const cuuint64_t strides[1] = {C * osz};
             const cuuint32_t box[2] = {ch, CDG_BM};
             r = enc(&p.tmD[i], dt, 2, dX, dims, strides, box, ones, CU_TENSOR_MAP_INTERLEAVE_NONE,
                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        } else if (p.d_mode == CDG_D_ROWS) {
+        } else {
             // phase (0,0): rows n*hph + i are s*W*C elements apart because H = s*hph
             const cuuint64_t dims[3] = {C, static_cast<cuuint64_t>(f.wph),
                                         static_cast<cuuint64_t>(h->N) * static_cast<cuuint64_t>(f.hph)};
             const cuuint64_t strides[2] = {s * C * osz, s * W * C * osz};
             const cuuint32_t box[3] = {ch, static_cast<cuuint32_t>(f.wph), static_cast<cuuint32_t>(p.rows_per_tile)};
             r = enc(&p.tmD[i], dt, 3, dX, dims, strides, box, ones, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        } else {
-            char *base = static_cast<char *>(dX) + (static_cast<cuuint64_t>(f.ph) * W + f.pw) * C * osz;
-            const cuuint64_t dims[4] = {C, static_cast<cuuint64_t>(f.wph), static_cast<cuuint64_t>(f.hph),
-                                        static_cast<cuuint64_t>(h->N)};
-            const cuuint64_t strides[3] = {s * C * osz, s * W * C * osz, H * W * C * osz};
-            const cuuint32_t box[4] = {ch, static_cast<cuuint32_t>(p.box_w), static_cast<cuuint32_t>(p.box_h),
-                                       static_cast<cuuint32_t>(p.box_n)};
-            r = enc(&p.tmD[i], dt, 4, base, dims, strides, box, ones, CU_TENSOR_MAP_INTERLEAVE_NONE,
                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         }
         if (r != CUDA_SUCCESS) return CDG_ERR_CUDA;

@@ -12,7 +12,13 @@
 #define CDG_BM 128          // dX pixels per tile = TMEM lanes = UMMA M
 #define CDG_BK 64           // dY channels per pipeline stage (128 B of fp16/bf16)
 #define CDG_MAX_DYN_SMEM 232448  // sm_103 opt-in dynamic shared memory per CTA (227 KB)
-#define CDG_THREADS 192     // warp 0 TMA producer, warp 1 MMA issuer, warps 2-5 epilogue
+// Warp roles: warps 0, 2, 3 load operands with TMA (pipeline stages taken
+// round-robin: a TMA issue holds its thread for a few hundred cycles, so one
+// issuing thread cannot keep the tensor core fed); warp 1 issues tcgen05.mma;
+// warps 4-7 run the epilogue (warp w reads TMEM lanes 32*(w%4)..+31).
+#define CDG_THREADS 256
+#define CDG_LOADERS 3
+#define CDG_EPI_WARP0 4
 #define CDG_WAIT_LIMIT_NS 4000000000ull  // a pipeline wait gives up after 4 s
 // Shared memory after the operand ring: two 16 KB output staging buffers
 // (128 rows x 128 B, the box a TMA store writes), then mbarriers and flags
@@ -29,11 +35,10 @@ struct CdgPhase {
     int ph, pw;
     int hph, wph;
     int tap_begin, tap_count;
-    int linear;            // tile rows = a linear range of (n, i, j); else 4-D boxes
-    int tiles_w, tiles_h;  // 4-D box tiles along j and i
+    int zbw, zbh;          // phases without taps: box (zbw x zbh x 1 positions) of one zero-fill store
+    int tiles_w, tiles_h;  // box tiles along j and i (4-D halo boxes, or the zero-fill box)
     int tiles_m;           // M tiles of this phase
     int items;             // tiles_m * (N tiles): work items of this phase
-    int item_begin;        // first work item of this phase in the launch
 };
 
 struct CdgTap {
@@ -52,7 +57,7 @@ enum {
 struct CdgParams {  // CUtensorMap members carry their own (128-byte) alignment
     CUtensorMap tmA;  // dY: 4-D {K, Q, P, N} halo boxes, or 2-D {K, N*P*Q} rows
     CUtensorMap tmB;  // packed weights: 3-D {K, C, R*S}
-    CUtensorMap tmD[CDG_MAX_PHASES];  // dX stores, one map per phase with taps (index = phase slot)
+    CUtensorMap tmD[CDG_MAX_PHASES];  // dX stores, one map per phase (index = phase slot)
     void *dX;
     const void *mask;
     int *status;

@@ -107,10 +107,14 @@ struct Ring {
     uint32_t acc_full0, acc_empty0, drain;
 };
 
-// ------------------------------------------------------------------ producer
-// Whole warp runs the loop (converged control flow); lane 0 issues.
-__device__ __forceinline__ void run_producer(const CdgParams &p, const Ring &R, const CdgPhase *tab,
-                                             const CdgTap *taps, Ctl ctl, bool leader)
+// ------------------------------------------------------------------ loaders
+// CDG_LOADERS warps walk the same (item, tap, k-block) sequence; the loader
+// with index li issues the stages whose global counter is li modulo
+// CDG_LOADERS.  The whole warp runs the loop; lane 0 issues.  The parity of
+// each slot's latest load is recorded in shared memory for the abort drain.
+__device__ __forceinline__ void run_loader(const CdgParams &p, const Ring &R, const CdgPhase *tab,
+                                           const CdgTap *taps, Ctl ctl, int li, bool leader,
+                                           volatile uint32_t *slot_parity)
 {
     const uint64_t mapA = reinterpret_cast<uint64_t>(&p.tmA);
     const uint64_t mapB = reinterpret_cast<uint64_t>(&p.tmB);
@@ -126,7 +130,7 @@ __device__ __forceinline__ void run_producer(const CdgParams &p, const Ring &R, 
 
     int stage = 0;
     uint32_t parity = 0;
-    uint32_t used_mask = 0, last_parity = 0;  // for the final drain
+    int owner = 0;  // loader index of the current global stage
     bool ok = true;
     for (ItemWalk w(tab, p.nphases); ok && w.valid(); w.next()) {
         const CdgPhase &ph = tab[w.phase];
@@ -142,23 +146,25 @@ __device__ __forceinline__ void run_producer(const CdgParams &p, const Ring &R, 
             const CdgTap tap = taps[ph.tap_begin + tt];
             const int y = j0 + tap.ds, z = i0 + tap.dr, t = tap.t;
             for (int kb = 0; kb < KB; ++kb) {
-                const uint32_t full = full0 + 8u * stage;
-                if (!wait_bar(empty0 + 8u * stage, parity ^ 1u, ctl)) {
-                    ok = false;
-                    break;
+                if (owner == li) {
+                    const uint32_t full = full0 + 8u * stage;
+                    if (!wait_bar(empty0 + 8u * stage, parity ^ 1u, ctl)) {
+                        ok = false;
+                        break;
+                    }
+                    if (leader) {
+                        slot_parity[stage] = parity | 2u;  // bit 1: slot used
+                        mbar_arrive_expect_tx(full, tx);
+                        const uint32_t sa = a0 + stage * sbytes;
+                        if (flat)
+                            tma_load_2d(sa, mapA, full, kb * CDG_BK, m0);
+                        else
+                            tma_load_4d(sa, mapA, full, kb * CDG_BK, y, z, n0);
+                        tma_load_3d(sa + CDG_BM * 128, mapB, full, kb * CDG_BK, c0, t);
+                    }
+                    __syncwarp();
                 }
-                if (leader) {
-                    mbar_arrive_expect_tx(full, tx);
-                    const uint32_t sa = a0 + stage * sbytes;
-                    if (flat)
-                        tma_load_2d(sa, mapA, full, kb * CDG_BK, m0);
-                    else
-                        tma_load_4d(sa, mapA, full, kb * CDG_BK, y, z, n0);
-                    tma_load_3d(sa + CDG_BM * 128, mapB, full, kb * CDG_BK, c0, t);
-                }
-                __syncwarp();
-                used_mask |= 1u << stage;
-                last_parity = (last_parity & ~(1u << stage)) | (parity << stage);
+                if (++owner == CDG_LOADERS) owner = 0;
                 if (++stage == stages) {
                     stage = 0;
                     parity ^= 1u;
@@ -166,13 +172,20 @@ __device__ __forceinline__ void run_producer(const CdgParams &p, const Ring &R, 
             }
         }
     }
-    // Every copy this warp started must land before the CTA may exit.  On the
-    // normal path they all have (the MMA warp waited for each) and this
-    // returns at once; after an abort it waits, bounded, for copies in flight.
+}
+
+// After an abort: wait (bounded) until the latest load of every used slot has
+// landed, so that no TMA still writes shared memory when the CTA exits.  On
+// the normal path the MMA warp has already waited for every load.
+__device__ __forceinline__ void drain_loads(const Ring &R, int stages, int *status,
+                                            const volatile uint32_t *slot_parity)
+{
     volatile uint32_t no_abort = 0;
-    const Ctl drain_ctl{&no_abort, ctl.status};
-    for (int s = 0; s < stages; ++s)
-        if (used_mask & (1u << s)) wait_bar(full0 + 8u * s, (last_parity >> s) & 1u, drain_ctl);
+    const Ctl drain_ctl{&no_abort, status};
+    for (int s = 0; s < stages; ++s) {
+        const uint32_t v = slot_parity[s];
+        if (v & 2u) wait_bar(R.full0 + 8u * s, v & 1u, drain_ctl);
+    }
 }
 
 // ------------------------------------------------------------------ MMA issuer
@@ -291,19 +304,21 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int quad = warp & 3;  // this warp may read TMEM lanes [32*quad, 32*quad + 32)
     const int row = quad * 32 + lane;
-    const int et = threadIdx.x - 64;  // 0..127 over the epilogue warps
-    const bool leader = et == 0;
+    const int ew = warp - CDG_EPI_WARP0;  // epilogue warp 0..3
     const int tiles_n = p.tiles_n, BN = p.BN, C = p.C, N = p.N, H = p.H, W = p.W, stride = p.stride;
     // box dims are 0 in the linear operand modes; keep the divisions defined
     const int bw = max(p.box_w, 1), bh = max(p.box_h, 1), bn = max(p.box_n, 1);
     const int d_mode = p.d_mode, m_step = p.m_step, rpt = max(p.rows_per_tile, 1);
     const uint32_t acc_stride = p.acc_stride;
-    char *const dX = static_cast<char *>(p.dX);
     const uint16_t *const xg = static_cast<const uint16_t *>(p.mask);
     const int jl = row % bw, il = (row / bw) % bh, nl = row / (bw * bh);  // tile row -> box position
     const uint32_t srow_off = static_cast<uint32_t>(row) * 128u;
     const uint32_t sw = static_cast<uint32_t>(row & 7);
+    const uint32_t zero_buf = R.out0;  // staging buffer 0 doubles as the zero source
+    bool zero_ready = false;
 
+    // TMA stores are spread over the four warps' lane 0 (an issue holds its
+    // thread for a few hundred cycles): chunk k is stored by epilogue warp k % 4.
     uint32_t acc_count = 0, chunk_count = 0;
     for (ItemWalk w(tab, p.nphases); w.valid(); w.next()) {
         const CdgPhase &ph = tab[w.phase];
@@ -311,33 +326,38 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
         const int nt = w.local - mt * tiles_n;
         const int c_begin = nt * BN;
         const int c_end = min(C, c_begin + BN);
+        const uint64_t mapD = reinterpret_cast<uint64_t>(&p.tmD[w.phase]);
 
         if (ph.tap_count == 0) {
-            // No tap reaches this phase: dX = +0.0 over 128 consecutive sub-grid
-            // positions.  Each epilogue warp takes every fourth row; its lanes
-            // cover the row's channels with coalesced 16-byte stores.
-            const int n16 = (c_end - c_begin) * OSZ / 16;
-            const int plane = ph.hph * ph.wph;  // N * plane < 2^31 (checked by the planner)
-            int m = mt * CDG_BM + et / 32;
-            int n = m / plane;
-            int i = (m - n * plane) / ph.wph;
-            int j = m - n * plane - i * ph.wph;
-            for (int r = et / 32; r < CDG_BM && n < N; r += 4) {
-                const long long pix = (static_cast<long long>(n) * H + (stride * i + ph.ph)) * W + (stride * j + ph.pw);
-                uint4 *dst = reinterpret_cast<uint4 *>(dX + (pix * C + c_begin) * OSZ);
-                for (int q = lane; q < n16; q += 32) dst[q] = make_uint4(0, 0, 0, 0);
-                j += 4;  // next row of this warp: four positions on
-                while (j >= ph.wph) {
-                    j -= ph.wph;
-                    if (++i == ph.hph) {
-                        i = 0;
-                        ++n;
-                    }
-                }
+            // No tap reaches this phase: dX = +0.0, stored box by box from a
+            // zeroed staging buffer.
+            if (!zero_ready) {
+                if (lane == 0) bulk_wait_group_read<0>();  // no store may still read the buffer
+                named_bar_sync(1, 128);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) st_shared_v4(zero_buf + srow_off + (q << 4), 0u, 0u, 0u, 0u);
+                fence_proxy_async_smem();
+                named_bar_sync(1, 128);
+                zero_ready = true;
             }
+            int j0, i0, n0;
+            box_origin(ph, mt, ph.zbw, ph.zbh, 1, j0, i0, n0);
+            const int nchunks = (c_end - c_begin + CH - 1) / CH;
+            if (lane == 0)
+                for (int q = ew; q < nchunks; q += 4) {
+                    tma_store_4d(mapD, zero_buf, c_begin + q * CH, j0, i0, n0);
+                    bulk_commit_group();
+                }
             continue;
         }
 
+        if (zero_ready) {
+            // back from zero-fill items (the planner orders them last, so this
+            // is only a safeguard): every zero store must have read its source
+            if (lane == 0) bulk_wait_group_read<0>();
+            named_bar_sync(1, 128);
+            zero_ready = false;
+        }
         // tile origin in the store map's coordinates, and (for the gate) this row's pixel
         int j0 = 0, i0 = 0, n0 = 0;
         long long pix = -1;
@@ -353,7 +373,6 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
                 pix = phase_pixel(ph, n, rem / ph.wph, rem % ph.wph, N, H, W, stride);
             }
         }
-        const uint64_t mapD = reinterpret_cast<uint64_t>(&p.tmD[w.phase]);
 
         const uint32_t acc = acc_count & 1u;
         const uint32_t acc_parity = (acc_count >> 1) & 1u;
@@ -361,10 +380,11 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
         tc_fence_after();
         const uint32_t taddr = tmem_base + acc * acc_stride + (static_cast<uint32_t>(quad * 32) << 16);
         for (int cc = 0; cc < BN; cc += CH) {
-            const uint32_t buf = R.out0 + (chunk_count & 1u) * (128u * 128u);
-            ++chunk_count;
-            // the TMA store that last read this staging buffer must be done with it
-            if (leader) bulk_wait_group_read<1>();
+            const uint32_t k = chunk_count++;
+            const uint32_t buf = R.out0 + (k & 1u) * (128u * 128u);
+            // the store that last read this buffer (chunk k-2, issued by warp
+            // (k-2) % 4) must be done with it
+            if (k >= 2 && lane == 0 && static_cast<uint32_t>(ew) == ((k - 2) & 3u)) bulk_wait_group_read<0>();
             named_bar_sync(1, 128);
             uint32_t r[CH];
 #pragma unroll
@@ -398,7 +418,7 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
             }
             fence_proxy_async_smem();
             named_bar_sync(1, 128);
-            if (leader) {
+            if (lane == 0 && static_cast<uint32_t>(ew) == (k & 3u)) {
                 const int c = c_begin + cc;
                 if (d_mode == CDG_D_BOX4)
                     tma_store_4d(mapD, buf, c, j0, i0, n0);
@@ -411,7 +431,7 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
         }
         ++acc_count;
     }
-    if (leader) bulk_wait_group_all();
+    if (lane == 0) bulk_wait_group_all();
 }
 
 // ------------------------------------------------------------------ kernel
@@ -435,6 +455,7 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_cons
     uint8_t *const tail = smem_raw + (bars - raw);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tail + 8 * (2 * stages + 5));
     volatile uint32_t *abort_flag = tmem_slot + 1;
+    volatile uint32_t *slot_parity = tmem_slot + 2;  // [stages] (<= 8 entries)
     CdgPhase *tab = reinterpret_cast<CdgPhase *>(tail + CDG_SMEM_TABLES);
     CdgTap *taps = reinterpret_cast<CdgTap *>(tab + CDG_MAX_PHASES);
 
@@ -452,6 +473,7 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_cons
         }
         mbar_init(R.drain, 1);
         *abort_flag = 0u;
+        for (int s = 0; s < stages; ++s) slot_parity[s] = 0u;
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -464,13 +486,15 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_cons
     const uint32_t tmem_base = *tmem_slot;
     const Ctl ctl{abort_flag, p.status};
 
-    if (warp == 0)
-        run_producer(p, R, tab, taps, ctl, lane == 0);
-    else if (warp == 1)
+    if (warp == 1)
         run_mma(p, R, tab, ctl, tmem_base, lane == 0);
-    else
+    else if (warp >= CDG_EPI_WARP0)
         run_epilogue<OUT_T, MASK, IN_T>(p, R, tab, ctl, tmem_base);
+    else
+        run_loader(p, R, tab, taps, ctl, warp == 0 ? 0 : warp - 1, lane == 0, slot_parity);
 
+    __syncthreads();
+    if (*abort_flag && threadIdx.x == 0) drain_loads(R, stages, p.status, slot_parity);
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
