@@ -18,6 +18,7 @@
 
 #include <algorithm>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 #include <vector>
@@ -186,14 +187,22 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
                     t.dr = static_cast<int16_t>(th / stride);  // exact: th is a multiple of stride
                     t.ds = static_cast<int16_t>(tw / stride);
                     t.t = static_cast<int16_t>(r * S + s);
-                    t.unused = 0;
+                    t.hoff = 0;
                     mine.push_back(t);
                 }
             }
-            f.tap_count = static_cast<int>(mine.size());
+            f.tap_count = static_cast<int16_t>(mine.size());
             phase_taps_by_index[ph * stride + pw] = f.tap_count;
             if (f.hph == 0 || f.wph == 0) continue;  // no dX pixel in this residue class
-            f.tap_begin = static_cast<int>(taps.size());
+            f.tap_begin = static_cast<int16_t>(taps.size());
+            if (!mine.empty()) {
+                f.dr_min = mine[0].dr;
+                f.ds_min = mine[0].ds;
+                for (const CdgTap &t : mine) {
+                    f.dr_min = std::min(f.dr_min, t.dr);
+                    f.ds_min = std::min(f.ds_min, t.ds);
+                }
+            }
             taps.insert(taps.end(), mine.begin(), mine.end());
             phases.push_back(f);
         }
@@ -222,13 +231,70 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     if (!flat) choose_box(phases, N, bw, bh, bnb);
     const int BN = choose_bn(C);
     const int tiles_n = ceil_div(C, BN);
+    const int ring_budget = kMaxSmem - 1024 - CDG_SMEM_STAGING - CDG_SMEM_TAIL;
+
+    // ---- halo operand mode (opt-in: CDG_HALO=1): a tile is halo_bh full-width
+    // rows of one image's phase sub-grid; one TMA box of (width + tap span) x
+    // (rows + tap span) positions of dY serves every tap of the phase, each
+    // tap's operand starting hoff rows into it.  Tile row a*halo_wb + b is
+    // output (a, b); rows with b >= halo_wt are padding.  It cuts the operand
+    // bytes written to shared memory, but on GB300 it measured slower than
+    // per-tap boxes on every ResNet-50 3x3 layer (the taps' operands start at
+    // rows that are not 1024-byte aligned), so the planner does not pick it
+    // unless asked; when asked it is used wherever the geometry allows.
+    bool halo = false;
+    int hwb = 0, hwt = 0, hbh = 0, hhb = 0, hrows = 0, a_stages = 0, b_stages = 0;
+    const char *halo_env = std::getenv("CDG_HALO");
+    if (!flat && halo_env && halo_env[0] == '1') {
+        int span_r = 0, span_s = 0, wt = 0, hmax = 0, maxtaps = 0;
+        for (const CdgPhase &f : phases) {
+            if (f.tap_count == 0) continue;
+            int dr_max = f.dr_min, ds_max = f.ds_min;
+            for (int t = f.tap_begin; t < f.tap_begin + f.tap_count; ++t) {
+                dr_max = std::max<int>(dr_max, taps[t].dr);
+                ds_max = std::max<int>(ds_max, taps[t].ds);
+            }
+            span_r = std::max(span_r, dr_max - f.dr_min);
+            span_s = std::max(span_s, ds_max - f.ds_min);
+            wt = std::max(wt, f.wph);
+            hmax = std::max(hmax, f.hph);
+            maxtaps = std::max<int>(maxtaps, f.tap_count);
+        }
+        const int wb = wt + span_s;
+        if (maxtaps >= 2 && wb <= CDG_BM) {
+            const int rows_per_tile = std::min(hmax, CDG_BM / wb);
+            const int hb = rows_per_tile + span_r;
+            const int off_max = span_r * wb + span_s;
+            const int rows = ((std::max(wb * hb, off_max + CDG_BM) + 7) / 8) * 8;
+            const int a_bytes = rows * 128, b_bytes = BN * 128;
+            const int as = (3 * a_bytes + 4 * b_bytes <= ring_budget) ? 3 : 2;
+            const int bs = std::min(std::min(kMaxStages, CDG_MAX_STAGES_TOTAL - as), (ring_budget - as * a_bytes) / b_bytes);
+            if (hb <= 256 && bs >= 2) {
+                halo = true;
+                hwb = wb;
+                hwt = wt;
+                hbh = rows_per_tile;
+                hhb = hb;
+                hrows = rows;
+                a_stages = as;
+                b_stages = bs;
+                for (CdgPhase &f : phases)
+                    for (int t = f.tap_begin; t < f.tap_begin + f.tap_count; ++t)
+                        taps[t].hoff = static_cast<int16_t>((taps[t].dr - f.dr_min) * wb + (taps[t].ds - f.ds_min));
+                bw = hwt;
+                bh = hbh;
+                bnb = 1;
+            }
+        }
+    }
+
     int items = 0;
     for (CdgPhase &f : phases) {
         if (f.tap_count == 0) {
             // zero-filled with TMA stores of a zeroed 128-row staging buffer:
             // boxes of up to 128 sub-grid positions, whole rows where possible
-            f.zbw = std::min(f.wph, CDG_BM);
-            f.zbh = std::min(f.hph, std::max(1, CDG_BM / f.zbw));
+            f.zbw = static_cast<int16_t>(std::min(f.wph, CDG_BM));
+            f.zbh = static_cast<int16_t>(std::min(f.hph, std::max(1, CDG_BM / f.zbw)));
             f.tiles_w = ceil_div(f.wph, f.zbw);
             f.tiles_h = ceil_div(f.hph, f.zbh);
             f.tiles_m = f.tiles_w * f.tiles_h * N;
@@ -244,8 +310,8 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
         items += f.items;
     }
     const int stage_bytes = CDG_BM * 128 + BN * 128;
-    const int stages =
-        std::min(kMaxStages, (kMaxSmem - 1024 - CDG_SMEM_STAGING - CDG_SMEM_TAIL) / stage_bytes);
+    const int stages = halo ? a_stages + b_stages : std::min(kMaxStages, ring_budget / stage_bytes);
+    const int ring_bytes = halo ? a_stages * hrows * 128 + b_stages * BN * 128 : stages * stage_bytes;
     // two accumulators, each at least as wide as the 64-column chunks the epilogue reads
     int tmem_cols = 32;
     while (tmem_cols < 2 * (((BN + 63) / 64) * 64)) tmem_cols *= 2;
@@ -265,6 +331,16 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     p.d_mode = d_mode;
     p.m_step = m_step;
     p.rows_per_tile = rpt;
+    p.halo = halo ? 1 : 0;
+    p.halo_wb = hwb;
+    p.halo_wt = hwt;
+    p.halo_bh = hbh;
+    p.a_stages = halo ? a_stages : stages;
+    p.b_stages = b_stages;
+    p.a_stage_bytes = static_cast<uint32_t>(halo ? hrows * 128 : stage_bytes);
+    p.halo_hb = hhb;
+    p.tx_a = static_cast<uint32_t>(hwb * hhb * 128);
+    p.tx_b = static_cast<uint32_t>(BN * 128);
     const uint32_t ab = dtype == CDG_BF16 ? 1u : 0u;
     p.idesc = (1u << 4) | (ab << 7) | (ab << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
               (static_cast<uint32_t>(CDG_BM >> 4) << 24);
@@ -274,7 +350,7 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     for (size_t i = 0; i < phases.size(); ++i) p.phase[i] = phases[i];
     for (size_t i = 0; i < taps.size(); ++i) p.tap[i] = taps[i];
 
-    h->smem = static_cast<size_t>(1024 + stages * stage_bytes + CDG_SMEM_STAGING + CDG_SMEM_TAIL);
+    h->smem = static_cast<size_t>(1024 + ring_bytes + CDG_SMEM_STAGING + CDG_SMEM_TAIL);
     h->grid = std::max(1, std::min(num_sms, items));
 
     cdg_plan_info_t &inf = h->info;
@@ -283,7 +359,7 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     inf.num_phases = stride * stride;
     for (int i = 0; i < stride * stride; ++i) inf.phase_taps[i] = phase_taps_by_index[i];
     inf.tile_m = CDG_BM; inf.tile_n = BN; inf.tile_k = CDG_BK;
-    inf.a_mode = flat ? 1 : 0;
+    inf.a_mode = halo ? 2 : (flat ? 1 : 0);
     inf.box_w = bw; inf.box_h = bh; inf.box_n = bnb;
     inf.stages = stages;
     inf.work_items = items;
@@ -337,8 +413,9 @@ int encode_operand_maps(cdg_plan_st *h, const void *dY, const void *Wp)
                                     static_cast<cuuint64_t>(h->P), static_cast<cuuint64_t>(h->N)};
         const cuuint64_t strides[3] = {static_cast<cuuint64_t>(h->K) * 2, static_cast<cuuint64_t>(h->Q) * h->K * 2,
                                        static_cast<cuuint64_t>(h->P) * h->Q * h->K * 2};
-        const cuuint32_t box[4] = {CDG_BK, static_cast<cuuint32_t>(p.box_w), static_cast<cuuint32_t>(p.box_h),
-                                   static_cast<cuuint32_t>(p.box_n)};
+        const cuuint32_t box[4] = {CDG_BK, static_cast<cuuint32_t>(p.halo ? p.halo_wb : p.box_w),
+                                   static_cast<cuuint32_t>(p.halo ? p.halo_hb : p.box_h),
+                                   static_cast<cuuint32_t>(p.halo ? 1 : p.box_n)};
         r = enc(&p.tmA, dt, 4, const_cast<void *>(dY), dims, strides, box, ones, CU_TENSOR_MAP_INTERLEAVE_NONE,
                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     }

@@ -26,25 +26,27 @@
 #define CDG_SMEM_STAGING (2 * 128 * 128)
 #define CDG_SMEM_TAIL 2048
 #define CDG_SMEM_TABLES 256
+#define CDG_MAX_STAGES_TOTAL 10  // all ring stages together (their mbarriers live in the 256-byte area)
 
 // One phase sub-convolution of a (possibly strided) dgrad.  The dX pixels with
 // h = stride*i + ph, w = stride*j + pw (0 <= i < hph, 0 <= j < wph) form the
 // phase sub-grid; the filter taps whose contributions land on it are
 // tap[tap_begin .. tap_begin + tap_count), each reading dY at (i + dr, j + ds).
 struct CdgPhase {
-    int ph, pw;
     int hph, wph;
-    int tap_begin, tap_count;
-    int zbw, zbh;          // phases without taps: box (zbw x zbh x 1 positions) of one zero-fill store
     int tiles_w, tiles_h;  // box tiles along j and i (4-D halo boxes, or the zero-fill box)
     int tiles_m;           // M tiles of this phase
     int items;             // tiles_m * (N tiles): work items of this phase
+    int16_t ph, pw;
+    int16_t tap_begin, tap_count;
+    int16_t zbw, zbh;        // phases without taps: box (zbw x zbh x 1 positions) of one zero-fill store
+    int16_t dr_min, ds_min;  // halo operand mode: smallest tap offsets (origin of the halo box)
 };
 
 struct CdgTap {
     int16_t dr, ds;  // dY row/column offset relative to the phase sub-grid position
     int16_t t;       // tap index r*S + s into the packed weights
-    int16_t unused;
+    int16_t hoff;    // halo operand mode: row of the halo box where this tap's operand starts
 };
 
 // How a tile's rows map onto dX and how the epilogue's TMA store addresses them.
@@ -65,6 +67,13 @@ struct CdgParams {  // CUtensorMap members carry their own (128-byte) alignment
     int BN, KB, stages, tiles_n, nphases, ntaps, total_items;
     int a_flat, box_w, box_h, box_n;
     int d_mode;           // CDG_D_*
+    int halo;             // 1: one dY halo box per (tile, K block) serves every tap (see dgrad_sm103.cu)
+    int halo_wb;          // halo box width = row pitch of the halo tile rows (tile width + tap span)
+    int halo_wt, halo_bh; // output tile: halo_wt columns x halo_bh rows of one image
+    int halo_hb;          // halo box height (halo_bh + tap span)
+    int a_stages, b_stages;   // halo mode: separate rings for halo boxes and weight tiles
+    uint32_t a_stage_bytes;   // halo mode: bytes of one halo stage (>= the box, room for every tap's 128 rows)
+    uint32_t tx_a, tx_b;      // halo mode: bytes one halo stage / one weight stage receives
     int m_step;           // linear operand modes: dY rows per M tile (128, or whole sub-grid rows)
     int rows_per_tile;    // CDG_D_ROWS: sub-grid rows per tile
     uint32_t idesc;       // tcgen05 instruction descriptor (kind::f16, M=128, N=BN)

@@ -101,7 +101,9 @@ __device__ __forceinline__ void box_origin(const CdgPhase &ph, int mt, int bw, i
 
 struct Ring {
     uint32_t a0;           // shared address of stage 0's A tile (1024-aligned)
-    uint32_t stage_bytes;  // A tile + B tile
+    uint32_t stage_bytes;  // A tile + B tile (halo mode: one halo box stage)
+    uint32_t b0;           // halo mode: first weight stage
+    uint32_t b_bytes;      // halo mode: bytes of one weight stage
     uint32_t out0;         // first of the two 16 KB output staging buffers
     uint32_t full0, empty0;
     uint32_t acc_full0, acc_empty0, drain;
@@ -188,6 +190,156 @@ __device__ __forceinline__ void drain_loads(const Ring &R, int stages, int *stat
     }
 }
 
+// ------------------------------------------------------------------ halo-mode loaders
+// Loader 0 streams one dY halo box per (tile, K block) into the A ring;
+// loaders 1.. stream the per-tap weight tiles into the B ring, round-robin.
+__device__ __forceinline__ void run_loader_halo(const CdgParams &p, const Ring &R, const CdgPhase *tab,
+                                                const CdgTap *taps, Ctl ctl, int li, bool leader,
+                                                volatile uint32_t *slot_parity)
+{
+    const uint64_t mapA = reinterpret_cast<uint64_t>(&p.tmA);
+    const uint64_t mapB = reinterpret_cast<uint64_t>(&p.tmB);
+    if (leader) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(mapA) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(mapB) : "memory");
+    }
+    const int KB = p.KB, tiles_n = p.tiles_n, BN = p.BN;
+    const int as = p.a_stages, bs = p.b_stages, bh = p.halo_bh, wt = p.halo_wt;
+    const uint32_t tx_a = p.tx_a, tx_b = p.tx_b;
+    int a_stage = 0, b_stage = 0, owner = 1;
+    uint32_t a_par = 0, b_par = 0;
+    bool ok = true;
+    for (ItemWalk w(tab, p.nphases); ok && w.valid(); w.next()) {
+        const CdgPhase &ph = tab[w.phase];
+        const int ntap = ph.tap_count;
+        if (ntap == 0) continue;
+        const int mt = tiles_n == 1 ? w.local : w.local / tiles_n;
+        const int nt = w.local - mt * tiles_n;
+        int j0, i0, n0;
+        box_origin(ph, mt, wt, bh, 1, j0, i0, n0);
+        const int c0 = nt * BN;
+        for (int kb = 0; ok && kb < KB; ++kb) {
+            if (li == 0) {
+                const uint32_t full = R.full0 + 8u * a_stage;
+                if (!wait_bar(R.empty0 + 8u * a_stage, a_par ^ 1u, ctl)) {
+                    ok = false;
+                    break;
+                }
+                if (leader) {
+                    slot_parity[a_stage] = a_par | 2u;
+                    mbar_arrive_expect_tx(full, tx_a);
+                    tma_load_4d(R.a0 + a_stage * R.stage_bytes, mapA, full, kb * CDG_BK, j0 + ph.ds_min,
+                                i0 + ph.dr_min, n0);
+                }
+                __syncwarp();
+                if (++a_stage == as) {
+                    a_stage = 0;
+                    a_par ^= 1u;
+                }
+            } else {
+                for (int tt = 0; tt < ntap; ++tt) {
+                    if (owner == li) {
+                        const int slot = as + b_stage;
+                        const uint32_t full = R.full0 + 8u * slot;
+                        if (!wait_bar(R.empty0 + 8u * slot, b_par ^ 1u, ctl)) {
+                            ok = false;
+                            break;
+                        }
+                        if (leader) {
+                            slot_parity[slot] = b_par | 2u;
+                            mbar_arrive_expect_tx(full, tx_b);
+                            tma_load_3d(R.b0 + b_stage * R.b_bytes, mapB, full, kb * CDG_BK, c0,
+                                        taps[ph.tap_begin + tt].t);
+                        }
+                        __syncwarp();
+                    }
+                    if (++owner == CDG_LOADERS) owner = 1;
+                    if (++b_stage == bs) {
+                        b_stage = 0;
+                        b_par ^= 1u;
+                    }
+                }
+            }
+        }
+    }
+}
+
+// Halo-mode MMA issuer: per K block one halo stage; per tap one weight stage
+// and four MMAs whose A operand starts at the tap's row of the halo box.
+__device__ __forceinline__ void run_mma_halo(const CdgParams &p, const Ring &R, const CdgPhase *tab,
+                                             const CdgTap *taps, Ctl ctl, uint32_t tmem_base, bool leader)
+{
+    const int KB = p.KB, as = p.a_stages, bs = p.b_stages;
+    const uint32_t idesc = p.idesc, acc_stride = p.acc_stride;
+    const uint64_t adesc0 = sdesc_k128_sw128(R.a0);
+    const uint64_t bdesc0 = sdesc_k128_sw128(R.b0);
+    const uint32_t astep = R.stage_bytes >> 4, bstep = R.b_bytes >> 4;  // descriptor units per stage
+    int a_stage = 0, b_stage = 0;
+    uint32_t a_par = 0, b_par = 0, acc_count = 0;
+    bool ok = true;
+    bool b_ready = false;  // full barrier of the current weight stage already seen complete
+    for (ItemWalk w(tab, p.nphases); ok && w.valid(); w.next()) {
+        const CdgPhase &ph = tab[w.phase];
+        const int ntap = ph.tap_count;
+        if (ntap == 0) continue;
+        const uint32_t acc = acc_count & 1u;
+        const uint32_t acc_parity = (acc_count >> 1) & 1u;
+        if (!wait_bar(R.acc_empty0 + 8u * acc, acc_parity ^ 1u, ctl)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * acc_stride;
+        for (int kb = 0; ok && kb < KB; ++kb) {
+            if (!wait_bar(R.full0 + 8u * a_stage, a_par, ctl)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint64_t abase = adesc0 + static_cast<uint64_t>(a_stage * astep);
+            for (int tt = 0; tt < ntap; ++tt) {
+                const int slot = as + b_stage;
+                if (!b_ready && !wait_bar(R.full0 + 8u * slot, b_par, ctl)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                {  // test the next weight stage while this tap's MMAs issue
+                    const int nb = b_stage + 1 == bs ? 0 : b_stage + 1;
+                    b_ready = mbar_test_wait(R.full0 + 8u * (as + nb), nb == 0 ? b_par ^ 1u : b_par);
+                }
+                if (leader) {
+                    // 128-byte rows: a row offset of hoff is 8*hoff descriptor units
+                    const uint64_t adesc = abase + 8u * static_cast<uint32_t>(taps[ph.tap_begin + tt].hoff);
+                    const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(b_stage * bstep);
+#pragma unroll
+                    for (int k = 0; k < CDG_BK / 16; ++k)
+                        umma_f16(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, (kb | tt | k) != 0);
+                    umma_commit(R.empty0 + 8u * slot);
+                }
+                __syncwarp();
+                if (++b_stage == bs) {
+                    b_stage = 0;
+                    b_par ^= 1u;
+                }
+            }
+            if (!ok) break;
+            if (leader) umma_commit(R.empty0 + 8u * a_stage);
+            __syncwarp();
+            if (++a_stage == as) {
+                a_stage = 0;
+                a_par ^= 1u;
+            }
+        }
+        if (!ok) break;
+        if (leader) umma_commit(R.acc_full0 + 8u * acc);
+        __syncwarp();
+        ++acc_count;
+    }
+    if (leader) umma_commit(R.drain);
+    __syncwarp();
+    volatile uint32_t no_abort = 0;
+    const Ctl drain_ctl{&no_abort, ctl.status};
+    wait_bar(R.drain, 0, drain_ctl);
+}
+
 // ------------------------------------------------------------------ MMA issuer
 // Whole warp runs the loop; lane 0 issues tcgen05.mma / tcgen05.commit.
 __device__ __forceinline__ void run_mma(const CdgParams &p, const Ring &R, const CdgPhase *tab, Ctl ctl,
@@ -204,6 +356,7 @@ __device__ __forceinline__ void run_mma(const CdgParams &p, const Ring &R, const
     uint32_t parity = 0;
     uint32_t acc_count = 0;
     bool ok = true;
+    bool ready = false;  // full barrier of `stage` already seen complete
     for (ItemWalk w(tab, p.nphases); ok && w.valid(); w.next()) {
         const int ntap = tab[w.phase].tap_count;
         if (ntap == 0) continue;
@@ -214,11 +367,20 @@ __device__ __forceinline__ void run_mma(const CdgParams &p, const Ring &R, const
         const uint32_t d_tmem = tmem_base + acc * acc_stride;
         const int nk = ntap * KB;
         for (int kk = 0; kk < nk; ++kk) {
-            if (!wait_bar(full0 + 8u * stage, parity, ctl)) {
+            if (!ready && !wait_bar(full0 + 8u * stage, parity, ctl)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
+            int next = stage + 1;
+            uint32_t next_parity = parity;
+            if (next == stages) {
+                next = 0;
+                next_parity ^= 1u;
+            }
+            // Test the next stage now, so that the test's latency overlaps this
+            // stage's MMAs instead of idling the tensor pipe between stages.
+            ready = mbar_test_wait(full0 + 8u * next, next_parity);
             if (leader) {
                 const uint64_t adesc = adesc0 + static_cast<uint64_t>(stage * dstep);
                 const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(stage * dstep);
@@ -228,10 +390,8 @@ __device__ __forceinline__ void run_mma(const CdgParams &p, const Ring &R, const
                 umma_commit(empty0 + 8u * stage);
             }
             __syncwarp();
-            if (++stage == stages) {
-                stage = 0;
-                parity ^= 1u;
-            }
+            stage = next;
+            parity = next_parity;
         }
         if (!ok) break;
         if (leader) umma_commit(R.acc_full0 + 8u * acc);
@@ -295,7 +455,7 @@ __device__ __forceinline__ long long phase_pixel(const CdgPhase &ph, int n, int 
     return (static_cast<long long>(n) * H + (stride * i + ph.ph)) * W + (stride * j + ph.pw);
 }
 
-template <int OUT_T, bool MASK, int IN_T>
+template <int OUT_T, bool MASK, int IN_T, bool HALO>
 __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, const CdgPhase *tab, Ctl ctl,
                                              uint32_t tmem_base)
 {
@@ -311,9 +471,23 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
     const int d_mode = p.d_mode, m_step = p.m_step, rpt = max(p.rows_per_tile, 1);
     const uint32_t acc_stride = p.acc_stride;
     const uint16_t *const xg = static_cast<const uint16_t *>(p.mask);
-    const int jl = row % bw, il = (row / bw) % bh, nl = row / (bw * bh);  // tile row -> box position
-    const uint32_t srow_off = static_cast<uint32_t>(row) * 128u;
-    const uint32_t sw = static_cast<uint32_t>(row & 7);
+    // tile row -> box position, and the staging row it fills (halo mode: row
+    // a*halo_wb + b is output (a, b); padding rows b >= halo_wt are dropped)
+    int jl, il, nl, srow;
+    if (HALO) {
+        const int a = row / p.halo_wb, b = row - (row / p.halo_wb) * p.halo_wb;
+        jl = b;
+        il = a;
+        nl = (b < p.halo_wt && a < p.halo_bh) ? 0 : 1;
+        srow = nl == 0 ? a * p.halo_wt + b : -1;
+    } else {
+        jl = row % bw;
+        il = (row / bw) % bh;
+        nl = row / (bw * bh);
+        srow = row;
+    }
+    const uint32_t srow_off = static_cast<uint32_t>(max(srow, 0)) * 128u;
+    const uint32_t sw = static_cast<uint32_t>(srow & 7);
     const uint32_t zero_buf = R.out0;  // staging buffer 0 doubles as the zero source
     bool zero_ready = false;
 
@@ -335,7 +509,7 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
                 if (lane == 0) bulk_wait_group_read<0>();  // no store may still read the buffer
                 named_bar_sync(1, 128);
 #pragma unroll
-                for (int q = 0; q < 8; ++q) st_shared_v4(zero_buf + srow_off + (q << 4), 0u, 0u, 0u, 0u);
+                for (int q = 0; q < 8; ++q) st_shared_v4(zero_buf + static_cast<uint32_t>(row) * 128u + (q << 4), 0u, 0u, 0u, 0u);
                 fence_proxy_async_smem();
                 named_bar_sync(1, 128);
                 zero_ready = true;
@@ -414,7 +588,8 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
 #pragma unroll
                     for (int e = 0; e < 4; ++e) wv[e] = pack2(v[2 * e], v[2 * e + 1], OUT_T);
                 }
-                st_shared_v4(buf + srow_off + ((static_cast<uint32_t>(q) ^ sw) << 4), wv[0], wv[1], wv[2], wv[3]);
+                if (srow >= 0)
+                    st_shared_v4(buf + srow_off + ((static_cast<uint32_t>(q) ^ sw) << 4), wv[0], wv[1], wv[2], wv[3]);
             }
             fence_proxy_async_smem();
             named_bar_sync(1, 128);
@@ -435,17 +610,20 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
 }
 
 // ------------------------------------------------------------------ kernel
-template <int OUT_T, bool MASK, int IN_T>
+template <int OUT_T, bool MASK, int IN_T, bool HALO>
 __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_constant__ CdgParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    const int stages = p.stages;
+    // shared memory: operand ring(s) | 2 x 16 KB output staging | mbarriers, flags | phase and tap tables
+    const int stages = HALO ? p.a_stages + p.b_stages : p.stages;  // mbarrier pairs
     Ring R;
     R.a0 = base;
-    R.stage_bytes = CDG_BM * 128 + p.BN * 128;
-    R.out0 = base + stages * R.stage_bytes;
+    R.stage_bytes = HALO ? p.a_stage_bytes : CDG_BM * 128 + p.BN * 128;
+    R.b0 = base + p.a_stages * R.stage_bytes;
+    R.b_bytes = p.BN * 128;
+    R.out0 = HALO ? R.b0 + p.b_stages * R.b_bytes : base + stages * R.stage_bytes;
     const uint32_t bars = R.out0 + CDG_SMEM_STAGING;
     R.full0 = bars;
     R.empty0 = bars + 8u * stages;
@@ -455,10 +633,14 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_cons
     uint8_t *const tail = smem_raw + (bars - raw);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tail + 8 * (2 * stages + 5));
     volatile uint32_t *abort_flag = tmem_slot + 1;
-    volatile uint32_t *slot_parity = tmem_slot + 2;  // [stages] (<= 8 entries)
+    volatile uint32_t *slot_parity = tmem_slot + 2;  // [stages] (<= CDG_MAX_STAGES_TOTAL entries)
     CdgPhase *tab = reinterpret_cast<CdgPhase *>(tail + CDG_SMEM_TABLES);
     CdgTap *taps = reinterpret_cast<CdgTap *>(tab + CDG_MAX_PHASES);
-
+    static_assert(8 * (2 * CDG_MAX_STAGES_TOTAL + 5) + 8 + 4 * CDG_MAX_STAGES_TOTAL <= CDG_SMEM_TABLES,
+                  "mbarrier area overflows");
+    static_assert(CDG_SMEM_TABLES + CDG_MAX_PHASES * sizeof(CdgPhase) + CDG_MAX_TAPS * sizeof(CdgTap) <=
+                      CDG_SMEM_TAIL,
+                  "phase and tap tables overflow the shared-memory tail");
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     for (int i = threadIdx.x; i < p.nphases; i += blockDim.x) tab[i] = p.phase[i];
     for (int i = threadIdx.x; i < p.ntaps; i += blockDim.x) taps[i] = p.tap[i];
@@ -486,10 +668,16 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_cons
     const uint32_t tmem_base = *tmem_slot;
     const Ctl ctl{abort_flag, p.status};
 
-    if (warp == 1)
-        run_mma(p, R, tab, ctl, tmem_base, lane == 0);
+    if (warp == 1) {
+        if (HALO)
+            run_mma_halo(p, R, tab, taps, ctl, tmem_base, lane == 0);
+        else
+            run_mma(p, R, tab, ctl, tmem_base, lane == 0);
+    }
     else if (warp >= CDG_EPI_WARP0)
-        run_epilogue<OUT_T, MASK, IN_T>(p, R, tab, ctl, tmem_base);
+        run_epilogue<OUT_T, MASK, IN_T, HALO>(p, R, tab, ctl, tmem_base);
+    else if (HALO)
+        run_loader_halo(p, R, tab, taps, ctl, warp == 0 ? 0 : warp - 1, lane == 0, slot_parity);
     else
         run_loader(p, R, tab, taps, ctl, warp == 0 ? 0 : warp - 1, lane == 0, slot_parity);
 
@@ -531,16 +719,21 @@ namespace {
 typedef void (*DgradFn)(CdgParams);
 
 template <int OUT_T, bool MASK, int IN_T>
-DgradFn pick() { return cdg::dgrad_kernel<OUT_T, MASK, IN_T>; }
+DgradFn pick(bool halo)
+{
+    return halo ? cdg::dgrad_kernel<OUT_T, MASK, IN_T, true> : cdg::dgrad_kernel<OUT_T, MASK, IN_T, false>;
+}
 
-DgradFn select_kernel(int out_type, int in_type, bool mask)
+DgradFn select_kernel(int out_type, int in_type, bool mask, bool halo)
 {
     if (in_type == CDG_T_F16) {
-        if (out_type == CDG_T_F32) return mask ? pick<CDG_T_F32, true, CDG_T_F16>() : pick<CDG_T_F32, false, CDG_T_F16>();
-        return mask ? pick<CDG_T_F16, true, CDG_T_F16>() : pick<CDG_T_F16, false, CDG_T_F16>();
+        if (out_type == CDG_T_F32)
+            return mask ? pick<CDG_T_F32, true, CDG_T_F16>(halo) : pick<CDG_T_F32, false, CDG_T_F16>(halo);
+        return mask ? pick<CDG_T_F16, true, CDG_T_F16>(halo) : pick<CDG_T_F16, false, CDG_T_F16>(halo);
     }
-    if (out_type == CDG_T_F32) return mask ? pick<CDG_T_F32, true, CDG_T_BF16>() : pick<CDG_T_F32, false, CDG_T_BF16>();
-    return mask ? pick<CDG_T_BF16, true, CDG_T_BF16>() : pick<CDG_T_BF16, false, CDG_T_BF16>();
+    if (out_type == CDG_T_F32)
+        return mask ? pick<CDG_T_F32, true, CDG_T_BF16>(halo) : pick<CDG_T_F32, false, CDG_T_BF16>(halo);
+    return mask ? pick<CDG_T_BF16, true, CDG_T_BF16>(halo) : pick<CDG_T_BF16, false, CDG_T_BF16>(halo);
 }
 
 }  // namespace
@@ -552,15 +745,19 @@ DgradFn select_kernel(int out_type, int in_type, bool mask)
 cudaError_t cdg_prepare_dgrad(int out_type, int in_type, bool mask, size_t smem)
 {
     if (smem > static_cast<size_t>(CDG_MAX_DYN_SMEM)) return cudaErrorInvalidValue;
-    DgradFn fn = select_kernel(out_type, in_type, mask);
-    return cudaFuncSetAttribute(reinterpret_cast<const void *>(fn), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                CDG_MAX_DYN_SMEM);
+    for (int halo = 0; halo < 2; ++halo) {
+        DgradFn fn = select_kernel(out_type, in_type, mask, halo != 0);
+        const cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void *>(fn),
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, CDG_MAX_DYN_SMEM);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 cudaError_t cdg_launch_dgrad(const CdgParams &p, int out_type, int in_type, bool mask, int grid, size_t smem,
                              cudaStream_t stream)
 {
-    DgradFn fn = select_kernel(out_type, in_type, mask);
+    DgradFn fn = select_kernel(out_type, in_type, mask, p.halo != 0);
     fn<<<grid, CDG_THREADS, smem, stream>>>(p);
     return cudaGetLastError();
 }

@@ -160,3 +160,13 @@ def test_interleaved_plans():
         assert run.status() == 0
         ref = oracle_full(run)
         assert_close(got, ref, run.odt, run.layer.name)
+
+
+@pytest.mark.parametrize("L", [SWEEP[0], SWEEP[1], SWEEP[4], SWEEP[5], SWEEP[12], SWEEP[14], BATCH8[0]],
+                         ids=lambda L: L.name)
+def test_halo_operand_mode(L, monkeypatch):
+    """The opt-in halo operand mode (one dY box per tile and K block serves
+    every tap) gives the same results."""
+    monkeypatch.setenv("CDG_HALO", "1")
+    run, _, _ = check_layer(L)
+    assert run.plan.info()["a_mode"] == 2
