@@ -23,13 +23,17 @@ LIB_PATH = os.path.join(HERE, "libcdg.so")
 
 OK = 0
 STATUS_NAMES = {0: "CDG_OK", 1: "CDG_ERR_INVALID_ARG", 2: "CDG_ERR_UNSUPPORTED", 3: "CDG_ERR_ALIGNMENT",
-                4: "CDG_ERR_ALIAS", 5: "CDG_ERR_CUDA", 6: "CDG_ERR_TIMEOUT", 7: "CDG_ERR_NO_DEVICE"}
+                4: "CDG_ERR_ALIAS", 5: "CDG_ERR_CUDA", 6: "CDG_ERR_TIMEOUT", 7: "CDG_ERR_NO_DEVICE",
+                8: "CDG_ERR_SCRATCH_TOO_SMALL"}
+ERR_SCRATCH_TOO_SMALL = 8
+NOALLOC_MAX_WEIGHT_BYTES = 8 << 20
 F16, BF16 = 0, 1
 EPI_RELU_BWD, EPI_OUT_F32 = 1, 2
 DTYPES = {"f16": F16, "bf16": BF16}
 
 EXPORTS = ("cdg_plan", "cdg_plan_host", "cdg_destroy", "cdg_get_output_dims", "cdg_packed_weight_bytes",
-           "cdg_plan_get_info", "cdg_prepack_weights", "cdg_dgrad", "cdg_device_status", "cdg_status_string")
+           "cdg_plan_get_info", "cdg_prepack_weights", "cdg_dgrad", "cdg_device_status", "cdg_status_string",
+           "cdg_dgrad_noalloc")
 
 
 class CdgError(RuntimeError):
@@ -89,6 +93,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.cdg_device_status.restype = i
     lib.cdg_status_string.argtypes = [i]
     lib.cdg_status_string.restype = ctypes.c_char_p
+    lib.cdg_dgrad_noalloc.argtypes = [hp, vp, vp, vp, vp, vp]
+    lib.cdg_dgrad_noalloc.restype = i
     if path == LIB_PATH:
         _lib = lib
     return lib
@@ -187,6 +193,15 @@ class Plan:
                                 _stream(stream))
         if rc != OK:
             raise CdgError(rc, "cdg_dgrad")
+
+    def dgrad_noalloc(self, dY, W_krsc, dX, relu_mask=None, stream=None) -> None:
+        """dgrad from the unpacked KRSC filter without any device allocation
+        (the packed weights live in the library's own scratch array; see
+        cdg_dgrad_noalloc in cdg.h for the size limit and the sharing rules)."""
+        rc = self.lib.cdg_dgrad_noalloc(self.handle, _addr(dY), _addr(W_krsc), _addr(dX), _addr(relu_mask),
+                                        _stream(stream))
+        if rc != OK:
+            raise CdgError(rc, "cdg_dgrad_noalloc")
 
     def device_status(self, stream=None) -> int:
         return int(self.lib.cdg_device_status(self.handle, _stream(stream)))

@@ -612,8 +612,91 @@ const char *cdg_status_string(int status)
     case CDG_ERR_CUDA: return "CUDA runtime or launch error";
     case CDG_ERR_TIMEOUT: return "device pipeline wait timed out";
     case CDG_ERR_NO_DEVICE: return "handle was planned without a device";
+    case CDG_ERR_SCRATCH_TOO_SMALL:
+        return "packed weights exceed the 8 MiB scratch of cdg_dgrad_noalloc (R*S*C*K must be <= 4194304)";
     default: return "unknown status";
     }
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------ allocation-free entry point
+// Scratch for cdg_dgrad_noalloc: [0, 256) the kernel's status word, then the
+// packed weights.  Device code could name it directly; host code needs its
+// device address, which cudaGetSymbolAddress returns per device.
+#define CDG_NOALLOC_STATUS_BYTES 256
+static __device__ __align__(256) unsigned char cdg_noalloc_scratch[CDG_NOALLOC_STATUS_BYTES + CDG_NOALLOC_MAX_WEIGHT_BYTES];
+
+#include <mutex>
+
+namespace {
+
+constexpr int kNoallocMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+unsigned char *g_noalloc_addr[kNoallocMaxDevices];  // device address of the scratch, per device
+unsigned g_noalloc_prepared[kNoallocMaxDevices];     // kernels whose shared-memory limit was raised
+
+// Once per device (with that device current): the scratch's device address,
+// and the dynamic shared-memory opt-in of the kernel instantiation `key`.
+int noalloc_setup(int dev, const cdg_plan_st *h, unsigned char **scratch)
+{
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_addr[dev]) {
+        void *addr = nullptr;
+        if (cudaGetSymbolAddress(&addr, cdg_noalloc_scratch) != cudaSuccess || !addr) return CDG_ERR_CUDA;
+        g_noalloc_addr[dev] = static_cast<unsigned char *>(addr);
+    }
+    const unsigned key = 1u << (h->out_type * 4 + h->in_type * 2 + (h->mask ? 1 : 0));
+    if (!(g_noalloc_prepared[dev] & key)) {
+        if (cdg_prepare_dgrad(h->out_type, h->in_type, h->mask, h->smem) != cudaSuccess) return CDG_ERR_CUDA;
+        g_noalloc_prepared[dev] |= key;
+    }
+    *scratch = g_noalloc_addr[dev];
+    return CDG_OK;
+}
+
+}  // namespace
+
+extern "C" int cdg_dgrad_noalloc(cdg_handle_t h, const void *dY, const void *W_krsc, void *dX,
+                                 const void *relu_mask, cdg_stream_t stream)
+{
+    if (!h || !dY || !W_krsc || !dX) return CDG_ERR_INVALID_ARG;
+    if (h->mask != (relu_mask != nullptr)) return CDG_ERR_INVALID_ARG;
+    const size_t wbytes = cdg_packed_weight_bytes(h);
+    if (wbytes > CDG_NOALLOC_MAX_WEIGHT_BYTES) return CDG_ERR_SCRATCH_TOO_SMALL;
+    if (!aligned16(dY) || !aligned16(W_krsc) || !aligned16(dX) || (relu_mask && !aligned16(relu_mask)))
+        return CDG_ERR_ALIGNMENT;
+    const size_t dx_bytes = static_cast<size_t>(h->N) * h->H * h->W * h->C * (h->out_type == CDG_T_F32 ? 4 : 2);
+    const size_t dy_bytes = static_cast<size_t>(h->N) * h->P * h->Q * h->K * 2;
+    const size_t x_bytes = static_cast<size_t>(h->N) * h->H * h->W * h->C * 2;
+    if (overlaps(dX, dx_bytes, dY, dy_bytes) || overlaps(dX, dx_bytes, W_krsc, wbytes) ||
+        (relu_mask && overlaps(dX, dx_bytes, relu_mask, x_bytes)))
+        return CDG_ERR_ALIAS;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return CDG_ERR_CUDA;
+    if (dev < 0 || dev >= kNoallocMaxDevices) return CDG_ERR_UNSUPPORTED;
+    unsigned char *scratch = nullptr;
+    const int rc = noalloc_setup(dev, h, &scratch);
+    if (rc != CDG_OK) return rc;
+    int *status = reinterpret_cast<int *>(scratch);
+    void *Wp = scratch + CDG_NOALLOC_STATUS_BYTES;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(status, 0, sizeof(int), s) != cudaSuccess) return CDG_ERR_CUDA;
+    if (cdg_launch_prepack(W_krsc, Wp, h->K, h->R * h->S, h->C, s) != cudaSuccess) return CDG_ERR_CUDA;
+    if (dY != h->cached_dY || Wp != h->cached_Wp) {
+        const int e = encode_operand_maps(h, dY, Wp);
+        if (e != CDG_OK) return e;
+    }
+    if (dX != h->cached_dX) {
+        const int e = encode_store_maps(h, dX);
+        if (e != CDG_OK) return e;
+    }
+    CdgParams &p = h->prm;
+    p.dX = dX;
+    p.mask = relu_mask;
+    p.status = status;
+    if (cdg_launch_dgrad(p, h->out_type, h->in_type, h->mask, h->grid, h->smem, s) != cudaSuccess)
+        return CDG_ERR_CUDA;
+    return CDG_OK;
+}

@@ -59,7 +59,9 @@ typedef enum {
     CDG_ERR_ALIAS = 4,        /* dX overlaps dY, the packed weights or x          */
     CDG_ERR_CUDA = 5,         /* a CUDA runtime/driver call or launch failed      */
     CDG_ERR_TIMEOUT = 6,      /* a kernel gave up a bounded pipeline wait         */
-    CDG_ERR_NO_DEVICE = 7     /* the handle was planned without a device          */
+    CDG_ERR_NO_DEVICE = 7,    /* the handle was planned without a device          */
+    CDG_ERR_SCRATCH_TOO_SMALL = 8 /* cdg_dgrad_noalloc: packed weights exceed     */
+                                  /* CDG_NOALLOC_MAX_WEIGHT_BYTES                 */
 } cdg_status_t;
 
 typedef enum { CDG_F16 = 0, CDG_BF16 = 1 } cdg_dtype_t;
@@ -155,6 +157,46 @@ int cdg_device_status(cdg_handle_t h, cdg_stream_t stream);
 
 /* Static text for a status code. */
 const char *cdg_status_string(int status);
+
+/*
+ * dgrad for callers that cannot allocate device memory -- code that runs
+ * where cudaMalloc is off limits (inside a memory pool that must not grow,
+ * a real-time loop that may not block on the allocator, an embedding runtime
+ * that owns all device memory).  This entry point has no counterpart in the
+ * pages the method is described on; it is an addition of this library.
+ *
+ * It computes exactly what cdg_prepack_weights followed by cdg_dgrad
+ * computes, but takes the forward filter W in its stored KRSC layout and
+ * needs neither a packed-weight buffer nor a device status word from the
+ * caller: both live in one scratch array compiled into the library
+ * (a file-scope __device__ array that every GPU which loads the library keeps
+ * until the process exits).  It calls no cudaMalloc, no cudaFree and no
+ * allocating library routine.
+ *
+ *   h          a plan from cdg_plan, or from cdg_plan_host (which touches no
+ *              device; pass the device's SM count as num_sms)
+ *   dY, dX, relu_mask   as for cdg_dgrad (device pointers, 16-byte aligned)
+ *   W_krsc     the forward filter [K][R][S][C], device pointer
+ *
+ * Limit: the packed weights (R*S*C*K elements of 2 bytes) must fit in
+ * CDG_NOALLOC_MAX_WEIGHT_BYTES (8 MiB: 4,194,304 weights, enough for every
+ * ResNet-50 convolution); larger filters return CDG_ERR_SCRATCH_TOO_SMALL
+ * before anything is launched.
+ *
+ * The first call on a device finds the scratch array's device address
+ * (cudaGetSymbolAddress, with that device current) and raises the kernels'
+ * shared-memory limit; make that first call before any stream capture.
+ *
+ * Every call on a device shares the one scratch array, which keeps the last
+ * call's packed weights; each call clears the status word and re-packs W on
+ * its stream first.  Calls whose work overlaps on the GPU (different streams,
+ * or different host threads) race on the scratch array and give wrong
+ * results: serialise them.  A device-side pipeline timeout is recorded in the
+ * scratch status word and not returned here.
+ */
+#define CDG_NOALLOC_MAX_WEIGHT_BYTES (8u << 20)
+int cdg_dgrad_noalloc(cdg_handle_t h, const void *dY, const void *W_krsc, void *dX, const void *relu_mask,
+                      cdg_stream_t stream);
 
 #ifdef __cplusplus
 }
