@@ -50,6 +50,30 @@ def load_peaks():
     return dict(FALLBACK_PEAKS, source="fallback")
 
 
+def kernel_sources_sha256() -> str:
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "implicit_gemm_dgrad_gb300", "csrc", "*"))):
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def profiled_traffic(layer_name: str):
+    """DRAM bytes (read + write) of one launch from the committed ncu capture,
+    or None when that capture is of another layer or of other kernel sources."""
+    path = os.path.join(ROOT, "profiles", "dgrad_kernel_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    if d.get("layer") != layer_name or d.get("sources_sha256") != kernel_sources_sha256():
+        return None
+    return int(d["dram_read_bytes"]) + int(d["dram_write_bytes"])
+
+
 def roofline_time_s(layer, peaks):
     t_tc = layer.flops / (peaks["bf16_tflops_sustained"] * 1e12)
     t_hbm = layer.bytes / (peaks["hbm_gbs"] * 1e9)
@@ -269,7 +293,8 @@ def main():
     else:
         achieved, peak, unit = Ld.bytes / td / 1e9, peaks["hbm_gbs"], "GB/s"
     roofline = {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
-                "frac": round(achieved / peak, 4), "traffic": None, "kernel": f"dgrad_kernel ({Ld.name})",
+                "frac": round(achieved / peak, 4), "traffic": profiled_traffic(Ld.name),
+                "algorithmic_bytes": Ld.bytes, "kernel": f"dgrad_kernel ({Ld.name})",
                 "peak_source": peaks["source"] + (" sustained bf16" if bound == "tensor" else " copy bandwidth"),
                 "share_of_step": round(per_layer_ms[dom] / float(np.sum(per_layer_ms)), 4),
                 "step_roofline_frac": round(sum(roofline_time_s(L, peaks)[0] for (L, *_r) in state)

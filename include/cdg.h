@@ -117,8 +117,9 @@ typedef struct {
     int tile_m;           /* dX pixels per tile (GEMM M tile)                      */
     int tile_n;           /* channels per tile (GEMM N tile)                       */
     int tile_k;           /* dY channels per pipeline stage (GEMM K block)         */
-    int a_mode;           /* 0: 4-D halo boxes over dY, 1: dY rows as a 2-D matrix */
-    int box_w, box_h, box_n; /* 4-D box (a_mode 0)                                 */
+    int a_mode;           /* 0: 4-D boxes over dY per tap, 1: dY rows as a matrix, */
+                          /* 2: one halo box per K block for all taps (opt-in)     */
+    int box_w, box_h, box_n; /* output tile box (a_mode 0 and 2)                   */
     int stages;           /* shared-memory pipeline depth                          */
     int work_items;       /* (phase, m-tile, n-tile) items in one launch           */
     int grid;             /* persistent CTAs                                       */
