@@ -288,6 +288,23 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
         }
     }
 
+    // ---- CTA pairs: two CTAs (a cluster) share each 256-row tile through the
+    // 2-SM MMA, each holding its 128 rows of dY and half of the weight tile.
+    // Measured on GB300 over the ResNet-50 layers: pairs win (4-8 %) for
+    // 256-channel N tiles whose tiles run at least 9 pipeline stages, and lose
+    // elsewhere (short tiles couple two SMs' epilogues and rings).
+    int tap_phases = 0, tap_sum = 0;
+    for (const CdgPhase &f : phases)
+        if (f.tap_count > 0) {
+            ++tap_phases;
+            tap_sum += f.tap_count;
+        }
+    const double stages_per_tile = tap_phases ? double(tap_sum) / tap_phases * ceil_div(K, CDG_BK) : 0.0;
+    const char *pair_env = std::getenv("CDG_PAIR");  // "0": never, "1": whenever BN allows
+    bool pair = !halo && BN == 256 && num_sms >= 2 && stages_per_tile >= 9.0;
+    if (pair_env && pair_env[0] == '0') pair = false;
+    if (pair_env && pair_env[0] == '1') pair = !halo && BN >= 128 && num_sms >= 2;
+
     int items = 0;
     for (CdgPhase &f : phases) {
         if (f.tap_count == 0) {
@@ -306,10 +323,12 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
             f.tiles_h = ceil_div(f.hph, bh);
             f.tiles_m = f.tiles_w * f.tiles_h * ceil_div(N, bnb);
         }
-        f.items = f.tiles_m * tiles_n;
+        // a pair takes M tiles 2t and 2t + 1 (an odd last tile's partner reads
+        // and writes only out-of-range coordinates, which TMA fills and drops)
+        f.items = (pair ? (f.tiles_m + 1) / 2 : f.tiles_m) * tiles_n;
         items += f.items;
     }
-    const int stage_bytes = CDG_BM * 128 + BN * 128;
+    const int stage_bytes = CDG_BM * 128 + (pair ? BN / 2 : BN) * 128;
     const int stages = halo ? a_stages + b_stages : std::min(kMaxStages, ring_budget / stage_bytes);
     const int ring_bytes = halo ? a_stages * hrows * 128 + b_stages * BN * 128 : stages * stage_bytes;
     // two accumulators, each at least as wide as the 64-column chunks the epilogue reads
@@ -342,16 +361,20 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     p.tx_a = static_cast<uint32_t>(hwb * hhb * 128);
     p.tx_b = static_cast<uint32_t>(BN * 128);
     const uint32_t ab = dtype == CDG_BF16 ? 1u : 0u;
+    const int mma_m = pair ? 2 * CDG_BM : CDG_BM;
     p.idesc = (1u << 4) | (ab << 7) | (ab << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
-              (static_cast<uint32_t>(CDG_BM >> 4) << 24);
-    p.tx_bytes = static_cast<uint32_t>((flat ? CDG_BM : bw * bh * bnb) * 128 + BN * 128);
+              (static_cast<uint32_t>(mma_m >> 4) << 24);
+    // bytes one stage's full barrier waits for (a pair's leader: both CTAs' copies)
+    const int a_bytes = (flat ? CDG_BM : bw * bh * bnb) * 128;
+    p.tx_bytes = static_cast<uint32_t>(pair ? 2 * (a_bytes + (BN / 2) * 128) : a_bytes + BN * 128);
+    p.pair = pair ? 1 : 0;
     p.tmem_cols = static_cast<uint32_t>(tmem_cols);
     p.acc_stride = static_cast<uint32_t>(tmem_cols / 2);
     for (size_t i = 0; i < phases.size(); ++i) p.phase[i] = phases[i];
     for (size_t i = 0; i < taps.size(); ++i) p.tap[i] = taps[i];
 
     h->smem = static_cast<size_t>(1024 + ring_bytes + CDG_SMEM_STAGING + CDG_SMEM_TAIL);
-    h->grid = std::max(1, std::min(num_sms, items));
+    h->grid = pair ? 2 * std::max(1, std::min(num_sms / 2, items)) : std::max(1, std::min(num_sms, items));
 
     cdg_plan_info_t &inf = h->info;
     std::memset(&inf, 0, sizeof inf);
@@ -366,7 +389,19 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     inf.grid = h->grid;
     inf.smem_bytes = static_cast<int>(h->smem);
     inf.tmem_cols = tmem_cols;
+    inf.cta_pair = pair ? 1 : 0;
 
+    if (!host_only && pair) {
+        // pairs must be co-resident on one GPC: size the persistent grid by
+        // how many the device can hold at once, not by the SM count alone
+        if (cdg_prepare_dgrad(h->out_type, h->in_type, h->mask, h->smem) != cudaSuccess) {
+            delete h;
+            return CDG_ERR_CUDA;
+        }
+        const int pairs = cdg_max_active_pairs(h->out_type, h->in_type, h->mask, h->smem);
+        if (pairs >= 1) h->grid = 2 * std::max(1, std::min(pairs, items));
+        inf.grid = h->grid;
+    }
     if (!host_only) {
         if (cudaGetDevice(&h->device) != cudaSuccess ||
             cdg_prepare_dgrad(h->out_type, h->in_type, h->mask, h->smem) != cudaSuccess ||
@@ -423,7 +458,7 @@ int encode_operand_maps(cdg_plan_st *h, const void *dY, const void *Wp)
     const cuuint64_t bdims[3] = {static_cast<cuuint64_t>(h->K), static_cast<cuuint64_t>(h->C),
                                  static_cast<cuuint64_t>(h->R) * h->S};
     const cuuint64_t bstrides[2] = {static_cast<cuuint64_t>(h->K) * 2, static_cast<cuuint64_t>(h->C) * h->K * 2};
-    const cuuint32_t bbox[3] = {CDG_BK, static_cast<cuuint32_t>(p.BN), 1};
+    const cuuint32_t bbox[3] = {CDG_BK, static_cast<cuuint32_t>(p.pair ? p.BN / 2 : p.BN), 1};
     r = enc(&p.tmB, dt, 3, const_cast<void *>(Wp), bdims, bstrides, bbox, ones, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return CDG_ERR_CUDA;

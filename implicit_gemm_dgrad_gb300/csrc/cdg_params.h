@@ -68,6 +68,7 @@ struct CdgParams {  // CUtensorMap members carry their own (128-byte) alignment
     int a_flat, box_w, box_h, box_n;
     int d_mode;           // CDG_D_*
     int halo;             // 1: one dY halo box per (tile, K block) serves every tap (see dgrad_sm103.cu)
+    int pair;             // 1: CTA pairs (clusters of 2) share 256-row tiles through 2-SM MMAs
     int halo_wb;          // halo box width = row pitch of the halo tile rows (tile width + tap span)
     int halo_wt, halo_bh; // output tile: halo_wt columns x halo_bh rows of one image
     int halo_hb;          // halo box height (halo_bh + tap span)
@@ -92,3 +93,4 @@ cudaError_t cdg_launch_dgrad(const CdgParams &p, int out_type, int in_type, bool
                              int grid, size_t smem, cudaStream_t stream);
 cudaError_t cdg_prepare_dgrad(int out_type, int in_type, bool mask, size_t smem);
 cudaError_t cdg_launch_prepack(const void *W, void *Wp, int K, int T, int C, cudaStream_t stream);
+int cdg_max_active_pairs(int out_type, int in_type, bool mask, size_t smem);

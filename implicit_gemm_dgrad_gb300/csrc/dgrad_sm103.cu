@@ -65,9 +65,12 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Ctl ctl)
 // as (phase, index within the phase), phases read from the shared-memory copy.
 struct ItemWalk {
     const CdgPhase *tab;
-    int nph;
+    int nph, step;
     int phase, local;
-    __device__ __forceinline__ ItemWalk(const CdgPhase *t, int n) : tab(t), nph(n), phase(0), local(blockIdx.x)
+    // items start, start + step, ...: one CTA's (step = gridDim.x) or one CTA
+    // pair's (step = number of pairs) share of the work list
+    __device__ __forceinline__ ItemWalk(const CdgPhase *t, int n, int start, int stp)
+        : tab(t), nph(n), step(stp), phase(0), local(start)
     {
         settle();
     }
@@ -81,8 +84,20 @@ struct ItemWalk {
     __device__ __forceinline__ bool valid() const { return phase < nph; }
     __device__ __forceinline__ void next()
     {
-        local += gridDim.x;
+        local += step;
         settle();
+    }
+};
+
+// Work distribution: which items this CTA walks, and (pairs) its M tile in a pair.
+struct Sched {
+    int start, step;
+    int pair;   // 1: CTA pairs share each item (M tiles 2*t and 2*t + 1)
+    int rank;   // rank in the pair (0 = leader, issues the MMAs)
+    __device__ __forceinline__ int m_tile(int local, int tiles_n) const
+    {
+        const int t = tiles_n == 1 ? local : local / tiles_n;
+        return pair ? 2 * t + rank : t;
     }
 };
 
@@ -114,9 +129,10 @@ struct Ring {
 // with index li issues the stages whose global counter is li modulo
 // CDG_LOADERS.  The whole warp runs the loop; lane 0 issues.  The parity of
 // each slot's latest load is recorded in shared memory for the abort drain.
+template <bool PAIR>
 __device__ __forceinline__ void run_loader(const CdgParams &p, const Ring &R, const CdgPhase *tab,
                                            const CdgTap *taps, Ctl ctl, int li, bool leader,
-                                           volatile uint32_t *slot_parity)
+                                           volatile uint32_t *slot_parity, Sched S)
 {
     const uint64_t mapA = reinterpret_cast<uint64_t>(&p.tmA);
     const uint64_t mapB = reinterpret_cast<uint64_t>(&p.tmB);
@@ -129,20 +145,23 @@ __device__ __forceinline__ void run_loader(const CdgParams &p, const Ring &R, co
     const bool flat = p.a_flat != 0;
     const uint32_t tx = p.tx_bytes;
     const uint32_t a0 = R.a0, sbytes = R.stage_bytes, full0 = R.full0, empty0 = R.empty0;
+    const uint32_t lead_full0 = PAIR ? mapa_shared(full0, 0) : full0;
 
     int stage = 0;
     uint32_t parity = 0;
     int owner = 0;  // loader index of the current global stage
     bool ok = true;
-    for (ItemWalk w(tab, p.nphases); ok && w.valid(); w.next()) {
+    for (ItemWalk w(tab, p.nphases, S.start, S.step); ok && w.valid(); w.next()) {
         const CdgPhase &ph = tab[w.phase];
         const int ntap = ph.tap_count;
         if (ntap == 0) continue;
-        const int mt = tiles_n == 1 ? w.local : w.local / tiles_n;
-        const int nt = w.local - mt * tiles_n;
+        const int tq = tiles_n == 1 ? w.local : w.local / tiles_n;
+        const int nt = w.local - tq * tiles_n;
+        const int mt = S.m_tile(w.local, tiles_n);
         int j0 = 0, i0 = 0, n0 = 0;
         if (!flat) box_origin(ph, mt, bw, bh, bn, j0, i0, n0);
-        const int c0 = nt * BN;
+        // a pair splits the N tile's weight rows: this CTA loads its half
+        const int c0 = nt * BN + (PAIR ? S.rank * (BN / 2) : 0);
         const int m0 = mt * m_step;
         for (int tt = 0; ok && tt < ntap; ++tt) {
             const CdgTap tap = taps[ph.tap_begin + tt];
@@ -156,13 +175,25 @@ __device__ __forceinline__ void run_loader(const CdgParams &p, const Ring &R, co
                     }
                     if (leader) {
                         slot_parity[stage] = parity | 2u;  // bit 1: slot used
-                        mbar_arrive_expect_tx(full, tx);
                         const uint32_t sa = a0 + stage * sbytes;
-                        if (flat)
-                            tma_load_2d(sa, mapA, full, kb * CDG_BK, m0);
-                        else
-                            tma_load_4d(sa, mapA, full, kb * CDG_BK, y, z, n0);
-                        tma_load_3d(sa + CDG_BM * 128, mapB, full, kb * CDG_BK, c0, t);
+                        if (PAIR) {
+                            // both CTAs' copies complete on the leader's barrier,
+                            // which expects the bytes of both
+                            const uint32_t lead = lead_full0 + 8u * stage;
+                            if (S.rank == 0) mbar_arrive_expect_tx(full, tx);
+                            if (flat)
+                                tma_load_2d_pair(sa, mapA, lead, kb * CDG_BK, m0);
+                            else
+                                tma_load_4d_pair(sa, mapA, lead, kb * CDG_BK, y, z, n0);
+                            tma_load_3d_pair(sa + CDG_BM * 128, mapB, lead, kb * CDG_BK, c0, t);
+                        } else {
+                            mbar_arrive_expect_tx(full, tx);
+                            if (flat)
+                                tma_load_2d(sa, mapA, full, kb * CDG_BK, m0);
+                            else
+                                tma_load_4d(sa, mapA, full, kb * CDG_BK, y, z, n0);
+                            tma_load_3d(sa + CDG_BM * 128, mapB, full, kb * CDG_BK, c0, t);
+                        }
                     }
                     __syncwarp();
                 }
@@ -195,7 +226,7 @@ __device__ __forceinline__ void drain_loads(const Ring &R, int stages, int *stat
 // loaders 1.. stream the per-tap weight tiles into the B ring, round-robin.
 __device__ __forceinline__ void run_loader_halo(const CdgParams &p, const Ring &R, const CdgPhase *tab,
                                                 const CdgTap *taps, Ctl ctl, int li, bool leader,
-                                                volatile uint32_t *slot_parity)
+                                                volatile uint32_t *slot_parity, Sched S)
 {
     const uint64_t mapA = reinterpret_cast<uint64_t>(&p.tmA);
     const uint64_t mapB = reinterpret_cast<uint64_t>(&p.tmB);
@@ -209,12 +240,12 @@ __device__ __forceinline__ void run_loader_halo(const CdgParams &p, const Ring &
     int a_stage = 0, b_stage = 0, owner = 1;
     uint32_t a_par = 0, b_par = 0;
     bool ok = true;
-    for (ItemWalk w(tab, p.nphases); ok && w.valid(); w.next()) {
+    for (ItemWalk w(tab, p.nphases, S.start, S.step); ok && w.valid(); w.next()) {
         const CdgPhase &ph = tab[w.phase];
         const int ntap = ph.tap_count;
         if (ntap == 0) continue;
-        const int mt = tiles_n == 1 ? w.local : w.local / tiles_n;
-        const int nt = w.local - mt * tiles_n;
+        const int mt = S.m_tile(w.local, tiles_n);
+        const int nt = w.local - (tiles_n == 1 ? w.local : w.local / tiles_n) * tiles_n;
         int j0, i0, n0;
         box_origin(ph, mt, wt, bh, 1, j0, i0, n0);
         const int c0 = nt * BN;
@@ -267,7 +298,7 @@ __device__ __forceinline__ void run_loader_halo(const CdgParams &p, const Ring &
 // Halo-mode MMA issuer: per K block one halo stage; per tap one weight stage
 // and four MMAs whose A operand starts at the tap's row of the halo box.
 __device__ __forceinline__ void run_mma_halo(const CdgParams &p, const Ring &R, const CdgPhase *tab,
-                                             const CdgTap *taps, Ctl ctl, uint32_t tmem_base, bool leader)
+                                             const CdgTap *taps, Ctl ctl, uint32_t tmem_base, bool leader, Sched S)
 {
     const int KB = p.KB, as = p.a_stages, bs = p.b_stages;
     const uint32_t idesc = p.idesc, acc_stride = p.acc_stride;
@@ -278,7 +309,7 @@ __device__ __forceinline__ void run_mma_halo(const CdgParams &p, const Ring &R, 
     uint32_t a_par = 0, b_par = 0, acc_count = 0;
     bool ok = true;
     bool b_ready = false;  // full barrier of the current weight stage already seen complete
-    for (ItemWalk w(tab, p.nphases); ok && w.valid(); w.next()) {
+    for (ItemWalk w(tab, p.nphases, S.start, S.step); ok && w.valid(); w.next()) {
         const CdgPhase &ph = tab[w.phase];
         const int ntap = ph.tap_count;
         if (ntap == 0) continue;
@@ -342,8 +373,9 @@ __device__ __forceinline__ void run_mma_halo(const CdgParams &p, const Ring &R, 
 
 // ------------------------------------------------------------------ MMA issuer
 // Whole warp runs the loop; lane 0 issues tcgen05.mma / tcgen05.commit.
+template <bool PAIR>
 __device__ __forceinline__ void run_mma(const CdgParams &p, const Ring &R, const CdgPhase *tab, Ctl ctl,
-                                        uint32_t tmem_base, bool leader)
+                                        uint32_t tmem_base, bool leader, Sched S)
 {
     const int KB = p.KB, stages = p.stages;
     const uint32_t idesc = p.idesc, acc_stride = p.acc_stride;
@@ -357,7 +389,7 @@ __device__ __forceinline__ void run_mma(const CdgParams &p, const Ring &R, const
     uint32_t acc_count = 0;
     bool ok = true;
     bool ready = false;  // full barrier of `stage` already seen complete
-    for (ItemWalk w(tab, p.nphases); ok && w.valid(); w.next()) {
+    for (ItemWalk w(tab, p.nphases, S.start, S.step); ok && w.valid(); w.next()) {
         const int ntap = tab[w.phase].tap_count;
         if (ntap == 0) continue;
         const uint32_t acc = acc_count & 1u;
@@ -385,21 +417,38 @@ __device__ __forceinline__ void run_mma(const CdgParams &p, const Ring &R, const
                 const uint64_t adesc = adesc0 + static_cast<uint64_t>(stage * dstep);
                 const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(stage * dstep);
 #pragma unroll
-                for (int k = 0; k < CDG_BK / 16; ++k)  // 16 elements = 32 bytes = 2 descriptor units
-                    umma_f16(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, (kk | k) != 0);
-                umma_commit(empty0 + 8u * stage);
+                for (int k = 0; k < CDG_BK / 16; ++k) {  // 16 elements = 32 bytes = 2 descriptor units
+                    if (PAIR)
+                        umma_f16_pair(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, (kk | k) != 0);
+                    else
+                        umma_f16(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, (kk | k) != 0);
+                }
+                if (PAIR)
+                    umma_commit_pair(empty0 + 8u * stage);  // frees the slot in both CTAs
+                else
+                    umma_commit(empty0 + 8u * stage);
             }
             __syncwarp();
             stage = next;
             parity = next_parity;
         }
         if (!ok) break;
-        if (leader) umma_commit(R.acc_full0 + 8u * acc);
+        if (leader) {
+            if (PAIR)
+                umma_commit_pair(R.acc_full0 + 8u * acc);
+            else
+                umma_commit(R.acc_full0 + 8u * acc);
+        }
         __syncwarp();
         ++acc_count;
     }
     // All MMAs issued by this warp complete before TMEM is released.
-    if (leader) umma_commit(R.drain);
+    if (leader) {
+        if (PAIR)
+            umma_commit_pair(R.drain);
+        else
+            umma_commit(R.drain);
+    }
     __syncwarp();
     volatile uint32_t no_abort = 0;
     const Ctl drain_ctl{&no_abort, ctl.status};
@@ -455,9 +504,9 @@ __device__ __forceinline__ long long phase_pixel(const CdgPhase &ph, int n, int 
     return (static_cast<long long>(n) * H + (stride * i + ph.ph)) * W + (stride * j + ph.pw);
 }
 
-template <int OUT_T, bool MASK, int IN_T, bool HALO>
+template <int OUT_T, bool MASK, int IN_T, bool HALO, bool PAIR>
 __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, const CdgPhase *tab, Ctl ctl,
-                                             uint32_t tmem_base)
+                                             uint32_t tmem_base, Sched S)
 {
     constexpr int OSZ = OUT_T == CDG_T_F32 ? 4 : 2;
     constexpr int CH = 128 / OSZ;  // channels per 128-byte staging row
@@ -494,10 +543,10 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
     // TMA stores are spread over the four warps' lane 0 (an issue holds its
     // thread for a few hundred cycles): chunk k is stored by epilogue warp k % 4.
     uint32_t acc_count = 0, chunk_count = 0;
-    for (ItemWalk w(tab, p.nphases); w.valid(); w.next()) {
+    for (ItemWalk w(tab, p.nphases, S.start, S.step); w.valid(); w.next()) {
         const CdgPhase &ph = tab[w.phase];
-        const int mt = tiles_n == 1 ? w.local : w.local / tiles_n;
-        const int nt = w.local - mt * tiles_n;
+        const int mt = S.m_tile(w.local, tiles_n);
+        const int nt = w.local - (tiles_n == 1 ? w.local : w.local / tiles_n) * tiles_n;
         const int c_begin = nt * BN;
         const int c_end = min(C, c_begin + BN);
         const uint64_t mapD = reinterpret_cast<uint64_t>(&p.tmD[w.phase]);
@@ -568,7 +617,12 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
             if (cc + CH >= BN) {  // last read of this accumulator: hand it back to the MMA warp
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(R.acc_empty0 + 8u * acc);
+                if (lane == 0) {
+                    if (PAIR && S.rank != 0)  // the pair's MMA warp lives in the leader CTA
+                        mbar_arrive_cluster(mapa_shared(R.acc_empty0 + 8u * acc, 0));
+                    else
+                        mbar_arrive(R.acc_empty0 + 8u * acc);
+                }
             }
 #pragma unroll
             for (int q = 0; q < 8; ++q) {  // 16-byte pieces of this row
@@ -610,9 +664,16 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
 }
 
 // ------------------------------------------------------------------ kernel
-template <int OUT_T, bool MASK, int IN_T, bool HALO>
+// MODE: 0 per-tap operand boxes, one CTA per tile; 1 halo operand mode;
+//       2 per-tap boxes, CTA pairs (cluster of 2) sharing 256-row tiles through
+//         tcgen05.mma.cta_group::2: each CTA holds its own 128 rows of A and
+//         half of the weight tile, which halves the B bytes every SM's shared
+//         memory takes in and hands to the tensor core.
+template <int OUT_T, bool MASK, int IN_T, int MODE>
 __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_constant__ CdgParams p)
 {
+    constexpr bool HALO = MODE == 1;
+    constexpr bool PAIR = MODE == 2;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -620,7 +681,7 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_cons
     const int stages = HALO ? p.a_stages + p.b_stages : p.stages;  // mbarrier pairs
     Ring R;
     R.a0 = base;
-    R.stage_bytes = HALO ? p.a_stage_bytes : CDG_BM * 128 + p.BN * 128;
+    R.stage_bytes = p.a_stage_bytes;
     R.b0 = base + p.a_stages * R.stage_bytes;
     R.b_bytes = p.BN * 128;
     R.out0 = HALO ? R.b0 + p.b_stages * R.b_bytes : base + stages * R.stage_bytes;
@@ -642,6 +703,21 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_cons
                       CDG_SMEM_TAIL,
                   "phase and tap tables overflow the shared-memory tail");
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    Sched S;
+    if (PAIR) {
+        uint32_t cid, ncl;
+        asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(cid));
+        asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(ncl));
+        S.start = static_cast<int>(cid);
+        S.step = static_cast<int>(ncl);
+        S.pair = 1;
+        S.rank = static_cast<int>(cluster_ctarank());
+    } else {
+        S.start = blockIdx.x;
+        S.step = gridDim.x;
+        S.pair = 0;
+        S.rank = 0;
+    }
     for (int i = threadIdx.x; i < p.nphases; i += blockDim.x) tab[i] = p.phase[i];
     for (int i = threadIdx.x; i < p.ntaps; i += blockDim.x) taps[i] = p.tap[i];
     if (threadIdx.x == 0) {
@@ -651,7 +727,8 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_cons
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(R.acc_full0 + 8u * a, 1);
-            mbar_init(R.acc_empty0 + 8u * a, 4);  // one arrival per epilogue warp
+            // one arrival per epilogue warp (in a pair, the leader's counts both CTAs' warps)
+            mbar_init(R.acc_empty0 + 8u * a, PAIR && S.rank == 0 ? 8 : 4);
         }
         mbar_init(R.drain, 1);
         *abort_flag = 0u;
@@ -659,35 +736,61 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_cons
         fence_mbar_init();
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), p.tmem_cols);
-        tmem_relinquish();
+        if (PAIR) {
+            tmem_alloc_pair(smem_u32(tmem_slot), p.tmem_cols);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_u32(tmem_slot), p.tmem_cols);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
     __syncthreads();
+    if (PAIR) cluster_sync();  // both CTAs' barriers exist before any copy or arrive crosses over
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const Ctl ctl{abort_flag, p.status};
 
     if (warp == 1) {
-        if (HALO)
-            run_mma_halo(p, R, tab, taps, ctl, tmem_base, lane == 0);
-        else
-            run_mma(p, R, tab, ctl, tmem_base, lane == 0);
+        if (HALO) {
+            run_mma_halo(p, R, tab, taps, ctl, tmem_base, lane == 0, S);
+        } else if (!PAIR || S.rank == 0) {
+            run_mma<PAIR>(p, R, tab, ctl, tmem_base, lane == 0, S);
+        } else {
+            // the leader issues the pair's MMAs; wait until they are all done
+            // with this CTA's tensor memory
+            volatile uint32_t no_abort = 0;
+            wait_bar(R.drain, 0, Ctl{&no_abort, p.status});
+        }
+    } else if (warp >= CDG_EPI_WARP0) {
+        run_epilogue<OUT_T, MASK, IN_T, HALO, PAIR>(p, R, tab, ctl, tmem_base, S);
+    } else if (HALO) {
+        run_loader_halo(p, R, tab, taps, ctl, warp == 0 ? 0 : warp - 1, lane == 0, slot_parity, S);
+    } else {
+        run_loader<PAIR>(p, R, tab, taps, ctl, warp == 0 ? 0 : warp - 1, lane == 0, slot_parity, S);
     }
-    else if (warp >= CDG_EPI_WARP0)
-        run_epilogue<OUT_T, MASK, IN_T, HALO>(p, R, tab, ctl, tmem_base);
-    else if (HALO)
-        run_loader_halo(p, R, tab, taps, ctl, warp == 0 ? 0 : warp - 1, lane == 0, slot_parity);
-    else
-        run_loader(p, R, tab, taps, ctl, warp == 0 ? 0 : warp - 1, lane == 0, slot_parity);
 
     __syncthreads();
-    if (*abort_flag && threadIdx.x == 0) drain_loads(R, stages, p.status, slot_parity);
+    if (*abort_flag && threadIdx.x == 0) {
+        if (!PAIR || S.rank == 0) {
+            drain_loads(R, stages, p.status, slot_parity);
+        } else {
+            // this CTA's copies complete on the leader's barriers; give any
+            // still in flight time to land before the pair may exit
+            const uint64_t t0 = global_timer_ns();
+            while (global_timer_ns() - t0 < 200000ull) {
+            }
+        }
+    }
     tc_fence_before();
     __syncthreads();
+    if (PAIR) cluster_sync();  // neither CTA leaves while the other may still signal it
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, p.tmem_cols);
+        if (PAIR)
+            tmem_dealloc_pair(tmem_base, p.tmem_cols);
+        else
+            tmem_dealloc(tmem_base, p.tmem_cols);
     }
 }
 
@@ -719,22 +822,26 @@ namespace {
 typedef void (*DgradFn)(CdgParams);
 
 template <int OUT_T, bool MASK, int IN_T>
-DgradFn pick(bool halo)
+DgradFn pick(int mode)
 {
-    return halo ? cdg::dgrad_kernel<OUT_T, MASK, IN_T, true> : cdg::dgrad_kernel<OUT_T, MASK, IN_T, false>;
+    if (mode == 1) return cdg::dgrad_kernel<OUT_T, MASK, IN_T, 1>;
+    if (mode == 2) return cdg::dgrad_kernel<OUT_T, MASK, IN_T, 2>;
+    return cdg::dgrad_kernel<OUT_T, MASK, IN_T, 0>;
 }
 
-DgradFn select_kernel(int out_type, int in_type, bool mask, bool halo)
+DgradFn select_kernel(int out_type, int in_type, bool mask, int mode)
 {
     if (in_type == CDG_T_F16) {
         if (out_type == CDG_T_F32)
-            return mask ? pick<CDG_T_F32, true, CDG_T_F16>(halo) : pick<CDG_T_F32, false, CDG_T_F16>(halo);
-        return mask ? pick<CDG_T_F16, true, CDG_T_F16>(halo) : pick<CDG_T_F16, false, CDG_T_F16>(halo);
+            return mask ? pick<CDG_T_F32, true, CDG_T_F16>(mode) : pick<CDG_T_F32, false, CDG_T_F16>(mode);
+        return mask ? pick<CDG_T_F16, true, CDG_T_F16>(mode) : pick<CDG_T_F16, false, CDG_T_F16>(mode);
     }
     if (out_type == CDG_T_F32)
-        return mask ? pick<CDG_T_F32, true, CDG_T_BF16>(halo) : pick<CDG_T_F32, false, CDG_T_BF16>(halo);
-    return mask ? pick<CDG_T_BF16, true, CDG_T_BF16>(halo) : pick<CDG_T_BF16, false, CDG_T_BF16>(halo);
+        return mask ? pick<CDG_T_F32, true, CDG_T_BF16>(mode) : pick<CDG_T_F32, false, CDG_T_BF16>(mode);
+    return mask ? pick<CDG_T_BF16, true, CDG_T_BF16>(mode) : pick<CDG_T_BF16, false, CDG_T_BF16>(mode);
 }
+
+int kernel_mode(const CdgParams &p) { return p.halo ? 1 : (p.pair ? 2 : 0); }
 
 }  // namespace
 
@@ -745,8 +852,8 @@ DgradFn select_kernel(int out_type, int in_type, bool mask, bool halo)
 cudaError_t cdg_prepare_dgrad(int out_type, int in_type, bool mask, size_t smem)
 {
     if (smem > static_cast<size_t>(CDG_MAX_DYN_SMEM)) return cudaErrorInvalidValue;
-    for (int halo = 0; halo < 2; ++halo) {
-        DgradFn fn = select_kernel(out_type, in_type, mask, halo != 0);
+    for (int mode = 0; mode < 3; ++mode) {
+        DgradFn fn = select_kernel(out_type, in_type, mask, mode);
         const cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void *>(fn),
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize, CDG_MAX_DYN_SMEM);
         if (e != cudaSuccess) return e;
@@ -757,9 +864,44 @@ cudaError_t cdg_prepare_dgrad(int out_type, int in_type, bool mask, size_t smem)
 cudaError_t cdg_launch_dgrad(const CdgParams &p, int out_type, int in_type, bool mask, int grid, size_t smem,
                              cudaStream_t stream)
 {
-    DgradFn fn = select_kernel(out_type, in_type, mask, p.halo != 0);
-    fn<<<grid, CDG_THREADS, smem, stream>>>(p);
-    return cudaGetLastError();
+    DgradFn fn = select_kernel(out_type, in_type, mask, kernel_mode(p));
+    if (!p.pair) {
+        fn<<<grid, CDG_THREADS, smem, stream>>>(p);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(CDG_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fn, p);
+}
+
+// Largest number of CTA pairs of this kernel that can be resident at once.
+int cdg_max_active_pairs(int out_type, int in_type, bool mask, size_t smem)
+{
+    DgradFn fn = select_kernel(out_type, in_type, mask, 2);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(CDG_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void *>(fn), &cfg) != cudaSuccess) return -1;
+    return n;
 }
 
 cudaError_t cdg_launch_prepack(const void *W, void *Wp, int K, int T, int C, cudaStream_t stream)

@@ -125,6 +125,7 @@ typedef struct {
     int grid;             /* persistent CTAs                                       */
     int smem_bytes;       /* dynamic shared memory per CTA                         */
     int tmem_cols;        /* tensor-memory columns per CTA                         */
+    int cta_pair;         /* 1: CTA pairs share 256-row tiles (2-SM MMA)            */
 } cdg_plan_info_t;
 
 int cdg_plan_get_info(cdg_handle_t h, cdg_plan_info_t *info);
