@@ -127,7 +127,7 @@ struct Ring {
 // ------------------------------------------------------------------ loaders
 // CDG_LOADERS warps walk the same (item, tap, k-block) sequence; the loader
 // with index li issues the stages whose global counter is li modulo
-// CDG_LOADERS.  The whole warp runs the loop; lane 0 issues.  The parity of
+// CDG_LOADERS.  The whole warp runs the loop; one elected lane issues.  The parity of
 // each slot's latest load is recorded in shared memory for the abort drain.
 template <bool PAIR>
 __device__ __forceinline__ void run_loader(const CdgParams &p, const Ring &R, const CdgPhase *tab,
@@ -372,7 +372,7 @@ __device__ __forceinline__ void run_mma_halo(const CdgParams &p, const Ring &R, 
 }
 
 // ------------------------------------------------------------------ MMA issuer
-// Whole warp runs the loop; lane 0 issues tcgen05.mma / tcgen05.commit.
+// Whole warp runs the loop; one elected lane issues tcgen05.mma / tcgen05.commit.
 template <bool PAIR>
 __device__ __forceinline__ void run_mma(const CdgParams &p, const Ring &R, const CdgPhase *tab, Ctl ctl,
                                         uint32_t tmem_base, bool leader, Sched S)
@@ -511,6 +511,7 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
     constexpr int OSZ = OUT_T == CDG_T_F32 ? 4 : 2;
     constexpr int CH = 128 / OSZ;  // channels per 128-byte staging row
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const bool elected = elect_one_sync();  // this warp's issuing lane for stores and arrivals
     const int quad = warp & 3;  // this warp may read TMEM lanes [32*quad, 32*quad + 32)
     const int row = quad * 32 + lane;
     const int ew = warp - CDG_EPI_WARP0;  // epilogue warp 0..3
@@ -540,7 +541,7 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
     const uint32_t zero_buf = R.out0;  // staging buffer 0 doubles as the zero source
     bool zero_ready = false;
 
-    // TMA stores are spread over the four warps' lane 0 (an issue holds its
+    // TMA stores are spread over the four warps' elected lanes (an issue holds its
     // thread for a few hundred cycles): chunk k is stored by epilogue warp k % 4.
     uint32_t acc_count = 0, chunk_count = 0;
     for (ItemWalk w(tab, p.nphases, S.start, S.step); w.valid(); w.next()) {
@@ -555,7 +556,7 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
             // No tap reaches this phase: dX = +0.0, stored box by box from a
             // zeroed staging buffer.
             if (!zero_ready) {
-                if (lane == 0) bulk_wait_group_read<0>();  // no store may still read the buffer
+                if (elected) bulk_wait_group_read<0>();  // no store may still read the buffer
                 named_bar_sync(1, 128);
 #pragma unroll
                 for (int q = 0; q < 8; ++q) st_shared_v4(zero_buf + static_cast<uint32_t>(row) * 128u + (q << 4), 0u, 0u, 0u, 0u);
@@ -566,7 +567,7 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
             int j0, i0, n0;
             box_origin(ph, mt, ph.zbw, ph.zbh, 1, j0, i0, n0);
             const int nchunks = (c_end - c_begin + CH - 1) / CH;
-            if (lane == 0)
+            if (elected)
                 for (int q = ew; q < nchunks; q += 4) {
                     tma_store_4d(mapD, zero_buf, c_begin + q * CH, j0, i0, n0);
                     bulk_commit_group();
@@ -577,7 +578,7 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
         if (zero_ready) {
             // back from zero-fill items (the planner orders them last, so this
             // is only a safeguard): every zero store must have read its source
-            if (lane == 0) bulk_wait_group_read<0>();
+            if (elected) bulk_wait_group_read<0>();
             named_bar_sync(1, 128);
             zero_ready = false;
         }
@@ -607,7 +608,7 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
             const uint32_t buf = R.out0 + (k & 1u) * (128u * 128u);
             // the store that last read this buffer (chunk k-2, issued by warp
             // (k-2) % 4) must be done with it
-            if (k >= 2 && lane == 0 && static_cast<uint32_t>(ew) == ((k - 2) & 3u)) bulk_wait_group_read<0>();
+            if (k >= 2 && elected && static_cast<uint32_t>(ew) == ((k - 2) & 3u)) bulk_wait_group_read<0>();
             named_bar_sync(1, 128);
             uint32_t r[CH];
 #pragma unroll
@@ -617,7 +618,7 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
             if (cc + CH >= BN) {  // last read of this accumulator: hand it back to the MMA warp
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) {
+                if (elected) {
                     if (PAIR && S.rank != 0)  // the pair's MMA warp lives in the leader CTA
                         mbar_arrive_cluster(mapa_shared(R.acc_empty0 + 8u * acc, 0));
                     else
@@ -647,7 +648,7 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
             }
             fence_proxy_async_smem();
             named_bar_sync(1, 128);
-            if (lane == 0 && static_cast<uint32_t>(ew) == (k & 3u)) {
+            if (elected && static_cast<uint32_t>(ew) == (k & 3u)) {
                 const int c = c_begin + cc;
                 if (d_mode == CDG_D_BOX4)
                     tma_store_4d(mapD, buf, c, j0, i0, n0);
@@ -660,7 +661,7 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
         }
         ++acc_count;
     }
-    if (lane == 0) bulk_wait_group_all();
+    if (elected) bulk_wait_group_all();
 }
 
 // ------------------------------------------------------------------ kernel
@@ -753,9 +754,9 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_cons
 
     if (warp == 1) {
         if (HALO) {
-            run_mma_halo(p, R, tab, taps, ctl, tmem_base, lane == 0, S);
+            run_mma_halo(p, R, tab, taps, ctl, tmem_base, elect_one_sync(), S);
         } else if (!PAIR || S.rank == 0) {
-            run_mma<PAIR>(p, R, tab, ctl, tmem_base, lane == 0, S);
+            run_mma<PAIR>(p, R, tab, ctl, tmem_base, elect_one_sync(), S);
         } else {
             // the leader issues the pair's MMAs; wait until they are all done
             // with this CTA's tensor memory
@@ -765,9 +766,9 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_cons
     } else if (warp >= CDG_EPI_WARP0) {
         run_epilogue<OUT_T, MASK, IN_T, HALO, PAIR>(p, R, tab, ctl, tmem_base, S);
     } else if (HALO) {
-        run_loader_halo(p, R, tab, taps, ctl, warp == 0 ? 0 : warp - 1, lane == 0, slot_parity, S);
+        run_loader_halo(p, R, tab, taps, ctl, warp == 0 ? 0 : warp - 1, elect_one_sync(), slot_parity, S);
     } else {
-        run_loader<PAIR>(p, R, tab, taps, ctl, warp == 0 ? 0 : warp - 1, lane == 0, slot_parity, S);
+        run_loader<PAIR>(p, R, tab, taps, ctl, warp == 0 ? 0 : warp - 1, elect_one_sync(), slot_parity, S);
     }
 
     __syncthreads();
