@@ -703,7 +703,7 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_cons
     static_assert(CDG_SMEM_TABLES + CDG_MAX_PHASES * sizeof(CdgPhase) + CDG_MAX_TAPS * sizeof(CdgTap) <=
                       CDG_SMEM_TAIL,
                   "phase and tap tables overflow the shared-memory tail");
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int warp = threadIdx.x / 32;
     Sched S;
     if (PAIR) {
         uint32_t cid, ncl;
