@@ -368,6 +368,10 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     const int a_bytes = (flat ? CDG_BM : bw * bh * bnb) * 128;
     p.tx_bytes = static_cast<uint32_t>(pair ? 2 * (a_bytes + (BN / 2) * 128) : a_bytes + BN * 128);
     p.pair = pair ? 1 : 0;
+    // Programmatic dependent launch: the kernel's set-up overlaps the end of the
+    // previous kernel in the stream ("0" turns it off).
+    const char *pdl_env = std::getenv("CDG_PDL");
+    p.pdl = (pdl_env && pdl_env[0] == '0') ? 0 : 1;
     p.tmem_cols = static_cast<uint32_t>(tmem_cols);
     p.acc_stride = static_cast<uint32_t>(tmem_cols / 2);
     for (size_t i = 0; i < phases.size(); ++i) p.phase[i] = phases[i];

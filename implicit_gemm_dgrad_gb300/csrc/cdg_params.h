@@ -69,6 +69,7 @@ struct CdgParams {  // CUtensorMap members carry their own (128-byte) alignment
     int d_mode;           // CDG_D_*
     int halo;             // 1: one dY halo box per (tile, K block) serves every tap (see dgrad_sm103.cu)
     int pair;             // 1: CTA pairs (clusters of 2) share 256-row tiles through 2-SM MMAs
+    int pdl;              // 1: launch with programmatic stream serialization (host side only)
     int halo_wb;          // halo box width = row pitch of the halo tile rows (tile width + tap span)
     int halo_wt, halo_bh; // output tile: halo_wt columns x halo_bh rows of one image
     int halo_hb;          // halo box height (halo_bh + tap span)

@@ -719,6 +719,9 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_cons
         S.pair = 0;
         S.rank = 0;
     }
+    // The next kernel in the stream may be scheduled now: with one CTA per SM
+    // its CTAs take SMs only as this grid's CTAs exit.
+    grid_dep_launch_dependents();
     for (int i = threadIdx.x; i < p.nphases; i += blockDim.x) tab[i] = p.phase[i];
     for (int i = threadIdx.x; i < p.ntaps; i += blockDim.x) taps[i] = p.tap[i];
     if (threadIdx.x == 0) {
@@ -736,6 +739,11 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_cons
         for (int s = 0; s < stages; ++s) slot_parity[s] = 0u;
         fence_mbar_init();
     }
+    // Everything above touches only shared memory and kernel parameters.  Global
+    // memory (dY, W, x, dX, the status word) and tensor memory are used only
+    // after the kernels this launch depends on have completed; allocating TMEM
+    // after the wait means a waiting CTA never holds TMEM another kernel needs.
+    grid_dep_wait();
     if (warp == 1) {
         if (PAIR) {
             tmem_alloc_pair(smem_u32(tmem_slot), p.tmem_cols);
@@ -866,22 +874,27 @@ cudaError_t cdg_launch_dgrad(const CdgParams &p, int out_type, int in_type, bool
                              cudaStream_t stream)
 {
     DgradFn fn = select_kernel(out_type, in_type, mask, kernel_mode(p));
-    if (!p.pair) {
-        fn<<<grid, CDG_THREADS, smem, stream>>>(p);
-        return cudaGetLastError();
-    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(CDG_THREADS);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
+    if (p.pair) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = 2;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    if (p.pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, fn, p);
 }
 

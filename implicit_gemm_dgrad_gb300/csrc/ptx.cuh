@@ -208,6 +208,13 @@ __device__ __forceinline__ void bulk_wait_group_all() { asm volatile("cp.async.b
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // Named barrier over `count` threads (ids 1..15; id 0 is __syncthreads).
+// Programmatic dependent launch.  launch_dependents lets the next kernel of the
+// stream (if launched with programmatic stream serialization) be scheduled
+// now; wait blocks until every grid this one depends on has completed and its
+// memory is visible (it returns at once when there is none).
+__device__ __forceinline__ void grid_dep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Elect one lane of a converged warp (elect.sync over the full mask).  Single-lane
 // issue of tcgen05.mma and TMA under this predicate measured about twice as fast
 // on GB300 as under (lane == 0) for N <= 128 MMA tiles: the operands stay

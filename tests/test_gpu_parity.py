@@ -170,3 +170,31 @@ def test_halo_operand_mode(L, monkeypatch):
     monkeypatch.setenv("CDG_HALO", "1")
     run, _, _ = check_layer(L)
     assert run.plan.info()["a_mode"] == 2
+
+
+def test_chained_launches_keep_stream_order():
+    """Launches on one stream start their set-up while the previous launch
+    finishes (programmatic dependent launch), but must still see stream order:
+    a dgrad that reads the previous dgrad's dX as its dY, then a dgrad that
+    overwrites that dX while the reader may still be draining."""
+    import torch
+    A = _case(2, 20, 20, 64, 64, 3, 3, 1, 1, 1, "bf16", idx=3)
+    B = _case(2, 40, 40, 32, 64, 3, 3, 2, 1, 1, "bf16", idx=4)  # B's dY has A's dX shape
+    ra, rb = GpuRun(A), GpuRun(B)
+    assert rb.plan.output_dims == (A.H, A.W)
+    ra.run()
+    first = ra.result_bytes().copy()  # A's dX, synchronised
+    ra.out.body().view(torch.int16).fill_(0x7E01)  # NaN again
+    neg_dY = -ra.d_dY  # exact in bf16: A's dX becomes its negation
+    torch.cuda.synchronize()
+    # the chain, with no synchronisation inside it
+    ra.run()
+    rb.plan.dgrad(ra.out.ptr, rb.d_Wp, rb.out.ptr, None)
+    ra.plan.dgrad(neg_dY, ra.d_Wp, ra.out.ptr, None)
+    got_b = rb.result()
+    last_a = ra.result_bytes()
+    assert ra.status() == 0 and rb.status() == 0
+    assert_close(decode_out(last_a, ra.odt), -decode_out(first, ra.odt), ra.odt, "A rewritten after B")
+    dY_b = first.view(np.uint16).reshape(A.N, A.H, A.W, A.C)
+    ref_b = oracle.dgrad(dY_b, rb.W, B.H, B.W, B.stride, B.pad, B.dil, dtype=B.dtype)
+    assert_close(got_b, ref_b, rb.odt, "B after A")
