@@ -85,7 +85,10 @@ def roofline_time_s(layer, peaks):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms in the background."""
+    """nvidia-smi clocks and throttle reasons sampled every 50 ms in the
+    background.  Entering waits (up to 5 s) for the first sample, so sampling
+    is running when the timed region starts; the summary counts only the
+    samples taken after that first one."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -101,9 +104,19 @@ class ClockSampler:
             self.out = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=self.out, stderr=subprocess.DEVNULL)
+                 "-lms", "50"], stdout=self.out, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+        self.skip = 0
+        if self.proc is not None:
+            t0 = time.perf_counter()
+            while time.perf_counter() - t0 < 5.0 and self.proc.poll() is None:
+                with open(self.path) as f:
+                    n = sum(1 for _ in f)
+                if n >= 1:
+                    self.skip = n
+                    break
+                time.sleep(0.01)
         return self
 
     def __exit__(self, *exc):
@@ -121,18 +134,21 @@ class ClockSampler:
         sm, smax, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
-            for line in f:
-                parts = [x.strip() for x in line.split(",")]
-                if len(parts) < 9:
-                    continue
-                try:
-                    sm.append(float(parts[1]))
-                    smax = float(parts[2])
-                except ValueError:
-                    continue
-                for name, val in zip(names, parts[5:9]):
-                    if val.lower().startswith("active"):
-                        reasons.add(name)
+            lines = f.readlines()
+        # samples from the timed region; if it was shorter than one period, the last one before it
+        lines = lines[self.skip:] or lines[-1:]
+        for line in lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
         os.unlink(self.path)
         return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": smax,
                 "reasons": sorted(reasons), "samples": len(sm)}

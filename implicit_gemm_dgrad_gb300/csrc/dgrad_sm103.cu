@@ -325,6 +325,8 @@ __device__ __forceinline__ void run_mma_halo(const CdgParams &p, const Ring &R, 
             }
             tc_fence_after();
             const uint64_t abase = adesc0 + static_cast<uint64_t>(a_stage * astep);
+            const CdgTap *ptap = taps + ph.tap_begin;
+            int hoff = ptap[0].hoff;  // loaded a stage ahead: its latency overlaps MMA issue
             for (int tt = 0; tt < ntap; ++tt) {
                 const int slot = as + b_stage;
                 if (!b_ready && !wait_bar(R.full0 + 8u * slot, b_par, ctl)) {
@@ -336,9 +338,10 @@ __device__ __forceinline__ void run_mma_halo(const CdgParams &p, const Ring &R, 
                     const int nb = b_stage + 1 == bs ? 0 : b_stage + 1;
                     b_ready = mbar_test_wait(R.full0 + 8u * (as + nb), nb == 0 ? b_par ^ 1u : b_par);
                 }
+                const int hnext = tt + 1 < ntap ? ptap[tt + 1].hoff : 0;
                 if (leader) {
                     // 128-byte rows: a row offset of hoff is 8*hoff descriptor units
-                    const uint64_t adesc = abase + 8u * static_cast<uint32_t>(taps[ph.tap_begin + tt].hoff);
+                    const uint64_t adesc = abase + 8u * static_cast<uint32_t>(hoff);
                     const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(b_stage * bstep);
 #pragma unroll
                     for (int k = 0; k < CDG_BK / 16; ++k)
@@ -346,6 +349,7 @@ __device__ __forceinline__ void run_mma_halo(const CdgParams &p, const Ring &R, 
                     umma_commit(R.empty0 + 8u * slot);
                 }
                 __syncwarp();
+                hoff = hnext;
                 if (++b_stage == bs) {
                     b_stage = 0;
                     b_par ^= 1u;
