@@ -48,7 +48,8 @@ class PlanInfo(ctypes.Structure):
                 ("tile_k", ctypes.c_int), ("a_mode", ctypes.c_int), ("box_w", ctypes.c_int),
                 ("box_h", ctypes.c_int), ("box_n", ctypes.c_int), ("stages", ctypes.c_int),
                 ("work_items", ctypes.c_int), ("grid", ctypes.c_int), ("smem_bytes", ctypes.c_int),
-                ("tmem_cols", ctypes.c_int), ("cta_pair", ctypes.c_int)]
+                ("tmem_cols", ctypes.c_int), ("cta_pair", ctypes.c_int),
+                ("mma_warps", ctypes.c_int)]
 
     def as_dict(self) -> dict:
         d = {name: getattr(self, name) for name, _ in self._fields_}

@@ -329,11 +329,23 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
         items += f.items;
     }
     const int stage_bytes = CDG_BM * 128 + (pair ? BN / 2 : BN) * 128;
-    const int stages = halo ? a_stages + b_stages : std::min(kMaxStages, ring_budget / stage_bytes);
+    const int max_stages = halo ? a_stages + b_stages : std::min(kMaxStages, ring_budget / stage_bytes);
+    // ---- dual issue: for N tiles of up to 128 channels two MMA warps take
+    // alternate work items, each with half of the stages and two accumulators
+    // of its own.  One warp alone stalls on its per-stage barrier handshake
+    // (measured on GB300: ~350 cycles per 64-channel stage against ~200 of
+    // tensor work); with two, the other warp's MMAs fill that gap.  Tiles of
+    // fewer than four stages gain nothing (the epilogue dominates them).
+    const char *dual_env = std::getenv("CDG_DUAL");  // "0": never
+    bool dual = !halo && !pair && BN <= 128 && max_stages >= 4 && stages_per_tile >= 4.0;
+    if (dual_env && dual_env[0] == '0') dual = false;
+    const int stages = dual ? (max_stages / 2) * 2 : max_stages;
     const int ring_bytes = halo ? a_stages * hrows * 128 + b_stages * BN * 128 : stages * stage_bytes;
-    // two accumulators, each at least as wide as the 64-column chunks the epilogue reads
+    // two accumulators per MMA warp, each at least as wide as the 64-column
+    // chunks the epilogue reads
+    const int n_acc = dual ? 4 : 2;
     int tmem_cols = 32;
-    while (tmem_cols < 2 * (((BN + 63) / 64) * 64)) tmem_cols *= 2;
+    while (tmem_cols < n_acc * (((BN + 63) / 64) * 64)) tmem_cols *= 2;
 
     CdgParams &p = h->prm;
     std::memset(&p, 0, sizeof p);
@@ -372,8 +384,9 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     // previous kernel in the stream ("0" turns it off).
     const char *pdl_env = std::getenv("CDG_PDL");
     p.pdl = (pdl_env && pdl_env[0] == '0') ? 0 : 1;
+    p.dual = dual ? 1 : 0;
     p.tmem_cols = static_cast<uint32_t>(tmem_cols);
-    p.acc_stride = static_cast<uint32_t>(tmem_cols / 2);
+    p.acc_stride = static_cast<uint32_t>(tmem_cols / n_acc);
     for (size_t i = 0; i < phases.size(); ++i) p.phase[i] = phases[i];
     for (size_t i = 0; i < taps.size(); ++i) p.tap[i] = taps[i];
 
@@ -394,6 +407,7 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     inf.smem_bytes = static_cast<int>(h->smem);
     inf.tmem_cols = tmem_cols;
     inf.cta_pair = pair ? 1 : 0;
+    inf.mma_warps = dual ? 2 : 1;
 
     if (!host_only && pair) {
         // pairs must be co-resident on one GPC: size the persistent grid by

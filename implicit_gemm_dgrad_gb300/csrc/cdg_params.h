@@ -22,11 +22,11 @@
 #define CDG_WAIT_LIMIT_NS 4000000000ull  // a pipeline wait gives up after 4 s
 // Shared memory after the operand ring: two 16 KB output staging buffers
 // (128 rows x 128 B, the box a TMA store writes), then mbarriers and flags
-// (256 B), then the phase and tap tables copied out of the parameter block.
+// (320 B), then the phase and tap tables copied out of the parameter block.
 #define CDG_SMEM_STAGING (2 * 128 * 128)
 #define CDG_SMEM_TAIL 2048
-#define CDG_SMEM_TABLES 256
-#define CDG_MAX_STAGES_TOTAL 10  // all ring stages together (their mbarriers live in the 256-byte area)
+#define CDG_SMEM_TABLES 320
+#define CDG_MAX_STAGES_TOTAL 10  // all ring stages together (their mbarriers live in the 320-byte area)
 
 // One phase sub-convolution of a (possibly strided) dgrad.  The dX pixels with
 // h = stride*i + ph, w = stride*j + pw (0 <= i < hph, 0 <= j < wph) form the
@@ -70,6 +70,7 @@ struct CdgParams {  // CUtensorMap members carry their own (128-byte) alignment
     int halo;             // 1: one dY halo box per (tile, K block) serves every tap (see dgrad_sm103.cu)
     int pair;             // 1: CTA pairs (clusters of 2) share 256-row tiles through 2-SM MMAs
     int pdl;              // 1: launch with programmatic stream serialization (host side only)
+    int dual;             // 1: two MMA warps, each with half of the stages and two accumulators
     int halo_wb;          // halo box width = row pitch of the halo tile rows (tile width + tap span)
     int halo_wt, halo_bh; // output tile: halo_wt columns x halo_bh rows of one image
     int halo_hb;          // halo box height (halo_bh + tap span)

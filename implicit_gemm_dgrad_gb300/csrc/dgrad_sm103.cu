@@ -115,6 +115,7 @@ __device__ __forceinline__ void box_origin(const CdgPhase &ph, int mt, int bw, i
 }
 
 struct Ring {
+    int stages;            // stages of this ring (dual issue: each MMA warp has a ring of its own)
     uint32_t a0;           // shared address of stage 0's A tile (1024-aligned)
     uint32_t stage_bytes;  // A tile + B tile (halo mode: one halo box stage)
     uint32_t b0;           // halo mode: first weight stage
@@ -125,13 +126,13 @@ struct Ring {
 };
 
 // ------------------------------------------------------------------ loaders
-// CDG_LOADERS warps walk the same (item, tap, k-block) sequence; the loader
+// nloaders warps walk the same (item, tap, k-block) sequence; the loader
 // with index li issues the stages whose global counter is li modulo
-// CDG_LOADERS.  The whole warp runs the loop; one elected lane issues.  The parity of
+// nloaders.  The whole warp runs the loop; one elected lane issues.  The parity of
 // each slot's latest load is recorded in shared memory for the abort drain.
 template <bool PAIR>
 __device__ __forceinline__ void run_loader(const CdgParams &p, const Ring &R, const CdgPhase *tab,
-                                           const CdgTap *taps, Ctl ctl, int li, bool leader,
+                                           const CdgTap *taps, Ctl ctl, int li, int nloaders, bool leader,
                                            volatile uint32_t *slot_parity, Sched S)
 {
     const uint64_t mapA = reinterpret_cast<uint64_t>(&p.tmA);
@@ -140,7 +141,7 @@ __device__ __forceinline__ void run_loader(const CdgParams &p, const Ring &R, co
         asm volatile("prefetch.tensormap [%0];" ::"l"(mapA) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(mapB) : "memory");
     }
-    const int KB = p.KB, stages = p.stages, tiles_n = p.tiles_n, BN = p.BN, m_step = p.m_step;
+    const int KB = p.KB, stages = R.stages, tiles_n = p.tiles_n, BN = p.BN, m_step = p.m_step;
     const int bw = p.box_w, bh = p.box_h, bn = p.box_n;
     const bool flat = p.a_flat != 0;
     const uint32_t tx = p.tx_bytes;
@@ -197,7 +198,7 @@ __device__ __forceinline__ void run_loader(const CdgParams &p, const Ring &R, co
                     }
                     __syncwarp();
                 }
-                if (++owner == CDG_LOADERS) owner = 0;
+                if (++owner == nloaders) owner = 0;
                 if (++stage == stages) {
                     stage = 0;
                     parity ^= 1u;
@@ -381,7 +382,7 @@ template <bool PAIR>
 __device__ __forceinline__ void run_mma(const CdgParams &p, const Ring &R, const CdgPhase *tab, Ctl ctl,
                                         uint32_t tmem_base, bool leader, Sched S)
 {
-    const int KB = p.KB, stages = p.stages;
+    const int KB = p.KB, stages = R.stages;
     const uint32_t idesc = p.idesc, acc_stride = p.acc_stride;
     const uint64_t adesc0 = sdesc_k128_sw128(R.a0);
     const uint64_t bdesc0 = sdesc_k128_sw128(R.a0 + CDG_BM * 128);
@@ -508,7 +509,7 @@ __device__ __forceinline__ long long phase_pixel(const CdgPhase &ph, int n, int 
     return (static_cast<long long>(n) * H + (stride * i + ph.ph)) * W + (stride * j + ph.pw);
 }
 
-template <int OUT_T, bool MASK, int IN_T, bool HALO, bool PAIR>
+template <int OUT_T, bool MASK, int IN_T, bool HALO, bool PAIR, bool DUAL>
 __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, const CdgPhase *tab, Ctl ctl,
                                              uint32_t tmem_base, Sched S)
 {
@@ -547,8 +548,11 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
 
     // TMA stores are spread over the four warps' elected lanes (an issue holds its
     // thread for a few hundred cycles): chunk k is stored by epilogue warp k % 4.
-    uint32_t acc_count = 0, chunk_count = 0;
-    for (ItemWalk w(tab, p.nphases, S.start, S.step); w.valid(); w.next()) {
+    // accumulators filled so far by each MMA warp (dual issue: items alternate
+    // between two MMA warps, each with two accumulators of its own)
+    uint32_t acc_count[2] = {0u, 0u}, chunk_count = 0;
+    uint32_t item_index = 0;
+    for (ItemWalk w(tab, p.nphases, S.start, S.step); w.valid(); w.next(), ++item_index) {
         const CdgPhase &ph = tab[w.phase];
         const int mt = S.m_tile(w.local, tiles_n);
         const int nt = w.local - (tiles_n == 1 ? w.local : w.local / tiles_n) * tiles_n;
@@ -602,8 +606,10 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
             }
         }
 
-        const uint32_t acc = acc_count & 1u;
-        const uint32_t acc_parity = (acc_count >> 1) & 1u;
+        const uint32_t issuer = DUAL ? (item_index & 1u) : 0u;
+        const uint32_t n_acc = acc_count[issuer]++;
+        const uint32_t acc = 2u * issuer + (n_acc & 1u);  // accumulator slot
+        const uint32_t acc_parity = (n_acc >> 1) & 1u;
         if (!wait_bar(R.acc_full0 + 8u * acc, acc_parity, ctl)) break;
         tc_fence_after();
         const uint32_t taddr = tmem_base + acc * acc_stride + (static_cast<uint32_t>(quad * 32) << 16);
@@ -663,7 +669,6 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
                 bulk_commit_group();
             }
         }
-        ++acc_count;
     }
     if (elected) bulk_wait_group_all();
 }
@@ -679,30 +684,33 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_cons
 {
     constexpr bool HALO = MODE == 1;
     constexpr bool PAIR = MODE == 2;
+    constexpr bool DUAL = MODE == 3;  // two MMA warps, each with its own ring and accumulators
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     // shared memory: operand ring(s) | 2 x 16 KB output staging | mbarriers, flags | phase and tap tables
     const int stages = HALO ? p.a_stages + p.b_stages : p.stages;  // mbarrier pairs
     Ring R;
+    R.stages = stages;
     R.a0 = base;
     R.stage_bytes = p.a_stage_bytes;
     R.b0 = base + p.a_stages * R.stage_bytes;
     R.b_bytes = p.BN * 128;
     R.out0 = HALO ? R.b0 + p.b_stages * R.b_bytes : base + stages * R.stage_bytes;
     const uint32_t bars = R.out0 + CDG_SMEM_STAGING;
+    // mbarriers: full[stages], empty[stages], acc_full[4], acc_empty[4], drain[2]
     R.full0 = bars;
     R.empty0 = bars + 8u * stages;
     R.acc_full0 = bars + 16u * stages;
-    R.acc_empty0 = bars + 16u * stages + 16u;
-    R.drain = bars + 16u * stages + 32u;
+    R.acc_empty0 = bars + 16u * stages + 32u;
+    R.drain = bars + 16u * stages + 64u;
     uint8_t *const tail = smem_raw + (bars - raw);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tail + 8 * (2 * stages + 5));
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tail + 8 * (2 * stages + 10));
     volatile uint32_t *abort_flag = tmem_slot + 1;
     volatile uint32_t *slot_parity = tmem_slot + 2;  // [stages] (<= CDG_MAX_STAGES_TOTAL entries)
     CdgPhase *tab = reinterpret_cast<CdgPhase *>(tail + CDG_SMEM_TABLES);
     CdgTap *taps = reinterpret_cast<CdgTap *>(tab + CDG_MAX_PHASES);
-    static_assert(8 * (2 * CDG_MAX_STAGES_TOTAL + 5) + 8 + 4 * CDG_MAX_STAGES_TOTAL <= CDG_SMEM_TABLES,
+    static_assert(8 * (2 * CDG_MAX_STAGES_TOTAL + 10) + 8 + 4 * CDG_MAX_STAGES_TOTAL <= CDG_SMEM_TABLES,
                   "mbarrier area overflows");
     static_assert(CDG_SMEM_TABLES + CDG_MAX_PHASES * sizeof(CdgPhase) + CDG_MAX_TAPS * sizeof(CdgTap) <=
                       CDG_SMEM_TAIL,
@@ -733,12 +741,13 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_cons
             mbar_init(R.full0 + 8u * s, 1);
             mbar_init(R.empty0 + 8u * s, 1);
         }
-        for (int a = 0; a < 2; ++a) {
+        for (int a = 0; a < 4; ++a) {
             mbar_init(R.acc_full0 + 8u * a, 1);
             // one arrival per epilogue warp (in a pair, the leader's counts both CTAs' warps)
             mbar_init(R.acc_empty0 + 8u * a, PAIR && S.rank == 0 ? 8 : 4);
         }
         mbar_init(R.drain, 1);
+        mbar_init(R.drain + 8u, 1);
         *abort_flag = 0u;
         for (int s = 0; s < stages; ++s) slot_parity[s] = 0u;
         fence_mbar_init();
@@ -764,7 +773,38 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_cons
     const uint32_t tmem_base = *tmem_slot;
     const Ctl ctl{abort_flag, p.status};
 
-    if (warp == 1) {
+    // dual issue: MMA warp j (warp 1 + 2j) and loader warp j (warp 2j) serve the
+    // items at odd/even positions of this CTA's walk, through ring j (half of
+    // the stages) and accumulator slots 2j, 2j + 1
+    auto ring_of = [&](int j) {
+        Ring Rj = R;
+        Rj.stages = stages / 2;
+        Rj.a0 = R.a0 + static_cast<uint32_t>(j * Rj.stages) * R.stage_bytes;
+        Rj.full0 = R.full0 + 8u * static_cast<uint32_t>(j * Rj.stages);
+        Rj.empty0 = R.empty0 + 8u * static_cast<uint32_t>(j * Rj.stages);
+        Rj.acc_full0 = R.acc_full0 + 16u * j;
+        Rj.acc_empty0 = R.acc_empty0 + 16u * j;
+        Rj.drain = R.drain + 8u * j;
+        return Rj;
+    };
+    auto sched_of = [&](int j) {
+        Sched Sj = S;
+        Sj.start = S.start + j * S.step;
+        Sj.step = 2 * S.step;
+        return Sj;
+    };
+    if (DUAL) {
+        if (warp == 1 || warp == 3) {
+            const int j = warp >> 1;
+            run_mma<false>(p, ring_of(j), tab, ctl, tmem_base + 2u * j * p.acc_stride, elect_one_sync(), sched_of(j));
+        } else if (warp >= CDG_EPI_WARP0) {
+            run_epilogue<OUT_T, MASK, IN_T, false, false, true>(p, R, tab, ctl, tmem_base, S);
+        } else {
+            const int j = warp >> 1;  // warps 0 and 2
+            run_loader<false>(p, ring_of(j), tab, taps, ctl, 0, 1, elect_one_sync(),
+                              slot_parity + j * (stages / 2), sched_of(j));
+        }
+    } else if (warp == 1) {
         if (HALO) {
             run_mma_halo(p, R, tab, taps, ctl, tmem_base, elect_one_sync(), S);
         } else if (!PAIR || S.rank == 0) {
@@ -776,11 +816,12 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_cons
             wait_bar(R.drain, 0, Ctl{&no_abort, p.status});
         }
     } else if (warp >= CDG_EPI_WARP0) {
-        run_epilogue<OUT_T, MASK, IN_T, HALO, PAIR>(p, R, tab, ctl, tmem_base, S);
+        run_epilogue<OUT_T, MASK, IN_T, HALO, PAIR, false>(p, R, tab, ctl, tmem_base, S);
     } else if (HALO) {
         run_loader_halo(p, R, tab, taps, ctl, warp == 0 ? 0 : warp - 1, elect_one_sync(), slot_parity, S);
     } else {
-        run_loader<PAIR>(p, R, tab, taps, ctl, warp == 0 ? 0 : warp - 1, elect_one_sync(), slot_parity, S);
+        run_loader<PAIR>(p, R, tab, taps, ctl, warp == 0 ? 0 : warp - 1, CDG_LOADERS, elect_one_sync(), slot_parity,
+                         S);
     }
 
     __syncthreads();
@@ -839,6 +880,7 @@ DgradFn pick(int mode)
 {
     if (mode == 1) return cdg::dgrad_kernel<OUT_T, MASK, IN_T, 1>;
     if (mode == 2) return cdg::dgrad_kernel<OUT_T, MASK, IN_T, 2>;
+    if (mode == 3) return cdg::dgrad_kernel<OUT_T, MASK, IN_T, 3>;
     return cdg::dgrad_kernel<OUT_T, MASK, IN_T, 0>;
 }
 
@@ -854,7 +896,7 @@ DgradFn select_kernel(int out_type, int in_type, bool mask, int mode)
     return mask ? pick<CDG_T_BF16, true, CDG_T_BF16>(mode) : pick<CDG_T_BF16, false, CDG_T_BF16>(mode);
 }
 
-int kernel_mode(const CdgParams &p) { return p.halo ? 1 : (p.pair ? 2 : 0); }
+int kernel_mode(const CdgParams &p) { return p.halo ? 1 : (p.pair ? 2 : (p.dual ? 3 : 0)); }
 
 }  // namespace
 
@@ -865,7 +907,7 @@ int kernel_mode(const CdgParams &p) { return p.halo ? 1 : (p.pair ? 2 : 0); }
 cudaError_t cdg_prepare_dgrad(int out_type, int in_type, bool mask, size_t smem)
 {
     if (smem > static_cast<size_t>(CDG_MAX_DYN_SMEM)) return cudaErrorInvalidValue;
-    for (int mode = 0; mode < 3; ++mode) {
+    for (int mode = 0; mode < 4; ++mode) {
         DgradFn fn = select_kernel(out_type, in_type, mask, mode);
         const cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void *>(fn),
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize, CDG_MAX_DYN_SMEM);

@@ -126,6 +126,8 @@ typedef struct {
     int smem_bytes;       /* dynamic shared memory per CTA                         */
     int tmem_cols;        /* tensor-memory columns per CTA                         */
     int cta_pair;         /* 1: CTA pairs share 256-row tiles (2-SM MMA)            */
+    int mma_warps;        /* MMA-issuing warps per CTA: 2 splits the work items and */
+                          /* the pipeline stages between two issuers (N tile <= 128) */
 } cdg_plan_info_t;
 
 int cdg_plan_get_info(cdg_handle_t h, cdg_plan_info_t *info);
