@@ -233,19 +233,23 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     const int tiles_n = ceil_div(C, BN);
     const int ring_budget = kMaxSmem - 1024 - CDG_SMEM_STAGING - CDG_SMEM_TAIL;
 
-    // ---- halo operand mode (opt-in: CDG_HALO=1): a tile is halo_bh full-width
-    // rows of one image's phase sub-grid; one TMA box of (width + tap span) x
-    // (rows + tap span) positions of dY serves every tap of the phase, each
-    // tap's operand starting hoff rows into it.  Tile row a*halo_wb + b is
-    // output (a, b); rows with b >= halo_wt are padding.  It cuts the operand
-    // bytes written to shared memory, but on GB300 it measured slower than
-    // per-tap boxes on every ResNet-50 3x3 layer (the taps' operands start at
-    // rows that are not 1024-byte aligned), so the planner does not pick it
-    // unless asked; when asked it is used wherever the geometry allows.
-    bool halo = false;
-    int hwb = 0, hwt = 0, hbh = 0, hhb = 0, hrows = 0, a_stages = 0, b_stages = 0;
+    // ---- halo operand mode: a tile is halo_bh full-width rows of one image's
+    // phase sub-grid; one TMA box of (width + tap span) x (rows + tap span)
+    // positions of dY serves every tap of the phase, each tap's operand
+    // starting hoff rows into it.  Tile row a*halo_wb + b is output (a, b);
+    // rows with b >= halo_wt are padding.  With the weights resident (the
+    // whole filter of a single N tile fits beside the halo stages) a tile
+    // costs one pipeline handshake for all its taps, which measured faster
+    // than per-tap boxes on GB300 (ResNet-50 3x3 64->64: 76 vs 84 us), so the
+    // planner picks it by default.  With streamed weights it measured slower
+    // (one weight handshake per tap, as in per-tap mode, on top of the halo
+    // stage), so that form is used only when asked (CDG_HALO=1), wherever the
+    // geometry allows; CDG_HALO=0 turns halo mode off.
+    bool halo = false, b_res = false;
+    int hwb = 0, hwt = 0, hbh = 0, hhb = 0, hrows = 0, a_stages = 0, b_stages = 0, b_res_bytes = 0;
     const char *halo_env = std::getenv("CDG_HALO");
-    if (!flat && halo_env && halo_env[0] == '1') {
+    const bool halo_forced = halo_env && halo_env[0] == '1';
+    if (!flat && !(halo_env && halo_env[0] == '0')) {
         int span_r = 0, span_s = 0, wt = 0, hmax = 0, maxtaps = 0;
         for (const CdgPhase &f : phases) {
             if (f.tap_count == 0) continue;
@@ -267,9 +271,19 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
             const int off_max = span_r * wb + span_s;
             const int rows = ((std::max(wb * hb, off_max + CDG_BM) + 7) / 8) * 8;
             const int a_bytes = rows * 128, b_bytes = BN * 128;
-            const int as = (3 * a_bytes + 4 * b_bytes <= ring_budget) ? 3 : 2;
-            const int bs = std::min(std::min(kMaxStages, CDG_MAX_STAGES_TOTAL - as), (ring_budget - as * a_bytes) / b_bytes);
-            if (hb <= 256 && bs >= 2) {
+            int as = (3 * a_bytes + 4 * b_bytes <= ring_budget) ? 3 : 2;
+            int bs = std::min(std::min(kMaxStages, CDG_MAX_STAGES_TOTAL - as), (ring_budget - as * a_bytes) / b_bytes);
+            // the whole packed filter of a single N tile fits next to at least
+            // two halo stages: load it once per CTA and keep it resident, so a
+            // tile needs one pipeline handshake (its halo box) for all taps
+            const long long res_bytes = 1LL * static_cast<long long>(taps.size()) * ceil_div(K, CDG_BK) * BN * 128;
+            if (tiles_n == 1 && res_bytes + 2LL * a_bytes <= ring_budget) {
+                b_res = true;
+                b_res_bytes = static_cast<int>(res_bytes);
+                as = std::min<int>(CDG_MAX_STAGES_TOTAL - 1, (ring_budget - b_res_bytes) / a_bytes);
+                bs = 1;  // one barrier: the resident weights have landed
+            }
+            if (hb <= 256 && bs >= (b_res ? 1 : 2) && (b_res || halo_forced)) {
                 halo = true;
                 hwb = wb;
                 hwt = wt;
@@ -287,6 +301,8 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
             }
         }
     }
+
+    if (!halo) b_res = false;
 
     // ---- CTA pairs: two CTAs (a cluster) share each 256-row tile through the
     // 2-SM MMA, each holding its 128 rows of dY and half of the weight tile.
@@ -340,7 +356,8 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     bool dual = !halo && !pair && BN <= 128 && max_stages >= 4 && stages_per_tile >= 4.0;
     if (dual_env && dual_env[0] == '0') dual = false;
     const int stages = dual ? (max_stages / 2) * 2 : max_stages;
-    const int ring_bytes = halo ? a_stages * hrows * 128 + b_stages * BN * 128 : stages * stage_bytes;
+    const int ring_bytes = halo ? a_stages * hrows * 128 + (b_res ? b_res_bytes : b_stages * BN * 128)
+                                : stages * stage_bytes;
     // two accumulators per MMA warp, each at least as wide as the 64-column
     // chunks the epilogue reads
     const int n_acc = dual ? 4 : 2;
@@ -370,6 +387,8 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     p.b_stages = b_stages;
     p.a_stage_bytes = static_cast<uint32_t>(halo ? hrows * 128 : stage_bytes);
     p.halo_hb = hhb;
+    p.b_res = b_res ? 1 : 0;
+    p.b_res_bytes = static_cast<uint32_t>(b_res_bytes);
     p.tx_a = static_cast<uint32_t>(hwb * hhb * 128);
     p.tx_b = static_cast<uint32_t>(BN * 128);
     const uint32_t ab = dtype == CDG_BF16 ? 1u : 0u;
@@ -399,7 +418,7 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     inf.num_phases = stride * stride;
     for (int i = 0; i < stride * stride; ++i) inf.phase_taps[i] = phase_taps_by_index[i];
     inf.tile_m = CDG_BM; inf.tile_n = BN; inf.tile_k = CDG_BK;
-    inf.a_mode = halo ? 2 : (flat ? 1 : 0);
+    inf.a_mode = halo ? (b_res ? 3 : 2) : (flat ? 1 : 0);
     inf.box_w = bw; inf.box_h = bh; inf.box_n = bnb;
     inf.stages = stages;
     inf.work_items = items;

@@ -241,6 +241,20 @@ __device__ __forceinline__ void run_loader_halo(const CdgParams &p, const Ring &
     int a_stage = 0, b_stage = 0, owner = 1;
     uint32_t a_par = 0, b_par = 0;
     bool ok = true;
+    if (p.b_res && li == 1) {
+        // every (tap, K block) weight tile of the single N tile, in the order of
+        // the tap table (phase by phase), completing on the one weight barrier
+        const uint32_t full = R.full0 + 8u * as;
+        if (leader) {
+            slot_parity[as] = 2u;
+            mbar_arrive_expect_tx(full, p.b_res_bytes);
+            for (int q = 0; q < p.ntaps; ++q)
+                for (int kb = 0; kb < KB; ++kb)
+                    tma_load_3d(R.b0 + static_cast<uint32_t>(q * KB + kb) * R.b_bytes, mapB, full, kb * CDG_BK, 0,
+                                taps[q].t);
+        }
+        __syncwarp();
+    }
     for (ItemWalk w(tab, p.nphases, S.start, S.step); ok && w.valid(); w.next()) {
         const CdgPhase &ph = tab[w.phase];
         const int ntap = ph.tap_count;
@@ -268,6 +282,8 @@ __device__ __forceinline__ void run_loader_halo(const CdgParams &p, const Ring &
                     a_stage = 0;
                     a_par ^= 1u;
                 }
+            } else if (p.b_res) {
+                // resident weights: loaded once, before the first tile, below
             } else {
                 for (int tt = 0; tt < ntap; ++tt) {
                     if (owner == li) {
@@ -310,6 +326,8 @@ __device__ __forceinline__ void run_mma_halo(const CdgParams &p, const Ring &R, 
     uint32_t a_par = 0, b_par = 0, acc_count = 0;
     bool ok = true;
     bool b_ready = false;  // full barrier of the current weight stage already seen complete
+    const bool res = p.b_res != 0;
+    if (res && !wait_bar(R.full0 + 8u * as, 0, ctl)) ok = false;  // resident weights landed
     for (ItemWalk w(tab, p.nphases, S.start, S.step); ok && w.valid(); w.next()) {
         const CdgPhase &ph = tab[w.phase];
         const int ntap = ph.tap_count;
@@ -328,32 +346,52 @@ __device__ __forceinline__ void run_mma_halo(const CdgParams &p, const Ring &R, 
             const uint64_t abase = adesc0 + static_cast<uint64_t>(a_stage * astep);
             const CdgTap *ptap = taps + ph.tap_begin;
             int hoff = ptap[0].hoff;  // loaded a stage ahead: its latency overlaps MMA issue
-            for (int tt = 0; tt < ntap; ++tt) {
-                const int slot = as + b_stage;
-                if (!b_ready && !wait_bar(R.full0 + 8u * slot, b_par, ctl)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                {  // test the next weight stage while this tap's MMAs issue
-                    const int nb = b_stage + 1 == bs ? 0 : b_stage + 1;
-                    b_ready = mbar_test_wait(R.full0 + 8u * (as + nb), nb == 0 ? b_par ^ 1u : b_par);
-                }
-                const int hnext = tt + 1 < ntap ? ptap[tt + 1].hoff : 0;
-                if (leader) {
-                    // 128-byte rows: a row offset of hoff is 8*hoff descriptor units
-                    const uint64_t adesc = abase + 8u * static_cast<uint32_t>(hoff);
-                    const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(b_stage * bstep);
+            if (res) {
+                // all taps of this K block back to back: one handshake per halo box
+                const uint32_t bunit = R.b_bytes >> 4;  // descriptor units per weight tile
+                const int tbase = ph.tap_begin * KB + kb;
+                for (int tt = 0; tt < ntap; ++tt) {
+                    if (leader) {
+                        const uint64_t adesc = abase + 8u * static_cast<uint32_t>(hoff);
+                        const uint64_t bdesc =
+                            bdesc0 + static_cast<uint64_t>(static_cast<uint32_t>(tbase + tt * KB) * bunit);
 #pragma unroll
-                    for (int k = 0; k < CDG_BK / 16; ++k)
-                        umma_f16(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, (kb | tt | k) != 0);
-                    umma_commit(R.empty0 + 8u * slot);
+                        for (int k = 0; k < CDG_BK / 16; ++k)
+                            umma_f16(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, (kb | tt | k) != 0);
+                    }
+                    __syncwarp();
+                    // the next tap's row offset is read only once this tap's MMAs
+                    // are queued: an outstanding shared-memory load delays MMA issue
+                    if (tt + 1 < ntap) hoff = ptap[tt + 1].hoff;
                 }
-                __syncwarp();
-                hoff = hnext;
-                if (++b_stage == bs) {
-                    b_stage = 0;
-                    b_par ^= 1u;
+            } else {
+                for (int tt = 0; tt < ntap; ++tt) {
+                    const int slot = as + b_stage;
+                    if (!b_ready && !wait_bar(R.full0 + 8u * slot, b_par, ctl)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    {  // test the next weight stage while this tap's MMAs issue
+                        const int nb = b_stage + 1 == bs ? 0 : b_stage + 1;
+                        b_ready = mbar_test_wait(R.full0 + 8u * (as + nb), nb == 0 ? b_par ^ 1u : b_par);
+                    }
+                    const int hnext = tt + 1 < ntap ? ptap[tt + 1].hoff : 0;
+                    if (leader) {
+                        // 128-byte rows: a row offset of hoff is 8*hoff descriptor units
+                        const uint64_t adesc = abase + 8u * static_cast<uint32_t>(hoff);
+                        const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(b_stage * bstep);
+#pragma unroll
+                        for (int k = 0; k < CDG_BK / 16; ++k)
+                            umma_f16(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, (kb | tt | k) != 0);
+                        umma_commit(R.empty0 + 8u * slot);
+                    }
+                    __syncwarp();
+                    hoff = hnext;
+                    if (++b_stage == bs) {
+                        b_stage = 0;
+                        b_par ^= 1u;
+                    }
                 }
             }
             if (!ok) break;
@@ -696,7 +734,7 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_cons
     R.stage_bytes = p.a_stage_bytes;
     R.b0 = base + p.a_stages * R.stage_bytes;
     R.b_bytes = p.BN * 128;
-    R.out0 = HALO ? R.b0 + p.b_stages * R.b_bytes : base + stages * R.stage_bytes;
+    R.out0 = HALO ? R.b0 + (p.b_res ? p.b_res_bytes : p.b_stages * R.b_bytes) : base + stages * R.stage_bytes;
     const uint32_t bars = R.out0 + CDG_SMEM_STAGING;
     // mbarriers: full[stages], empty[stages], acc_full[4], acc_empty[4], drain[2]
     R.full0 = bars;

@@ -140,3 +140,21 @@ def test_workload_plans():
         else:
             assert info["box_w"] * info["box_h"] * info["box_n"] <= 128
         assert p.packed_weight_bytes == 2 * L.K * L.R * L.S * L.C
+        if info["mma_warps"] == 2:  # dual issue: two rings, two accumulators per MMA warp
+            assert info["stages"] % 2 == 0 and info["stages"] >= 4
+            assert info["tmem_cols"] >= 4 * info["tile_n"] and info["cta_pair"] == 0
+
+
+def test_halo_resident_weights_when_the_filter_fits(monkeypatch):
+    """A filter whose packed weights for the one N tile fit beside two halo
+    stages is kept resident with halo operand boxes (a_mode 3, the default);
+    a larger one uses per-tap boxes by default (a_mode 0) and streamed halo
+    weights only when asked (a_mode 2); CDG_HALO=0 turns halo mode off."""
+    monkeypatch.delenv("CDG_HALO", raising=False)
+    small = cdg.plan_host(256, 56, 56, 64, 64, 3, 3, 1, 1, 1, "bf16", num_sms=148).info()
+    assert small["a_mode"] == 3 and small["smem_bytes"] <= 232448
+    assert cdg.plan_host(256, 28, 28, 128, 128, 3, 3, 1, 1, 1, "bf16", num_sms=148).info()["a_mode"] == 0
+    monkeypatch.setenv("CDG_HALO", "1")
+    assert cdg.plan_host(256, 28, 28, 128, 128, 3, 3, 1, 1, 1, "bf16", num_sms=148).info()["a_mode"] == 2
+    monkeypatch.setenv("CDG_HALO", "0")
+    assert cdg.plan_host(256, 56, 56, 64, 64, 3, 3, 1, 1, 1, "bf16", num_sms=148).info()["a_mode"] == 0

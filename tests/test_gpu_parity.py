@@ -165,11 +165,12 @@ def test_interleaved_plans():
 @pytest.mark.parametrize("L", [SWEEP[0], SWEEP[1], SWEEP[4], SWEEP[5], SWEEP[12], SWEEP[14], BATCH8[0]],
                          ids=lambda L: L.name)
 def test_halo_operand_mode(L, monkeypatch):
-    """The opt-in halo operand mode (one dY box per tile and K block serves
-    every tap) gives the same results."""
+    """The halo operand mode (one dY box per tile and K block serves every
+    tap; weights streamed per tap, or resident when the whole filter of a
+    single N tile fits) gives the same results."""
     monkeypatch.setenv("CDG_HALO", "1")
     run, _, _ = check_layer(L)
-    assert run.plan.info()["a_mode"] == 2
+    assert run.plan.info()["a_mode"] in (2, 3)
 
 
 def test_chained_launches_keep_stream_order():
