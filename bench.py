@@ -66,16 +66,18 @@ def kernel_sources_sha256() -> str:
 
 
 def profiled_traffic(layer_name: str):
-    """DRAM bytes (read + write) of one launch from the committed ncu capture,
-    or None when that capture is of another layer or of other kernel sources."""
+    """DRAM bytes (read + write) of one launch of `layer_name` from the
+    committed ncu capture, or None when the capture has no such layer or was
+    taken of other kernel sources."""
     path = os.path.join(ROOT, "profiles", "dgrad_kernel_traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
-    if d.get("layer") != layer_name or d.get("sources_sha256") != kernel_sources_sha256():
+    rec = d.get("layers", {}).get(layer_name)
+    if rec is None or d.get("sources_sha256") != kernel_sources_sha256():
         return None
-    return int(d["dram_read_bytes"]) + int(d["dram_write_bytes"])
+    return int(rec["dram_read_bytes"]) + int(rec["dram_write_bytes"])
 
 
 def roofline_time_s(layer, peaks):

@@ -118,7 +118,10 @@ typedef struct {
     int tile_n;           /* channels per tile (GEMM N tile)                       */
     int tile_k;           /* dY channels per pipeline stage (GEMM K block)         */
     int a_mode;           /* 0: 4-D boxes over dY per tap, 1: dY rows as a matrix, */
-                          /* 2: one halo box per K block for all taps (opt-in)     */
+                          /* 2: one halo box per K block for all taps, weights     */
+                          /*    streamed per tap (opt-in),                         */
+                          /* 3: halo boxes with every weight tile resident in      */
+                          /*    shared memory (chosen when the filter fits)        */
     int box_w, box_h, box_n; /* output tile box (a_mode 0 and 2)                   */
     int stages;           /* shared-memory pipeline depth                          */
     int work_items;       /* (phase, m-tile, n-tile) items in one launch           */
