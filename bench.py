@@ -201,7 +201,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=3)
-    ap.add_argument("--cpu-images", type=int, default=48)
+    ap.add_argument("--cpu-images", type=int, default=256,
+                    help="images per layer in the CPU-oracle baseline (256 = the whole batch, ~13 s on 16 cores)")
     ap.add_argument("--ref-images", type=int, default=8, help="images per layer per reference-arm step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", default="", help="comma-separated layer names (default: all 22)")
@@ -356,22 +357,47 @@ def main():
     h2d = sum(t.numel() * 2 for t in h_dY)
     d2h = sum(t.numel() * 2 for t in h_dX)
 
+    # uploads, kernels and read-backs run on three streams: layer i's upload
+    # overlaps layer i-1's kernel and layer i-2's read-back.  Events keep each
+    # layer's order (upload -> kernel -> read-back) and, across steps, keep an
+    # upload from overwriting a dY the previous step's kernel still reads and a
+    # kernel from overwriting a dX not yet read back.
+    s_in = torch.cuda.Stream(device=dev)
+    s_out = torch.cuda.Stream(device=dev)
+    ev_in = [torch.cuda.Event() for _ in state]
+    ev_done = [torch.cuda.Event() for _ in state]
+    ev_out = [torch.cuda.Event() for _ in state]
+
     def e2e_step():
         for i, (_, p, d_dY, d_Wp, d_dX) in enumerate(state):
-            d_dY.copy_(h_dY[i], non_blocking=True)
+            s_in.wait_event(ev_done[i])  # no-op before the event's first record
+            with torch.cuda.stream(s_in):
+                d_dY.copy_(h_dY[i], non_blocking=True)
+            ev_in[i].record(s_in)
+            stream.wait_event(ev_in[i])
+            stream.wait_event(ev_out[i])
             p.dgrad(d_dY, d_Wp, d_dX, None, stream)
-            h_dX[i].copy_(d_dX, non_blocking=True)
+            ev_done[i].record(stream)
+            s_out.wait_event(ev_done[i])
+            with torch.cuda.stream(s_out):
+                h_dX[i].copy_(d_dX, non_blocking=True)
+            ev_out[i].record(s_out)
 
-    with torch.cuda.stream(stream):
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    s_in.wait_event(e0)
+    s_out.wait_event(e0)
+    for _ in range(args.e2e_steps):
         e2e_step()
-        torch.cuda.synchronize()
-        barrier()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.e2e_steps):
-            e2e_step()
-        e1.record(stream)
-        torch.cuda.synchronize()
+    stream.wait_event(ev_out[-1])  # the last read-back (s_out runs in order)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    for i, (L, p, d_dY, d_Wp, d_dX) in enumerate(state):  # the read-backs hold the kernels' results
+        if not torch.equal(h_dX[i][::4099], d_dX[::4099].cpu()):
+            raise RuntimeError(f"end-to-end read-back of {L.name} differs from the device result")
     barrier()
     e2e_ms = e0.elapsed_time(e1)
     if world > 1:
@@ -402,7 +428,8 @@ def main():
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": args.e2e_steps},
+                "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
+                "copies": "pinned host buffers; uploads, kernels and read-backs on three streams"},
         "gpu_launches": nL * args.steps,
         "clocks": clocks.summary(),
         "host_wall_s_timed": round(t_host1 - t_host0, 4),
