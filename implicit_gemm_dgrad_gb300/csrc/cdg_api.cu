@@ -404,6 +404,19 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     const char *pdl_env = std::getenv("CDG_PDL");
     p.pdl = (pdl_env && pdl_env[0] == '0') ? 0 : 1;
     p.dual = dual ? 1 : 0;
+    // phases with taps (sorted first) of equal item counts are interleaved item
+    // by item, so that their tiles over the same dY run close together (a
+    // strided 3x3 layer's four phases otherwise read dY from DRAM once each)
+    {
+        int ntp = 0;
+        while (ntp < static_cast<int>(phases.size()) && phases[ntp].tap_count > 0) ++ntp;
+        bool equal = ntp >= 2;
+        for (int i = 1; i < ntp; ++i) equal = equal && phases[i].items == phases[0].items;
+        const char *il_env = std::getenv("CDG_INTERLEAVE");  // "0": off
+        if (il_env && il_env[0] == '0') equal = false;
+        p.interleave = equal ? ntp : 0;
+        p.il_items = equal ? phases[0].items : 0;
+    }  // p.il_round is set once the grid is final (below)
     p.tmem_cols = static_cast<uint32_t>(tmem_cols);
     p.acc_stride = static_cast<uint32_t>(tmem_cols / n_acc);
     for (size_t i = 0; i < phases.size(); ++i) p.phase[i] = phases[i];
@@ -411,6 +424,18 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
 
     h->smem = static_cast<size_t>(1024 + ring_bytes + CDG_SMEM_STAGING + CDG_SMEM_TAIL);
     h->grid = pair ? 2 * std::max(1, std::min(num_sms / 2, items)) : std::max(1, std::min(num_sms, items));
+
+    auto set_round = [&]() {
+        // interleaving needs every round of G items to hold whole groups of
+        // `interleave` items (G = CTAs, or CTA pairs)
+        const int G = pair ? h->grid / 2 : h->grid;
+        if (p.interleave > 0 && (G % p.interleave != 0 || 1LL * p.interleave * p.il_items < G)) {
+            p.interleave = 0;
+            p.il_items = 0;
+        }
+        p.il_round = G;
+    };
+    set_round();
 
     cdg_plan_info_t &inf = h->info;
     std::memset(&inf, 0, sizeof inf);
@@ -438,6 +463,7 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
         const int pairs = cdg_max_active_pairs(h->out_type, h->in_type, h->mask, h->smem);
         if (pairs >= 1) h->grid = 2 * std::max(1, std::min(pairs, items));
         inf.grid = h->grid;
+        set_round();
     }
     if (!host_only) {
         if (cudaGetDevice(&h->device) != cudaSuccess ||

@@ -71,6 +71,9 @@ struct CdgParams {  // CUtensorMap members carry their own (128-byte) alignment
     int pair;             // 1: CTA pairs (clusters of 2) share 256-row tiles through 2-SM MMAs
     int pdl;              // 1: launch with programmatic stream serialization (host side only)
     int dual;             // 1: two MMA warps, each with half of the stages and two accumulators
+    int interleave;       // >= 2: the first `interleave` phases' items are interleaved (il_items each)
+    int il_items;
+    int il_round;         // items per scheduling round (CTAs, or CTA pairs), a multiple of interleave
     int halo_wb;          // halo box width = row pitch of the halo tile rows (tile width + tap span)
     int halo_wt, halo_bh; // output tile: halo_wt columns x halo_bh rows of one image
     int halo_hb;          // halo box height (halo_bh + tap span)

@@ -61,21 +61,41 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Ctl ctl)
     return wait_slow(bar, parity, ctl);
 }
 
-// Walk over this CTA's work items g = blockIdx.x, blockIdx.x + gridDim.x, ...
-// as (phase, index within the phase), phases read from the shared-memory copy.
+// Walk over this CTA's work items g = start, start + step, ... as (phase,
+// index within the phase), phases read from the shared-memory copy.  The
+// first `il` phases (il >= 2, all with il_items items) are interleaved: the
+// items of scheduling round r (G consecutive items, one per CTA or CTA pair;
+// G a multiple of il) are tiles r*G/il .. (r+1)*G/il - 1 of every one of those
+// phases, so the phases' tiles over the same region of dY run together and
+// share it through L2; position pos = il*a + b of the round is tile
+// r*G/il + a of phase (b + r) mod il, which rotates each CTA through the
+// phases (their tap counts differ) from round to round.  The remaining phases
+// follow one after another.
 struct ItemWalk {
     const CdgPhase *tab;
-    int nph, step;
-    int phase, local;
+    int nph, step, il, il_items, il_round;
+    int g, phase, local;
     // items start, start + step, ...: one CTA's (step = gridDim.x) or one CTA
     // pair's (step = number of pairs) share of the work list
-    __device__ __forceinline__ ItemWalk(const CdgPhase *t, int n, int start, int stp)
-        : tab(t), nph(n), step(stp), phase(0), local(start)
+    __device__ __forceinline__ ItemWalk(const CdgPhase *t, int n, int start, int stp, int il_, int il_items_,
+                                        int il_round_)
+        : tab(t), nph(n), step(stp), il(il_), il_items(il_items_), il_round(il_round_), g(start), phase(0), local(0)
     {
         settle();
     }
     __device__ __forceinline__ void settle()
     {
+        if (il > 0 && g < il * il_items) {
+            const int r = g / il_round;
+            const int pos = g - r * il_round;
+            const int a = pos / il;
+            const int b = pos - a * il;
+            phase = (b + r) % il;
+            local = r * (il_round / il) + a;
+            return;
+        }
+        phase = il;
+        local = g - il * il_items;
         while (phase < nph && local >= tab[phase].items) {
             local -= tab[phase].items;
             ++phase;
@@ -84,7 +104,7 @@ struct ItemWalk {
     __device__ __forceinline__ bool valid() const { return phase < nph; }
     __device__ __forceinline__ void next()
     {
-        local += step;
+        g += step;
         settle();
     }
 };
@@ -152,7 +172,7 @@ __device__ __forceinline__ void run_loader(const CdgParams &p, const Ring &R, co
     uint32_t parity = 0;
     int owner = 0;  // loader index of the current global stage
     bool ok = true;
-    for (ItemWalk w(tab, p.nphases, S.start, S.step); ok && w.valid(); w.next()) {
+    for (ItemWalk w(tab, p.nphases, S.start, S.step, p.interleave, p.il_items, p.il_round); ok && w.valid(); w.next()) {
         const CdgPhase &ph = tab[w.phase];
         const int ntap = ph.tap_count;
         if (ntap == 0) continue;
@@ -255,7 +275,7 @@ __device__ __forceinline__ void run_loader_halo(const CdgParams &p, const Ring &
         }
         __syncwarp();
     }
-    for (ItemWalk w(tab, p.nphases, S.start, S.step); ok && w.valid(); w.next()) {
+    for (ItemWalk w(tab, p.nphases, S.start, S.step, p.interleave, p.il_items, p.il_round); ok && w.valid(); w.next()) {
         const CdgPhase &ph = tab[w.phase];
         const int ntap = ph.tap_count;
         if (ntap == 0) continue;
@@ -328,7 +348,7 @@ __device__ __forceinline__ void run_mma_halo(const CdgParams &p, const Ring &R, 
     bool b_ready = false;  // full barrier of the current weight stage already seen complete
     const bool res = p.b_res != 0;
     if (res && !wait_bar(R.full0 + 8u * as, 0, ctl)) ok = false;  // resident weights landed
-    for (ItemWalk w(tab, p.nphases, S.start, S.step); ok && w.valid(); w.next()) {
+    for (ItemWalk w(tab, p.nphases, S.start, S.step, p.interleave, p.il_items, p.il_round); ok && w.valid(); w.next()) {
         const CdgPhase &ph = tab[w.phase];
         const int ntap = ph.tap_count;
         if (ntap == 0) continue;
@@ -432,7 +452,7 @@ __device__ __forceinline__ void run_mma(const CdgParams &p, const Ring &R, const
     uint32_t acc_count = 0;
     bool ok = true;
     bool ready = false;  // full barrier of `stage` already seen complete
-    for (ItemWalk w(tab, p.nphases, S.start, S.step); ok && w.valid(); w.next()) {
+    for (ItemWalk w(tab, p.nphases, S.start, S.step, p.interleave, p.il_items, p.il_round); ok && w.valid(); w.next()) {
         const int ntap = tab[w.phase].tap_count;
         if (ntap == 0) continue;
         const uint32_t acc = acc_count & 1u;
@@ -590,7 +610,7 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
     // between two MMA warps, each with two accumulators of its own)
     uint32_t acc_count[2] = {0u, 0u}, chunk_count = 0;
     uint32_t item_index = 0;
-    for (ItemWalk w(tab, p.nphases, S.start, S.step); w.valid(); w.next(), ++item_index) {
+    for (ItemWalk w(tab, p.nphases, S.start, S.step, p.interleave, p.il_items, p.il_round); w.valid(); w.next(), ++item_index) {
         const CdgPhase &ph = tab[w.phase];
         const int mt = S.m_tile(w.local, tiles_n);
         const int nt = w.local - (tiles_n == 1 ? w.local : w.local / tiles_n) * tiles_n;
