@@ -199,3 +199,31 @@ def test_chained_launches_keep_stream_order():
     dY_b = first.view(np.uint16).reshape(A.N, A.H, A.W, A.C)
     ref_b = oracle.dgrad(dY_b, rb.W, B.H, B.W, B.stride, B.pad, B.dil, dtype=B.dtype)
     assert_close(got_b, ref_b, rb.odt, "B after A")
+
+
+# Shapes that reach the planner's special paths by default: a CTA pair (256
+# channels, 36 stages per tile), a pair whose partner M tile lies wholly out of
+# range (one 9x9 tile), and four equal stride-2 phases with dual MMA issue and
+# interleaved items.
+MODE_CASES = [_case(2, 14, 14, 256, 256, 3, 3, 1, 1, 1, "bf16", idx=5),
+              _case(1, 9, 9, 256, 128, 3, 3, 1, 1, 1, "bf16", idx=6),
+              _case(4, 16, 16, 128, 256, 3, 3, 2, 1, 1, "bf16", relu=True, idx=7)]
+
+
+def test_mode_cases_reach_their_paths():
+    import implicit_gemm_dgrad_gb300 as cdg
+    infos = [cdg.plan(L.N, L.H, L.W, L.C, L.K, L.R, L.S, L.stride, L.pad, L.dil, L.dtype, relu=L.relu).info()
+             for L in MODE_CASES]
+    assert infos[0]["cta_pair"] == 1 and infos[1]["cta_pair"] == 1
+    assert infos[2]["mma_warps"] == 2 and infos[2]["num_phases"] == 4
+
+
+@pytest.mark.parametrize("env", ["", "CDG_PAIR=0", "CDG_PAIR=1", "CDG_DUAL=0", "CDG_INTERLEAVE=0", "CDG_HALO=0",
+                                 "CDG_PDL=0"])
+@pytest.mark.parametrize("L", MODE_CASES, ids=lambda L: L.name)
+def test_planner_mode_overrides(L, env, monkeypatch):
+    """Every planner mode and its override gives the oracle's result."""
+    if env:
+        key, val = env.split("=")
+        monkeypatch.setenv(key, val)
+    check_layer(L)
