@@ -86,11 +86,46 @@ def roofline_time_s(layer, peaks):
     return max(t_tc, t_hbm), ("tensor" if t_tc >= t_hbm else "hbm")
 
 
+class _NvmlClocks:
+    """SM clock, power and clock-event reasons read through NVML (ctypes,
+    read-only queries), or None when the library is missing."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, index: int):
+        import ctypes
+        self.c = ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.lib = lib
+        self.dev = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.dev)) != 0:
+            raise OSError("no NVML device")
+        v = ctypes.c_uint()
+        self.max_sm = float(v.value) if lib.nvmlDeviceGetMaxClockInfo(self.dev, 1, ctypes.byref(v)) == 0 else None
+        self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+
+    def sample(self):
+        c = self.c
+        v, r, pw = c.c_uint(), c.c_ulonglong(), c.c_uint()
+        sm = float(v.value) if self.lib.nvmlDeviceGetClockInfo(self.dev, 1, c.byref(v)) == 0 else None
+        reasons = r.value if self.reasons_fn(self.dev, c.byref(r)) == 0 else 0
+        power = pw.value / 1000.0 if self.lib.nvmlDeviceGetPowerUsage(self.dev, c.byref(pw)) == 0 else None
+        return sm, reasons, power
+
+    def close(self):
+        self.lib.nvmlShutdown()
+
+
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 50 ms in the
-    background.  Entering waits (up to 5 s) for the first sample, so sampling
-    is running when the timed region starts; the summary counts only the
-    samples taken after that first one."""
+    """SM clocks, power and clock-event (throttle) reasons sampled during the
+    timed region: every 2 ms on a thread through NVML (read-only
+    queries), or, where NVML cannot be loaded, every 50 ms by nvidia-smi (the
+    sampler then waits for its first sample before the region starts and
+    reports the samples taken after it)."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -99,9 +134,27 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
+        self.nvml = None
+        self.samples = []
         self.path = os.path.join("/tmp", f"cdg_clocks_{os.getpid()}.csv")
 
     def __enter__(self):
+        try:
+            self.nvml = _NvmlClocks(self.gpu)
+        except Exception:  # noqa: BLE001 - fall back to nvidia-smi
+            self.nvml = None
+        if self.nvml is not None:
+            import threading
+            self.stop = threading.Event()
+
+            def loop():
+                while not self.stop.is_set():
+                    self.samples.append(self.nvml.sample())
+                    time.sleep(0.002)
+            self.samples.append(self.nvml.sample())
+            self.thread = threading.Thread(target=loop, daemon=True)
+            self.thread.start()
+            return self
         try:
             self.out = open(self.path, "w")
             self.proc = subprocess.Popen(
@@ -122,6 +175,11 @@ class ClockSampler:
         return self
 
     def __exit__(self, *exc):
+        if self.nvml is not None:
+            self.stop.set()
+            self.thread.join(timeout=5)
+            self.samples.append(self.nvml.sample())
+            return
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -131,6 +189,19 @@ class ClockSampler:
             self.out.close()
 
     def summary(self):
+        if self.nvml is not None:
+            sm = [x[0] for x in self.samples if x[0] is not None]
+            reasons = set()
+            for _, bits, _ in self.samples:
+                for bit, name in _NvmlClocks.REASONS.items():
+                    if bits & bit:
+                        reasons.add(name)
+            power = [x[2] for x in self.samples if x[2] is not None]
+            out = {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": self.nvml.max_sm,
+                   "sm_min_mhz": min(sm) if sm else None, "reasons": sorted(reasons), "samples": len(self.samples),
+                   "power_w_max": max(power) if power else None, "source": "nvml, 2 ms"}
+            self.nvml.close()
+            return out
         if self.proc is None or not os.path.exists(self.path):
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         sm, smax, reasons = [], None, set()
@@ -153,7 +224,7 @@ class ClockSampler:
                     reasons.add(name)
         os.unlink(self.path)
         return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": smax,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "source": "nvidia-smi, 50 ms"}
 
 
 def cpu_oracle_sample(layers, arrays, images: int):
