@@ -116,12 +116,12 @@ void choose_box(const std::vector<CdgPhase> &phases, int N, int &bw, int &bh, in
 // granule).  C > 256: several tiles, each a multiple of 64 so that the
 // epilogue's 64-channel store boxes never reach into the neighbouring tile;
 // least padding wins, larger tiles on ties.
-int choose_bn(int C)
+int choose_bn(int C, int max_bn)
 {
-    if (C <= 256) return ((C + 15) / 16) * 16;
-    int best = 256;
+    if (C <= max_bn) return ((C + 15) / 16) * 16;
+    int best = max_bn;
     long long best_waste = -1;
-    for (int bn = 256; bn >= 64; bn -= 64) {
+    for (int bn = max_bn; bn >= 64; bn -= 64) {
         const long long waste = 1LL * ceil_div(C, bn) * bn - C;
         if (best_waste < 0 || waste < best_waste) {
             best_waste = waste;
@@ -229,7 +229,11 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     const bool flat = d_mode != CDG_D_BOX4;
     int bw = 0, bh = 0, bnb = 0;
     if (!flat) choose_box(phases, N, bw, bh, bnb);
-    const int BN = choose_bn(C);
+    // N tile: all of C up to 256 channels, else the multiple of 64 up to 256
+    // with the least padding ("CDG_MAX_BN=128" caps it at 128)
+    const char *bn_env = std::getenv("CDG_MAX_BN");
+    const int max_bn = (bn_env && std::atoi(bn_env) == 128) ? 128 : 256;
+    const int BN = choose_bn(C, max_bn);
     const int tiles_n = ceil_div(C, BN);
     const int ring_budget = kMaxSmem - 1024 - CDG_SMEM_STAGING - CDG_SMEM_TAIL;
 
