@@ -9,10 +9,14 @@
 //     exactly the taps (r, s) with ph + pad - r*dil = 0 (mod stride) and
 //     likewise for s, reading dY at p = i + (ph + pad - r*dil)/stride;
 //   * the operand mode: 1x1 pad-0 filters read dY rows as a plain 2-D matrix,
-//     everything else reads 4-D (channel, column, row, image) halo boxes whose
-//     out-of-range part the TMA unit fills with zeros;
+//     everything else reads 4-D (channel, column, row, image) boxes per tap,
+//     or one halo box per tile for all taps with the weights resident when
+//     the filter fits; the TMA unit fills out-of-range parts with zeros;
+//   * the issue variant: CTA pairs (2-SM MMA) for long 256-channel tiles,
+//     two MMA warps for N tiles of up to 128 channels;
 //   * the tile shape, pipeline depth and work list (phases ordered by tap
-//     count, longest first, then M tiles, then N tiles).
+//     count, longest first, then M tiles, then N tiles; equal phases
+//     interleaved round by round).
 #include <cuda.h>
 #include <cuda_runtime.h>
 

@@ -10,15 +10,21 @@
 // zero-inserted multiply is ever issued; phases that no tap reaches are
 // written as zeros by the epilogue.
 //
-// CTA layout (192 threads, one CTA per SM, persistent over work items):
-//   warp 0     TMA producer: per (tap, 64-channel block) one dY box and one
-//              weight box into a shared-memory ring, mbarrier full/empty.
-//   warp 1     owns TMEM; one thread issues tcgen05.mma (M=128, N=BN, K=16)
-//              into one of two fp32 accumulators and commits stages back.
-//   warps 2-5  epilogue: tcgen05.ld of the accumulator, optional ReLU-backward
-//              gate, conversion, 16-byte stores into NHWC dX.
-// Every wait is bounded: past CDG_WAIT_LIMIT_NS the kernel records
-// CDG_ERR_TIMEOUT in the status word and all roles leave their loops.
+// CTA layout (256 threads, one CTA per SM, persistent over work items,
+// launched with programmatic stream serialization):
+//   warps 0, 2, 3  TMA loaders: per (tap, 64-channel block of K) one dY box
+//                  and one weight box into a ring of stages (mbarrier
+//                  full/empty), stages taken round-robin;
+//   warp 1         owns TMEM; one elected lane issues tcgen05.mma (M=128,
+//                  N=BN, K=16) into one of two fp32 accumulators and commits
+//                  stages back;
+//   warps 4-7      epilogue: tcgen05.ld of the accumulator, optional
+//                  ReLU-backward gate, RNE conversion into a swizzled staging
+//                  buffer, TMA bulk stores into NHWC dX.
+// Modes (MODE below): halo boxes (one dY box per tile and K block for all
+// taps, weights resident or streamed), CTA pairs (2-SM MMA over 256-row
+// tiles), dual issue (warps 1 and 3 issue MMAs for alternate items, each fed
+// by its own loader warp 0 or 2 and ring half, with two accumulators each).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -732,11 +738,15 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
 }
 
 // ------------------------------------------------------------------ kernel
-// MODE: 0 per-tap operand boxes, one CTA per tile; 1 halo operand mode;
-//       2 per-tap boxes, CTA pairs (cluster of 2) sharing 256-row tiles through
-//         tcgen05.mma.cta_group::2: each CTA holds its own 128 rows of A and
-//         half of the weight tile, which halves the B bytes every SM's shared
-//         memory takes in and hands to the tensor core.
+// MODE: 0 per-tap operand boxes (or row boxes for 1x1 filters), one CTA per
+//         tile, one MMA warp;
+//       1 halo operand mode (weights resident when they fit, else streamed);
+//       2 per-tap or row boxes, CTA pairs (cluster of 2) sharing 256-row tiles
+//         through tcgen05.mma.cta_group::2: each CTA holds its own 128 rows of
+//         A and half of the weight tile, which halves the B bytes every SM's
+//         shared memory takes in and hands to the tensor core;
+//       3 per-tap or row boxes, two MMA warps (dual issue) for N tiles of up to
+//         128 channels.
 template <int OUT_T, bool MASK, int IN_T, int MODE>
 __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_constant__ CdgParams p)
 {
