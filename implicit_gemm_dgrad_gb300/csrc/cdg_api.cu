@@ -254,7 +254,7 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     // stage), so that form is used only when asked (CDG_HALO=1), wherever the
     // geometry allows; CDG_HALO=0 turns halo mode off.
     bool halo = false, b_res = false;
-    int hwb = 0, hwt = 0, hbh = 0, hhb = 0, hrows = 0, a_stages = 0, b_stages = 0, b_res_bytes = 0;
+    int hwb = 0, hwt = 0, hbh = 0, hhb = 0, hrows = 0, a_stages = 0, b_stages = 0, b_res_bytes = 0, halo_tg = 1;
     const char *halo_env = std::getenv("CDG_HALO");
     const bool halo_forced = halo_env && halo_env[0] == '1';
     if (!flat && !(halo_env && halo_env[0] == '0')) {
@@ -279,8 +279,17 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
             const int off_max = span_r * wb + span_s;
             const int rows = ((std::max(wb * hb, off_max + CDG_BM) + 7) / 8) * 8;
             const int a_bytes = rows * 128, b_bytes = BN * 128;
-            int as = (3 * a_bytes + 4 * b_bytes <= ring_budget) ? 3 : 2;
-            int bs = std::min(std::min(kMaxStages, CDG_MAX_STAGES_TOTAL - as), (ring_budget - as * a_bytes) / b_bytes);
+            // streamed weights: stages of tg taps, one handshake per group; the
+            // largest tg (up to 4, and at most the longest phase's taps) that
+            // leaves at least two halo and three weight stages
+            int tg = 1;
+            for (int t = std::min(4, maxtaps); t >= 1; --t)
+                if (2 * a_bytes + 3 * t * b_bytes <= ring_budget) {
+                    tg = t;
+                    break;
+                }
+            int as = (3 * a_bytes + 4 * tg * b_bytes <= ring_budget) ? 3 : 2;
+            int bs = std::min(std::min(kMaxStages, CDG_MAX_STAGES_TOTAL - as), (ring_budget - as * a_bytes) / (tg * b_bytes));
             // the whole packed filter of a single N tile fits next to at least
             // two halo stages: load it once per CTA and keep it resident, so a
             // tile needs one pipeline handshake (its halo box) for all taps
@@ -290,6 +299,7 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
                 b_res_bytes = static_cast<int>(res_bytes);
                 as = std::min<int>(CDG_MAX_STAGES_TOTAL - 1, (ring_budget - b_res_bytes) / a_bytes);
                 bs = 1;  // one barrier: the resident weights have landed
+                tg = 1;
             }
             if (hb <= 256 && bs >= (b_res ? 1 : 2) && (b_res || halo_forced)) {
                 halo = true;
@@ -300,6 +310,7 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
                 hrows = rows;
                 a_stages = as;
                 b_stages = bs;
+                halo_tg = tg;
                 for (CdgPhase &f : phases)
                     for (int t = f.tap_begin; t < f.tap_begin + f.tap_count; ++t)
                         taps[t].hoff = static_cast<int16_t>((taps[t].dr - f.dr_min) * wb + (taps[t].ds - f.ds_min));
@@ -364,7 +375,7 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     bool dual = !halo && !pair && BN <= 128 && max_stages >= 4 && stages_per_tile >= 4.0;
     if (dual_env && dual_env[0] == '0') dual = false;
     const int stages = dual ? (max_stages / 2) * 2 : max_stages;
-    const int ring_bytes = halo ? a_stages * hrows * 128 + (b_res ? b_res_bytes : b_stages * BN * 128)
+    const int ring_bytes = halo ? a_stages * hrows * 128 + (b_res ? b_res_bytes : b_stages * halo_tg * BN * 128)
                                 : stages * stage_bytes;
     // two accumulators per MMA warp, each at least as wide as the 64-column
     // chunks the epilogue reads
@@ -396,6 +407,7 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     p.a_stage_bytes = static_cast<uint32_t>(halo ? hrows * 128 : stage_bytes);
     p.halo_hb = hhb;
     p.b_res = b_res ? 1 : 0;
+    p.halo_tg = halo_tg;
     p.b_res_bytes = static_cast<uint32_t>(b_res_bytes);
     p.tx_a = static_cast<uint32_t>(hwb * hhb * 128);
     p.tx_b = static_cast<uint32_t>(BN * 128);

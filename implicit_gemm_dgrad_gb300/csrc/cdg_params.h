@@ -79,6 +79,7 @@ struct CdgParams {  // CUtensorMap members carry their own (128-byte) alignment
     int halo_hb;          // halo box height (halo_bh + tap span)
     int a_stages, b_stages;   // halo mode: separate rings for halo boxes and weight tiles
     int b_res;            // halo mode: every weight tile resident in shared memory, loaded once
+    int halo_tg;          // halo mode, streamed weights: taps per weight stage (>= 1)
     uint32_t b_res_bytes; // bytes of the resident weights (taps x K blocks x BN rows x 128 B)
     uint32_t a_stage_bytes;   // halo mode: bytes of one halo stage (>= the box, room for every tap's 128 rows)
     uint32_t tx_a, tx_b;      // halo mode: bytes one halo stage / one weight stage receives

@@ -250,7 +250,8 @@ __device__ __forceinline__ void drain_loads(const Ring &R, int stages, int *stat
 
 // ------------------------------------------------------------------ halo-mode loaders
 // Loader 0 streams one dY halo box per (tile, K block) into the A ring;
-// loaders 1.. stream the per-tap weight tiles into the B ring, round-robin.
+// loaders 1.. stream the weight tiles, up to tg taps per stage, into the B
+// ring round-robin (or loader 1 loads every weight tile once, when resident).
 __device__ __forceinline__ void run_loader_halo(const CdgParams &p, const Ring &R, const CdgPhase *tab,
                                                 const CdgTap *taps, Ctl ctl, int li, bool leader,
                                                 volatile uint32_t *slot_parity, Sched S)
@@ -262,8 +263,9 @@ __device__ __forceinline__ void run_loader_halo(const CdgParams &p, const Ring &
         asm volatile("prefetch.tensormap [%0];" ::"l"(mapB) : "memory");
     }
     const int KB = p.KB, tiles_n = p.tiles_n, BN = p.BN;
-    const int as = p.a_stages, bs = p.b_stages, bh = p.halo_bh, wt = p.halo_wt;
-    const uint32_t tx_a = p.tx_a, tx_b = p.tx_b;
+    const int as = p.a_stages, bs = p.b_stages, bh = p.halo_bh, wt = p.halo_wt, tg = p.halo_tg;
+    const uint32_t tx_a = p.tx_a;
+    const uint32_t gstride = static_cast<uint32_t>(tg) * R.b_bytes;  // bytes of one weight stage
     int a_stage = 0, b_stage = 0, owner = 1;
     uint32_t a_par = 0, b_par = 0;
     bool ok = true;
@@ -309,9 +311,11 @@ __device__ __forceinline__ void run_loader_halo(const CdgParams &p, const Ring &
                     a_par ^= 1u;
                 }
             } else if (p.b_res) {
-                // resident weights: loaded once, before the first tile, below
+                // resident weights: loaded once, before the first tile (above)
             } else {
-                for (int tt = 0; tt < ntap; ++tt) {
+                // weight stages of up to tg taps each: one handshake per group
+                for (int g0 = 0; g0 < ntap; g0 += tg) {
+                    const int n_in = min(tg, ntap - g0);
                     if (owner == li) {
                         const int slot = as + b_stage;
                         const uint32_t full = R.full0 + 8u * slot;
@@ -321,9 +325,10 @@ __device__ __forceinline__ void run_loader_halo(const CdgParams &p, const Ring &
                         }
                         if (leader) {
                             slot_parity[slot] = b_par | 2u;
-                            mbar_arrive_expect_tx(full, tx_b);
-                            tma_load_3d(R.b0 + b_stage * R.b_bytes, mapB, full, kb * CDG_BK, c0,
-                                        taps[ph.tap_begin + tt].t);
+                            mbar_arrive_expect_tx(full, static_cast<uint32_t>(n_in) * R.b_bytes);
+                            for (int i = 0; i < n_in; ++i)
+                                tma_load_3d(R.b0 + b_stage * gstride + static_cast<uint32_t>(i) * R.b_bytes, mapB,
+                                            full, kb * CDG_BK, c0, taps[ph.tap_begin + g0 + i].t);
                         }
                         __syncwarp();
                     }
@@ -338,16 +343,17 @@ __device__ __forceinline__ void run_loader_halo(const CdgParams &p, const Ring &
     }
 }
 
-// Halo-mode MMA issuer: per K block one halo stage; per tap one weight stage
-// and four MMAs whose A operand starts at the tap's row of the halo box.
+// Halo-mode MMA issuer: per K block one halo stage; per group of up to tg taps
+// one weight stage (or the resident weights), and per tap four MMAs whose A
+// operand starts at the tap's row of the halo box.
 __device__ __forceinline__ void run_mma_halo(const CdgParams &p, const Ring &R, const CdgPhase *tab,
                                              const CdgTap *taps, Ctl ctl, uint32_t tmem_base, bool leader, Sched S)
 {
-    const int KB = p.KB, as = p.a_stages, bs = p.b_stages;
+    const int KB = p.KB, as = p.a_stages, bs = p.b_stages, tg = p.halo_tg;
     const uint32_t idesc = p.idesc, acc_stride = p.acc_stride;
     const uint64_t adesc0 = sdesc_k128_sw128(R.a0);
     const uint64_t bdesc0 = sdesc_k128_sw128(R.b0);
-    const uint32_t astep = R.stage_bytes >> 4, bstep = R.b_bytes >> 4;  // descriptor units per stage
+    const uint32_t astep = R.stage_bytes >> 4;  // descriptor units per halo stage
     int a_stage = 0, b_stage = 0;
     uint32_t a_par = 0, b_par = 0, acc_count = 0;
     bool ok = true;
@@ -391,32 +397,39 @@ __device__ __forceinline__ void run_mma_halo(const CdgParams &p, const Ring &R, 
                     if (tt + 1 < ntap) hoff = ptap[tt + 1].hoff;
                 }
             } else {
-                for (int tt = 0; tt < ntap; ++tt) {
+                const uint32_t bunit = R.b_bytes >> 4;  // descriptor units per weight tile
+                for (int g0 = 0; g0 < ntap; g0 += tg) {
+                    const int n_in = min(tg, ntap - g0);
                     const int slot = as + b_stage;
                     if (!b_ready && !wait_bar(R.full0 + 8u * slot, b_par, ctl)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    {  // test the next weight stage while this tap's MMAs issue
-                        const int nb = b_stage + 1 == bs ? 0 : b_stage + 1;
-                        b_ready = mbar_test_wait(R.full0 + 8u * (as + nb), nb == 0 ? b_par ^ 1u : b_par);
-                    }
-                    const int hnext = tt + 1 < ntap ? ptap[tt + 1].hoff : 0;
-                    if (leader) {
-                        // 128-byte rows: a row offset of hoff is 8*hoff descriptor units
-                        const uint64_t adesc = abase + 8u * static_cast<uint32_t>(hoff);
-                        const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(b_stage * bstep);
+                    for (int i = 0; i < n_in; ++i) {
+                        const int tt = g0 + i;
+                        if (leader) {
+                            // 128-byte rows: a row offset of hoff is 8*hoff descriptor units
+                            const uint64_t adesc = abase + 8u * static_cast<uint32_t>(hoff);
+                            const uint64_t bdesc =
+                                bdesc0 + static_cast<uint64_t>(static_cast<uint32_t>(b_stage * tg + i) * bunit);
 #pragma unroll
-                        for (int k = 0; k < CDG_BK / 16; ++k)
-                            umma_f16(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, (kb | tt | k) != 0);
-                        umma_commit(R.empty0 + 8u * slot);
+                            for (int k = 0; k < CDG_BK / 16; ++k)
+                                umma_f16(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, (kb | tt | k) != 0);
+                        }
+                        __syncwarp();
+                        // the next tap's row offset is read only once this tap's MMAs
+                        // are queued: an outstanding shared-memory load delays MMA issue
+                        if (tt + 1 < ntap) hoff = ptap[tt + 1].hoff;
                     }
+                    if (leader) umma_commit(R.empty0 + 8u * slot);
                     __syncwarp();
-                    hoff = hnext;
                     if (++b_stage == bs) {
                         b_stage = 0;
                         b_par ^= 1u;
+                    }
+                    {  // test the next weight stage (its latency overlaps the queued MMAs)
+                        b_ready = mbar_test_wait(R.full0 + 8u * (as + b_stage), b_par);
                     }
                 }
             }
@@ -764,7 +777,7 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_cons
     R.stage_bytes = p.a_stage_bytes;
     R.b0 = base + p.a_stages * R.stage_bytes;
     R.b_bytes = p.BN * 128;
-    R.out0 = HALO ? R.b0 + (p.b_res ? p.b_res_bytes : p.b_stages * R.b_bytes) : base + stages * R.stage_bytes;
+    R.out0 = HALO ? R.b0 + (p.b_res ? p.b_res_bytes : p.b_stages * p.halo_tg * R.b_bytes) : base + stages * R.stage_bytes;
     const uint32_t bars = R.out0 + CDG_SMEM_STAGING;
     // mbarriers: full[stages], empty[stages], acc_full[4], acc_empty[4], drain[2]
     R.full0 = bars;
