@@ -242,11 +242,32 @@ def cpu_oracle_sample(layers, arrays, images: int):
             "seconds": dt}
 
 
+def max_over_ranks(x: float, world: int) -> float:
+    """The largest of every rank's x (the slowest replica's time), reduced over
+    the gloo control group; x itself when there is one rank."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def select_layers(names: str):
+    layers = RESNET50_B256
+    if names:
+        keep = set(names.split(","))
+        layers = [L for L in layers if L.name in keep]
+    return layers
+
+
 def run_reference(args, rank, world):
-    """The reference arm: the CPU oracle, as it stands, on a bounded sample."""
+    """The reference arm: the CPU oracle, as it stands, on a bounded sample.
+    Under torchrun only rank 0 runs it; the other ranks return at once."""
     if rank != 0:
         return
-    layers = RESNET50_B256
+    layers = select_layers(args.layers)
     n = args.ref_images
     arrays = [synth.make_inputs(L.shape(), L.dtype, L.dist, L.workload, L.index, batch=n) for L in layers]
     for _ in range(args.warmup):
@@ -256,7 +277,7 @@ def run_reference(args, rank, world):
         res = cpu_oracle_sample(layers, arrays, n)
         times.append(res["seconds"])
     value = res["value"]
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 1,
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * float(np.mean(times)),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": WORKLOAD, "images_per_layer_per_step": n, "layers": len(layers)},
@@ -300,10 +321,7 @@ def main():
     stream = torch.cuda.Stream(device=dev)
     peaks = load_peaks()
 
-    layers = RESNET50_B256
-    if args.layers:
-        keep = set(args.layers.split(","))
-        layers = [L for L in layers if L.name in keep]
+    layers = select_layers(args.layers)
 
     # ---- inputs (seeded, host), upload, plan, prepack
     host, state = [], []
@@ -386,11 +404,7 @@ def main():
     barrier()
     step_ms = [ev0[k].elapsed_time(ev1[k]) for k in range(args.steps)]
     dom_ms = float(np.mean([dv0[k].elapsed_time(dv1[k]) for k in range(args.steps)]))
-    total_ms = float(np.sum(step_ms))
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(float(np.sum(step_ms)), world)
     ms_per_step = total_ms / args.steps
     flops_step = sum(L.flops for (L, *_r) in state)
     value = world * flops_step * args.steps / (total_ms * 1e-3) / 1e12
@@ -470,11 +484,7 @@ def main():
         if not torch.equal(h_dX[i][::4099], d_dX[::4099].cpu()):
             raise RuntimeError(f"end-to-end read-back of {L.name} differs from the device result")
     barrier()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
     e2e_value = world * flops_step * args.e2e_steps / (e2e_ms * 1e-3) / 1e12
     for (_, p, *_rest) in state:
         st = p.device_status(stream)
