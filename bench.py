@@ -298,6 +298,8 @@ def main():
     ap.add_argument("--ref-images", type=int, default=8, help="images per layer per reference-arm step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", default="", help="comma-separated layer names (default: all 22)")
+    ap.add_argument("--autotune", type=int, default=0,
+                    help="1: tune every layer's plan with cdg_autotune during set-up (untimed)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -337,6 +339,12 @@ def main():
             p.prepack_weights(d_W, d_Wp, stream)
             state.append((L, p, d_dY, d_Wp, d_dX))
     torch.cuda.synchronize()
+    tuned_ms = {}
+    if args.autotune:
+        # plan-time tuning (cuDNN-Find style), before and outside every timed region
+        for (L, p, d_dY, d_Wp, d_dX) in state:
+            tuned_ms[L.name] = p.autotune(d_dY, d_Wp, d_dX, None, stream, reps=5)
+        torch.cuda.synchronize()
 
     def step():
         for (_, p, d_dY, d_Wp, d_dX) in state:
@@ -413,7 +421,10 @@ def main():
     for i, (L, p, *_r) in enumerate(state):
         t = per_layer_ms[i] * 1e-3
         t_roof, bound = roofline_time_s(L, peaks)
+        inf = p.info()
         per_layer.append({"layer": L.name, "ms": round(per_layer_ms[i], 5),
+                          "plan": {"a_mode": inf["a_mode"], "cta_pair": inf["cta_pair"], "mma_warps": inf["mma_warps"],
+                                   "tile_n": inf["tile_n"], "stages": inf["stages"], "tuned": inf["tuned"]},
                           "tflops": round(L.flops / t / 1e12, 2),
                           "gbs": round(L.bytes / t / 1e9, 1), "bound": bound,
                           "roofline_frac": round(t_roof / t, 4),
@@ -505,7 +516,9 @@ def main():
         "config": {"workload": WORKLOAD, "global_batch": 256 * world, "layers": nL,
                    "l2": "inputs larger than L2: the step cycles ~5 GB of operands, so each layer's data is "
                          "evicted before its next use",
-                   "flops_per_step": flops_step, "parallelism": f"replicas x{world}"},
+                   "flops_per_step": flops_step, "parallelism": f"replicas x{world}",
+                   "plans": "autotuned at set-up (cdg_autotune, 5 cold-cache launches per candidate)" if args.autotune
+                   else "planner defaults"},
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,

@@ -33,7 +33,7 @@ DTYPES = {"f16": F16, "bf16": BF16}
 
 EXPORTS = ("cdg_plan", "cdg_plan_host", "cdg_destroy", "cdg_get_output_dims", "cdg_packed_weight_bytes",
            "cdg_plan_get_info", "cdg_prepack_weights", "cdg_dgrad", "cdg_device_status", "cdg_status_string",
-           "cdg_dgrad_noalloc")
+           "cdg_dgrad_noalloc", "cdg_autotune")
 
 
 class CdgError(RuntimeError):
@@ -49,7 +49,7 @@ class PlanInfo(ctypes.Structure):
                 ("box_h", ctypes.c_int), ("box_n", ctypes.c_int), ("stages", ctypes.c_int),
                 ("work_items", ctypes.c_int), ("grid", ctypes.c_int), ("smem_bytes", ctypes.c_int),
                 ("tmem_cols", ctypes.c_int), ("cta_pair", ctypes.c_int),
-                ("mma_warps", ctypes.c_int)]
+                ("mma_warps", ctypes.c_int), ("tuned", ctypes.c_int)]
 
     def as_dict(self) -> dict:
         d = {name: getattr(self, name) for name, _ in self._fields_}
@@ -96,6 +96,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.cdg_status_string.restype = ctypes.c_char_p
     lib.cdg_dgrad_noalloc.argtypes = [hp, vp, vp, vp, vp, vp]
     lib.cdg_dgrad_noalloc.restype = i
+    lib.cdg_autotune.argtypes = [hp, vp, vp, vp, vp, vp, i, ctypes.POINTER(ctypes.c_float)]
+    lib.cdg_autotune.restype = i
     if path == LIB_PATH:
         _lib = lib
     return lib
@@ -203,6 +205,17 @@ class Plan:
                                         _stream(stream))
         if rc != OK:
             raise CdgError(rc, "cdg_dgrad_noalloc")
+
+    def autotune(self, dY, W_packed, dX, relu_mask=None, stream=None, reps: int = 3) -> float:
+        """Time every configuration the planner can produce for this shape on
+        these tensors and keep the fastest (cdg_autotune); returns its mean
+        launch time in ms.  dX receives the correct result."""
+        best = ctypes.c_float()
+        rc = self.lib.cdg_autotune(self.handle, _addr(dY), _addr(W_packed), _addr(dX), _addr(relu_mask),
+                                   _stream(stream), int(reps), ctypes.byref(best))
+        if rc != OK:
+            raise CdgError(rc, "cdg_autotune")
+        return float(best.value)
 
     def device_status(self, stream=None) -> int:
         return int(self.lib.cdg_device_status(self.handle, _stream(stream)))

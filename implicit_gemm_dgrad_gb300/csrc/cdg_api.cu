@@ -65,8 +65,20 @@ int floor_mod(int a, int m)
 
 }  // namespace
 
+// Planner choices that can be overridden (environment variables, or the
+// candidates cdg_autotune times); -1 leaves the choice to the planner.
+struct PlanOpts {
+    int halo = -1;        // 0 off, 1 halo boxes wherever the geometry allows
+    int pair = -1;        // 0 never, 1 whenever BN >= 128
+    int dual = -1;        // 0 one MMA warp
+    int interleave = -1;  // 0 phases one after another
+    int max_bn = 256;     // 128 caps the N tile
+    int pdl = 1;          // 0 plain launches
+};
+
 struct cdg_plan_st {
     int N, H, W, C, K, R, S, stride, pad, dil, dtype, epi;
+    PlanOpts opts;
     int P, Q;
     bool host_only;
     int device;
@@ -135,8 +147,26 @@ int choose_bn(int C, int max_bn)
     return best;
 }
 
+PlanOpts opts_from_env()
+{
+    PlanOpts o;
+    auto flag = [](const char *name) -> int {
+        const char *v = std::getenv(name);
+        if (!v || !v[0]) return -1;
+        return v[0] == '0' ? 0 : (v[0] == '1' ? 1 : -1);
+    };
+    o.halo = flag("CDG_HALO");
+    o.pair = flag("CDG_PAIR");
+    o.dual = flag("CDG_DUAL") == 0 ? 0 : -1;
+    o.interleave = flag("CDG_INTERLEAVE") == 0 ? 0 : -1;
+    const char *bn = std::getenv("CDG_MAX_BN");
+    o.max_bn = (bn && std::atoi(bn) == 128) ? 128 : 256;
+    o.pdl = flag("CDG_PDL") == 0 ? 0 : 1;
+    return o;
+}
+
 int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int pad, int dil, int dtype, int epilogue,
-              int num_sms, bool host_only, cdg_handle_t *out)
+              int num_sms, bool host_only, const PlanOpts &opt, cdg_handle_t *out)
 {
     if (!out) return CDG_ERR_INVALID_ARG;
     *out = nullptr;
@@ -164,6 +194,7 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     h->P = P; h->Q = Q;
     h->host_only = host_only;
     h->num_sms = num_sms;
+    h->opts = opt;
     h->in_type = dtype == CDG_F16 ? CDG_T_F16 : CDG_T_BF16;
     h->out_type = (epilogue & CDG_EPI_OUT_F32) ? CDG_T_F32 : h->in_type;
     h->mask = (epilogue & CDG_EPI_RELU_BWD) != 0;
@@ -234,10 +265,8 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     int bw = 0, bh = 0, bnb = 0;
     if (!flat) choose_box(phases, N, bw, bh, bnb);
     // N tile: all of C up to 256 channels, else the multiple of 64 up to 256
-    // with the least padding ("CDG_MAX_BN=128" caps it at 128)
-    const char *bn_env = std::getenv("CDG_MAX_BN");
-    const int max_bn = (bn_env && std::atoi(bn_env) == 128) ? 128 : 256;
-    const int BN = choose_bn(C, max_bn);
+    // with the least padding (max_bn 128 caps it at 128)
+    const int BN = choose_bn(C, opt.max_bn == 128 ? 128 : 256);
     const int tiles_n = ceil_div(C, BN);
     const int ring_budget = kMaxSmem - 1024 - CDG_SMEM_STAGING - CDG_SMEM_TAIL;
 
@@ -255,9 +284,8 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     // geometry allows; CDG_HALO=0 turns halo mode off.
     bool halo = false, b_res = false;
     int hwb = 0, hwt = 0, hbh = 0, hhb = 0, hrows = 0, a_stages = 0, b_stages = 0, b_res_bytes = 0, halo_tg = 1;
-    const char *halo_env = std::getenv("CDG_HALO");
-    const bool halo_forced = halo_env && halo_env[0] == '1';
-    if (!flat && !(halo_env && halo_env[0] == '0')) {
+    const bool halo_forced = opt.halo == 1;
+    if (!flat && opt.halo != 0) {
         int span_r = 0, span_s = 0, wt = 0, hmax = 0, maxtaps = 0;
         for (const CdgPhase &f : phases) {
             if (f.tap_count == 0) continue;
@@ -335,10 +363,9 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
             tap_sum += f.tap_count;
         }
     const double stages_per_tile = tap_phases ? double(tap_sum) / tap_phases * ceil_div(K, CDG_BK) : 0.0;
-    const char *pair_env = std::getenv("CDG_PAIR");  // "0": never, "1": whenever BN allows
     bool pair = !halo && BN == 256 && num_sms >= 2 && stages_per_tile >= 9.0;
-    if (pair_env && pair_env[0] == '0') pair = false;
-    if (pair_env && pair_env[0] == '1') pair = !halo && BN >= 128 && num_sms >= 2;
+    if (opt.pair == 0) pair = false;
+    if (opt.pair == 1) pair = !halo && BN >= 128 && num_sms >= 2;
 
     int items = 0;
     for (CdgPhase &f : phases) {
@@ -371,9 +398,8 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     // (measured on GB300: ~350 cycles per 64-channel stage against ~200 of
     // tensor work); with two, the other warp's MMAs fill that gap.  Tiles of
     // fewer than four stages gain nothing (the epilogue dominates them).
-    const char *dual_env = std::getenv("CDG_DUAL");  // "0": never
     bool dual = !halo && !pair && BN <= 128 && max_stages >= 4 && stages_per_tile >= 4.0;
-    if (dual_env && dual_env[0] == '0') dual = false;
+    if (opt.dual == 0) dual = false;
     const int stages = dual ? (max_stages / 2) * 2 : max_stages;
     const int ring_bytes = halo ? a_stages * hrows * 128 + (b_res ? b_res_bytes : b_stages * halo_tg * BN * 128)
                                 : stages * stage_bytes;
@@ -421,8 +447,7 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     p.pair = pair ? 1 : 0;
     // Programmatic dependent launch: the kernel's set-up overlaps the end of the
     // previous kernel in the stream ("0" turns it off).
-    const char *pdl_env = std::getenv("CDG_PDL");
-    p.pdl = (pdl_env && pdl_env[0] == '0') ? 0 : 1;
+    p.pdl = opt.pdl == 0 ? 0 : 1;
     p.dual = dual ? 1 : 0;
     // phases with taps (sorted first) of equal item counts are interleaved item
     // by item, so that their tiles over the same dY run close together (a
@@ -432,8 +457,7 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
         while (ntp < static_cast<int>(phases.size()) && phases[ntp].tap_count > 0) ++ntp;
         bool equal = ntp >= 2;
         for (int i = 1; i < ntp; ++i) equal = equal && phases[i].items == phases[0].items;
-        const char *il_env = std::getenv("CDG_INTERLEAVE");  // "0": off
-        if (il_env && il_env[0] == '0') equal = false;
+        if (opt.interleave == 0) equal = false;
         p.interleave = equal ? ntp : 0;
         p.il_items = equal ? phases[0].items : 0;
     }  // p.il_round is set once the grid is final (below)
@@ -611,13 +635,14 @@ int cdg_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int pa
     int dev = 0, sms = 0;
     // validate first so that argument errors never depend on a device
     cdg_handle_t probe = nullptr;
-    int rc = make_plan(N, H, W, C, K, R, S, stride, pad, dil, dtype, epilogue, 1, true, &probe);
+    const PlanOpts opt = opts_from_env();
+    int rc = make_plan(N, H, W, C, K, R, S, stride, pad, dil, dtype, epilogue, 1, true, opt, &probe);
     if (rc != CDG_OK) return rc;
     cdg_destroy(probe);
     if (cudaGetDevice(&dev) != cudaSuccess) return CDG_ERR_CUDA;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
         return CDG_ERR_CUDA;
-    return make_plan(N, H, W, C, K, R, S, stride, pad, dil, dtype, epilogue, sms, false, out);
+    return make_plan(N, H, W, C, K, R, S, stride, pad, dil, dtype, epilogue, sms, false, opt, out);
 }
 
 int cdg_plan_host(int N, int H, int W, int C, int K, int R, int S, int stride, int pad, int dil, int dtype,
@@ -627,7 +652,7 @@ int cdg_plan_host(int N, int H, int W, int C, int K, int R, int S, int stride, i
         if (out) *out = nullptr;
         return CDG_ERR_INVALID_ARG;
     }
-    return make_plan(N, H, W, C, K, R, S, stride, pad, dil, dtype, epilogue, num_sms, true, out);
+    return make_plan(N, H, W, C, K, R, S, stride, pad, dil, dtype, epilogue, num_sms, true, opts_from_env(), out);
 }
 
 void cdg_destroy(cdg_handle_t h)
@@ -700,6 +725,127 @@ int cdg_dgrad(cdg_handle_t h, const void *dY, const void *Wpacked, void *dX, con
     if (cdg_launch_dgrad(p, h->out_type, h->in_type, h->mask, h->grid, h->smem, static_cast<cudaStream_t>(stream)) !=
         cudaSuccess)
         return CDG_ERR_CUDA;
+    return CDG_OK;
+}
+
+// Plan-time autotuning: the planner's candidate configurations for this
+// shape, each timed on the caller's tensors; the fastest replaces the plan.
+int cdg_autotune(cdg_handle_t h, const void *dY, const void *Wpacked, void *dX, const void *relu_mask,
+                 cdg_stream_t stream, int reps, float *best_ms)
+{
+    if (!h || !dY || !Wpacked || !dX || reps < 1 || reps > 1000) return CDG_ERR_INVALID_ARG;
+    if (h->mask != (relu_mask != nullptr)) return CDG_ERR_INVALID_ARG;
+    if (h->host_only) return CDG_ERR_NO_DEVICE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    std::vector<PlanOpts> cands;
+    const PlanOpts base = h->opts;
+    cands.push_back(base);
+    auto variant = [&](int pair, int dual, int halo, int interleave, int max_bn) {
+        PlanOpts o = base;
+        if (pair != -2) o.pair = pair;
+        if (dual != -2) o.dual = dual;
+        if (halo != -2) o.halo = halo;
+        if (interleave != -2) o.interleave = interleave;
+        if (max_bn) o.max_bn = max_bn;
+        cands.push_back(o);
+    };
+    variant(0, -2, -2, -2, 0);    // no CTA pairs
+    variant(1, -2, -2, -2, 0);    // CTA pairs wherever BN >= 128
+    variant(-2, 0, -2, -2, 0);    // one MMA warp
+    variant(-2, -2, 0, -2, 0);    // no halo boxes
+    variant(-2, -2, 1, -2, 0);    // halo boxes wherever the geometry allows
+    variant(-2, -2, -2, 0, 0);    // phases one after another
+    variant(-2, -2, -2, -2, 128); // 128-channel N tiles
+    variant(1, -2, -2, -2, 128);
+    variant(-2, 0, -2, -2, 128);
+
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) {
+        if (e0) cudaEventDestroy(e0);
+        return CDG_ERR_CUDA;
+    }
+    // each timed launch follows a write of twice the L2 size, so every
+    // candidate starts with cold caches, as a layer inside a network step does
+    int l2 = 0;
+    size_t flush_bytes = 0;
+    void *flush = nullptr;
+    if (cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, h->device) == cudaSuccess && l2 > 0) {
+        flush_bytes = 2 * static_cast<size_t>(l2);
+        if (cudaMalloc(&flush, flush_bytes) != cudaSuccess) {
+            flush = nullptr;
+            cudaGetLastError();  // clear the failed allocation; time without flushing
+        }
+    }
+    // plans that come out identical are timed once
+    struct Sig {
+        int a_mode, pair, warps, bn, stages, box_w, box_h, box_n, interleave, tg, pdl;
+        bool operator==(const Sig &o) const { return std::memcmp(this, &o, sizeof *this) == 0; }
+    };
+    std::vector<Sig> seen;
+    cdg_plan_st *best = nullptr;
+    bool best_is_default = false;
+    float best_t = 0.0f;
+    int rc = CDG_OK;
+    for (const PlanOpts &o : cands) {
+        cdg_handle_t c = nullptr;
+        if (make_plan(h->N, h->H, h->W, h->C, h->K, h->R, h->S, h->stride, h->pad, h->dil, h->dtype, h->epi,
+                      h->num_sms, false, o, &c) != CDG_OK)
+            continue;
+        Sig sig;
+        std::memset(&sig, 0, sizeof sig);
+        sig = Sig{c->info.a_mode, c->info.cta_pair, c->info.mma_warps, c->info.tile_n, c->info.stages,
+                  c->info.box_w, c->info.box_h, c->info.box_n, c->prm.interleave, c->prm.halo_tg, c->prm.pdl};
+        if (std::find(seen.begin(), seen.end(), sig) != seen.end()) {
+            cdg_destroy(c);
+            continue;
+        }
+        seen.push_back(sig);
+        // one untimed launch (it also encodes the tensor maps), then reps timed
+        rc = cdg_dgrad(c, dY, Wpacked, dX, relu_mask, stream);
+        float ms = 0.0f;
+        for (int i = 0; rc == CDG_OK && i < reps; ++i) {
+            float one = 0.0f;
+            if (flush && cudaMemsetAsync(flush, i & 0xff, flush_bytes, s) != cudaSuccess) rc = CDG_ERR_CUDA;
+            if (rc == CDG_OK && cudaEventRecord(e0, s) != cudaSuccess) rc = CDG_ERR_CUDA;
+            if (rc == CDG_OK) rc = cdg_dgrad(c, dY, Wpacked, dX, relu_mask, stream);
+            if (rc == CDG_OK && (cudaEventRecord(e1, s) != cudaSuccess || cudaEventSynchronize(e1) != cudaSuccess ||
+                                 cudaEventElapsedTime(&one, e0, e1) != cudaSuccess))
+                rc = CDG_ERR_CUDA;
+            ms += one;
+        }
+        if (rc == CDG_OK) rc = cdg_device_status(c, stream);
+        if (rc != CDG_OK) {  // a failed launch or a device timeout ends the search
+            cdg_destroy(c);
+            break;
+        }
+        ms /= static_cast<float>(reps);
+        // the planner's own choice (the first candidate) is kept unless another
+        // is at least 2 % faster: closer timings are within launch-to-launch noise
+        const float margin = best_is_default ? 0.98f : 1.0f;
+        if (!best || ms < best_t * margin) {
+            if (best) cdg_destroy(best);
+            best_is_default = &o == &cands[0];
+            best = c;
+            best_t = ms;
+        } else {
+            cdg_destroy(c);
+        }
+    }
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    if (flush) cudaFree(flush);
+    if (rc != CDG_OK || !best) {
+        if (best) cdg_destroy(best);
+        return rc != CDG_OK ? rc : CDG_ERR_UNSUPPORTED;
+    }
+    // the handle takes the best plan (and keeps its own status word)
+    int *status = h->d_status;
+    *h = *best;
+    h->d_status = status;
+    h->info.tuned = 1;
+    cdg_destroy(best);
+    if (best_ms) *best_ms = best_t;
     return CDG_OK;
 }
 

@@ -131,6 +131,7 @@ typedef struct {
     int cta_pair;         /* 1: CTA pairs share 256-row tiles (2-SM MMA)            */
     int mma_warps;        /* MMA-issuing warps per CTA: 2 splits the work items and */
                           /* the pipeline stages between two issuers (N tile <= 128) */
+    int tuned;            /* 1 once cdg_autotune has chosen this plan              */
 } cdg_plan_info_t;
 
 int cdg_plan_get_info(cdg_handle_t h, cdg_plan_info_t *info);
@@ -161,6 +162,31 @@ int cdg_dgrad(cdg_handle_t h, const void *dY, const void *Wpacked, void *dX,
  * bounded wait (its dX is then incomplete).
  */
 int cdg_device_status(cdg_handle_t h, cdg_stream_t stream);
+
+/*
+ * Plan-time autotuning, in the manner of cuDNN's Find (the pages' comparison of
+ * cuDNN's Get and Find algorithm selection): run the dgrad of this plan's shape
+ * under each configuration the planner can produce for it (the planner's own
+ * choice; without or with CTA pairs; one MMA warp; with or without halo
+ * operand boxes; phases in order; 128-channel N tiles), reps timed launches
+ * each after one untimed launch, and keep the fastest in the handle
+ * (cdg_plan_get_info then reports it, with tuned = 1).  Configurations that
+ * come out identical are timed once.  Each timed launch follows a write of a
+ * scratch buffer twice the L2 size, so candidates are compared with cold
+ * caches, as layers run inside a network step.  The planner's own choice is
+ * kept unless another configuration is at least 2 % faster.
+ *
+ *   dY, Wpacked, dX, relu_mask   as for cdg_dgrad; dX is overwritten (with the
+ *                                correct result) many times
+ *   reps                         timed launches per configuration, 1..1000
+ *   best_ms                      if not NULL, receives the best mean launch time
+ *
+ * Synchronises stream.  Allocates a 4-byte status word per candidate plan and
+ * the flush buffer (all freed before returning).  On CDG_ERR_CUDA or
+ * CDG_ERR_TIMEOUT the handle keeps its previous plan.
+ */
+int cdg_autotune(cdg_handle_t h, const void *dY, const void *Wpacked, void *dX, const void *relu_mask,
+                 cdg_stream_t stream, int reps, float *best_ms);
 
 /* Static text for a status code. */
 const char *cdg_status_string(int status);

@@ -81,6 +81,21 @@ def test_host_plan_refuses_device_work():
     with pytest.raises(cdg.CdgError) as e:
         p.prepack_weights(16, 1024 * 1024)
     assert e.value.status == 7
+    with pytest.raises(cdg.CdgError) as e:
+        p.autotune(16, 16, 1024 * 1024)
+    assert e.value.status == 7
+    assert p.info()["tuned"] == 0
+
+
+@pytest.mark.parametrize("reps", [0, -1, 1001])
+def test_autotune_argument_errors(reps):
+    p = cdg.plan_host(1, 8, 8, 16, 16, 3, 3, 1, 1, 1, "f16")
+    with pytest.raises(cdg.CdgError) as e:
+        p.autotune(16, 16, 1024 * 1024, reps=reps)
+    assert e.value.status == 1
+    with pytest.raises(cdg.CdgError) as e:  # a gated plan needs the mask, an ungated one refuses it
+        p.autotune(16, 16, 1024 * 1024, relu_mask=4096)
+    assert e.value.status == 1
 
 
 def test_misaligned_and_aliased_pointers_rejected_before_launch():

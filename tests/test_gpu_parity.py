@@ -227,3 +227,20 @@ def test_planner_mode_overrides(L, env, monkeypatch):
         key, val = env.split("=")
         monkeypatch.setenv(key, val)
     check_layer(L)
+
+
+@pytest.mark.parametrize("L", [SWEEP[1], SWEEP[5], SWEEP[13], BATCH8[0]] + MODE_CASES, ids=lambda L: L.name)
+def test_autotuned_plan_matches_oracle(L):
+    """cdg_autotune times the planner's candidate configurations on the
+    caller's tensors and keeps the fastest: the dX it leaves and every later
+    call give the oracle's result."""
+    run = GpuRun(L)
+    best = run.plan.autotune(run.d_dY, run.d_Wp, run.out.ptr, run.d_x, reps=2)
+    assert best > 0 and run.plan.info()["tuned"] == 1
+    ref = oracle_full(run)
+    assert_close(run.result(), ref, run.odt, L.name + " (autotune output)")
+    assert run.out.guards_intact()
+    run.out.body().fill_(0xA5)  # garbage, then the tuned plan again
+    run.run()
+    assert_close(run.result(), ref, run.odt, L.name + " (tuned plan)")
+    assert run.status() == 0
