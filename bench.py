@@ -17,6 +17,11 @@ resident in HBM.  Prints one JSON line:
   cpu_baseline the CPU oracle on a bounded sample (first images of each layer)
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--gate none|x|bits] [--autotune 1] [--layers L01,...]
+
+--gate x|bits runs every layer with the fused ReLU-backward gate, reading the
+saved activation or its 1-bit packed mask; algorithmic bytes, the roofline and
+the end-to-end uploads then include that input.
 
 N > 1 (torchrun, one rank per GPU): every rank runs the full workload on its
 own GPU (replicas; dgrad has no exchange step), barrier + max over ranks.
@@ -80,9 +85,19 @@ def profiled_traffic(layer_name: str):
     return int(rec["dram_read_bytes"]) + int(rec["dram_write_bytes"])
 
 
-def roofline_time_s(layer, peaks):
+def gate_bytes(layer, gate: str) -> int:
+    """Algorithmic HBM bytes of one launch: dY + W + dX, plus the gate input
+    read once: the saved activation (2 B per dX element) or the packed mask
+    (one bit per dX element, each pixel's row padded to 16-byte units)."""
+    el = layer.N * layer.H * layer.W * layer.C
+    base = layer.bytes - (2 * el if layer.relu else 0)
+    mask = layer.N * layer.H * layer.W * 16 * ((layer.C + 127) // 128)
+    return base + {"none": 0, "x": 2 * el, "bits": mask}[gate]
+
+
+def roofline_time_s(layer, peaks, gate="none"):
     t_tc = layer.flops / (peaks["bf16_tflops_sustained"] * 1e12)
-    t_hbm = layer.bytes / (peaks["hbm_gbs"] * 1e9)
+    t_hbm = gate_bytes(layer, gate) / (peaks["hbm_gbs"] * 1e9)
     return max(t_tc, t_hbm), ("tensor" if t_tc >= t_hbm else "hbm")
 
 
@@ -228,12 +243,14 @@ class ClockSampler:
 
 
 def cpu_oracle_sample(layers, arrays, images: int):
-    """Time the CPU oracle on the first `images` images of every layer."""
+    """Time the CPU oracle on the first `images` images of every layer (gated
+    by the saved activation where the arrays carry one)."""
     import oracle
     t0 = time.perf_counter()
     flops = 0
     for L, (dY, W, x) in zip(layers, arrays):
-        oracle.dgrad(dY[:images], W, L.H, L.W, L.stride, L.pad, L.dil, x=None, dtype=L.dtype)
+        oracle.dgrad(dY[:images], W, L.H, L.W, L.stride, L.pad, L.dil,
+                     x=None if x is None else x[:images], dtype=L.dtype)
         flops += L.flops * images // L.N
     dt = time.perf_counter() - t0
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
@@ -300,6 +317,9 @@ def main():
     ap.add_argument("--layers", default="", help="comma-separated layer names (default: all 22)")
     ap.add_argument("--autotune", type=int, default=0,
                     help="1: tune every layer's plan with cdg_autotune during set-up (untimed)")
+    ap.add_argument("--gate", default="none", choices=["none", "x", "bits"],
+                    help="fused ReLU-backward gate on every layer: none; x = the saved bf16 activation; "
+                         "bits = its 1-bit packed mask (packed once at set-up, as a forward pass would store it)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -326,29 +346,44 @@ def main():
     layers = select_layers(args.layers)
 
     # ---- inputs (seeded, host), upload, plan, prepack
-    host, state = [], []
+    gate = args.gate
+    host, state, gates, h_gate = [], [], [], []
     with torch.cuda.stream(stream):
         for L in layers:
-            dY, W, _ = synth.make_inputs(L.shape(), L.dtype, L.dist, L.workload, L.index)
-            host.append((dY, W, None))
-            p = cdg.plan(L.N, L.H, L.W, L.C, L.K, L.R, L.S, L.stride, L.pad, L.dil, L.dtype)
+            dY, W, x = synth.make_inputs(L.shape(), L.dtype, L.dist, L.workload, L.index, with_x=(gate != "none"))
+            host.append((dY, W, x))
+            p = cdg.plan(L.N, L.H, L.W, L.C, L.K, L.R, L.S, L.stride, L.pad, L.dil, L.dtype,
+                         relu=(gate == "x"), relu_bits=(gate == "bits"))
             d_dY = torch.from_numpy(dY.view(np.int16)).to(dev)
             d_W = torch.from_numpy(W.view(np.int16)).to(dev)
             d_Wp = torch.empty(p.packed_weight_bytes // 2, dtype=torch.int16, device=dev)
             d_dX = torch.empty(L.N * L.H * L.W * L.C, dtype=torch.int16, device=dev)
             p.prepack_weights(d_W, d_Wp, stream)
             state.append((L, p, d_dY, d_Wp, d_dX))
+            if gate == "none":
+                gates.append(None)
+                continue
+            d_x = torch.from_numpy(x.reshape(-1).view(np.int16)).to(dev)
+            if gate == "x":
+                gates.append(d_x)
+            else:
+                pixels = L.N * L.H * L.W
+                d_bits = torch.empty(cdg.relu_mask_bytes(pixels, L.C), dtype=torch.uint8, device=dev)
+                cdg.pack_relu_mask(d_x, d_bits, pixels, L.C, L.dtype, stream)
+                gates.append(d_bits)
+                del d_x
+            h_gate.append(gates[-1].cpu().pin_memory())  # the gate input the end-to-end leg uploads
     torch.cuda.synchronize()
     tuned_ms = {}
     if args.autotune:
         # plan-time tuning (cuDNN-Find style), before and outside every timed region
         for (L, p, d_dY, d_Wp, d_dX) in state:
-            tuned_ms[L.name] = p.autotune(d_dY, d_Wp, d_dX, None, stream, reps=5)
+            tuned_ms[L.name] = p.autotune(d_dY, d_Wp, d_dX, gates[len(tuned_ms)], stream, reps=5)
         torch.cuda.synchronize()
 
     def step():
-        for (_, p, d_dY, d_Wp, d_dX) in state:
-            p.dgrad(d_dY, d_Wp, d_dX, None, stream)
+        for i, (_, p, d_dY, d_Wp, d_dX) in enumerate(state):
+            p.dgrad(d_dY, d_Wp, d_dX, gates[i], stream)
 
     def barrier():
         if world > 1:
@@ -374,7 +409,7 @@ def main():
         for k in range(steps):
             evs[k][0].record(stream)
             for i, (_, p, d_dY, d_Wp, d_dX) in enumerate(state):
-                p.dgrad(d_dY, d_Wp, d_dX, None, stream)
+                p.dgrad(d_dY, d_Wp, d_dX, gates[i], stream)
                 evs[k][i + 1].record(stream)
         torch.cuda.synchronize()
         ms = np.zeros(nL)
@@ -403,7 +438,7 @@ def main():
             for i, (_, p, d_dY, d_Wp, d_dX) in enumerate(state):
                 if i == dom:
                     dv0[k].record(stream)
-                p.dgrad(d_dY, d_Wp, d_dX, None, stream)
+                p.dgrad(d_dY, d_Wp, d_dX, gates[i], stream)
                 if i == dom:
                     dv1[k].record(stream)
             ev1[k].record(stream)
@@ -420,37 +455,38 @@ def main():
     per_layer = []
     for i, (L, p, *_r) in enumerate(state):
         t = per_layer_ms[i] * 1e-3
-        t_roof, bound = roofline_time_s(L, peaks)
+        t_roof, bound = roofline_time_s(L, peaks, gate)
         inf = p.info()
         per_layer.append({"layer": L.name, "ms": round(per_layer_ms[i], 5),
                           "plan": {"a_mode": inf["a_mode"], "cta_pair": inf["cta_pair"], "mma_warps": inf["mma_warps"],
                                    "tile_n": inf["tile_n"], "stages": inf["stages"], "tuned": inf["tuned"]},
                           "tflops": round(L.flops / t / 1e12, 2),
-                          "gbs": round(L.bytes / t / 1e9, 1), "bound": bound,
+                          "gbs": round(gate_bytes(L, gate) / t / 1e9, 1), "bound": bound,
                           "roofline_frac": round(t_roof / t, 4),
                           "tensor_peak_frac": round(L.flops / t / 1e12 / peaks["bf16_tflops_sustained"], 4)})
 
     # dominant launch: the layer with the largest share of the step, timed inside the timed region
     Ld = state[dom][0]
     td = dom_ms * 1e-3
-    _, bound = roofline_time_s(Ld, peaks)
+    _, bound = roofline_time_s(Ld, peaks, gate)
     if bound == "tensor":
         achieved, peak, unit = Ld.flops / td / 1e12, peaks["bf16_tflops_sustained"], "TFLOP/s"
     else:
-        achieved, peak, unit = Ld.bytes / td / 1e9, peaks["hbm_gbs"], "GB/s"
+        achieved, peak, unit = gate_bytes(Ld, gate) / td / 1e9, peaks["hbm_gbs"], "GB/s"
     roofline = {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
-                "frac": round(achieved / peak, 4), "traffic": profiled_traffic(Ld.name),
-                "algorithmic_bytes": Ld.bytes, "kernel": f"dgrad_kernel ({Ld.name})",
+                "frac": round(achieved / peak, 4),
+                "traffic": profiled_traffic(Ld.name) if gate == "none" else None,
+                "algorithmic_bytes": gate_bytes(Ld, gate), "kernel": f"dgrad_kernel ({Ld.name})",
                 "peak_source": peaks["source"] + (" sustained bf16" if bound == "tensor" else " copy bandwidth"),
                 "launch_ms": round(dom_ms, 5),
                 "share_of_step": round(dom_ms / ms_per_step, 4),
-                "step_roofline_frac": round(sum(roofline_time_s(L, peaks)[0] for (L, *_r) in state)
+                "step_roofline_frac": round(sum(roofline_time_s(L, peaks, gate)[0] for (L, *_r) in state)
                                             / (ms_per_step * 1e-3), 4)}
 
     # ---- end to end: dY from pinned host memory, dX back to pinned host memory, every step
     h_dY = [torch.from_numpy(h[0].view(np.int16)).pin_memory() for h in host]
     h_dX = [torch.empty(L.N * L.H * L.W * L.C, dtype=torch.int16).pin_memory() for (L, *_r) in state]
-    h2d = sum(t.numel() * 2 for t in h_dY)
+    h2d = sum(t.numel() * 2 for t in h_dY) + sum(t.numel() * t.element_size() for t in h_gate)
     d2h = sum(t.numel() * 2 for t in h_dX)
 
     # uploads, kernels and read-backs run on three streams: layer i's upload
@@ -469,10 +505,12 @@ def main():
             s_in.wait_event(ev_done[i])  # no-op before the event's first record
             with torch.cuda.stream(s_in):
                 d_dY.copy_(h_dY[i], non_blocking=True)
+                if h_gate:
+                    gates[i].copy_(h_gate[i], non_blocking=True)
             ev_in[i].record(s_in)
             stream.wait_event(ev_in[i])
             stream.wait_event(ev_out[i])
-            p.dgrad(d_dY, d_Wp, d_dX, None, stream)
+            p.dgrad(d_dY, d_Wp, d_dX, gates[i], stream)
             ev_done[i].record(stream)
             s_out.wait_event(ev_done[i])
             with torch.cuda.stream(s_out):
@@ -513,10 +551,11 @@ def main():
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "global_batch": 256 * world, "layers": nL,
+        "config": {"workload": WORKLOAD + {"none": "", "x": "_relu_bwd_x", "bits": "_relu_bwd_bits"}[gate],
+                   "global_batch": 256 * world, "layers": nL,
                    "l2": "inputs larger than L2: the step cycles ~5 GB of operands, so each layer's data is "
                          "evicted before its next use",
-                   "flops_per_step": flops_step, "parallelism": f"replicas x{world}",
+                   "flops_per_step": flops_step, "parallelism": f"replicas x{world}", "gate": gate,
                    "plans": "autotuned at set-up (cdg_autotune, 5 cold-cache launches per candidate)" if args.autotune
                    else "planner defaults"},
         "roofline": roofline,

@@ -25,15 +25,16 @@ OK = 0
 STATUS_NAMES = {0: "CDG_OK", 1: "CDG_ERR_INVALID_ARG", 2: "CDG_ERR_UNSUPPORTED", 3: "CDG_ERR_ALIGNMENT",
                 4: "CDG_ERR_ALIAS", 5: "CDG_ERR_CUDA", 6: "CDG_ERR_TIMEOUT", 7: "CDG_ERR_NO_DEVICE",
                 8: "CDG_ERR_SCRATCH_TOO_SMALL"}
+ERR_INVALID_ARG = 1
 ERR_SCRATCH_TOO_SMALL = 8
 NOALLOC_MAX_WEIGHT_BYTES = 8 << 20
 F16, BF16 = 0, 1
-EPI_RELU_BWD, EPI_OUT_F32 = 1, 2
+EPI_RELU_BWD, EPI_OUT_F32, EPI_RELU_BWD_BITS = 1, 2, 4
 DTYPES = {"f16": F16, "bf16": BF16}
 
 EXPORTS = ("cdg_plan", "cdg_plan_host", "cdg_destroy", "cdg_get_output_dims", "cdg_packed_weight_bytes",
            "cdg_plan_get_info", "cdg_prepack_weights", "cdg_dgrad", "cdg_device_status", "cdg_status_string",
-           "cdg_dgrad_noalloc", "cdg_autotune")
+           "cdg_dgrad_noalloc", "cdg_autotune", "cdg_pack_relu_mask", "cdg_relu_mask_bytes")
 
 
 class CdgError(RuntimeError):
@@ -98,6 +99,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.cdg_dgrad_noalloc.restype = i
     lib.cdg_autotune.argtypes = [hp, vp, vp, vp, vp, vp, i, ctypes.POINTER(ctypes.c_float)]
     lib.cdg_autotune.restype = i
+    lib.cdg_pack_relu_mask.argtypes = [vp, vp, ctypes.c_longlong, i, i, vp]
+    lib.cdg_pack_relu_mask.restype = i
+    lib.cdg_relu_mask_bytes.argtypes = [ctypes.c_longlong, i]
+    lib.cdg_relu_mask_bytes.restype = ctypes.c_longlong
     if path == LIB_PATH:
         _lib = lib
     return lib
@@ -136,13 +141,13 @@ class Plan:
     """One planned dgrad shape (a ``cdg_handle_t``)."""
 
     def __init__(self, N, H, W, C, K, R, S, stride=1, pad=0, dil=1, dtype="bf16", relu=False,
-                 out_f32=False, host_sms: int | None = None):
+                 out_f32=False, host_sms: int | None = None, relu_bits=False):
         self.lib = load_library()
         self.shape = dict(N=N, H=H, W=W, C=C, K=K, R=R, S=S, stride=stride, pad=pad, dil=dil)
         self.dtype = dtype
         self.relu = relu
         self.out_f32 = out_f32
-        epi = (EPI_RELU_BWD if relu else 0) | (EPI_OUT_F32 if out_f32 else 0)
+        epi = (EPI_RELU_BWD if relu else 0) | (EPI_OUT_F32 if out_f32 else 0) | (EPI_RELU_BWD_BITS if relu_bits else 0)
         h = ctypes.c_void_p()
         dt = DTYPES[dtype] if isinstance(dtype, str) else int(dtype)
         if host_sms is None:
@@ -221,10 +226,30 @@ class Plan:
         return int(self.lib.cdg_device_status(self.handle, _stream(stream)))
 
 
-def plan(N, H, W, C, K, R, S, stride=1, pad=0, dil=1, dtype="bf16", relu=False, out_f32=False) -> Plan:
-    return Plan(N, H, W, C, K, R, S, stride, pad, dil, dtype, relu, out_f32)
+def plan(N, H, W, C, K, R, S, stride=1, pad=0, dil=1, dtype="bf16", relu=False, out_f32=False,
+         relu_bits=False) -> Plan:
+    return Plan(N, H, W, C, K, R, S, stride, pad, dil, dtype, relu, out_f32, relu_bits=relu_bits)
+
+
+def relu_mask_bytes(pixels: int, C: int) -> int:
+    """Bytes of the packed ReLU mask of `pixels` pixels of C channels (cdg_relu_mask_bytes)."""
+    n = load_library().cdg_relu_mask_bytes(int(pixels), int(C))
+    if n < 0:
+        raise CdgError(ERR_INVALID_ARG, "cdg_relu_mask_bytes")
+    return n
+
+
+def pack_relu_mask(x, bits, pixels: int, C: int, dtype="bf16", stream=None) -> None:
+    """bits (relu_mask_bytes(pixels, C) bytes) = the packed mask (x > 0) of the
+    NHWC activation x, one bit per element in 16-byte units per pixel
+    (cdg_pack_relu_mask), for plans made with relu_bits=True."""
+    lib = load_library()
+    dt = DTYPES[dtype] if isinstance(dtype, str) else int(dtype)
+    rc = lib.cdg_pack_relu_mask(_addr(x), _addr(bits), int(pixels), int(C), dt, _stream(stream))
+    if rc != OK:
+        raise CdgError(rc, "cdg_pack_relu_mask")
 
 
 def plan_host(N, H, W, C, K, R, S, stride=1, pad=0, dil=1, dtype="bf16", relu=False, out_f32=False,
-              num_sms=148) -> Plan:
-    return Plan(N, H, W, C, K, R, S, stride, pad, dil, dtype, relu, out_f32, host_sms=num_sms)
+              num_sms=148, relu_bits=False) -> Plan:
+    return Plan(N, H, W, C, K, R, S, stride, pad, dil, dtype, relu, out_f32, host_sms=num_sms, relu_bits=relu_bits)

@@ -84,13 +84,15 @@ struct cdg_plan_st {
     int device;
     int num_sms;
     int out_type, in_type;
-    bool mask;
+    bool mask;       // gated epilogue (x or packed bits)
+    bool mask_bits;  // the gate reads a packed bit mask
     size_t smem;
     int grid;
     int *d_status;
     CdgParams prm;  // tensor maps and pointers are filled per call
     const void *cached_dY, *cached_Wp;
     void *cached_dX;
+    const void *cached_mask;
     cdg_plan_info_t info;
 };
 
@@ -132,12 +134,12 @@ void choose_box(const std::vector<CdgPhase> &phases, int N, int &bw, int &bh, in
 // granule).  C > 256: several tiles, each a multiple of 64 so that the
 // epilogue's 64-channel store boxes never reach into the neighbouring tile;
 // least padding wins, larger tiles on ties.
-int choose_bn(int C, int max_bn)
+int choose_bn(int C, int max_bn, int step)
 {
     if (C <= max_bn) return ((C + 15) / 16) * 16;
     int best = max_bn;
     long long best_waste = -1;
-    for (int bn = max_bn; bn >= 64; bn -= 64) {
+    for (int bn = max_bn; bn >= step; bn -= step) {
         const long long waste = 1LL * ceil_div(C, bn) * bn - C;
         if (best_waste < 0 || waste < best_waste) {
             best_waste = waste;
@@ -173,7 +175,8 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     if (N < 1 || H < 1 || W < 1 || C < 1 || K < 1 || R < 1 || S < 1 || stride < 1 || pad < 0 || dil < 1)
         return CDG_ERR_INVALID_ARG;
     if (dtype != CDG_F16 && dtype != CDG_BF16) return CDG_ERR_INVALID_ARG;
-    if (epilogue & ~(CDG_EPI_RELU_BWD | CDG_EPI_OUT_F32)) return CDG_ERR_INVALID_ARG;
+    if (epilogue & ~(CDG_EPI_RELU_BWD | CDG_EPI_OUT_F32 | CDG_EPI_RELU_BWD_BITS)) return CDG_ERR_INVALID_ARG;
+    if ((epilogue & CDG_EPI_RELU_BWD) && (epilogue & CDG_EPI_RELU_BWD_BITS)) return CDG_ERR_INVALID_ARG;
     const long long spanH = 1LL * H + 2LL * pad - 1LL * dil * (R - 1) - 1;
     const long long spanW = 1LL * W + 2LL * pad - 1LL * dil * (S - 1) - 1;
     if (spanH < 0 || spanW < 0) return CDG_ERR_INVALID_ARG;
@@ -197,7 +200,8 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     h->opts = opt;
     h->in_type = dtype == CDG_F16 ? CDG_T_F16 : CDG_T_BF16;
     h->out_type = (epilogue & CDG_EPI_OUT_F32) ? CDG_T_F32 : h->in_type;
-    h->mask = (epilogue & CDG_EPI_RELU_BWD) != 0;
+    h->mask = (epilogue & (CDG_EPI_RELU_BWD | CDG_EPI_RELU_BWD_BITS)) != 0;
+    h->mask_bits = (epilogue & CDG_EPI_RELU_BWD_BITS) != 0;
 
     // ---- phases and their taps
     std::vector<CdgPhase> phases;
@@ -265,10 +269,14 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     int bw = 0, bh = 0, bnb = 0;
     if (!flat) choose_box(phases, N, bw, bh, bnb);
     // N tile: all of C up to 256 channels, else the multiple of 64 up to 256
-    // with the least padding (max_bn 128 caps it at 128)
-    const int BN = choose_bn(C, opt.max_bn == 128 ? 128 : 256);
+    // with the least padding (max_bn 128 caps it at 128).  With the packed mask
+    // a tile's mask bytes must start on a 16-byte unit: multiples of 128.
+    const int BN = choose_bn(C, opt.max_bn == 128 ? 128 : 256, h->mask_bits ? 128 : 64);
     const int tiles_n = ceil_div(C, BN);
-    const int ring_budget = kMaxSmem - 1024 - CDG_SMEM_STAGING - CDG_SMEM_TAIL;
+    // output staging; gated by the activation: four buffers, its chunks land in
+    // them ahead of use; by the packed mask: a ring of mask tiles besides
+    const int staging = CDG_SMEM_STAGING + (h->mask ? (h->mask_bits ? CDG_GATE_RING : CDG_SMEM_STAGING) : 0);
+    const int ring_budget = kMaxSmem - 1024 - staging - CDG_SMEM_TAIL;
 
     // ---- halo operand mode: a tile is halo_bh full-width rows of one image's
     // phase sub-grid; one TMA box of (width + tap span) x (rows + tap span)
@@ -448,6 +456,15 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     // Programmatic dependent launch: the kernel's set-up overlaps the end of the
     // previous kernel in the stream ("0" turns it off).
     p.pdl = opt.pdl == 0 ? 0 : 1;
+    p.mask_bits = h->mask_bits ? 1 : 0;
+    // gate loads take the dX store box: its rows x the activation chunk's bytes
+    // (64 channels; 32 with fp32 output) or the item's mask bytes per row
+    {
+        const int box_rows = d_mode == CDG_D_BOX4 ? bw * bh * bnb : m_step;
+        const int mask_row = tiles_n == 1 ? 16 * ceil_div(C, 128) : BN / 8;
+        p.gate_row_bytes = h->mask_bits ? mask_row : (h->out_type == CDG_T_F32 ? 64 : 128);
+        p.gate_tx = h->mask ? static_cast<uint32_t>(box_rows * p.gate_row_bytes) : 0u;
+    }
     p.dual = dual ? 1 : 0;
     // phases with taps (sorted first) of equal item counts are interleaved item
     // by item, so that their tiles over the same dY run close together (a
@@ -466,7 +483,7 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     for (size_t i = 0; i < phases.size(); ++i) p.phase[i] = phases[i];
     for (size_t i = 0; i < taps.size(); ++i) p.tap[i] = taps[i];
 
-    h->smem = static_cast<size_t>(1024 + ring_bytes + CDG_SMEM_STAGING + CDG_SMEM_TAIL);
+    h->smem = static_cast<size_t>(1024 + ring_bytes + staging + CDG_SMEM_TAIL);
     h->grid = pair ? 2 * std::max(1, std::min(num_sms / 2, items)) : std::max(1, std::min(num_sms, items));
 
     auto set_round = [&]() {
@@ -530,6 +547,16 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb)
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Bytes of a packed mask row: a pixel's C bits in whole 16-byte units.
+long long mask_row_bytes(int C) { return 16LL * ((C + 127) / 128); }
+
+// Bytes of the gate's input: x (2 bytes per element) or the packed mask.
+size_t mask_bytes(const cdg_plan_st *h)
+{
+    const size_t pixels = static_cast<size_t>(h->N) * h->H * h->W;
+    return h->mask_bits ? pixels * mask_row_bytes(h->C) : 2 * pixels * h->C;
+}
 
 CUtensorMapDataType tmap_type(int dtype)
 {
@@ -624,6 +651,59 @@ int encode_store_maps(cdg_plan_st *h, void *dX)
     return CDG_OK;
 }
 
+// Gate load maps: the dX store maps' geometry over the saved activation (the
+// input type; 64-channel boxes with the staging's 128-byte swizzle, or plain
+// 32-channel boxes of 64-byte rows for fp32 output) or over the packed mask
+// (bytes; rows of mask_row_bytes(C) per pixel; boxes of gate_row_bytes).
+// Phases without taps need none.
+int encode_gate_maps(cdg_plan_st *h, const void *gate)
+{
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return CDG_ERR_CUDA;
+    CdgParams &p = h->prm;
+    const cuuint32_t ones[4] = {1, 1, 1, 1};
+    const bool bits = h->mask_bits;
+    const cuuint64_t esz = bits ? 1 : 2;
+    const cuuint64_t row = bits ? static_cast<cuuint64_t>(mask_row_bytes(h->C)) : static_cast<cuuint64_t>(h->C);
+    const cuuint32_t inner = static_cast<cuuint32_t>(bits ? p.gate_row_bytes : p.gate_row_bytes / 2);
+    const CUtensorMapDataType dt = bits ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : tmap_type(h->dtype);
+    const CUtensorMapSwizzle sw =
+        (!bits && h->out_type != CDG_T_F32) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
+    const cuuint64_t W = h->W, H = h->H, s = h->stride;
+    char *base0 = static_cast<char *>(const_cast<void *>(gate));
+    for (int i = 0; i < p.nphases; ++i) {
+        const CdgPhase &f = p.phase[i];
+        if (f.tap_count == 0) continue;
+        CUresult r;
+        if (p.d_mode == CDG_D_BOX4) {
+            char *base = base0 + (static_cast<cuuint64_t>(f.ph) * W + f.pw) * row * esz;
+            const cuuint64_t dims[4] = {row, static_cast<cuuint64_t>(f.wph), static_cast<cuuint64_t>(f.hph),
+                                        static_cast<cuuint64_t>(h->N)};
+            const cuuint64_t strides[3] = {s * row * esz, s * W * row * esz, H * W * row * esz};
+            const cuuint32_t box[4] = {inner, static_cast<cuuint32_t>(p.box_w), static_cast<cuuint32_t>(p.box_h),
+                                       static_cast<cuuint32_t>(p.box_n)};
+            r = enc(&p.tmG[i], dt, 4, base, dims, strides, box, ones, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        } else if (p.d_mode == CDG_D_LINEAR) {
+            const cuuint64_t dims[2] = {row, static_cast<cuuint64_t>(h->N) * H * W};
+            const cuuint64_t strides[1] = {row * esz};
+            const cuuint32_t box[2] = {inner, CDG_BM};
+            r = enc(&p.tmG[i], dt, 2, base0, dims, strides, box, ones, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        } else {
+            const cuuint64_t dims[3] = {row, static_cast<cuuint64_t>(f.wph),
+                                        static_cast<cuuint64_t>(h->N) * static_cast<cuuint64_t>(f.hph)};
+            const cuuint64_t strides[2] = {s * row * esz, s * W * row * esz};
+            const cuuint32_t box[3] = {inner, static_cast<cuuint32_t>(f.wph), static_cast<cuuint32_t>(p.rows_per_tile)};
+            r = enc(&p.tmG[i], dt, 3, base0, dims, strides, box, ones, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        }
+        if (r != CUDA_SUCCESS) return CDG_ERR_CUDA;
+    }
+    h->cached_mask = gate;
+    return CDG_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -706,9 +786,8 @@ int cdg_dgrad(cdg_handle_t h, const void *dY, const void *Wpacked, void *dX, con
         return CDG_ERR_ALIGNMENT;
     const size_t dx_bytes = static_cast<size_t>(h->N) * h->H * h->W * h->C * (h->out_type == CDG_T_F32 ? 4 : 2);
     const size_t dy_bytes = static_cast<size_t>(h->N) * h->P * h->Q * h->K * 2;
-    const size_t x_bytes = static_cast<size_t>(h->N) * h->H * h->W * h->C * 2;
     if (overlaps(dX, dx_bytes, dY, dy_bytes) || overlaps(dX, dx_bytes, Wpacked, cdg_packed_weight_bytes(h)) ||
-        (relu_mask && overlaps(dX, dx_bytes, relu_mask, x_bytes)))
+        (relu_mask && overlaps(dX, dx_bytes, relu_mask, mask_bytes(h))))
         return CDG_ERR_ALIAS;
     if (dY != h->cached_dY || Wpacked != h->cached_Wp) {
         const int rc = encode_operand_maps(h, dY, Wpacked);
@@ -716,6 +795,10 @@ int cdg_dgrad(cdg_handle_t h, const void *dY, const void *Wpacked, void *dX, con
     }
     if (dX != h->cached_dX) {
         const int rc = encode_store_maps(h, dX);
+        if (rc != CDG_OK) return rc;
+    }
+    if (relu_mask && relu_mask != h->cached_mask) {
+        const int rc = encode_gate_maps(h, relu_mask);
         if (rc != CDG_OK) return rc;
     }
     CdgParams &p = h->prm;
@@ -865,6 +948,25 @@ int cdg_device_status(cdg_handle_t h, cdg_stream_t stream)
     return v;
 }
 
+long long cdg_relu_mask_bytes(long long pixels, int C)
+{
+    if (pixels < 0 || C <= 0 || C % 8 != 0) return -1;
+    return pixels * mask_row_bytes(C);
+}
+
+int cdg_pack_relu_mask(const void *x, void *bits, long long pixels, int C, int dtype, cdg_stream_t stream)
+{
+    if (!x || !bits || pixels < 0 || C <= 0 || C % 8 != 0) return CDG_ERR_INVALID_ARG;
+    if (dtype != CDG_F16 && dtype != CDG_BF16) return CDG_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(bits)) return CDG_ERR_ALIGNMENT;
+    if (overlaps(x, static_cast<size_t>(pixels) * C * 2, bits, static_cast<size_t>(pixels * mask_row_bytes(C))))
+        return CDG_ERR_ALIAS;
+    if (cdg_launch_pack_mask(x, bits, pixels, C, dtype == CDG_F16 ? CDG_T_F16 : CDG_T_BF16,
+                             static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return CDG_ERR_CUDA;
+    return CDG_OK;
+}
+
 const char *cdg_status_string(int status)
 {
     switch (status) {
@@ -932,9 +1034,8 @@ extern "C" int cdg_dgrad_noalloc(cdg_handle_t h, const void *dY, const void *W_k
         return CDG_ERR_ALIGNMENT;
     const size_t dx_bytes = static_cast<size_t>(h->N) * h->H * h->W * h->C * (h->out_type == CDG_T_F32 ? 4 : 2);
     const size_t dy_bytes = static_cast<size_t>(h->N) * h->P * h->Q * h->K * 2;
-    const size_t x_bytes = static_cast<size_t>(h->N) * h->H * h->W * h->C * 2;
     if (overlaps(dX, dx_bytes, dY, dy_bytes) || overlaps(dX, dx_bytes, W_krsc, wbytes) ||
-        (relu_mask && overlaps(dX, dx_bytes, relu_mask, x_bytes)))
+        (relu_mask && overlaps(dX, dx_bytes, relu_mask, mask_bytes(h))))
         return CDG_ERR_ALIAS;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return CDG_ERR_CUDA;
@@ -954,6 +1055,10 @@ extern "C" int cdg_dgrad_noalloc(cdg_handle_t h, const void *dY, const void *W_k
     }
     if (dX != h->cached_dX) {
         const int e = encode_store_maps(h, dX);
+        if (e != CDG_OK) return e;
+    }
+    if (relu_mask && relu_mask != h->cached_mask) {
+        const int e = encode_gate_maps(h, relu_mask);
         if (e != CDG_OK) return e;
     }
     CdgParams &p = h->prm;

@@ -21,9 +21,13 @@
 #define CDG_EPI_WARP0 4
 #define CDG_WAIT_LIMIT_NS 4000000000ull  // a pipeline wait gives up after 4 s
 // Shared memory after the operand ring: two 16 KB output staging buffers
-// (128 rows x 128 B, the box a TMA store writes), then mbarriers and flags
+// (128 rows x 128 B, the box a TMA store writes; four when the ReLU-backward
+// gate reads the saved activation, whose chunks land in them ahead of use; two
+// plus a 16 KB ring of mask tiles when it reads the packed mask), then mbarriers and flags
 // (320 B), then the phase and tap tables copied out of the parameter block.
 #define CDG_SMEM_STAGING (2 * 128 * 128)
+#define CDG_GATE_SLOT 4096   // one item's packed-mask tile: 128 rows x up to 32 bytes
+#define CDG_GATE_RING (4 * CDG_GATE_SLOT)
 #define CDG_SMEM_TAIL 2048
 #define CDG_SMEM_TABLES 320
 #define CDG_MAX_STAGES_TOTAL 10  // all ring stages together (their mbarriers live in the 320-byte area)
@@ -60,6 +64,7 @@ struct CdgParams {  // CUtensorMap members carry their own (128-byte) alignment
     CUtensorMap tmA;  // dY: 4-D {K, Q, P, N} halo boxes, or 2-D {K, N*P*Q} rows
     CUtensorMap tmB;  // packed weights: 3-D {K, C, R*S}
     CUtensorMap tmD[CDG_MAX_PHASES];  // dX stores, one map per phase (index = phase slot)
+    CUtensorMap tmG[CDG_MAX_PHASES];  // gate loads (saved activation or packed mask) in the stores' geometry
     void *dX;
     const void *mask;
     int *status;
@@ -70,6 +75,9 @@ struct CdgParams {  // CUtensorMap members carry their own (128-byte) alignment
     int halo;             // 1: one dY halo box per (tile, K block) serves every tap (see dgrad_sm103.cu)
     int pair;             // 1: CTA pairs (clusters of 2) share 256-row tiles through 2-SM MMAs
     int pdl;              // 1: launch with programmatic stream serialization (host side only)
+    int mask_bits;        // 1: the gate reads the packed bit mask (rows of 16-byte units per pixel), not x
+    int gate_row_bytes;   // bytes of one tile row of a gate load (activation chunk, or mask tile)
+    uint32_t gate_tx;     // bytes one gate load delivers (the store box's rows x gate_row_bytes)
     int dual;             // 1: two MMA warps, each with half of the stages and two accumulators
     int interleave;       // >= 2: the first `interleave` phases' items are interleaved (il_items each)
     int il_items;
@@ -97,6 +105,8 @@ struct CdgParams {  // CUtensorMap members carry their own (128-byte) alignment
 enum { CDG_T_F16 = 0, CDG_T_BF16 = 1, CDG_T_F32 = 2 };
 
 // Launchers implemented in dgrad_sm103.cu.
+cudaError_t cdg_launch_pack_mask(const void *x, void *bits, long long pixels, int C, int in_type,
+                                 cudaStream_t stream);
 cudaError_t cdg_launch_dgrad(const CdgParams &p, int out_type, int in_type, bool mask,
                              int grid, size_t smem, cudaStream_t stream);
 cudaError_t cdg_prepare_dgrad(int out_type, int in_type, bool mask, size_t smem);

@@ -146,9 +146,11 @@ struct Ring {
     uint32_t stage_bytes;  // A tile + B tile (halo mode: one halo box stage)
     uint32_t b0;           // halo mode: first weight stage
     uint32_t b_bytes;      // halo mode: bytes of one weight stage
-    uint32_t out0;         // first of the two 16 KB output staging buffers
+    uint32_t out0;         // first of the 16 KB output staging buffers (two; four when gated by the activation)
     uint32_t full0, empty0;
     uint32_t acc_full0, acc_empty0, drain;
+    uint32_t gfull0;       // gate loads: four mbarriers
+    uint32_t gate0;        // packed-mask ring (four CDG_GATE_SLOT slots)
 };
 
 // ------------------------------------------------------------------ loaders
@@ -555,22 +557,72 @@ __device__ __forceinline__ uint32_t pack2(float a, float b, int out_t)
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-// ReLU-backward gate on PER (8 or 4) consecutive channels: v = (x > 0) ? v : +0.0.
-template <int IN_T, int PER>
-__device__ __forceinline__ void gate(float *v, const uint16_t *x)
+__device__ __forceinline__ void ld_shared_v2(uint32_t addr, uint32_t (&v)[2])
 {
-    uint32_t w[PER / 2];
-    if constexpr (PER == 8) {
-        const uint4 u = __ldg(reinterpret_cast<const uint4 *>(x));
-        w[0] = u.x;
-        w[1] = u.y;
-        w[2] = u.z;
-        w[3] = u.w;
-    } else {
-        const uint2 u = __ldg(reinterpret_cast<const uint2 *>(x));
-        w[0] = u.x;
-        w[1] = u.y;
+    asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v[0]), "=r"(v[1]) : "r"(addr) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t (&v)[4])
+{
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+                 : "r"(addr)
+                 : "memory");
+}
+
+// The gate's lookahead: a position in this CTA's sequence of gate loads, one
+// per output chunk (CH channels of a work item with taps: saved activation) or
+// one per such item (packed mask).  Items without taps come after all items
+// with taps in every CTA's walk (the planner sorts those phases last and
+// interleaves only phases with taps), so the sequence ends at the first one.
+struct GateCursor {
+    ItemWalk w;
+    int cc;  // channel offset of the chunk within the item's N tile
+    __device__ __forceinline__ bool valid() const { return w.valid() && w.tab[w.phase].tap_count > 0; }
+    __device__ __forceinline__ void next(int step, int BN)
+    {
+        cc += step;
+        if (cc >= BN) {
+            cc = 0;
+            w.next();
+        }
     }
+};
+
+// Issue the TMA load of the cursor's gate tile: the dX store box of that chunk
+// or item, read from the saved activation (the chunk's channels, laid out as
+// the chunk's output staging) or from the packed mask (the item's bytes of each
+// pixel row).  Completion lands on `bar` (expecting p.gate_tx bytes).
+__device__ __forceinline__ void gate_issue(const CdgParams &p, const GateCursor &gc, const Sched &S, uint32_t dst,
+                                           uint32_t bar)
+{
+    const CdgPhase &ph = gc.w.tab[gc.w.phase];
+    const int mt = S.m_tile(gc.w.local, p.tiles_n);
+    const int nt = gc.w.local - (p.tiles_n == 1 ? gc.w.local : gc.w.local / p.tiles_n) * p.tiles_n;
+    const int x0 = p.mask_bits ? (p.tiles_n == 1 ? 0 : nt * (p.BN / 8)) : nt * p.BN + gc.cc;
+    const uint64_t map = reinterpret_cast<uint64_t>(&p.tmG[gc.w.phase]);
+    mbar_arrive_expect_tx(bar, p.gate_tx);
+    if (p.d_mode == CDG_D_BOX4) {
+        int j0, i0, n0;
+        box_origin(ph, mt, max(p.box_w, 1), max(p.box_h, 1), max(p.box_n, 1), j0, i0, n0);
+        tma_load_4d(dst, map, bar, x0, j0, i0, n0);
+    } else if (p.d_mode == CDG_D_LINEAR) {
+        tma_load_2d(dst, map, bar, x0, mt * p.m_step);
+    } else {
+        tma_load_3d(dst, map, bar, x0, 0, mt * p.rows_per_tile);
+    }
+}
+
+// ReLU-backward gate on PER consecutive values: v = (x > 0) ? v : +0.0 (a
+// select, so masked outputs are +0.0 whatever the accumulator holds).
+template <int IN_T, int PER>
+__device__ __forceinline__ void gate_x(float *v, const uint32_t *w)
+{
 #pragma unroll
     for (int e = 0; e < PER / 2; ++e) {
         if (!(gate_value<IN_T>(static_cast<uint16_t>(w[e] & 0xFFFFu)) > 0.0f)) v[2 * e] = 0.0f;
@@ -578,12 +630,12 @@ __device__ __forceinline__ void gate(float *v, const uint16_t *x)
     }
 }
 
-// dX pixel index (n*H + h)*W + w of a sub-grid position of a phase, or -1.
-__device__ __forceinline__ long long phase_pixel(const CdgPhase &ph, int n, int i, int j, int N, int H, int W,
-                                                 int stride)
+template <int PER>
+__device__ __forceinline__ void gate_mask(float *v, uint32_t bits)
 {
-    if (n >= N || i >= ph.hph || j >= ph.wph) return -1;
-    return (static_cast<long long>(n) * H + (stride * i + ph.ph)) * W + (stride * j + ph.pw);
+#pragma unroll
+    for (int e = 0; e < PER; ++e)
+        if (!((bits >> e) & 1u)) v[e] = 0.0f;
 }
 
 template <int OUT_T, bool MASK, int IN_T, bool HALO, bool PAIR, bool DUAL>
@@ -597,12 +649,14 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
     const int quad = warp & 3;  // this warp may read TMEM lanes [32*quad, 32*quad + 32)
     const int row = quad * 32 + lane;
     const int ew = warp - CDG_EPI_WARP0;  // epilogue warp 0..3
-    const int tiles_n = p.tiles_n, BN = p.BN, C = p.C, N = p.N, H = p.H, W = p.W, stride = p.stride;
+    const int tiles_n = p.tiles_n, BN = p.BN, C = p.C;
     // box dims are 0 in the linear operand modes; keep the divisions defined
     const int bw = max(p.box_w, 1), bh = max(p.box_h, 1), bn = max(p.box_n, 1);
     const int d_mode = p.d_mode, m_step = p.m_step, rpt = max(p.rows_per_tile, 1);
     const uint32_t acc_stride = p.acc_stride;
-    const uint16_t *const xg = static_cast<const uint16_t *>(p.mask);
+    const bool mask_bits = p.mask_bits != 0;
+    // staging buffers: four when the activation's chunks land in them two chunks ahead
+    const uint32_t nbuf = (MASK && !mask_bits) ? 4u : 2u;
     // tile row -> box position, and the staging row it fills (halo mode: row
     // a*halo_wb + b is output (a, b); padding rows b >= halo_wt are dropped)
     int jl, il, nl, srow;
@@ -629,6 +683,31 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
     // between two MMA warps, each with two accumulators of its own)
     uint32_t acc_count[2] = {0u, 0u}, chunk_count = 0;
     uint32_t item_index = 0;
+    // Gate inputs arrive by TMA ahead of use: chunk k's activation tile into
+    // staging buffer k % 4 while chunk k - 2 is processed; the mask tile of the
+    // i-th item with taps into ring slot i % 4 three items ahead.  Load n
+    // completes on gate barrier n % 4 (phase n / 4) and is issued by epilogue
+    // warp n % 4 (an issue holds its thread for a few hundred cycles, so one
+    // warp issuing them all would pace the epilogue); every epilogue thread
+    // walks the cursor in step.  For chunk k + 2 that is warp (k - 2) % 4, which
+    // has just seen store k - 2 finish reading the same buffer.
+    GateCursor gc{ItemWalk(tab, p.nphases, S.start, S.step, p.interleave, p.il_items, p.il_round), 0};
+    const int gstep = mask_bits ? BN : CH;
+    const uint32_t gring = mask_bits ? R.gate0 : R.out0;
+    const uint32_t gslot = mask_bits ? static_cast<uint32_t>(CDG_GATE_SLOT) : 128u * 128u;
+    const uint32_t grow = static_cast<uint32_t>(p.gate_row_bytes);
+    uint32_t g_issued = 0, g_used = 0;  // gate loads issued and waited for (the same count in every thread)
+    uint32_t gated_items = 0;
+    auto gate_ahead = [&]() {
+        if (!gc.valid()) return;
+        const uint32_t n = g_issued++;
+        if (elected && static_cast<uint32_t>(ew) == (n & 3u))
+            gate_issue(p, gc, S, gring + (n & 3u) * gslot, R.gfull0 + 8u * (n & 3u));
+        gc.next(gstep, BN);
+    };
+    if (MASK)
+        for (int j = 0; j < (mask_bits ? 3 : 2); ++j) gate_ahead();
+    bool ok = true;
     for (ItemWalk w(tab, p.nphases, S.start, S.step, p.interleave, p.il_items, p.il_round); w.valid(); w.next(), ++item_index) {
         const CdgPhase &ph = tab[w.phase];
         const int mt = S.m_tile(w.local, tiles_n);
@@ -667,20 +746,16 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
             named_bar_sync(1, 128);
             zero_ready = false;
         }
-        // tile origin in the store map's coordinates, and (for the gate) this row's pixel
+        // tile origin in the store map's coordinates
         int j0 = 0, i0 = 0, n0 = 0;
-        long long pix = -1;
-        if (d_mode == CDG_D_BOX4) {
-            box_origin(ph, mt, bw, bh, bn, j0, i0, n0);
-            if (MASK && nl < bn) pix = phase_pixel(ph, n0 + nl, i0 + il, j0 + jl, N, H, W, stride);
-        } else if (MASK) {
-            const long long m = static_cast<long long>(mt) * m_step + row;
-            const long long plane = static_cast<long long>(ph.hph) * ph.wph;
-            if (row < m_step && m < plane * N) {
-                const int n = static_cast<int>(m / plane);
-                const int rem = static_cast<int>(m - plane * n);
-                pix = phase_pixel(ph, n, rem / ph.wph, rem % ph.wph, N, H, W, stride);
-            }
+        if (d_mode == CDG_D_BOX4) box_origin(ph, mt, bw, bh, bn, j0, i0, n0);
+        uint32_t mrow = 0;  // packed mask: this row's bytes in the item's mask tile
+        if (MASK && mask_bits) {
+            gate_ahead();  // into the slot the previous item's tile has left
+            const uint32_t n = gated_items++;
+            if (!wait_bar(R.gfull0 + 8u * (n & 3u), (n >> 2) & 1u, ctl)) break;
+            ++g_used;
+            mrow = R.gate0 + (n & 3u) * static_cast<uint32_t>(CDG_GATE_SLOT) + static_cast<uint32_t>(max(srow, 0)) * grow;
         }
 
         const uint32_t issuer = DUAL ? (item_index & 1u) : 0u;
@@ -692,11 +767,38 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
         const uint32_t taddr = tmem_base + acc * acc_stride + (static_cast<uint32_t>(quad * 32) << 16);
         for (int cc = 0; cc < BN; cc += CH) {
             const uint32_t k = chunk_count++;
-            const uint32_t buf = R.out0 + (k & 1u) * (128u * 128u);
-            // the store that last read this buffer (chunk k-2, issued by warp
-            // (k-2) % 4) must be done with it
+            const uint32_t buf = R.out0 + (k & (nbuf - 1u)) * (128u * 128u);
+            // the store of chunk k-2 (issued by warp (k-2) % 4) must be done
+            // reading its buffer: with two buffers that is this chunk's, with
+            // four it is the one chunk k+2's gate goes into
             if (k >= 2 && elected && static_cast<uint32_t>(ew) == ((k - 2) & 3u)) bulk_wait_group_read<0>();
             named_bar_sync(1, 128);
+            uint32_t gw[2] = {0u, 0u};  // packed mask: the chunk's bits 0-31 and 32-63
+            uint32_t xf[OSZ == 4 ? 16 : 1];  // fp32 output: the chunk's 32 activation values
+            if (MASK && mask_bits && srow >= 0) {
+                if (OSZ == 2) {
+                    ld_shared_v2(mrow + static_cast<uint32_t>(cc >> 3), gw);
+                } else {
+                    gw[0] = ld_shared_u32(mrow + static_cast<uint32_t>(cc >> 3));
+                }
+            } else if (MASK && !mask_bits) {
+                gate_ahead();  // chunk k + 2 into the buffer store k - 2 has finished reading
+                if (!wait_bar(R.gfull0 + 8u * (k & 3u), (k >> 2) & 1u, ctl)) {
+                    ok = false;
+                    break;
+                }
+                ++g_used;
+                if (OSZ == 4) {
+                    // fp32 output: the activation tile holds 64-byte rows; read this
+                    // row before any thread writes the wider output over the buffer
+                    if (srow >= 0)
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            ld_shared_v4(buf + static_cast<uint32_t>(srow) * 64u + 16u * q,
+                                         *reinterpret_cast<uint32_t(*)[4]>(&xf[(4 * q) % (OSZ == 4 ? 16 : 1)]));
+                    named_bar_sync(1, 128);
+                }
+            }
             uint32_t r[CH];
 #pragma unroll
             for (int q = 0; q < CH / 16; ++q)
@@ -718,9 +820,16 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
                 float v[PER];
 #pragma unroll
                 for (int e = 0; e < PER; ++e) v[e] = __uint_as_float(r[PER * q + e]);
-                if (MASK) {
-                    const int c = c_begin + cc + PER * q;
-                    if (pix >= 0 && c < c_end) gate<IN_T, PER>(v, xg + pix * C + c);
+                if (MASK && srow >= 0) {
+                    if (mask_bits) {
+                        gate_mask<PER>(v, gw[(PER * q) >> 5] >> ((PER * q) & 31));
+                    } else if (OSZ == 2) {  // x piece q sits where output piece q goes
+                        uint32_t xw[4];
+                        ld_shared_v4(buf + srow_off + ((static_cast<uint32_t>(q) ^ sw) << 4), xw);
+                        gate_x<IN_T, PER>(v, xw);
+                    } else {  // fp32 output: values 4q .. 4q+3 of the chunk
+                        gate_x<IN_T, PER>(v, &xf[(2 * q) % (OSZ == 4 ? 16 : 1)]);
+                    }
                 }
                 uint32_t wv[4];
                 if (OUT_T == CDG_T_F32) {
@@ -746,6 +855,13 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
                 bulk_commit_group();
             }
         }
+        if (!ok) break;
+    }
+    if (MASK && ew == 0 && elected && g_used != g_issued) {
+        // aborted: let the gate loads still in flight land before the CTA exits
+        volatile uint32_t no_abort = 0;
+        const Ctl drain_ctl{&no_abort, ctl.status};
+        for (uint32_t n = g_used; n < g_issued; ++n) wait_bar(R.gfull0 + 8u * (n & 3u), (n >> 2) & 1u, drain_ctl);
     }
     if (elected) bulk_wait_group_all();
 }
@@ -769,7 +885,7 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_cons
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    // shared memory: operand ring(s) | 2 x 16 KB output staging | mbarriers, flags | phase and tap tables
+    // shared memory: operand ring(s) | 2 x 16 KB output staging | gate buffers | mbarriers, flags | phase and tap tables
     const int stages = HALO ? p.a_stages + p.b_stages : p.stages;  // mbarrier pairs
     Ring R;
     R.stages = stages;
@@ -778,20 +894,24 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_cons
     R.b0 = base + p.a_stages * R.stage_bytes;
     R.b_bytes = p.BN * 128;
     R.out0 = HALO ? R.b0 + (p.b_res ? p.b_res_bytes : p.b_stages * p.halo_tg * R.b_bytes) : base + stages * R.stage_bytes;
-    const uint32_t bars = R.out0 + CDG_SMEM_STAGING;
-    // mbarriers: full[stages], empty[stages], acc_full[4], acc_empty[4], drain[2]
+    // gated by the activation: four staging buffers; by the packed mask: two and the mask ring
+    R.gate0 = R.out0 + CDG_SMEM_STAGING;
+    const uint32_t bars =
+        R.out0 + CDG_SMEM_STAGING + (MASK ? (p.mask_bits ? CDG_GATE_RING : CDG_SMEM_STAGING) : 0u);
+    // mbarriers: full[stages], empty[stages], acc_full[4], acc_empty[4], drain[2], gate[4]
     R.full0 = bars;
     R.empty0 = bars + 8u * stages;
     R.acc_full0 = bars + 16u * stages;
     R.acc_empty0 = bars + 16u * stages + 32u;
     R.drain = bars + 16u * stages + 64u;
+    R.gfull0 = bars + 16u * stages + 80u;
     uint8_t *const tail = smem_raw + (bars - raw);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tail + 8 * (2 * stages + 10));
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tail + 8 * (2 * stages + 14));
     volatile uint32_t *abort_flag = tmem_slot + 1;
     volatile uint32_t *slot_parity = tmem_slot + 2;  // [stages] (<= CDG_MAX_STAGES_TOTAL entries)
     CdgPhase *tab = reinterpret_cast<CdgPhase *>(tail + CDG_SMEM_TABLES);
     CdgTap *taps = reinterpret_cast<CdgTap *>(tab + CDG_MAX_PHASES);
-    static_assert(8 * (2 * CDG_MAX_STAGES_TOTAL + 10) + 8 + 4 * CDG_MAX_STAGES_TOTAL <= CDG_SMEM_TABLES,
+    static_assert(8 * (2 * CDG_MAX_STAGES_TOTAL + 14) + 8 + 4 * CDG_MAX_STAGES_TOTAL <= CDG_SMEM_TABLES,
                   "mbarrier area overflows");
     static_assert(CDG_SMEM_TABLES + CDG_MAX_PHASES * sizeof(CdgPhase) + CDG_MAX_TAPS * sizeof(CdgTap) <=
                       CDG_SMEM_TAIL,
@@ -829,6 +949,7 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_cons
         }
         mbar_init(R.drain, 1);
         mbar_init(R.drain + 8u, 1);
+        for (int g = 0; g < 4; ++g) mbar_init(R.gfull0 + 8u * g, 1);
         *abort_flag = 0u;
         for (int s = 0; s < stages; ++s) slot_parity[s] = 0u;
         fence_mbar_init();
@@ -949,6 +1070,31 @@ __global__ void prepack_kernel(const uint16_t *__restrict__ W, uint16_t *__restr
     }
 }
 
+// Packed ReLU mask: each pixel's C channels as bits padded to whole 16-byte
+// units (cb bytes a pixel), channel c of pixel p in bit c % 8 of byte
+// p*cb + c/8, set when x[p][c] > 0.  One thread per byte: its eight channels in
+// one 16-byte load; bytes past C are 0.
+__global__ void pack_relu_mask_kernel(const uint16_t *__restrict__ x, uint8_t *__restrict__ bits, long long nbytes,
+                                      int C, int cb, int in_type)
+{
+    const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= nbytes) return;
+    const long long pix = i / cb;
+    const int c0 = 8 * static_cast<int>(i - pix * cb);
+    uint32_t byte = 0;
+    if (c0 < C) {
+        const uint4 u = __ldg(reinterpret_cast<const uint4 *>(x + pix * C + c0));
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const uint16_t h = static_cast<uint16_t>(w[e >> 1] >> (16 * (e & 1)));
+            const float v = in_type == CDG_T_BF16 ? gate_value<CDG_T_BF16>(h) : gate_value<CDG_T_F16>(h);
+            if (v > 0.0f) byte |= 1u << e;
+        }
+    }
+    bits[i] = static_cast<uint8_t>(byte);
+}
+
 }  // namespace cdg
 
 // ------------------------------------------------------------------ launchers
@@ -995,6 +1141,18 @@ cudaError_t cdg_prepare_dgrad(int out_type, int in_type, bool mask, size_t smem)
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
+}
+
+cudaError_t cdg_launch_pack_mask(const void *x, void *bits, long long pixels, int C, int in_type,
+                                 cudaStream_t stream)
+{
+    const int cb = 16 * ((C + 127) / 128);
+    const long long nbytes = pixels * cb;
+    if (nbytes <= 0) return cudaSuccess;
+    const long long blocks = (nbytes + 255) / 256;
+    cdg::pack_relu_mask_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        static_cast<const uint16_t *>(x), static_cast<uint8_t *>(bits), nbytes, C, cb, in_type);
+    return cudaGetLastError();
 }
 
 cudaError_t cdg_launch_dgrad(const CdgParams &p, int out_type, int in_type, bool mask, int grid, size_t smem,

@@ -68,8 +68,11 @@ typedef enum { CDG_F16 = 0, CDG_BF16 = 1 } cdg_dtype_t;
 
 /* Epilogue flags (bit set). */
 enum {
-    CDG_EPI_RELU_BWD = 1, /* gate by the saved activation: out = (x > 0) ? v : +0.0 */
-    CDG_EPI_OUT_F32 = 2   /* write dX as fp32 instead of the input type             */
+    CDG_EPI_RELU_BWD = 1,     /* gate by the saved activation: out = (x > 0) ? v : +0.0 */
+    CDG_EPI_OUT_F32 = 2,      /* write dX as fp32 instead of the input type             */
+    CDG_EPI_RELU_BWD_BITS = 4 /* the same gate from a packed bit mask (one bit per      */
+                              /* element, see cdg_pack_relu_mask): out = bit ? v : +0.0 */
+                              /* (not together with CDG_EPI_RELU_BWD)                   */
 };
 
 /*
@@ -146,8 +149,10 @@ int cdg_prepack_weights(cdg_handle_t h, const void *W_krsc, void *Wpacked, cdg_s
 
 /*
  * dX = dgrad(dY, W) for the planned shape, one kernel launch, asynchronous
- * on stream.  relu_mask is the saved activation x (NULL unless the plan has
- * CDG_EPI_RELU_BWD).  Every element of dX is written, including pixels no
+ * on stream.  relu_mask is the saved activation x for a plan with
+ * CDG_EPI_RELU_BWD (NHWC like dX, input dtype), the packed mask for
+ * CDG_EPI_RELU_BWD_BITS (cdg_pack_relu_mask's layout), else NULL; it must not
+ * overlap dX.  Every element of dX is written, including pixels no
  * filter tap reaches (+0.0); dX is never read, so its prior contents do not
  * matter.  dY, Wpacked and x are only read.  No workspace, no allocation.
  * A device-side pipeline timeout (which a correct launch never hits) is
@@ -187,6 +192,27 @@ int cdg_device_status(cdg_handle_t h, cdg_stream_t stream);
  */
 int cdg_autotune(cdg_handle_t h, const void *dY, const void *Wpacked, void *dX, const void *relu_mask,
                  cdg_stream_t stream, int reps, float *best_ms);
+
+/*
+ * Pack the ReLU-backward mask of a saved activation x (NHWC, pixels = N*H*W
+ * rows of C channels, dtype CDG_F16 or CDG_BF16) for a plan with
+ * CDG_EPI_RELU_BWD_BITS.  Layout: each pixel's C channels as bits, the row
+ * padded to whole 16-byte units (cdg_relu_mask_bytes(1, C) bytes a pixel);
+ * channel c of pixel p is bit c % 8 of byte p*row + c/8, set when x > 0
+ * (x <= 0, -0.0 and NaN give 0); padding bits are 0.  For C a multiple of 128
+ * this is exactly one bit per element; the padding lets the dgrad fetch a
+ * tile's mask with the same tensor copies as its output, and for C < 128 it
+ * still cuts the gate's reads 8x against x.  This variant of the pages'
+ * ReLU-backward epilogue fusion is an addition of this library (the pages gate
+ * with the activation itself).  C % 8 == 0; x and bits 16-byte aligned, not
+ * overlapping; bits holds cdg_relu_mask_bytes(pixels, C) bytes, all of which
+ * are written.  Asynchronous on stream.
+ */
+int cdg_pack_relu_mask(const void *x, void *bits, long long pixels, int C, int dtype, cdg_stream_t stream);
+
+/* Bytes of a packed ReLU mask of `pixels` pixels of C channels (see
+ * cdg_pack_relu_mask), or -1 for pixels < 0, C <= 0 or C % 8 != 0.  Host only. */
+long long cdg_relu_mask_bytes(long long pixels, int C);
 
 /* Static text for a status code. */
 const char *cdg_status_string(int status);

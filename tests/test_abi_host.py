@@ -17,7 +17,8 @@ HEADER = os.path.join(ROOT, "include", "cdg.h")
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    names = re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(cdg_[a-z_0-9]+)\s*\(", text, flags=re.M)
+    names = re.findall(r"^\s*(?:const\s+)?(?:[a-z_0-9]+\s+)*[a-z_0-9]+\s*\*?\s*(cdg_[a-z_0-9]+)\s*\(", text,
+                       flags=re.M)
     return sorted(set(names))
 
 
@@ -55,7 +56,7 @@ GOOD = (2, 8, 8, 16, 16, 3, 3, 1, 1, 1, cdg.BF16, 0)
 @pytest.mark.parametrize("host", [True, False])
 @pytest.mark.parametrize("field,value,expect", [
     (0, 0, 1), (1, 0, 1), (3, 0, 1), (5, 0, 1), (7, 0, 1), (8, -1, 1), (9, 0, 1),
-    (10, 2, 1), (11, 4, 1),
+    (10, 2, 1), (11, 8, 1), (11, 5, 1),  # unknown epilogue flag; both ReLU gates at once
     (3, 12, 2), (4, 20, 2), (7, 5, 2),
 ])
 def test_argument_validation_needs_no_device(host, field, value, expect):
@@ -173,3 +174,53 @@ def test_halo_resident_weights_when_the_filter_fits(monkeypatch):
     assert cdg.plan_host(256, 28, 28, 128, 128, 3, 3, 1, 1, 1, "bf16", num_sms=148).info()["a_mode"] == 2
     monkeypatch.setenv("CDG_HALO", "0")
     assert cdg.plan_host(256, 56, 56, 64, 64, 3, 3, 1, 1, 1, "bf16", num_sms=148).info()["a_mode"] == 0
+
+
+@pytest.mark.parametrize("x,bits,pixels,C,dtype,expect", [
+    (0, 4096, 4, 64, "bf16", 1),          # NULL activation
+    (4096, 0, 4, 64, "bf16", 1),          # NULL mask
+    (4096, 8192, -1, 64, "bf16", 1),      # negative pixel count
+    (4096, 8192, 4, 0, "bf16", 1),        # no channels
+    (4096, 8192, 4, 12, "bf16", 1),       # C not a multiple of 8
+    (4096, 8192, 4, 64, 2, 1),            # f32 activations are not packed
+    (4104, 8192, 4, 64, "f16", 3),        # x not 16-byte aligned
+    (4096, 8200, 4, 64, "f16", 3),        # mask not 16-byte aligned
+    (4096, 4352, 4, 64, "bf16", 4),       # mask overlaps x (x spans 512 bytes)
+])
+def test_pack_relu_mask_argument_errors(x, bits, pixels, C, dtype, expect):
+    with pytest.raises(cdg.CdgError) as e:
+        cdg.pack_relu_mask(x, bits, pixels, C, dtype)
+    assert e.value.status == expect
+
+
+def test_pack_relu_mask_empty_is_a_no_op():
+    cdg.pack_relu_mask(4096, 8192, 0, 64, "bf16")  # no launch, so no device needed
+
+
+@pytest.mark.parametrize("pixels,C,expect", [
+    (1, 8, 16), (1, 128, 16), (1, 136, 32), (3, 256, 96), (10, 64, 160), (0, 64, 0), (7, 2048, 7 * 256)])
+def test_relu_mask_bytes(pixels, C, expect):
+    """A pixel's C bits fill whole 16-byte units: 16 * ceil(C / 128) bytes."""
+    assert cdg.relu_mask_bytes(pixels, C) == expect
+
+
+@pytest.mark.parametrize("pixels,C", [(-1, 64), (4, 0), (4, 12)])
+def test_relu_mask_bytes_invalid(pixels, C):
+    with pytest.raises(cdg.CdgError):
+        cdg.relu_mask_bytes(pixels, C)
+
+
+def test_bits_gate_tiles_start_on_mask_units():
+    """With the packed mask, N tiles of a wide layer are multiples of 128
+    channels, so each tile's mask bytes start on a 16-byte unit."""
+    for C in (320, 384, 640, 1024, 2048):
+        info = cdg.plan_host(8, 14, 14, C, 64, 1, 1, 1, 0, 1, "bf16", relu_bits=True, num_sms=148).info()
+        assert info["tile_n"] % 128 == 0, (C, info["tile_n"])
+    assert cdg.plan_host(8, 14, 14, 72, 64, 1, 1, 1, 0, 1, "bf16", relu_bits=True, num_sms=148).info()["tile_n"] == 80
+
+
+def test_bits_gated_plan_needs_the_mask():
+    q = cdg.plan_host(1, 8, 8, 16, 16, 3, 3, 1, 1, 1, "bf16", relu_bits=True)
+    with pytest.raises(cdg.CdgError) as e:
+        q.dgrad(16, 16, 4096, None)
+    assert e.value.status == 1

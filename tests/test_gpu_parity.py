@@ -244,3 +244,97 @@ def test_autotuned_plan_matches_oracle(L):
     run.run()
     assert_close(run.result(), ref, run.odt, L.name + " (tuned plan)")
     assert run.status() == 0
+
+
+def _packed_mask_numpy(x_bits: np.ndarray, dtype: str, C: int) -> np.ndarray:
+    """The layout cdg_pack_relu_mask documents: per pixel, C bits (x > 0),
+    channel c in bit c % 8 of byte c / 8, the row zero-padded to whole 16-byte
+    units."""
+    pos = synth.bits_to_f32(x_bits.reshape(-1, C), dtype) > 0  # NaN and -0 give False
+    row = 16 * ((C + 127) // 128)
+    padded = np.zeros((pos.shape[0], 8 * row), bool)
+    padded[:, :C] = pos
+    return np.packbits(padded, axis=1, bitorder="little").reshape(-1)
+
+
+BITS_CASES = [_case(2, 11, 13, 72, 136, 3, 3, 2, 1, 1, "f16", relu=True, idx=10),
+              _case(2, 9, 9, 40, 24, 2, 3, 2, 2, 1, "bf16", relu=True, idx=11),
+              _case(2, 12, 12, 64, 64, 3, 3, 1, 1, 1, "bf16", relu=True, idx=12),
+              _case(2, 10, 10, 32, 48, 3, 3, 2, 1, 1, "f16", out="f32", relu=True, idx=13)]
+
+
+def _bits_gated(L, x_override=None):
+    """Pack the saved activation with cdg_pack_relu_mask (checked against numpy)
+    and run the bit-gated dgrad; returns (raw dX bytes, x bits, output dtype, plan)."""
+    import torch
+    import implicit_gemm_dgrad_gb300 as cdg
+    from gpu_util import GuardedOutput, to_dev
+    dY, W, x = synth.make_inputs(L.shape(), L.dtype, L.dist, L.workload, L.index, with_x=True)
+    if x_override is not None:
+        x = x_override(x)
+    pixels = L.N * L.H * L.W
+    d_x = to_dev(x, L.dtype)
+    d_bits = torch.full((cdg.relu_mask_bytes(pixels, L.C),), 0xA5, dtype=torch.uint8, device="cuda")
+    cdg.pack_relu_mask(d_x, d_bits, pixels, L.C, L.dtype)
+    torch.cuda.synchronize()
+    assert np.array_equal(d_bits.cpu().numpy(), _packed_mask_numpy(x, L.dtype, L.C))
+    p = cdg.plan(L.N, L.H, L.W, L.C, L.K, L.R, L.S, L.stride, L.pad, L.dil, L.dtype, out_f32=(L.out == "f32"),
+                 relu_bits=True)
+    d_dY, d_W = to_dev(dY, L.dtype), to_dev(W, L.dtype)
+    d_Wp = torch.empty(p.packed_weight_bytes // 2, dtype=torch.int16, device="cuda")
+    p.prepack_weights(d_W, d_Wp)
+    odt = "f32" if L.out == "f32" else L.dtype
+    out = GuardedOutput(L.N * L.H * L.W * L.C, 4 if odt == "f32" else 2)
+    p.dgrad(d_dY, d_Wp, out.ptr, d_bits)
+    torch.cuda.synchronize()
+    raw = out.body().cpu().numpy()
+    assert out.guards_intact() and p.device_status() == 0
+    ref = oracle.dgrad(dY, W, L.H, L.W, L.stride, L.pad, L.dil, x=x, dtype=L.dtype)
+    check_gate_zero_pattern(raw, x, odt, L.dtype)
+    assert_close(decode_out(raw, odt).reshape(L.N, L.H, L.W, L.C), ref, odt, L.name)
+    return raw, x, odt, p
+
+
+@pytest.mark.parametrize("L", BITS_CASES, ids=lambda L: L.name)
+def test_packed_relu_mask_gate(L):
+    """CDG_EPI_RELU_BWD_BITS: the mask packed by cdg_pack_relu_mask equals the
+    numpy packing of (x > 0), and the dgrad gated by it equals the oracle gated
+    by x, with +0.0 exactly where x <= 0, -0.0 or NaN."""
+    special = None
+    if L.index == 12:  # special values in the saved activation
+        specials = np.array([0x3F80, 0x0000, 0x8000, 0x7FC0, 0xBF80, 0x0001, 0x7F80, 0xFF80], np.uint16)
+        special = lambda x: np.resize(specials, x.shape).astype(np.uint16)  # noqa: E731
+    _bits_gated(L, special)
+
+
+# (layer, planner override, what the plan must reach): the gate's inputs are
+# copied ahead into the staging buffers in every kernel mode
+GATE_CASES = [
+    (_case(3, 13, 11, 200, 72, 1, 1, 1, 0, 1, "bf16", relu=True, idx=14), "", {"a_mode": 1}),  # rows, 8-ch tail chunk
+    (_case(2, 14, 14, 64, 128, 1, 1, 2, 0, 1, "bf16", relu=True, idx=15), "", {"a_mode": 1}),  # rows, zero phases
+    (_case(2, 13, 13, 64, 64, 1, 1, 2, 0, 1, "f16", relu=True, idx=16), "", {"a_mode": 0}),    # 4-D boxes, zero phases
+    (_case(2, 20, 20, 64, 64, 3, 3, 1, 1, 1, "bf16", relu=True, idx=17), "", {"a_mode": 3}),   # halo, resident weights
+    (_case(2, 12, 12, 128, 128, 3, 3, 1, 1, 1, "bf16", relu=True, idx=18), "CDG_HALO=1", {"a_mode": 2}),
+    (_case(2, 14, 14, 256, 256, 3, 3, 1, 1, 1, "bf16", relu=True, idx=19), "", {"cta_pair": 1}),
+    (_case(4, 16, 16, 128, 256, 3, 3, 2, 1, 1, "bf16", relu=True, idx=20), "", {"mma_warps": 2}),
+    (_case(2, 10, 10, 96, 48, 3, 3, 1, 1, 1, "f16", out="f32", relu=True, idx=21), "", {}),
+    (_case(2, 9, 9, 64, 64, 1, 1, 1, 0, 1, "bf16", out="f32", relu=True, idx=22), "", {"a_mode": 1}),
+]
+
+
+@pytest.mark.parametrize("gate", ["x", "bits"])
+@pytest.mark.parametrize("L,env,reach", GATE_CASES, ids=lambda v: v.name if isinstance(v, Layer) else None)
+def test_gate_in_every_mode(L, env, reach, gate, monkeypatch):
+    """The fused ReLU-backward gate, from the saved activation or its packed
+    mask, gives the oracle's result and +0.0 exactly where x <= 0 in every
+    operand, tile and issue mode."""
+    if env:
+        key, val = env.split("=")
+        monkeypatch.setenv(key, val)
+    if gate == "x":
+        run, _, _ = check_layer(L)
+        info = run.plan.info()
+    else:
+        info = _bits_gated(L)[3].info()
+    for k, v in reach.items():
+        assert info[k] == v, (k, info)
