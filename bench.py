@@ -85,14 +85,26 @@ def profiled_traffic(layer_name: str):
     return int(rec["dram_read_bytes"]) + int(rec["dram_write_bytes"])
 
 
+def tap_pixels(layer) -> int:
+    """dX pixels that some (p, r) and (q, s) reach, h = p*stride - pad + r*dil
+    and w = q*stride - pad + s*dil: reachable rows x reachable columns.
+    Elsewhere dX is +0.0 whatever the gate holds, so an algorithm need read
+    the gate input only here."""
+    L = layer
+    rows = {p * L.stride - L.pad + r * L.dil for p in range(L.P) for r in range(L.R)}
+    cols = {q * L.stride - L.pad + s * L.dil for q in range(L.Q) for s in range(L.S)}
+    return L.N * sum(0 <= h < L.H for h in rows) * sum(0 <= w < L.W for w in cols)
+
+
 def gate_bytes(layer, gate: str) -> int:
     """Algorithmic HBM bytes of one launch: dY + W + dX, plus the gate input
-    read once: the saved activation (2 B per dX element) or the packed mask
-    (one bit per dX element, each pixel's row padded to 16-byte units)."""
+    read once where dX can be non-zero (tap_pixels): the saved activation
+    (2 B per element) or the packed mask (each pixel's C bits padded to
+    16-byte units)."""
     el = layer.N * layer.H * layer.W * layer.C
     base = layer.bytes - (2 * el if layer.relu else 0)
-    mask = layer.N * layer.H * layer.W * 16 * ((layer.C + 127) // 128)
-    return base + {"none": 0, "x": 2 * el, "bits": mask}[gate]
+    px = tap_pixels(layer)
+    return base + {"none": 0, "x": 2 * px * layer.C, "bits": px * 16 * ((layer.C + 127) // 128)}[gate]
 
 
 def roofline_time_s(layer, peaks, gate="none"):

@@ -1,0 +1,51 @@
+"""The algorithmic byte counts bench.py divides by: the gated bytes count the
+gate input only where some filter tap reaches dX (elsewhere dX is +0.0
+whatever the gate holds), checked by brute force over the definition."""
+import importlib.util
+import itertools
+import os
+
+import pytest
+
+from implicit_gemm_dgrad_gb300.workloads import RESNET50_B256, Layer
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _bench():
+    spec = importlib.util.spec_from_file_location("bench_mod_bytes", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def _reached_pixels(L) -> int:
+    """dX pixels h = p*stride - pad + r*dil, w = q*stride - pad + s*dil that
+    some (p, q, r, s) reaches, counted one image at a time."""
+    hit = set()
+    for p, q, r, s in itertools.product(range(L.P), range(L.Q), range(L.R), range(L.S)):
+        h = p * L.stride - L.pad + r * L.dil
+        w = q * L.stride - L.pad + s * L.dil
+        if 0 <= h < L.H and 0 <= w < L.W:
+            hit.add((h, w))
+    return L.N * len(hit)
+
+
+@pytest.mark.parametrize("shape", [
+    (2, 9, 9, 8, 8, 1, 1, 2, 0, 1), (1, 10, 10, 8, 8, 3, 3, 2, 1, 1), (1, 12, 11, 8, 8, 1, 1, 3, 0, 1),
+    (1, 13, 13, 8, 8, 2, 2, 2, 0, 1), (1, 16, 16, 8, 8, 3, 3, 4, 1, 2), (1, 7, 7, 8, 8, 3, 3, 1, 1, 1),
+    (1, 14, 14, 8, 8, 1, 1, 2, 0, 1), (1, 11, 9, 8, 8, 5, 3, 3, 2, 1)])
+def test_tap_pixels_match_the_definition(shape):
+    L = Layer("t", *shape)
+    assert _bench().tap_pixels(L) == _reached_pixels(L)
+
+
+def test_gate_bytes_per_mode():
+    b = _bench()
+    for L in RESNET50_B256:
+        px = b.tap_pixels(L)
+        assert b.gate_bytes(L, "none") == L.bytes
+        assert b.gate_bytes(L, "x") == L.bytes + 2 * px * L.C
+        assert b.gate_bytes(L, "bits") == L.bytes + px * 16 * ((L.C + 127) // 128)
+        if L.R == 1 and L.stride == 2:
+            assert px * 4 == L.N * L.H * L.W  # three of four phases get no tap
