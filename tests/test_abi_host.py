@@ -224,3 +224,21 @@ def test_bits_gated_plan_needs_the_mask():
     with pytest.raises(cdg.CdgError) as e:
         q.dgrad(16, 16, 4096, None)
     assert e.value.status == 1
+
+
+@pytest.mark.parametrize("gate", ["x", "bits"])
+@pytest.mark.parametrize("out_f32", [False, True])
+def test_gated_plans_fit_shared_memory(gate, out_f32):
+    """Gated plans carry four staging buffers (activation) or a mask-tile
+    ring (packed mask) besides the operand ring: every ResNet-50 layer still
+    plans within the 227 KB of shared memory with at least three stages, and
+    bit-gated N tiles start on 16-byte mask units."""
+    from implicit_gemm_dgrad_gb300.workloads import RESNET50_B256
+    for L in RESNET50_B256:
+        p = cdg.plan_host(L.N, L.H, L.W, L.C, L.K, L.R, L.S, L.stride, L.pad, L.dil, L.dtype,
+                          relu=(gate == "x"), relu_bits=(gate == "bits"), out_f32=out_f32, num_sms=148)
+        info = p.info()
+        assert info["smem_bytes"] <= 232448, (L.name, info)
+        assert info["stages"] >= 3, (L.name, info)
+        if gate == "bits" and info["tile_n"] < L.C:
+            assert info["tile_n"] % 128 == 0, (L.name, info)
