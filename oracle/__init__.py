@@ -2,7 +2,8 @@
 
 A ctypes wrapper around ``oracle.c``: the plain double-precision statement of
 the operation the GPU library computes (the gradient of a cross-correlation
-Conv2d with respect to its input, "Conv2d dgrad" in apache/tvm PR #10110).
+Conv2d with respect to its input, "Conv2d dgrad" in apache/tvm PR #10110),
+and of the weight gradient (wgrad) that the page names as its follow-up.
 
 Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
 leg may import this package.  The GPU library never touches it; the two share
@@ -55,6 +56,8 @@ def _load():
             lib.oracle_dgrad_pixels.restype = i
             lib.oracle_conv_fwd.argtypes = [vp, vp, i, vp] + [i] * 10
             lib.oracle_conv_fwd.restype = i
+            lib.oracle_wgrad.argtypes = [vp, vp, i, vp] + [i] * 10
+            lib.oracle_wgrad.restype = i
             lib.oracle_out_extent.argtypes = [i] * 5
             lib.oracle_out_extent.restype = i
             lib.oracle_half_to_double.argtypes = [ctypes.c_uint16]
@@ -144,6 +147,25 @@ def dgrad_pixels(dY, W, H, Wd, pix, stride=1, pad=0, dil=1, x=None, dtype=None):
     if rc:
         raise RuntimeError("oracle_dgrad_pixels failed")
     return out
+
+
+def wgrad(dY, x, R, S, stride=1, pad=0, dil=1, dtype=None):
+    """dW (float64, KRSC [K][R][S][C]) from dY [N][P][Q][K] and the forward
+    input x [N][H][W][C]: the weight gradient of the same cross-correlation."""
+    code = _dtype_of(dY, dtype)
+    N, P, Q, K = dY.shape
+    N2, H, Wd, C = x.shape
+    if N2 != N:
+        raise ValueError("N mismatch")
+    if (out_extent(H, R, stride, pad, dil), out_extent(Wd, S, stride, pad, dil)) != (P, Q):
+        raise ValueError("dY spatial shape does not match the geometry")
+    _check(dY, code)
+    _check(x, code)
+    dW = np.empty((K, R, S, C), np.float64)
+    rc = _load().oracle_wgrad(_ptr(dY), _ptr(x), code, _ptr(dW), N, H, Wd, C, K, R, S, stride, pad, dil)
+    if rc:
+        raise RuntimeError("oracle_wgrad failed")
+    return dW
 
 
 def conv_fwd(x, W, stride=1, pad=0, dil=1, dtype=None):

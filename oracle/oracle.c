@@ -37,6 +37,9 @@
  * matrix (brute force), the adjoint identity with the forward convolution
  * below, closed forms (1x1 GEMM, impulse response, identity filter), a
  * hand-worked case, integer-exact results and an independent library routine.
+ *
+ * The file also states the weight gradient (wgrad) of the same convolution,
+ * the page's announced follow-up, pinned the same ways (oracle_wgrad below).
  */
 #include <math.h>
 #include <stdint.h>
@@ -280,6 +283,56 @@ int oracle_conv_fwd(const void *x, const void *Wt, int dtype, double *y,
                     y[(((size_t)n * P + p) * Q + q) * (size_t)K + k] = acc;
                 }
     free(Wd);
+    return 0;
+}
+
+/*
+ * Weight gradient (wgrad) of the same cross-correlation: the gradient of y
+ * above with respect to the filter, which the apache/tvm PR #10110 page
+ * ("[CUTLASS] Conv2d dgrad") names as the follow-up to dgrad (opening
+ * description; merge comment: "wgrad + parallel split-k").  The page gives
+ * no formula; this is the definition written out:
+ *   dW[k,r,s,c] = sum over n, p, q of
+ *                 dY[n,p,q,k] * x[n, p*stride - pad + r*dil, q*stride - pad + s*dil, c]
+ * with out-of-range input positions contributing zero (the padding the
+ * forward pass read as zero).  dY is NHWC [N][P][Q][K], x NHWC [N][H][W][C],
+ * both of `dtype`; dW is written as doubles, KRSC [K][R][S][C].  Each filter
+ * element's sum runs over (n, p, q) in that order; nothing else is reordered.
+ */
+int oracle_wgrad(const void *dY, const void *x, int dtype, double *dW,
+                 int N, int H, int W, int C, int K, int R, int S,
+                 int stride, int pad, int dil)
+{
+    int P, Q;
+    if (check_geometry(N, H, W, C, K, R, S, stride, pad, dil, &P, &Q)) return -1;
+    double *g = decode_all(dY, (size_t)N * P * Q * K, dtype);
+    double *xd = decode_all(x, (size_t)N * H * W * C, dtype);
+    if (!g || !xd) {
+        free(g);
+        free(xd);
+        return -1;
+    }
+#pragma omp parallel for collapse(3) schedule(dynamic, 1)
+    for (int k = 0; k < K; ++k)
+        for (int r = 0; r < R; ++r)
+            for (int s = 0; s < S; ++s) {
+                double *out = dW + (((size_t)k * R + r) * S + s) * (size_t)C;
+                for (int c = 0; c < C; ++c) out[c] = 0.0;
+                for (int n = 0; n < N; ++n)
+                    for (int p = 0; p < P; ++p) {
+                        int h = p * stride - pad + r * dil;
+                        if (h < 0 || h >= H) continue;
+                        for (int q = 0; q < Q; ++q) {
+                            int w = q * stride - pad + s * dil;
+                            if (w < 0 || w >= W) continue;
+                            const double gv = g[(((size_t)n * P + p) * Q + q) * (size_t)K + k];
+                            const double *xrow = xd + (((size_t)n * H + h) * W + w) * (size_t)C;
+                            for (int c = 0; c < C; ++c) out[c] += gv * xrow[c];
+                        }
+                    }
+            }
+    free(g);
+    free(xd);
     return 0;
 }
 
