@@ -315,6 +315,89 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def run_wgrad(args, rank, world, local_rank):
+    """The weight gradient of the same 22 layers: per layer one split-K GEMM
+    launch and one ordered-reduction launch; inputs resident; per-layer event
+    times from a separate pass, then K timed steps."""
+    import torch
+    import implicit_gemm_dgrad_gb300 as cdg
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.Stream(device=dev)
+    peaks = load_peaks()
+    layers = select_layers(args.layers)
+    state = []
+    with torch.cuda.stream(stream):
+        for L in layers:
+            dY, W, x = synth.make_inputs(L.shape(), L.dtype, L.dist, L.workload, L.index, with_x=True)
+            p = cdg.wgrad_plan(L.N, L.H, L.W, L.C, L.K, L.R, L.S, L.stride, L.pad, L.dil, L.dtype)
+            d_dY = torch.from_numpy(dY.view(np.int16)).to(dev)
+            d_x = torch.from_numpy(x.reshape(-1).view(np.int16)).to(dev)
+            d_dW = torch.empty(L.K * L.R * L.S * L.C, dtype=torch.int16, device=dev)
+            ws = torch.empty(p.workspace_bytes // 4, dtype=torch.float32, device=dev)
+            state.append((L, p, d_dY, d_x, d_dW, ws))
+    torch.cuda.synchronize()
+
+    def step():
+        for (_, p, d_dY, d_x, d_dW, ws) in state:
+            p.wgrad(d_dY, d_x, d_dW, ws, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    for (L, p, *_r) in state:
+        if p.device_status(stream) != 0:
+            raise RuntimeError(f"wgrad device status after warm-up ({L.name})")
+    nL = len(state)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nL + 1)] for _ in range(args.steps)]
+    for k in range(args.steps):
+        evs[k][0].record(stream)
+        for i, (_, p, d_dY, d_x, d_dW, ws) in enumerate(state):
+            p.wgrad(d_dY, d_x, d_dW, ws, stream)
+            evs[k][i + 1].record(stream)
+    torch.cuda.synchronize()
+    per_ms = np.mean([[evs[k][i].elapsed_time(evs[k][i + 1]) for i in range(nL)] for k in range(args.steps)], axis=0)
+    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clocks:
+        for k in range(args.steps):
+            e0[k].record(stream)
+            step()
+            e1[k].record(stream)
+        torch.cuda.synchronize()
+    total_ms = max_over_ranks(float(sum(e0[k].elapsed_time(e1[k]) for k in range(args.steps))), world)
+    ms_per_step = total_ms / args.steps
+    flops_step = sum(L.flops for (L, *_r) in state)
+    per_layer = []
+    for i, (L, p, *_r) in enumerate(state):
+        t = per_ms[i] * 1e-3
+        inf = p.info()
+        per_layer.append({"layer": L.name, "ms": round(float(per_ms[i]), 5), "tflops": round(L.flops / t / 1e12, 2),
+                          "tensor_peak_frac": round(L.flops / t / 1e12 / peaks["bf16_tflops_sustained"], 4),
+                          "plan": {"splits": inf["splits"], "tile_n": inf["tile_n"], "pos_box": inf["pos_box"],
+                                   "stages": inf["stages"], "work_items": inf["work_items"]}})
+    if rank != 0:
+        return
+    dom = int(np.argmax(per_ms))
+    Ld = state[dom][0]
+    achieved = Ld.flops / (per_ms[dom] * 1e-3) / 1e12
+    line = {"metric": "wgrad TFLOP/s per ResNet-50 layer (1 GB300)", "op": "wgrad",
+            "value": round(world * flops_step * args.steps / (total_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD.replace("dgrad", "wgrad"), "global_batch": 256 * world, "layers": nL,
+                       "flops_per_step": flops_step, "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2"},
+            "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops_sustained"],
+                         "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops_sustained"], 4),
+                         "traffic": None, "kernel": f"wgrad_kernel + reduce ({Ld.name})",
+                         "launch_ms": round(float(per_ms[dom]), 5),
+                         "peak_source": peaks["source"] + " sustained bf16"},
+            "gpu_launches": 2 * nL * args.steps, "clocks": clocks.summary(), "per_layer": per_layer,
+            "per_layer_timing": "separate pass, one CUDA event pair around each layer's two launches"}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -329,6 +412,8 @@ def main():
     ap.add_argument("--layers", default="", help="comma-separated layer names (default: all 22)")
     ap.add_argument("--autotune", type=int, default=0,
                     help="1: tune every layer's plan with cdg_autotune during set-up (untimed)")
+    ap.add_argument("--op", default="dgrad", choices=["dgrad", "wgrad"],
+                    help="wgrad: time the weight gradient (split-K GEMM + ordered reduction) of the same layers")
     ap.add_argument("--gate", default="none", choices=["none", "x", "bits"],
                     help="fused ReLU-backward gate on every layer: none; x = the saved bf16 activation; "
                          "bits = its 1-bit packed mask (packed once at set-up, as a forward pass would store it)")
@@ -351,6 +436,9 @@ def main():
     if world > 1:
         dist.init_process_group("gloo")  # control path only: barrier and max-over-ranks
     torch.cuda.set_device(local_rank)
+    if args.op == "wgrad":
+        run_wgrad(args, rank, world, local_rank)
+        return
     dev = torch.device("cuda", local_rank)
     stream = torch.cuda.Stream(device=dev)
     peaks = load_peaks()

@@ -34,7 +34,9 @@ DTYPES = {"f16": F16, "bf16": BF16}
 
 EXPORTS = ("cdg_plan", "cdg_plan_host", "cdg_destroy", "cdg_get_output_dims", "cdg_packed_weight_bytes",
            "cdg_plan_get_info", "cdg_prepack_weights", "cdg_dgrad", "cdg_device_status", "cdg_status_string",
-           "cdg_dgrad_noalloc", "cdg_autotune", "cdg_pack_relu_mask", "cdg_relu_mask_bytes")
+           "cdg_dgrad_noalloc", "cdg_autotune", "cdg_pack_relu_mask", "cdg_relu_mask_bytes",
+           "cdg_wgrad_plan", "cdg_wgrad_plan_host", "cdg_wgrad_destroy", "cdg_wgrad_workspace_bytes",
+           "cdg_wgrad_get_info", "cdg_wgrad", "cdg_wgrad_device_status")
 
 
 class CdgError(RuntimeError):
@@ -103,6 +105,20 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.cdg_pack_relu_mask.restype = i
     lib.cdg_relu_mask_bytes.argtypes = [ctypes.c_longlong, i]
     lib.cdg_relu_mask_bytes.restype = ctypes.c_longlong
+    lib.cdg_wgrad_plan.argtypes = [i] * 13 + [ctypes.POINTER(hp)]
+    lib.cdg_wgrad_plan.restype = i
+    lib.cdg_wgrad_plan_host.argtypes = [i] * 14 + [ctypes.POINTER(hp)]
+    lib.cdg_wgrad_plan_host.restype = i
+    lib.cdg_wgrad_destroy.argtypes = [hp]
+    lib.cdg_wgrad_destroy.restype = None
+    lib.cdg_wgrad_workspace_bytes.argtypes = [hp]
+    lib.cdg_wgrad_workspace_bytes.restype = ctypes.c_size_t
+    lib.cdg_wgrad_get_info.argtypes = [hp, ctypes.POINTER(WgradInfo)]
+    lib.cdg_wgrad_get_info.restype = i
+    lib.cdg_wgrad.argtypes = [hp, vp, vp, vp, vp, vp]
+    lib.cdg_wgrad.restype = i
+    lib.cdg_wgrad_device_status.argtypes = [hp, vp]
+    lib.cdg_wgrad_device_status.restype = i
     if path == LIB_PATH:
         _lib = lib
     return lib
@@ -224,6 +240,73 @@ class Plan:
 
     def device_status(self, stream=None) -> int:
         return int(self.lib.cdg_device_status(self.handle, _stream(stream)))
+
+
+class WgradInfo(ctypes.Structure):
+    _fields_ = [("P", ctypes.c_int), ("Q", ctypes.c_int), ("tile_m", ctypes.c_int), ("tile_n", ctypes.c_int),
+                ("splits", ctypes.c_int), ("pos_box", ctypes.c_int * 3), ("blocks", ctypes.c_int),
+                ("stages", ctypes.c_int), ("work_items", ctypes.c_int), ("grid", ctypes.c_int),
+                ("smem_bytes", ctypes.c_int), ("tmem_cols", ctypes.c_int)]
+
+    def as_dict(self) -> dict:
+        d = {name: getattr(self, name) for name, _ in self._fields_}
+        d["pos_box"] = list(self.pos_box)
+        return d
+
+
+class WgradPlan:
+    """One planned wgrad shape (a ``cdg_wgrad_t``): dW = wgrad(dY, x)."""
+
+    def __init__(self, N, H, W, C, K, R, S, stride=1, pad=0, dil=1, dtype="bf16", out_f32=False, splits=0,
+                 host_sms: int | None = None):
+        self.lib = load_library()
+        self.shape = dict(N=N, H=H, W=W, C=C, K=K, R=R, S=S, stride=stride, pad=pad, dil=dil)
+        h = ctypes.c_void_p()
+        dt = DTYPES[dtype] if isinstance(dtype, str) else int(dtype)
+        args = (N, H, W, C, K, R, S, stride, pad, dil, dt, int(bool(out_f32)), int(splits))
+        if host_sms is None:
+            rc = self.lib.cdg_wgrad_plan(*args, ctypes.byref(h))
+        else:
+            rc = self.lib.cdg_wgrad_plan_host(*args, host_sms, ctypes.byref(h))
+        if rc != OK:
+            raise CdgError(rc, "cdg_wgrad_plan")
+        self.handle = h
+
+    def close(self):
+        if getattr(self, "handle", None) is not None and self.handle.value:
+            self.lib.cdg_wgrad_destroy(self.handle)
+        self.handle = None
+
+    def __del__(self):
+        self.close()
+
+    @property
+    def workspace_bytes(self) -> int:
+        return int(self.lib.cdg_wgrad_workspace_bytes(self.handle))
+
+    def info(self) -> dict:
+        inf = WgradInfo()
+        rc = self.lib.cdg_wgrad_get_info(self.handle, ctypes.byref(inf))
+        if rc != OK:
+            raise CdgError(rc, "cdg_wgrad_get_info")
+        return inf.as_dict()
+
+    def wgrad(self, dY, x, dW, workspace, stream=None) -> None:
+        rc = self.lib.cdg_wgrad(self.handle, _addr(dY), _addr(x), _addr(dW), _addr(workspace), _stream(stream))
+        if rc != OK:
+            raise CdgError(rc, "cdg_wgrad")
+
+    def device_status(self, stream=None) -> int:
+        return int(self.lib.cdg_wgrad_device_status(self.handle, _stream(stream)))
+
+
+def wgrad_plan(N, H, W, C, K, R, S, stride=1, pad=0, dil=1, dtype="bf16", out_f32=False, splits=0) -> WgradPlan:
+    return WgradPlan(N, H, W, C, K, R, S, stride, pad, dil, dtype, out_f32, splits)
+
+
+def wgrad_plan_host(N, H, W, C, K, R, S, stride=1, pad=0, dil=1, dtype="bf16", out_f32=False, splits=0,
+                    num_sms=148) -> WgradPlan:
+    return WgradPlan(N, H, W, C, K, R, S, stride, pad, dil, dtype, out_f32, splits, host_sms=num_sms)
 
 
 def plan(N, H, W, C, K, R, S, stride=1, pad=0, dil=1, dtype="bf16", relu=False, out_f32=False,

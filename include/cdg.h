@@ -257,6 +257,75 @@ const char *cdg_status_string(int status);
 int cdg_dgrad_noalloc(cdg_handle_t h, const void *dY, const void *W_krsc, void *dX, const void *relu_mask,
                       cdg_stream_t stream);
 
+/*
+ * Weight gradient (wgrad) of the same cross-correlation Conv2d, the
+ * follow-up the apache/tvm PR #10110 page ("[CUTLASS] Conv2d dgrad") names
+ * for dgrad, "wgrad + parallel split-k" (merge comment).  The page gives no
+ * formula; this library computes the definition
+ *
+ *   dW[k,r,s,c] = sum over n, p, q of
+ *                 dY[n,p,q,k] * x[n, p*stride - pad + r*dil, q*stride - pad + s*dil, c]
+ *
+ * with x read as zero outside the image.  dY NHWC [N][P][Q][K] and the
+ * forward input x NHWC [N][H][W][C] in dtype; dW KRSC [K][R][S][C] in dtype,
+ * or fp32 with out_f32 = 1.  fp32 accumulation.  The reduction over the
+ * N*P*Q positions is split into `splits` parts that run in parallel; their
+ * fp32 partials go to a caller-provided workspace and are added in a fixed
+ * order, so results are deterministic.
+ */
+typedef struct cdg_wgrad_st *cdg_wgrad_t;
+
+typedef struct {
+    int P, Q;
+    int tile_m;           /* dY channels per tile (GEMM M tile, 128)             */
+    int tile_n;           /* x channels per tile (GEMM N tile)                    */
+    int splits;           /* reduction splits                                     */
+    int pos_box[3];       /* positions per block along q, p, n (product 64)      */
+    int blocks;           /* position blocks of 64 in the reduction              */
+    int stages;           /* shared-memory pipeline depth                         */
+    int work_items;       /* (split, tap, m-tile, n-tile) items in one launch     */
+    int grid;             /* persistent CTAs                                      */
+    int smem_bytes;       /* dynamic shared memory per CTA                        */
+    int tmem_cols;        /* tensor-memory columns per CTA                        */
+} cdg_wgrad_info_t;
+
+/*
+ * Plan one wgrad shape on the current device.  Arguments as for cdg_plan
+ * (H, W are x's sizes); out_f32 0 or 1; splits = 0 lets the planner choose
+ * (enough work items to fill the SMs), k >= 1 asks for k (capped at the
+ * number of position blocks).  Errors: CDG_ERR_INVALID_ARG for bad sizes or
+ * flags, CDG_ERR_UNSUPPORTED when C or K is not a multiple of 8, stride > 4,
+ * R*S > 128, or H or W is smaller than the stride.  Free with
+ * cdg_wgrad_destroy.
+ */
+int cdg_wgrad_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int pad, int dil, int dtype,
+                   int out_f32, int splits, cdg_wgrad_t *out);
+
+/* The same planning without a device (num_sms stands in for the SM count);
+ * cdg_wgrad on such a handle returns CDG_ERR_NO_DEVICE. */
+int cdg_wgrad_plan_host(int N, int H, int W, int C, int K, int R, int S, int stride, int pad, int dil, int dtype,
+                        int out_f32, int splits, int num_sms, cdg_wgrad_t *out);
+
+void cdg_wgrad_destroy(cdg_wgrad_t h);
+
+/* Bytes of the fp32 workspace cdg_wgrad needs: splits * K * R * S * C * 4. */
+size_t cdg_wgrad_workspace_bytes(cdg_wgrad_t h);
+
+int cdg_wgrad_get_info(cdg_wgrad_t h, cdg_wgrad_info_t *info);
+
+/*
+ * dW = wgrad(dY, x): two kernel launches on stream (the split GEMM, then the
+ * ordered reduction), asynchronous.  All pointers are device pointers,
+ * 16-byte aligned; workspace holds cdg_wgrad_workspace_bytes(h) bytes and is
+ * overwritten; dW may not overlap dY, x or the workspace, nor the workspace
+ * dY or x (CDG_ERR_ALIAS).  dY and x are only read.  No allocation.  A
+ * device-side pipeline timeout is reported by cdg_wgrad_device_status.
+ */
+int cdg_wgrad(cdg_wgrad_t h, const void *dY, const void *x, void *dW, void *workspace, cdg_stream_t stream);
+
+/* Synchronise stream, then read and clear the plan's device status word. */
+int cdg_wgrad_device_status(cdg_wgrad_t h, cdg_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

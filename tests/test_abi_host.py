@@ -242,3 +242,65 @@ def test_gated_plans_fit_shared_memory(gate, out_f32):
         assert info["stages"] >= 3, (L.name, info)
         if gate == "bits" and info["tile_n"] < L.C:
             assert info["tile_n"] % 128 == 0, (L.name, info)
+
+
+WG_GOOD = (2, 8, 8, 16, 16, 3, 3, 1, 1, 1, cdg.BF16, 0, 0)
+
+
+@pytest.mark.parametrize("field,value,expect", [
+    (0, 0, 1), (3, 0, 1), (5, 0, 1), (8, -1, 1), (9, 0, 1), (10, 2, 1), (11, 2, 1), (12, -1, 1),
+    (3, 12, 2), (4, 20, 2), (7, 5, 2),
+    (1, 1, 0),  # H = 1 with a 3x3 pad-1 filter: P = 1, a valid geometry
+])
+def test_wgrad_argument_validation(field, value, expect):
+    args = list(WG_GOOD)
+    args[field] = value
+    lib = cdg.load_library()
+    h = ctypes.c_void_p()
+    rc = lib.cdg_wgrad_plan_host(*args, 148, ctypes.byref(h))
+    if h.value:
+        lib.cdg_wgrad_destroy(h)
+    assert rc == expect
+
+
+def test_wgrad_input_smaller_than_stride_is_unsupported():
+    with pytest.raises(cdg.CdgError) as e:
+        cdg.wgrad_plan_host(1, 1, 5, 8, 8, 1, 1, 2, 0, 1, "bf16")
+    assert e.value.status == 2
+
+
+@pytest.mark.parametrize("shape", [
+    (256, 56, 56, 64, 64, 1, 1, 1, 0, 1), (256, 56, 56, 64, 64, 3, 3, 1, 1, 1), (256, 28, 28, 128, 128, 3, 3, 1, 1, 1),
+    (256, 14, 14, 256, 256, 3, 3, 1, 1, 1), (256, 7, 7, 512, 512, 3, 3, 1, 1, 1), (256, 56, 56, 128, 128, 3, 3, 2, 1, 1),
+    (256, 14, 14, 1024, 2048, 1, 1, 2, 0, 1), (3, 9, 9, 8, 8, 3, 3, 2, 1, 1), (2, 7, 6, 320, 72, 3, 2, 1, 2, 2)])
+def test_wgrad_plans(shape):
+    """Position blocks hold exactly 64 positions; the splits divide the
+    blocks without an empty range; the workspace holds every split's dW;
+    shared memory and tensor memory stay within the SM's limits."""
+    N, H, W, C, K, R, S, st, pd, dl = shape
+    p = cdg.wgrad_plan_host(*shape, num_sms=148)
+    i = p.info()
+    qb, pb, nb = i["pos_box"]
+    assert qb * pb * nb == 64
+    P, Q = i["P"], i["Q"]
+    assert i["blocks"] == -(-Q // qb) * -(-P // pb) * -(-N // nb)
+    assert 1 <= i["splits"] <= i["blocks"]
+    tiles = R * S * -(-K // 128) * -(-C // i["tile_n"])
+    assert i["work_items"] == i["splits"] * tiles
+    assert i["work_items"] <= 148 or i["splits"] == 1
+    assert p.workspace_bytes == i["splits"] * K * R * S * C * 4
+    assert i["tile_n"] % 64 == 0 and i["tile_n"] <= 256
+    assert i["smem_bytes"] <= 232448 and i["stages"] >= 3
+    assert 2 * i["tile_n"] <= i["tmem_cols"] <= 512
+
+
+def test_wgrad_explicit_splits_are_capped_by_the_blocks():
+    p = cdg.wgrad_plan_host(1, 8, 8, 16, 16, 3, 3, 1, 1, 1, "bf16", splits=1000)
+    assert p.info()["splits"] == p.info()["blocks"] == 1
+
+
+def test_wgrad_host_plan_refuses_device_work():
+    p = cdg.wgrad_plan_host(1, 8, 8, 16, 16, 3, 3, 1, 1, 1, "bf16")
+    with pytest.raises(cdg.CdgError) as e:
+        p.wgrad(4096, 8192, 1 << 20, 1 << 24)
+    assert e.value.status == 7
