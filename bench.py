@@ -59,13 +59,16 @@ def load_peaks():
     return dict(FALLBACK_PEAKS, source="fallback")
 
 
+DGRAD_SOURCES = ("cdg_api.cu", "cdg_params.h", "dgrad_sm103.cu", "ptx.cuh", "wait.cuh")
+
+
 def kernel_sources_sha256() -> str:
-    import glob
+    """Hash of the files the dgrad kernel and its planner are built from."""
     import hashlib
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "implicit_gemm_dgrad_gb300", "csrc", "*"))):
-        h.update(os.path.basename(f).encode())
-        with open(f, "rb") as fh:
+    for name in DGRAD_SOURCES:
+        h.update(name.encode())
+        with open(os.path.join(ROOT, "implicit_gemm_dgrad_gb300", "csrc", name), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
 
