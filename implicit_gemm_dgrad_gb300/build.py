@@ -20,7 +20,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libcdg.so")
 BUILD_DIR = os.path.join(HERE, "_build")
-SOURCES = ["cdg_api.cu", "dgrad_sm103.cu", "wgrad_sm103.cu"]
+SOURCES = ["cdg_api.cu", "cwg_api.cu", "dgrad_sm103.cu", "wgrad_sm103.cu"]
 HEADERS = ["cdg_params.h", "cwg_params.h", "ptx.cuh", "wait.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

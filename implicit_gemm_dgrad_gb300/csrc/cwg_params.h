@@ -21,16 +21,18 @@ struct CwgParams {
     int *status;
     int N, H, W, C, K, P, Q, stride;
     int T;                // filter taps R*S
-    int BN;               // channels of x per tile (multiple of 64, <= 256)
+    int BN;               // channels of x per tile and tap (multiple of 64, <= 256)
+    int G;                // taps per work item: their B tiles side by side along N (G*BN <= 256)
+    int ngroups;          // ceil(T / G)
     int tiles_m, tiles_n; // ceil(K/128), ceil(C/BN)
     int splits;           // reduction splits
     int qb, pb, nb;       // position box (qb*pb*nb = 64)
     int bq, bp;           // boxes along q and p (blocks are numbered q fastest, then p, then n)
     int nblk;             // position blocks in all
     int stages;
-    int total_items;      // splits * T * tiles_m * tiles_n
-    uint32_t idesc;       // tcgen05 instruction descriptor (kind::f16, M=128, N=BN, both operands MN-major)
-    uint32_t stage_bytes; // A (2 slices x 8 KB) + B (BN/64 slices x 8 KB)
+    int total_items;      // splits * ngroups * tiles_m * tiles_n
+    uint32_t idesc;       // tcgen05 instruction descriptor (kind::f16, M=128, N=G*BN, both operands MN-major)
+    uint32_t stage_bytes; // A (2 slices x 8 KB) + B (G*BN/64 slices x 8 KB)
     uint32_t tmem_cols;   // two accumulators
     uint32_t acc_stride;
     int16_t tap_phase[CDG_MAX_TAPS];  // phase index (ph*stride + pw) of tap t

@@ -19,9 +19,12 @@
 // item's fp32 partial goes to its own slice of a workspace; a second kernel
 // adds the slices in split order (deterministic) and converts to dW's type.
 //
+// Narrow layers (C <= 128) put G taps side by side along N: the dY block is
+// the same for every tap, so one MMA of N = G*BN serves G taps' dW tiles.
+//
 // Roles per CTA (256 threads, one CTA per SM): warps 0, 2, 3 load the stages
-// round-robin (2 + BN/64 TMA copies each); warp 1 issues the MMAs; warps 4-7
-// read the accumulator and store fp32 rows of 32 channels with TMA.
+// round-robin (2 + G*BN/64 TMA copies each); warp 1 issues the MMAs; warps
+// 4-7 read the accumulator and store fp32 rows of 32 channels with TMA.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -59,17 +62,18 @@ struct WgRing {
     uint32_t full0, empty0, acc_full0, acc_empty0, drain;
 };
 
-// Work item g = ((split * T + t) * tiles_m + mt) * tiles_n + nt.
+// Work item g = ((split * ngroups + group) * tiles_m + mt) * tiles_n + nt;
+// group covers taps t0 .. t0 + G - 1 (those below T).
 struct WgItem {
-    int split, t, mt, nt;
+    int split, t0, mt, nt;
     __device__ __forceinline__ WgItem(const CwgParams &p, int g)
     {
         nt = g % p.tiles_n;
         int r = g / p.tiles_n;
         mt = r % p.tiles_m;
         r /= p.tiles_m;
-        t = r % p.T;
-        split = r / p.T;
+        t0 = (r % p.ngroups) * p.G;
+        split = r / p.ngroups;
     }
 };
 
@@ -85,7 +89,7 @@ __device__ __forceinline__ void run_wg_loader(const CwgParams &p, const WgRing &
 {
     const uint64_t mapA = reinterpret_cast<uint64_t>(&p.tmA);
     if (leader) asm volatile("prefetch.tensormap [%0];" ::"l"(mapA) : "memory");
-    const int nbs = p.BN / 64;
+    const int nbs = p.BN / 64;  // B slices per tap
     const uint32_t tx = p.stage_bytes;
     int stage = 0, owner = 0;
     uint32_t parity = 0;
@@ -94,8 +98,6 @@ __device__ __forceinline__ void run_wg_loader(const CwgParams &p, const WgRing &
         const WgItem it(p, g);
         int b0, b1;
         split_range(p, it.split, b0, b1);
-        const uint64_t mapB = reinterpret_cast<uint64_t>(&p.tmB[p.tap_phase[it.t]]);
-        const int di = p.tap_di[it.t], dj = p.tap_dj[it.t];
         const int k0 = it.mt * 128, c0 = it.nt * p.BN;
         for (int b = b0; b < b1; ++b) {
             if (owner == li) {
@@ -112,8 +114,16 @@ __device__ __forceinline__ void run_wg_loader(const CwgParams &p, const WgRing &
                     mbar_arrive_expect_tx(full, tx);
                     tma_load_4d(sa, mapA, full, k0, q0, p0, n0);
                     tma_load_4d(sa + kSlice, mapA, full, k0 + 64, q0, p0, n0);
-                    for (int j = 0; j < nbs; ++j)
-                        tma_load_4d(sa + 2 * kSlice + j * kSlice, mapB, full, c0 + 64 * j, q0 + dj, p0 + di, n0);
+                    for (int u = 0; u < p.G; ++u) {
+                        // tap t0 + u's x slices; a tap past T (short last group)
+                        // loads a box wholly past the images: zeros, never stored
+                        const int t = min(it.t0 + u, p.T - 1);
+                        const int nz = it.t0 + u < p.T ? n0 : n0 + p.N;
+                        const uint64_t mapB = reinterpret_cast<uint64_t>(&p.tmB[p.tap_phase[t]]);
+                        for (int j = 0; j < nbs; ++j)
+                            tma_load_4d(sa + static_cast<uint32_t>((2 + u * nbs + j) * kSlice), mapB, full, c0 + 64 * j,
+                                        q0 + p.tap_dj[t], p0 + p.tap_di[t], nz);
+                    }
                 }
                 __syncwarp();
             }
@@ -190,7 +200,8 @@ __device__ __forceinline__ void run_wg_epilogue(const CwgParams &p, const WgRing
         if (!wait_bar(R.acc_full0 + 8u * acc, (acc_count >> 1) & 1u, ctl)) break;
         tc_fence_after();
         const uint32_t taddr = tmem_base + acc * p.acc_stride + (static_cast<uint32_t>(quad * 32) << 16);
-        for (int cc = 0; cc < p.BN; cc += 32) {
+        const int NW = p.G * p.BN;  // accumulator columns: G taps x BN channels
+        for (int cc = 0; cc < NW; cc += 32) {
             const uint32_t k = chunk++;
             const uint32_t buf = R.out0 + (k & 1u) * (128u * 128u);
             if (k >= 2 && elected && static_cast<uint32_t>(ew) == ((k - 2) & 3u)) bulk_wait_group_read<0>();
@@ -199,7 +210,7 @@ __device__ __forceinline__ void run_wg_epilogue(const CwgParams &p, const WgRing
             tmem_ld_32x32b_x16(taddr + cc, *reinterpret_cast<uint32_t(*)[16]>(&r[0]));
             tmem_ld_32x32b_x16(taddr + cc + 16, *reinterpret_cast<uint32_t(*)[16]>(&r[16]));
             tmem_ld_wait();
-            if (cc + 32 >= p.BN) {  // last read of this accumulator
+            if (cc + 32 >= NW) {  // last read of this accumulator
                 tc_fence_before();
                 __syncwarp();
                 if (elected) mbar_arrive(R.acc_empty0 + 8u * acc);
@@ -210,8 +221,9 @@ __device__ __forceinline__ void run_wg_epilogue(const CwgParams &p, const WgRing
                              r[4 * q + 2], r[4 * q + 3]);
             fence_proxy_async_smem();
             named_bar_sync(1, 128);
-            if (elected && static_cast<uint32_t>(ew) == (k & 3u)) {
-                tma_store_4d(mapW, buf, it.nt * p.BN + cc, it.t, it.mt * 128, it.split);
+            const int u = cc / p.BN, t = it.t0 + u;
+            if (t < p.T && elected && static_cast<uint32_t>(ew) == (k & 3u)) {
+                tma_store_4d(mapW, buf, it.nt * p.BN + (cc - u * p.BN), t, it.mt * 128, it.split);
                 bulk_commit_group();
             }
         }

@@ -278,12 +278,13 @@ typedef struct cdg_wgrad_st *cdg_wgrad_t;
 typedef struct {
     int P, Q;
     int tile_m;           /* dY channels per tile (GEMM M tile, 128)             */
-    int tile_n;           /* x channels per tile (GEMM N tile)                    */
+    int tile_n;           /* x channels per tile and tap                          */
+    int taps_per_item;    /* taps whose tiles share one MMA along N (narrow C)    */
     int splits;           /* reduction splits                                     */
     int pos_box[3];       /* positions per block along q, p, n (product 64)      */
     int blocks;           /* position blocks of 64 in the reduction              */
     int stages;           /* shared-memory pipeline depth                         */
-    int work_items;       /* (split, tap, m-tile, n-tile) items in one launch     */
+    int work_items;       /* (split, tap group, m-tile, n-tile) items in one launch */
     int grid;             /* persistent CTAs                                      */
     int smem_bytes;       /* dynamic shared memory per CTA                        */
     int tmem_cols;        /* tensor-memory columns per CTA                        */

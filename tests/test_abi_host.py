@@ -285,13 +285,17 @@ def test_wgrad_plans(shape):
     P, Q = i["P"], i["Q"]
     assert i["blocks"] == -(-Q // qb) * -(-P // pb) * -(-N // nb)
     assert 1 <= i["splits"] <= i["blocks"]
-    tiles = R * S * -(-K // 128) * -(-C // i["tile_n"])
+    G = i["taps_per_item"]
+    assert 1 <= G and G * i["tile_n"] <= 256
+    if -(-C // i["tile_n"]) > 1:
+        assert G == 1
+    tiles = -(-(R * S) // G) * -(-K // 128) * -(-C // i["tile_n"])
     assert i["work_items"] == i["splits"] * tiles
     assert i["work_items"] <= 148 or i["splits"] == 1
     assert p.workspace_bytes == i["splits"] * K * R * S * C * 4
     assert i["tile_n"] % 64 == 0 and i["tile_n"] <= 256
     assert i["smem_bytes"] <= 232448 and i["stages"] >= 3
-    assert 2 * i["tile_n"] <= i["tmem_cols"] <= 512
+    assert 2 * G * i["tile_n"] <= i["tmem_cols"] <= 512
 
 
 def test_wgrad_explicit_splits_are_capped_by_the_blocks():

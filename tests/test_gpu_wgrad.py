@@ -25,6 +25,7 @@ CASES = [
     (3, 12, 12, 320, 64, 3, 3, 2, 1, 1, "bf16", "same", 5),
     (64, 7, 7, 256, 128, 3, 3, 1, 1, 1, "bf16", "same", 0),
     (2, 14, 14, 256, 256, 1, 1, 2, 0, 1, "bf16", "same", 1),
+    (2, 10, 9, 64, 64, 5, 1, 1, 2, 1, "bf16", "same", 0),   # taps in groups of 3 and 2
 ]
 
 
