@@ -17,11 +17,16 @@ resident in HBM.  Prints one JSON line:
   cpu_baseline the CPU oracle on a bounded sample (first images of each layer)
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--gate none|x|bits] [--autotune 1] [--layers L01,...]
+                    [--gate none|x|bits] [--autotune 1] [--layers L01,...] [--op dgrad|wgrad]
 
 --gate x|bits runs every layer with the fused ReLU-backward gate, reading the
 saved activation or its 1-bit packed mask; algorithmic bytes, the roofline and
 the end-to-end uploads then include that input.
+
+--op wgrad times the weight gradient of the same 22 layers instead (per layer
+one split-K GEMM launch and one ordered-reduction launch; dY and the forward
+input resident), with per-layer tensor fractions; it prints its own JSON line
+(metric "wgrad TFLOP/s ...").
 
 N > 1 (torchrun, one rank per GPU): every rank runs the full workload on its
 own GPU (replicas; dgrad has no exchange step), barrier + max over ranks.
