@@ -104,6 +104,33 @@ def tap_pixels(layer) -> int:
     return L.N * sum(0 <= h < L.H for h in rows) * sum(0 <= w < L.W for w in cols)
 
 
+def toolchain() -> dict:
+    """nvcc and driver versions (read-only queries; None where unavailable)."""
+    out = {"nvcc": None, "driver": None, "torch": None}
+    try:
+        import torch
+        out["torch"] = torch.__version__
+    except Exception:  # noqa: BLE001 - a missing version must not fail the bench
+        pass
+    try:
+        r = subprocess.run(["nvcc", "--version"], capture_output=True, text=True, timeout=20)
+        line = [x for x in r.stdout.splitlines() if "release" in x]
+        out["nvcc"] = line[-1].strip() if line else None
+    except Exception:  # noqa: BLE001
+        pass
+    try:
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() == 0:
+            buf = ctypes.create_string_buffer(96)
+            if lib.nvmlSystemGetDriverVersion(buf, ctypes.c_uint(96)) == 0:
+                out["driver"] = buf.value.decode()
+            lib.nvmlShutdown()
+    except Exception:  # noqa: BLE001
+        pass
+    return out
+
+
 def gate_bytes(layer, gate: str) -> int:
     """Algorithmic HBM bytes of one launch: dY + W + dX, plus the gate input
     read once where dX can be non-zero (tap_pixels): the saved activation
@@ -677,6 +704,7 @@ def main():
         "per_layer": per_layer,
         "per_layer_timing": "separate pass before the timed region, one CUDA event pair around every launch",
         "peaks": peaks,
+        "toolchain": toolchain(),
     }
     print(json.dumps(line), flush=True)
 
