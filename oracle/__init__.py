@@ -58,6 +58,8 @@ def _load():
             lib.oracle_conv_fwd.restype = i
             lib.oracle_wgrad.argtypes = [vp, vp, i, vp] + [i] * 10
             lib.oracle_wgrad.restype = i
+            lib.oracle_wgrad_elements.argtypes = [vp, vp, i, vp, ctypes.c_int64, vp] + [i] * 10
+            lib.oracle_wgrad_elements.restype = i
             lib.oracle_out_extent.argtypes = [i] * 5
             lib.oracle_out_extent.restype = i
             lib.oracle_half_to_double.argtypes = [ctypes.c_uint16]
@@ -166,6 +168,22 @@ def wgrad(dY, x, R, S, stride=1, pad=0, dil=1, dtype=None):
     if rc:
         raise RuntimeError("oracle_wgrad failed")
     return dW
+
+
+def wgrad_elements(dY, x, R, S, idx, stride=1, pad=0, dil=1, dtype=None):
+    """dW at the filter elements ``idx`` (int array [n][4] of (k, r, s, c)) -> [n]."""
+    code = _dtype_of(dY, dtype)
+    N, P, Q, K = dY.shape
+    _, H, Wd, C = x.shape
+    _check(dY, code)
+    _check(x, code)
+    idx = np.ascontiguousarray(idx, dtype=np.int32).reshape(-1, 4)
+    out = np.empty(idx.shape[0], np.float64)
+    rc = _load().oracle_wgrad_elements(_ptr(dY), _ptr(x), code, idx.ctypes.data_as(ctypes.c_void_p), idx.shape[0],
+                                       _ptr(out), N, H, Wd, C, K, R, S, stride, pad, dil)
+    if rc:
+        raise RuntimeError("oracle_wgrad_elements failed")
+    return out
 
 
 def conv_fwd(x, W, stride=1, pad=0, dil=1, dtype=None):

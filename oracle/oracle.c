@@ -336,6 +336,40 @@ int oracle_wgrad(const void *dY, const void *x, int dtype, double *dW,
     return 0;
 }
 
+/*
+ * Selected elements of the same weight gradient: idx holds nidx rows of
+ * (k, r, s, c); out[i] = dW[k,r,s,c] by the definition above, each summed over
+ * (n, p, q) in that order.  For spot checks of full-size problems: nothing is
+ * decoded ahead, every operand is read where the sum needs it.
+ */
+int oracle_wgrad_elements(const void *dY, const void *x, int dtype, const int32_t *idx, int64_t nidx,
+                          double *out, int N, int H, int W, int C, int K, int R, int S,
+                          int stride, int pad, int dil)
+{
+    int P, Q;
+    if (check_geometry(N, H, W, C, K, R, S, stride, pad, dil, &P, &Q)) return -1;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < nidx; ++i) {
+        const int k = idx[4 * i], r = idx[4 * i + 1], s = idx[4 * i + 2], c = idx[4 * i + 3];
+        double acc = 0.0;
+        if (k >= 0 && k < K && r >= 0 && r < R && s >= 0 && s < S && c >= 0 && c < C) {
+            for (int n = 0; n < N; ++n)
+                for (int p = 0; p < P; ++p) {
+                    const int h = p * stride - pad + r * dil;
+                    if (h < 0 || h >= H) continue;
+                    for (int q = 0; q < Q; ++q) {
+                        const int w = q * stride - pad + s * dil;
+                        if (w < 0 || w >= W) continue;
+                        acc += load_one(dY, (((size_t)n * P + p) * Q + q) * (size_t)K + k, dtype) *
+                               load_one(x, (((size_t)n * H + h) * W + w) * (size_t)C + c, dtype);
+                    }
+                }
+        }
+        out[i] = acc;
+    }
+    return 0;
+}
+
 /* Threads an OpenMP region of this library would use. */
 int oracle_num_threads(void)
 {

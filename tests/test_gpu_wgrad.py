@@ -89,3 +89,32 @@ def test_wgrad_splits_agree():
     _, three, _, _ = _run(tuple(c))
     assert_close(one, ref, odt, "one split")
     assert_close(three, ref, odt, "three splits")
+
+
+FULL = ["L01_1x1_64-64_56", "L04_3x3_64_56", "L06_3x3s2_128_56-28", "L20_1x1_2048-512_7", "L21_3x3_512_7"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_wgrad_full_size_sampled(name):
+    """Batch-256 ResNet-50 layers in the configuration bench.py --op wgrad
+    times (planner defaults: up to 152 splits, tap groups, 1x1x64 position
+    boxes), checked at 64 sampled filter elements (corners included) against
+    the oracle's element-by-element definition."""
+    import torch
+    import implicit_gemm_dgrad_gb300 as cdg
+    from implicit_gemm_dgrad_gb300.workloads import by_name
+    L = by_name(name)
+    dY, _, x = synth.make_inputs(L.shape(), L.dtype, L.dist, L.workload, L.index, with_x=True)
+    p = cdg.wgrad_plan(L.N, L.H, L.W, L.C, L.K, L.R, L.S, L.stride, L.pad, L.dil, L.dtype)
+    dW = GuardedOutput(L.K * L.R * L.S * L.C, 2)
+    ws = torch.empty(p.workspace_bytes // 4, dtype=torch.float32, device="cuda")
+    p.wgrad(to_dev(dY, L.dtype), to_dev(x.reshape(-1), L.dtype), dW.ptr, ws)
+    torch.cuda.synchronize()
+    assert p.device_status() == 0 and dW.guards_intact()
+    got = decode_out(dW.body().cpu().numpy(), L.dtype).reshape(L.K, L.R, L.S, L.C)
+    rng = np.random.default_rng(97)
+    idx = np.stack([rng.integers(0, L.K, 62), rng.integers(0, L.R, 62), rng.integers(0, L.S, 62),
+                    rng.integers(0, L.C, 62)], axis=1)
+    idx = np.concatenate([idx, [[0, 0, 0, 0], [L.K - 1, L.R - 1, L.S - 1, L.C - 1]]]).astype(np.int32)
+    ref = oracle.wgrad_elements(dY, x, L.R, L.S, idx, L.stride, L.pad, L.dil, dtype=L.dtype)
+    assert_close(got[idx[:, 0], idx[:, 1], idx[:, 2], idx[:, 3]], ref, L.dtype, name)

@@ -117,3 +117,15 @@ def test_wgrad_integer_inputs_exact(dtype):
         if 0 <= h < H and 0 <= w < W:
             exact[k, r, s] += dYi[n, p, q, k] * xi[n, h, w]
     assert np.array_equal(got, exact)
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+def test_wgrad_elements_agree_with_the_full_oracle(shape):
+    """The spot-check form (each element summed on its own) equals the pinned
+    full wgrad at every element."""
+    N, H, W, C, K, R, S, st, pd, dl = shape
+    dY, x = _case(shape, 41)
+    full = oracle.wgrad(dY, x, R, S, st, pd, dl)
+    idx = np.array(list(itertools.product(range(K), range(R), range(S), range(C))), np.int32)
+    got = oracle.wgrad_elements(dY, x, R, S, idx, st, pd, dl)
+    np.testing.assert_allclose(got, full.reshape(-1), rtol=1e-12, atol=1e-12)
