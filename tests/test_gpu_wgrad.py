@@ -118,3 +118,31 @@ def test_wgrad_full_size_sampled(name):
     idx = np.concatenate([idx, [[0, 0, 0, 0], [L.K - 1, L.R - 1, L.S - 1, L.C - 1]]]).astype(np.int32)
     ref = oracle.wgrad_elements(dY, x, L.R, L.S, idx, L.stride, L.pad, L.dil, dtype=L.dtype)
     assert_close(got[idx[:, 0], idx[:, 1], idx[:, 2], idx[:, 3]], ref, L.dtype, name)
+
+
+def test_wgrad_rejects_misaligned_and_aliased_tensors_before_launch():
+    """Pointer checks of cdg_wgrad on a device plan: 16-byte alignment of every
+    tensor and no overlap of dW or the workspace with an input or each other;
+    nothing is launched when they fail."""
+    import torch
+    import implicit_gemm_dgrad_gb300 as cdg
+    p = cdg.wgrad_plan(1, 8, 8, 16, 16, 3, 3, 1, 1, 1, "bf16")
+    dY = torch.zeros(8 * 8 * 16 + 64, dtype=torch.int16, device="cuda")
+    x = torch.zeros(8 * 8 * 16 + 64, dtype=torch.int16, device="cuda")
+    dW = torch.zeros(16 * 9 * 16 + 64, dtype=torch.int16, device="cuda")
+    ws = torch.zeros(p.workspace_bytes // 4 + 64, dtype=torch.float32, device="cuda")
+    base = (dY.data_ptr(), x.data_ptr(), dW.data_ptr(), ws.data_ptr())
+    for i in range(4):  # one pointer 8 bytes off alignment at a time
+        args = list(base)
+        args[i] += 8
+        with pytest.raises(cdg.CdgError) as e:
+            p.wgrad(*args)
+        assert e.value.status == 3
+    with pytest.raises(cdg.CdgError) as e:  # dW inside the workspace
+        p.wgrad(base[0], base[1], base[3], base[3])
+    assert e.value.status == 4
+    with pytest.raises(cdg.CdgError) as e:  # workspace over dY
+        p.wgrad(base[0], base[1], base[2], base[0])
+    assert e.value.status == 4
+    torch.cuda.synchronize()
+    assert p.device_status() == 0
