@@ -342,10 +342,13 @@ __global__ void wgrad_reduce_kernel(const float4 *__restrict__ ws, void *__restr
 }  // namespace
 }  // namespace cdg
 
+// The kernel's shared-memory limit is raised to the opt-in maximum once, not
+// to one plan's size: a later plan with a smaller footprint must not lower
+// the limit under an earlier plan that is still launched.
 cudaError_t cwg_prepare(size_t smem)
 {
-    return cudaFuncSetAttribute(cdg::wgrad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(smem));
+    if (smem > static_cast<size_t>(CDG_MAX_DYN_SMEM)) return cudaErrorInvalidValue;
+    return cudaFuncSetAttribute(cdg::wgrad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, CDG_MAX_DYN_SMEM);
 }
 
 cudaError_t cwg_launch(const CwgParams &p, int grid, size_t smem, cudaStream_t stream)

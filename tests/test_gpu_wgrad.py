@@ -146,3 +146,23 @@ def test_wgrad_rejects_misaligned_and_aliased_tensors_before_launch():
     assert e.value.status == 4
     torch.cuda.synchronize()
     assert p.device_status() == 0
+
+
+def test_wgrad_plans_with_different_footprints_coexist():
+    """A plan made after another, with less shared memory, leaves the earlier
+    plan launchable (the kernel's shared-memory limit is not lowered)."""
+    import torch
+    import implicit_gemm_dgrad_gb300 as cdg
+    big, small = CASES[5], CASES[1]  # 227 KB (256-channel tiles) and less (three 64-channel taps)
+    N, H, W, C, K, R, S, st, pd, dl, dtype, _, splits = big
+    a = cdg.wgrad_plan(N, H, W, C, K, R, S, st, pd, dl, dtype, splits=splits)
+    b = cdg.wgrad_plan(*small[:11], splits=small[12])
+    assert a.info()["smem_bytes"] > b.info()["smem_bytes"]
+    dY, x = _inputs(big, 11)
+    dW = GuardedOutput(K * R * S * C, 2)
+    ws = torch.empty(a.workspace_bytes // 4, dtype=torch.float32, device="cuda")
+    a.wgrad(to_dev(dY, dtype), to_dev(x, dtype), dW.ptr, ws)  # the earlier plan, launched last
+    torch.cuda.synchronize()
+    assert a.device_status() == 0 and dW.guards_intact()
+    got = decode_out(dW.body().cpu().numpy(), dtype).reshape(K, R, S, C)
+    assert_close(got, oracle.wgrad(dY, x, R, S, st, pd, dl, dtype=dtype), dtype, "earlier plan after a smaller one")
