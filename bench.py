@@ -142,6 +142,13 @@ def gate_bytes(layer, gate: str) -> int:
     return base + {"none": 0, "x": 2 * px * layer.C, "bits": px * 16 * ((layer.C + 127) // 128)}[gate]
 
 
+def wgrad_bytes(layer) -> int:
+    """Algorithmic HBM bytes of one wgrad: dY and the forward input x read
+    once, dW written once (2-byte elements)."""
+    L = layer
+    return 2 * (L.N * L.P * L.Q * L.K + L.N * L.H * L.W * L.C + L.K * L.R * L.S * L.C)
+
+
 def roofline_time_s(layer, peaks, gate="none"):
     t_tc = layer.flops / (peaks["bf16_tflops_sustained"] * 1e12)
     t_hbm = gate_bytes(layer, gate) / (peaks["hbm_gbs"] * 1e9)
@@ -403,11 +410,19 @@ def run_wgrad(args, rank, world, local_rank):
     total_ms = max_over_ranks(float(sum(e0[k].elapsed_time(e1[k]) for k in range(args.steps))), world)
     ms_per_step = total_ms / args.steps
     flops_step = sum(L.flops for (L, *_r) in state)
+    def roof(L):
+        t_tc = L.flops / (peaks["bf16_tflops_sustained"] * 1e12)
+        t_hbm = wgrad_bytes(L) / (peaks["hbm_gbs"] * 1e9)
+        return max(t_tc, t_hbm), ("tensor" if t_tc >= t_hbm else "hbm")
+
     per_layer = []
     for i, (L, p, *_r) in enumerate(state):
         t = per_ms[i] * 1e-3
         inf = p.info()
+        t_roof, bound = roof(L)
         per_layer.append({"layer": L.name, "ms": round(float(per_ms[i]), 5), "tflops": round(L.flops / t / 1e12, 2),
+                          "gbs": round(wgrad_bytes(L) / t / 1e9, 1), "bound": bound,
+                          "roofline_frac": round(t_roof / t, 4),
                           "tensor_peak_frac": round(L.flops / t / 1e12 / peaks["bf16_tflops_sustained"], 4),
                           "plan": {"splits": inf["splits"], "tile_n": inf["tile_n"], "pos_box": inf["pos_box"],
                                    "stages": inf["stages"], "work_items": inf["work_items"]}})
@@ -415,7 +430,12 @@ def run_wgrad(args, rank, world, local_rank):
         return
     dom = int(np.argmax(per_ms))
     Ld = state[dom][0]
-    achieved = Ld.flops / (per_ms[dom] * 1e-3) / 1e12
+    td = per_ms[dom] * 1e-3
+    _, dbound = roof(Ld)
+    if dbound == "tensor":
+        achieved, dpeak, dunit = Ld.flops / td / 1e12, peaks["bf16_tflops_sustained"], "TFLOP/s"
+    else:
+        achieved, dpeak, dunit = wgrad_bytes(Ld) / td / 1e9, peaks["hbm_gbs"], "GB/s"
     line = {"metric": "wgrad TFLOP/s per ResNet-50 layer (1 GB300)", "op": "wgrad",
             "value": round(world * flops_step * args.steps / (total_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
@@ -423,11 +443,12 @@ def run_wgrad(args, rank, world, local_rank):
             "config": {"workload": WORKLOAD.replace("dgrad", "wgrad"), "global_batch": 256 * world, "layers": nL,
                        "flops_per_step": flops_step, "parallelism": f"replicas x{world}",
                        "l2": "inputs larger than L2"},
-            "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops_sustained"],
-                         "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops_sustained"], 4),
-                         "traffic": None, "kernel": f"wgrad_kernel + reduce ({Ld.name})",
+            "roofline": {"bound": dbound, "achieved": round(achieved, 2), "peak": dpeak, "unit": dunit,
+                         "frac": round(achieved / dpeak, 4), "traffic": None,
+                         "algorithmic_bytes": wgrad_bytes(Ld), "kernel": f"wgrad_kernel + reduce ({Ld.name})",
                          "launch_ms": round(float(per_ms[dom]), 5),
-                         "peak_source": peaks["source"] + " sustained bf16"},
+                         "peak_source": peaks["source"] + (" sustained bf16" if dbound == "tensor" else " copy bandwidth"),
+                         "step_roofline_frac": round(sum(roof(L)[0] for (L, *_r) in state) / (ms_per_step * 1e-3), 4)},
             "gpu_launches": 2 * nL * args.steps, "clocks": clocks.summary(), "per_layer": per_layer,
             "per_layer_timing": "separate pass, one CUDA event pair around each layer's two launches"}
     print(json.dumps(line), flush=True)

@@ -49,3 +49,13 @@ def test_gate_bytes_per_mode():
         assert b.gate_bytes(L, "bits") == L.bytes + px * 16 * ((L.C + 127) // 128)
         if L.R == 1 and L.stride == 2:
             assert px * 4 == L.N * L.H * L.W  # three of four phases get no tap
+
+
+def test_wgrad_bytes():
+    """wgrad reads dY and the forward input once and writes dW once."""
+    b = _bench()
+    L = Layer("t", 2, 9, 7, 16, 24, 3, 3, 2, 1, 1)
+    assert b.wgrad_bytes(L) == 2 * (2 * L.P * L.Q * 24 + 2 * 9 * 7 * 16 + 24 * 9 * 16)
+    from implicit_gemm_dgrad_gb300.workloads import by_name
+    L01 = by_name("L01_1x1_64-64_56")  # 2 x 102.8 MB of activations, a 8 KB filter
+    assert abs(b.wgrad_bytes(L01) / 1e6 - 205.5) < 0.1
