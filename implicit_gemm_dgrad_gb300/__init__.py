@@ -139,6 +139,21 @@ def _addr(t) -> int | None:
     return t.data_ptr()
 
 
+def _check_buffer(t, nbytes: int, what: str) -> None:
+    """A tensor argument must be a contiguous CUDA tensor of at least nbytes
+    (the kernels read and write exactly the planned extents, which the C ABI
+    cannot check).  Raw integer pointers are passed through unchecked."""
+    if t is None or isinstance(t, int):
+        return
+    if not getattr(t, "is_cuda", False):
+        raise ValueError(f"{what} must be a CUDA tensor (or a device pointer)")
+    if not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+    have = t.numel() * t.element_size()
+    if have < nbytes:
+        raise ValueError(f"{what} holds {have} bytes; the plan needs {nbytes}")
+
+
 def _stream(s) -> int | None:
     if s is None:
         try:
@@ -162,6 +177,7 @@ class Plan:
         self.shape = dict(N=N, H=H, W=W, C=C, K=K, R=R, S=S, stride=stride, pad=pad, dil=dil)
         self.dtype = dtype
         self.relu = relu
+        self.relu_bits = relu_bits
         self.out_f32 = out_f32
         epi = (EPI_RELU_BWD if relu else 0) | (EPI_OUT_F32 if out_f32 else 0) | (EPI_RELU_BWD_BITS if relu_bits else 0)
         h = ctypes.c_void_p()
@@ -207,12 +223,35 @@ class Plan:
             raise CdgError(rc, "cdg_plan_get_info")
         return inf.as_dict()
 
+    def _sizes(self) -> dict:
+        """Bytes of each tensor of this plan's dgrad."""
+        d = self.shape
+        P, Q = self.output_dims
+        pixels = d["N"] * d["H"] * d["W"]
+        mask = 0
+        if self.relu_bits:
+            mask = relu_mask_bytes(pixels, d["C"])
+        elif self.relu:
+            mask = 2 * pixels * d["C"]
+        return {"dY": 2 * d["N"] * P * Q * d["K"], "W": 2 * d["K"] * d["R"] * d["S"] * d["C"],
+                "dX": (4 if self.out_f32 else 2) * pixels * d["C"], "mask": mask}
+
+    def _check(self, dY=None, W=None, W_packed=None, dX=None, relu_mask=None) -> None:
+        z = self._sizes()
+        _check_buffer(dY, z["dY"], "dY")
+        _check_buffer(W, z["W"], "W")
+        _check_buffer(W_packed, z["W"], "W_packed")
+        _check_buffer(dX, z["dX"], "dX")
+        _check_buffer(relu_mask, z["mask"], "relu_mask")
+
     def prepack_weights(self, W_krsc, W_packed, stream=None) -> None:
+        self._check(W=W_krsc, W_packed=W_packed)
         rc = self.lib.cdg_prepack_weights(self.handle, _addr(W_krsc), _addr(W_packed), _stream(stream))
         if rc != OK:
             raise CdgError(rc, "cdg_prepack_weights")
 
     def dgrad(self, dY, W_packed, dX, relu_mask=None, stream=None) -> None:
+        self._check(dY=dY, W_packed=W_packed, dX=dX, relu_mask=relu_mask)
         rc = self.lib.cdg_dgrad(self.handle, _addr(dY), _addr(W_packed), _addr(dX), _addr(relu_mask),
                                 _stream(stream))
         if rc != OK:
@@ -222,6 +261,7 @@ class Plan:
         """dgrad from the unpacked KRSC filter without any device allocation
         (the packed weights live in the library's own scratch array; see
         cdg_dgrad_noalloc in cdg.h for the size limit and the sharing rules)."""
+        self._check(dY=dY, W=W_krsc, dX=dX, relu_mask=relu_mask)
         rc = self.lib.cdg_dgrad_noalloc(self.handle, _addr(dY), _addr(W_krsc), _addr(dX), _addr(relu_mask),
                                         _stream(stream))
         if rc != OK:
@@ -231,6 +271,7 @@ class Plan:
         """Time every configuration the planner can produce for this shape on
         these tensors and keep the fastest (cdg_autotune); returns its mean
         launch time in ms.  dX receives the correct result."""
+        self._check(dY=dY, W_packed=W_packed, dX=dX, relu_mask=relu_mask)
         best = ctypes.c_float()
         rc = self.lib.cdg_autotune(self.handle, _addr(dY), _addr(W_packed), _addr(dX), _addr(relu_mask),
                                    _stream(stream), int(reps), ctypes.byref(best))
@@ -261,6 +302,7 @@ class WgradPlan:
                  host_sms: int | None = None):
         self.lib = load_library()
         self.shape = dict(N=N, H=H, W=W, C=C, K=K, R=R, S=S, stride=stride, pad=pad, dil=dil)
+        self.out_f32 = bool(out_f32)
         h = ctypes.c_void_p()
         dt = DTYPES[dtype] if isinstance(dtype, str) else int(dtype)
         args = (N, H, W, C, K, R, S, stride, pad, dil, dt, int(bool(out_f32)), int(splits))
@@ -292,6 +334,12 @@ class WgradPlan:
         return inf.as_dict()
 
     def wgrad(self, dY, x, dW, workspace, stream=None) -> None:
+        d = self.shape
+        inf = self.info()
+        _check_buffer(dY, 2 * d["N"] * inf["P"] * inf["Q"] * d["K"], "dY")
+        _check_buffer(x, 2 * d["N"] * d["H"] * d["W"] * d["C"], "x")
+        _check_buffer(dW, (4 if self.out_f32 else 2) * d["K"] * d["R"] * d["S"] * d["C"], "dW")
+        _check_buffer(workspace, self.workspace_bytes, "workspace")
         rc = self.lib.cdg_wgrad(self.handle, _addr(dY), _addr(x), _addr(dW), _addr(workspace), _stream(stream))
         if rc != OK:
             raise CdgError(rc, "cdg_wgrad")
@@ -328,6 +376,9 @@ def pack_relu_mask(x, bits, pixels: int, C: int, dtype="bf16", stream=None) -> N
     (cdg_pack_relu_mask), for plans made with relu_bits=True."""
     lib = load_library()
     dt = DTYPES[dtype] if isinstance(dtype, str) else int(dtype)
+    if int(pixels) >= 0 and int(C) > 0 and int(C) % 8 == 0:
+        _check_buffer(x, 2 * int(pixels) * int(C), "x")
+        _check_buffer(bits, relu_mask_bytes(pixels, C), "bits")
     rc = lib.cdg_pack_relu_mask(_addr(x), _addr(bits), int(pixels), int(C), dt, _stream(stream))
     if rc != OK:
         raise CdgError(rc, "cdg_pack_relu_mask")
