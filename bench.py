@@ -7,7 +7,10 @@ resident in HBM.  Prints one JSON line:
                layers / device time of the step), whole job over all ranks
   per_layer    each layer's TFLOP/s and its fraction of the slower-of
                (tensor, HBM) roofline, from a separate pass with one event
-               pair around every launch
+               pair around every launch; the tensor peak is the burst bf16
+               figure when the SM clock held its maximum during the timed
+               region, else the sustained one (roofline.peak_basis), and the
+               fraction on the other basis is printed beside it
   roofline     for the launch with the largest share of the step, timed with
                events around it inside the timed region (the other launches
                of a timed step run back to back, each overlapping its
@@ -15,6 +18,9 @@ resident in HBM.  Prints one JSON line:
   e2e          the same metric with dY uploaded from pinned host memory and
                dX read back every step, through the same C-ABI calls
   cpu_baseline the CPU oracle on a bounded sample (first images of each layer)
+  other_configs  after the timed region: the tiny 8x8 layer, the three batch-8
+               layers with warm and cold L2, the two x-gated batch-256 layers of
+               the fused ReLU-backward config, and each layer's weight prepack
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--gate none|x|bits] [--autotune 1] [--layers L01,...] [--op dgrad|wgrad]
@@ -149,10 +155,38 @@ def wgrad_bytes(layer) -> int:
     return 2 * (L.N * L.P * L.Q * L.K + L.N * L.H * L.W * L.C + L.K * L.R * L.S * L.C)
 
 
-def roofline_time_s(layer, peaks, gate="none"):
-    t_tc = layer.flops / (peaks["bf16_tflops_sustained"] * 1e12)
+def tensor_peak(peaks, basis: str) -> float:
+    """bf16 tensor peak in TFLOP/s: the burst figure (a GEMM timed alone, at
+    full clock) or the sustained one (seconds under the power cap)."""
+    return peaks["bf16_tflops"] if basis == "burst" else peaks["bf16_tflops_sustained"]
+
+
+def peak_basis(clocks: dict) -> str:
+    """Which tensor peak the timed region ran under: "burst" when the SM
+    clock sampled during it held (median within 5 % of the maximum), else
+    "sustained" (also when no clock could be read)."""
+    sm, smax = clocks.get("sm_mhz"), clocks.get("sm_max_mhz")
+    if sm and smax and sm >= 0.95 * smax:
+        return "burst"
+    return "sustained"
+
+
+def roofline_time_s(layer, peaks, gate="none", basis="burst"):
+    t_tc = layer.flops / (tensor_peak(peaks, basis) * 1e12)
     t_hbm = gate_bytes(layer, gate) / (peaks["hbm_gbs"] * 1e9)
     return max(t_tc, t_hbm), ("tensor" if t_tc >= t_hbm else "hbm")
+
+
+def layer_record(L, ms, peaks, basis, gate="none"):
+    """TFLOP/s, GB/s and the slower-of roofline fraction of one launch of
+    layer L that took `ms`, on the chosen tensor-peak basis (and on both)."""
+    t = ms * 1e-3
+    t_roof, bound = roofline_time_s(L, peaks, gate, basis)
+    other = "sustained" if basis == "burst" else "burst"
+    return {"ms": round(float(ms), 5), "tflops": round(L.flops / t / 1e12, 2),
+            "gbs": round(gate_bytes(L, gate) / t / 1e9, 1), "bound": bound, "roofline_frac": round(t_roof / t, 4),
+            f"roofline_frac_{other}": round(roofline_time_s(L, peaks, gate, other)[0] / t, 4),
+            "tensor_peak_frac": round(L.flops / t / 1e12 / tensor_peak(peaks, basis), 4)}
 
 
 class _NvmlClocks:
@@ -313,6 +347,108 @@ def cpu_oracle_sample(layers, arrays, images: int):
             "seconds": dt}
 
 
+def time_launches(torch, stream, fn, reps: int, flush=None) -> list:
+    """Device time (ms) of each of `reps` calls of fn, one CUDA event pair
+    around each on `stream`.  With `flush` (a byte buffer larger than L2), the
+    buffer is overwritten before every call, outside the events, so each call
+    starts with a cold L2."""
+    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(reps)]
+    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(reps)]
+    torch.cuda.synchronize()
+    for k in range(reps):
+        if flush is not None:
+            with torch.cuda.stream(stream):
+                flush.fill_(k & 0xFF)
+        e0[k].record(stream)
+        fn()
+        e1[k].record(stream)
+    torch.cuda.synchronize()
+    return [e0[k].elapsed_time(e1[k]) for k in range(reps)]
+
+
+def other_configs(torch, cdg, dev, stream, peaks, basis, host, state, reps=20):
+    """The workloads besides the batch-256 step, each timed on its own
+    (outside the timed region): the tiny 8x8 layer (launch-latency bound),
+    the three batch-8 layers with warm and with cold L2 (a buffer of twice the
+    L2 size written between calls), the two x-gated batch-256 layers of the
+    fused ReLU-backward config, and the weight prepack of every layer."""
+    from implicit_gemm_dgrad_gb300.workloads import BATCH8, FUSED_RELU, TINY
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or (128 << 20)
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    out = {"l2_flush_bytes": 2 * l2, "reps": reps}
+
+    def setup(L):
+        dY, W, x = synth.make_inputs(L.shape(), L.dtype, L.dist, L.workload, L.index, with_x=L.relu)
+        p = cdg.plan(L.N, L.H, L.W, L.C, L.K, L.R, L.S, L.stride, L.pad, L.dil, L.dtype, relu=L.relu,
+                     out_f32=(L.out == "f32"))
+        d_dY = torch.from_numpy(dY.view(np.int16)).to(dev)
+        d_W = torch.from_numpy(W.view(np.int16)).to(dev)
+        d_x = torch.from_numpy(x.reshape(-1).view(np.int16)).to(dev) if L.relu else None
+        d_Wp = torch.empty(p.packed_weight_bytes // 2, dtype=torch.int16, device=dev)
+        d_dX = torch.empty(L.N * L.H * L.W * L.C * (2 if L.out == "f32" else 1), dtype=torch.int16, device=dev)
+        p.prepack_weights(d_W, d_Wp, stream)
+        return p, (lambda: p.dgrad(d_dY, d_Wp, d_dX, d_x, stream))
+
+    def record(L, ms_list, gate="none"):
+        ms = float(np.median(ms_list))
+        rec = {"layer": L.name, "dtype": L.dtype, "out": L.out}
+        rec.update(layer_record(L, ms, peaks, basis, gate))
+        rec["ms_min"] = round(float(np.min(ms_list)), 5)
+        return rec
+
+    # tiny: 8x8x16, 3x3, fp16 in, fp32 out
+    p, run = setup(TINY)
+    for _ in range(5):
+        run()
+    ms = time_launches(torch, stream, run, reps)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(200):
+        run()
+    t1 = time.perf_counter()
+    torch.cuda.synchronize()
+    rec = record(TINY, ms)
+    rec["host_us_per_call"] = round((t1 - t0) / 200 * 1e6, 2)
+    rec["note"] = "launch-latency bound: the whole problem is 11 KB and 0.3 MFLOP"
+    if p.device_status(stream) != 0:
+        raise RuntimeError("device status after the tiny config")
+    out["tiny"] = rec
+
+    out["batch8"] = []
+    for L in BATCH8:
+        p, run = setup(L)
+        for _ in range(5):
+            run()
+        warm = time_launches(torch, stream, run, reps)
+        cold = time_launches(torch, stream, run, reps, flush)
+        if p.device_status(stream) != 0:
+            raise RuntimeError(f"device status after {L.name}")
+        rec = {"layer": L.name, "cold_l2": record(L, cold), "warm_l2": record(L, warm)}
+        out["batch8"].append(rec)
+
+    out["fused_relu_x"] = []
+    for L in FUSED_RELU:
+        p, run = setup(L)
+        for _ in range(5):
+            run()
+        ms = time_launches(torch, stream, run, reps, flush)
+        if p.device_status(stream) != 0:
+            raise RuntimeError(f"device status after {L.name}")
+        rec = record(L, ms, "x")
+        rec["gate"] = "saved bf16 activation x, read once where dX can be non-zero; cold L2"
+        out["fused_relu_x"].append(rec)
+
+    # weight prepack (KRSC -> packed B operand), once per weight update; not part of the metric
+    prep = {}
+    for (L, p, _d_dY, d_Wp, _d_dX), (_dY, W, _x) in zip(state, host):
+        d_W = torch.from_numpy(W.view(np.int16)).to(dev)
+        ms = time_launches(torch, stream, lambda: p.prepack_weights(d_W, d_Wp, stream), 5, flush)
+        prep[L.name] = round(float(np.median(ms)), 5)
+    out["prepack_ms"] = prep
+    del flush
+    return out
+
+
 def max_over_ranks(x: float, world: int) -> float:
     """The largest of every rank's x (the slowest replica's time), reduced over
     the gloo control group; x itself when there is one rank."""
@@ -410,8 +546,11 @@ def run_wgrad(args, rank, world, local_rank):
     total_ms = max_over_ranks(float(sum(e0[k].elapsed_time(e1[k]) for k in range(args.steps))), world)
     ms_per_step = total_ms / args.steps
     flops_step = sum(L.flops for (L, *_r) in state)
-    def roof(L):
-        t_tc = L.flops / (peaks["bf16_tflops_sustained"] * 1e12)
+    clk = clocks.summary()
+    basis = peak_basis(clk)
+
+    def roof(L, b=basis):
+        t_tc = L.flops / (tensor_peak(peaks, b) * 1e12)
         t_hbm = wgrad_bytes(L) / (peaks["hbm_gbs"] * 1e9)
         return max(t_tc, t_hbm), ("tensor" if t_tc >= t_hbm else "hbm")
 
@@ -423,7 +562,9 @@ def run_wgrad(args, rank, world, local_rank):
         per_layer.append({"layer": L.name, "ms": round(float(per_ms[i]), 5), "tflops": round(L.flops / t / 1e12, 2),
                           "gbs": round(wgrad_bytes(L) / t / 1e9, 1), "bound": bound,
                           "roofline_frac": round(t_roof / t, 4),
-                          "tensor_peak_frac": round(L.flops / t / 1e12 / peaks["bf16_tflops_sustained"], 4),
+                          "roofline_frac_sustained" if basis == "burst" else "roofline_frac_burst":
+                              round(roof(L, "sustained" if basis == "burst" else "burst")[0] / t, 4),
+                          "tensor_peak_frac": round(L.flops / t / 1e12 / tensor_peak(peaks, basis), 4),
                           "plan": {"splits": inf["splits"], "tile_n": inf["tile_n"], "pos_box": inf["pos_box"],
                                    "stages": inf["stages"], "work_items": inf["work_items"]}})
     if rank != 0:
@@ -433,7 +574,7 @@ def run_wgrad(args, rank, world, local_rank):
     td = per_ms[dom] * 1e-3
     _, dbound = roof(Ld)
     if dbound == "tensor":
-        achieved, dpeak, dunit = Ld.flops / td / 1e12, peaks["bf16_tflops_sustained"], "TFLOP/s"
+        achieved, dpeak, dunit = Ld.flops / td / 1e12, tensor_peak(peaks, basis), "TFLOP/s"
     else:
         achieved, dpeak, dunit = wgrad_bytes(Ld) / td / 1e9, peaks["hbm_gbs"], "GB/s"
     line = {"metric": "wgrad TFLOP/s per ResNet-50 layer (1 GB300)", "op": "wgrad",
@@ -447,9 +588,10 @@ def run_wgrad(args, rank, world, local_rank):
                          "frac": round(achieved / dpeak, 4), "traffic": None,
                          "algorithmic_bytes": wgrad_bytes(Ld), "kernel": f"wgrad_kernel + reduce ({Ld.name})",
                          "launch_ms": round(float(per_ms[dom]), 5),
-                         "peak_source": peaks["source"] + (" sustained bf16" if dbound == "tensor" else " copy bandwidth"),
+                         "peak_source": peaks["source"] + (f" {basis} bf16" if dbound == "tensor" else " copy bandwidth"),
+                         "peak_basis": basis,
                          "step_roofline_frac": round(sum(roof(L)[0] for (L, *_r) in state) / (ms_per_step * 1e-3), 4)},
-            "gpu_launches": 2 * nL * args.steps, "clocks": clocks.summary(), "per_layer": per_layer,
+            "gpu_launches": 2 * nL * args.steps, "clocks": clk, "per_layer": per_layer,
             "per_layer_timing": "separate pass, one CUDA event pair around each layer's two launches"}
     print(json.dumps(line), flush=True)
 
@@ -465,6 +607,8 @@ def main():
                     help="images per layer in the CPU-oracle baseline (256 = the whole batch, ~13 s on 16 cores)")
     ap.add_argument("--ref-images", type=int, default=8, help="images per layer per reference-arm step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-configs", action="store_true",
+                    help="skip the tiny, batch-8, x-gated and prepack measurements after the timed region")
     ap.add_argument("--layers", default="", help="comma-separated layer names (default: all 22)")
     ap.add_argument("--autotune", type=int, default=0,
                     help="1: tune every layer's plan with cdg_autotune during set-up (untimed)")
@@ -608,36 +752,38 @@ def main():
     flops_step = sum(L.flops for (L, *_r) in state)
     value = world * flops_step * args.steps / (total_ms * 1e-3) / 1e12
 
+    clk = clocks.summary()
+    basis = peak_basis(clk)
     per_layer = []
     for i, (L, p, *_r) in enumerate(state):
-        t = per_layer_ms[i] * 1e-3
-        t_roof, bound = roofline_time_s(L, peaks, gate)
         inf = p.info()
-        per_layer.append({"layer": L.name, "ms": round(per_layer_ms[i], 5),
-                          "plan": {"a_mode": inf["a_mode"], "cta_pair": inf["cta_pair"], "mma_warps": inf["mma_warps"],
-                                   "tile_n": inf["tile_n"], "stages": inf["stages"], "tuned": inf["tuned"]},
-                          "tflops": round(L.flops / t / 1e12, 2),
-                          "gbs": round(gate_bytes(L, gate) / t / 1e9, 1), "bound": bound,
-                          "roofline_frac": round(t_roof / t, 4),
-                          "tensor_peak_frac": round(L.flops / t / 1e12 / peaks["bf16_tflops_sustained"], 4)})
+        rec = {"layer": L.name}
+        rec.update(layer_record(L, per_layer_ms[i], peaks, basis, gate))
+        rec["plan"] = {"a_mode": inf["a_mode"], "cta_pair": inf["cta_pair"], "mma_warps": inf["mma_warps"],
+                       "tile_n": inf["tile_n"], "stages": inf["stages"], "tuned": inf["tuned"]}
+        per_layer.append(rec)
 
     # dominant launch: the layer with the largest share of the step, timed inside the timed region
     Ld = state[dom][0]
     td = dom_ms * 1e-3
-    _, bound = roofline_time_s(Ld, peaks, gate)
+    _, bound = roofline_time_s(Ld, peaks, gate, basis)
     if bound == "tensor":
-        achieved, peak, unit = Ld.flops / td / 1e12, peaks["bf16_tflops_sustained"], "TFLOP/s"
+        achieved, peak, unit = Ld.flops / td / 1e12, tensor_peak(peaks, basis), "TFLOP/s"
     else:
         achieved, peak, unit = gate_bytes(Ld, gate) / td / 1e9, peaks["hbm_gbs"], "GB/s"
+    step_roof = {b: sum(roofline_time_s(L, peaks, gate, b)[0] for (L, *_r) in state) / (ms_per_step * 1e-3)
+                 for b in ("burst", "sustained")}
     roofline = {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
                 "frac": round(achieved / peak, 4),
                 "traffic": profiled_traffic(Ld.name) if gate == "none" else None,
                 "algorithmic_bytes": gate_bytes(Ld, gate), "kernel": f"dgrad_kernel ({Ld.name})",
-                "peak_source": peaks["source"] + (" sustained bf16" if bound == "tensor" else " copy bandwidth"),
+                "peak_source": peaks["source"] + (f" {basis} bf16" if bound == "tensor" else " copy bandwidth"),
+                "peak_basis": basis,
                 "launch_ms": round(dom_ms, 5),
                 "share_of_step": round(dom_ms / ms_per_step, 4),
-                "step_roofline_frac": round(sum(roofline_time_s(L, peaks, gate)[0] for (L, *_r) in state)
-                                            / (ms_per_step * 1e-3), 4)}
+                "step_roofline_frac": round(step_roof[basis], 4),
+                "step_roofline_frac_burst": round(step_roof["burst"], 4),
+                "step_roofline_frac_sustained": round(step_roof["sustained"], 4)}
 
     # ---- end to end: dY from pinned host memory, dX back to pinned host memory, every step
     h_dY = [torch.from_numpy(h[0].view(np.int16)).pin_memory() for h in host]
@@ -698,6 +844,7 @@ def main():
 
     if rank != 0:
         return
+    configs = None if args.no_other_configs else other_configs(torch, cdg, dev, stream, peaks, basis, host, state)
     cpu = None
     if not args.no_cpu_baseline:
         c = cpu_oracle_sample([s[0] for s in state], host, args.cpu_images)
@@ -720,10 +867,11 @@ def main():
                 "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
                 "copies": "pinned host buffers; uploads, kernels and read-backs on three streams"},
         "gpu_launches": nL * args.steps,
-        "clocks": clocks.summary(),
+        "clocks": clk,
         "host_wall_s_timed": round(t_host1 - t_host0, 4),
         "per_layer": per_layer,
         "per_layer_timing": "separate pass before the timed region, one CUDA event pair around every launch",
+        "other_configs": configs,
         "peaks": peaks,
         "toolchain": toolchain(),
     }

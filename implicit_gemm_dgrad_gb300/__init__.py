@@ -34,7 +34,8 @@ DTYPES = {"f16": F16, "bf16": BF16}
 
 EXPORTS = ("cdg_plan", "cdg_plan_host", "cdg_destroy", "cdg_get_output_dims", "cdg_packed_weight_bytes",
            "cdg_plan_get_info", "cdg_prepack_weights", "cdg_dgrad", "cdg_device_status", "cdg_status_string",
-           "cdg_dgrad_noalloc", "cdg_autotune", "cdg_pack_relu_mask", "cdg_relu_mask_bytes",
+           "cdg_dgrad_noalloc", "cdg_dgrad_noalloc_status", "cdg_autotune", "cdg_plan_set_wait_limit",
+           "cdg_plan_withhold_load_for_test", "cdg_pack_relu_mask", "cdg_relu_mask_bytes",
            "cdg_wgrad_plan", "cdg_wgrad_plan_host", "cdg_wgrad_destroy", "cdg_wgrad_workspace_bytes",
            "cdg_wgrad_get_info", "cdg_wgrad", "cdg_wgrad_device_status")
 
@@ -99,6 +100,12 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.cdg_status_string.restype = ctypes.c_char_p
     lib.cdg_dgrad_noalloc.argtypes = [hp, vp, vp, vp, vp, vp]
     lib.cdg_dgrad_noalloc.restype = i
+    lib.cdg_dgrad_noalloc_status.argtypes = [vp]
+    lib.cdg_plan_set_wait_limit.argtypes = [hp, ctypes.c_ulonglong]
+    lib.cdg_plan_set_wait_limit.restype = i
+    lib.cdg_plan_withhold_load_for_test.argtypes = [hp, i]
+    lib.cdg_plan_withhold_load_for_test.restype = i
+    lib.cdg_dgrad_noalloc_status.restype = i
     lib.cdg_autotune.argtypes = [hp, vp, vp, vp, vp, vp, i, ctypes.POINTER(ctypes.c_float)]
     lib.cdg_autotune.restype = i
     lib.cdg_pack_relu_mask.argtypes = [vp, vp, ctypes.c_longlong, i, i, vp]
@@ -147,6 +154,14 @@ def _check_buffer(t, nbytes: int, what: str) -> None:
         return
     if not getattr(t, "is_cuda", False):
         raise ValueError(f"{what} must be a CUDA tensor (or a device pointer)")
+    idx = getattr(getattr(t, "device", None), "index", None)
+    if idx is not None:
+        import torch
+        cur = torch.cuda.current_device()
+        if idx != cur:
+            # the library launches on the current device; a pointer into
+            # another GPU's memory would be read by this one's kernels
+            raise ValueError(f"{what} is on cuda:{idx}, but the current device is cuda:{cur}")
     if not t.is_contiguous():
         raise ValueError(f"{what} must be contiguous")
     have = t.numel() * t.element_size()
@@ -267,6 +282,13 @@ class Plan:
         if rc != OK:
             raise CdgError(rc, "cdg_dgrad_noalloc")
 
+    @staticmethod
+    def noalloc_status(stream=None) -> int:
+        """Read and clear the status word of cdg_dgrad_noalloc launches on the
+        current device (cdg_dgrad_noalloc_status): 0, or the CDG_ERR_TIMEOUT
+        code of a launch that gave up a bounded wait."""
+        return int(load_library().cdg_dgrad_noalloc_status(_stream(stream)))
+
     def autotune(self, dY, W_packed, dX, relu_mask=None, stream=None, reps: int = 3) -> float:
         """Time every configuration the planner can produce for this shape on
         these tensors and keep the fastest (cdg_autotune); returns its mean
@@ -281,6 +303,21 @@ class Plan:
 
     def device_status(self, stream=None) -> int:
         return int(self.lib.cdg_device_status(self.handle, _stream(stream)))
+
+    def set_wait_limit(self, ns: int) -> None:
+        """Longest time any single pipeline wait of this plan's kernel may
+        take before the launch aborts with CDG_ERR_TIMEOUT (cdg_plan_set_wait_limit)."""
+        rc = self.lib.cdg_plan_set_wait_limit(self.handle, int(ns))
+        if rc != OK:
+            raise CdgError(rc, "cdg_plan_set_wait_limit")
+
+    def withhold_load_for_test(self, stage: int) -> None:
+        """Test only: make launches withhold the operand load of pipeline stage
+        `stage` in every CTA, so they take the bounded-wait timeout path
+        (cdg_plan_withhold_load_for_test); -1 restores normal launches."""
+        rc = self.lib.cdg_plan_withhold_load_for_test(self.handle, int(stage))
+        if rc != OK:
+            raise CdgError(rc, "cdg_plan_withhold_load_for_test")
 
 
 class WgradInfo(ctypes.Structure):

@@ -93,6 +93,8 @@ struct cdg_plan_st {
     const void *cached_dY, *cached_Wp;
     void *cached_dX;
     const void *cached_mask;
+    int il_phases, il_items;  // interleaving the planner would use, before the grid is known
+    bool noalloc_grid_checked;  // host plan: pair grid checked against the device (cdg_dgrad_noalloc)
     cdg_plan_info_t info;
 };
 
@@ -147,6 +149,21 @@ int choose_bn(int C, int max_bn, int step)
         }
     }
     return best;
+}
+
+// Set the persistent grid and the interleaving that goes with it: every
+// scheduling round of G items (G = CTAs, or CTA pairs) must hold whole groups
+// of `il_phases` items, else the phases run one after another.
+void apply_grid(cdg_plan_st *h, int grid)
+{
+    CdgParams &p = h->prm;
+    h->grid = grid;
+    h->info.grid = grid;
+    const int G = p.pair ? grid / 2 : grid;
+    const bool ok = h->il_phases > 0 && G % h->il_phases == 0 && 1LL * h->il_phases * h->il_items >= G;
+    p.interleave = ok ? h->il_phases : 0;
+    p.il_items = ok ? h->il_items : 0;
+    p.il_round = G;
 }
 
 PlanOpts opts_from_env()
@@ -456,6 +473,8 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     // Programmatic dependent launch: the kernel's set-up overlaps the end of the
     // previous kernel in the stream ("0" turns it off).
     p.pdl = opt.pdl == 0 ? 0 : 1;
+    p.wait_limit_ns = CDG_WAIT_LIMIT_NS;
+    p.withhold_stage = -1;
     p.mask_bits = h->mask_bits ? 1 : 0;
     // gate loads take the dX store box: its rows x the activation chunk's bytes
     // (64 channels; 32 with fp32 output) or the item's mask bytes per row
@@ -486,17 +505,9 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     h->smem = static_cast<size_t>(1024 + ring_bytes + staging + CDG_SMEM_TAIL);
     h->grid = pair ? 2 * std::max(1, std::min(num_sms / 2, items)) : std::max(1, std::min(num_sms, items));
 
-    auto set_round = [&]() {
-        // interleaving needs every round of G items to hold whole groups of
-        // `interleave` items (G = CTAs, or CTA pairs)
-        const int G = pair ? h->grid / 2 : h->grid;
-        if (p.interleave > 0 && (G % p.interleave != 0 || 1LL * p.interleave * p.il_items < G)) {
-            p.interleave = 0;
-            p.il_items = 0;
-        }
-        p.il_round = G;
-    };
-    set_round();
+    h->il_phases = p.interleave;
+    h->il_items = p.il_items;
+    apply_grid(h, h->grid);
 
     cdg_plan_info_t &inf = h->info;
     std::memset(&inf, 0, sizeof inf);
@@ -522,9 +533,7 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
             return CDG_ERR_CUDA;
         }
         const int pairs = cdg_max_active_pairs(h->out_type, h->in_type, h->mask, h->smem);
-        if (pairs >= 1) h->grid = 2 * std::max(1, std::min(pairs, items));
-        inf.grid = h->grid;
-        set_round();
+        if (pairs >= 1) apply_grid(h, 2 * std::max(1, std::min(pairs, items)));
     }
     if (!host_only) {
         if (cudaGetDevice(&h->device) != cudaSuccess ||
@@ -932,6 +941,22 @@ int cdg_autotune(cdg_handle_t h, const void *dY, const void *Wpacked, void *dX, 
     return CDG_OK;
 }
 
+int cdg_plan_set_wait_limit(cdg_handle_t h, unsigned long long ns)
+{
+    if (!h || ns < 100000ull || ns > 60000000000ull) return CDG_ERR_INVALID_ARG;
+    h->prm.wait_limit_ns = ns;
+    return CDG_OK;
+}
+
+int cdg_plan_withhold_load_for_test(cdg_handle_t h, int stage)
+{
+    if (!h || stage < -1) return CDG_ERR_INVALID_ARG;
+    // only the per-tap / row loaders of single CTAs honour it
+    if (stage >= 0 && (h->prm.halo || h->prm.pair)) return CDG_ERR_UNSUPPORTED;
+    h->prm.withhold_stage = stage;
+    return CDG_OK;
+}
+
 int cdg_device_status(cdg_handle_t h, cdg_stream_t stream)
 {
     if (!h) return CDG_ERR_INVALID_ARG;
@@ -1004,20 +1029,34 @@ unsigned g_noalloc_prepared[kNoallocMaxDevices];     // kernels whose shared-mem
 
 // Once per device (with that device current): the scratch's device address,
 // and the dynamic shared-memory opt-in of the kernel instantiation `key`.
-int noalloc_setup(int dev, const cdg_plan_st *h, unsigned char **scratch)
+int noalloc_address(int dev, unsigned char **scratch)
 {
-    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
     if (!g_noalloc_addr[dev]) {
         void *addr = nullptr;
         if (cudaGetSymbolAddress(&addr, cdg_noalloc_scratch) != cudaSuccess || !addr) return CDG_ERR_CUDA;
         g_noalloc_addr[dev] = static_cast<unsigned char *>(addr);
     }
+    *scratch = g_noalloc_addr[dev];
+    return CDG_OK;
+}
+
+int noalloc_setup(int dev, cdg_plan_st *h, unsigned char **scratch)
+{
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    const int rc = noalloc_address(dev, scratch);
+    if (rc != CDG_OK) return rc;
     const unsigned key = 1u << (h->out_type * 4 + h->in_type * 2 + (h->mask ? 1 : 0));
     if (!(g_noalloc_prepared[dev] & key)) {
         if (cdg_prepare_dgrad(h->out_type, h->in_type, h->mask, h->smem) != cudaSuccess) return CDG_ERR_CUDA;
         g_noalloc_prepared[dev] |= key;
     }
-    *scratch = g_noalloc_addr[dev];
+    // A plan made without a device sized a CTA-pair grid from the SM count
+    // alone; on this device only as many pairs as fit at once run per round.
+    if (h->host_only && h->prm.pair && !h->noalloc_grid_checked) {
+        const int pairs = cdg_max_active_pairs(h->out_type, h->in_type, h->mask, h->smem);
+        if (pairs >= 1 && 2 * pairs < h->grid) apply_grid(h, 2 * pairs);
+        h->noalloc_grid_checked = true;
+    }
     return CDG_OK;
 }
 
@@ -1068,4 +1107,27 @@ extern "C" int cdg_dgrad_noalloc(cdg_handle_t h, const void *dY, const void *W_k
     if (cdg_launch_dgrad(p, h->out_type, h->in_type, h->mask, h->grid, h->smem, s) != cudaSuccess)
         return CDG_ERR_CUDA;
     return CDG_OK;
+}
+
+extern "C" int cdg_dgrad_noalloc_status(cdg_stream_t stream)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return CDG_ERR_CUDA;
+    if (dev < 0 || dev >= kNoallocMaxDevices) return CDG_ERR_UNSUPPORTED;
+    unsigned char *scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+        const int rc = noalloc_address(dev, &scratch);
+        if (rc != CDG_OK) return rc;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int v = 0;
+    if (cudaMemcpyAsync(&v, scratch, sizeof v, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return CDG_ERR_CUDA;
+    if (v != 0) {
+        if (cudaMemsetAsync(scratch, 0, sizeof(int), s) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess)
+            return CDG_ERR_CUDA;
+    }
+    return v;
 }

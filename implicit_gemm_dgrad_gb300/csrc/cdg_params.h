@@ -19,7 +19,7 @@
 #define CDG_THREADS 256
 #define CDG_LOADERS 3
 #define CDG_EPI_WARP0 4
-#define CDG_WAIT_LIMIT_NS 4000000000ull  // a pipeline wait gives up after 4 s
+#define CDG_WAIT_LIMIT_NS 4000000000ull  // a pipeline wait gives up after 4 s (default)
 // Shared memory after the operand ring: two 16 KB output staging buffers
 // (128 rows x 128 B, the box a TMA store writes; four when the ReLU-backward
 // gate reads the saved activation, whose chunks land in them ahead of use; two
@@ -97,6 +97,10 @@ struct CdgParams {  // CUtensorMap members carry their own (128-byte) alignment
     uint32_t tx_bytes;    // bytes one pipeline stage receives (A box + B box)
     uint32_t tmem_cols;   // allocated TMEM columns (two accumulators)
     uint32_t acc_stride;  // column offset of the second accumulator
+    unsigned long long wait_limit_ns;  // a pipeline wait gives up (status CDG_ERR_TIMEOUT) after this long
+    int withhold_stage;   // test only: >= 0 makes every per-tap/row loader skip the load (and its
+                          // transaction count) of its stage with this sequence number, so the MMA
+                          // warp's wait for it runs out; -1 in normal use
     CdgPhase phase[CDG_MAX_PHASES];
     CdgTap tap[CDG_MAX_TAPS];
 };

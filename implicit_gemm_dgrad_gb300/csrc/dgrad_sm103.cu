@@ -147,6 +147,8 @@ __device__ __forceinline__ void run_loader(const CdgParams &p, const Ring &R, co
     int stage = 0;
     uint32_t parity = 0;
     int owner = 0;  // loader index of the current global stage
+    int seq = 0;    // sequence number of the current stage (all loaders count every stage)
+    const int withhold = p.withhold_stage;
     bool ok = true;
     for (ItemWalk w(tab, p.nphases, S.start, S.step, p.interleave, p.il_items, p.il_round); ok && w.valid(); w.next()) {
         const CdgPhase &ph = tab[w.phase];
@@ -170,7 +172,11 @@ __device__ __forceinline__ void run_loader(const CdgParams &p, const Ring &R, co
                         ok = false;
                         break;
                     }
-                    if (leader) {
+                    // (test only) a withheld stage gets neither its copies nor
+                    // their byte count, and is not recorded for the abort drain:
+                    // its full barrier never completes, so the consumer's
+                    // bounded wait runs out and the launch aborts
+                    if (leader && seq != withhold) {
                         slot_parity[stage] = parity | 2u;  // bit 1: slot used
                         const uint32_t sa = a0 + stage * sbytes;
                         if (PAIR) {
@@ -195,6 +201,7 @@ __device__ __forceinline__ void run_loader(const CdgParams &p, const Ring &R, co
                     __syncwarp();
                 }
                 if (++owner == nloaders) owner = 0;
+                ++seq;
                 if (++stage == stages) {
                     stage = 0;
                     parity ^= 1u;
@@ -207,11 +214,11 @@ __device__ __forceinline__ void run_loader(const CdgParams &p, const Ring &R, co
 // After an abort: wait (bounded) until the latest load of every used slot has
 // landed, so that no TMA still writes shared memory when the CTA exits.  On
 // the normal path the MMA warp has already waited for every load.
-__device__ __forceinline__ void drain_loads(const Ring &R, int stages, int *status,
+__device__ __forceinline__ void drain_loads(const Ring &R, int stages, int *status, uint64_t limit,
                                             const volatile uint32_t *slot_parity)
 {
     volatile uint32_t no_abort = 0;
-    const Ctl drain_ctl{&no_abort, status};
+    const Ctl drain_ctl{&no_abort, status, limit};
     for (int s = 0; s < stages; ++s) {
         const uint32_t v = slot_parity[s];
         if (v & 2u) wait_bar(R.full0 + 8u * s, v & 1u, drain_ctl);
@@ -419,7 +426,7 @@ __device__ __forceinline__ void run_mma_halo(const CdgParams &p, const Ring &R, 
     if (leader) umma_commit(R.drain);
     __syncwarp();
     volatile uint32_t no_abort = 0;
-    const Ctl drain_ctl{&no_abort, ctl.status};
+    const Ctl drain_ctl{&no_abort, ctl.status, ctl.limit};
     wait_bar(R.drain, 0, drain_ctl);
 }
 
@@ -503,7 +510,7 @@ __device__ __forceinline__ void run_mma(const CdgParams &p, const Ring &R, const
     }
     __syncwarp();
     volatile uint32_t no_abort = 0;
-    const Ctl drain_ctl{&no_abort, ctl.status};
+    const Ctl drain_ctl{&no_abort, ctl.status, ctl.limit};
     wait_bar(R.drain, 0, drain_ctl);
 }
 
@@ -666,6 +673,15 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
     const uint32_t grow = static_cast<uint32_t>(p.gate_row_bytes);
     uint32_t g_issued = 0, g_used = 0;  // gate loads issued and waited for (the same count in every thread)
     uint32_t gated_items = 0;
+    // Gate tiles are loaded by this CTA and always land, so their waits do not
+    // give up when another role aborts (only after the time limit): the four
+    // warps then never disagree about a gate wait.  The accumulator wait can
+    // legitimately fail (the MMA warp aborted); its outcome is agreed by all
+    // 128 epilogue threads in a reducing barrier before anyone leaves, because
+    // a thread that left while others went on to the next named barrier would
+    // leave them waiting there for good.
+    volatile uint32_t gate_no_abort = 0;
+    const Ctl gate_ctl{&gate_no_abort, ctl.status, ctl.limit};
     auto gate_ahead = [&]() {
         if (!gc.valid()) return;
         const uint32_t n = g_issued++;
@@ -721,7 +737,7 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
         if (MASK && mask_bits) {
             gate_ahead();  // into the slot the previous item's tile has left
             const uint32_t n = gated_items++;
-            if (!wait_bar(R.gfull0 + 8u * (n & 3u), (n >> 2) & 1u, ctl)) break;
+            if (!wait_bar(R.gfull0 + 8u * (n & 3u), (n >> 2) & 1u, gate_ctl)) break;
             ++g_used;
             mrow = R.gate0 + (n & 3u) * static_cast<uint32_t>(CDG_GATE_SLOT) + static_cast<uint32_t>(max(srow, 0)) * grow;
         }
@@ -730,7 +746,8 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
         const uint32_t n_acc = acc_count[issuer]++;
         const uint32_t acc = 2u * issuer + (n_acc & 1u);  // accumulator slot
         const uint32_t acc_parity = (n_acc >> 1) & 1u;
-        if (!wait_bar(R.acc_full0 + 8u * acc, acc_parity, ctl)) break;
+        const bool acc_ok = wait_bar(R.acc_full0 + 8u * acc, acc_parity, ctl);
+        if (named_bar_red_or(1, 128, !acc_ok)) break;
         tc_fence_after();
         const uint32_t taddr = tmem_base + acc * acc_stride + (static_cast<uint32_t>(quad * 32) << 16);
         for (int cc = 0; cc < BN; cc += CH) {
@@ -751,7 +768,7 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
                 }
             } else if (MASK && !mask_bits) {
                 gate_ahead();  // chunk k + 2 into the buffer store k - 2 has finished reading
-                if (!wait_bar(R.gfull0 + 8u * (k & 3u), (k >> 2) & 1u, ctl)) {
+                if (!wait_bar(R.gfull0 + 8u * (k & 3u), (k >> 2) & 1u, gate_ctl)) {
                     ok = false;
                     break;
                 }
@@ -828,7 +845,7 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
     if (MASK && ew == 0 && elected && g_used != g_issued) {
         // aborted: let the gate loads still in flight land before the CTA exits
         volatile uint32_t no_abort = 0;
-        const Ctl drain_ctl{&no_abort, ctl.status};
+        const Ctl drain_ctl{&no_abort, ctl.status, ctl.limit};
         for (uint32_t n = g_used; n < g_issued; ++n) wait_bar(R.gfull0 + 8u * (n & 3u), (n >> 2) & 1u, drain_ctl);
     }
     if (elected) bulk_wait_group_all();
@@ -941,7 +958,7 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_cons
     if (PAIR) cluster_sync();  // both CTAs' barriers exist before any copy or arrive crosses over
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const Ctl ctl{abort_flag, p.status};
+    const Ctl ctl{abort_flag, p.status, p.wait_limit_ns};
 
     // dual issue: MMA warp j (warp 1 + 2j) and loader warp j (warp 2j) serve the
     // items at odd/even positions of this CTA's walk, through ring j (half of
@@ -983,7 +1000,7 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_cons
             // the leader issues the pair's MMAs; wait until they are all done
             // with this CTA's tensor memory
             volatile uint32_t no_abort = 0;
-            wait_bar(R.drain, 0, Ctl{&no_abort, p.status});
+            wait_bar(R.drain, 0, Ctl{&no_abort, p.status, p.wait_limit_ns});
         }
     } else if (warp >= CDG_EPI_WARP0) {
         run_epilogue<OUT_T, MASK, IN_T, HALO, PAIR, false>(p, R, tab, ctl, tmem_base, S);
@@ -997,7 +1014,7 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_cons
     __syncthreads();
     if (*abort_flag && threadIdx.x == 0) {
         if (!PAIR || S.rank == 0) {
-            drain_loads(R, stages, p.status, slot_parity);
+            drain_loads(R, stages, p.status, p.wait_limit_ns, slot_parity);
         } else {
             // this CTA's copies complete on the leader's barriers; give any
             // still in flight time to land before the pair may exit

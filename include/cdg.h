@@ -169,6 +169,30 @@ int cdg_dgrad(cdg_handle_t h, const void *dY, const void *Wpacked, void *dX,
 int cdg_device_status(cdg_handle_t h, cdg_stream_t stream);
 
 /*
+ * How long any single pipeline wait of this plan's kernel may take before the
+ * launch gives up: it then records CDG_ERR_TIMEOUT (read by
+ * cdg_device_status), leaves every loop, waits (again bounded) for its own
+ * copies and tensor-core work in flight, releases its tensor memory and
+ * returns, leaving dX incomplete.  A correct launch never comes near the
+ * default of 4 s; a caller with a watchdog of its own may lower it.
+ * ns in [1e5, 6e10] (0.1 ms .. 60 s), else CDG_ERR_INVALID_ARG.  Host only;
+ * applies to launches made after the call.
+ */
+int cdg_plan_set_wait_limit(cdg_handle_t h, unsigned long long ns);
+
+/*
+ * TEST ONLY.  stage >= 0: every launch of this plan withholds one operand
+ * load -- in each CTA, the pipeline stage with that sequence number gets
+ * neither its tensor copies nor their byte count -- so the MMA warp's bounded
+ * wait for it runs out and the launch takes the timeout path above (status
+ * CDG_ERR_TIMEOUT, dX incomplete).  This exercises the failure path without
+ * any fault: every wait in the kernel is bounded.  stage = -1 restores normal
+ * launches.  Plans in the halo operand mode or with CTA pairs return
+ * CDG_ERR_UNSUPPORTED (their loaders do not take the option).  Host only.
+ */
+int cdg_plan_withhold_load_for_test(cdg_handle_t h, int stage);
+
+/*
  * Plan-time autotuning, in the manner of cuDNN's Find (the pages' comparison of
  * cuDNN's Get and Find algorithm selection): run the dgrad of this plan's shape
  * under each configuration the planner can produce for it (the planner's own
@@ -251,11 +275,27 @@ const char *cdg_status_string(int status);
  * its stream first.  Calls whose work overlaps on the GPU (different streams,
  * or different host threads) race on the scratch array and give wrong
  * results: serialise them.  A device-side pipeline timeout is recorded in the
- * scratch status word and not returned here.
+ * scratch status word, not returned here: read it with
+ * cdg_dgrad_noalloc_status.
+ *
+ * A plan from cdg_plan_host that chose CTA pairs has its persistent grid
+ * checked against the device (how many pairs fit at once) on its first
+ * cdg_dgrad_noalloc call, and reduced if needed.
  */
 #define CDG_NOALLOC_MAX_WEIGHT_BYTES (8u << 20)
 int cdg_dgrad_noalloc(cdg_handle_t h, const void *dY, const void *W_krsc, void *dX, const void *relu_mask,
                       cdg_stream_t stream);
+
+/*
+ * The status word cdg_dgrad_noalloc launches report into, on the current
+ * device: synchronise stream, read the word and clear it.  Returns CDG_OK, or
+ * CDG_ERR_TIMEOUT if a cdg_dgrad_noalloc launch since the last read gave up a
+ * bounded wait (its dX is then incomplete), or CDG_ERR_CUDA.  Allocates
+ * nothing (the word is in the library's scratch array).  Because every
+ * cdg_dgrad_noalloc call on a device shares the word, read it after each call
+ * (or each batch of serialised calls) whose result matters.
+ */
+int cdg_dgrad_noalloc_status(cdg_stream_t stream);
 
 /*
  * Weight gradient (wgrad) of the same cross-correlation Conv2d, the

@@ -308,3 +308,28 @@ def test_wgrad_host_plan_refuses_device_work():
     with pytest.raises(cdg.CdgError) as e:
         p.wgrad(4096, 8192, 1 << 20, 1 << 24)
     assert e.value.status == 7
+
+
+def test_wait_limit_and_withheld_load_arguments():
+    """The wait limit takes 0.1 ms .. 60 s; the test-only withheld load takes
+    stage >= -1 and only plans whose loaders honour it (per-tap or row boxes,
+    no CTA pairs, no halo boxes)."""
+    p = cdg.plan_host(2, 12, 12, 64, 64, 3, 3, 1, 1, 1, "bf16", num_sms=148)
+    assert p.info()["a_mode"] == 3  # halo boxes with resident weights
+    for bad in (0, 99_999, 60_000_000_001):
+        with pytest.raises(cdg.CdgError):
+            p.set_wait_limit(bad)
+    p.set_wait_limit(100_000)
+    p.set_wait_limit(60_000_000_000)
+    with pytest.raises(cdg.CdgError) as e:
+        p.withhold_load_for_test(0)
+    assert e.value.status == 2
+    p.withhold_load_for_test(-1)  # restoring is always allowed
+    with pytest.raises(cdg.CdgError):
+        p.withhold_load_for_test(-2)
+    pair = cdg.plan_host(2, 14, 14, 256, 256, 3, 3, 1, 1, 1, "bf16", num_sms=148)
+    assert pair.info()["cta_pair"] == 1
+    with pytest.raises(cdg.CdgError):
+        pair.withhold_load_for_test(3)
+    rows = cdg.plan_host(4, 14, 14, 256, 64, 1, 1, 1, 0, 1, "bf16", num_sms=148)
+    rows.withhold_load_for_test(1)

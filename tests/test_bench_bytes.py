@@ -59,3 +59,24 @@ def test_wgrad_bytes():
     from implicit_gemm_dgrad_gb300.workloads import by_name
     L01 = by_name("L01_1x1_64-64_56")  # 2 x 102.8 MB of activations, a 8 KB filter
     assert abs(b.wgrad_bytes(L01) / 1e6 - 205.5) < 0.1
+
+
+def test_peak_basis_follows_the_sampled_clock():
+    """The tensor roofline uses the burst bf16 peak when the SM clock held its
+    maximum during the timed region, else the sustained one; both fractions
+    are printed."""
+    b = _bench()
+    assert b.peak_basis({"sm_mhz": 2070.0, "sm_max_mhz": 2070.0}) == "burst"
+    assert b.peak_basis({"sm_mhz": 1440.0, "sm_max_mhz": 2070.0}) == "sustained"
+    assert b.peak_basis({"sm_mhz": None, "sm_max_mhz": None}) == "sustained"
+    peaks = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+    L = [x for x in RESNET50_B256 if x.name.startswith("L21")][0]  # tensor-bound
+    ms = L.flops / 950e12 * 1e3  # runs at 950 TFLOP/s
+    burst = b.layer_record(L, ms, peaks, "burst")
+    sus = b.layer_record(L, ms, peaks, "sustained")
+    assert burst["bound"] == "tensor" and abs(burst["roofline_frac"] - 0.5) < 1e-3
+    assert abs(sus["roofline_frac"] - 950 / 1700) < 1e-3 and abs(burst["roofline_frac_sustained"] - sus["roofline_frac"]) < 1e-9
+    H = [x for x in RESNET50_B256 if x.name.startswith("L01")][0]  # HBM-bound: the basis does not matter
+    ms = H.bytes / 3400e9 * 1e3
+    assert abs(b.layer_record(H, ms, peaks, "burst")["roofline_frac"] - 0.5) < 1e-3
+    assert b.layer_record(H, ms, peaks, "sustained")["roofline_frac"] == b.layer_record(H, ms, peaks, "burst")["roofline_frac"]

@@ -104,3 +104,25 @@ def test_pack_relu_mask_short_buffers():
         cdg.pack_relu_mask(FakeCuda(2 * 100 * 64), FakeCuda(n - 1, 1), 100, 64)
     with pytest.raises(ValueError, match="x"):
         cdg.pack_relu_mask(FakeCuda(2 * 100 * 64 - 2), FakeCuda(n, 1), 100, 64)
+
+
+def test_tensor_on_another_device_is_rejected(monkeypatch):
+    """A tensor on a GPU other than the current one raises ValueError before
+    any call (the kernels launch on the current device)."""
+    import types
+
+    import torch
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: 0)
+    L = RESNET50_B256[0]
+    p = cdg.plan_host(L.N, L.H, L.W, L.C, L.K, L.R, L.S, L.stride, L.pad, L.dil, L.dtype, num_sms=148)
+    dy, w, dx, _ = _dgrad_sizes(L, "none", False)
+    args = [FakeCuda(dy), FakeCuda(w), FakeCuda(dx)]
+    for t in args:
+        t.device = types.SimpleNamespace(index=0)
+    args[2].device = types.SimpleNamespace(index=1)
+    with pytest.raises(ValueError, match="cuda:1"):
+        p.dgrad(*args)
+    args[2].device = types.SimpleNamespace(index=0)
+    with pytest.raises(cdg.CdgError) as e:  # same device: the host-only plan refuses device work
+        p.dgrad(*args)
+    assert e.value.status == 7

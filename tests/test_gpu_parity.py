@@ -3,7 +3,9 @@
 Bar (per element): |gpu - oracle| <= 2e-3*max(1,|oracle|) for fp32 dX and
 1e-2*max(1,|oracle|) for fp16/bf16 dX; integer inputs must give the oracle's
 value rounded once to the output type, bit for bit; the ReLU-backward gate
-must leave +0.0 at exactly the gated-off positions.  dX is pre-filled with NaN
+must leave +0.0 at every gated-off position and no zero at any other position
+unless the oracle's value there rounds to zero in the output type (the zero
+pattern is checked in both directions).  dX is pre-filled with NaN
 (or garbage) and surrounded by sentinel guard bands for every call.
 """
 import numpy as np
@@ -32,7 +34,7 @@ def check_layer(L, prefill="nan", dist=None):
     ref = oracle_full(run)
     assert_close(got, ref, run.odt, L.name)
     if L.relu:
-        check_gate_zero_pattern(run.result_bytes(), run.x, run.odt, L.dtype)
+        check_gate_zero_pattern(run.result_bytes(), run.x, ref, run.odt, L.dtype)
     return run, got, ref
 
 
@@ -127,9 +129,11 @@ def test_gate_special_values():
     run = GpuRun(L, inputs=(dY, W, x))
     run.run()
     raw = run.result_bytes()
-    check_gate_zero_pattern(raw, x, run.odt, "f16")
     got = decode_out(raw, run.odt).reshape(1, 4, 4, 16)
     ref = oracle.dgrad(dY, W, 4, 4, 1, 0, 1, x=x, dtype="f16")
+    counts = check_gate_zero_pattern(raw, x, ref, run.odt, "f16")
+    # +0, -0, two NaNs and -1 are masked; 1.0, the subnormal and +Inf pass
+    assert counts["masked"] == 5 * 4 * 4 * 16 // 8 and counts["unmasked_oracle_zero"] == 0
     assert_close(got, ref, run.odt, "specials")
 
 
@@ -290,7 +294,7 @@ def _bits_gated(L, x_override=None):
     raw = out.body().cpu().numpy()
     assert out.guards_intact() and p.device_status() == 0
     ref = oracle.dgrad(dY, W, L.H, L.W, L.stride, L.pad, L.dil, x=x, dtype=L.dtype)
-    check_gate_zero_pattern(raw, x, odt, L.dtype)
+    check_gate_zero_pattern(raw, x, ref, odt, L.dtype)
     assert_close(decode_out(raw, odt).reshape(L.N, L.H, L.W, L.C), ref, odt, L.name)
     return raw, x, odt, p
 
