@@ -29,13 +29,13 @@ ERR_INVALID_ARG = 1
 ERR_SCRATCH_TOO_SMALL = 8
 NOALLOC_MAX_WEIGHT_BYTES = 8 << 20
 F16, BF16 = 0, 1
-EPI_RELU_BWD, EPI_OUT_F32, EPI_RELU_BWD_BITS = 1, 2, 4
+EPI_RELU_BWD, EPI_OUT_F32, EPI_RELU_BWD_BITS, EPI_SUM, EPI_SUM_X = 1, 2, 4, 8, 16
 DTYPES = {"f16": F16, "bf16": BF16}
 
 EXPORTS = ("cdg_plan", "cdg_plan_host", "cdg_destroy", "cdg_get_output_dims", "cdg_packed_weight_bytes",
            "cdg_plan_get_info", "cdg_prepack_weights", "cdg_dgrad", "cdg_device_status", "cdg_status_string",
            "cdg_dgrad_noalloc", "cdg_dgrad_noalloc_status", "cdg_autotune", "cdg_plan_set_wait_limit",
-           "cdg_plan_withhold_load_for_test", "cdg_pack_relu_mask", "cdg_relu_mask_bytes",
+           "cdg_plan_withhold_load_for_test", "cdg_dgrad_sums", "cdg_sums_workspace_bytes", "cdg_pack_relu_mask", "cdg_relu_mask_bytes",
            "cdg_wgrad_plan", "cdg_wgrad_plan_host", "cdg_wgrad_destroy", "cdg_wgrad_workspace_bytes",
            "cdg_wgrad_get_info", "cdg_wgrad", "cdg_wgrad_device_status")
 
@@ -101,6 +101,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.cdg_dgrad_noalloc.argtypes = [hp, vp, vp, vp, vp, vp]
     lib.cdg_dgrad_noalloc.restype = i
     lib.cdg_dgrad_noalloc_status.argtypes = [vp]
+    lib.cdg_dgrad_sums.argtypes = [hp, vp, vp, vp, vp, vp, vp, vp]
+    lib.cdg_dgrad_sums.restype = i
+    lib.cdg_sums_workspace_bytes.argtypes = [hp]
+    lib.cdg_sums_workspace_bytes.restype = ctypes.c_size_t
     lib.cdg_plan_set_wait_limit.argtypes = [hp, ctypes.c_ulonglong]
     lib.cdg_plan_set_wait_limit.restype = i
     lib.cdg_plan_withhold_load_for_test.argtypes = [hp, i]
@@ -187,14 +191,16 @@ class Plan:
     """One planned dgrad shape (a ``cdg_handle_t``)."""
 
     def __init__(self, N, H, W, C, K, R, S, stride=1, pad=0, dil=1, dtype="bf16", relu=False,
-                 out_f32=False, host_sms: int | None = None, relu_bits=False):
+                 out_f32=False, host_sms: int | None = None, relu_bits=False, sums: int = 0):
         self.lib = load_library()
         self.shape = dict(N=N, H=H, W=W, C=C, K=K, R=R, S=S, stride=stride, pad=pad, dil=dil)
         self.dtype = dtype
         self.relu = relu
         self.relu_bits = relu_bits
         self.out_f32 = out_f32
+        self.sums = int(sums)
         epi = (EPI_RELU_BWD if relu else 0) | (EPI_OUT_F32 if out_f32 else 0) | (EPI_RELU_BWD_BITS if relu_bits else 0)
+        epi |= {0: 0, 1: EPI_SUM, 2: EPI_SUM | EPI_SUM_X}[self.sums]
         h = ctypes.c_void_p()
         dt = DTYPES[dtype] if isinstance(dtype, str) else int(dtype)
         if host_sms is None:
@@ -271,6 +277,22 @@ class Plan:
                                 _stream(stream))
         if rc != OK:
             raise CdgError(rc, "cdg_dgrad")
+
+    @property
+    def sums_workspace_bytes(self) -> int:
+        return int(self.lib.cdg_sums_workspace_bytes(self.handle))
+
+    def dgrad_sums(self, dY, W_packed, dX, sums, workspace, relu_mask=None, stream=None) -> None:
+        """dgrad plus the per-channel sums of its output (cdg_dgrad_sums):
+        sums (fp32, C values, or 2*C for sums=2) receives sum(out) per channel
+        and, for sums=2, sum(out * x) where the gate passes."""
+        self._check(dY=dY, W_packed=W_packed, dX=dX, relu_mask=relu_mask)
+        _check_buffer(sums, 4 * self.sums * self.shape["C"], "sums")
+        _check_buffer(workspace, self.sums_workspace_bytes, "workspace")
+        rc = self.lib.cdg_dgrad_sums(self.handle, _addr(dY), _addr(W_packed), _addr(dX), _addr(relu_mask),
+                                     _addr(sums), _addr(workspace), _stream(stream))
+        if rc != OK:
+            raise CdgError(rc, "cdg_dgrad_sums")
 
     def dgrad_noalloc(self, dY, W_krsc, dX, relu_mask=None, stream=None) -> None:
         """dgrad from the unpacked KRSC filter without any device allocation
@@ -395,8 +417,8 @@ def wgrad_plan_host(N, H, W, C, K, R, S, stride=1, pad=0, dil=1, dtype="bf16", o
 
 
 def plan(N, H, W, C, K, R, S, stride=1, pad=0, dil=1, dtype="bf16", relu=False, out_f32=False,
-         relu_bits=False) -> Plan:
-    return Plan(N, H, W, C, K, R, S, stride, pad, dil, dtype, relu, out_f32, relu_bits=relu_bits)
+         relu_bits=False, sums: int = 0) -> Plan:
+    return Plan(N, H, W, C, K, R, S, stride, pad, dil, dtype, relu, out_f32, relu_bits=relu_bits, sums=sums)
 
 
 def relu_mask_bytes(pixels: int, C: int) -> int:
@@ -422,5 +444,6 @@ def pack_relu_mask(x, bits, pixels: int, C: int, dtype="bf16", stream=None) -> N
 
 
 def plan_host(N, H, W, C, K, R, S, stride=1, pad=0, dil=1, dtype="bf16", relu=False, out_f32=False,
-              num_sms=148, relu_bits=False) -> Plan:
-    return Plan(N, H, W, C, K, R, S, stride, pad, dil, dtype, relu, out_f32, host_sms=num_sms, relu_bits=relu_bits)
+              num_sms=148, relu_bits=False, sums: int = 0) -> Plan:
+    return Plan(N, H, W, C, K, R, S, stride, pad, dil, dtype, relu, out_f32, host_sms=num_sms, relu_bits=relu_bits,
+                sums=sums)

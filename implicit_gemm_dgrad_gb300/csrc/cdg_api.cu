@@ -73,6 +73,7 @@ struct PlanOpts {
     int dual = -1;        // 0 one MMA warp
     int interleave = -1;  // 0 phases one after another
     int max_bn = 256;     // 128 caps the N tile
+    int bn = 0;           // > 0: this N tile (a multiple of 64, or of 128 with the packed mask), if it fits C
     int pdl = 1;          // 0 plain launches
 };
 
@@ -180,6 +181,8 @@ PlanOpts opts_from_env()
     o.interleave = flag("CDG_INTERLEAVE") == 0 ? 0 : -1;
     const char *bn = std::getenv("CDG_MAX_BN");
     o.max_bn = (bn && std::atoi(bn) == 128) ? 128 : 256;
+    const char *fbn = std::getenv("CDG_BN");
+    o.bn = fbn ? std::atoi(fbn) : 0;
     o.pdl = flag("CDG_PDL") == 0 ? 0 : 1;
     return o;
 }
@@ -192,8 +195,10 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     if (N < 1 || H < 1 || W < 1 || C < 1 || K < 1 || R < 1 || S < 1 || stride < 1 || pad < 0 || dil < 1)
         return CDG_ERR_INVALID_ARG;
     if (dtype != CDG_F16 && dtype != CDG_BF16) return CDG_ERR_INVALID_ARG;
-    if (epilogue & ~(CDG_EPI_RELU_BWD | CDG_EPI_OUT_F32 | CDG_EPI_RELU_BWD_BITS)) return CDG_ERR_INVALID_ARG;
+    if (epilogue & ~(CDG_EPI_RELU_BWD | CDG_EPI_OUT_F32 | CDG_EPI_RELU_BWD_BITS | CDG_EPI_SUM | CDG_EPI_SUM_X))
+        return CDG_ERR_INVALID_ARG;
     if ((epilogue & CDG_EPI_RELU_BWD) && (epilogue & CDG_EPI_RELU_BWD_BITS)) return CDG_ERR_INVALID_ARG;
+    if ((epilogue & CDG_EPI_SUM_X) && !(epilogue & CDG_EPI_RELU_BWD)) return CDG_ERR_INVALID_ARG;
     const long long spanH = 1LL * H + 2LL * pad - 1LL * dil * (R - 1) - 1;
     const long long spanW = 1LL * W + 2LL * pad - 1LL * dil * (S - 1) - 1;
     if (spanH < 0 || spanW < 0) return CDG_ERR_INVALID_ARG;
@@ -219,6 +224,7 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     h->out_type = (epilogue & CDG_EPI_OUT_F32) ? CDG_T_F32 : h->in_type;
     h->mask = (epilogue & (CDG_EPI_RELU_BWD | CDG_EPI_RELU_BWD_BITS)) != 0;
     h->mask_bits = (epilogue & CDG_EPI_RELU_BWD_BITS) != 0;
+    const int nsum = (epilogue & CDG_EPI_SUM_X) ? 2 : ((epilogue & CDG_EPI_SUM) ? 1 : 0);
 
     // ---- phases and their taps
     std::vector<CdgPhase> phases;
@@ -288,12 +294,16 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     // N tile: all of C up to 256 channels, else the multiple of 64 up to 256
     // with the least padding (max_bn 128 caps it at 128).  With the packed mask
     // a tile's mask bytes must start on a 16-byte unit: multiples of 128.
-    const int BN = choose_bn(C, opt.max_bn == 128 ? 128 : 256, h->mask_bits ? 128 : 64);
+    const int bn_step = h->mask_bits ? 128 : 64;
+    int BN = choose_bn(C, opt.max_bn == 128 ? 128 : 256, bn_step);
+    if (opt.bn > 0 && opt.bn % bn_step == 0 && opt.bn <= 256 && opt.bn < ((C + 15) / 16) * 16) BN = opt.bn;
     const int tiles_n = ceil_div(C, BN);
     // output staging; gated by the activation: four buffers, its chunks land in
     // them ahead of use; by the packed mask: a ring of mask tiles besides
     const int staging = CDG_SMEM_STAGING + (h->mask ? (h->mask_bits ? CDG_GATE_RING : CDG_SMEM_STAGING) : 0);
-    const int ring_budget = kMaxSmem - 1024 - staging - CDG_SMEM_TAIL;
+    // per-channel sums: the epilogue warps' partials of a chunk, after the tail
+    const int red_bytes = nsum ? CDG_SMEM_RED : 0;
+    const int ring_budget = kMaxSmem - 1024 - staging - CDG_SMEM_TAIL - red_bytes;
 
     // ---- halo operand mode: a tile is halo_bh full-width rows of one image's
     // phase sub-grid; one TMA box of (width + tap span) x (rows + tap span)
@@ -502,7 +512,9 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     for (size_t i = 0; i < phases.size(); ++i) p.phase[i] = phases[i];
     for (size_t i = 0; i < taps.size(); ++i) p.tap[i] = taps[i];
 
-    h->smem = static_cast<size_t>(1024 + ring_bytes + staging + CDG_SMEM_TAIL);
+    h->smem = static_cast<size_t>(1024 + ring_bytes + staging + CDG_SMEM_TAIL + red_bytes);
+    p.nsum = nsum;
+    p.red_ws = nullptr;
     h->grid = pair ? 2 * std::max(1, std::min(num_sms / 2, items)) : std::max(1, std::min(num_sms, items));
 
     h->il_phases = p.interleave;
@@ -713,6 +725,44 @@ int encode_gate_maps(cdg_plan_st *h, const void *gate)
     return CDG_OK;
 }
 
+// Validate the tensors of one dgrad, refresh the cached tensor maps and
+// launch the kernel (red_ws: the per-channel sums workspace, or NULL).
+int launch_plan(cdg_handle_t h, const void *dY, const void *Wpacked, void *dX, const void *relu_mask, float *red_ws,
+                cdg_stream_t stream)
+{
+    if (!h || !dY || !Wpacked || !dX) return CDG_ERR_INVALID_ARG;
+    if (h->mask != (relu_mask != nullptr)) return CDG_ERR_INVALID_ARG;
+    if (h->host_only) return CDG_ERR_NO_DEVICE;
+    if (!aligned16(dY) || !aligned16(Wpacked) || !aligned16(dX) || (relu_mask && !aligned16(relu_mask)))
+        return CDG_ERR_ALIGNMENT;
+    const size_t dx_bytes = static_cast<size_t>(h->N) * h->H * h->W * h->C * (h->out_type == CDG_T_F32 ? 4 : 2);
+    const size_t dy_bytes = static_cast<size_t>(h->N) * h->P * h->Q * h->K * 2;
+    if (overlaps(dX, dx_bytes, dY, dy_bytes) || overlaps(dX, dx_bytes, Wpacked, cdg_packed_weight_bytes(h)) ||
+        (relu_mask && overlaps(dX, dx_bytes, relu_mask, mask_bytes(h))))
+        return CDG_ERR_ALIAS;
+    if (dY != h->cached_dY || Wpacked != h->cached_Wp) {
+        const int rc = encode_operand_maps(h, dY, Wpacked);
+        if (rc != CDG_OK) return rc;
+    }
+    if (dX != h->cached_dX) {
+        const int rc = encode_store_maps(h, dX);
+        if (rc != CDG_OK) return rc;
+    }
+    if (relu_mask && relu_mask != h->cached_mask) {
+        const int rc = encode_gate_maps(h, relu_mask);
+        if (rc != CDG_OK) return rc;
+    }
+    CdgParams &p = h->prm;
+    p.dX = dX;
+    p.mask = relu_mask;
+    p.status = h->d_status;
+    p.red_ws = red_ws;
+    if (cdg_launch_dgrad(p, h->out_type, h->in_type, h->mask, h->grid, h->smem, static_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
+        return CDG_ERR_CUDA;
+    return CDG_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -788,34 +838,41 @@ int cdg_prepack_weights(cdg_handle_t h, const void *W_krsc, void *Wpacked, cdg_s
 int cdg_dgrad(cdg_handle_t h, const void *dY, const void *Wpacked, void *dX, const void *relu_mask,
               cdg_stream_t stream)
 {
-    if (!h || !dY || !Wpacked || !dX) return CDG_ERR_INVALID_ARG;
-    if (h->mask != (relu_mask != nullptr)) return CDG_ERR_INVALID_ARG;
-    if (h->host_only) return CDG_ERR_NO_DEVICE;
-    if (!aligned16(dY) || !aligned16(Wpacked) || !aligned16(dX) || (relu_mask && !aligned16(relu_mask)))
-        return CDG_ERR_ALIGNMENT;
+    if (h && h->prm.nsum) return CDG_ERR_INVALID_ARG;  // such plans run through cdg_dgrad_sums
+    return launch_plan(h, dY, Wpacked, dX, relu_mask, nullptr, stream);
+}
+
+size_t cdg_sums_workspace_bytes(cdg_handle_t h)
+{
+    if (!h) return 0;
+    // one row per CTA; no plan of this handle (autotuned ones included) has
+    // more CTAs than the device has SMs
+    return static_cast<size_t>(h->num_sms) * h->prm.nsum * h->C * sizeof(float);
+}
+
+int cdg_dgrad_sums(cdg_handle_t h, const void *dY, const void *Wpacked, void *dX, const void *relu_mask, float *sums,
+                   void *workspace, cdg_stream_t stream)
+{
+    if (!h || !sums || !workspace || !h->prm.nsum) return CDG_ERR_INVALID_ARG;
+    if (!aligned16(sums) || !aligned16(workspace)) return CDG_ERR_ALIGNMENT;
+    const size_t sb = static_cast<size_t>(h->prm.nsum) * h->C * sizeof(float);
+    const size_t wb = cdg_sums_workspace_bytes(h);
     const size_t dx_bytes = static_cast<size_t>(h->N) * h->H * h->W * h->C * (h->out_type == CDG_T_F32 ? 4 : 2);
     const size_t dy_bytes = static_cast<size_t>(h->N) * h->P * h->Q * h->K * 2;
-    if (overlaps(dX, dx_bytes, dY, dy_bytes) || overlaps(dX, dx_bytes, Wpacked, cdg_packed_weight_bytes(h)) ||
-        (relu_mask && overlaps(dX, dx_bytes, relu_mask, mask_bytes(h))))
-        return CDG_ERR_ALIAS;
-    if (dY != h->cached_dY || Wpacked != h->cached_Wp) {
-        const int rc = encode_operand_maps(h, dY, Wpacked);
-        if (rc != CDG_OK) return rc;
+    const void *outs[3] = {dX, sums, workspace};
+    const size_t outb[3] = {dx_bytes, sb, wb};
+    const void *ins[3] = {dY, Wpacked, relu_mask};
+    const size_t inb[3] = {dy_bytes, cdg_packed_weight_bytes(h), relu_mask ? mask_bytes(h) : 0};
+    for (int i = 0; i < 3; ++i) {
+        for (int j = 0; j < 3; ++j)
+            if (ins[j] && outs[i] && overlaps(outs[i], outb[i], ins[j], inb[j])) return CDG_ERR_ALIAS;
+        for (int j = i + 1; j < 3; ++j)
+            if (overlaps(outs[i], outb[i], outs[j], outb[j])) return CDG_ERR_ALIAS;
     }
-    if (dX != h->cached_dX) {
-        const int rc = encode_store_maps(h, dX);
-        if (rc != CDG_OK) return rc;
-    }
-    if (relu_mask && relu_mask != h->cached_mask) {
-        const int rc = encode_gate_maps(h, relu_mask);
-        if (rc != CDG_OK) return rc;
-    }
-    CdgParams &p = h->prm;
-    p.dX = dX;
-    p.mask = relu_mask;
-    p.status = h->d_status;
-    if (cdg_launch_dgrad(p, h->out_type, h->in_type, h->mask, h->grid, h->smem, static_cast<cudaStream_t>(stream)) !=
-        cudaSuccess)
+    int rc = launch_plan(h, dY, Wpacked, dX, relu_mask, static_cast<float *>(workspace), stream);
+    if (rc != CDG_OK) return rc;
+    if (cdg_launch_channel_sums(static_cast<const float *>(workspace), h->grid, h->prm.nsum, h->C, sums,
+                                static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return CDG_ERR_CUDA;
     return CDG_OK;
 }
@@ -828,6 +885,7 @@ int cdg_autotune(cdg_handle_t h, const void *dY, const void *Wpacked, void *dX, 
     if (!h || !dY || !Wpacked || !dX || reps < 1 || reps > 1000) return CDG_ERR_INVALID_ARG;
     if (h->mask != (relu_mask != nullptr)) return CDG_ERR_INVALID_ARG;
     if (h->host_only) return CDG_ERR_NO_DEVICE;
+    if (h->prm.nsum) return CDG_ERR_UNSUPPORTED;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
     std::vector<PlanOpts> cands;
@@ -1065,7 +1123,7 @@ int noalloc_setup(int dev, cdg_plan_st *h, unsigned char **scratch)
 extern "C" int cdg_dgrad_noalloc(cdg_handle_t h, const void *dY, const void *W_krsc, void *dX,
                                  const void *relu_mask, cdg_stream_t stream)
 {
-    if (!h || !dY || !W_krsc || !dX) return CDG_ERR_INVALID_ARG;
+    if (!h || !dY || !W_krsc || !dX || h->prm.nsum) return CDG_ERR_INVALID_ARG;
     if (h->mask != (relu_mask != nullptr)) return CDG_ERR_INVALID_ARG;
     const size_t wbytes = cdg_packed_weight_bytes(h);
     if (wbytes > CDG_NOALLOC_MAX_WEIGHT_BYTES) return CDG_ERR_SCRATCH_TOO_SMALL;
@@ -1104,6 +1162,7 @@ extern "C" int cdg_dgrad_noalloc(cdg_handle_t h, const void *dY, const void *W_k
     p.dX = dX;
     p.mask = relu_mask;
     p.status = status;
+    p.red_ws = nullptr;
     if (cdg_launch_dgrad(p, h->out_type, h->in_type, h->mask, h->grid, h->smem, s) != cudaSuccess)
         return CDG_ERR_CUDA;
     return CDG_OK;

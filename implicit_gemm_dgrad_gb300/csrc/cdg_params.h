@@ -30,6 +30,9 @@
 #define CDG_GATE_RING (4 * CDG_GATE_SLOT)
 #define CDG_SMEM_TAIL 2048
 #define CDG_SMEM_TABLES 320
+// Per-channel output sums (plans with CDG_EPI_SUM): after the tail, the four
+// epilogue warps' partial sums of one chunk, [sums][4 warps][64 channels] fp32.
+#define CDG_SMEM_RED (2 * 4 * 64 * 4)
 #define CDG_MAX_STAGES_TOTAL 10  // all ring stages together (their mbarriers live in the 320-byte area)
 
 // One phase sub-convolution of a (possibly strided) dgrad.  The dX pixels with
@@ -97,6 +100,9 @@ struct CdgParams {  // CUtensorMap members carry their own (128-byte) alignment
     uint32_t tx_bytes;    // bytes one pipeline stage receives (A box + B box)
     uint32_t tmem_cols;   // allocated TMEM columns (two accumulators)
     uint32_t acc_stride;  // column offset of the second accumulator
+    float *red_ws;        // per-channel sums: this launch's [grid][nsum][C] fp32 partials (one row per CTA)
+    int nsum;             // per-channel output sums the epilogue accumulates: 0, 1 (sum of dX) or
+                          // 2 (also the sum of dX * x where the gate passes)
     unsigned long long wait_limit_ns;  // a pipeline wait gives up (status CDG_ERR_TIMEOUT) after this long
     int withhold_stage;   // test only: >= 0 makes every per-tap/row loader skip the load (and its
                           // transaction count) of its stage with this sequence number, so the MMA
@@ -115,4 +121,5 @@ cudaError_t cdg_launch_dgrad(const CdgParams &p, int out_type, int in_type, bool
                              int grid, size_t smem, cudaStream_t stream);
 cudaError_t cdg_prepare_dgrad(int out_type, int in_type, bool mask, size_t smem);
 cudaError_t cdg_launch_prepack(const void *W, void *Wp, int K, int T, int C, cudaStream_t stream);
+cudaError_t cdg_launch_channel_sums(const float *ws, int rows, int nsum, int C, float *out, cudaStream_t stream);
 int cdg_max_active_pairs(int out_type, int in_type, bool mask, size_t smem);

@@ -119,6 +119,7 @@ struct Ring {
     uint32_t acc_full0, acc_empty0, drain;
     uint32_t gfull0;       // gate loads: four mbarriers
     uint32_t gate0;        // packed-mask ring (four CDG_GATE_SLOT slots)
+    uint32_t red0;         // per-channel sums: the warps' partials of one chunk, [sum][warp][64] fp32
 };
 
 // ------------------------------------------------------------------ loaders
@@ -595,14 +596,58 @@ __device__ __forceinline__ void gate_issue(const CdgParams &p, const GateCursor 
 
 // ReLU-backward gate on PER consecutive values: v = (x > 0) ? v : +0.0 (a
 // select, so masked outputs are +0.0 whatever the accumulator holds).
+// xp receives the gated value times x where the gate passes, +0.0 elsewhere
+// (the terms of the per-channel sum of dX * x).
 template <int IN_T, int PER>
-__device__ __forceinline__ void gate_x(float *v, const uint32_t *w)
+__device__ __forceinline__ void gate_x(float *v, const uint32_t *w, float *xp)
 {
 #pragma unroll
-    for (int e = 0; e < PER / 2; ++e) {
-        if (!(gate_value<IN_T>(static_cast<uint16_t>(w[e] & 0xFFFFu)) > 0.0f)) v[2 * e] = 0.0f;
-        if (!(gate_value<IN_T>(static_cast<uint16_t>(w[e] >> 16)) > 0.0f)) v[2 * e + 1] = 0.0f;
+    for (int e = 0; e < PER; ++e) {
+        const float x = gate_value<IN_T>(static_cast<uint16_t>(w[e >> 1] >> (16 * (e & 1))));
+        const bool pass = x > 0.0f;
+        v[e] = pass ? v[e] : 0.0f;
+        xp[e] = pass ? v[e] * x : 0.0f;
     }
+}
+
+// Sum PER values per lane over the 32 lanes of a warp: halving exchanges
+// while more than one value is left (lane bit 4, then 3, ... chooses which
+// half a lane keeps), then a butterfly over the remaining lane bits.  Lane l
+// returns the warp's total of value l / (32 / PER); the 32 / PER lanes that
+// share it hold the same sum.  Every lane takes part.
+template <int PER>
+__device__ __forceinline__ float warp_sum_spread(float (&a)[PER], int lane)
+{
+    constexpr int LOG = PER == 8 ? 3 : (PER == 4 ? 2 : (PER == 2 ? 1 : 0));
+    static_assert((1 << LOG) == PER, "PER must be 1, 2, 4 or 8");
+#pragma unroll
+    for (int step = 0; step < LOG; ++step) {
+        const int d = 16 >> step;
+        const bool upper = (lane & d) != 0;
+        constexpr int n0 = PER / 2;
+#pragma unroll
+        for (int i = 0; i < (n0 >> step); ++i) {
+            const int j = i + (n0 >> step);
+            const float send = upper ? a[i] : a[j];
+            const float keep = upper ? a[j] : a[i];
+            a[i] = keep + __shfl_xor_sync(0xffffffffu, send, d);
+        }
+    }
+    float t = a[0];
+#pragma unroll
+    for (int d = 16 >> LOG; d >= 1; d >>= 1) t += __shfl_xor_sync(0xffffffffu, t, d);
+    return t;
+}
+
+__device__ __forceinline__ void st_shared_f32(uint32_t addr, float v)
+{
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr)
+{
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
 }
 
 template <int PER>
@@ -651,6 +696,18 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
     const uint32_t sw = static_cast<uint32_t>(srow & 7);
     const uint32_t zero_buf = R.out0;  // staging buffer 0 doubles as the zero source
     bool zero_ready = false;
+
+    // Per-channel sums (p.nsum > 0): this CTA adds each chunk's column sums
+    // into its own row of the workspace, [CTA][sum][C] fp32.  Channel c is
+    // always handled by epilogue thread c % CH (N tiles are multiples of CH
+    // channels, or a single tile from channel 0), which zeroes it first, so
+    // the row needs no atomics and its sums keep one order from run to run.
+    const int nsum = p.nsum;
+    const int ethread = ew * 32 + lane;
+    float *const red_row = nsum ? p.red_ws + static_cast<size_t>(blockIdx.x) * nsum * C : nullptr;
+    if (nsum && ethread < CH)
+        for (int c = ethread; c < C; c += CH)
+            for (int k = 0; k < nsum; ++k) red_row[k * C + c] = 0.0f;
 
     // TMA stores are spread over the four warps' elected lanes (an issue holds its
     // thread for a few hundred cycles): chunk k is stored by epilogue warp k % 4.
@@ -733,6 +790,18 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
         // tile origin in the store map's coordinates
         int j0 = 0, i0 = 0, n0 = 0;
         if (d_mode == CDG_D_BOX4) box_origin(ph, mt, bw, bh, bn, j0, i0, n0);
+        // does this thread's tile row hold a dX pixel of the item?  (rows past
+        // the sub-grid's edges, halo padding rows and the tail of the last
+        // tile are computed but never stored; the sums must skip them too)
+        bool row_ok = false;
+        if (nsum) {
+            if (d_mode == CDG_D_BOX4)
+                row_ok = srow >= 0 && nl < bn && j0 + jl < ph.wph && i0 + il < ph.hph && n0 + nl < p.N;
+            else if (d_mode == CDG_D_LINEAR)
+                row_ok = mt * m_step + row < p.N * p.H * p.W;
+            else
+                row_ok = row < m_step && mt * rpt + row / ph.wph < p.N * ph.hph;
+        }
         uint32_t mrow = 0;  // packed mask: this row's bytes in the item's mask tile
         if (MASK && mask_bits) {
             gate_ahead();  // into the slot the previous item's tile has left
@@ -802,18 +871,38 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
 #pragma unroll
             for (int q = 0; q < 8; ++q) {  // 16-byte pieces of this row
                 constexpr int PER = 16 / OSZ;  // values per piece
-                float v[PER];
+                float v[PER], xp[PER];
 #pragma unroll
-                for (int e = 0; e < PER; ++e) v[e] = __uint_as_float(r[PER * q + e]);
+                for (int e = 0; e < PER; ++e) {
+                    v[e] = __uint_as_float(r[PER * q + e]);
+                    xp[e] = 0.0f;
+                }
                 if (MASK && srow >= 0) {
                     if (mask_bits) {
                         gate_mask<PER>(v, gw[(PER * q) >> 5] >> ((PER * q) & 31));
                     } else if (OSZ == 2) {  // x piece q sits where output piece q goes
                         uint32_t xw[4];
                         ld_shared_v4(buf + srow_off + ((static_cast<uint32_t>(q) ^ sw) << 4), xw);
-                        gate_x<IN_T, PER>(v, xw);
+                        gate_x<IN_T, PER>(v, xw, xp);
                     } else {  // fp32 output: values 4q .. 4q+3 of the chunk
-                        gate_x<IN_T, PER>(v, &xf[(2 * q) % (OSZ == 4 ? 16 : 1)]);
+                        gate_x<IN_T, PER>(v, &xf[(2 * q) % (OSZ == 4 ? 16 : 1)], xp);
+                    }
+                }
+                if (nsum) {
+                    // this piece's column sums over the warp's 32 rows, into
+                    // the warp's slot of the chunk's partials
+                    constexpr int SPREAD = 32 / PER;  // lanes that end up with the same channel
+                    float a[PER];
+#pragma unroll
+                    for (int e = 0; e < PER; ++e) a[e] = row_ok ? v[e] : 0.0f;
+                    const float t1 = warp_sum_spread<PER>(a, lane);
+                    const uint32_t slot = static_cast<uint32_t>(ew * 64 + PER * q + lane / SPREAD) * 4u;
+                    if (lane % SPREAD == 0) st_shared_f32(R.red0 + slot, t1);
+                    if (nsum == 2) {
+#pragma unroll
+                        for (int e = 0; e < PER; ++e) a[e] = row_ok ? xp[e] : 0.0f;
+                        const float t2 = warp_sum_spread<PER>(a, lane);
+                        if (lane % SPREAD == 0) st_shared_f32(R.red0 + 4u * 64u * 4u + slot, t2);
                     }
                 }
                 uint32_t wv[4];
@@ -838,6 +927,22 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
                 else
                     tma_store_3d(mapD, buf, c, 0, mt * rpt);
                 bulk_commit_group();
+            }
+            if (nsum && ethread < CH) {
+                // the chunk's column sums: the four warps' partials in warp
+                // order, added to this CTA's row (the next chunk overwrites the
+                // partials only after its first named barrier, which every
+                // thread reaches after this read)
+                const int c = c_begin + cc + ethread;
+                if (c < c_end) {
+                    const uint32_t col = static_cast<uint32_t>(ethread) * 4u;
+                    for (int k2 = 0; k2 < nsum; ++k2) {
+                        const uint32_t base = R.red0 + static_cast<uint32_t>(k2) * (4u * 64u * 4u) + col;
+                        const float t = ((ld_shared_f32(base) + ld_shared_f32(base + 256u)) + ld_shared_f32(base + 512u)) +
+                                        ld_shared_f32(base + 768u);
+                        red_row[k2 * C + c] += t;
+                    }
+                }
             }
         }
         if (!ok) break;
@@ -890,6 +995,7 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_cons
     R.acc_empty0 = bars + 16u * stages + 32u;
     R.drain = bars + 16u * stages + 64u;
     R.gfull0 = bars + 16u * stages + 80u;
+    R.red0 = bars + CDG_SMEM_TAIL;  // only plans with per-channel sums reserve it
     uint8_t *const tail = smem_raw + (bars - raw);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tail + 8 * (2 * stages + 14));
     volatile uint32_t *abort_flag = tmem_slot + 1;
@@ -1080,6 +1186,19 @@ __global__ void pack_relu_mask_kernel(const uint16_t *__restrict__ x, uint8_t *_
     bits[i] = static_cast<uint8_t>(byte);
 }
 
+// Per-channel sums: out[k][c] = sum over the workspace rows r = 0, 1, ... of
+// ws[r][k][c], added in row order (one row per CTA of the dgrad launch), so
+// the result does not depend on how the CTAs were scheduled.
+__global__ void channel_sums_kernel(const float *__restrict__ ws, int rows, int nsum, int C, float *__restrict__ out)
+{
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= nsum * C) return;
+    const int k = i / C, c = i - k * C;
+    float acc = 0.0f;
+    for (int r = 0; r < rows; ++r) acc += ws[(static_cast<size_t>(r) * nsum + k) * C + c];
+    out[i] = acc;
+}
+
 }  // namespace cdg
 
 // ------------------------------------------------------------------ launchers
@@ -1193,5 +1312,13 @@ cudaError_t cdg_launch_prepack(const void *W, void *Wp, int K, int T, int C, cud
     dim3 grid((C + 31) / 32, (K + 31) / 32, T), block(32, 8);
     cdg::prepack_kernel<<<grid, block, 0, stream>>>(static_cast<const uint16_t *>(W), static_cast<uint16_t *>(Wp),
                                                     K, T, C);
+    return cudaGetLastError();
+}
+
+cudaError_t cdg_launch_channel_sums(const float *ws, int rows, int nsum, int C, float *out, cudaStream_t stream)
+{
+    const int n = nsum * C;
+    if (n <= 0) return cudaSuccess;
+    cdg::channel_sums_kernel<<<(n + 255) / 256, 256, 0, stream>>>(ws, rows, nsum, C, out);
     return cudaGetLastError();
 }

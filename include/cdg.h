@@ -70,9 +70,12 @@ typedef enum { CDG_F16 = 0, CDG_BF16 = 1 } cdg_dtype_t;
 enum {
     CDG_EPI_RELU_BWD = 1,     /* gate by the saved activation: out = (x > 0) ? v : +0.0 */
     CDG_EPI_OUT_F32 = 2,      /* write dX as fp32 instead of the input type             */
-    CDG_EPI_RELU_BWD_BITS = 4 /* the same gate from a packed bit mask (one bit per      */
+    CDG_EPI_RELU_BWD_BITS = 4, /* the same gate from a packed bit mask (one bit per     */
                               /* element, see cdg_pack_relu_mask): out = bit ? v : +0.0 */
                               /* (not together with CDG_EPI_RELU_BWD)                   */
+    CDG_EPI_SUM = 8,          /* also the per-channel sums of the output (cdg_dgrad_sums) */
+    CDG_EPI_SUM_X = 16        /* CDG_EPI_SUM plus the per-channel sums of out * x where   */
+                              /* the gate passes; needs CDG_EPI_RELU_BWD                 */
 };
 
 /*
@@ -160,6 +163,44 @@ int cdg_prepack_weights(cdg_handle_t h, const void *W_krsc, void *Wpacked, cdg_s
  */
 int cdg_dgrad(cdg_handle_t h, const void *dY, const void *Wpacked, void *dX,
               const void *relu_mask, cdg_stream_t stream);
+
+/*
+ * dgrad with the per-channel sums of its output fused into the epilogue (the
+ * epilogue fusion of the Bolt reading notes: a reduction over the output is
+ * taken where the output is made, instead of by a second pass that re-reads
+ * it).  For a plan made with CDG_EPI_SUM, after dX = dgrad(dY, W) (gated as
+ * the plan says):
+ *
+ *     sums[c]     = sum over n, h, w of out[n,h,w,c]
+ *     sums[C + c] = sum over n, h, w with x[n,h,w,c] > 0 of out[n,h,w,c] * x[n,h,w,c]
+ *                   (CDG_EPI_SUM_X only)
+ *
+ * taken from the fp32 values before they are rounded to dX's type.  sums[c]
+ * is the bias gradient of a bias added before the ReLU, and BatchNorm's beta
+ * gradient; with x the BatchNorm output y = gamma*xhat + beta (the ReLU's
+ * input, or relu(y), which gives the same terms), BatchNorm's gamma gradient
+ * is (sums[C + c] - beta[c]*sums[c]) / gamma[c].  Positions the gate masks add
+ * nothing, whatever x holds there.
+ *
+ *   sums       device, fp32, C (CDG_EPI_SUM) or 2*C (CDG_EPI_SUM_X) values,
+ *              overwritten
+ *   workspace  device, cdg_sums_workspace_bytes(h) bytes, overwritten: each
+ *              CTA of the launch adds its tiles' column sums into a row of its
+ *              own, and a second kernel adds the rows in order
+ *
+ * Two kernel launches on stream.  The result does not depend on scheduling:
+ * every partial sum is taken in a fixed order, so repeated calls give the
+ * same bits.  Other arguments and errors as for cdg_dgrad; sums and workspace
+ * must be 16-byte aligned and overlap no other tensor (CDG_ERR_ALIAS).
+ * cdg_dgrad, cdg_dgrad_noalloc and cdg_autotune refuse plans made with the
+ * sum flags (CDG_ERR_INVALID_ARG, CDG_ERR_INVALID_ARG, CDG_ERR_UNSUPPORTED).
+ */
+int cdg_dgrad_sums(cdg_handle_t h, const void *dY, const void *Wpacked, void *dX, const void *relu_mask, float *sums,
+                   void *workspace, cdg_stream_t stream);
+
+/* Bytes of the workspace cdg_dgrad_sums needs: (SM count) x (1 or 2) x C x 4;
+ * 0 for a plan without the sum flags. */
+size_t cdg_sums_workspace_bytes(cdg_handle_t h);
 
 /*
  * Synchronise stream, then read and clear the handle's device status word:

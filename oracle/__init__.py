@@ -5,6 +5,9 @@ the operation the GPU library computes (the gradient of a cross-correlation
 Conv2d with respect to its input, "Conv2d dgrad" in apache/tvm PR #10110),
 and of the weight gradient (wgrad) that the page names as its follow-up.
 
+It also states the per-channel sums of the output that a fused epilogue
+produces (``channel_sums``).
+
 Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
 leg may import this package.  The GPU library never touches it; the two share
 no code.  Arrays are numpy: fp16/bf16 tensors are passed as ``uint16`` bit
@@ -60,6 +63,8 @@ def _load():
             lib.oracle_wgrad.restype = i
             lib.oracle_wgrad_elements.argtypes = [vp, vp, i, vp, ctypes.c_int64, vp] + [i] * 10
             lib.oracle_wgrad_elements.restype = i
+            lib.oracle_channel_sums.argtypes = [vp, vp, i, ctypes.c_int64, i, vp, vp, vp, vp]
+            lib.oracle_channel_sums.restype = i
             lib.oracle_out_extent.argtypes = [i] * 5
             lib.oracle_out_extent.restype = i
             lib.oracle_half_to_double.argtypes = [ctypes.c_uint16]
@@ -204,3 +209,27 @@ def conv_fwd(x, W, stride=1, pad=0, dil=1, dtype=None):
     if rc:
         raise RuntimeError("oracle_conv_fwd failed")
     return y
+
+
+def channel_sums(out, x=None, dtype=None):
+    """Per-channel sums of a dgrad output ``out`` (float64, [..., C], the
+    gated dX as ``dgrad`` returns it): returns (s1, s2, a1, a2) with
+    s1[c] = sum of out[..., c], s2[c] = sum of out*x over the positions where
+    x > 0 (None without x), and a1, a2 the sums of the absolute values of the
+    same terms.  ``x`` is the saved activation (uint16 bits of ``dtype``, same
+    shape as out)."""
+    out = np.ascontiguousarray(out, dtype=np.float64)
+    C = out.shape[-1]
+    pixels = out.size // C
+    code = 0
+    if x is not None:
+        code = _dtype_of(x, dtype)
+        _check(x, code)
+        if x.size != out.size:
+            raise ValueError("x must have out's shape")
+    s1, a1 = np.empty(C), np.empty(C)
+    s2, a2 = (np.empty(C), np.empty(C)) if x is not None else (None, None)
+    rc = _load().oracle_channel_sums(_ptr(out), _ptr(x), code, pixels, C, _ptr(s1), _ptr(s2), _ptr(a1), _ptr(a2))
+    if rc:
+        raise RuntimeError("oracle_channel_sums failed")
+    return s1, s2, a1, a2

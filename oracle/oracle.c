@@ -39,7 +39,9 @@
  * hand-worked case, integer-exact results and an independent library routine.
  *
  * The file also states the weight gradient (wgrad) of the same convolution,
- * the page's announced follow-up, pinned the same ways (oracle_wgrad below).
+ * the page's announced follow-up, pinned the same ways (oracle_wgrad below),
+ * and the per-channel sums of the output that a fused epilogue produces
+ * (oracle_channel_sums below).
  */
 #include <math.h>
 #include <stdint.h>
@@ -366,6 +368,54 @@ int oracle_wgrad_elements(const void *dY, const void *x, int dtype, const int32_
                 }
         }
         out[i] = acc;
+    }
+    return 0;
+}
+
+/*
+ * Per-channel sums of the dgrad output, the reductions a fused epilogue hands
+ * to the layer below (the epilogue fusion of the Bolt reading notes: work
+ * that would otherwise re-read the output is done where the output is made):
+ *
+ *   s1[c] = sum over n, h, w of out[n,h,w,c]
+ *   s2[c] = sum over n, h, w with x[n,h,w,c] > 0 of out[n,h,w,c] * x[n,h,w,c]
+ *
+ * out is the (gated) dX as this oracle computes it, in double, NHWC with
+ * `pixels` = N*H*W rows of C channels; x is the saved activation the gate
+ * reads (element type `dtype`; NULL: s2 is not computed).  s1 is the bias
+ * gradient of a bias added before the ReLU and BatchNorm's beta gradient;
+ * with x the BatchNorm output y (or relu(y)), s2 = sum out*y, from which
+ * BatchNorm's gamma gradient is (s2 - beta*s1)/gamma.  Positions the gate
+ * masks contribute nothing to s2, whatever x holds there (NaN included).
+ * a1[c] and a2[c] receive the sums of the absolute values of the same terms
+ * (the scale against which rounding errors of a reordered sum are bounded).
+ * Each channel's sums run over the pixels in order.
+ */
+int oracle_channel_sums(const double *out, const void *x, int dtype, int64_t pixels, int C,
+                        double *s1, double *s2, double *a1, double *a2)
+{
+    if (pixels < 0 || C <= 0) return -1;
+    for (int c = 0; c < C; ++c) {
+        s1[c] = 0.0;
+        a1[c] = 0.0;
+        if (x) {
+            s2[c] = 0.0;
+            a2[c] = 0.0;
+        }
+    }
+    for (int64_t i = 0; i < pixels; ++i) {
+        const double *row = out + (size_t)i * (size_t)C;
+        for (int c = 0; c < C; ++c) {
+            s1[c] += row[c];
+            a1[c] += fabs(row[c]);
+            if (x) {
+                double xv = load_one(x, (size_t)i * (size_t)C + c, dtype);
+                if (xv > 0.0) {
+                    s2[c] += row[c] * xv;
+                    a2[c] += fabs(row[c] * xv);
+                }
+            }
+        }
     }
     return 0;
 }

@@ -56,7 +56,8 @@ GOOD = (2, 8, 8, 16, 16, 3, 3, 1, 1, 1, cdg.BF16, 0)
 @pytest.mark.parametrize("host", [True, False])
 @pytest.mark.parametrize("field,value,expect", [
     (0, 0, 1), (1, 0, 1), (3, 0, 1), (5, 0, 1), (7, 0, 1), (8, -1, 1), (9, 0, 1),
-    (10, 2, 1), (11, 8, 1), (11, 5, 1),  # unknown epilogue flag; both ReLU gates at once
+    (10, 2, 1), (11, 32, 1), (11, 5, 1),  # unknown epilogue flag; both ReLU gates at once
+    (11, 16, 1), (11, 24, 1), (11, 28, 1),  # sums of out*x without the x gate (none, or the bit mask)
     (3, 12, 2), (4, 20, 2), (7, 5, 2),
 ])
 def test_argument_validation_needs_no_device(host, field, value, expect):
@@ -333,3 +334,25 @@ def test_wait_limit_and_withheld_load_arguments():
         pair.withhold_load_for_test(3)
     rows = cdg.plan_host(4, 14, 14, 256, 64, 1, 1, 1, 0, 1, "bf16", num_sms=148)
     rows.withhold_load_for_test(1)
+
+
+def test_sum_plans_reserve_the_partials_and_size_the_workspace():
+    """Plans with per-channel sums reserve 2 KB more shared memory for the
+    epilogue warps' partials and need a workspace of one row per SM."""
+    base = cdg.plan_host(4, 14, 14, 256, 64, 1, 1, 1, 0, 1, "bf16", num_sms=148)
+    s1 = cdg.plan_host(4, 14, 14, 256, 64, 1, 1, 1, 0, 1, "bf16", num_sms=148, sums=1)
+    s2 = cdg.plan_host(4, 14, 14, 256, 64, 1, 1, 1, 0, 1, "bf16", num_sms=148, relu=True, sums=2)
+    assert base.sums_workspace_bytes == 0
+    assert s1.sums_workspace_bytes == 148 * 256 * 4 and s2.sums_workspace_bytes == 148 * 2 * 256 * 4
+    assert s1.info()["smem_bytes"] <= 232448 and s2.info()["smem_bytes"] <= 232448
+    for p in (base, s1, s2):
+        assert p.info()["stages"] >= 2
+    with pytest.raises(cdg.CdgError) as e:  # plain cdg_dgrad refuses a plan with sums
+        s1.dgrad(1 << 20, 2 << 20, 3 << 20)
+    assert e.value.status == 1
+    with pytest.raises(cdg.CdgError) as e:  # and a plan without them has no sums to give
+        base.dgrad_sums(1 << 20, 2 << 20, 3 << 20, 4 << 20, 5 << 20)
+    assert e.value.status == 1
+    with pytest.raises(cdg.CdgError) as e:  # host-only plans refuse device work after the checks
+        s1.dgrad_sums(1 << 20, 2 << 20, 3 << 20, 4 << 20, 5 << 20)
+    assert e.value.status == 7
