@@ -347,14 +347,27 @@ def cpu_oracle_sample(layers, arrays, images: int):
             "seconds": dt}
 
 
+def hold_stream(torch, stream, ms: float = 2.0) -> None:
+    """Queue a ~ms busy-wait kernel on `stream` (no memory traffic), so that
+    the host enqueues the launches and events that follow before the GPU
+    reaches them: otherwise a launch shorter than the host's cost of issuing
+    it would be timed together with the idle gap before it."""
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(int(ms * 2.0e6))
+
+
 def time_launches(torch, stream, fn, reps: int, flush=None) -> list:
     """Device time (ms) of each of `reps` calls of fn, one CUDA event pair
     around each on `stream`.  With `flush` (a byte buffer larger than L2), the
     buffer is overwritten before every call, outside the events, so each call
-    starts with a cold L2."""
+    starts with a cold L2; without it, consecutive calls find their data in L2
+    (a busy-wait kernel queued first keeps the host's issue cost out of the
+    events)."""
     e0 = [torch.cuda.Event(enable_timing=True) for _ in range(reps)]
     e1 = [torch.cuda.Event(enable_timing=True) for _ in range(reps)]
     torch.cuda.synchronize()
+    if flush is None:
+        hold_stream(torch, stream)
     for k in range(reps):
         if flush is not None:
             with torch.cuda.stream(stream):
@@ -527,6 +540,7 @@ def run_wgrad(args, rank, world, local_rank):
             raise RuntimeError(f"wgrad device status after warm-up ({L.name})")
     nL = len(state)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nL + 1)] for _ in range(args.steps)]
+    hold_stream(torch, stream)
     for k in range(args.steps):
         evs[k][0].record(stream)
         for i, (_, p, d_dY, d_x, d_dW, ws) in enumerate(state):
@@ -538,6 +552,7 @@ def run_wgrad(args, rank, world, local_rank):
     e1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     torch.cuda.synchronize()
     with ClockSampler(local_rank) as clocks:
+        hold_stream(torch, stream)
         for k in range(args.steps):
             e0[k].record(stream)
             step()
@@ -706,6 +721,7 @@ def main():
         consecutive launches that the timed steps get)."""
         evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nL + 1)] for _ in range(steps)]
         torch.cuda.synchronize()
+        hold_stream(torch, stream)
         for k in range(steps):
             evs[k][0].record(stream)
             for i, (_, p, d_dY, d_Wp, d_dX) in enumerate(state):
@@ -733,6 +749,7 @@ def main():
     torch.cuda.synchronize()
     with ClockSampler(local_rank) as clocks:
         t_host0 = time.perf_counter()
+        hold_stream(torch, stream)  # before the first event: the timed region starts at ev0[0]
         for k in range(args.steps):
             ev0[k].record(stream)
             for i, (_, p, d_dY, d_Wp, d_dX) in enumerate(state):

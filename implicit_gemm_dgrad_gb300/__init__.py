@@ -30,6 +30,8 @@ ERR_SCRATCH_TOO_SMALL = 8
 NOALLOC_MAX_WEIGHT_BYTES = 8 << 20
 F16, BF16 = 0, 1
 EPI_RELU_BWD, EPI_OUT_F32, EPI_RELU_BWD_BITS, EPI_SUM, EPI_SUM_X = 1, 2, 4, 8, 16
+EPI_GELU_BWD, EPI_SILU_BWD = 32, 64
+ACT_FLAGS = {"relu": EPI_RELU_BWD, "gelu": EPI_GELU_BWD, "silu": EPI_SILU_BWD}
 DTYPES = {"f16": F16, "bf16": BF16}
 
 EXPORTS = ("cdg_plan", "cdg_plan_host", "cdg_destroy", "cdg_get_output_dims", "cdg_packed_weight_bytes",
@@ -191,15 +193,16 @@ class Plan:
     """One planned dgrad shape (a ``cdg_handle_t``)."""
 
     def __init__(self, N, H, W, C, K, R, S, stride=1, pad=0, dil=1, dtype="bf16", relu=False,
-                 out_f32=False, host_sms: int | None = None, relu_bits=False, sums: int = 0):
+                 out_f32=False, host_sms: int | None = None, relu_bits=False, sums: int = 0, act: str = "relu"):
         self.lib = load_library()
         self.shape = dict(N=N, H=H, W=W, C=C, K=K, R=R, S=S, stride=stride, pad=pad, dil=dil)
         self.dtype = dtype
-        self.relu = relu
+        self.relu = relu          # the gate reads a saved tensor of dX's shape (ReLU's x, or act's input)
         self.relu_bits = relu_bits
         self.out_f32 = out_f32
         self.sums = int(sums)
-        epi = (EPI_RELU_BWD if relu else 0) | (EPI_OUT_F32 if out_f32 else 0) | (EPI_RELU_BWD_BITS if relu_bits else 0)
+        gate = ACT_FLAGS[act] if relu else 0
+        epi = gate | (EPI_OUT_F32 if out_f32 else 0) | (EPI_RELU_BWD_BITS if relu_bits else 0)
         epi |= {0: 0, 1: EPI_SUM, 2: EPI_SUM | EPI_SUM_X}[self.sums]
         h = ctypes.c_void_p()
         dt = DTYPES[dtype] if isinstance(dtype, str) else int(dtype)
@@ -417,8 +420,11 @@ def wgrad_plan_host(N, H, W, C, K, R, S, stride=1, pad=0, dil=1, dtype="bf16", o
 
 
 def plan(N, H, W, C, K, R, S, stride=1, pad=0, dil=1, dtype="bf16", relu=False, out_f32=False,
-         relu_bits=False, sums: int = 0) -> Plan:
-    return Plan(N, H, W, C, K, R, S, stride, pad, dil, dtype, relu, out_f32, relu_bits=relu_bits, sums=sums)
+         relu_bits=False, sums: int = 0, act: str = "relu") -> Plan:
+    """relu=True: the epilogue applies the backward of activation `act`
+    ("relu" gate, "gelu", "silu") with the saved tensor passed to dgrad."""
+    return Plan(N, H, W, C, K, R, S, stride, pad, dil, dtype, relu, out_f32, relu_bits=relu_bits, sums=sums,
+                act=act)
 
 
 def relu_mask_bytes(pixels: int, C: int) -> int:
@@ -444,6 +450,6 @@ def pack_relu_mask(x, bits, pixels: int, C: int, dtype="bf16", stream=None) -> N
 
 
 def plan_host(N, H, W, C, K, R, S, stride=1, pad=0, dil=1, dtype="bf16", relu=False, out_f32=False,
-              num_sms=148, relu_bits=False, sums: int = 0) -> Plan:
+              num_sms=148, relu_bits=False, sums: int = 0, act: str = "relu") -> Plan:
     return Plan(N, H, W, C, K, R, S, stride, pad, dil, dtype, relu, out_f32, host_sms=num_sms, relu_bits=relu_bits,
-                sums=sums)
+                sums=sums, act=act)

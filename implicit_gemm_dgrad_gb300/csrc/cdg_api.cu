@@ -195,9 +195,12 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     if (N < 1 || H < 1 || W < 1 || C < 1 || K < 1 || R < 1 || S < 1 || stride < 1 || pad < 0 || dil < 1)
         return CDG_ERR_INVALID_ARG;
     if (dtype != CDG_F16 && dtype != CDG_BF16) return CDG_ERR_INVALID_ARG;
-    if (epilogue & ~(CDG_EPI_RELU_BWD | CDG_EPI_OUT_F32 | CDG_EPI_RELU_BWD_BITS | CDG_EPI_SUM | CDG_EPI_SUM_X))
+    if (epilogue & ~(CDG_EPI_RELU_BWD | CDG_EPI_OUT_F32 | CDG_EPI_RELU_BWD_BITS | CDG_EPI_SUM | CDG_EPI_SUM_X |
+                     CDG_EPI_GELU_BWD | CDG_EPI_SILU_BWD))
         return CDG_ERR_INVALID_ARG;
-    if ((epilogue & CDG_EPI_RELU_BWD) && (epilogue & CDG_EPI_RELU_BWD_BITS)) return CDG_ERR_INVALID_ARG;
+    const int gates = ((epilogue & CDG_EPI_RELU_BWD) != 0) + ((epilogue & CDG_EPI_RELU_BWD_BITS) != 0) +
+                      ((epilogue & CDG_EPI_GELU_BWD) != 0) + ((epilogue & CDG_EPI_SILU_BWD) != 0);
+    if (gates > 1) return CDG_ERR_INVALID_ARG;
     if ((epilogue & CDG_EPI_SUM_X) && !(epilogue & CDG_EPI_RELU_BWD)) return CDG_ERR_INVALID_ARG;
     const long long spanH = 1LL * H + 2LL * pad - 1LL * dil * (R - 1) - 1;
     const long long spanW = 1LL * W + 2LL * pad - 1LL * dil * (S - 1) - 1;
@@ -222,7 +225,7 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     h->opts = opt;
     h->in_type = dtype == CDG_F16 ? CDG_T_F16 : CDG_T_BF16;
     h->out_type = (epilogue & CDG_EPI_OUT_F32) ? CDG_T_F32 : h->in_type;
-    h->mask = (epilogue & (CDG_EPI_RELU_BWD | CDG_EPI_RELU_BWD_BITS)) != 0;
+    h->mask = (epilogue & (CDG_EPI_RELU_BWD | CDG_EPI_RELU_BWD_BITS | CDG_EPI_GELU_BWD | CDG_EPI_SILU_BWD)) != 0;
     h->mask_bits = (epilogue & CDG_EPI_RELU_BWD_BITS) != 0;
     const int nsum = (epilogue & CDG_EPI_SUM_X) ? 2 : ((epilogue & CDG_EPI_SUM) ? 1 : 0);
 
@@ -296,7 +299,9 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     // a tile's mask bytes must start on a 16-byte unit: multiples of 128.
     const int bn_step = h->mask_bits ? 128 : 64;
     int BN = choose_bn(C, opt.max_bn == 128 ? 128 : 256, bn_step);
-    if (opt.bn > 0 && opt.bn % bn_step == 0 && opt.bn <= 256 && opt.bn < ((C + 15) / 16) * 16) BN = opt.bn;
+    if (opt.bn > 0 && opt.bn % bn_step == 0 && opt.bn <= (opt.max_bn == 128 ? 128 : 256) &&
+        opt.bn < ((C + 15) / 16) * 16)
+        BN = opt.bn;
     const int tiles_n = ceil_div(C, BN);
     // output staging; gated by the activation: four buffers, its chunks land in
     // them ahead of use; by the packed mask: a ring of mask tiles besides
@@ -390,7 +395,8 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     // 2-SM MMA, each holding its 128 rows of dY and half of the weight tile.
     // Measured on GB300 over the ResNet-50 layers: pairs win (4-8 %) for
     // 256-channel N tiles whose tiles run at least 9 pipeline stages, and lose
-    // elsewhere (short tiles couple two SMs' epilogues and rings).
+    // elsewhere (short tiles couple two SMs' epilogues and rings); 192-channel
+    // tiles (below) behave alike.
     int tap_phases = 0, tap_sum = 0;
     for (const CdgPhase &f : phases)
         if (f.tap_count > 0) {
@@ -398,7 +404,7 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
             tap_sum += f.tap_count;
         }
     const double stages_per_tile = tap_phases ? double(tap_sum) / tap_phases * ceil_div(K, CDG_BK) : 0.0;
-    bool pair = !halo && BN == 256 && num_sms >= 2 && stages_per_tile >= 9.0;
+    bool pair = !halo && BN >= 192 && num_sms >= 2 && stages_per_tile >= 9.0;
     if (opt.pair == 0) pair = false;
     if (opt.pair == 1) pair = !halo && BN >= 128 && num_sms >= 2;
 
@@ -486,6 +492,7 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     p.wait_limit_ns = CDG_WAIT_LIMIT_NS;
     p.withhold_stage = -1;
     p.mask_bits = h->mask_bits ? 1 : 0;
+    p.act = (epilogue & CDG_EPI_GELU_BWD) ? 1 : ((epilogue & CDG_EPI_SILU_BWD) ? 2 : 0);
     // gate loads take the dX store box: its rows x the activation chunk's bytes
     // (64 channels; 32 with fp32 output) or the item's mask bytes per row
     {
@@ -763,6 +770,44 @@ int launch_plan(cdg_handle_t h, const void *dY, const void *Wpacked, void *dX, c
     return CDG_OK;
 }
 
+// Scheduling rounds x tile width of the items with taps: the tensor time of
+// the longest CTA, in tile-width units (every item of a layer does the same
+// number of pipeline stages per channel of its tile).
+long long round_cost(const cdg_plan_st *h)
+{
+    const CdgParams &p = h->prm;
+    long long items = 0;
+    for (int i = 0; i < p.nphases; ++i)
+        if (p.phase[i].tap_count > 0) items += p.phase[i].items;
+    const long long G = std::max(1, p.pair ? h->grid / 2 : h->grid);
+    return (items + G - 1) / G * p.BN;
+}
+
+// The planner's N tile for C > 256 channels is 256 (or the multiple of 64 with
+// the least padding); when the last scheduling round of those tiles is
+// nearly empty, 192-channel tiles can fill the rounds better.  Measured on
+// GB300 for the ResNet-50 layers: the 1x1 512 -> 2048 channel layer at 7x7
+// (98 M tiles x 2 N tiles over 76 CTA pairs = 1.29 rounds) runs 31.9 ->
+// 27.0 us with 192-channel tiles (3 N tiles, 1.93 rounds); every other layer
+// runs slower with them.  So 192 is taken only when its rounds x width comes
+// out at least 10 % below the default's.
+int choose_plan_bn(int N, int H, int W, int C, int K, int R, int S, int stride, int pad, int dil, int dtype,
+                   int epilogue, int num_sms, const PlanOpts &opt)
+{
+    if (opt.bn > 0 || C <= 256 || opt.max_bn != 256 || (epilogue & CDG_EPI_RELU_BWD_BITS)) return opt.bn;
+    cdg_handle_t a = nullptr, b = nullptr;
+    PlanOpts o192 = opt;
+    o192.bn = 192;
+    int bn = 0;
+    if (make_plan(N, H, W, C, K, R, S, stride, pad, dil, dtype, epilogue, num_sms, true, opt, &a) == CDG_OK &&
+        make_plan(N, H, W, C, K, R, S, stride, pad, dil, dtype, epilogue, num_sms, true, o192, &b) == CDG_OK &&
+        b->prm.BN == 192 && 10 * round_cost(b) <= 9 * round_cost(a))
+        bn = 192;
+    cdg_destroy(a);
+    cdg_destroy(b);
+    return bn;
+}
+
 }  // namespace
 
 extern "C" {
@@ -774,13 +819,14 @@ int cdg_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int pa
     int dev = 0, sms = 0;
     // validate first so that argument errors never depend on a device
     cdg_handle_t probe = nullptr;
-    const PlanOpts opt = opts_from_env();
+    PlanOpts opt = opts_from_env();
     int rc = make_plan(N, H, W, C, K, R, S, stride, pad, dil, dtype, epilogue, 1, true, opt, &probe);
     if (rc != CDG_OK) return rc;
     cdg_destroy(probe);
     if (cudaGetDevice(&dev) != cudaSuccess) return CDG_ERR_CUDA;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
         return CDG_ERR_CUDA;
+    opt.bn = choose_plan_bn(N, H, W, C, K, R, S, stride, pad, dil, dtype, epilogue, sms, opt);
     return make_plan(N, H, W, C, K, R, S, stride, pad, dil, dtype, epilogue, sms, false, opt, out);
 }
 
@@ -791,7 +837,9 @@ int cdg_plan_host(int N, int H, int W, int C, int K, int R, int S, int stride, i
         if (out) *out = nullptr;
         return CDG_ERR_INVALID_ARG;
     }
-    return make_plan(N, H, W, C, K, R, S, stride, pad, dil, dtype, epilogue, num_sms, true, opts_from_env(), out);
+    PlanOpts opt = opts_from_env();
+    opt.bn = choose_plan_bn(N, H, W, C, K, R, S, stride, pad, dil, dtype, epilogue, num_sms, opt);
+    return make_plan(N, H, W, C, K, R, S, stride, pad, dil, dtype, epilogue, num_sms, true, opt, out);
 }
 
 void cdg_destroy(cdg_handle_t h)
@@ -891,13 +939,14 @@ int cdg_autotune(cdg_handle_t h, const void *dY, const void *Wpacked, void *dX, 
     std::vector<PlanOpts> cands;
     const PlanOpts base = h->opts;
     cands.push_back(base);
-    auto variant = [&](int pair, int dual, int halo, int interleave, int max_bn) {
+    auto variant = [&](int pair, int dual, int halo, int interleave, int max_bn, int bn = -1) {
         PlanOpts o = base;
         if (pair != -2) o.pair = pair;
         if (dual != -2) o.dual = dual;
         if (halo != -2) o.halo = halo;
         if (interleave != -2) o.interleave = interleave;
         if (max_bn) o.max_bn = max_bn;
+        if (bn >= 0) o.bn = bn;
         cands.push_back(o);
     };
     variant(0, -2, -2, -2, 0);    // no CTA pairs
@@ -909,6 +958,8 @@ int cdg_autotune(cdg_handle_t h, const void *dY, const void *Wpacked, void *dX, 
     variant(-2, -2, -2, -2, 128); // 128-channel N tiles
     variant(1, -2, -2, -2, 128);
     variant(-2, 0, -2, -2, 128);
+    variant(-2, -2, -2, -2, 0, 0);    // the default N tile (256 channels when C > 256)
+    variant(-2, -2, -2, -2, 0, 192);  // 192-channel N tiles
 
     cudaEvent_t e0 = nullptr, e1 = nullptr;
     if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) {

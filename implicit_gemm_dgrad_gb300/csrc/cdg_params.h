@@ -79,6 +79,8 @@ struct CdgParams {  // CUtensorMap members carry their own (128-byte) alignment
     int pair;             // 1: CTA pairs (clusters of 2) share 256-row tiles through 2-SM MMAs
     int pdl;              // 1: launch with programmatic stream serialization (host side only)
     int mask_bits;        // 1: the gate reads the packed bit mask (rows of 16-byte units per pixel), not x
+    int act;              // activation whose backward the gate applies with x: 0 ReLU (select),
+                          // 1 GELU (erf form), 2 SiLU (out = dX * f'(x))
     int gate_row_bytes;   // bytes of one tile row of a gate load (activation chunk, or mask tile)
     uint32_t gate_tx;     // bytes one gate load delivers (the store box's rows x gate_row_bytes)
     int dual;             // 1: two MMA warps, each with half of the stages and two accumulators

@@ -596,17 +596,39 @@ __device__ __forceinline__ void gate_issue(const CdgParams &p, const GateCursor 
 
 // ReLU-backward gate on PER consecutive values: v = (x > 0) ? v : +0.0 (a
 // select, so masked outputs are +0.0 whatever the accumulator holds).
-// xp receives the gated value times x where the gate passes, +0.0 elsewhere
-// (the terms of the per-channel sum of dX * x).
+// Derivative of the activation at its saved input x: GELU in its erf form,
+// f'(x) = Phi(x) + x phi(x) with Phi(x) = (1 + erf(x / sqrt 2)) / 2 and
+// phi(x) = exp(-x^2 / 2) / sqrt(2 pi); SiLU, f'(x) = s (1 + x (1 - s)) with
+// s = 1 / (1 + exp(-x)).  erff and expf are CUDA's.
+__device__ __forceinline__ float act_grad(float x, int act)
+{
+    if (act == 1) {
+        const float Phi = 0.5f * (1.0f + erff(x * 0.70710678118654752f));
+        const float phi = 0.39894228040143268f * expf(-0.5f * x * x);
+        return fmaf(x, phi, Phi);
+    }
+    const float sg = 1.0f / (1.0f + expf(-x));
+    return sg * fmaf(x, 1.0f - sg, 1.0f);
+}
+
+// Backward of the activation whose saved input is x, on PER consecutive
+// values.  ReLU (act 0): v = (x > 0) ? v : +0.0 (a select, so masked outputs
+// are +0.0 whatever the accumulator holds), and xp receives v * x where the
+// gate passes, +0.0 elsewhere (the terms of the per-channel sum of dX * x).
+// GELU and SiLU: v = v * f'(x).
 template <int IN_T, int PER>
-__device__ __forceinline__ void gate_x(float *v, const uint32_t *w, float *xp)
+__device__ __forceinline__ void gate_x(float *v, const uint32_t *w, float *xp, int act)
 {
 #pragma unroll
     for (int e = 0; e < PER; ++e) {
         const float x = gate_value<IN_T>(static_cast<uint16_t>(w[e >> 1] >> (16 * (e & 1))));
-        const bool pass = x > 0.0f;
-        v[e] = pass ? v[e] : 0.0f;
-        xp[e] = pass ? v[e] * x : 0.0f;
+        if (act == 0) {
+            const bool pass = x > 0.0f;
+            v[e] = pass ? v[e] : 0.0f;
+            xp[e] = pass ? v[e] * x : 0.0f;
+        } else {
+            v[e] *= act_grad(x, act);
+        }
     }
 }
 
@@ -883,9 +905,9 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
                     } else if (OSZ == 2) {  // x piece q sits where output piece q goes
                         uint32_t xw[4];
                         ld_shared_v4(buf + srow_off + ((static_cast<uint32_t>(q) ^ sw) << 4), xw);
-                        gate_x<IN_T, PER>(v, xw, xp);
+                        gate_x<IN_T, PER>(v, xw, xp, p.act);
                     } else {  // fp32 output: values 4q .. 4q+3 of the chunk
-                        gate_x<IN_T, PER>(v, &xf[(2 * q) % (OSZ == 4 ? 16 : 1)], xp);
+                        gate_x<IN_T, PER>(v, &xf[(2 * q) % (OSZ == 4 ? 16 : 1)], xp, p.act);
                     }
                 }
                 if (nsum) {

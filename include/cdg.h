@@ -74,8 +74,14 @@ enum {
                               /* element, see cdg_pack_relu_mask): out = bit ? v : +0.0 */
                               /* (not together with CDG_EPI_RELU_BWD)                   */
     CDG_EPI_SUM = 8,          /* also the per-channel sums of the output (cdg_dgrad_sums) */
-    CDG_EPI_SUM_X = 16        /* CDG_EPI_SUM plus the per-channel sums of out * x where   */
+    CDG_EPI_SUM_X = 16,       /* CDG_EPI_SUM plus the per-channel sums of out * x where   */
                               /* the gate passes; needs CDG_EPI_RELU_BWD                 */
+    CDG_EPI_GELU_BWD = 32,    /* GELU backward: out = v * f'(x), x the GELU's saved      */
+                              /* input (same layout and type as for CDG_EPI_RELU_BWD),   */
+                              /* f(x) = x (1 + erf(x / sqrt 2)) / 2                      */
+    CDG_EPI_SILU_BWD = 64     /* SiLU backward: out = v * f'(x), f(x) = x / (1 + e^-x)   */
+                              /* (at most one of RELU_BWD, RELU_BWD_BITS, GELU_BWD,      */
+                              /* SILU_BWD)                                               */
 };
 
 /*
@@ -154,8 +160,9 @@ int cdg_prepack_weights(cdg_handle_t h, const void *W_krsc, void *Wpacked, cdg_s
  * dX = dgrad(dY, W) for the planned shape, one kernel launch, asynchronous
  * on stream.  relu_mask is the saved activation x for a plan with
  * CDG_EPI_RELU_BWD (NHWC like dX, input dtype), the packed mask for
- * CDG_EPI_RELU_BWD_BITS (cdg_pack_relu_mask's layout), else NULL; it must not
- * overlap dX.  Every element of dX is written, including pixels no
+ * CDG_EPI_RELU_BWD_BITS (cdg_pack_relu_mask's layout), the activation's saved
+ * input for CDG_EPI_GELU_BWD or CDG_EPI_SILU_BWD (NHWC like dX, input
+ * dtype), else NULL; it must not overlap dX.  Every element of dX is written, including pixels no
  * filter tap reaches (+0.0); dX is never read, so its prior contents do not
  * matter.  dY, Wpacked and x are only read.  No workspace, no allocation.
  * A device-side pipeline timeout (which a correct launch never hits) is

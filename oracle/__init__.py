@@ -27,6 +27,7 @@ SRC = os.path.join(HERE, "oracle.c")
 LIB = os.path.join(HERE, "liboracle.so")
 
 F16, BF16, F32, F64 = 0, 1, 2, 3
+ACTS = {"relu": 0, "gelu": 1, "silu": 2}
 DTYPE_CODES = {"f16": F16, "bf16": BF16, "f32": F32, "f64": F64}
 
 _lock = threading.Lock()
@@ -53,10 +54,12 @@ def _load():
             build()
             lib = ctypes.CDLL(LIB)
             vp, ip, i = ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32), ctypes.c_int
-            lib.oracle_dgrad.argtypes = [vp, vp, vp, i, vp] + [i] * 10
-            lib.oracle_dgrad.restype = i
-            lib.oracle_dgrad_pixels.argtypes = [vp, vp, vp, i, vp, ctypes.c_int64, vp] + [i] * 10
-            lib.oracle_dgrad_pixels.restype = i
+            lib.oracle_dgrad_act.argtypes = [vp, vp, vp, i, i, vp] + [i] * 10
+            lib.oracle_dgrad_act.restype = i
+            lib.oracle_dgrad_pixels_act.argtypes = [vp, vp, vp, i, i, vp, ctypes.c_int64, vp] + [i] * 10
+            lib.oracle_dgrad_pixels_act.restype = i
+            lib.oracle_act_grad.argtypes = [ctypes.c_double, i]
+            lib.oracle_act_grad.restype = ctypes.c_double
             lib.oracle_conv_fwd.argtypes = [vp, vp, i, vp] + [i] * 10
             lib.oracle_conv_fwd.restype = i
             lib.oracle_wgrad.argtypes = [vp, vp, i, vp] + [i] * 10
@@ -113,11 +116,18 @@ def bf16_to_double(bits: int) -> float:
     return _load().oracle_bf16_to_double(bits)
 
 
-def dgrad(dY, W, H, Wd, stride=1, pad=0, dil=1, x=None, dtype=None):
+def act_grad(x: float, act: str) -> float:
+    """Derivative of the activation ``act`` ("gelu": erf form, "silu") at x."""
+    return _load().oracle_act_grad(float(x), ACTS[act])
+
+
+def dgrad(dY, W, H, Wd, stride=1, pad=0, dil=1, x=None, dtype=None, act="relu"):
     """dX (float64, NHWC [N][H][Wd][C]) from dY [N][P][Q][K] and W [K][R][S][C].
 
     H and Wd are dX's spatial sizes.  ``x`` (same shape as dX, same element
-    type as dY) enables the ReLU-backward gate.
+    type as dY) enables the activation-backward epilogue: for act "relu" the
+    gate (x > 0) ? dX : +0.0, for "gelu" and "silu" dX * f'(x) with x the
+    activation's saved input.
     """
     code = _dtype_of(dY, dtype)
     N, P, Q, K = dY.shape
@@ -131,14 +141,14 @@ def dgrad(dY, W, H, Wd, stride=1, pad=0, dil=1, x=None, dtype=None):
     if x is not None and x.shape != (N, H, Wd, C):
         raise ValueError("x must have dX's shape")
     out = np.empty((N, H, Wd, C), np.float64)
-    rc = _load().oracle_dgrad(_ptr(dY), _ptr(W), _ptr(x), code, _ptr(out),
-                              N, H, Wd, C, K, R, S, stride, pad, dil)
+    rc = _load().oracle_dgrad_act(_ptr(dY), _ptr(W), _ptr(x), ACTS[act], code, _ptr(out),
+                                  N, H, Wd, C, K, R, S, stride, pad, dil)
     if rc:
         raise RuntimeError("oracle_dgrad failed")
     return out
 
 
-def dgrad_pixels(dY, W, H, Wd, pix, stride=1, pad=0, dil=1, x=None, dtype=None):
+def dgrad_pixels(dY, W, H, Wd, pix, stride=1, pad=0, dil=1, x=None, dtype=None, act="relu"):
     """dgrad at the pixels ``pix`` (int array [npix][3] of (n, h, w)) -> [npix][C]."""
     code = _dtype_of(dY, dtype)
     N, P, Q, K = dY.shape
@@ -147,8 +157,8 @@ def dgrad_pixels(dY, W, H, Wd, pix, stride=1, pad=0, dil=1, x=None, dtype=None):
         _check(a, code)
     pix = np.ascontiguousarray(pix, dtype=np.int32).reshape(-1, 3)
     out = np.empty((pix.shape[0], C), np.float64)
-    rc = _load().oracle_dgrad_pixels(_ptr(dY), _ptr(W), _ptr(x), code,
-                                     pix.ctypes.data_as(ctypes.c_void_p),
+    rc = _load().oracle_dgrad_pixels_act(_ptr(dY), _ptr(W), _ptr(x), ACTS[act], code,
+                                         pix.ctypes.data_as(ctypes.c_void_p),
                                      pix.shape[0], _ptr(out),
                                      N, H, Wd, C, K, R, S, stride, pad, dil)
     if rc:

@@ -25,6 +25,8 @@
  * Optional ReLU-backward epilogue (the "activation fusion" for dgrad that the
  * same page says is not enabled yet, last comments): the saved activation x
  * gates each output, out = (x > 0) ? dX : +0.0.  x <= 0, -0.0 and NaN give +0.0.
+ * Other activations (GELU, SiLU) multiply dX by the activation's derivative at
+ * the saved input x instead (oracle_act_grad).
  *
  * Precision: every product and sum is taken in IEEE double.  fp16 and bf16
  * inputs are decoded from their bit patterns (IEEE-754 binary16; bfloat16 =
@@ -43,7 +45,11 @@
  * and the per-channel sums of the output that a fused epilogue produces
  * (oracle_channel_sums below).
  */
+#define _USE_MATH_DEFINES
 #include <math.h>
+#ifndef M_PI
+#define M_PI 3.14159265358979323846
+#endif
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -155,12 +161,39 @@ static void pixel_sum(const void *dY, int dtype, const double *Wd, double *acc,
     }
 }
 
-/* ReLU-backward gate: keep where x > 0 (NaN, -0.0 and negatives give +0.0). */
-static void apply_gate(double *acc, const void *x, int dtype, size_t base, int C)
+/*
+ * Derivative of an activation function at x, for the activation-backward
+ * epilogues (the activation fusion of the tvm page's last comments, with
+ * activations other than ReLU):
+ *   act 1, GELU in its erf form:  f(x) = x * Phi(x),  Phi(x) = (1 + erf(x / sqrt 2)) / 2,
+ *                                 f'(x) = Phi(x) + x * phi(x),  phi(x) = exp(-x^2 / 2) / sqrt(2 pi)
+ *   act 2, SiLU:                  f(x) = x * s(x),  s(x) = 1 / (1 + exp(-x)),
+ *                                 f'(x) = s(x) * (1 + x * (1 - s(x)))
+ * (act 0, ReLU, is the select in apply_gate, not a product.)
+ */
+double oracle_act_grad(double x, int act)
+{
+    if (act == 1) {
+        const double Phi = 0.5 * (1.0 + erf(x / sqrt(2.0)));
+        const double phi = exp(-0.5 * x * x) / sqrt(2.0 * M_PI);
+        return Phi + x * phi;
+    }
+    const double sg = 1.0 / (1.0 + exp(-x));
+    return sg * (1.0 + x * (1.0 - sg));
+}
+
+/* Backward of the activation whose input was x: act 0 (ReLU) keeps the value
+ * where x > 0 (NaN, -0.0 and negatives give +0.0: a select); act 1 and 2
+ * multiply it by f'(x) (oracle_act_grad). */
+static void apply_gate(double *acc, const void *x, int dtype, size_t base, int C, int act)
 {
     for (int c = 0; c < C; ++c) {
         double xv = load_one(x, base + c, dtype);
-        if (!(xv > 0.0)) acc[c] = 0.0;
+        if (act == 0) {
+            if (!(xv > 0.0)) acc[c] = 0.0;
+        } else {
+            acc[c] *= oracle_act_grad(xv, act);
+        }
     }
 }
 
@@ -179,9 +212,9 @@ static int check_geometry(int N, int H, int W, int C, int K, int R, int S,
  * `dtype`; dX is written as doubles, NHWC.  Returns 0, or -1 on bad geometry
  * or allocation failure.  OpenMP-parallel over (n, h).
  */
-int oracle_dgrad(const void *dY, const void *Wt, const void *x, int dtype, double *dX,
-                 int N, int H, int W, int C, int K, int R, int S,
-                 int stride, int pad, int dil)
+int oracle_dgrad_act(const void *dY, const void *Wt, const void *x, int act, int dtype, double *dX,
+                     int N, int H, int W, int C, int K, int R, int S,
+                     int stride, int pad, int dil)
 {
     int P, Q;
     if (check_geometry(N, H, W, C, K, R, S, stride, pad, dil, &P, &Q)) return -1;
@@ -201,7 +234,7 @@ int oracle_dgrad(const void *dY, const void *Wt, const void *x, int dtype, doubl
                     for (int w = 0; w < W; ++w) {
                         pixel_sum(dY, dtype, Wd, acc, n, h, w, C, K, R, S, stride, pad, dil, P, Q);
                         size_t base = (((size_t)n * H + h) * W + w) * (size_t)C;
-                        if (x) apply_gate(acc, x, dtype, base, C);
+                        if (x) apply_gate(acc, x, dtype, base, C, act);
                         memcpy(dX + base, acc, (size_t)C * sizeof(double));
                     }
             free(acc);
@@ -216,10 +249,10 @@ int oracle_dgrad(const void *dY, const void *Wt, const void *x, int dtype, doubl
  * npix rows of C doubles.  Same arithmetic as oracle_dgrad, for checking
  * sampled outputs of problems too large to evaluate in full.
  */
-int oracle_dgrad_pixels(const void *dY, const void *Wt, const void *x, int dtype,
-                        const int32_t *pix, int64_t npix, double *out,
-                        int N, int H, int W, int C, int K, int R, int S,
-                        int stride, int pad, int dil)
+int oracle_dgrad_pixels_act(const void *dY, const void *Wt, const void *x, int act, int dtype,
+                            const int32_t *pix, int64_t npix, double *out,
+                            int N, int H, int W, int C, int K, int R, int S,
+                            int stride, int pad, int dil)
 {
     int P, Q;
     if (check_geometry(N, H, W, C, K, R, S, stride, pad, dil, &P, &Q)) return -1;
@@ -241,7 +274,7 @@ int oracle_dgrad_pixels(const void *dY, const void *Wt, const void *x, int dtype
             for (int64_t i = 0; i < npix; ++i) {
                 int n = pix[3 * i], h = pix[3 * i + 1], w = pix[3 * i + 2];
                 pixel_sum(dY, dtype, Wd, acc, n, h, w, C, K, R, S, stride, pad, dil, P, Q);
-                if (x) apply_gate(acc, x, dtype, (((size_t)n * H + h) * W + w) * (size_t)C, C);
+                if (x) apply_gate(acc, x, dtype, (((size_t)n * H + h) * W + w) * (size_t)C, C, act);
                 memcpy(out + (size_t)i * C, acc, (size_t)C * sizeof(double));
             }
             free(acc);
@@ -249,6 +282,22 @@ int oracle_dgrad_pixels(const void *dY, const void *Wt, const void *x, int dtype
     }
     free(Wd);
     return failed ? -1 : 0;
+}
+
+/* The ReLU-backward forms (x may be NULL: no gate). */
+int oracle_dgrad(const void *dY, const void *Wt, const void *x, int dtype, double *dX,
+                 int N, int H, int W, int C, int K, int R, int S,
+                 int stride, int pad, int dil)
+{
+    return oracle_dgrad_act(dY, Wt, x, 0, dtype, dX, N, H, W, C, K, R, S, stride, pad, dil);
+}
+
+int oracle_dgrad_pixels(const void *dY, const void *Wt, const void *x, int dtype,
+                        const int32_t *pix, int64_t npix, double *out,
+                        int N, int H, int W, int C, int K, int R, int S,
+                        int stride, int pad, int dil)
+{
+    return oracle_dgrad_pixels_act(dY, Wt, x, 0, dtype, pix, npix, out, N, H, W, C, K, R, S, stride, pad, dil);
 }
 
 /*

@@ -56,8 +56,9 @@ GOOD = (2, 8, 8, 16, 16, 3, 3, 1, 1, 1, cdg.BF16, 0)
 @pytest.mark.parametrize("host", [True, False])
 @pytest.mark.parametrize("field,value,expect", [
     (0, 0, 1), (1, 0, 1), (3, 0, 1), (5, 0, 1), (7, 0, 1), (8, -1, 1), (9, 0, 1),
-    (10, 2, 1), (11, 32, 1), (11, 5, 1),  # unknown epilogue flag; both ReLU gates at once
+    (10, 2, 1), (11, 128, 1), (11, 5, 1),  # unknown epilogue flag; both ReLU gates at once
     (11, 16, 1), (11, 24, 1), (11, 28, 1),  # sums of out*x without the x gate (none, or the bit mask)
+    (11, 33, 1), (11, 68, 1), (11, 96, 1), (11, 48, 1),  # two activations at once; GELU with sums of out*x
     (3, 12, 2), (4, 20, 2), (7, 5, 2),
 ])
 def test_argument_validation_needs_no_device(host, field, value, expect):

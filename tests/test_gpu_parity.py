@@ -342,3 +342,35 @@ def test_gate_in_every_mode(L, env, reach, gate, monkeypatch):
         info = _bits_gated(L)[3].info()
     for k, v in reach.items():
         assert info[k] == v, (k, info)
+
+
+@pytest.mark.parametrize("act", ["gelu", "silu"])
+@pytest.mark.parametrize("L,env,reach", GATE_CASES, ids=lambda v: v.name if isinstance(v, Layer) else None)
+def test_activation_backward_in_every_mode(L, env, reach, act, monkeypatch):
+    """GELU (erf form) and SiLU backward fused into the epilogue: out = dX *
+    f'(x) with x the activation's saved input (drawn N(0, 2^2), so both signs
+    and the derivative's negative dip occur), against the oracle, in every
+    operand, tile and issue mode."""
+    import torch
+    import implicit_gemm_dgrad_gb300 as cdg
+    from gpu_util import GuardedOutput, to_dev
+    if env:
+        key, val = env.split("=")
+        monkeypatch.setenv(key, val)
+    dY, W, _ = synth.make_inputs(L.shape(), L.dtype, L.dist, L.workload, L.index)
+    rng = np.random.default_rng(1000 + L.index)
+    x = synth.to_bits((2.0 * rng.standard_normal((L.N, L.H, L.W, L.C))).astype(np.float32), L.dtype)
+    p = cdg.plan(L.N, L.H, L.W, L.C, L.K, L.R, L.S, L.stride, L.pad, L.dil, L.dtype, relu=True, act=act,
+                 out_f32=(L.out == "f32"))
+    for k, v in reach.items():
+        assert p.info()[k] == v, (k, p.info())
+    d_W = to_dev(W, L.dtype)
+    d_Wp = torch.empty(p.packed_weight_bytes // 2, dtype=torch.int16, device="cuda")
+    p.prepack_weights(d_W, d_Wp)
+    odt = "f32" if L.out == "f32" else L.dtype
+    out = GuardedOutput(L.N * L.H * L.W * L.C, 4 if odt == "f32" else 2)
+    p.dgrad(to_dev(dY, L.dtype), d_Wp, out.ptr, to_dev(x, L.dtype))
+    torch.cuda.synchronize()
+    assert out.guards_intact() and p.device_status() == 0
+    ref = oracle.dgrad(dY, W, L.H, L.W, L.stride, L.pad, L.dil, x=x, dtype=L.dtype, act=act)
+    assert_close(decode_out(out.body().cpu().numpy(), odt).reshape(ref.shape), ref, odt, f"{L.name} {act}")
