@@ -31,13 +31,16 @@ NOALLOC_MAX_WEIGHT_BYTES = 8 << 20
 F16, BF16 = 0, 1
 EPI_RELU_BWD, EPI_OUT_F32, EPI_RELU_BWD_BITS, EPI_SUM, EPI_SUM_X = 1, 2, 4, 8, 16
 EPI_GELU_BWD, EPI_SILU_BWD = 32, 64
+FUSED_WRITE_G = 256
 ACT_FLAGS = {"relu": EPI_RELU_BWD, "gelu": EPI_GELU_BWD, "silu": EPI_SILU_BWD}
 DTYPES = {"f16": F16, "bf16": BF16}
 
 EXPORTS = ("cdg_plan", "cdg_plan_host", "cdg_destroy", "cdg_get_output_dims", "cdg_packed_weight_bytes",
            "cdg_plan_get_info", "cdg_prepack_weights", "cdg_dgrad", "cdg_device_status", "cdg_status_string",
            "cdg_dgrad_noalloc", "cdg_dgrad_noalloc_status", "cdg_autotune", "cdg_plan_set_wait_limit",
-           "cdg_plan_withhold_load_for_test", "cdg_dgrad_sums", "cdg_sums_workspace_bytes", "cdg_pack_relu_mask", "cdg_relu_mask_bytes",
+           "cdg_plan_withhold_load_for_test", "cdg_dgrad_sums", "cdg_sums_workspace_bytes",
+           "cdg_fused_plan", "cdg_fused_plan_host", "cdg_fused_destroy", "cdg_fused_packed_weight_bytes",
+           "cdg_fused_prepack_weights", "cdg_dgrad_fused", "cdg_fused_get_info", "cdg_fused_device_status", "cdg_pack_relu_mask", "cdg_relu_mask_bytes",
            "cdg_wgrad_plan", "cdg_wgrad_plan_host", "cdg_wgrad_destroy", "cdg_wgrad_workspace_bytes",
            "cdg_wgrad_get_info", "cdg_wgrad", "cdg_wgrad_device_status")
 
@@ -107,6 +110,22 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.cdg_dgrad_sums.restype = i
     lib.cdg_sums_workspace_bytes.argtypes = [hp]
     lib.cdg_sums_workspace_bytes.restype = ctypes.c_size_t
+    lib.cdg_fused_plan.argtypes = [i] * 12 + [ctypes.POINTER(hp)]
+    lib.cdg_fused_plan.restype = i
+    lib.cdg_fused_plan_host.argtypes = [i] * 13 + [ctypes.POINTER(hp)]
+    lib.cdg_fused_plan_host.restype = i
+    lib.cdg_fused_destroy.argtypes = [hp]
+    lib.cdg_fused_destroy.restype = None
+    lib.cdg_fused_packed_weight_bytes.argtypes = [hp, ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(ctypes.c_size_t)]
+    lib.cdg_fused_packed_weight_bytes.restype = i
+    lib.cdg_fused_prepack_weights.argtypes = [hp, vp, vp, vp, vp, vp]
+    lib.cdg_fused_prepack_weights.restype = i
+    lib.cdg_dgrad_fused.argtypes = [hp, vp, vp, vp, vp, vp, vp, vp]
+    lib.cdg_dgrad_fused.restype = i
+    lib.cdg_fused_get_info.argtypes = [hp, ctypes.POINTER(PlanInfo)]
+    lib.cdg_fused_get_info.restype = i
+    lib.cdg_fused_device_status.argtypes = [hp, vp]
+    lib.cdg_fused_device_status.restype = i
     lib.cdg_plan_set_wait_limit.argtypes = [hp, ctypes.c_ulonglong]
     lib.cdg_plan_set_wait_limit.restype = i
     lib.cdg_plan_withhold_load_for_test.argtypes = [hp, i]
@@ -343,6 +362,83 @@ class Plan:
         rc = self.lib.cdg_plan_withhold_load_for_test(self.handle, int(stage))
         if rc != OK:
             raise CdgError(rc, "cdg_plan_withhold_load_for_test")
+
+
+class FusedPlan:
+    """Back-to-back dgrads in one kernel (a ``cdg_fused_t``):
+    g = act_bwd(dgrad(dY2, W2), x2) for a stride-1 R2 x S2 layer with C2 = 64
+    channels, then dX1 = dgrad_1x1(g, W1) with C1 channels; g stays on chip
+    and is written only with write_g=True."""
+
+    def __init__(self, N, H, W, C1, C2, K2, R2, S2, pad2=1, dil2=1, dtype="bf16", act: str | None = "relu",
+                 write_g=False, host_sms: int | None = None):
+        self.lib = load_library()
+        self.shape = dict(N=N, H=H, W=W, C1=C1, C2=C2, K2=K2, R2=R2, S2=S2, pad2=pad2, dil2=dil2)
+        self.act = act
+        self.write_g = bool(write_g)
+        flags = (ACT_FLAGS[act] if act else 0) | (FUSED_WRITE_G if write_g else 0)
+        dt = DTYPES[dtype] if isinstance(dtype, str) else int(dtype)
+        h = ctypes.c_void_p()
+        args = (N, H, W, C1, C2, K2, R2, S2, pad2, dil2, dt, flags)
+        if host_sms is None:
+            rc = self.lib.cdg_fused_plan(*args, ctypes.byref(h))
+        else:
+            rc = self.lib.cdg_fused_plan_host(*args, host_sms, ctypes.byref(h))
+        if rc != OK:
+            raise CdgError(rc, "cdg_fused_plan")
+        self.handle = h
+
+    def close(self):
+        if getattr(self, "handle", None) is not None and self.handle.value:
+            self.lib.cdg_fused_destroy(self.handle)
+        self.handle = None
+
+    def __del__(self):
+        self.close()
+
+    @property
+    def packed_weight_bytes(self) -> tuple[int, int]:
+        b2, b1 = ctypes.c_size_t(), ctypes.c_size_t()
+        rc = self.lib.cdg_fused_packed_weight_bytes(self.handle, ctypes.byref(b2), ctypes.byref(b1))
+        if rc != OK:
+            raise CdgError(rc, "cdg_fused_packed_weight_bytes")
+        return int(b2.value), int(b1.value)
+
+    def info(self) -> dict:
+        inf = PlanInfo()
+        rc = self.lib.cdg_fused_get_info(self.handle, ctypes.byref(inf))
+        if rc != OK:
+            raise CdgError(rc, "cdg_fused_get_info")
+        return inf.as_dict()
+
+    def prepack_weights(self, W2, W1, W2p, W1p, stream=None) -> None:
+        b2, b1 = self.packed_weight_bytes
+        for t, n, what in ((W2, b2, "W2"), (W1, b1, "W1"), (W2p, b2, "W2p"), (W1p, b1, "W1p")):
+            _check_buffer(t, n, what)
+        rc = self.lib.cdg_fused_prepack_weights(self.handle, _addr(W2), _addr(W1), _addr(W2p), _addr(W1p),
+                                                _stream(stream))
+        if rc != OK:
+            raise CdgError(rc, "cdg_fused_prepack_weights")
+
+    def dgrad(self, dY2, W2p, x2, W1p, dX1, g=None, stream=None) -> None:
+        d = self.shape
+        P = d["H"] + 2 * d["pad2"] - d["dil2"] * (d["R2"] - 1)
+        Q = d["W"] + 2 * d["pad2"] - d["dil2"] * (d["S2"] - 1)
+        px = d["N"] * d["H"] * d["W"]
+        b2, b1 = self.packed_weight_bytes
+        _check_buffer(dY2, 2 * d["N"] * P * Q * d["K2"], "dY2")
+        _check_buffer(W2p, b2, "W2p")
+        _check_buffer(W1p, b1, "W1p")
+        _check_buffer(x2, 2 * px * d["C2"], "x2")
+        _check_buffer(dX1, 2 * px * d["C1"], "dX1")
+        _check_buffer(g, 2 * px * d["C2"], "g")
+        rc = self.lib.cdg_dgrad_fused(self.handle, _addr(dY2), _addr(W2p), _addr(x2), _addr(W1p), _addr(g),
+                                      _addr(dX1), _stream(stream))
+        if rc != OK:
+            raise CdgError(rc, "cdg_dgrad_fused")
+
+    def device_status(self, stream=None) -> int:
+        return int(self.lib.cdg_fused_device_status(self.handle, _stream(stream)))
 
 
 class WgradInfo(ctypes.Structure):

@@ -1241,3 +1241,232 @@ extern "C" int cdg_dgrad_noalloc_status(cdg_stream_t stream)
     }
     return v;
 }
+
+// ------------------------------------------------------------------ back-to-back fusion
+struct cdg_fused_st {
+    cdg_plan_st *g;  // GEMM 1: the first dgrad (stride 1, halo operand mode, resident weights)
+    int C1, BN2;     // dX1 channels and GEMM 2's N tile
+    bool write_g;
+    size_t smem;
+    const void *cached_W1p;
+    void *cached_dX1;
+};
+
+namespace {
+
+int fused_make(int N, int H, int W, int C1, int C2, int K2, int R2, int S2, int pad2, int dil2, int dtype, int flags,
+               int num_sms, bool host_only, cdg_fused_t *out)
+{
+    if (!out) return CDG_ERR_INVALID_ARG;
+    *out = nullptr;
+    const int gates = CDG_EPI_RELU_BWD | CDG_EPI_GELU_BWD | CDG_EPI_SILU_BWD;
+    if (flags & ~(gates | CDG_FUSED_WRITE_G)) return CDG_ERR_INVALID_ARG;
+    if (C1 < 1) return CDG_ERR_INVALID_ARG;
+    if (C2 != 64 || C1 % 8 || C1 > 256) return CDG_ERR_UNSUPPORTED;
+    PlanOpts opt = opts_from_env();
+    opt.halo = 1;
+    opt.bn = 0;
+    cdg_handle_t g = nullptr;
+    int rc = make_plan(N, H, W, C2, K2, R2, S2, 1, pad2, dil2, dtype, flags & gates, num_sms, host_only, opt, &g);
+    if (rc != CDG_OK) return rc;
+    CdgParams &p = g->prm;
+    // the first dgrad must be one phase in halo mode with its whole filter resident
+    if (!p.halo || !p.b_res || p.tiles_n != 1 || p.BN != 64 || p.nphases != 1 || p.phase[0].tap_count < 1) {
+        cdg_destroy(g);
+        return CDG_ERR_UNSUPPORTED;
+    }
+    const bool gated = (flags & gates) != 0;
+    const int BN2 = ((C1 + 15) / 16) * 16;
+    const int w1_bytes = BN2 * 128;
+    const int fixed = 1024 + static_cast<int>(p.b_res_bytes) + w1_bytes + (gated ? CDG_FUSED_X2_BYTES : 0) +
+                      CDG_SMEM_STAGING + CDG_SMEM_TAIL;
+    const int as = std::min(3, (kMaxSmem - fixed) / static_cast<int>(p.a_stage_bytes));
+    if (as < 2) {
+        cdg_destroy(g);
+        return CDG_ERR_UNSUPPORTED;
+    }
+    p.a_stages = as;
+    p.stages = as;
+    p.C1 = C1;
+    p.BN2 = BN2;
+    p.w1_bytes = static_cast<uint32_t>(w1_bytes);
+    p.write_g = (flags & CDG_FUSED_WRITE_G) ? 1 : 0;
+    const uint32_t ab = dtype == CDG_BF16 ? 1u : 0u;
+    p.idesc2 = (1u << 4) | (ab << 7) | (ab << 10) | (static_cast<uint32_t>(BN2 >> 3) << 17) | (static_cast<uint32_t>(CDG_BM >> 4) << 24);
+    cdg_fused_st *f = new (std::nothrow) cdg_fused_st();
+    if (!f) {
+        cdg_destroy(g);
+        return CDG_ERR_INVALID_ARG;
+    }
+    f->g = g;
+    f->C1 = C1;
+    f->BN2 = BN2;
+    f->write_g = p.write_g != 0;
+    f->smem = static_cast<size_t>(fixed + as * static_cast<int>(p.a_stage_bytes));
+    if (!host_only && cdg_prepare_fused(g->in_type, gated) != cudaSuccess) {
+        cdg_destroy(g);
+        delete f;
+        return CDG_ERR_CUDA;
+    }
+    *out = f;
+    return CDG_OK;
+}
+
+int encode_fused_maps(cdg_fused_st *f, const void *W1p, void *dX1)
+{
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return CDG_ERR_CUDA;
+    const cdg_plan_st *g = f->g;
+    CdgParams &p = f->g->prm;
+    const CUtensorMapDataType dt = tmap_type(g->dtype);
+    const cuuint32_t ones[4] = {1, 1, 1, 1};
+    const cuuint64_t C1 = f->C1, C2 = g->C;
+    const cuuint64_t wdims[3] = {C2, C1, 1};
+    const cuuint64_t wstrides[2] = {C2 * 2, C1 * C2 * 2};
+    const cuuint32_t wbox[3] = {CDG_BK, static_cast<cuuint32_t>(f->BN2), 1};
+    if (enc(&p.tmW1, dt, 3, const_cast<void *>(W1p), wdims, wstrides, wbox, ones, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
+        CUDA_SUCCESS)
+        return CDG_ERR_CUDA;
+    const cuuint64_t Wd = g->W, Hd = g->H;
+    const cuuint64_t xdims[4] = {C1, Wd, Hd, static_cast<cuuint64_t>(g->N)};
+    const cuuint64_t xstrides[3] = {C1 * 2, Wd * C1 * 2, Hd * Wd * C1 * 2};
+    const cuuint32_t xbox[4] = {64, static_cast<cuuint32_t>(p.halo_wt), static_cast<cuuint32_t>(p.halo_bh), 1};
+    if (enc(&p.tmX1, dt, 4, dX1, xdims, xstrides, xbox, ones, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return CDG_ERR_CUDA;
+    f->cached_W1p = W1p;
+    f->cached_dX1 = dX1;
+    return CDG_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int cdg_fused_plan(int N, int H, int W, int C1, int C2, int K2, int R2, int S2, int pad2, int dil2, int dtype,
+                   int flags, cdg_fused_t *out)
+{
+    if (out) *out = nullptr;
+    cdg_fused_t probe = nullptr;
+    int rc = fused_make(N, H, W, C1, C2, K2, R2, S2, pad2, dil2, dtype, flags, 1, true, &probe);
+    if (rc != CDG_OK) return rc;
+    cdg_fused_destroy(probe);
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return CDG_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+        return CDG_ERR_CUDA;
+    return fused_make(N, H, W, C1, C2, K2, R2, S2, pad2, dil2, dtype, flags, sms, false, out);
+}
+
+int cdg_fused_plan_host(int N, int H, int W, int C1, int C2, int K2, int R2, int S2, int pad2, int dil2, int dtype,
+                        int flags, int num_sms, cdg_fused_t *out)
+{
+    if (num_sms < 1) {
+        if (out) *out = nullptr;
+        return CDG_ERR_INVALID_ARG;
+    }
+    return fused_make(N, H, W, C1, C2, K2, R2, S2, pad2, dil2, dtype, flags, num_sms, true, out);
+}
+
+void cdg_fused_destroy(cdg_fused_t f)
+{
+    if (!f) return;
+    cdg_destroy(f->g);
+    delete f;
+}
+
+int cdg_fused_packed_weight_bytes(cdg_fused_t f, size_t *w2_bytes, size_t *w1_bytes)
+{
+    if (!f || !w2_bytes || !w1_bytes) return CDG_ERR_INVALID_ARG;
+    *w2_bytes = cdg_packed_weight_bytes(f->g);
+    *w1_bytes = static_cast<size_t>(f->C1) * f->g->C * 2;
+    return CDG_OK;
+}
+
+int cdg_fused_prepack_weights(cdg_fused_t f, const void *W2_krsc, const void *W1_krsc, void *W2p, void *W1p,
+                              cdg_stream_t stream)
+{
+    if (!f || !W2_krsc || !W1_krsc || !W2p || !W1p) return CDG_ERR_INVALID_ARG;
+    if (f->g->host_only) return CDG_ERR_NO_DEVICE;
+    if (!aligned16(W1_krsc) || !aligned16(W1p)) return CDG_ERR_ALIGNMENT;
+    size_t b2 = 0, b1 = 0;
+    cdg_fused_packed_weight_bytes(f, &b2, &b1);
+    if (overlaps(W1_krsc, b1, W1p, b1) || overlaps(W1p, b1, W2p, b2) || overlaps(W1p, b1, W2_krsc, b2) ||
+        overlaps(W2p, b2, W1_krsc, b1))
+        return CDG_ERR_ALIAS;
+    const int rc = cdg_prepack_weights(f->g, W2_krsc, W2p, stream);
+    if (rc != CDG_OK) return rc;
+    // the 1x1 layer: W1 [C2][1][1][C1] -> [1][C1][C2], its dgrad's B operand
+    if (cdg_launch_prepack(W1_krsc, W1p, f->g->C, 1, f->C1, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return CDG_ERR_CUDA;
+    return CDG_OK;
+}
+
+int cdg_dgrad_fused(cdg_fused_t f, const void *dY2, const void *W2p, const void *x2, const void *W1p, void *g,
+                    void *dX1, cdg_stream_t stream)
+{
+    if (!f || !dY2 || !W2p || !W1p || !dX1) return CDG_ERR_INVALID_ARG;
+    cdg_plan_st *h = f->g;
+    if (h->mask != (x2 != nullptr) || f->write_g != (g != nullptr)) return CDG_ERR_INVALID_ARG;
+    if (h->host_only) return CDG_ERR_NO_DEVICE;
+    if (!aligned16(dY2) || !aligned16(W2p) || !aligned16(W1p) || !aligned16(dX1) || (x2 && !aligned16(x2)) ||
+        (g && !aligned16(g)))
+        return CDG_ERR_ALIGNMENT;
+    size_t b2 = 0, b1 = 0;
+    cdg_fused_packed_weight_bytes(f, &b2, &b1);
+    const size_t px = static_cast<size_t>(h->N) * h->H * h->W;
+    const size_t dy_bytes = static_cast<size_t>(h->N) * h->P * h->Q * h->K * 2;
+    const void *ins[4] = {dY2, W2p, x2, W1p};
+    const size_t inb[4] = {dy_bytes, b2, x2 ? px * h->C * 2 : 0, b1};
+    void *outs[2] = {dX1, g};
+    const size_t outb[2] = {px * f->C1 * 2, g ? px * h->C * 2 : 0};
+    for (int i = 0; i < 2; ++i) {
+        if (!outs[i]) continue;
+        for (int j = 0; j < 4; ++j)
+            if (ins[j] && overlaps(outs[i], outb[i], ins[j], inb[j])) return CDG_ERR_ALIAS;
+    }
+    if (g && overlaps(dX1, outb[0], g, outb[1])) return CDG_ERR_ALIAS;
+    if (dY2 != h->cached_dY || W2p != h->cached_Wp) {
+        const int rc = encode_operand_maps(h, dY2, W2p);
+        if (rc != CDG_OK) return rc;
+    }
+    if (g && g != h->cached_dX) {
+        const int rc = encode_store_maps(h, g);
+        if (rc != CDG_OK) return rc;
+    }
+    if (x2 && x2 != h->cached_mask) {
+        const int rc = encode_gate_maps(h, x2);
+        if (rc != CDG_OK) return rc;
+    }
+    if (W1p != f->cached_W1p || dX1 != f->cached_dX1) {
+        const int rc = encode_fused_maps(f, W1p, dX1);
+        if (rc != CDG_OK) return rc;
+    }
+    CdgParams &p = h->prm;
+    p.dX = g;
+    p.mask = x2;
+    p.status = h->d_status;
+    p.red_ws = nullptr;
+    if (cdg_launch_fused(p, h->in_type, h->mask, h->grid, f->smem, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return CDG_ERR_CUDA;
+    return CDG_OK;
+}
+
+int cdg_fused_get_info(cdg_fused_t f, cdg_plan_info_t *info)
+{
+    if (!f || !info) return CDG_ERR_INVALID_ARG;
+    *info = f->g->info;
+    info->stages = f->g->prm.a_stages;
+    info->smem_bytes = static_cast<int>(f->smem);
+    info->tmem_cols = 512;
+    return CDG_OK;
+}
+
+int cdg_fused_device_status(cdg_fused_t f, cdg_stream_t stream)
+{
+    if (!f) return CDG_ERR_INVALID_ARG;
+    return cdg_device_status(f->g, stream);
+}
+
+}  // extern "C"

@@ -68,6 +68,10 @@ struct CdgParams {  // CUtensorMap members carry their own (128-byte) alignment
     CUtensorMap tmB;  // packed weights: 3-D {K, C, R*S}
     CUtensorMap tmD[CDG_MAX_PHASES];  // dX stores, one map per phase (index = phase slot)
     CUtensorMap tmG[CDG_MAX_PHASES];  // gate loads (saved activation or packed mask) in the stores' geometry
+    // back-to-back fusion (cdg_dgrad_fused): this stride-1 dgrad (GEMM 1) feeds,
+    // gated, a 1x1 dgrad (GEMM 2) whose A operand never leaves the CTA
+    CUtensorMap tmW1;     // packed 1x1 weights [1][C1][C2]: 3-D {C2, C1, 1}, box {64, BN2, 1}
+    CUtensorMap tmX1;     // dX1 stores: 4-D {C1, W, H, N}, the halo tile's store box, 64 channels
     void *dX;
     const void *mask;
     int *status;
@@ -105,6 +109,10 @@ struct CdgParams {  // CUtensorMap members carry their own (128-byte) alignment
     float *red_ws;        // per-channel sums: this launch's [grid][nsum][C] fp32 partials (one row per CTA)
     int nsum;             // per-channel output sums the epilogue accumulates: 0, 1 (sum of dX) or
                           // 2 (also the sum of dX * x where the gate passes)
+    int write_g;          // fused: also store the gated intermediate g (through tmD[0])
+    int C1, BN2;          // fused: dX1 channels; GEMM-2 N tile (C1 rounded up to 16)
+    uint32_t idesc2;      // fused: tcgen05 instruction descriptor of GEMM 2 (M = 128, N = BN2)
+    uint32_t w1_bytes;    // fused: bytes of the resident 1x1 weights (BN2 rows x 128 B)
     unsigned long long wait_limit_ns;  // a pipeline wait gives up (status CDG_ERR_TIMEOUT) after this long
     int withhold_stage;   // test only: >= 0 makes every per-tap/row loader skip the load (and its
                           // transaction count) of its stage with this sequence number, so the MMA
@@ -124,4 +132,9 @@ cudaError_t cdg_launch_dgrad(const CdgParams &p, int out_type, int in_type, bool
 cudaError_t cdg_prepare_dgrad(int out_type, int in_type, bool mask, size_t smem);
 cudaError_t cdg_launch_prepack(const void *W, void *Wp, int K, int T, int C, cudaStream_t stream);
 cudaError_t cdg_launch_channel_sums(const float *ws, int rows, int nsum, int C, float *out, cudaStream_t stream);
+cudaError_t cdg_prepare_fused(int in_type, bool gate);
+cudaError_t cdg_launch_fused(const CdgParams &p, int in_type, bool gate, int grid, size_t smem, cudaStream_t stream);
+// Shared memory of the fused kernel beyond the halo ring, W2 and W1: the gate
+// tile (16 KB, gated plans only), two 16 KB staging buffers, the tail.
+#define CDG_FUSED_X2_BYTES (128 * 128)
 int cdg_max_active_pairs(int out_type, int in_type, bool mask, size_t smem);

@@ -1163,6 +1163,365 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_cons
     }
 }
 
+// ------------------------------------------------------------------ back-to-back fusion
+// Persistent fusion of two dgrads (the persistent kernel fusion of the Bolt
+// reading notes, with threadblock residence): GEMM 1 is a stride-1 dgrad in
+// the halo operand mode with resident weights (a 3x3 layer, C2 = 64 output
+// channels: the whole channel count in one N tile), GEMM 2 the 1x1 dgrad of
+// GEMM 1's gated output g, g = act_bwd(dgrad(dY2, W2), x2), into dX1 with
+// C1 <= 256 channels.  A tile of g never leaves the CTA: the epilogue reads
+// GEMM 1's accumulator, applies the gate, rounds to the input type and writes
+// the tile into tensor memory, where it is GEMM 2's A operand (tcgen05.mma
+// reads A from TMEM); W1 stays resident in shared memory.  Only dX1 (and, if
+// asked, g) goes to HBM.
+//
+// Tensor memory (512 columns): GEMM-1 accumulators at columns 0 and 64, the
+// two g tiles (64 bf16 = 32 columns each) at 128 and 160, the GEMM-2
+// accumulator at 256.  Items alternate between the two GEMM-1 accumulators
+// and the two g tiles.  The MMA warp issues GEMM 1 of item i before GEMM 2 of
+// item i - 1, so the epilogue's gate of item i - 1 overlaps GEMM 1 of item i.
+constexpr uint32_t kFusedAcc1 = 64;   // columns of one GEMM-1 accumulator
+constexpr uint32_t kFusedA2 = 128;    // first g tile
+constexpr uint32_t kFusedAcc2 = 256;  // GEMM-2 accumulator
+
+struct FusedBars {
+    uint32_t acc1_full0, acc1_empty0;  // [2] each
+    uint32_t a2_full0, a2_empty0;      // [2] each: g tile written (4 epilogue warps) / consumed (MMA commit)
+    uint32_t acc2_full, acc2_empty;
+    uint32_t w1_full, gate_full, drain;
+};
+
+__device__ __forceinline__ void run_mma_fused(const CdgParams &p, const Ring &R, const FusedBars &B,
+                                              const CdgPhase *tab, const CdgTap *taps, Ctl ctl, uint32_t tmem_base,
+                                              bool leader, Sched S, uint32_t w1_smem)
+{
+    const int KB = p.KB, as = p.a_stages;
+    const uint32_t idesc = p.idesc, idesc2 = p.idesc2;
+    const uint64_t adesc0 = sdesc_k128_sw128(R.a0);
+    const uint64_t bdesc0 = sdesc_k128_sw128(R.b0);
+    const uint64_t w1desc = sdesc_k128_sw128(w1_smem);
+    const uint32_t astep = R.stage_bytes >> 4;  // descriptor units per halo stage
+    const uint32_t bunit = R.b_bytes >> 4;      // descriptor units per weight tile
+    int a_stage = 0;
+    uint32_t a_par = 0, n = 0;
+    // both weight sets are resident: GEMM-1 weights (loader 1), GEMM-2 weights (warp 3)
+    bool ok = wait_bar(R.full0 + 8u * as, 0, ctl) && wait_bar(B.w1_full, 0, ctl);
+    // GEMM 2 of item j: dX1 tile (acc2) = g tile j (TMEM) x W1^T, K = 64 channels of g
+    auto gemm2 = [&](uint32_t j) -> bool {
+        if (!wait_bar(B.a2_full0 + 8u * (j & 1u), (j >> 1) & 1u, ctl)) return false;
+        if (!wait_bar(B.acc2_empty, (j & 1u) ^ 1u, ctl)) return false;
+        tc_fence_after();
+        if (leader) {
+            const uint32_t a = tmem_base + kFusedA2 + 32u * (j & 1u);
+#pragma unroll
+            for (int k = 0; k < CDG_BK / 16; ++k)  // 16 values = 8 TMEM columns of A, 32 B of B
+                umma_f16_ts(tmem_base + kFusedAcc2, a + 8u * k, w1desc + 2u * k, idesc2, k != 0);
+            umma_commit(B.acc2_full);
+            umma_commit(B.a2_empty0 + 8u * (j & 1u));
+        }
+        __syncwarp();
+        return true;
+    };
+    for (ItemWalk w(tab, p.nphases, S.start, S.step, p.interleave, p.il_items, p.il_round); ok && w.valid(); w.next()) {
+        const CdgPhase &ph = tab[w.phase];
+        const int ntap = ph.tap_count;
+        const uint32_t acc = n & 1u;
+        if (!wait_bar(B.acc1_empty0 + 8u * acc, ((n >> 1) & 1u) ^ 1u, ctl)) {
+            ok = false;
+            break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * kFusedAcc1;
+        for (int kb = 0; ok && kb < KB; ++kb) {
+            if (!wait_bar(R.full0 + 8u * a_stage, a_par, ctl)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint64_t abase = adesc0 + static_cast<uint64_t>(a_stage * astep);
+            const CdgTap *ptap = taps + ph.tap_begin;
+            const int tbase = ph.tap_begin * KB + kb;
+            int hoff = ptap[0].hoff;
+            for (int tt = 0; tt < ntap; ++tt) {
+                if (leader) {
+                    const uint64_t adesc = abase + 8u * static_cast<uint32_t>(hoff);
+                    const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(static_cast<uint32_t>(tbase + tt * KB) * bunit);
+#pragma unroll
+                    for (int k = 0; k < CDG_BK / 16; ++k)
+                        umma_f16(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, (kb | tt | k) != 0);
+                }
+                __syncwarp();
+                if (tt + 1 < ntap) hoff = ptap[tt + 1].hoff;
+            }
+            if (leader) umma_commit(R.empty0 + 8u * a_stage);
+            __syncwarp();
+            if (++a_stage == as) {
+                a_stage = 0;
+                a_par ^= 1u;
+            }
+        }
+        if (!ok) break;
+        if (leader) umma_commit(B.acc1_full0 + 8u * acc);
+        __syncwarp();
+        if (n >= 1 && !gemm2(n - 1)) {
+            ok = false;
+            break;
+        }
+        ++n;
+    }
+    if (ok && n >= 1) gemm2(n - 1);
+    if (leader) umma_commit(B.drain);
+    __syncwarp();
+    volatile uint32_t no_abort = 0;
+    wait_bar(B.drain, 0, Ctl{&no_abort, ctl.status, ctl.limit});
+}
+
+template <int IN_T, bool GATE>
+__device__ __forceinline__ void run_epilogue_fused(const CdgParams &p, const Ring &R, const FusedBars &B,
+                                                   const CdgPhase *tab, Ctl ctl, uint32_t tmem_base, Sched S,
+                                                   uint32_t x2_smem)
+{
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const bool elected = elect_one_sync();
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const int ew = warp - CDG_EPI_WARP0;
+    // tile row a*halo_wb + b is output (a, b) of the halo tile; the store box
+    // (and the gate tile) holds the valid rows compacted, a*halo_wt + b
+    const int ha = row / p.halo_wb, hb = row - (row / p.halo_wb) * p.halo_wb;
+    const int srow = (hb < p.halo_wt && ha < p.halo_bh) ? ha * p.halo_wt + hb : -1;
+    const uint32_t srow_off = static_cast<uint32_t>(max(srow, 0)) * 128u;
+    const uint32_t sw = static_cast<uint32_t>(srow & 7);
+    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    const uint64_t mapX1 = reinterpret_cast<uint64_t>(&p.tmX1);
+    const uint64_t mapG = reinterpret_cast<uint64_t>(&p.tmD[0]);
+    const uint64_t mapGate = reinterpret_cast<uint64_t>(&p.tmG[0]);
+    volatile uint32_t gate_no_abort = 0;
+    const Ctl gate_ctl{&gate_no_abort, ctl.status, ctl.limit};
+    // the gate tile of the next item is loaded into the one gate buffer as
+    // soon as every thread has read the current one (issued by warp 0)
+    ItemWalk nx(tab, p.nphases, S.start, S.step, p.interleave, p.il_items, p.il_round);
+    uint32_t g_issued = 0, g_used = 0;
+    auto gate_issue = [&]() {
+        if (!GATE || !nx.valid()) return;
+        ++g_issued;
+        if (ew == 0 && elected) {
+            int j0, i0, n0;
+            box_origin(tab[nx.phase], S.m_tile(nx.local, 1), p.halo_wt, p.halo_bh, 1, j0, i0, n0);
+            mbar_arrive_expect_tx(B.gate_full, p.gate_tx);
+            tma_load_4d(x2_smem, mapGate, B.gate_full, 0, j0, i0, n0);
+        }
+        nx.next();
+    };
+    gate_issue();
+    uint32_t n = 0, chunk = 0;
+    // one 16 KB output chunk through staging buffer chunk % 2 (the same
+    // hand-over as the plain epilogue); `fill` writes this thread's row
+    auto store_chunk = [&](uint64_t map, int c, int j0, int i0, int n0, const uint32_t (&pk)[32]) {
+        const uint32_t k = chunk++;
+        const uint32_t buf = R.out0 + (k & 1u) * (128u * 128u);
+        if (k >= 2 && elected && static_cast<uint32_t>(ew) == ((k - 2) & 3u)) bulk_wait_group_read<0>();
+        named_bar_sync(1, 128);
+        if (srow >= 0)
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                st_shared_v4(buf + srow_off + ((static_cast<uint32_t>(q) ^ sw) << 4), pk[4 * q], pk[4 * q + 1],
+                             pk[4 * q + 2], pk[4 * q + 3]);
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (elected && static_cast<uint32_t>(ew) == (k & 3u)) {
+            tma_store_4d(map, buf, c, j0, i0, n0);
+            bulk_commit_group();
+        }
+    };
+    for (ItemWalk w(tab, p.nphases, S.start, S.step, p.interleave, p.il_items, p.il_round); w.valid(); w.next(), ++n) {
+        const CdgPhase &ph = tab[w.phase];
+        int j0, i0, n0;
+        box_origin(ph, S.m_tile(w.local, 1), p.halo_wt, p.halo_bh, 1, j0, i0, n0);
+        // ---- g = gate(GEMM 1): accumulator -> registers -> tensor memory (GEMM 2's A)
+        bool okw = wait_bar(B.acc1_full0 + 8u * (n & 1u), (n >> 1) & 1u, ctl);
+        okw = okw && wait_bar(B.a2_empty0 + 8u * (n & 1u), ((n >> 1) & 1u) ^ 1u, ctl);
+        if (named_bar_red_or(1, 128, !okw)) break;
+        tc_fence_after();
+        uint32_t xr[32];
+        if (GATE) {
+            wait_bar(B.gate_full, g_used & 1u, gate_ctl);
+            ++g_used;
+            if (srow >= 0) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    ld_shared_v4(x2_smem + srow_off + ((static_cast<uint32_t>(q) ^ sw) << 4),
+                                 *reinterpret_cast<uint32_t(*)[4]>(&xr[4 * q]));
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) xr[e] = 0u;
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(1, 128);  // every row read: the gate buffer takes the next tile
+            gate_issue();
+        }
+        uint32_t r[64];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            tmem_ld_32x32b_x16(tmem_base + (n & 1u) * kFusedAcc1 + lane_base + 16u * q,
+                               *reinterpret_cast<uint32_t(*)[16]>(&r[16 * q]));
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (elected) mbar_arrive(B.acc1_empty0 + 8u * (n & 1u));
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+            float v[2] = {__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1])};
+            if (GATE) {
+                float xp[2];
+                gate_x<IN_T, 2>(v, &xr[e], xp, p.act);
+            }
+            pk[e] = pack2(v[0], v[1], IN_T);
+        }
+        tmem_st_32x32b_x32(tmem_base + kFusedA2 + 32u * (n & 1u) + lane_base, pk);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (elected) mbar_arrive(B.a2_full0 + 8u * (n & 1u));
+        if (p.write_g) store_chunk(mapG, 0, j0, i0, n0, pk);
+        // ---- dX1 tile: GEMM 2's accumulator, in 64-channel chunks
+        okw = wait_bar(B.acc2_full, n & 1u, ctl);
+        if (named_bar_red_or(1, 128, !okw)) break;
+        tc_fence_after();
+        for (int cc = 0; cc < p.BN2; cc += 64) {
+            uint32_t o[64];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                tmem_ld_32x32b_x16(tmem_base + kFusedAcc2 + lane_base + static_cast<uint32_t>(cc) + 16u * q,
+                                   *reinterpret_cast<uint32_t(*)[16]>(&o[16 * q]));
+            tmem_ld_wait();
+            if (cc + 64 >= p.BN2) {  // last read of the accumulator: GEMM 2 of the next item may start
+                tc_fence_before();
+                __syncwarp();
+                if (elected) mbar_arrive(B.acc2_empty);
+            }
+#pragma unroll
+            for (int e = 0; e < 32; ++e) pk[e] = pack2(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1]), IN_T);
+            store_chunk(mapX1, cc, j0, i0, n0, pk);
+        }
+    }
+    if (GATE && ew == 0 && elected && g_used != g_issued) {
+        // left early: let the gate tile still in flight land before the CTA exits
+        volatile uint32_t no_abort = 0;
+        const Ctl drain_ctl{&no_abort, ctl.status, ctl.limit};
+        for (uint32_t k = g_used; k < g_issued; ++k) wait_bar(B.gate_full, k & 1u, drain_ctl);
+    }
+    if (elected) bulk_wait_group_all();
+}
+
+// Shared memory: halo ring | W2 (resident) | W1 (resident) | gate tile | 2 x
+// 16 KB staging | mbarriers, flags | phase and tap tables.
+template <int IN_T, bool GATE>
+__global__ void __launch_bounds__(CDG_THREADS, 1) fused_kernel(const __grid_constant__ CdgParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const int stages = p.a_stages + 1;  // halo stages and the resident-weights barrier
+    Ring R;
+    R.stages = stages;
+    R.a0 = base;
+    R.stage_bytes = p.a_stage_bytes;
+    R.b0 = base + p.a_stages * R.stage_bytes;
+    R.b_bytes = p.BN * 128;
+    const uint32_t w1_smem = R.b0 + p.b_res_bytes;
+    const uint32_t x2_smem = w1_smem + p.w1_bytes;
+    R.out0 = x2_smem + (GATE ? CDG_FUSED_X2_BYTES : 0u);
+    const uint32_t bars = R.out0 + CDG_SMEM_STAGING;
+    R.full0 = bars;
+    R.empty0 = bars + 8u * stages;
+    FusedBars B;
+    B.acc1_full0 = bars + 16u * stages;
+    B.acc1_empty0 = B.acc1_full0 + 16u;
+    B.a2_full0 = B.acc1_full0 + 32u;
+    B.a2_empty0 = B.acc1_full0 + 48u;
+    B.acc2_full = B.acc1_full0 + 64u;
+    B.acc2_empty = B.acc1_full0 + 72u;
+    B.w1_full = B.acc1_full0 + 80u;
+    B.gate_full = B.acc1_full0 + 88u;
+    B.drain = B.acc1_full0 + 96u;
+    uint8_t *const tail = smem_raw + (bars - raw);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tail + 16 * stages + 104);
+    volatile uint32_t *abort_flag = tmem_slot + 1;
+    volatile uint32_t *slot_parity = tmem_slot + 2;  // [stages]
+    CdgPhase *tab = reinterpret_cast<CdgPhase *>(tail + CDG_SMEM_TABLES);
+    CdgTap *taps = reinterpret_cast<CdgTap *>(tab + CDG_MAX_PHASES);
+    static_assert(16 * 4 + 104 + 8 + 4 * 4 <= CDG_SMEM_TABLES, "fused mbarrier area overflows");
+    const int warp = threadIdx.x / 32;
+    Sched S;
+    S.start = blockIdx.x;
+    S.step = gridDim.x;
+    S.pair = 0;
+    S.rank = 0;
+    grid_dep_launch_dependents();
+    for (int i = threadIdx.x; i < p.nphases; i += blockDim.x) tab[i] = p.phase[i];
+    for (int i = threadIdx.x; i < p.ntaps; i += blockDim.x) taps[i] = p.tap[i];
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(R.full0 + 8u * s, 1);
+            mbar_init(R.empty0 + 8u * s, 1);
+        }
+        for (int j = 0; j < 2; ++j) {
+            mbar_init(B.acc1_full0 + 8u * j, 1);
+            mbar_init(B.acc1_empty0 + 8u * j, 4);  // one arrival per epilogue warp
+            mbar_init(B.a2_full0 + 8u * j, 4);
+            mbar_init(B.a2_empty0 + 8u * j, 1);
+        }
+        mbar_init(B.acc2_full, 1);
+        mbar_init(B.acc2_empty, 4);
+        mbar_init(B.w1_full, 1);
+        mbar_init(B.gate_full, 1);
+        mbar_init(B.drain, 1);
+        *abort_flag = 0u;
+        for (int s = 0; s < stages; ++s) slot_parity[s] = 0u;
+        fence_mbar_init();
+    }
+    grid_dep_wait();
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const Ctl ctl{abort_flag, p.status, p.wait_limit_ns};
+    if (warp == 1) {
+        run_mma_fused(p, R, B, tab, taps, ctl, tmem_base, elect_one_sync(), S, w1_smem);
+    } else if (warp >= CDG_EPI_WARP0) {
+        run_epilogue_fused<IN_T, GATE>(p, R, B, tab, ctl, tmem_base, S, x2_smem);
+    } else if (warp == 3) {
+        // the 1x1 weights, once per CTA: BN2 rows of 64 channels (128 B) of g
+        if (elect_one_sync()) {
+            const uint64_t mapW1 = reinterpret_cast<uint64_t>(&p.tmW1);
+            mbar_arrive_expect_tx(B.w1_full, p.w1_bytes);
+            tma_load_3d(w1_smem, mapW1, B.w1_full, 0, 0, 0);
+        }
+        __syncwarp();
+    } else {
+        run_loader_halo(p, R, tab, taps, ctl, warp == 0 ? 0 : 1, elect_one_sync(), slot_parity, S);
+    }
+    __syncthreads();
+    if (*abort_flag && threadIdx.x == 0) {
+        drain_loads(R, stages, p.status, p.wait_limit_ns, slot_parity);
+        // the 1x1 weights' copy, if the launch gave up before the MMA warp saw it land
+        volatile uint32_t no_abort = 0;
+        wait_bar(B.w1_full, 0, Ctl{&no_abort, p.status, p.wait_limit_ns});
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, 512);
+    }
+}
+
 // ------------------------------------------------------------------ prepack
 // Wp[t][c][k] = W[k][t][c] for t = r*S + s: per tap, the C x K matrix with K
 // contiguous that the kernel's B operand expects.  32x32 tiles through shared
@@ -1343,4 +1702,41 @@ cudaError_t cdg_launch_channel_sums(const float *ws, int rows, int nsum, int C, 
     if (n <= 0) return cudaSuccess;
     cdg::channel_sums_kernel<<<(n + 255) / 256, 256, 0, stream>>>(ws, rows, nsum, C, out);
     return cudaGetLastError();
+}
+
+namespace {
+
+typedef void (*FusedFn)(CdgParams);
+
+FusedFn select_fused(int in_type, bool gate)
+{
+    if (in_type == CDG_T_F16) return gate ? cdg::fused_kernel<CDG_T_F16, true> : cdg::fused_kernel<CDG_T_F16, false>;
+    return gate ? cdg::fused_kernel<CDG_T_BF16, true> : cdg::fused_kernel<CDG_T_BF16, false>;
+}
+
+}  // namespace
+
+cudaError_t cdg_prepare_fused(int in_type, bool gate)
+{
+    return cudaFuncSetAttribute(reinterpret_cast<const void *>(select_fused(in_type, gate)),
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, CDG_MAX_DYN_SMEM);
+}
+
+cudaError_t cdg_launch_fused(const CdgParams &p, int in_type, bool gate, int grid, size_t smem, cudaStream_t stream)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(CDG_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    unsigned n = 0;
+    if (p.pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, select_fused(in_type, gate), p);
 }

@@ -346,6 +346,64 @@ int cdg_dgrad_noalloc(cdg_handle_t h, const void *dY, const void *W_krsc, void *
 int cdg_dgrad_noalloc_status(cdg_stream_t stream);
 
 /*
+ * Back-to-back dgrads in one persistent kernel: the backward of a
+ * bottleneck's 1x1 -> 3x3 forward pair (conv1 1x1 C1 -> C2, then the
+ * activation, then conv2 R2 x S2 C2 -> K2), which runs as
+ *
+ *     g   = act_bwd(dgrad(dY2, W2), x2)     (conv2's dgrad, gated)
+ *     dX1 = dgrad_1x1(g, W1)                 (conv1's dgrad)
+ *
+ * This is the persistent kernel fusion of the Bolt reading notes (page 5 of
+ * the pages, "Persistent kernel (GEMM/Conv) fusion"), with threadblock
+ * residence: each CTA computes a tile of g over all C2 channels (ThreadBlock_N
+ * = the first dgrad's output channels) and keeps it on chip -- in tensor
+ * memory, where it is the A operand of the second GEMM -- so g is never
+ * read back from HBM.  The second dgrad is 1x1, stride 1, so a tile of dX1
+ * needs exactly the same pixels of g.  g itself is written only if asked
+ * (conv1's weight gradient needs it).
+ *
+ *   conv2: stride 1, pad2, dil2, R2 x S2, C2 = 64 input channels (this kernel),
+ *          K2 output channels (dY2's), dY2 NHWC [N][P][Q][K2] with
+ *          P = H + 2*pad2 - dil2*(R2-1), W2 KRSC [K2][R2][S2][C2];
+ *          its weights and a halo tile of dY2 must fit in shared memory
+ *          together with W1 (CDG_ERR_UNSUPPORTED otherwise)
+ *   conv1: 1x1, stride 1, pad 0, C1 <= 256 input channels (C1 % 8 == 0),
+ *          W1 KRSC [C2][1][1][C1]
+ *   x2     the saved tensor of the activation between them, NHWC [N][H][W][C2]:
+ *          flags CDG_EPI_RELU_BWD (its output or input; g = (x2 > 0) ? v : +0.0),
+ *          CDG_EPI_GELU_BWD or CDG_EPI_SILU_BWD (its input; g = v * f'(x2)),
+ *          or none of them (no activation: x2 = NULL)
+ *   g      NHWC [N][H][W][C2], written only with CDG_FUSED_WRITE_G (else NULL)
+ *   dX1    NHWC [N][H][W][C1]
+ * All in dtype (dX1 and g in dtype too); fp32 accumulation in both GEMMs; g
+ * is rounded to dtype before the second GEMM, exactly as if it went through
+ * memory.  Weights are packed once with cdg_fused_prepack_weights.
+ */
+typedef struct cdg_fused_st *cdg_fused_t;
+#define CDG_FUSED_WRITE_G 256
+
+int cdg_fused_plan(int N, int H, int W, int C1, int C2, int K2, int R2, int S2, int pad2, int dil2, int dtype,
+                   int flags, cdg_fused_t *out);
+/* The same planning without a device (num_sms stands in for the SM count). */
+int cdg_fused_plan_host(int N, int H, int W, int C1, int C2, int K2, int R2, int S2, int pad2, int dil2, int dtype,
+                        int flags, int num_sms, cdg_fused_t *out);
+void cdg_fused_destroy(cdg_fused_t f);
+/* Bytes of the two packed weight buffers (W2: R2*S2*C2*K2, W1: C1*C2 elements). */
+int cdg_fused_packed_weight_bytes(cdg_fused_t f, size_t *w2_bytes, size_t *w1_bytes);
+/* Pack W2 and W1 (device, KRSC) into W2p and W1p; asynchronous on stream. */
+int cdg_fused_prepack_weights(cdg_fused_t f, const void *W2_krsc, const void *W1_krsc, void *W2p, void *W1p,
+                              cdg_stream_t stream);
+/* One launch on stream.  Errors as for cdg_dgrad (CDG_ERR_ALIAS when an
+ * output overlaps an input or the other output).  No allocation. */
+int cdg_dgrad_fused(cdg_fused_t f, const void *dY2, const void *W2p, const void *x2, const void *W1p, void *g,
+                    void *dX1, cdg_stream_t stream);
+/* The first dgrad's planner description (halo tiles, grid, stages), with the
+ * fused kernel's shared memory and tensor-memory columns. */
+int cdg_fused_get_info(cdg_fused_t f, cdg_plan_info_t *info);
+/* Synchronise stream, read and clear the fused plan's device status word. */
+int cdg_fused_device_status(cdg_fused_t f, cdg_stream_t stream);
+
+/*
  * Weight gradient (wgrad) of the same cross-correlation Conv2d, the
  * follow-up the apache/tvm PR #10110 page ("[CUTLASS] Conv2d dgrad") names
  * for dgrad, "wgrad + parallel split-k" (merge comment).  The page gives no

@@ -74,6 +74,10 @@ def _load():
             lib.oracle_half_to_double.restype = ctypes.c_double
             lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
             lib.oracle_bf16_to_double.restype = ctypes.c_double
+            lib.oracle_double_to_half.argtypes = [ctypes.c_double]
+            lib.oracle_double_to_half.restype = ctypes.c_uint16
+            lib.oracle_double_to_bf16.argtypes = [ctypes.c_double]
+            lib.oracle_double_to_bf16.restype = ctypes.c_uint16
             lib.oracle_num_threads.argtypes = []
             lib.oracle_num_threads.restype = i
             _lib = lib
@@ -243,3 +247,27 @@ def channel_sums(out, x=None, dtype=None):
     if rc:
         raise RuntimeError("oracle_channel_sums failed")
     return s1, s2, a1, a2
+
+
+def round_to(values, dtype: str) -> np.ndarray:
+    """Round float64 values once (to nearest, ties to even) to fp16 or bf16,
+    returned as uint16 bit patterns (the oracle's own encoder)."""
+    lib = _load()
+    fn = lib.oracle_double_to_half if dtype == "f16" else lib.oracle_double_to_bf16
+    flat = np.asarray(values, dtype=np.float64).reshape(-1)
+    out = np.fromiter((fn(float(v)) for v in flat), dtype=np.uint16, count=flat.size)
+    return out.reshape(np.shape(values))
+
+
+def dgrad_fused(dY2, W2, x2, W1, H, Wd, pad2=1, dil2=1, dtype=None, act="relu"):
+    """The back-to-back dgrads of a bottleneck's 1x1 -> 3x3 forward pair:
+    g = act_bwd(dgrad(dY2, W2), x2) (stride 1; x2 None: no activation),
+    rounded once to the storage type as a tensor written to memory would be,
+    then dX1 = dgrad_1x1(g, W1) with W1 [C2][1][1][C1].  Returns (dX1, g)
+    with dX1 in float64 and g as uint16 bits of ``dtype`` (float64, unrounded,
+    for float64 inputs)."""
+    g = dgrad(dY2, W2, H, Wd, 1, pad2, dil2, x=x2, dtype=dtype, act=act or "relu")
+    if dtype in ("f16", "bf16"):
+        g = round_to(g, dtype)
+    dX1 = dgrad(g, W1, H, Wd, 1, 0, 1, dtype=dtype)
+    return dX1, g

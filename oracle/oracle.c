@@ -84,6 +84,42 @@ double oracle_bf16_to_double(uint16_t b)
     return (double)f;
 }
 
+/*
+ * Round a double once, to nearest with ties to even, to a 16-bit binary
+ * format with `frac` fraction bits and `expo` exponent bits (IEEE-754
+ * binary16: 10 and 5; bfloat16: 7 and 8): subnormals kept, values beyond the
+ * largest finite one become infinities, NaN stays NaN (a quiet one).  The
+ * significand is scaled to an integer at the format's spacing for the value's
+ * binade (the smallest normal binade's spacing below it) and rounded with
+ * nearbyint in the default rounding mode, which rounds ties to even.
+ */
+static uint16_t encode_16(double x, int frac, int expo)
+{
+    const int bias = (1 << (expo - 1)) - 1, emin = 1 - bias, emax = bias;
+    const uint16_t sign = signbit(x) ? (uint16_t)0x8000u : (uint16_t)0;
+    const uint16_t inf = (uint16_t)(((1u << expo) - 1u) << frac);
+    if (isnan(x)) return (uint16_t)(sign | inf | (1u << (frac - 1)));
+    const double a = fabs(x);
+    if (isinf(a)) return (uint16_t)(sign | inf);
+    if (a == 0.0) return sign;
+    int e2;
+    frexp(a, &e2);           /* a = m * 2^e2, 0.5 <= m < 1 */
+    int E = e2 - 1;          /* a = (1.f...) * 2^E */
+    if (E < emin) E = emin;  /* subnormals share the smallest normal binade's spacing */
+    double r = nearbyint(ldexp(a, frac - E));
+    if (r >= ldexp(1.0, frac + 1)) { /* rounded up into the next binade */
+        r = ldexp(r, -1);
+        E += 1;
+    }
+    if (E > emax) return (uint16_t)(sign | inf);
+    const unsigned sig = (unsigned)r;
+    if (sig < (1u << frac)) return (uint16_t)(sign | sig); /* subnormal (E == emin) */
+    return (uint16_t)(sign | ((unsigned)(E + bias) << frac) | (sig - (1u << frac)));
+}
+
+uint16_t oracle_double_to_half(double x) { return encode_16(x, 10, 5); }
+uint16_t oracle_double_to_bf16(double x) { return encode_16(x, 7, 8); }
+
 /* Forward output extent along one axis; -1 when the geometry is empty. */
 int oracle_out_extent(int in, int filt, int stride, int pad, int dil)
 {
