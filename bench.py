@@ -23,7 +23,7 @@ resident in HBM.  Prints one JSON line:
                the fused ReLU-backward config, and each layer's weight prepack
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--gate none|x|bits] [--autotune 1] [--layers L01,...] [--op dgrad|wgrad]
+                    [--gate none|x|bits] [--autotune 1] [--layers L01,...] [--op dgrad|wgrad|fused]
 
 --gate x|bits runs every layer with the fused ReLU-backward gate, reading the
 saved activation or its 1-bit packed mask; algorithmic bytes, the roofline and
@@ -70,7 +70,8 @@ def load_peaks():
     return dict(FALLBACK_PEAKS, source="fallback")
 
 
-DGRAD_SOURCES = ("cdg_api.cu", "cdg_params.h", "dgrad_sm103.cu", "ptx.cuh", "wait.cuh")
+DGRAD_SOURCES = ("cdg_api.cu", "cdg_params.h", "dgrad_sm103.cu", "dgrad_plain_sm103.cu", "dgrad_ext_sm103.cu",
+                 "dgrad_device.cuh", "dgrad_variant.cuh", "ptx.cuh", "wait.cuh")
 
 
 def kernel_sources_sha256() -> str:
@@ -384,7 +385,9 @@ def other_configs(torch, cdg, dev, stream, peaks, basis, host, state, reps=20):
     (outside the timed region): the tiny 8x8 layer (launch-latency bound),
     the three batch-8 layers with warm and with cold L2 (a buffer of twice the
     L2 size written between calls), the two x-gated batch-256 layers of the
-    fused ReLU-backward config, and the weight prepack of every layer."""
+    fused ReLU-backward config, the back-to-back fused stage-1 pair against
+    its two separate launches, the cost of the fused per-channel sums, GELU
+    and SiLU backward on the F1 shape, and the weight prepack of every layer."""
     from implicit_gemm_dgrad_gb300.workloads import BATCH8, FUSED_RELU, TINY
     l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or (128 << 20)
     flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
@@ -450,6 +453,99 @@ def other_configs(torch, cdg, dev, stream, peaks, basis, host, state, reps=20):
         rec = record(L, ms, "x")
         rec["gate"] = "saved bf16 activation x, read once where dX can be non-zero; cold L2"
         out["fused_relu_x"].append(rec)
+
+    # back-to-back fusion: ResNet-50 stage 1's 3x3 64->64 dgrad at 56x56, gated
+    # by ReLU, feeding the 1x1 64->256 dgrad, one fused launch (g stays on
+    # chip) against the same two layers as two launches (g through HBM)
+    from implicit_gemm_dgrad_gb300.workloads import by_name
+    L4, L3 = by_name("L04_3x3_64_56"), by_name("L03_1x1_256-64_56")
+    dY2, W2, x2 = synth.make_inputs(L4.shape(), L4.dtype, L4.dist, L4.workload, L4.index, with_x=True)
+    _, W1, _ = synth.make_inputs(L3.shape(), L3.dtype, L3.dist, L3.workload, L3.index)
+    up = lambda a: torch.from_numpy(a.reshape(-1).view(np.int16)).to(dev)  # noqa: E731
+    d_dY2, d_W2, d_x2, d_W1 = up(dY2), up(W2), up(x2), up(W1)
+    f = cdg.FusedPlan(L4.N, L4.H, L4.W, L3.C, L4.C, L4.K, 3, 3, 1, 1, "bf16", act="relu")
+    b2, b1 = f.packed_weight_bytes
+    d_W2p = torch.empty(b2 // 2, dtype=torch.int16, device=dev)
+    d_W1p = torch.empty(b1 // 2, dtype=torch.int16, device=dev)
+    f.prepack_weights(d_W2, d_W1, d_W2p, d_W1p, stream)
+    d_dX1 = torch.empty(L3.N * L3.H * L3.W * L3.C, dtype=torch.int16, device=dev)
+    d_g = torch.empty(L4.N * L4.H * L4.W * L4.C, dtype=torch.int16, device=dev)
+    p4 = cdg.plan(L4.N, L4.H, L4.W, L4.C, L4.K, 3, 3, 1, 1, 1, "bf16", relu=True)
+    p3 = cdg.plan(L3.N, L3.H, L3.W, L3.C, L3.K, 1, 1, 1, 0, 1, "bf16")
+    d_W3p = torch.empty(p3.packed_weight_bytes // 2, dtype=torch.int16, device=dev)
+    p3.prepack_weights(d_W1, d_W3p, stream)
+    fused = lambda: f.dgrad(d_dY2, d_W2p, d_x2, d_W1p, d_dX1, None, stream)  # noqa: E731
+
+    def unfused():
+        p4.dgrad(d_dY2, d_W2p, d_g, d_x2, stream)
+        p3.dgrad(d_g, d_W3p, d_dX1, None, stream)
+    for _ in range(3):
+        fused()
+        unfused()
+    ms_f = float(np.median(time_launches(torch, stream, fused, reps, flush)))
+    ms_u = float(np.median(time_launches(torch, stream, unfused, reps, flush)))
+    if f.device_status(stream) != 0 or p4.device_status(stream) != 0 or p3.device_status(stream) != 0:
+        raise RuntimeError("device status after the fused pair")
+    flops = L4.flops + L3.flops
+    fbytes = 2 * (dY2.size + x2.size + W2.size + W1.size) + 2 * d_dX1.numel()
+    t_roof = max(flops / (tensor_peak(peaks, basis) * 1e12), fbytes / (peaks["hbm_gbs"] * 1e9))
+    out["fused_bottleneck_stage1"] = {
+        "what": "dX1 = dgrad_1x1(relu_bwd(dgrad_3x3(dY2, W2), x2), W1): L04 shape gated by ReLU, then L03 shape; "
+                "batch 256, bf16, cold L2",
+        "fused_ms": round(ms_f, 5), "two_launch_ms": round(ms_u, 5), "speedup": round(ms_u / ms_f, 3),
+        "tflops": round(flops / (ms_f * 1e-3) / 1e12, 2), "gbs": round(fbytes / (ms_f * 1e-3) / 1e9, 1),
+        "algorithmic_bytes": fbytes, "bound": "hbm" if fbytes / (peaks["hbm_gbs"] * 1e9) > flops /
+        (tensor_peak(peaks, basis) * 1e12) else "tensor", "roofline_frac": round(t_roof / (ms_f * 1e-3), 4),
+        "plan": {k: f.info()[k] for k in ("box_w", "box_h", "stages", "work_items", "grid", "smem_bytes")}}
+    del d_dY2, d_x2, d_g, d_dX1
+
+    # per-channel output sums fused into the epilogue: cost against the same layer without them
+    sums = []
+    for L, nsum in ((by_name("L03_1x1_256-64_56"), 1), (FUSED_RELU[0], 2)):
+        dY, W, x = synth.make_inputs(L.shape(), L.dtype, L.dist, L.workload, L.index, with_x=L.relu)
+        d_dY, d_W, d_x = up(dY), up(W), (up(x) if L.relu else None)
+        pl = cdg.plan(L.N, L.H, L.W, L.C, L.K, L.R, L.S, L.stride, L.pad, L.dil, L.dtype, relu=L.relu)
+        ps = cdg.plan(L.N, L.H, L.W, L.C, L.K, L.R, L.S, L.stride, L.pad, L.dil, L.dtype, relu=L.relu, sums=nsum)
+        d_Wp = torch.empty(pl.packed_weight_bytes // 2, dtype=torch.int16, device=dev)
+        pl.prepack_weights(d_W, d_Wp, stream)
+        d_dX = torch.empty(L.N * L.H * L.W * L.C, dtype=torch.int16, device=dev)
+        d_s = torch.empty(nsum * L.C, dtype=torch.float32, device=dev)
+        d_ws = torch.empty(ps.sums_workspace_bytes // 4, dtype=torch.float32, device=dev)
+        plain = lambda: pl.dgrad(d_dY, d_Wp, d_dX, d_x, stream)  # noqa: E731
+        with_sums = lambda: ps.dgrad_sums(d_dY, d_Wp, d_dX, d_s, d_ws, d_x, stream)  # noqa: E731
+        for _ in range(3):
+            plain()
+            with_sums()
+        m0 = float(np.median(time_launches(torch, stream, plain, reps, flush)))
+        m1 = float(np.median(time_launches(torch, stream, with_sums, reps, flush)))
+        if ps.device_status(stream) != 0:
+            raise RuntimeError(f"device status after the sums of {L.name}")
+        sums.append({"layer": L.name, "sums": ["sum dX"] + (["sum dX*x"] if nsum == 2 else []),
+                     "plain_ms": round(m0, 5), "with_sums_ms": round(m1, 5), "overhead": round(m1 / m0 - 1, 4)})
+    out["channel_sums"] = sums
+
+    # activation backward other than ReLU, on the F1 shape (x = the activation's saved input)
+    L = FUSED_RELU[0]
+    dY, W, _ = synth.make_inputs(L.shape(), L.dtype, L.dist, L.workload, L.index)
+    z = synth.to_bits((2.0 * np.random.default_rng(77).standard_normal((L.N, L.H, L.W, L.C))).astype(np.float32),
+                      L.dtype)
+    d_dY, d_W, d_z = up(dY), up(W), up(z)
+    d_dX = torch.empty(L.N * L.H * L.W * L.C, dtype=torch.int16, device=dev)
+    acts = []
+    for act in ("relu", "gelu", "silu"):
+        pa = cdg.plan(L.N, L.H, L.W, L.C, L.K, L.R, L.S, L.stride, L.pad, L.dil, L.dtype, relu=True, act=act)
+        d_Wp = torch.empty(pa.packed_weight_bytes // 2, dtype=torch.int16, device=dev)
+        pa.prepack_weights(d_W, d_Wp, stream)
+        run = lambda: pa.dgrad(d_dY, d_Wp, d_dX, d_z, stream)  # noqa: E731
+        for _ in range(3):
+            run()
+        ms = float(np.median(time_launches(torch, stream, run, reps, flush)))
+        if pa.device_status(stream) != 0:
+            raise RuntimeError(f"device status after {act}")
+        rec = {"act": act}
+        rec.update(layer_record(L, ms, peaks, basis, "x"))
+        acts.append(rec)
+    out["activation_bwd_F1"] = acts
 
     # weight prepack (KRSC -> packed B operand), once per weight update; not part of the metric
     prep = {}
@@ -611,6 +707,69 @@ def run_wgrad(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def run_fused(args, rank, world, local_rank):
+    """The back-to-back fused dgrad of ResNet-50 stage 1 alone (the 3x3 64->64
+    layer at 56x56 gated by ReLU, feeding the 1x1 64->256 layer, g kept on
+    chip): K timed launches, inputs resident (larger than L2)."""
+    import torch
+    import implicit_gemm_dgrad_gb300 as cdg
+    from implicit_gemm_dgrad_gb300.workloads import by_name
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.Stream(device=dev)
+    peaks = load_peaks()
+    L4, L3 = by_name("L04_3x3_64_56"), by_name("L03_1x1_256-64_56")
+    dY2, W2, x2 = synth.make_inputs(L4.shape(), L4.dtype, L4.dist, L4.workload, L4.index, with_x=True)
+    _, W1, _ = synth.make_inputs(L3.shape(), L3.dtype, L3.dist, L3.workload, L3.index)
+    up = lambda a: torch.from_numpy(a.reshape(-1).view(np.int16)).to(dev)  # noqa: E731
+    with torch.cuda.stream(stream):
+        d_dY2, d_W2, d_x2, d_W1 = up(dY2), up(W2), up(x2), up(W1)
+        f = cdg.FusedPlan(L4.N, L4.H, L4.W, L3.C, L4.C, L4.K, 3, 3, 1, 1, "bf16", act="relu")
+        b2, b1 = f.packed_weight_bytes
+        d_W2p = torch.empty(b2 // 2, dtype=torch.int16, device=dev)
+        d_W1p = torch.empty(b1 // 2, dtype=torch.int16, device=dev)
+        f.prepack_weights(d_W2, d_W1, d_W2p, d_W1p, stream)
+        d_dX1 = torch.empty(L3.N * L3.H * L3.W * L3.C, dtype=torch.int16, device=dev)
+    torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        f.dgrad(d_dY2, d_W2p, d_x2, d_W1p, d_dX1, None, stream)
+    torch.cuda.synchronize()
+    if f.device_status(stream) != 0:
+        raise RuntimeError("fused device status after warm-up")
+    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(local_rank) as clocks:
+        hold_stream(torch, stream)
+        for k in range(args.steps):
+            e0[k].record(stream)
+            f.dgrad(d_dY2, d_W2p, d_x2, d_W1p, d_dX1, None, stream)
+            e1[k].record(stream)
+        torch.cuda.synchronize()
+    total_ms = max_over_ranks(float(sum(e0[k].elapsed_time(e1[k]) for k in range(args.steps))), world)
+    if rank != 0:
+        return
+    clk = clocks.summary()
+    basis = peak_basis(clk)
+    ms = total_ms / args.steps
+    flops = L4.flops + L3.flops
+    fbytes = 2 * (dY2.size + x2.size + W2.size + W1.size) + 2 * d_dX1.numel()
+    t_tc, t_hbm = flops / (tensor_peak(peaks, basis) * 1e12), fbytes / (peaks["hbm_gbs"] * 1e9)
+    bound = "tensor" if t_tc >= t_hbm else "hbm"
+    achieved = fbytes / (ms * 1e-3) / 1e9 if bound == "hbm" else flops / (ms * 1e-3) / 1e12
+    peak = peaks["hbm_gbs"] if bound == "hbm" else tensor_peak(peaks, basis)
+    line = {"metric": "fused back-to-back dgrad TFLOP/s (ResNet-50 stage 1: 3x3 64->64 + ReLU bwd + 1x1 64->256)",
+            "op": "fused", "value": round(world * flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "resnet50_stage1_fused_3x3_relu_1x1_b256_bf16", "global_batch": 256 * world,
+                       "l2": "inputs larger than L2", "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": bound, "achieved": round(achieved, 2), "peak": peak,
+                         "unit": "GB/s" if bound == "hbm" else "TFLOP/s", "frac": round(achieved / peak, 4),
+                         "traffic": None, "algorithmic_bytes": fbytes, "kernel": "fused_kernel",
+                         "peak_basis": basis},
+            "gpu_launches": args.steps, "clocks": clk, "plan": f.info()}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -627,8 +786,9 @@ def main():
     ap.add_argument("--layers", default="", help="comma-separated layer names (default: all 22)")
     ap.add_argument("--autotune", type=int, default=0,
                     help="1: tune every layer's plan with cdg_autotune during set-up (untimed)")
-    ap.add_argument("--op", default="dgrad", choices=["dgrad", "wgrad"],
-                    help="wgrad: time the weight gradient (split-K GEMM + ordered reduction) of the same layers")
+    ap.add_argument("--op", default="dgrad", choices=["dgrad", "wgrad", "fused"],
+                    help="wgrad: time the weight gradient (split-K GEMM + ordered reduction) of the same layers; "
+                         "fused: time the back-to-back fused dgrad of ResNet-50 stage 1 alone")
     ap.add_argument("--gate", default="none", choices=["none", "x", "bits"],
                     help="fused ReLU-backward gate on every layer: none; x = the saved bf16 activation; "
                          "bits = its 1-bit packed mask (packed once at set-up, as a forward pass would store it)")
@@ -653,6 +813,9 @@ def main():
     torch.cuda.set_device(local_rank)
     if args.op == "wgrad":
         run_wgrad(args, rank, world, local_rank)
+        return
+    if args.op == "fused":
+        run_fused(args, rank, world, local_rank)
         return
     dev = torch.device("cuda", local_rank)
     stream = torch.cuda.Stream(device=dev)

@@ -74,6 +74,7 @@ struct PlanOpts {
     int interleave = -1;  // 0 phases one after another
     int max_bn = 256;     // 128 caps the N tile
     int bn = 0;           // > 0: this N tile (a multiple of 64, or of 128 with the packed mask), if it fits C
+    int nacc = 2;         // halo plans: accumulators in flight (2 or 4)
     int pdl = 1;          // 0 plain launches
 };
 
@@ -183,6 +184,8 @@ PlanOpts opts_from_env()
     o.max_bn = (bn && std::atoi(bn) == 128) ? 128 : 256;
     const char *fbn = std::getenv("CDG_BN");
     o.bn = fbn ? std::atoi(fbn) : 0;
+    const char *na = std::getenv("CDG_NACC");
+    o.nacc = (na && std::atoi(na) == 4) ? 4 : 2;
     o.pdl = flag("CDG_PDL") == 0 ? 0 : 1;
     return o;
 }
@@ -446,7 +449,7 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
                                 : stages * stage_bytes;
     // two accumulators per MMA warp, each at least as wide as the 64-column
     // chunks the epilogue reads
-    const int n_acc = dual ? 4 : 2;
+    const int n_acc = dual ? 4 : (halo && opt.nacc == 4 ? 4 : 2);
     int tmem_cols = 32;
     while (tmem_cols < n_acc * (((BN + 63) / 64) * 64)) tmem_cols *= 2;
 
@@ -516,6 +519,7 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     }  // p.il_round is set once the grid is final (below)
     p.tmem_cols = static_cast<uint32_t>(tmem_cols);
     p.acc_stride = static_cast<uint32_t>(tmem_cols / n_acc);
+    p.acc_ring = dual ? 2u : static_cast<uint32_t>(n_acc);
     for (size_t i = 0; i < phases.size(); ++i) p.phase[i] = phases[i];
     for (size_t i = 0; i < taps.size(); ++i) p.tap[i] = taps[i];
 

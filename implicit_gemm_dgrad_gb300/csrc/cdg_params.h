@@ -106,6 +106,7 @@ struct CdgParams {  // CUtensorMap members carry their own (128-byte) alignment
     uint32_t tx_bytes;    // bytes one pipeline stage receives (A box + B box)
     uint32_t tmem_cols;   // allocated TMEM columns (two accumulators)
     uint32_t acc_stride;  // column offset of the second accumulator
+    uint32_t acc_ring;    // accumulators an MMA warp cycles through (2; 4 for halo plans that ask)
     float *red_ws;        // per-channel sums: this launch's [grid][nsum][C] fp32 partials (one row per CTA)
     int nsum;             // per-channel output sums the epilogue accumulates: 0, 1 (sum of dX) or
                           // 2 (also the sum of dX * x where the gate passes)
@@ -138,3 +139,12 @@ cudaError_t cdg_launch_fused(const CdgParams &p, int in_type, bool gate, int gri
 // tile (16 KB, gated plans only), two 16 KB staging buffers, the tail.
 #define CDG_FUSED_X2_BYTES (128 * 128)
 int cdg_max_active_pairs(int out_type, int in_type, bool mask, size_t smem);
+// One variant of the dgrad kernels (EXT: with the extended epilogue), each
+// instantiated in its own translation unit.
+template <bool EXT>
+cudaError_t cdg_dgrad_prepare_variant(int out_type, int in_type, bool mask);
+template <bool EXT>
+cudaError_t cdg_dgrad_launch_variant(const CdgParams &p, int out_type, int in_type, bool mask, int grid, size_t smem,
+                                     cudaStream_t stream);
+template <bool EXT>
+int cdg_dgrad_max_pairs_variant(int out_type, int in_type, bool mask, size_t smem);

@@ -1,0 +1,101 @@
+// Kernel selection and launch for one variant of the dgrad kernels (EXT:
+// the extended epilogue with per-channel sums and activations other than
+// ReLU, or not).  Each variant is instantiated in a translation unit of its
+// own (dgrad_plain_sm103.cu, dgrad_ext_sm103.cu), so that the two sets of
+// kernels compile in parallel.
+#pragma once
+
+#include "dgrad_device.cuh"
+
+namespace {
+
+typedef void (*DgradFn)(CdgParams);
+
+template <int OUT_T, bool MASK, int IN_T, bool EXT>
+DgradFn pick_mode(int mode)
+{
+    if (mode == 1) return cdg::dgrad_kernel<OUT_T, MASK, IN_T, 1, EXT>;
+    if (mode == 2) return cdg::dgrad_kernel<OUT_T, MASK, IN_T, 2, EXT>;
+    if (mode == 3) return cdg::dgrad_kernel<OUT_T, MASK, IN_T, 3, EXT>;
+    return cdg::dgrad_kernel<OUT_T, MASK, IN_T, 0, EXT>;
+}
+
+template <bool EXT>
+DgradFn select_kernel(int out_type, int in_type, bool mask, int mode)
+{
+    if (in_type == CDG_T_F16) {
+        if (out_type == CDG_T_F32)
+            return mask ? pick_mode<CDG_T_F32, true, CDG_T_F16, EXT>(mode) : pick_mode<CDG_T_F32, false, CDG_T_F16, EXT>(mode);
+        return mask ? pick_mode<CDG_T_F16, true, CDG_T_F16, EXT>(mode) : pick_mode<CDG_T_F16, false, CDG_T_F16, EXT>(mode);
+    }
+    if (out_type == CDG_T_F32)
+        return mask ? pick_mode<CDG_T_F32, true, CDG_T_BF16, EXT>(mode) : pick_mode<CDG_T_F32, false, CDG_T_BF16, EXT>(mode);
+    return mask ? pick_mode<CDG_T_BF16, true, CDG_T_BF16, EXT>(mode) : pick_mode<CDG_T_BF16, false, CDG_T_BF16, EXT>(mode);
+}
+
+}  // namespace
+
+// Raise the dynamic shared-memory limit of every kernel of this variant for
+// the given types to the largest size any plan may request.
+template <bool EXT>
+cudaError_t cdg_dgrad_prepare_variant(int out_type, int in_type, bool mask)
+{
+    for (int mode = 0; mode < 4; ++mode) {
+        DgradFn fn = select_kernel<EXT>(out_type, in_type, mask, mode);
+        const cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void *>(fn),
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, CDG_MAX_DYN_SMEM);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+template <bool EXT>
+cudaError_t cdg_dgrad_launch_variant(const CdgParams &p, int out_type, int in_type, bool mask, int grid, size_t smem,
+                                     cudaStream_t stream)
+{
+    const int mode = p.halo ? 1 : (p.pair ? 2 : (p.dual ? 3 : 0));
+    DgradFn fn = select_kernel<EXT>(out_type, in_type, mask, mode);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(CDG_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
+    if (p.pair) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = 2;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    if (p.pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, fn, p);
+}
+
+// Largest number of CTA pairs of this variant's pair kernel resident at once.
+template <bool EXT>
+int cdg_dgrad_max_pairs_variant(int out_type, int in_type, bool mask, size_t smem)
+{
+    DgradFn fn = select_kernel<EXT>(out_type, in_type, mask, 2);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(CDG_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void *>(fn), &cfg) != cudaSuccess) return -1;
+    return n;
+}

@@ -166,13 +166,16 @@ def test_interleaved_plans():
         assert_close(got, ref, run.odt, run.layer.name)
 
 
+@pytest.mark.parametrize("nacc", ["2", "4"])
 @pytest.mark.parametrize("L", [SWEEP[0], SWEEP[1], SWEEP[4], SWEEP[5], SWEEP[12], SWEEP[14], BATCH8[0]],
                          ids=lambda L: L.name)
-def test_halo_operand_mode(L, monkeypatch):
+def test_halo_operand_mode(L, nacc, monkeypatch):
     """The halo operand mode (one dY box per tile and K block serves every
     tap; weights streamed per tap, or resident when the whole filter of a
-    single N tile fits) gives the same results."""
+    single N tile fits) gives the same results, with two or four
+    accumulators in flight."""
     monkeypatch.setenv("CDG_HALO", "1")
+    monkeypatch.setenv("CDG_NACC", nacc)
     run, _, _ = check_layer(L)
     assert run.plan.info()["a_mode"] in (2, 3)
 
