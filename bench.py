@@ -71,7 +71,7 @@ def load_peaks():
 
 
 DGRAD_SOURCES = ("cdg_api.cu", "cdg_params.h", "dgrad_sm103.cu", "dgrad_plain_sm103.cu", "dgrad_ext_sm103.cu",
-                 "dgrad_device.cuh", "dgrad_variant.cuh", "ptx.cuh", "wait.cuh")
+                 "dgrad_act_sm103.cu", "dgrad_device.cuh", "dgrad_variant.cuh", "ptx.cuh", "wait.cuh")
 
 
 def kernel_sources_sha256() -> str:

@@ -2,9 +2,9 @@
 
     python -m implicit_gemm_dgrad_gb300.build [--force]
 
-Six translation units compiled in parallel (the dgrad and wgrad host APIs,
-the plain and the extended dgrad kernel variants, the other dgrad kernels,
-the wgrad kernels), then linked
+Seven translation units compiled in parallel (the dgrad and wgrad host APIs,
+the plain, per-channel-sum and activation variants of the dgrad kernels, the
+other dgrad kernels, the wgrad kernels), then linked
 into a shared library next to this file.  The CUDA runtime is linked
 statically; the driver API is reached through cudaGetDriverEntryPointByVersion.
 """
@@ -23,7 +23,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libcdg.so")
 BUILD_DIR = os.path.join(HERE, "_build")
 SOURCES = ["cdg_api.cu", "cwg_api.cu", "dgrad_sm103.cu", "dgrad_plain_sm103.cu", "dgrad_ext_sm103.cu",
-           "wgrad_sm103.cu"]
+           "dgrad_act_sm103.cu", "wgrad_sm103.cu"]
 HEADERS = ["cdg_params.h", "cwg_params.h", "ptx.cuh", "wait.cuh", "dgrad_device.cuh", "dgrad_variant.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

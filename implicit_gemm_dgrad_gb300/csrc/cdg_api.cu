@@ -310,7 +310,8 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     // them ahead of use; by the packed mask: a ring of mask tiles besides
     const int staging = CDG_SMEM_STAGING + (h->mask ? (h->mask_bits ? CDG_GATE_RING : CDG_SMEM_STAGING) : 0);
     // per-channel sums: the epilogue warps' partials of a chunk, after the tail
-    const int red_bytes = nsum ? CDG_SMEM_RED : 0;
+    // and the CTA's per-channel accumulators ([sum][C] fp32)
+    const int red_bytes = nsum ? CDG_SMEM_RED + ((nsum * C * 4 + 127) / 128) * 128 : 0;
     const int ring_budget = kMaxSmem - 1024 - staging - CDG_SMEM_TAIL - red_bytes;
 
     // ---- halo operand mode: a tile is halo_bh full-width rows of one image's
@@ -1307,7 +1308,7 @@ int fused_make(int N, int H, int W, int C1, int C2, int K2, int R2, int S2, int 
     f->BN2 = BN2;
     f->write_g = p.write_g != 0;
     f->smem = static_cast<size_t>(fixed + as * static_cast<int>(p.a_stage_bytes));
-    if (!host_only && cdg_prepare_fused(g->in_type, gated) != cudaSuccess) {
+    if (!host_only && cdg_prepare_fused(g->in_type, gated ? p.act : -1) != cudaSuccess) {
         cdg_destroy(g);
         delete f;
         return CDG_ERR_CUDA;
@@ -1452,7 +1453,8 @@ int cdg_dgrad_fused(cdg_fused_t f, const void *dY2, const void *W2p, const void 
     p.mask = x2;
     p.status = h->d_status;
     p.red_ws = nullptr;
-    if (cdg_launch_fused(p, h->in_type, h->mask, h->grid, f->smem, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    if (cdg_launch_fused(p, h->in_type, h->mask ? p.act : -1, h->grid, f->smem, static_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
         return CDG_ERR_CUDA;
     return CDG_OK;
 }

@@ -31,7 +31,8 @@
 #define CDG_SMEM_TAIL 2048
 #define CDG_SMEM_TABLES 320
 // Per-channel output sums (plans with CDG_EPI_SUM): after the tail, the four
-// epilogue warps' partial sums of one chunk, [sums][4 warps][64 channels] fp32.
+// epilogue warps' partial sums of one chunk, [sums][4 warps][64 channels]
+// fp32, then the CTA's accumulators, [sums][C] fp32 (in 128-byte units).
 #define CDG_SMEM_RED (2 * 4 * 64 * 4)
 #define CDG_MAX_STAGES_TOTAL 10  // all ring stages together (their mbarriers live in the 320-byte area)
 
@@ -133,18 +134,19 @@ cudaError_t cdg_launch_dgrad(const CdgParams &p, int out_type, int in_type, bool
 cudaError_t cdg_prepare_dgrad(int out_type, int in_type, bool mask, size_t smem);
 cudaError_t cdg_launch_prepack(const void *W, void *Wp, int K, int T, int C, cudaStream_t stream);
 cudaError_t cdg_launch_channel_sums(const float *ws, int rows, int nsum, int C, float *out, cudaStream_t stream);
-cudaError_t cdg_prepare_fused(int in_type, bool gate);
-cudaError_t cdg_launch_fused(const CdgParams &p, int in_type, bool gate, int grid, size_t smem, cudaStream_t stream);
 // Shared memory of the fused kernel beyond the halo ring, W2 and W1: the gate
 // tile (16 KB, gated plans only), two 16 KB staging buffers, the tail.
 #define CDG_FUSED_X2_BYTES (128 * 128)
 int cdg_max_active_pairs(int out_type, int in_type, bool mask, size_t smem);
-// One variant of the dgrad kernels (EXT: with the extended epilogue), each
-// instantiated in its own translation unit.
-template <bool EXT>
+// One epilogue variant of the dgrad kernels (EPI: 0 plain, 1 per-channel
+// sums, 2 GELU backward, 3 SiLU backward), each instantiated in a
+// translation unit of its own.
+template <int EPI>
 cudaError_t cdg_dgrad_prepare_variant(int out_type, int in_type, bool mask);
-template <bool EXT>
+template <int EPI>
 cudaError_t cdg_dgrad_launch_variant(const CdgParams &p, int out_type, int in_type, bool mask, int grid, size_t smem,
                                      cudaStream_t stream);
-template <bool EXT>
+template <int EPI>
 int cdg_dgrad_max_pairs_variant(int out_type, int in_type, bool mask, size_t smem);
+cudaError_t cdg_prepare_fused(int in_type, int act);
+cudaError_t cdg_launch_fused(const CdgParams &p, int in_type, int act, int grid, size_t smem, cudaStream_t stream);

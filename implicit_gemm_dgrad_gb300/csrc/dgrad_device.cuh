@@ -605,34 +605,37 @@ __device__ __forceinline__ void gate_issue(const CdgParams &p, const GateCursor 
 // f'(x) = Phi(x) + x phi(x) with Phi(x) = (1 + erf(x / sqrt 2)) / 2 and
 // phi(x) = exp(-x^2 / 2) / sqrt(2 pi); SiLU, f'(x) = s (1 + x (1 - s)) with
 // s = 1 / (1 + exp(-x)).  erff and expf are CUDA's.
-__device__ __forceinline__ float act_grad(float x, int act)
+// (__expf is the hardware exponential, accurate to a few ulp of fp32: far
+// below the 16-bit output's rounding.)
+template <int ACT>
+__device__ __forceinline__ float act_grad(float x)
 {
-    if (act == 1) {
+    if (ACT == 1) {
         const float Phi = 0.5f * (1.0f + erff(x * 0.70710678118654752f));
-        const float phi = 0.39894228040143268f * expf(-0.5f * x * x);
+        const float phi = 0.39894228040143268f * __expf(-0.5f * x * x);
         return fmaf(x, phi, Phi);
     }
-    const float sg = 1.0f / (1.0f + expf(-x));
+    const float sg = __frcp_rn(1.0f + __expf(-x));
     return sg * fmaf(x, 1.0f - sg, 1.0f);
 }
 
 // Backward of the activation whose saved input is x, on PER consecutive
-// values.  ReLU (act 0): v = (x > 0) ? v : +0.0 (a select, so masked outputs
+// values.  ReLU (ACT 0): v = (x > 0) ? v : +0.0 (a select, so masked outputs
 // are +0.0 whatever the accumulator holds), and xp receives v * x where the
 // gate passes, +0.0 elsewhere (the terms of the per-channel sum of dX * x).
-// GELU and SiLU: v = v * f'(x).
-template <int IN_T, int PER>
-__device__ __forceinline__ void gate_x(float *v, const uint32_t *w, float *xp, int act)
+// GELU (ACT 1) and SiLU (ACT 2): v = v * f'(x).
+template <int IN_T, int PER, int ACT>
+__device__ __forceinline__ void gate_x(float *v, const uint32_t *w, float *xp)
 {
 #pragma unroll
     for (int e = 0; e < PER; ++e) {
         const float x = gate_value<IN_T>(static_cast<uint16_t>(w[e >> 1] >> (16 * (e & 1))));
-        if (act == 0) {
+        if (ACT == 0) {
             const bool pass = x > 0.0f;
             v[e] = pass ? v[e] : 0.0f;
             xp[e] = pass ? v[e] * x : 0.0f;
         } else {
-            v[e] *= act_grad(x, act);
+            v[e] *= act_grad<ACT>(x);
         }
     }
 }
@@ -697,10 +700,11 @@ __device__ __forceinline__ void gate_mask(float *v, uint32_t bits)
         if (!((bits >> e) & 1u)) v[e] = 0.0f;
 }
 
-// EXT: the extended epilogue (per-channel sums, activation backward other
-// than ReLU).  Plain kernels are built without it, so that its code does not
-// enlarge their unrolled per-element loop.
-template <int OUT_T, bool MASK, int IN_T, bool HALO, bool PAIR, bool DUAL, bool EXT>
+// EPI, the epilogue variant: 0 plain (the ReLU gate or none), 1 with the
+// per-channel sums, 2 GELU backward, 3 SiLU backward (these two with or
+// without the sums).  Each is its own kernel, so that no variant's code
+// enlarges another's unrolled per-element loop.
+template <int OUT_T, bool MASK, int IN_T, bool HALO, bool PAIR, bool DUAL, int EPI>
 __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, const CdgPhase *tab, Ctl ctl,
                                              uint32_t tmem_base, Sched S)
 {
@@ -740,16 +744,19 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
     bool zero_ready = false;
 
     // Per-channel sums (p.nsum > 0): this CTA adds each chunk's column sums
-    // into its own row of the workspace, [CTA][sum][C] fp32.  Channel c is
-    // always handled by epilogue thread c % CH (N tiles are multiples of CH
-    // channels, or a single tile from channel 0), which zeroes it first, so
-    // the row needs no atomics and its sums keep one order from run to run.
-    const int nsum = EXT ? p.nsum : 0;
+    // into its own accumulators in shared memory, [sum][C] fp32, and writes
+    // them to its row of the workspace, [CTA][sum][C], once at the end.
+    // Channel c is always handled by epilogue thread c % CH (N tiles are
+    // multiples of CH channels, or a single tile from channel 0), which zeroes,
+    // adds and writes it, so nothing needs atomics or a barrier, and the sums
+    // keep one order from run to run.
+    const int nsum = EPI != 0 ? p.nsum : 0;
+    constexpr int ACT = EPI >= 2 ? EPI - 1 : 0;  // activation of the x gate (0 ReLU, 1 GELU, 2 SiLU)
     const int ethread = ew * 32 + lane;
-    float *const red_row = nsum ? p.red_ws + static_cast<size_t>(blockIdx.x) * nsum * C : nullptr;
+    const uint32_t red_acc0 = R.red0 + CDG_SMEM_RED;
     if (nsum && ethread < CH)
         for (int c = ethread; c < C; c += CH)
-            for (int k = 0; k < nsum; ++k) red_row[k * C + c] = 0.0f;
+            for (int k = 0; k < nsum; ++k) st_shared_f32(red_acc0 + 4u * static_cast<uint32_t>(k * C + c), 0.0f);
 
     // TMA stores are spread over the four warps' elected lanes (an issue holds its
     // thread for a few hundred cycles): chunk k is stored by epilogue warp k % 4.
@@ -926,13 +933,13 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
                     } else if (OSZ == 2) {  // x piece q sits where output piece q goes
                         uint32_t xw[4];
                         ld_shared_v4(buf + srow_off + ((static_cast<uint32_t>(q) ^ sw) << 4), xw);
-                        if (EXT)
-                            gate_x<IN_T, PER>(v, xw, xp, p.act);
+                        if (EPI != 0)
+                            gate_x<IN_T, PER, ACT>(v, xw, xp);
                         else
                             gate_relu<IN_T, PER>(v, xw);
                     } else {  // fp32 output: values 4q .. 4q+3 of the chunk
-                        if (EXT)
-                            gate_x<IN_T, PER>(v, &xf[(2 * q) % (OSZ == 4 ? 16 : 1)], xp, p.act);
+                        if (EPI != 0)
+                            gate_x<IN_T, PER, ACT>(v, &xf[(2 * q) % (OSZ == 4 ? 16 : 1)], xp);
                         else
                             gate_relu<IN_T, PER>(v, &xf[(2 * q) % (OSZ == 4 ? 16 : 1)]);
                     }
@@ -989,12 +996,19 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
                         const uint32_t base = R.red0 + static_cast<uint32_t>(k2) * (4u * 64u * 4u) + col;
                         const float t = ((ld_shared_f32(base) + ld_shared_f32(base + 256u)) + ld_shared_f32(base + 512u)) +
                                         ld_shared_f32(base + 768u);
-                        red_row[k2 * C + c] += t;
+                        const uint32_t a = red_acc0 + 4u * static_cast<uint32_t>(k2 * C + c);
+                        st_shared_f32(a, ld_shared_f32(a) + t);
                     }
                 }
             }
         }
         if (!ok) break;
+    }
+    if (nsum && ethread < CH) {
+        // this thread's channels, added by it alone, to the CTA's workspace row
+        float *const row_out = p.red_ws + static_cast<size_t>(blockIdx.x) * nsum * C;
+        for (int c = ethread; c < C; c += CH)
+            for (int k = 0; k < nsum; ++k) row_out[k * C + c] = ld_shared_f32(red_acc0 + 4u * static_cast<uint32_t>(k * C + c));
     }
     if (MASK && ew == 0 && elected && g_used != g_issued) {
         // aborted: let the gate loads still in flight land before the CTA exits
@@ -1015,7 +1029,7 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
 //         shared memory takes in and hands to the tensor core;
 //       3 per-tap or row boxes, two MMA warps (dual issue) for N tiles of up to
 //         128 channels.
-template <int OUT_T, bool MASK, int IN_T, int MODE, bool EXT>
+template <int OUT_T, bool MASK, int IN_T, int MODE, int EPI>
 __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_constant__ CdgParams p)
 {
     constexpr bool HALO = MODE == 1;
@@ -1140,7 +1154,7 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_cons
             const int j = warp >> 1;
             run_mma<false>(p, ring_of(j), tab, ctl, tmem_base + 2u * j * p.acc_stride, elect_one_sync(), sched_of(j));
         } else if (warp >= CDG_EPI_WARP0) {
-            run_epilogue<OUT_T, MASK, IN_T, false, false, true, EXT>(p, R, tab, ctl, tmem_base, S);
+            run_epilogue<OUT_T, MASK, IN_T, false, false, true, EPI>(p, R, tab, ctl, tmem_base, S);
         } else {
             const int j = warp >> 1;  // warps 0 and 2
             run_loader<false>(p, ring_of(j), tab, taps, ctl, 0, 1, elect_one_sync(),
@@ -1158,7 +1172,7 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_cons
             wait_bar(R.drain, 0, Ctl{&no_abort, p.status, p.wait_limit_ns});
         }
     } else if (warp >= CDG_EPI_WARP0) {
-        run_epilogue<OUT_T, MASK, IN_T, HALO, PAIR, false, EXT>(p, R, tab, ctl, tmem_base, S);
+        run_epilogue<OUT_T, MASK, IN_T, HALO, PAIR, false, EPI>(p, R, tab, ctl, tmem_base, S);
     } else if (HALO) {
         run_loader_halo(p, R, tab, taps, ctl, warp == 0 ? 0 : warp - 1, elect_one_sync(), slot_parity, S);
     } else {
@@ -1303,11 +1317,12 @@ __device__ __forceinline__ void run_mma_fused(const CdgParams &p, const Ring &R,
     wait_bar(B.drain, 0, Ctl{&no_abort, ctl.status, ctl.limit});
 }
 
-template <int IN_T, bool GATE>
+template <int IN_T, int ACT>
 __device__ __forceinline__ void run_epilogue_fused(const CdgParams &p, const Ring &R, const FusedBars &B,
                                                    const CdgPhase *tab, Ctl ctl, uint32_t tmem_base, Sched S,
                                                    uint32_t x2_smem)
 {
+    constexpr bool GATE = ACT >= 0;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const bool elected = elect_one_sync();
     const int quad = warp & 3;
@@ -1341,9 +1356,9 @@ __device__ __forceinline__ void run_epilogue_fused(const CdgParams &p, const Rin
         nx.next();
     };
     gate_issue();
-    uint32_t n = 0, chunk = 0;
+    uint32_t chunk = 0;
     // one 16 KB output chunk through staging buffer chunk % 2 (the same
-    // hand-over as the plain epilogue); `fill` writes this thread's row
+    // hand-over as the plain epilogue); each thread writes its row
     auto store_chunk = [&](uint64_t map, int c, int j0, int i0, int n0, const uint32_t (&pk)[32]) {
         const uint32_t k = chunk++;
         const uint32_t buf = R.out0 + (k & 1u) * (128u * 128u);
@@ -1361,6 +1376,36 @@ __device__ __forceinline__ void run_epilogue_fused(const CdgParams &p, const Rin
             bulk_commit_group();
         }
     };
+    // dX1 of item j: GEMM 2's accumulator in 64-channel chunks; false if the
+    // launch is giving up
+    auto stage_b = [&](uint32_t j, int j0, int i0, int n0) -> bool {
+        const bool okw = wait_bar(B.acc2_full, j & 1u, ctl);
+        if (named_bar_red_or(1, 128, !okw)) return false;
+        tc_fence_after();
+        for (int cc = 0; cc < p.BN2; cc += 64) {
+            uint32_t o[64], pk[32];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                tmem_ld_32x32b_x16(tmem_base + kFusedAcc2 + lane_base + static_cast<uint32_t>(cc) + 16u * q,
+                                   *reinterpret_cast<uint32_t(*)[16]>(&o[16 * q]));
+            tmem_ld_wait();
+            if (cc + 64 >= p.BN2) {  // last read of the accumulator: GEMM 2 of the next item may start
+                tc_fence_before();
+                __syncwarp();
+                if (elected) mbar_arrive(B.acc2_empty);
+            }
+#pragma unroll
+            for (int e = 0; e < 32; ++e) pk[e] = pack2(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1]), IN_T);
+            store_chunk(mapX1, cc, j0, i0, n0, pk);
+        }
+        return true;
+    };
+    // Order: g of item n, then dX1 of item n - 1.  GEMM 2 of item n - 1 runs on
+    // the tensor pipe while this thread makes g of item n, so dX1's chunks
+    // never wait for it, and the stores (the bound) keep flowing.
+    uint32_t n = 0;
+    int pj0 = 0, pi0 = 0, pn0 = 0;  // the previous item's tile origin
+    bool ok = true;
     for (ItemWalk w(tab, p.nphases, S.start, S.step, p.interleave, p.il_items, p.il_round); w.valid(); w.next(), ++n) {
         const CdgPhase &ph = tab[w.phase];
         int j0, i0, n0;
@@ -1368,7 +1413,10 @@ __device__ __forceinline__ void run_epilogue_fused(const CdgParams &p, const Rin
         // ---- g = gate(GEMM 1): accumulator -> registers -> tensor memory (GEMM 2's A)
         bool okw = wait_bar(B.acc1_full0 + 8u * (n & 1u), (n >> 1) & 1u, ctl);
         okw = okw && wait_bar(B.a2_empty0 + 8u * (n & 1u), ((n >> 1) & 1u) ^ 1u, ctl);
-        if (named_bar_red_or(1, 128, !okw)) break;
+        if (named_bar_red_or(1, 128, !okw)) {
+            ok = false;
+            break;
+        }
         tc_fence_after();
         uint32_t xr[32];
         if (GATE) {
@@ -1402,7 +1450,7 @@ __device__ __forceinline__ void run_epilogue_fused(const CdgParams &p, const Rin
             float v[2] = {__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1])};
             if (GATE) {
                 float xp[2];
-                gate_x<IN_T, 2>(v, &xr[e], xp, p.act);
+                gate_x<IN_T, 2, (ACT < 0 ? 0 : ACT)>(v, &xr[e], xp);
             }
             pk[e] = pack2(v[0], v[1], IN_T);
         }
@@ -1412,27 +1460,16 @@ __device__ __forceinline__ void run_epilogue_fused(const CdgParams &p, const Rin
         __syncwarp();
         if (elected) mbar_arrive(B.a2_full0 + 8u * (n & 1u));
         if (p.write_g) store_chunk(mapG, 0, j0, i0, n0, pk);
-        // ---- dX1 tile: GEMM 2's accumulator, in 64-channel chunks
-        okw = wait_bar(B.acc2_full, n & 1u, ctl);
-        if (named_bar_red_or(1, 128, !okw)) break;
-        tc_fence_after();
-        for (int cc = 0; cc < p.BN2; cc += 64) {
-            uint32_t o[64];
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                tmem_ld_32x32b_x16(tmem_base + kFusedAcc2 + lane_base + static_cast<uint32_t>(cc) + 16u * q,
-                                   *reinterpret_cast<uint32_t(*)[16]>(&o[16 * q]));
-            tmem_ld_wait();
-            if (cc + 64 >= p.BN2) {  // last read of the accumulator: GEMM 2 of the next item may start
-                tc_fence_before();
-                __syncwarp();
-                if (elected) mbar_arrive(B.acc2_empty);
-            }
-#pragma unroll
-            for (int e = 0; e < 32; ++e) pk[e] = pack2(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1]), IN_T);
-            store_chunk(mapX1, cc, j0, i0, n0, pk);
+        // ---- dX1 of the previous item
+        if (n >= 1 && !stage_b(n - 1, pj0, pi0, pn0)) {
+            ok = false;
+            break;
         }
+        pj0 = j0;
+        pi0 = i0;
+        pn0 = n0;
     }
+    if (ok && n >= 1) stage_b(n - 1, pj0, pi0, pn0);
     if (GATE && ew == 0 && elected && g_used != g_issued) {
         // left early: let the gate tile still in flight land before the CTA exits
         volatile uint32_t no_abort = 0;
@@ -1444,9 +1481,10 @@ __device__ __forceinline__ void run_epilogue_fused(const CdgParams &p, const Rin
 
 // Shared memory: halo ring | W2 (resident) | W1 (resident) | gate tile | 2 x
 // 16 KB staging | mbarriers, flags | phase and tap tables.
-template <int IN_T, bool GATE>
+template <int IN_T, int ACT>
 __global__ void __launch_bounds__(CDG_THREADS, 1) fused_kernel(const __grid_constant__ CdgParams p)
 {
+    constexpr bool GATE = ACT >= 0;  // ACT: -1 no activation, 0 ReLU, 1 GELU, 2 SiLU
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -1522,7 +1560,7 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) fused_kernel(const __grid_cons
     if (warp == 1) {
         run_mma_fused(p, R, B, tab, taps, ctl, tmem_base, elect_one_sync(), S, w1_smem);
     } else if (warp >= CDG_EPI_WARP0) {
-        run_epilogue_fused<IN_T, GATE>(p, R, B, tab, ctl, tmem_base, S, x2_smem);
+        run_epilogue_fused<IN_T, ACT>(p, R, B, tab, ctl, tmem_base, S, x2_smem);
     } else if (warp == 3) {
         // the 1x1 weights, once per CTA: BN2 rows of 64 channels (128 B) of g
         if (elect_one_sync()) {

@@ -1,7 +1,7 @@
-// The dgrad kernels without the extended epilogue (per-channel sums, activation
-// backward other than ReLU): the plain kernels every default plan launches.
+// The dgrad kernels with the plain epilogue (the ReLU gate or none): what every
+// default plan launches.
 #include "dgrad_variant.cuh"
 
-template cudaError_t cdg_dgrad_prepare_variant<false>(int, int, bool);
-template cudaError_t cdg_dgrad_launch_variant<false>(const CdgParams &, int, int, bool, int, size_t, cudaStream_t);
-template int cdg_dgrad_max_pairs_variant<false>(int, int, bool, size_t);
+template cudaError_t cdg_dgrad_prepare_variant<0>(int, int, bool);
+template cudaError_t cdg_dgrad_launch_variant<0>(const CdgParams &, int, int, bool, int, size_t, cudaStream_t);
+template int cdg_dgrad_max_pairs_variant<0>(int, int, bool, size_t);

@@ -74,24 +74,26 @@ __global__ void channel_sums_kernel(const float *__restrict__ ws, int rows, int 
 cudaError_t cdg_prepare_dgrad(int out_type, int in_type, bool mask, size_t smem)
 {
     if (smem > static_cast<size_t>(CDG_MAX_DYN_SMEM)) return cudaErrorInvalidValue;
-    cudaError_t e = cdg_dgrad_prepare_variant<false>(out_type, in_type, mask);
-    if (e == cudaSuccess) e = cdg_dgrad_prepare_variant<true>(out_type, in_type, mask);
+    cudaError_t e = cdg_dgrad_prepare_variant<0>(out_type, in_type, mask);
+    if (e == cudaSuccess) e = cdg_dgrad_prepare_variant<1>(out_type, in_type, mask);
+    if (e == cudaSuccess) e = cdg_dgrad_prepare_variant<2>(out_type, in_type, mask);
+    if (e == cudaSuccess) e = cdg_dgrad_prepare_variant<3>(out_type, in_type, mask);
     return e;
 }
 
 cudaError_t cdg_launch_dgrad(const CdgParams &p, int out_type, int in_type, bool mask, int grid, size_t smem,
                              cudaStream_t stream)
 {
-    // the extended epilogue only where a plan needs it: per-channel sums, or
-    // an activation other than ReLU
-    if (p.nsum != 0 || p.act != 0)
-        return cdg_dgrad_launch_variant<true>(p, out_type, in_type, mask, grid, smem, stream);
-    return cdg_dgrad_launch_variant<false>(p, out_type, in_type, mask, grid, smem, stream);
+    // each epilogue variant only where a plan needs it
+    if (p.act == 1) return cdg_dgrad_launch_variant<2>(p, out_type, in_type, mask, grid, smem, stream);
+    if (p.act == 2) return cdg_dgrad_launch_variant<3>(p, out_type, in_type, mask, grid, smem, stream);
+    if (p.nsum != 0) return cdg_dgrad_launch_variant<1>(p, out_type, in_type, mask, grid, smem, stream);
+    return cdg_dgrad_launch_variant<0>(p, out_type, in_type, mask, grid, smem, stream);
 }
 
 int cdg_max_active_pairs(int out_type, int in_type, bool mask, size_t smem)
 {
-    return cdg_dgrad_max_pairs_variant<false>(out_type, in_type, mask, smem);
+    return cdg_dgrad_max_pairs_variant<0>(out_type, in_type, mask, smem);
 }
 
 cudaError_t cdg_launch_pack_mask(const void *x, void *bits, long long pixels, int C, int in_type,
@@ -126,21 +128,30 @@ namespace {
 
 typedef void (*FusedFn)(CdgParams);
 
-FusedFn select_fused(int in_type, bool gate)
+// act: -1 no activation between the two dgrads, 0 ReLU, 1 GELU, 2 SiLU
+template <int IN_T>
+FusedFn select_fused_t(int act)
 {
-    if (in_type == CDG_T_F16) return gate ? cdg::fused_kernel<CDG_T_F16, true> : cdg::fused_kernel<CDG_T_F16, false>;
-    return gate ? cdg::fused_kernel<CDG_T_BF16, true> : cdg::fused_kernel<CDG_T_BF16, false>;
+    if (act == 0) return cdg::fused_kernel<IN_T, 0>;
+    if (act == 1) return cdg::fused_kernel<IN_T, 1>;
+    if (act == 2) return cdg::fused_kernel<IN_T, 2>;
+    return cdg::fused_kernel<IN_T, -1>;
+}
+
+FusedFn select_fused(int in_type, int act)
+{
+    return in_type == CDG_T_F16 ? select_fused_t<CDG_T_F16>(act) : select_fused_t<CDG_T_BF16>(act);
 }
 
 }  // namespace
 
-cudaError_t cdg_prepare_fused(int in_type, bool gate)
+cudaError_t cdg_prepare_fused(int in_type, int act)
 {
-    return cudaFuncSetAttribute(reinterpret_cast<const void *>(select_fused(in_type, gate)),
+    return cudaFuncSetAttribute(reinterpret_cast<const void *>(select_fused(in_type, act)),
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, CDG_MAX_DYN_SMEM);
 }
 
-cudaError_t cdg_launch_fused(const CdgParams &p, int in_type, bool gate, int grid, size_t smem, cudaStream_t stream)
+cudaError_t cdg_launch_fused(const CdgParams &p, int in_type, int act, int grid, size_t smem, cudaStream_t stream)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
@@ -156,5 +167,5 @@ cudaError_t cdg_launch_fused(const CdgParams &p, int in_type, bool gate, int gri
     }
     cfg.attrs = attr;
     cfg.numAttrs = n;
-    return cudaLaunchKernelEx(&cfg, select_fused(in_type, gate), p);
+    return cudaLaunchKernelEx(&cfg, select_fused(in_type, act), p);
 }

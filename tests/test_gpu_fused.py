@@ -2,11 +2,21 @@
 oracle's composition (oracle.dgrad_fused): g = act_bwd(dgrad(dY2, W2), x2),
 rounded once to the storage type, then dX1 = dgrad_1x1(g, W1).
 
-dX1 is compared element by element under the usual 16-bit tolerance; g,
-when written, likewise.  Integer inputs make both GEMMs exact, so dX1 must
-equal the oracle's bit for bit (the rounding of g included).  The batch-256
-ResNet-50 stage-1 pair (3x3 64 -> 64 at 56x56, then 1x1 64 -> 256) runs at
-full size, every element of dX1 checked."""
+The comparison follows the two rounding steps:
+  * g (written on request) against the oracle's g under the usual 16-bit
+    element tolerance;
+  * dX1 against the oracle's 1x1 dgrad of the GPU's own g (the same input
+    to the second layer) under the usual tolerance;
+  * dX1 against the oracle's end-to-end dX1 under the usual tolerance plus
+    the sum over the 1x1 filter of ulp(g) * |W1|: g is rounded once to
+    bf16 from an fp32 sum, so an element whose exact value lies within the
+    fp32 error of a rounding boundary may take the neighbouring bf16 value,
+    one unit in the last place away from the oracle's, and that difference
+    passes through the 1x1 layer.
+Integer inputs make both GEMMs exact, so dX1 and g must equal the oracle's
+bit for bit.  The batch-256 ResNet-50 stage-1 pair (3x3 64 -> 64 at 56x56,
+gated by ReLU, then 1x1 64 -> 256) runs at full size, every element of dX1
+checked."""
 import numpy as np
 import pytest
 
@@ -36,6 +46,26 @@ def _inputs(N, H, W, C1, C2, K2, R2, S2, pad2, dil2, dtype, dist, seed, act):
     elif act:
         x2 = synth.to_bits(draw((N, H, W, C2), 2.0), dtype)
     return dY2, W2, W1, x2
+
+
+def bf16_ulp(bits: np.ndarray) -> np.ndarray:
+    """One unit in the last place of each bf16 value (bit patterns), as float64."""
+    e = (bits.astype(np.int64) >> 7) & 0xFF
+    return np.ldexp(1.0, np.maximum(e, 1) - 127 - 7)
+
+
+def end_to_end_bound(g_bits, W1, H, W):
+    """sum over the 1x1 filter of ulp(g) * |W1|, per dX1 element (oracle dgrad)."""
+    absW1 = np.abs(synth.bits_to_f32(W1, "bf16").astype(np.float64))
+    return oracle.dgrad(bf16_ulp(g_bits), absW1, H, W, 1, 0, 1)
+
+
+def assert_fused_close(got, ref, g_bits, W1, H, W, what):
+    extra = end_to_end_bound(g_bits, W1, H, W)
+    err = np.abs(got - ref)
+    bad = ~(err <= 1e-2 * np.maximum(1.0, np.abs(ref)) + extra)
+    assert not bad.any(), (f"{what}: {int(bad.sum())} of {bad.size} out of the bound, "
+                           f"first at {np.argwhere(bad)[:3].tolist()}")
 
 
 def run_fused(geom, dtype="bf16", dist="normal", act="relu", write_g=True, seed=0):
@@ -74,9 +104,12 @@ def test_fused_matches_oracle(geom, act):
     f, (dY2, W2, W1, x2), out, gout = run_fused(geom, act=act, seed=hash((geom, act)) % 1000)
     ref, g_ref = oracle.dgrad_fused(dY2, W2, x2, W1, H, W, pad2, dil2, dtype="bf16", act=act or "relu")
     got = decode_out(out.body().cpu().numpy(), "bf16").reshape(ref.shape)
-    assert_close(got, ref, "bf16", f"dX1 {geom} {act}")
-    g_got = decode_out(gout.body().cpu().numpy(), "bf16").reshape(N, H, W, C2)
+    g_bits = gout.body().cpu().numpy().view(np.uint16).reshape(N, H, W, C2)
+    g_got = synth.bits_to_f32(g_bits, "bf16").astype(np.float64)
     assert_close(g_got, synth.bits_to_f32(g_ref, "bf16").astype(np.float64), "bf16", f"g {geom} {act}")
+    second = oracle.dgrad(np.ascontiguousarray(g_bits), W1, H, W, 1, 0, 1, dtype="bf16")
+    assert_close(got, second, "bf16", f"dX1 against the 1x1 dgrad of the GPU's g {geom} {act}")
+    assert_fused_close(got, ref, g_ref, W1, H, W, f"dX1 end to end {geom} {act}")
 
 
 @pytest.mark.parametrize("geom", CASES[:4], ids=lambda g: "x".join(map(str, g)))
@@ -96,8 +129,9 @@ def test_fused_without_writing_g():
     geom = CASES[0]
     N, H, W, C1, C2, K2, R2, S2, pad2, dil2 = geom
     f, (dY2, W2, W1, x2), out, _ = run_fused(geom, write_g=False)
-    ref, _ = oracle.dgrad_fused(dY2, W2, x2, W1, H, W, pad2, dil2, dtype="bf16")
-    assert_close(decode_out(out.body().cpu().numpy(), "bf16").reshape(ref.shape), ref, "bf16", "dX1 without g")
+    ref, g_ref = oracle.dgrad_fused(dY2, W2, x2, W1, H, W, pad2, dil2, dtype="bf16")
+    assert_fused_close(decode_out(out.body().cpu().numpy(), "bf16").reshape(ref.shape), ref, g_ref, W1, H, W,
+                       "dX1 without g")
 
 
 def test_fused_resnet50_stage1_pair_full_size():
@@ -110,9 +144,10 @@ def test_fused_resnet50_stage1_pair_full_size():
     bits = out.body().view(torch.int16).view(N, -1)
     chunk = 16
     for n0 in range(0, N, chunk):
-        ref, _ = oracle.dgrad_fused(dY2[n0:n0 + chunk], W2, x2[n0:n0 + chunk], W1, H, W, pad2, dil2, dtype="bf16")
+        ref, g_ref = oracle.dgrad_fused(dY2[n0:n0 + chunk], W2, x2[n0:n0 + chunk], W1, H, W, pad2, dil2,
+                                        dtype="bf16")
         got = decode_out(bits[n0:n0 + chunk].cpu().numpy().view(np.uint8), "bf16").reshape(ref.shape)
-        assert_close(got, ref, "bf16", f"dX1 images {n0}..{n0 + chunk - 1}")
+        assert_fused_close(got, ref, g_ref, W1, H, W, f"dX1 images {n0}..{n0 + chunk - 1}")
 
 
 def test_fused_plan_limits():
