@@ -75,6 +75,7 @@ struct PlanOpts {
     int max_bn = 256;     // 128 caps the N tile
     int bn = 0;           // > 0: this N tile (a multiple of 64, or of 128 with the packed mask), if it fits C
     int nacc = 2;         // halo plans: accumulators in flight (2 or 4)
+    int prefetch = 1;     // 0: no L2 prefetch of operand and gate tiles
     int pdl = 1;          // 0 plain launches
 };
 
@@ -184,6 +185,7 @@ PlanOpts opts_from_env()
     o.max_bn = (bn && std::atoi(bn) == 128) ? 128 : 256;
     const char *fbn = std::getenv("CDG_BN");
     o.bn = fbn ? std::atoi(fbn) : 0;
+    o.prefetch = flag("CDG_PREFETCH") == 0 ? 0 : 1;
     const char *na = std::getenv("CDG_NACC");
     o.nacc = (na && std::atoi(na) == 4) ? 4 : 2;
     o.pdl = flag("CDG_PDL") == 0 ? 0 : 1;
@@ -493,6 +495,7 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     // Programmatic dependent launch: the kernel's set-up overlaps the end of the
     // previous kernel in the stream ("0" turns it off).
     p.pdl = opt.pdl == 0 ? 0 : 1;
+    p.prefetch = opt.prefetch == 0 ? 0 : 1;
     p.wait_limit_ns = CDG_WAIT_LIMIT_NS;
     p.withhold_stage = -1;
     p.mask_bits = h->mask_bits ? 1 : 0;

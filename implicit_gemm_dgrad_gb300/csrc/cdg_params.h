@@ -83,6 +83,7 @@ struct CdgParams {  // CUtensorMap members carry their own (128-byte) alignment
     int halo;             // 1: one dY halo box per (tile, K block) serves every tap (see dgrad_sm103.cu)
     int pair;             // 1: CTA pairs (clusters of 2) share 256-row tiles through 2-SM MMAs
     int pdl;              // 1: launch with programmatic stream serialization (host side only)
+    int prefetch;         // 1: operand and gate tiles are prefetched into L2 ahead of their loads
     int mask_bits;        // 1: the gate reads the packed bit mask (rows of 16-byte units per pixel), not x
     int act;              // activation whose backward the gate applies with x: 0 ReLU (select),
                           // 1 GELU (erf form), 2 SiLU (out = dX * f'(x))

@@ -154,6 +154,23 @@ __device__ __forceinline__ void run_loader(const CdgParams &p, const Ring &R, co
     int owner = 0;  // loader index of the current global stage
     int seq = 0;    // sequence number of the current stage (all loaders count every stage)
     const int withhold = p.withhold_stage;
+    // Row-matrix operands (1x1 filters): the dY rows of the stage kPrefetchStages
+    // ahead are prefetched into L2 by the owner of the current stage, so that
+    // the ring's loads find them there (dY is read from DRAM exactly once, and
+    // the ring alone holds too few bytes in flight to cover DRAM latency).
+    constexpr int kPrefetchStages = 8;
+    ItemWalk pw(tab, p.nphases, S.start, S.step, p.interleave, p.il_items, p.il_round);
+    int pkb = 0;
+    auto pf_advance = [&]() {
+        if (!pw.valid()) return;
+        if (++pkb == KB) {
+            pkb = 0;
+            pw.next();
+        }
+    };
+    const bool prefetch = flat && p.prefetch;
+    if (prefetch)
+        for (int i = 0; i < kPrefetchStages; ++i) pf_advance();
     bool ok = true;
     for (ItemWalk w(tab, p.nphases, S.start, S.step, p.interleave, p.il_items, p.il_round); ok && w.valid(); w.next()) {
         const CdgPhase &ph = tab[w.phase];
@@ -177,6 +194,8 @@ __device__ __forceinline__ void run_loader(const CdgParams &p, const Ring &R, co
                         ok = false;
                         break;
                     }
+                    if (prefetch && leader && pw.valid() && tab[pw.phase].tap_count > 0)
+                        tma_prefetch_2d(mapA, pkb * CDG_BK, S.m_tile(pw.local, tiles_n) * m_step);
                     // (test only) a withheld stage gets neither its copies nor
                     // their byte count, and is not recorded for the abort drain:
                     // its full barrier never completes, so the consumer's
@@ -207,6 +226,7 @@ __device__ __forceinline__ void run_loader(const CdgParams &p, const Ring &R, co
                 }
                 if (++owner == nloaders) owner = 0;
                 ++seq;
+                if (prefetch) pf_advance();
                 if (++stage == stages) {
                     stage = 0;
                     parity ^= 1u;
@@ -251,6 +271,21 @@ __device__ __forceinline__ void run_loader_halo(const CdgParams &p, const Ring &
     int a_stage = 0, b_stage = 0, owner = 1;
     uint32_t a_par = 0, b_par = 0;
     bool ok = true;
+    // loader 0 prefetches into L2 the halo box kPrefetchBoxes (tile, K block)
+    // steps ahead of the one it loads (dY comes from DRAM once; the ring holds
+    // only two to four boxes)
+    constexpr int kPrefetchBoxes = 4;
+    ItemWalk pw(tab, p.nphases, S.start, S.step, p.interleave, p.il_items, p.il_round);
+    int pkb = 0;
+    auto pf_advance = [&]() {
+        if (!pw.valid()) return;
+        if (++pkb == KB) {
+            pkb = 0;
+            pw.next();
+        }
+    };
+    if (li == 0)
+        for (int i = 0; i < kPrefetchBoxes; ++i) pf_advance();
     if (p.b_res && li == 1) {
         // every (tap, K block) weight tile of the single N tile, in the order of
         // the tap table (phase by phase), completing on the one weight barrier
@@ -286,8 +321,15 @@ __device__ __forceinline__ void run_loader_halo(const CdgParams &p, const Ring &
                     mbar_arrive_expect_tx(full, tx_a);
                     tma_load_4d(R.a0 + a_stage * R.stage_bytes, mapA, full, kb * CDG_BK, j0 + ph.ds_min,
                                 i0 + ph.dr_min, n0);
+                    if (p.prefetch && pw.valid() && tab[pw.phase].tap_count > 0) {
+                        const CdgPhase &pph = tab[pw.phase];
+                        int pj, pi, pn;
+                        box_origin(pph, S.m_tile(pw.local, tiles_n), wt, bh, 1, pj, pi, pn);
+                        tma_prefetch_4d(mapA, pkb * CDG_BK, pj + pph.ds_min, pi + pph.dr_min, pn);
+                    }
                 }
                 __syncwarp();
+                pf_advance();
                 if (++a_stage == as) {
                     a_stage = 0;
                     a_par ^= 1u;
@@ -579,6 +621,9 @@ struct GateCursor {
 // or item, read from the saved activation (the chunk's channels, laid out as
 // the chunk's output staging) or from the packed mask (the item's bytes of each
 // pixel row).  Completion lands on `bar` (expecting p.gate_tx bytes).
+// With PREFETCH the same box is only prefetched into L2 (no destination, no
+// barrier), further ahead than the loads.
+template <bool PREFETCH>
 __device__ __forceinline__ void gate_issue(const CdgParams &p, const GateCursor &gc, const Sched &S, uint32_t dst,
                                            uint32_t bar)
 {
@@ -587,17 +632,32 @@ __device__ __forceinline__ void gate_issue(const CdgParams &p, const GateCursor 
     const int nt = gc.w.local - (p.tiles_n == 1 ? gc.w.local : gc.w.local / p.tiles_n) * p.tiles_n;
     const int x0 = p.mask_bits ? (p.tiles_n == 1 ? 0 : nt * (p.BN / 8)) : nt * p.BN + gc.cc;
     const uint64_t map = reinterpret_cast<uint64_t>(&p.tmG[gc.w.phase]);
-    mbar_arrive_expect_tx(bar, p.gate_tx);
+    if (!PREFETCH) mbar_arrive_expect_tx(bar, p.gate_tx);
     if (p.d_mode == CDG_D_BOX4) {
         int j0, i0, n0;
         box_origin(ph, mt, max(p.box_w, 1), max(p.box_h, 1), max(p.box_n, 1), j0, i0, n0);
-        tma_load_4d(dst, map, bar, x0, j0, i0, n0);
+        if (PREFETCH)
+            tma_prefetch_4d(map, x0, j0, i0, n0);
+        else
+            tma_load_4d(dst, map, bar, x0, j0, i0, n0);
     } else if (p.d_mode == CDG_D_LINEAR) {
-        tma_load_2d(dst, map, bar, x0, mt * p.m_step);
+        if (PREFETCH)
+            tma_prefetch_2d(map, x0, mt * p.m_step);
+        else
+            tma_load_2d(dst, map, bar, x0, mt * p.m_step);
     } else {
-        tma_load_3d(dst, map, bar, x0, 0, mt * p.rows_per_tile);
+        if (PREFETCH)
+            tma_prefetch_3d(map, x0, 0, mt * p.rows_per_tile);
+        else
+            tma_load_3d(dst, map, bar, x0, 0, mt * p.rows_per_tile);
     }
 }
+
+// Gate tiles are prefetched into L2 this many loads ahead of their loads
+// into shared memory (the loads run only two chunks, or three items, ahead:
+// as far as the staging buffers allow; a gate tile comes from DRAM cold).
+constexpr int kGatePrefetchChunks = 6;
+constexpr int kGatePrefetchItems = 3;
 
 // ReLU-backward gate on PER consecutive values: v = (x > 0) ? v : +0.0 (a
 // select, so masked outputs are +0.0 whatever the accumulator holds).
@@ -652,33 +712,28 @@ __device__ __forceinline__ void gate_relu(float *v, const uint32_t *w)
     }
 }
 
-// Sum PER values per lane over the 32 lanes of a warp: halving exchanges
-// while more than one value is left (lane bit 4, then 3, ... chooses which
-// half a lane keeps), then a butterfly over the remaining lane bits.  Lane l
-// returns the warp's total of value l / (32 / PER); the 32 / PER lanes that
-// share it hold the same sum.  Every lane takes part.
-template <int PER>
-__device__ __forceinline__ float warp_sum_spread(float (&a)[PER], int lane)
+// Column sums of a warp's 32 rows: each lane holds N values (one row), and
+// afterwards lane l holds in a[0 .. N/32) the warp's totals of values
+// (N/32)*l + j.  Five exchange steps with the lane at distance d = 16, 8, 4,
+// 2, 1: a lane keeps the upper half of its current values when its lane bit
+// d is set, the lower half otherwise, and adds the partner's copy of that
+// half.  Each step's N/2, N/4, ... exchanges are independent of one another.
+template <int N>
+__device__ __forceinline__ void warp_transpose_sum(float (&a)[N], int lane)
 {
-    constexpr int LOG = PER == 8 ? 3 : (PER == 4 ? 2 : (PER == 2 ? 1 : 0));
-    static_assert((1 << LOG) == PER, "PER must be 1, 2, 4 or 8");
+    static_assert(N == 32 || N == 64, "a chunk holds 32 or 64 channels");
 #pragma unroll
-    for (int step = 0; step < LOG; ++step) {
+    for (int step = 0; step < 5; ++step) {
         const int d = 16 >> step;
+        const int h = N >> (step + 1);
         const bool upper = (lane & d) != 0;
-        constexpr int n0 = PER / 2;
 #pragma unroll
-        for (int i = 0; i < (n0 >> step); ++i) {
-            const int j = i + (n0 >> step);
-            const float send = upper ? a[i] : a[j];
-            const float keep = upper ? a[j] : a[i];
+        for (int i = 0; i < h; ++i) {
+            const float send = upper ? a[i] : a[i + h];
+            const float keep = upper ? a[i + h] : a[i];
             a[i] = keep + __shfl_xor_sync(0xffffffffu, send, d);
         }
     }
-    float t = a[0];
-#pragma unroll
-    for (int d = 16 >> LOG; d >= 1; d >>= 1) t += __shfl_xor_sync(0xffffffffu, t, d);
-    return t;
 }
 
 __device__ __forceinline__ void st_shared_f32(uint32_t addr, float v)
@@ -779,6 +834,16 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
     const uint32_t grow = static_cast<uint32_t>(p.gate_row_bytes);
     uint32_t g_issued = 0, g_used = 0;  // gate loads issued and waited for (the same count in every thread)
     uint32_t gated_items = 0;
+    // the prefetch cursor runs ahead of gc by the loads' lookahead plus
+    // kGatePrefetch* loads; its issues rotate over the warps like the loads'
+    GateCursor pf{ItemWalk(tab, p.nphases, S.start, S.step, p.interleave, p.il_items, p.il_round), 0};
+    uint32_t pf_issued = 0;
+    auto gate_prefetch = [&]() {
+        if (!p.prefetch || !pf.valid()) return;
+        const uint32_t n = pf_issued++;
+        if (elected && static_cast<uint32_t>(ew) == (n & 3u)) gate_issue<true>(p, pf, S, 0u, 0u);
+        pf.next(mask_bits ? BN : CH, BN);
+    };
     // Gate tiles are loaded by this CTA and always land, so their waits do not
     // give up when another role aborts (only after the time limit): the four
     // warps then never disagree about a gate wait.  The accumulator wait can
@@ -792,11 +857,18 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
         if (!gc.valid()) return;
         const uint32_t n = g_issued++;
         if (elected && static_cast<uint32_t>(ew) == (n & 3u))
-            gate_issue(p, gc, S, gring + (n & 3u) * gslot, R.gfull0 + 8u * (n & 3u));
+            gate_issue<false>(p, gc, S, gring + (n & 3u) * gslot, R.gfull0 + 8u * (n & 3u));
         gc.next(gstep, BN);
+        gate_prefetch();
     };
-    if (MASK)
-        for (int j = 0; j < (mask_bits ? 3 : 2); ++j) gate_ahead();
+    if (MASK) {
+        const int ahead = mask_bits ? 3 : 2;
+        // skip the prefetch cursor past the loads issued at once, then run it
+        // kGatePrefetch* loads further
+        for (int j = 0; j < ahead; ++j) pf.next(mask_bits ? BN : CH, BN);
+        for (int j = 0; j < (mask_bits ? kGatePrefetchItems : kGatePrefetchChunks); ++j) gate_prefetch();
+        for (int j = 0; j < ahead; ++j) gate_ahead();
+    }
     bool ok = true;
     for (ItemWalk w(tab, p.nphases, S.start, S.step, p.interleave, p.il_items, p.il_round); w.valid(); w.next(), ++item_index) {
         const CdgPhase &ph = tab[w.phase];
@@ -904,6 +976,7 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
                 }
             }
             uint32_t r[CH];
+            float xs[EPI != 0 ? CH : 1];  // the chunk's terms of the sum of dX * x (sums plans)
 #pragma unroll
             for (int q = 0; q < CH / 16; ++q)
                 tmem_ld_32x32b_x16(taddr + cc + 16 * q, *reinterpret_cast<uint32_t(*)[16]>(&r[16 * q]));
@@ -945,20 +1018,12 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
                     }
                 }
                 if (nsum) {
-                    // this piece's column sums over the warp's 32 rows, into
-                    // the warp's slot of the chunk's partials
-                    constexpr int SPREAD = 32 / PER;  // lanes that end up with the same channel
-                    float a[PER];
+                    // keep the chunk's gated values (and their products with x)
+                    // for the column sums below; r[] is not read again
 #pragma unroll
-                    for (int e = 0; e < PER; ++e) a[e] = row_ok ? v[e] : 0.0f;
-                    const float t1 = warp_sum_spread<PER>(a, lane);
-                    const uint32_t slot = static_cast<uint32_t>(ew * 64 + PER * q + lane / SPREAD) * 4u;
-                    if (lane % SPREAD == 0) st_shared_f32(R.red0 + slot, t1);
-                    if (nsum == 2) {
-#pragma unroll
-                        for (int e = 0; e < PER; ++e) a[e] = row_ok ? xp[e] : 0.0f;
-                        const float t2 = warp_sum_spread<PER>(a, lane);
-                        if (lane % SPREAD == 0) st_shared_f32(R.red0 + 4u * 64u * 4u + slot, t2);
+                    for (int e = 0; e < PER; ++e) {
+                        r[PER * q + e] = __float_as_uint(row_ok ? v[e] : 0.0f);
+                        if constexpr (EPI != 0) xs[PER * q + e] = row_ok ? xp[e] : 0.0f;
                     }
                 }
                 uint32_t wv[4];
@@ -971,6 +1036,25 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
                 }
                 if (srow >= 0)
                     st_shared_v4(buf + srow_off + ((static_cast<uint32_t>(q) ^ sw) << 4), wv[0], wv[1], wv[2], wv[3]);
+            }
+            if constexpr (EPI != 0) if (nsum) {
+                // the chunk's column sums over this warp's 32 rows into the
+                // warp's slot of the partials: lane l ends with channels
+                // (CH/32)*l + j
+                float t[CH];
+#pragma unroll
+                for (int i = 0; i < CH; ++i) t[i] = __uint_as_float(r[i]);
+                warp_transpose_sum<CH>(t, lane);
+#pragma unroll
+                for (int j = 0; j < CH / 32; ++j)
+                    st_shared_f32(R.red0 + static_cast<uint32_t>(ew * 64 + (CH / 32) * lane + j) * 4u, t[j]);
+                if (nsum == 2) {
+                    warp_transpose_sum<CH>(xs, lane);
+#pragma unroll
+                    for (int j = 0; j < CH / 32; ++j)
+                        st_shared_f32(R.red0 + 4u * 64u * 4u + static_cast<uint32_t>(ew * 64 + (CH / 32) * lane + j) * 4u,
+                                      xs[j]);
+                }
             }
             fence_proxy_async_smem();
             named_bar_sync(1, 128);
@@ -1343,6 +1427,10 @@ __device__ __forceinline__ void run_epilogue_fused(const CdgParams &p, const Rin
     // the gate tile of the next item is loaded into the one gate buffer as
     // soon as every thread has read the current one (issued by warp 0)
     ItemWalk nx(tab, p.nphases, S.start, S.step, p.interleave, p.il_items, p.il_round);
+    // and the tile two items beyond that is prefetched into L2 meanwhile
+    ItemWalk px(tab, p.nphases, S.start, S.step, p.interleave, p.il_items, p.il_round);
+    px.next();
+    px.next();
     uint32_t g_issued = 0, g_used = 0;
     auto gate_issue = [&]() {
         if (!GATE || !nx.valid()) return;
@@ -1352,8 +1440,13 @@ __device__ __forceinline__ void run_epilogue_fused(const CdgParams &p, const Rin
             box_origin(tab[nx.phase], S.m_tile(nx.local, 1), p.halo_wt, p.halo_bh, 1, j0, i0, n0);
             mbar_arrive_expect_tx(B.gate_full, p.gate_tx);
             tma_load_4d(x2_smem, mapGate, B.gate_full, 0, j0, i0, n0);
+            if (p.prefetch && px.valid()) {
+                box_origin(tab[px.phase], S.m_tile(px.local, 1), p.halo_wt, p.halo_bh, 1, j0, i0, n0);
+                tma_prefetch_4d(mapGate, 0, j0, i0, n0);
+            }
         }
         nx.next();
+        px.next();
     };
     gate_issue();
     uint32_t chunk = 0;

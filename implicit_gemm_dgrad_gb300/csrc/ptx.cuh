@@ -96,6 +96,28 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, uint64_t map, uint32_t
         : "memory");
 }
 
+// Tile prefetch into L2 (no shared memory, no barrier): a later tensor load
+// of the same box then finds its bytes in L2 instead of DRAM.
+__device__ __forceinline__ void tma_prefetch_2d(uint64_t map, int x, int y)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map), "r"(x), "r"(y)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_3d(uint64_t map, int x, int y, int z)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(map), "r"(x), "r"(y),
+                 "r"(z)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_4d(uint64_t map, int x, int y, int z, int w)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(map), "r"(x),
+                 "r"(y), "r"(z), "r"(w)
+                 : "memory");
+}
+
 // ---------------------------------------------------------------- TMEM / tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols)
 {
