@@ -21,20 +21,21 @@
 #define CDG_EPI_WARP0 4
 #define CDG_WAIT_LIMIT_NS 4000000000ull  // a pipeline wait gives up after 4 s (default)
 // Shared memory after the operand ring: two 16 KB output staging buffers
-// (128 rows x 128 B, the box a TMA store writes; four when the ReLU-backward
-// gate reads the saved activation, whose chunks land in them ahead of use; two
-// plus a 16 KB ring of mask tiles when it reads the packed mask), then mbarriers and flags
-// (320 B), then the phase and tap tables copied out of the parameter block.
+// (128 rows x 128 B, the box a TMA store writes; six when the ReLU-backward
+// gate reads the saved activation, whose chunks land in them four chunks
+// ahead of use; two plus a 16 KB ring of mask tiles when it reads the packed
+// mask), then mbarriers and flags (384 B), then the phase and tap tables
+// copied out of the parameter block.
 #define CDG_SMEM_STAGING (2 * 128 * 128)
 #define CDG_GATE_SLOT 4096   // one item's packed-mask tile: 128 rows x up to 32 bytes
 #define CDG_GATE_RING (4 * CDG_GATE_SLOT)
 #define CDG_SMEM_TAIL 2048
-#define CDG_SMEM_TABLES 320
+#define CDG_SMEM_TABLES 384
 // Per-channel output sums (plans with CDG_EPI_SUM): after the tail, the four
 // epilogue warps' partial sums of one chunk, [sums][4 warps][64 channels]
 // fp32, then the CTA's accumulators, [sums][C] fp32 (in 128-byte units).
 #define CDG_SMEM_RED (2 * 4 * 64 * 4)
-#define CDG_MAX_STAGES_TOTAL 10  // all ring stages together (their mbarriers live in the 320-byte area)
+#define CDG_MAX_STAGES_TOTAL 10  // all ring stages together (their mbarriers live in the 384-byte area)
 
 // One phase sub-convolution of a (possibly strided) dgrad.  The dX pixels with
 // h = stride*i + ph, w = stride*j + pw (0 <= i < hph, 0 <= j < wph) form the
@@ -84,10 +85,13 @@ struct CdgParams {  // CUtensorMap members carry their own (128-byte) alignment
     int pair;             // 1: CTA pairs (clusters of 2) share 256-row tiles through 2-SM MMAs
     int pdl;              // 1: launch with programmatic stream serialization (host side only)
     int prefetch;         // 1: operand and gate tiles are prefetched into L2 ahead of their loads
+                          // (opt-in, CDG_PREFETCH=1: measured slower on GB300)
     int mask_bits;        // 1: the gate reads the packed bit mask (rows of 16-byte units per pixel), not x
     int act;              // activation whose backward the gate applies with x: 0 ReLU (select),
                           // 1 GELU (erf form), 2 SiLU (out = dX * f'(x))
     int gate_row_bytes;   // bytes of one tile row of a gate load (activation chunk, or mask tile)
+    int gate_bufs;        // gated by the activation: staging buffers (6: its chunks land four chunks
+                          // ahead; 4, where the ring would keep fewer than three stages: two ahead)
     uint32_t gate_tx;     // bytes one gate load delivers (the store box's rows x gate_row_bytes)
     int dual;             // 1: two MMA warps, each with half of the stages and two accumulators
     int interleave;       // >= 2: the first `interleave` phases' items are interleaved (il_items each)

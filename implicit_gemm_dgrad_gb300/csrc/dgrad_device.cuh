@@ -154,10 +154,11 @@ __device__ __forceinline__ void run_loader(const CdgParams &p, const Ring &R, co
     int owner = 0;  // loader index of the current global stage
     int seq = 0;    // sequence number of the current stage (all loaders count every stage)
     const int withhold = p.withhold_stage;
-    // Row-matrix operands (1x1 filters): the dY rows of the stage kPrefetchStages
-    // ahead are prefetched into L2 by the owner of the current stage, so that
-    // the ring's loads find them there (dY is read from DRAM exactly once, and
-    // the ring alone holds too few bytes in flight to cover DRAM latency).
+    // Row-matrix operands (1x1 filters), with p.prefetch: the dY rows of the
+    // stage kPrefetchStages ahead are prefetched into L2 by the owner of the
+    // current stage, so that the ring's loads find them there.  Measured on
+    // GB300 this makes the 1x1 layers slower (the ring already covers the
+    // latency), so plans leave it off unless asked.
     constexpr int kPrefetchStages = 8;
     ItemWalk pw(tab, p.nphases, S.start, S.step, p.interleave, p.il_items, p.il_round);
     int pkb = 0;
@@ -271,9 +272,9 @@ __device__ __forceinline__ void run_loader_halo(const CdgParams &p, const Ring &
     int a_stage = 0, b_stage = 0, owner = 1;
     uint32_t a_par = 0, b_par = 0;
     bool ok = true;
-    // loader 0 prefetches into L2 the halo box kPrefetchBoxes (tile, K block)
-    // steps ahead of the one it loads (dY comes from DRAM once; the ring holds
-    // only two to four boxes)
+    // with p.prefetch (off unless asked: measured slower), loader 0 prefetches
+    // into L2 the halo box kPrefetchBoxes (tile, K block) steps ahead of the
+    // one it loads
     constexpr int kPrefetchBoxes = 4;
     ItemWalk pw(tab, p.nphases, S.start, S.step, p.interleave, p.il_items, p.il_round);
     int pkb = 0;
@@ -653,9 +654,9 @@ __device__ __forceinline__ void gate_issue(const CdgParams &p, const GateCursor 
     }
 }
 
-// Gate tiles are prefetched into L2 this many loads ahead of their loads
-// into shared memory (the loads run only two chunks, or three items, ahead:
-// as far as the staging buffers allow; a gate tile comes from DRAM cold).
+// With p.prefetch (off unless asked: measured slower on GB300), gate tiles
+// are prefetched into L2 this many loads ahead of their loads into shared
+// memory.
 constexpr int kGatePrefetchChunks = 6;
 constexpr int kGatePrefetchItems = 3;
 
@@ -776,8 +777,10 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
     const int d_mode = p.d_mode, m_step = p.m_step, rpt = max(p.rows_per_tile, 1);
     const uint32_t acc_stride = p.acc_stride;
     const bool mask_bits = p.mask_bits != 0;
-    // staging buffers: four when the activation's chunks land in them two chunks ahead
-    const uint32_t nbuf = (MASK && !mask_bits) ? 4u : 2u;
+    // staging buffers: p.gate_bufs (6 or 4) when the activation's chunks land
+    // in them ahead of use (two outputs in flight, the rest gate tiles ahead),
+    // else two
+    const uint32_t nbuf = (MASK && !mask_bits) ? static_cast<uint32_t>(p.gate_bufs) : 2u;
     // tile row -> box position, and the staging row it fills (halo mode: row
     // a*halo_wb + b is output (a, b); padding rows b >= halo_wt are dropped)
     int jl, il, nl, srow;
@@ -820,13 +823,16 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
     uint32_t acc_count[2] = {0u, 0u}, chunk_count = 0;
     uint32_t item_index = 0;
     // Gate inputs arrive by TMA ahead of use: chunk k's activation tile into
-    // staging buffer k % 4 while chunk k - 2 is processed; the mask tile of the
-    // i-th item with taps into ring slot i % 4 three items ahead.  Load n
-    // completes on gate barrier n % 4 (phase n / 4) and is issued by epilogue
-    // warp n % 4 (an issue holds its thread for a few hundred cycles, so one
-    // warp issuing them all would pace the epilogue); every epilogue thread
-    // walks the cursor in step.  For chunk k + 2 that is warp (k - 2) % 4, which
-    // has just seen store k - 2 finish reading the same buffer.
+    // staging buffer k % 6 while chunk k - 4 is processed (its load is issued
+    // once chunk k - 4's own tile has landed and store k - 6, the buffer's
+    // previous user, has finished reading it; with four buffers, k % 4 and
+    // k - 2); the mask tile of the i-th item
+    // with taps into ring slot i % 4 three items ahead.  Load n is issued by
+    // epilogue warp n % 4 (an issue holds its thread for a few hundred cycles,
+    // so one warp issuing them all would pace the epilogue); every epilogue
+    // thread walks the cursor in step.  The x tiles take four chunks of
+    // lookahead because they come from DRAM cold: measured with two, the
+    // x-gated 3x3 stride-2 256-channel layer ran 1.7x its ungated time.
     GateCursor gc{ItemWalk(tab, p.nphases, S.start, S.step, p.interleave, p.il_items, p.il_round), 0};
     const int gstep = mask_bits ? BN : CH;
     const uint32_t gring = mask_bits ? R.gate0 : R.out0;
@@ -853,16 +859,22 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
     // leave them waiting there for good.
     volatile uint32_t gate_no_abort = 0;
     const Ctl gate_ctl{&gate_no_abort, ctl.status, ctl.limit};
+    // Gate load n: the packed mask's tile into ring slot n % 4 on barrier
+    // n % 4; the activation's chunk into staging buffer n % 6 on barrier n % 8
+    // (phase n / 8), so that no barrier is re-armed before its last load was
+    // waited for.
     auto gate_ahead = [&]() {
         if (!gc.valid()) return;
         const uint32_t n = g_issued++;
+        const uint32_t slot = mask_bits ? (n & 3u) : (n % nbuf);
+        const uint32_t bar = mask_bits ? (n & 3u) : (n & 7u);
         if (elected && static_cast<uint32_t>(ew) == (n & 3u))
-            gate_issue<false>(p, gc, S, gring + (n & 3u) * gslot, R.gfull0 + 8u * (n & 3u));
+            gate_issue<false>(p, gc, S, gring + slot * gslot, R.gfull0 + 8u * bar);
         gc.next(gstep, BN);
         gate_prefetch();
     };
     if (MASK) {
-        const int ahead = mask_bits ? 3 : 2;
+        const int ahead = mask_bits ? 3 : static_cast<int>(nbuf) - 2;
         // skip the prefetch cursor past the loads issued at once, then run it
         // kGatePrefetch* loads further
         for (int j = 0; j < ahead; ++j) pf.next(mask_bits ? BN : CH, BN);
@@ -943,10 +955,10 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
         const uint32_t taddr = tmem_base + acc * acc_stride + (static_cast<uint32_t>(quad * 32) << 16);
         for (int cc = 0; cc < BN; cc += CH) {
             const uint32_t k = chunk_count++;
-            const uint32_t buf = R.out0 + (k & (nbuf - 1u)) * (128u * 128u);
+            const uint32_t buf = R.out0 + (nbuf == 2u ? (k & 1u) : (k % nbuf)) * (128u * 128u);
             // the store of chunk k-2 (issued by warp (k-2) % 4) must be done
             // reading its buffer: with two buffers that is this chunk's, with
-            // four it is the one chunk k+2's gate goes into
+            // nbuf it is the one chunk k + nbuf - 2's gate goes into
             if (k >= 2 && elected && static_cast<uint32_t>(ew) == ((k - 2) & 3u)) bulk_wait_group_read<0>();
             named_bar_sync(1, 128);
             uint32_t gw[2] = {0u, 0u};  // packed mask: the chunk's bits 0-31 and 32-63
@@ -958,12 +970,12 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
                     gw[0] = ld_shared_u32(mrow + static_cast<uint32_t>(cc >> 3));
                 }
             } else if (MASK && !mask_bits) {
-                gate_ahead();  // chunk k + 2 into the buffer store k - 2 has finished reading
-                if (!wait_bar(R.gfull0 + 8u * (k & 3u), (k >> 2) & 1u, gate_ctl)) {
+                if (!wait_bar(R.gfull0 + 8u * (k & 7u), (k >> 3) & 1u, gate_ctl)) {
                     ok = false;
                     break;
                 }
                 ++g_used;
+                gate_ahead();  // chunk k + nbuf - 2 into the buffer store k - 2 has finished reading
                 if (OSZ == 4) {
                     // fp32 output: the activation tile holds 64-byte rows; read this
                     // row before any thread writes the wider output over the buffer
@@ -1098,7 +1110,12 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
         // aborted: let the gate loads still in flight land before the CTA exits
         volatile uint32_t no_abort = 0;
         const Ctl drain_ctl{&no_abort, ctl.status, ctl.limit};
-        for (uint32_t n = g_used; n < g_issued; ++n) wait_bar(R.gfull0 + 8u * (n & 3u), (n >> 2) & 1u, drain_ctl);
+        for (uint32_t n = g_used; n < g_issued; ++n) {
+            if (mask_bits)
+                wait_bar(R.gfull0 + 8u * (n & 3u), (n >> 2) & 1u, drain_ctl);
+            else
+                wait_bar(R.gfull0 + 8u * (n & 7u), (n >> 3) & 1u, drain_ctl);
+        }
     }
     if (elected) bulk_wait_group_all();
 }
@@ -1131,11 +1148,12 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_cons
     R.b0 = base + p.a_stages * R.stage_bytes;
     R.b_bytes = p.BN * 128;
     R.out0 = HALO ? R.b0 + (p.b_res ? p.b_res_bytes : p.b_stages * p.halo_tg * R.b_bytes) : base + stages * R.stage_bytes;
-    // gated by the activation: four staging buffers; by the packed mask: two and the mask ring
+    // gated by the activation: p.gate_bufs staging buffers; by the packed mask: two and the mask ring
     R.gate0 = R.out0 + CDG_SMEM_STAGING;
     const uint32_t bars =
-        R.out0 + CDG_SMEM_STAGING + (MASK ? (p.mask_bits ? CDG_GATE_RING : CDG_SMEM_STAGING) : 0u);
-    // mbarriers: full[stages], empty[stages], acc_full[4], acc_empty[4], drain[2], gate[4]
+        R.out0 + CDG_SMEM_STAGING +
+        (MASK ? (p.mask_bits ? CDG_GATE_RING : static_cast<uint32_t>(p.gate_bufs - 2) * (CDG_SMEM_STAGING / 2)) : 0u);
+    // mbarriers: full[stages], empty[stages], acc_full[4], acc_empty[4], drain[2], gate[8]
     R.full0 = bars;
     R.empty0 = bars + 8u * stages;
     R.acc_full0 = bars + 16u * stages;
@@ -1144,12 +1162,12 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_cons
     R.gfull0 = bars + 16u * stages + 80u;
     R.red0 = bars + CDG_SMEM_TAIL;  // only plans with per-channel sums reserve it
     uint8_t *const tail = smem_raw + (bars - raw);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tail + 8 * (2 * stages + 14));
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tail + 8 * (2 * stages + 18));
     volatile uint32_t *abort_flag = tmem_slot + 1;
     volatile uint32_t *slot_parity = tmem_slot + 2;  // [stages] (<= CDG_MAX_STAGES_TOTAL entries)
     CdgPhase *tab = reinterpret_cast<CdgPhase *>(tail + CDG_SMEM_TABLES);
     CdgTap *taps = reinterpret_cast<CdgTap *>(tab + CDG_MAX_PHASES);
-    static_assert(8 * (2 * CDG_MAX_STAGES_TOTAL + 14) + 8 + 4 * CDG_MAX_STAGES_TOTAL <= CDG_SMEM_TABLES,
+    static_assert(8 * (2 * CDG_MAX_STAGES_TOTAL + 18) + 8 + 4 * CDG_MAX_STAGES_TOTAL <= CDG_SMEM_TABLES,
                   "mbarrier area overflows");
     static_assert(CDG_SMEM_TABLES + CDG_MAX_PHASES * sizeof(CdgPhase) + CDG_MAX_TAPS * sizeof(CdgTap) <=
                       CDG_SMEM_TAIL,
@@ -1187,7 +1205,7 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_cons
         }
         mbar_init(R.drain, 1);
         mbar_init(R.drain + 8u, 1);
-        for (int g = 0; g < 4; ++g) mbar_init(R.gfull0 + 8u * g, 1);
+        for (int g = 0; g < 8; ++g) mbar_init(R.gfull0 + 8u * g, 1);
         *abort_flag = 0u;
         for (int s = 0; s < stages; ++s) slot_parity[s] = 0u;
         fence_mbar_init();

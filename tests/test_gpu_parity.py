@@ -226,7 +226,7 @@ def test_mode_cases_reach_their_paths():
 
 
 @pytest.mark.parametrize("env", ["", "CDG_PAIR=0", "CDG_PAIR=1", "CDG_DUAL=0", "CDG_INTERLEAVE=0", "CDG_HALO=0",
-                                 "CDG_PDL=0", "CDG_PREFETCH=0"])
+                                 "CDG_PDL=0", "CDG_PREFETCH=1"])
 @pytest.mark.parametrize("L", MODE_CASES, ids=lambda L: L.name)
 def test_planner_mode_overrides(L, env, monkeypatch):
     """Every planner mode and its override gives the oracle's result."""
