@@ -76,7 +76,7 @@ struct PlanOpts {
     int bn = 0;           // > 0: this N tile (a multiple of 64, or of 128 with the packed mask), if it fits C
     int nacc = 2;         // halo plans: accumulators in flight (2 or 4)
     int prefetch = 0;     // 1: L2 prefetch of operand and gate tiles ahead of their loads (measured slower)
-    int gate_bufs = 6;    // gated by the saved activation: staging buffers (6, or 4)
+    int gate_bufs = 4;    // gated by the saved activation: staging buffers (4; 6 measured slower)
     int pdl = 1;          // 0 plain launches
 };
 
@@ -187,6 +187,8 @@ PlanOpts opts_from_env()
     const char *fbn = std::getenv("CDG_BN");
     o.bn = fbn ? std::atoi(fbn) : 0;
     o.prefetch = flag("CDG_PREFETCH") == 1 ? 1 : 0;
+    const char *gb = std::getenv("CDG_GATE_BUFS");
+    o.gate_bufs = (gb && std::atoi(gb) == 6) ? 6 : 4;
     const char *na = std::getenv("CDG_NACC");
     o.nacc = (na && std::atoi(na) == 4) ? 4 : 2;
     o.pdl = flag("CDG_PDL") == 0 ? 0 : 1;
@@ -312,11 +314,11 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     // per-channel sums: the epilogue warps' partials of a chunk, after the tail
     // and the CTA's per-channel accumulators ([sum][C] fp32)
     const int red_bytes = nsum ? CDG_SMEM_RED + ((nsum * C * 4 + 127) / 128) * 128 : 0;
-    // output staging; gated by the activation: six buffers, its chunks land in
-    // them four chunks ahead of use (four buffers, two ahead, where six would
-    // leave the ring fewer than three stages or cost the halo mode: see
-    // choose_gate_bufs); by the packed mask: a ring of mask tiles besides
-    const int gate_bufs = (h->mask && !h->mask_bits) ? (opt.gate_bufs == 4 ? 4 : 6) : 0;
+    // output staging; gated by the activation: four buffers, its chunks land
+    // in them two chunks ahead of use (six, four ahead, with CDG_GATE_BUFS=6:
+    // measured slower, the ring loses a stage); by the packed mask: a ring of
+    // mask tiles besides
+    const int gate_bufs = (h->mask && !h->mask_bits) ? (opt.gate_bufs == 6 ? 6 : 4) : 0;
     const int staging =
         CDG_SMEM_STAGING + (h->mask ? (h->mask_bits ? CDG_GATE_RING : (gate_bufs - 2) * (CDG_SMEM_STAGING / 2)) : 0);
     const int ring_budget = kMaxSmem - 1024 - staging - CDG_SMEM_TAIL - red_bytes;
@@ -822,29 +824,6 @@ int choose_plan_bn(int N, int H, int W, int C, int K, int R, int S, int stride, 
     return bn;
 }
 
-// Plans gated by the saved activation load its tiles four chunks ahead into
-// six staging buffers, unless that leaves the operand ring fewer than three
-// stages or costs the operand mode four buffers would get (the halo mode's
-// resident weights): then four buffers, two chunks ahead.
-int choose_gate_bufs(int N, int H, int W, int C, int K, int R, int S, int stride, int pad, int dil, int dtype,
-                     int epilogue, int num_sms, const PlanOpts &opt)
-{
-    const int x_gate = CDG_EPI_RELU_BWD | CDG_EPI_GELU_BWD | CDG_EPI_SILU_BWD;
-    if (!(epilogue & x_gate) || opt.gate_bufs == 4) return opt.gate_bufs;
-    cdg_handle_t a = nullptr, b = nullptr;
-    PlanOpts o4 = opt, o6 = opt;
-    o4.gate_bufs = 4;
-    o6.gate_bufs = 6;
-    int bufs = 4;
-    if (make_plan(N, H, W, C, K, R, S, stride, pad, dil, dtype, epilogue, num_sms, true, o6, &a) == CDG_OK &&
-        make_plan(N, H, W, C, K, R, S, stride, pad, dil, dtype, epilogue, num_sms, true, o4, &b) == CDG_OK &&
-        (a->prm.halo || a->prm.stages >= 3) && a->info.a_mode == b->info.a_mode)
-        bufs = 6;
-    cdg_destroy(a);
-    cdg_destroy(b);
-    return bufs;
-}
-
 }  // namespace
 
 extern "C" {
@@ -864,7 +843,6 @@ int cdg_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int pa
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
         return CDG_ERR_CUDA;
     opt.bn = choose_plan_bn(N, H, W, C, K, R, S, stride, pad, dil, dtype, epilogue, sms, opt);
-    opt.gate_bufs = choose_gate_bufs(N, H, W, C, K, R, S, stride, pad, dil, dtype, epilogue, sms, opt);
     return make_plan(N, H, W, C, K, R, S, stride, pad, dil, dtype, epilogue, sms, false, opt, out);
 }
 
@@ -877,7 +855,6 @@ int cdg_plan_host(int N, int H, int W, int C, int K, int R, int S, int stride, i
     }
     PlanOpts opt = opts_from_env();
     opt.bn = choose_plan_bn(N, H, W, C, K, R, S, stride, pad, dil, dtype, epilogue, num_sms, opt);
-    opt.gate_bufs = choose_gate_bufs(N, H, W, C, K, R, S, stride, pad, dil, dtype, epilogue, num_sms, opt);
     return make_plan(N, H, W, C, K, R, S, stride, pad, dil, dtype, epilogue, num_sms, true, opt, out);
 }
 
@@ -1305,6 +1282,7 @@ int fused_make(int N, int H, int W, int C1, int C2, int K2, int R2, int S2, int 
     PlanOpts opt = opts_from_env();
     opt.halo = 1;
     opt.bn = 0;
+    opt.gate_bufs = 4;  // the fused kernel lays out its own shared memory
     cdg_handle_t g = nullptr;
     int rc = make_plan(N, H, W, C2, K2, R2, S2, 1, pad2, dil2, dtype, flags & gates, num_sms, host_only, opt, &g);
     if (rc != CDG_OK) return rc;

@@ -21,8 +21,8 @@
 #define CDG_EPI_WARP0 4
 #define CDG_WAIT_LIMIT_NS 4000000000ull  // a pipeline wait gives up after 4 s (default)
 // Shared memory after the operand ring: two 16 KB output staging buffers
-// (128 rows x 128 B, the box a TMA store writes; six when the ReLU-backward
-// gate reads the saved activation, whose chunks land in them four chunks
+// (128 rows x 128 B, the box a TMA store writes; four (or six) when the
+// ReLU-backward gate reads the saved activation, whose chunks land in them
 // ahead of use; two plus a 16 KB ring of mask tiles when it reads the packed
 // mask), then mbarriers and flags (384 B), then the phase and tap tables
 // copied out of the parameter block.
@@ -90,8 +90,8 @@ struct CdgParams {  // CUtensorMap members carry their own (128-byte) alignment
     int act;              // activation whose backward the gate applies with x: 0 ReLU (select),
                           // 1 GELU (erf form), 2 SiLU (out = dX * f'(x))
     int gate_row_bytes;   // bytes of one tile row of a gate load (activation chunk, or mask tile)
-    int gate_bufs;        // gated by the activation: staging buffers (6: its chunks land four chunks
-                          // ahead; 4, where the ring would keep fewer than three stages: two ahead)
+    int gate_bufs;        // gated by the activation: staging buffers (4: its chunks land two chunks
+                          // ahead; 6 with CDG_GATE_BUFS=6: four ahead, measured slower)
     uint32_t gate_tx;     // bytes one gate load delivers (the store box's rows x gate_row_bytes)
     int dual;             // 1: two MMA warps, each with half of the stages and two accumulators
     int interleave;       // >= 2: the first `interleave` phases' items are interleaved (il_items each)

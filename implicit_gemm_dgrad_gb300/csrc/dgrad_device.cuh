@@ -830,9 +830,8 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
     // with taps into ring slot i % 4 three items ahead.  Load n is issued by
     // epilogue warp n % 4 (an issue holds its thread for a few hundred cycles,
     // so one warp issuing them all would pace the epilogue); every epilogue
-    // thread walks the cursor in step.  The x tiles take four chunks of
-    // lookahead because they come from DRAM cold: measured with two, the
-    // x-gated 3x3 stride-2 256-channel layer ran 1.7x its ungated time.
+    // thread walks the cursor in step.  (Four chunks of lookahead, six
+    // buffers, measured slower on GB300: the operand ring loses a stage.)
     GateCursor gc{ItemWalk(tab, p.nphases, S.start, S.step, p.interleave, p.il_items, p.il_round), 0};
     const int gstep = mask_bits ? BN : CH;
     const uint32_t gring = mask_bits ? R.gate0 : R.out0;
