@@ -150,10 +150,11 @@ def gate_bytes(layer, gate: str) -> int:
 
 
 def wgrad_bytes(layer) -> int:
-    """Algorithmic HBM bytes of one wgrad: dY and the forward input x read
-    once, dW written once (2-byte elements)."""
+    """Algorithmic HBM bytes of one wgrad: dY read once, the forward input x
+    read once where some filter tap reaches it (tap_pixels: a 1x1 stride-2
+    layer uses one pixel in four), dW written once (2-byte elements)."""
     L = layer
-    return 2 * (L.N * L.P * L.Q * L.K + L.N * L.H * L.W * L.C + L.K * L.R * L.S * L.C)
+    return 2 * (L.N * L.P * L.Q * L.K + tap_pixels(L) * L.C + L.K * L.R * L.S * L.C)
 
 
 def tensor_peak(peaks, basis: str) -> float:

@@ -52,13 +52,17 @@ def test_gate_bytes_per_mode():
 
 
 def test_wgrad_bytes():
-    """wgrad reads dY and the forward input once and writes dW once."""
+    """wgrad reads dY once, the forward input once where a tap reaches it,
+    and writes dW once."""
     b = _bench()
-    L = Layer("t", 2, 9, 7, 16, 24, 3, 3, 2, 1, 1)
+    L = Layer("t", 2, 9, 7, 16, 24, 3, 3, 2, 1, 1)  # a 3x3 filter reaches every pixel
     assert b.wgrad_bytes(L) == 2 * (2 * L.P * L.Q * 24 + 2 * 9 * 7 * 16 + 24 * 9 * 16)
     from implicit_gemm_dgrad_gb300.workloads import by_name
     L01 = by_name("L01_1x1_64-64_56")  # 2 x 102.8 MB of activations, a 8 KB filter
     assert abs(b.wgrad_bytes(L01) / 1e6 - 205.5) < 0.1
+    # 1x1 stride 2 (56 -> 28): x is read at the 28 x 28 pixels the filter reaches
+    L10 = by_name("L10_1x1s2_256-512_56-28")
+    assert b.wgrad_bytes(L10) == 2 * (256 * 28 * 28 * 512 + 256 * 28 * 28 * 256 + 512 * 256)
 
 
 def test_peak_basis_follows_the_sampled_clock():
