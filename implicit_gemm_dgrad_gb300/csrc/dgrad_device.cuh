@@ -255,10 +255,17 @@ __device__ __forceinline__ void drain_loads(const Ring &R, int stages, int *stat
 // Loader 0 streams one dY halo box per (tile, K block) into the A ring;
 // loaders 1.. stream the weight tiles, up to tg taps per stage, into the B
 // ring round-robin (or loader 1 loads every weight tile once, when resident).
+// CTA pairs (PAIR): each CTA loads the halo box of its own M tile and its half
+// of every weight tile's rows, and all of them complete on the leader's
+// barriers, which expect the bytes of both CTAs.
+template <bool PAIR>
 __device__ __forceinline__ void run_loader_halo(const CdgParams &p, const Ring &R, const CdgPhase *tab,
                                                 const CdgTap *taps, Ctl ctl, int li, bool leader,
                                                 volatile uint32_t *slot_parity, Sched S)
 {
+    const uint32_t lead_full0 = PAIR ? mapa_shared(R.full0, 0) : R.full0;
+    const uint32_t pair_mul = PAIR ? 2u : 1u;  // the leader's barriers count both CTAs' bytes
+    const int b_row0 = PAIR ? S.rank * (p.BN / 2) : 0;
     const uint64_t mapA = reinterpret_cast<uint64_t>(&p.tmA);
     const uint64_t mapB = reinterpret_cast<uint64_t>(&p.tmB);
     if (leader) {
@@ -293,11 +300,15 @@ __device__ __forceinline__ void run_loader_halo(const CdgParams &p, const Ring &
         const uint32_t full = R.full0 + 8u * as;
         if (leader) {
             slot_parity[as] = 2u;
-            mbar_arrive_expect_tx(full, p.b_res_bytes);
+            if (!PAIR || S.rank == 0) mbar_arrive_expect_tx(full, pair_mul * p.b_res_bytes);
             for (int q = 0; q < p.ntaps; ++q)
-                for (int kb = 0; kb < KB; ++kb)
-                    tma_load_3d(R.b0 + static_cast<uint32_t>(q * KB + kb) * R.b_bytes, mapB, full, kb * CDG_BK, 0,
-                                taps[q].t);
+                for (int kb = 0; kb < KB; ++kb) {
+                    const uint32_t dst = R.b0 + static_cast<uint32_t>(q * KB + kb) * R.b_bytes;
+                    if (PAIR)
+                        tma_load_3d_pair(dst, mapB, lead_full0 + 8u * as, kb * CDG_BK, b_row0, taps[q].t);
+                    else
+                        tma_load_3d(dst, mapB, full, kb * CDG_BK, 0, taps[q].t);
+                }
         }
         __syncwarp();
     }
@@ -319,9 +330,13 @@ __device__ __forceinline__ void run_loader_halo(const CdgParams &p, const Ring &
                 }
                 if (leader) {
                     slot_parity[a_stage] = a_par | 2u;
-                    mbar_arrive_expect_tx(full, tx_a);
-                    tma_load_4d(R.a0 + a_stage * R.stage_bytes, mapA, full, kb * CDG_BK, j0 + ph.ds_min,
-                                i0 + ph.dr_min, n0);
+                    if (!PAIR || S.rank == 0) mbar_arrive_expect_tx(full, pair_mul * tx_a);
+                    if (PAIR)
+                        tma_load_4d_pair(R.a0 + a_stage * R.stage_bytes, mapA, lead_full0 + 8u * a_stage, kb * CDG_BK,
+                                         j0 + ph.ds_min, i0 + ph.dr_min, n0);
+                    else
+                        tma_load_4d(R.a0 + a_stage * R.stage_bytes, mapA, full, kb * CDG_BK, j0 + ph.ds_min,
+                                    i0 + ph.dr_min, n0);
                     if (p.prefetch && pw.valid() && tab[pw.phase].tap_count > 0) {
                         const CdgPhase &pph = tab[pw.phase];
                         int pj, pi, pn;
@@ -350,10 +365,16 @@ __device__ __forceinline__ void run_loader_halo(const CdgParams &p, const Ring &
                         }
                         if (leader) {
                             slot_parity[slot] = b_par | 2u;
-                            mbar_arrive_expect_tx(full, static_cast<uint32_t>(n_in) * R.b_bytes);
-                            for (int i = 0; i < n_in; ++i)
-                                tma_load_3d(R.b0 + b_stage * gstride + static_cast<uint32_t>(i) * R.b_bytes, mapB,
-                                            full, kb * CDG_BK, c0, taps[ph.tap_begin + g0 + i].t);
+                            if (!PAIR || S.rank == 0)
+                                mbar_arrive_expect_tx(full, pair_mul * static_cast<uint32_t>(n_in) * R.b_bytes);
+                            for (int i = 0; i < n_in; ++i) {
+                                const uint32_t dst = R.b0 + b_stage * gstride + static_cast<uint32_t>(i) * R.b_bytes;
+                                if (PAIR)
+                                    tma_load_3d_pair(dst, mapB, lead_full0 + 8u * slot, kb * CDG_BK, c0 + b_row0,
+                                                     taps[ph.tap_begin + g0 + i].t);
+                                else
+                                    tma_load_3d(dst, mapB, full, kb * CDG_BK, c0, taps[ph.tap_begin + g0 + i].t);
+                            }
                         }
                         __syncwarp();
                     }
@@ -370,12 +391,27 @@ __device__ __forceinline__ void run_loader_halo(const CdgParams &p, const Ring &
 
 // Halo-mode MMA issuer: per K block one halo stage; per group of up to tg taps
 // one weight stage (or the resident weights), and per tap four MMAs whose A
-// operand starts at the tap's row of the halo box.
+// operand starts at the tap's row of the halo box.  With CTA pairs (PAIR) the
+// leader issues 2-SM MMAs over both CTAs' halo boxes (the same layout, so the
+// same descriptors) and weight halves, and its commits reach both CTAs.
+template <bool PAIR>
 __device__ __forceinline__ void run_mma_halo(const CdgParams &p, const Ring &R, const CdgPhase *tab,
                                              const CdgTap *taps, Ctl ctl, uint32_t tmem_base, bool leader, Sched S)
 {
+    auto mma = [&](uint32_t d, uint64_t a, uint64_t b, uint32_t acc) {
+        if (PAIR)
+            umma_f16_pair(d, a, b, p.idesc, acc);
+        else
+            umma_f16(d, a, b, p.idesc, acc);
+    };
+    auto commit = [&](uint32_t bar) {
+        if (PAIR)
+            umma_commit_pair(bar);
+        else
+            umma_commit(bar);
+    };
     const int KB = p.KB, as = p.a_stages, bs = p.b_stages, tg = p.halo_tg;
-    const uint32_t idesc = p.idesc, acc_stride = p.acc_stride;
+    const uint32_t acc_stride = p.acc_stride;
     const uint64_t adesc0 = sdesc_k128_sw128(R.a0);
     const uint64_t bdesc0 = sdesc_k128_sw128(R.b0);
     const uint32_t astep = R.stage_bytes >> 4;  // descriptor units per halo stage
@@ -415,7 +451,7 @@ __device__ __forceinline__ void run_mma_halo(const CdgParams &p, const Ring &R, 
                             bdesc0 + static_cast<uint64_t>(static_cast<uint32_t>(tbase + tt * KB) * bunit);
 #pragma unroll
                         for (int k = 0; k < CDG_BK / 16; ++k)
-                            umma_f16(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, (kb | tt | k) != 0);
+                            mma(d_tmem, adesc + 2u * k, bdesc + 2u * k, (kb | tt | k) != 0);
                     }
                     __syncwarp();
                     // the next tap's row offset is read only once this tap's MMAs
@@ -441,14 +477,14 @@ __device__ __forceinline__ void run_mma_halo(const CdgParams &p, const Ring &R, 
                                 bdesc0 + static_cast<uint64_t>(static_cast<uint32_t>(b_stage * tg + i) * bunit);
 #pragma unroll
                             for (int k = 0; k < CDG_BK / 16; ++k)
-                                umma_f16(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, (kb | tt | k) != 0);
+                                mma(d_tmem, adesc + 2u * k, bdesc + 2u * k, (kb | tt | k) != 0);
                         }
                         __syncwarp();
                         // the next tap's row offset is read only once this tap's MMAs
                         // are queued: an outstanding shared-memory load delays MMA issue
                         if (tt + 1 < ntap) hoff = ptap[tt + 1].hoff;
                     }
-                    if (leader) umma_commit(R.empty0 + 8u * slot);
+                    if (leader) commit(R.empty0 + 8u * slot);
                     __syncwarp();
                     if (++b_stage == bs) {
                         b_stage = 0;
@@ -460,7 +496,7 @@ __device__ __forceinline__ void run_mma_halo(const CdgParams &p, const Ring &R, 
                 }
             }
             if (!ok) break;
-            if (leader) umma_commit(R.empty0 + 8u * a_stage);
+            if (leader) commit(R.empty0 + 8u * a_stage);
             __syncwarp();
             if (++a_stage == as) {
                 a_stage = 0;
@@ -468,11 +504,11 @@ __device__ __forceinline__ void run_mma_halo(const CdgParams &p, const Ring &R, 
             }
         }
         if (!ok) break;
-        if (leader) umma_commit(R.acc_full0 + 8u * acc);
+        if (leader) commit(R.acc_full0 + 8u * acc);
         __syncwarp();
         ++acc_count;
     }
-    if (leader) umma_commit(R.drain);
+    if (leader) commit(R.drain);
     __syncwarp();
     volatile uint32_t no_abort = 0;
     const Ctl drain_ctl{&no_abort, ctl.status, ctl.limit};
@@ -1123,6 +1159,7 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
 // MODE: 0 per-tap operand boxes (or row boxes for 1x1 filters), one CTA per
 //         tile, one MMA warp;
 //       1 halo operand mode (weights resident when they fit, else streamed);
+//       4 the halo operand mode with CTA pairs (2-SM MMAs over two halo tiles);
 //       2 per-tap or row boxes, CTA pairs (cluster of 2) sharing 256-row tiles
 //         through tcgen05.mma.cta_group::2: each CTA holds its own 128 rows of
 //         A and half of the weight tile, which halves the B bytes every SM's
@@ -1132,8 +1169,8 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
 template <int OUT_T, bool MASK, int IN_T, int MODE, int EPI>
 __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_constant__ CdgParams p)
 {
-    constexpr bool HALO = MODE == 1;
-    constexpr bool PAIR = MODE == 2;
+    constexpr bool HALO = MODE == 1 || MODE == 4;
+    constexpr bool PAIR = MODE == 2 || MODE == 4;
     constexpr bool DUAL = MODE == 3;  // two MMA warps, each with its own ring and accumulators
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -1145,7 +1182,7 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_cons
     R.a0 = base;
     R.stage_bytes = p.a_stage_bytes;
     R.b0 = base + p.a_stages * R.stage_bytes;
-    R.b_bytes = p.BN * 128;
+    R.b_bytes = (PAIR ? p.BN / 2 : p.BN) * 128;  // halo mode: this CTA's rows of one weight tile
     R.out0 = HALO ? R.b0 + (p.b_res ? p.b_res_bytes : p.b_stages * p.halo_tg * R.b_bytes) : base + stages * R.stage_bytes;
     // gated by the activation: p.gate_bufs staging buffers; by the packed mask: two and the mask ring
     R.gate0 = R.out0 + CDG_SMEM_STAGING;
@@ -1262,9 +1299,9 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_cons
                               slot_parity + j * (stages / 2), sched_of(j));
         }
     } else if (warp == 1) {
-        if (HALO) {
-            run_mma_halo(p, R, tab, taps, ctl, tmem_base, elect_one_sync(), S);
-        } else if (!PAIR || S.rank == 0) {
+        if (HALO && (!PAIR || S.rank == 0)) {
+            run_mma_halo<PAIR>(p, R, tab, taps, ctl, tmem_base, elect_one_sync(), S);
+        } else if (!HALO && (!PAIR || S.rank == 0)) {
             run_mma<PAIR>(p, R, tab, ctl, tmem_base, elect_one_sync(), S);
         } else {
             // the leader issues the pair's MMAs; wait until they are all done
@@ -1275,7 +1312,7 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_cons
     } else if (warp >= CDG_EPI_WARP0) {
         run_epilogue<OUT_T, MASK, IN_T, HALO, PAIR, false, EPI>(p, R, tab, ctl, tmem_base, S);
     } else if (HALO) {
-        run_loader_halo(p, R, tab, taps, ctl, warp == 0 ? 0 : warp - 1, elect_one_sync(), slot_parity, S);
+        run_loader_halo<PAIR>(p, R, tab, taps, ctl, warp == 0 ? 0 : warp - 1, elect_one_sync(), slot_parity, S);
     } else {
         run_loader<PAIR>(p, R, tab, taps, ctl, warp == 0 ? 0 : warp - 1, CDG_LOADERS, elect_one_sync(), slot_parity,
                          S);
@@ -1680,7 +1717,7 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) fused_kernel(const __grid_cons
         }
         __syncwarp();
     } else {
-        run_loader_halo(p, R, tab, taps, ctl, warp == 0 ? 0 : 1, elect_one_sync(), slot_parity, S);
+        run_loader_halo<false>(p, R, tab, taps, ctl, warp == 0 ? 0 : 1, elect_one_sync(), slot_parity, S);
     }
     __syncthreads();
     if (*abort_flag && threadIdx.x == 0) {

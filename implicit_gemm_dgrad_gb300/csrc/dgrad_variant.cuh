@@ -17,6 +17,7 @@ DgradFn pick_mode(int mode)
     if (mode == 1) return cdg::dgrad_kernel<OUT_T, MASK, IN_T, 1, EPI>;
     if (mode == 2) return cdg::dgrad_kernel<OUT_T, MASK, IN_T, 2, EPI>;
     if (mode == 3) return cdg::dgrad_kernel<OUT_T, MASK, IN_T, 3, EPI>;
+    if (mode == 4) return cdg::dgrad_kernel<OUT_T, MASK, IN_T, 4, EPI>;
     return cdg::dgrad_kernel<OUT_T, MASK, IN_T, 0, EPI>;
 }
 
@@ -48,7 +49,7 @@ DgradFn select_kernel(int out_type, int in_type, bool mask, int mode)
 template <int EPI>
 cudaError_t cdg_dgrad_prepare_variant(int out_type, int in_type, bool mask)
 {
-    for (int mode = 0; mode < 4; ++mode) {
+    for (int mode = 0; mode < 5; ++mode) {
         DgradFn fn = select_kernel<EPI>(out_type, in_type, mask, mode);
         if (!fn) return cudaSuccess;  // no such variant for these types (activation without gate)
         const cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void *>(fn),
@@ -62,7 +63,7 @@ template <int EPI>
 cudaError_t cdg_dgrad_launch_variant(const CdgParams &p, int out_type, int in_type, bool mask, int grid, size_t smem,
                                      cudaStream_t stream)
 {
-    const int mode = p.halo ? 1 : (p.pair ? 2 : (p.dual ? 3 : 0));
+    const int mode = p.halo ? (p.pair ? 4 : 1) : (p.pair ? 2 : (p.dual ? 3 : 0));
     DgradFn fn = select_kernel<EPI>(out_type, in_type, mask, mode);
     if (!fn) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};

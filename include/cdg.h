@@ -245,7 +245,8 @@ int cdg_plan_withhold_load_for_test(cdg_handle_t h, int stage);
  * cuDNN's Get and Find algorithm selection): run the dgrad of this plan's shape
  * under each configuration the planner can produce for it (the planner's own
  * choice; without or with CTA pairs; one MMA warp; with or without halo
- * operand boxes; phases in order; 128-channel N tiles), reps timed launches
+ * operand boxes; halo boxes with CTA pairs; phases in order; 128- and
+ * 192-channel N tiles), reps timed launches
  * each after one untimed launch, and keep the fastest in the handle
  * (cdg_plan_get_info then reports it, with tuned = 1).  Configurations that
  * come out identical are timed once.  Each timed launch follows a write of a

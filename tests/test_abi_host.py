@@ -165,17 +165,66 @@ def test_workload_plans():
 
 def test_halo_resident_weights_when_the_filter_fits(monkeypatch):
     """A filter whose packed weights for the one N tile fit beside two halo
-    stages is kept resident with halo operand boxes (a_mode 3, the default);
-    a larger one uses per-tap boxes by default (a_mode 0) and streamed halo
-    weights only when asked (a_mode 2); CDG_HALO=0 turns halo mode off."""
+    stages is kept resident with halo operand boxes (a_mode 3, the default).
+    A stride-1 filter that fits only as halves (N tile of 128 channels or
+    more) is kept resident by CTA pairs, half in each CTA.  Otherwise the
+    default is per-tap boxes (a_mode 0), with streamed halo weights only when
+    asked (a_mode 2).  CDG_HALO=0 turns halo mode off, and CDG_PAIR=0 the pairs."""
     monkeypatch.delenv("CDG_HALO", raising=False)
+    monkeypatch.delenv("CDG_PAIR", raising=False)
     small = cdg.plan_host(256, 56, 56, 64, 64, 3, 3, 1, 1, 1, "bf16", num_sms=148).info()
-    assert small["a_mode"] == 3 and small["smem_bytes"] <= 232448
+    assert small["a_mode"] == 3 and small["cta_pair"] == 0 and small["smem_bytes"] <= 232448
+    halves = cdg.plan_host(256, 28, 28, 128, 128, 3, 3, 1, 1, 1, "bf16", num_sms=148).info()
+    assert halves["a_mode"] == 3 and halves["cta_pair"] == 1 and halves["smem_bytes"] <= 232448
+    # strided, or too large even as halves: per-tap boxes
+    assert cdg.plan_host(256, 56, 56, 128, 128, 3, 3, 2, 1, 1, "bf16", num_sms=148).info()["a_mode"] == 0
+    assert cdg.plan_host(256, 14, 14, 256, 256, 3, 3, 1, 1, 1, "bf16", num_sms=148).info()["a_mode"] == 0
+    # gated by the saved activation: four staging buffers leave no room for the halves
+    gated = cdg.plan_host(256, 28, 28, 128, 128, 3, 3, 1, 1, 1, "bf16", relu=True, num_sms=148).info()
+    assert gated["a_mode"] == 0
+    monkeypatch.setenv("CDG_PAIR", "0")
     assert cdg.plan_host(256, 28, 28, 128, 128, 3, 3, 1, 1, 1, "bf16", num_sms=148).info()["a_mode"] == 0
+    monkeypatch.delenv("CDG_PAIR")
     monkeypatch.setenv("CDG_HALO", "1")
-    assert cdg.plan_host(256, 28, 28, 128, 128, 3, 3, 1, 1, 1, "bf16", num_sms=148).info()["a_mode"] == 2
+    info = cdg.plan_host(256, 28, 28, 128, 128, 3, 3, 1, 1, 1, "bf16", num_sms=148).info()
+    assert info["a_mode"] == 2 and info["cta_pair"] == 0
     monkeypatch.setenv("CDG_HALO", "0")
     assert cdg.plan_host(256, 56, 56, 64, 64, 3, 3, 1, 1, 1, "bf16", num_sms=148).info()["a_mode"] == 0
+    assert cdg.plan_host(256, 28, 28, 128, 128, 3, 3, 1, 1, 1, "bf16", num_sms=148).info()["a_mode"] == 0
+
+
+def test_four_accumulators_only_where_they_fit_tensor_memory(monkeypatch):
+    """CDG_NACC=4 asks halo plans for four accumulators; N tiles over 128
+    channels keep two, so no plan asks for more than the 512 TMEM columns."""
+    monkeypatch.setenv("CDG_HALO", "1")
+    monkeypatch.setenv("CDG_NACC", "4")
+    for pair in ("0", "1"):
+        monkeypatch.setenv("CDG_PAIR", pair)
+        for C in (64, 128, 192, 256, 320, 520):
+            for shape in ((256, 14, 14, C, C, 3, 3, 1, 1, 1), (8, 28, 28, C, 64, 3, 3, 2, 1, 1)):
+                info = cdg.plan_host(*shape, "bf16", num_sms=152).info()
+                assert info["tmem_cols"] <= 512, (shape, pair, info)
+                assert info["tmem_cols"] in (32, 64, 128, 256, 512)
+
+
+def test_halo_boxes_with_cta_pairs_when_asked(monkeypatch):
+    """CDG_HALO=1 with CDG_PAIR=1 gives halo boxes with CTA pairs (N tiles of
+    64 channels or more) wherever the geometry allows: resident halves where
+    half of the filter fits, else streamed weight halves."""
+    monkeypatch.setenv("CDG_HALO", "1")
+    monkeypatch.setenv("CDG_PAIR", "1")
+    info = cdg.plan_host(256, 28, 28, 128, 128, 3, 3, 1, 1, 1, "bf16", num_sms=152).info()
+    assert info["a_mode"] == 3 and info["cta_pair"] == 1
+    assert info["smem_bytes"] <= 232448 and info["grid"] % 2 == 0
+    info = cdg.plan_host(256, 14, 14, 256, 256, 3, 3, 1, 1, 1, "bf16", num_sms=152).info()
+    assert info["a_mode"] == 2 and info["cta_pair"] == 1
+    info = cdg.plan_host(256, 28, 28, 256, 256, 3, 3, 2, 1, 1, "bf16", num_sms=152).info()
+    assert info["a_mode"] == 2 and info["cta_pair"] == 1
+    # 64-channel N tiles pair too (32 weight rows per CTA); narrower ones never
+    info = cdg.plan_host(256, 56, 56, 64, 64, 3, 3, 1, 1, 1, "bf16", num_sms=152).info()
+    assert info["a_mode"] == 3 and info["cta_pair"] == 1 and info["tile_n"] == 64
+    info = cdg.plan_host(2, 10, 10, 48, 48, 3, 3, 1, 1, 1, "bf16", num_sms=152).info()
+    assert info["tile_n"] < 64 and info["cta_pair"] == 0
 
 
 @pytest.mark.parametrize("x,bits,pixels,C,dtype,expect", [

@@ -167,17 +167,45 @@ def test_interleaved_plans():
 
 
 @pytest.mark.parametrize("nacc", ["2", "4"])
-@pytest.mark.parametrize("L", [SWEEP[0], SWEEP[1], SWEEP[4], SWEEP[5], SWEEP[12], SWEEP[14], BATCH8[0]],
+@pytest.mark.parametrize("L", [SWEEP[0], SWEEP[1], SWEEP[4], SWEEP[5], SWEEP[10], SWEEP[12], SWEEP[14], BATCH8[0]],
                          ids=lambda L: L.name)
 def test_halo_operand_mode(L, nacc, monkeypatch):
     """The halo operand mode (one dY box per tile and K block serves every
     tap; weights streamed per tap, or resident when the whole filter of a
     single N tile fits) gives the same results, with two or four
-    accumulators in flight."""
+    accumulators in flight (four only for N tiles up to 128 channels: wider
+    ones would need more than the 512 TMEM columns, and keep two)."""
     monkeypatch.setenv("CDG_HALO", "1")
     monkeypatch.setenv("CDG_NACC", nacc)
     run, _, _ = check_layer(L)
     assert run.plan.info()["a_mode"] in (2, 3)
+
+
+# halo boxes with CTA pairs (opt-in: CDG_HALO=1 CDG_PAIR=1): resident weight
+# halves (a 3x3 128 -> 128 filter, twice what one CTA holds), streamed weight
+# halves with an odd tile count (the partner tile lies out of range), four
+# stride-2 phases under the ReLU gate, several N tiles, fp32 output
+HALO_PAIR_CASES = [
+    (_case(2, 28, 28, 128, 128, 3, 3, 1, 1, 1, "bf16", idx=30), {"a_mode": 3, "cta_pair": 1}),
+    (_case(1, 9, 9, 256, 128, 3, 3, 1, 1, 1, "bf16", idx=31), {"a_mode": 2, "cta_pair": 1}),
+    (_case(2, 14, 14, 128, 64, 3, 3, 2, 1, 1, "f16", relu=True, idx=32), {"cta_pair": 1}),
+    (_case(1, 30, 30, 520, 64, 3, 3, 1, 1, 1, "bf16", idx=33), {"a_mode": 2, "cta_pair": 1}),
+    (_case(2, 10, 10, 128, 48, 3, 3, 1, 1, 1, "f16", out="f32", idx=34), {"cta_pair": 1}),
+]
+
+
+@pytest.mark.parametrize("L,reach", HALO_PAIR_CASES, ids=lambda v: v.name if isinstance(v, Layer) else None)
+def test_halo_operand_mode_with_cta_pairs(L, reach, monkeypatch):
+    """Halo boxes with CTA pairs: each CTA of a pair loads its own tile's halo
+    box and half of every weight tile, and the leader's 2-SM MMAs cover both
+    tiles; the result is the oracle's."""
+    monkeypatch.setenv("CDG_HALO", "1")
+    monkeypatch.setenv("CDG_PAIR", "1")
+    run, _, _ = check_layer(L)
+    info = run.plan.info()
+    assert info["a_mode"] in (2, 3)
+    for k, v in reach.items():
+        assert info[k] == v, (k, info)
 
 
 def test_chained_launches_keep_stream_order():
@@ -230,8 +258,8 @@ def test_mode_cases_reach_their_paths():
 @pytest.mark.parametrize("L", MODE_CASES, ids=lambda L: L.name)
 def test_planner_mode_overrides(L, env, monkeypatch):
     """Every planner mode and its override gives the oracle's result."""
-    if env:
-        key, val = env.split("=")
+    for kv in env.split():
+        key, val = kv.split("=")
         monkeypatch.setenv(key, val)
     check_layer(L)
 
@@ -322,6 +350,8 @@ GATE_CASES = [
     (_case(2, 13, 13, 64, 64, 1, 1, 2, 0, 1, "f16", relu=True, idx=16), "", {"a_mode": 0}),    # 4-D boxes, zero phases
     (_case(2, 20, 20, 64, 64, 3, 3, 1, 1, 1, "bf16", relu=True, idx=17), "", {"a_mode": 3}),   # halo, resident weights
     (_case(2, 12, 12, 128, 128, 3, 3, 1, 1, 1, "bf16", relu=True, idx=18), "CDG_HALO=1", {"a_mode": 2}),
+    (_case(2, 12, 12, 128, 128, 3, 3, 1, 1, 1, "bf16", relu=True, idx=23), "CDG_HALO=1 CDG_PAIR=1",
+     {"cta_pair": 1}),
     (_case(2, 14, 14, 256, 256, 3, 3, 1, 1, 1, "bf16", relu=True, idx=19), "", {"cta_pair": 1}),
     (_case(4, 16, 16, 128, 256, 3, 3, 2, 1, 1, "bf16", relu=True, idx=20), "", {"mma_warps": 2}),
     (_case(2, 10, 10, 96, 48, 3, 3, 1, 1, 1, "f16", out="f32", relu=True, idx=21), "", {}),
@@ -335,8 +365,8 @@ def test_gate_in_every_mode(L, env, reach, gate, monkeypatch):
     """The fused ReLU-backward gate, from the saved activation or its packed
     mask, gives the oracle's result and +0.0 exactly where x <= 0 in every
     operand, tile and issue mode."""
-    if env:
-        key, val = env.split("=")
+    for kv in env.split():
+        key, val = kv.split("=")
         monkeypatch.setenv(key, val)
     if gate == "x":
         run, _, _ = check_layer(L)
@@ -357,8 +387,8 @@ def test_activation_backward_in_every_mode(L, env, reach, act, monkeypatch):
     import torch
     import implicit_gemm_dgrad_gb300 as cdg
     from gpu_util import GuardedOutput, to_dev
-    if env:
-        key, val = env.split("=")
+    for kv in env.split():
+        key, val = kv.split("=")
         monkeypatch.setenv(key, val)
     dY, W, _ = synth.make_inputs(L.shape(), L.dtype, L.dist, L.workload, L.index)
     rng = np.random.default_rng(1000 + L.index)
