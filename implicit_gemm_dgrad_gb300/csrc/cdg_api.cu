@@ -78,6 +78,7 @@ struct PlanOpts {
     int prefetch = 0;     // 1: L2 prefetch of operand and gate tiles ahead of their loads (measured slower)
     int gate_bufs = 4;    // gated by the saved activation: staging buffers (4; 6 measured slower)
     int pdl = 1;          // 0 plain launches
+    int max_grid = 0;     // > 0: at most this many CTAs (tests: many work items per CTA on small problems)
 };
 
 struct cdg_plan_st {
@@ -161,6 +162,7 @@ int choose_bn(int C, int max_bn, int step)
 void apply_grid(cdg_plan_st *h, int grid)
 {
     CdgParams &p = h->prm;
+    if (h->opts.max_grid > 0) grid = std::min(grid, std::max(p.pair ? 2 : 1, p.pair ? h->opts.max_grid & ~1 : h->opts.max_grid));
     h->grid = grid;
     h->info.grid = grid;
     const int G = p.pair ? grid / 2 : grid;
@@ -180,7 +182,7 @@ PlanOpts opts_from_env()
     };
     o.halo = flag("CDG_HALO");
     o.pair = flag("CDG_PAIR");
-    o.dual = flag("CDG_DUAL") == 0 ? 0 : -1;
+    o.dual = flag("CDG_DUAL");
     o.interleave = flag("CDG_INTERLEAVE") == 0 ? 0 : -1;
     const char *bn = std::getenv("CDG_MAX_BN");
     o.max_bn = (bn && std::atoi(bn) == 128) ? 128 : 256;
@@ -192,6 +194,8 @@ PlanOpts opts_from_env()
     const char *na = std::getenv("CDG_NACC");
     o.nacc = (na && std::atoi(na) == 4) ? 4 : 2;
     o.pdl = flag("CDG_PDL") == 0 ? 0 : 1;
+    const char *mg = std::getenv("CDG_MAX_GRID");
+    o.max_grid = mg ? std::max(0, std::atoi(mg)) : 0;
     return o;
 }
 
@@ -473,8 +477,20 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     // tensor work); with two, the other warp's MMAs fill that gap.  Tiles of
     // fewer than four stages gain nothing (the epilogue dominates them).
     bool dual = !halo && !pair && BN <= 128 && max_stages >= 4 && stages_per_tile >= 4.0;
+    // Halo boxes with resident weights: two MMA warps take alternate items
+    // from the one halo ring, so that one warp's per-tile hand-offs (commits,
+    // item bookkeeping, barrier waits: ~1,400 cycles a tile, measured with a
+    // cycle-counter trace) overlap the other's MMAs.  Measured on GB300: the
+    // 3x3 64 -> 64 layer at 56x56 79.7 -> 57.8 us; the 128-channel layer in
+    // CTA pairs unchanged.  (Each warp has full barriers of its own for the
+    // halo stages: at most six halo stages keep every barrier within the
+    // kernel's 384-byte area.)
+    if (halo && b_res && BN <= 128 && a_stages >= 2 && opt.dual != 0) {
+        dual = true;
+        a_stages = std::min(a_stages, 6);
+    }
     if (opt.dual == 0) dual = false;
-    const int stages = dual ? (max_stages / 2) * 2 : max_stages;
+    const int stages = dual && !halo ? (max_stages / 2) * 2 : (halo ? a_stages + b_stages : max_stages);
     const int ring_bytes = halo ? a_stages * hrows * 128 + (b_res ? b_res_bytes : b_stages * halo_tg * b_rows * 128)
                                 : stages * stage_bytes;
     // two accumulators per MMA warp, each at least as wide as the 64-column
@@ -1307,6 +1323,7 @@ int fused_make(int N, int H, int W, int C1, int C2, int K2, int R2, int S2, int 
     opt.halo = 1;
     opt.bn = 0;
     opt.gate_bufs = 4;  // the fused kernel lays out its own shared memory
+    opt.dual = 0;       // and issues its MMAs from one warp
     cdg_handle_t g = nullptr;
     int rc = make_plan(N, H, W, C2, K2, R2, S2, 1, pad2, dil2, dtype, flags & gates, num_sms, host_only, opt, &g);
     if (rc != CDG_OK) return rc;

@@ -258,7 +258,10 @@ __device__ __forceinline__ void drain_loads(const Ring &R, int stages, int *stat
 // CTA pairs (PAIR): each CTA loads the halo box of its own M tile and its half
 // of every weight tile's rows, and all of them complete on the leader's
 // barriers, which expect the bytes of both CTAs.
-template <bool PAIR>
+// Two MMA warps (DUALH): the halo box of the n-th item with taps completes on
+// the full barrier of its stage for MMA warp n % 2: stage s for warp 0,
+// a_stages + b_stages + s for warp 1.
+template <bool PAIR, bool DUALH = false>
 __device__ __forceinline__ void run_loader_halo(const CdgParams &p, const Ring &R, const CdgPhase *tab,
                                                 const CdgTap *taps, Ctl ctl, int li, bool leader,
                                                 volatile uint32_t *slot_parity, Sched S)
@@ -312,6 +315,8 @@ __device__ __forceinline__ void run_loader_halo(const CdgParams &p, const Ring &
         }
         __syncwarp();
     }
+    uint32_t n_item = 0;             // items with taps so far (two MMA warps: item n is warp n % 2's)
+    uint32_t wpar[2] = {0u, 0u};     // two MMA warps: parity bit per stage of each warp's full barriers
     for (ItemWalk w(tab, p.nphases, S.start, S.step, p.interleave, p.il_items, p.il_round); ok && w.valid(); w.next()) {
         const CdgPhase &ph = tab[w.phase];
         const int ntap = ph.tap_count;
@@ -321,18 +326,24 @@ __device__ __forceinline__ void run_loader_halo(const CdgParams &p, const Ring &
         int j0, i0, n0;
         box_origin(ph, mt, wt, bh, 1, j0, i0, n0);
         const int c0 = nt * BN;
+        const uint32_t wj = DUALH ? (n_item & 1u) : 0u;
+        ++n_item;
         for (int kb = 0; ok && kb < KB; ++kb) {
             if (li == 0) {
-                const uint32_t full = R.full0 + 8u * a_stage;
+                // this stage's full barrier (two MMA warps: the item's warp's own)
+                const int fidx = wj ? as + bs + a_stage : a_stage;
+                const uint32_t fpar = DUALH ? (wpar[wj] >> a_stage) & 1u : a_par;
+                if (DUALH) wpar[wj] ^= 1u << a_stage;
+                const uint32_t full = R.full0 + 8u * fidx;
                 if (!wait_bar(R.empty0 + 8u * a_stage, a_par ^ 1u, ctl)) {
                     ok = false;
                     break;
                 }
                 if (leader) {
-                    slot_parity[a_stage] = a_par | 2u;
+                    slot_parity[fidx] = fpar | 2u;
                     if (!PAIR || S.rank == 0) mbar_arrive_expect_tx(full, pair_mul * tx_a);
                     if (PAIR)
-                        tma_load_4d_pair(R.a0 + a_stage * R.stage_bytes, mapA, lead_full0 + 8u * a_stage, kb * CDG_BK,
+                        tma_load_4d_pair(R.a0 + a_stage * R.stage_bytes, mapA, lead_full0 + 8u * fidx, kb * CDG_BK,
                                          j0 + ph.ds_min, i0 + ph.dr_min, n0);
                     else
                         tma_load_4d(R.a0 + a_stage * R.stage_bytes, mapA, full, kb * CDG_BK, j0 + ph.ds_min,
@@ -394,9 +405,14 @@ __device__ __forceinline__ void run_loader_halo(const CdgParams &p, const Ring &
 // operand starts at the tap's row of the halo box.  With CTA pairs (PAIR) the
 // leader issues 2-SM MMAs over both CTAs' halo boxes (the same layout, so the
 // same descriptors) and weight halves, and its commits reach both CTAs.
-template <bool PAIR>
+// With two MMA warps (DUALH; resident weights only) warp j takes the items
+// at positions j, j + 2, ... of the CTA's walk (S as given), and the halo
+// stages of those items: the ring is filled in item order by one loader, so
+// stage n (n = item position x KB + K block) is the warp's when its item is.
+template <bool PAIR, bool DUALH = false>
 __device__ __forceinline__ void run_mma_halo(const CdgParams &p, const Ring &R, const CdgPhase *tab,
-                                             const CdgTap *taps, Ctl ctl, uint32_t tmem_base, bool leader, Sched S)
+                                             const CdgTap *taps, Ctl ctl, uint32_t tmem_base, bool leader, Sched S,
+                                             int j = 0)
 {
     auto mma = [&](uint32_t d, uint64_t a, uint64_t b, uint32_t acc) {
         if (PAIR)
@@ -417,6 +433,19 @@ __device__ __forceinline__ void run_mma_halo(const CdgParams &p, const Ring &R, 
     const uint32_t astep = R.stage_bytes >> 4;  // descriptor units per halo stage
     int a_stage = 0, b_stage = 0;
     uint32_t a_par = 0, b_par = 0, acc_count = 0;
+    // advance the halo-stage cursor by n stages
+    auto a_skip = [&](int n) {
+        for (int i = 0; i < n; ++i)
+            if (++a_stage == as) {
+                a_stage = 0;
+                a_par ^= 1u;
+            }
+    };
+    if (DUALH) a_skip(j * KB);  // warp 1's first item is the CTA's second
+    // two MMA warps: this warp's full barriers (stage s: s, or a_stages +
+    // b_stages + s for warp 1) and their parities, one bit per stage
+    const uint32_t full_w = R.full0 + (DUALH && j ? 8u * static_cast<uint32_t>(as + bs) : 0u);
+    uint32_t wpar = 0u;
     bool ok = true;
     bool b_ready = false;  // full barrier of the current weight stage already seen complete
     const bool res = p.b_res != 0;
@@ -432,7 +461,9 @@ __device__ __forceinline__ void run_mma_halo(const CdgParams &p, const Ring &R, 
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * acc_stride;
         for (int kb = 0; ok && kb < KB; ++kb) {
-            if (!wait_bar(R.full0 + 8u * a_stage, a_par, ctl)) {
+            const uint32_t fpar = DUALH ? (wpar >> a_stage) & 1u : a_par;
+            if (DUALH) wpar ^= 1u << a_stage;
+            if (!wait_bar(full_w + 8u * a_stage, fpar, ctl)) {
                 ok = false;
                 break;
             }
@@ -507,6 +538,7 @@ __device__ __forceinline__ void run_mma_halo(const CdgParams &p, const Ring &R, 
         if (leader) commit(R.acc_full0 + 8u * acc);
         __syncwarp();
         ++acc_count;
+        if (DUALH) a_skip(KB);  // the other warp's item
     }
     if (leader) commit(R.drain);
     __syncwarp();
@@ -1165,13 +1197,16 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
 //         A and half of the weight tile, which halves the B bytes every SM's
 //         shared memory takes in and hands to the tensor core;
 //       3 per-tap or row boxes, two MMA warps (dual issue) for N tiles of up to
-//         128 channels.
+//         128 channels;
+//       5 the halo operand mode with resident weights and two MMA warps taking
+//         alternate items from the one halo ring; 6 the same with CTA pairs.
 template <int OUT_T, bool MASK, int IN_T, int MODE, int EPI>
 __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_constant__ CdgParams p)
 {
-    constexpr bool HALO = MODE == 1 || MODE == 4;
-    constexpr bool PAIR = MODE == 2 || MODE == 4;
-    constexpr bool DUAL = MODE == 3;  // two MMA warps, each with its own ring and accumulators
+    constexpr bool HALO = MODE == 1 || MODE == 4 || MODE == 5 || MODE == 6;
+    constexpr bool PAIR = MODE == 2 || MODE == 4 || MODE == 6;
+    // two MMA warps, each with two accumulators (and, without halo boxes, its own ring)
+    constexpr bool DUAL = MODE == 3 || MODE == 5 || MODE == 6;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -1189,18 +1224,24 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_cons
     const uint32_t bars =
         R.out0 + CDG_SMEM_STAGING +
         (MASK ? (p.mask_bits ? CDG_GATE_RING : static_cast<uint32_t>(p.gate_bufs - 2) * (CDG_SMEM_STAGING / 2)) : 0u);
-    // mbarriers: full[stages], empty[stages], acc_full[4], acc_empty[4], drain[2], gate[8]
+    // mbarriers: full[nfull], empty[stages], acc_full[4], acc_empty[4], drain[2], gate[8].
+    // With two MMA warps over the one halo ring, each warp waits on full
+    // barriers of its own (a_stages more after the stage ones): a stage
+    // alternates between the warps when the ring has an odd number of stages,
+    // and a shared barrier could then be waited on two phases ahead, whose
+    // parity test would pass on the older phase.
+    const int nfull = (HALO && DUAL) ? stages + p.a_stages : stages;
     R.full0 = bars;
-    R.empty0 = bars + 8u * stages;
-    R.acc_full0 = bars + 16u * stages;
-    R.acc_empty0 = bars + 16u * stages + 32u;
-    R.drain = bars + 16u * stages + 64u;
-    R.gfull0 = bars + 16u * stages + 80u;
+    R.empty0 = bars + 8u * nfull;
+    R.acc_full0 = bars + 8u * (nfull + stages);
+    R.acc_empty0 = R.acc_full0 + 32u;
+    R.drain = R.acc_full0 + 64u;
+    R.gfull0 = R.acc_full0 + 80u;
     R.red0 = bars + CDG_SMEM_TAIL;  // only plans with per-channel sums reserve it
     uint8_t *const tail = smem_raw + (bars - raw);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tail + 8 * (2 * stages + 18));
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tail + 8 * (nfull + stages + 18));
     volatile uint32_t *abort_flag = tmem_slot + 1;
-    volatile uint32_t *slot_parity = tmem_slot + 2;  // [stages] (<= CDG_MAX_STAGES_TOTAL entries)
+    volatile uint32_t *slot_parity = tmem_slot + 2;  // [nfull]: the planner keeps all of it within the tables' offset
     CdgPhase *tab = reinterpret_cast<CdgPhase *>(tail + CDG_SMEM_TABLES);
     CdgTap *taps = reinterpret_cast<CdgTap *>(tab + CDG_MAX_PHASES);
     static_assert(8 * (2 * CDG_MAX_STAGES_TOTAL + 18) + 8 + 4 * CDG_MAX_STAGES_TOTAL <= CDG_SMEM_TABLES,
@@ -1230,10 +1271,8 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_cons
     for (int i = threadIdx.x; i < p.nphases; i += blockDim.x) tab[i] = p.phase[i];
     for (int i = threadIdx.x; i < p.ntaps; i += blockDim.x) taps[i] = p.tap[i];
     if (threadIdx.x == 0) {
-        for (int s = 0; s < stages; ++s) {
-            mbar_init(R.full0 + 8u * s, 1);
-            mbar_init(R.empty0 + 8u * s, 1);
-        }
+        for (int s = 0; s < nfull; ++s) mbar_init(R.full0 + 8u * s, 1);
+        for (int s = 0; s < stages; ++s) mbar_init(R.empty0 + 8u * s, 1);
         for (int a = 0; a < 4; ++a) {
             mbar_init(R.acc_full0 + 8u * a, 1);
             // one arrival per epilogue warp (in a pair, the leader's counts both CTAs' warps)
@@ -1243,7 +1282,7 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_cons
         mbar_init(R.drain + 8u, 1);
         for (int g = 0; g < 8; ++g) mbar_init(R.gfull0 + 8u * g, 1);
         *abort_flag = 0u;
-        for (int s = 0; s < stages; ++s) slot_parity[s] = 0u;
+        for (int s = 0; s < nfull; ++s) slot_parity[s] = 0u;
         fence_mbar_init();
     }
     // Everything above touches only shared memory and kernel parameters.  Global
@@ -1287,7 +1326,29 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_cons
         Sj.step = 2 * S.step;
         return Sj;
     };
-    if (DUAL) {
+    if (DUAL && HALO) {
+        // warps 1 and 3 issue the MMAs of alternate items from the one halo
+        // ring (accumulator slots 2j, 2j + 1); warp 0 loads the halo boxes and
+        // warp 2 the resident weights
+        if (warp == 1 || warp == 3) {
+            const int j = warp >> 1;
+            Ring Rj = R;
+            Rj.acc_full0 = R.acc_full0 + 16u * j;
+            Rj.acc_empty0 = R.acc_empty0 + 16u * j;
+            Rj.drain = R.drain + 8u * j;
+            if (!PAIR || S.rank == 0) {
+                run_mma_halo<PAIR, true>(p, Rj, tab, taps, ctl, tmem_base + 2u * j * p.acc_stride, elect_one_sync(),
+                                         sched_of(j), j);
+            } else {
+                volatile uint32_t no_abort = 0;
+                wait_bar(Rj.drain, 0, Ctl{&no_abort, p.status, p.wait_limit_ns});
+            }
+        } else if (warp >= CDG_EPI_WARP0) {
+            run_epilogue<OUT_T, MASK, IN_T, HALO, PAIR, true, EPI>(p, R, tab, ctl, tmem_base, S);
+        } else {
+            run_loader_halo<PAIR, true>(p, R, tab, taps, ctl, warp == 0 ? 0 : 1, elect_one_sync(), slot_parity, S);
+        }
+    } else if (DUAL) {
         if (warp == 1 || warp == 3) {
             const int j = warp >> 1;
             run_mma<false>(p, ring_of(j), tab, ctl, tmem_base + 2u * j * p.acc_stride, elect_one_sync(), sched_of(j));
@@ -1321,7 +1382,7 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_cons
     __syncthreads();
     if (*abort_flag && threadIdx.x == 0) {
         if (!PAIR || S.rank == 0) {
-            drain_loads(R, stages, p.status, p.wait_limit_ns, slot_parity);
+            drain_loads(R, nfull, p.status, p.wait_limit_ns, slot_parity);
         } else {
             // this CTA's copies complete on the leader's barriers; give any
             // still in flight time to land before the pair may exit

@@ -18,6 +18,8 @@ DgradFn pick_mode(int mode)
     if (mode == 2) return cdg::dgrad_kernel<OUT_T, MASK, IN_T, 2, EPI>;
     if (mode == 3) return cdg::dgrad_kernel<OUT_T, MASK, IN_T, 3, EPI>;
     if (mode == 4) return cdg::dgrad_kernel<OUT_T, MASK, IN_T, 4, EPI>;
+    if (mode == 5) return cdg::dgrad_kernel<OUT_T, MASK, IN_T, 5, EPI>;
+    if (mode == 6) return cdg::dgrad_kernel<OUT_T, MASK, IN_T, 6, EPI>;
     return cdg::dgrad_kernel<OUT_T, MASK, IN_T, 0, EPI>;
 }
 
@@ -49,7 +51,7 @@ DgradFn select_kernel(int out_type, int in_type, bool mask, int mode)
 template <int EPI>
 cudaError_t cdg_dgrad_prepare_variant(int out_type, int in_type, bool mask)
 {
-    for (int mode = 0; mode < 5; ++mode) {
+    for (int mode = 0; mode < 7; ++mode) {
         DgradFn fn = select_kernel<EPI>(out_type, in_type, mask, mode);
         if (!fn) return cudaSuccess;  // no such variant for these types (activation without gate)
         const cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void *>(fn),
@@ -63,7 +65,7 @@ template <int EPI>
 cudaError_t cdg_dgrad_launch_variant(const CdgParams &p, int out_type, int in_type, bool mask, int grid, size_t smem,
                                      cudaStream_t stream)
 {
-    const int mode = p.halo ? (p.pair ? 4 : 1) : (p.pair ? 2 : (p.dual ? 3 : 0));
+    const int mode = p.halo ? (p.pair ? (p.dual ? 6 : 4) : (p.dual ? 5 : 1)) : (p.pair ? 2 : (p.dual ? 3 : 0));
     DgradFn fn = select_kernel<EPI>(out_type, in_type, mask, mode);
     if (!fn) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};

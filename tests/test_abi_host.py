@@ -158,9 +158,14 @@ def test_workload_plans():
         else:
             assert info["box_w"] * info["box_h"] * info["box_n"] <= 128
         assert p.packed_weight_bytes == 2 * L.K * L.R * L.S * L.C
-        if info["mma_warps"] == 2:  # dual issue: two rings, two accumulators per MMA warp
+        if info["mma_warps"] == 2 and info["a_mode"] in (0, 1):
+            # dual issue over per-tap or row boxes: two rings, two accumulators per MMA warp
             assert info["stages"] % 2 == 0 and info["stages"] >= 4
             assert info["tmem_cols"] >= 4 * info["tile_n"] and info["cta_pair"] == 0
+        elif info["mma_warps"] == 2:
+            # two MMA warps over the one halo ring with resident weights: at
+            # most six halo stages and the weights' barrier
+            assert info["a_mode"] == 3 and info["stages"] <= 7 and info["tmem_cols"] >= 4 * info["tile_n"]
 
 
 def test_halo_resident_weights_when_the_filter_fits(monkeypatch):
@@ -191,6 +196,26 @@ def test_halo_resident_weights_when_the_filter_fits(monkeypatch):
     monkeypatch.setenv("CDG_HALO", "0")
     assert cdg.plan_host(256, 56, 56, 64, 64, 3, 3, 1, 1, 1, "bf16", num_sms=148).info()["a_mode"] == 0
     assert cdg.plan_host(256, 28, 28, 128, 128, 3, 3, 1, 1, 1, "bf16", num_sms=148).info()["a_mode"] == 0
+
+
+def test_grid_cap_and_dual_halo_option(monkeypatch):
+    """CDG_MAX_GRID caps the persistent grid (to an even count for CTA
+    pairs); CDG_DUAL=1 gives halo plans with resident weights two MMA warps
+    and at most six halo stages."""
+    monkeypatch.setenv("CDG_MAX_GRID", "5")
+    info = cdg.plan_host(256, 56, 56, 64, 64, 3, 3, 1, 1, 1, "bf16", num_sms=152).info()
+    assert info["grid"] == 5
+    info = cdg.plan_host(256, 28, 28, 128, 128, 3, 3, 1, 1, 1, "bf16", num_sms=152).info()
+    assert info["cta_pair"] == 1 and info["grid"] == 4
+    monkeypatch.setenv("CDG_MAX_GRID", "1")
+    assert cdg.plan_host(256, 28, 28, 128, 128, 3, 3, 1, 1, 1, "bf16", num_sms=152).info()["grid"] == 2
+    monkeypatch.delenv("CDG_MAX_GRID")
+    monkeypatch.setenv("CDG_DUAL", "1")
+    for shape in ((256, 56, 56, 64, 64, 3, 3, 1, 1, 1), (256, 28, 28, 128, 128, 3, 3, 1, 1, 1),
+                  (16, 12, 12, 64, 64, 3, 3, 1, 1, 1)):
+        info = cdg.plan_host(*shape, "bf16", num_sms=152).info()
+        assert info["a_mode"] == 3 and info["mma_warps"] == 2 and info["tmem_cols"] <= 512
+        assert info["stages"] <= 7  # six halo stages and the resident weights' barrier
 
 
 def test_four_accumulators_only_where_they_fit_tensor_memory(monkeypatch):

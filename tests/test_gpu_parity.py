@@ -208,6 +208,33 @@ def test_halo_operand_mode_with_cta_pairs(L, reach, monkeypatch):
         assert info[k] == v, (k, info)
 
 
+# two MMA warps over the halo ring (opt-in: CDG_DUAL=1).  The grid is capped
+# (CDG_MAX_GRID) so that every CTA walks many items and the halo ring wraps
+# around many times: three halo stages (odd, so a stage alternates between
+# the warps) as for ResNet-50's 3x3 64-channel layer, six, two with CTA
+# pairs, four stride-2 phases under the ReLU gate, fp32 output.
+HALO_DUAL_CASES = [
+    (_case(8, 56, 56, 64, 64, 3, 3, 1, 1, 1, "bf16", idx=40), "6", {"a_mode": 3, "mma_warps": 2, "cta_pair": 0}),
+    (_case(16, 12, 12, 64, 64, 3, 3, 1, 1, 1, "bf16", idx=41), "2", {"a_mode": 3, "mma_warps": 2, "cta_pair": 0}),
+    (_case(8, 28, 28, 128, 128, 3, 3, 1, 1, 1, "bf16", idx=42), "6", {"a_mode": 3, "mma_warps": 2, "cta_pair": 1}),
+    (_case(8, 14, 14, 64, 64, 3, 3, 2, 1, 1, "bf16", relu=True, idx=43), "2", {"a_mode": 3, "mma_warps": 2}),
+    (_case(40, 9, 7, 64, 64, 3, 3, 1, 1, 1, "f16", out="f32", relu=True, idx=44), "6", {"a_mode": 3, "mma_warps": 2}),
+]
+
+
+@pytest.mark.parametrize("L,grid,reach", HALO_DUAL_CASES, ids=lambda v: v.name if isinstance(v, Layer) else None)
+def test_halo_dual_issue(L, grid, reach, monkeypatch):
+    """Halo boxes with resident weights and two MMA warps taking alternate
+    items from the one halo ring give the oracle's result."""
+    monkeypatch.setenv("CDG_DUAL", "1")
+    monkeypatch.setenv("CDG_MAX_GRID", grid)
+    run, _, _ = check_layer(L)
+    info = run.plan.info()
+    for k, v in reach.items():
+        assert info[k] == v, (k, info)
+    assert info["grid"] <= int(grid) and info["work_items"] >= 4 * (info["grid"] // (2 if info["cta_pair"] else 1))
+
+
 def test_chained_launches_keep_stream_order():
     """Launches on one stream start their set-up while the previous launch
     finishes (programmatic dependent launch), but must still see stream order:
@@ -254,7 +281,7 @@ def test_mode_cases_reach_their_paths():
 
 
 @pytest.mark.parametrize("env", ["", "CDG_PAIR=0", "CDG_PAIR=1", "CDG_DUAL=0", "CDG_INTERLEAVE=0", "CDG_HALO=0",
-                                 "CDG_PDL=0", "CDG_PREFETCH=1"])
+                                 "CDG_PDL=0", "CDG_PREFETCH=1", "CDG_MAX_GRID=3"])
 @pytest.mark.parametrize("L", MODE_CASES, ids=lambda L: L.name)
 def test_planner_mode_overrides(L, env, monkeypatch):
     """Every planner mode and its override gives the oracle's result."""
