@@ -170,6 +170,8 @@ void apply_grid(cdg_plan_st *h, int grid)
     p.interleave = ok ? h->il_phases : 0;
     p.il_items = ok ? h->il_items : 0;
     p.il_round = G;
+    p.div_il = cdg_make_div(static_cast<uint32_t>(std::max(1, p.interleave)));
+    p.div_il_round = cdg_make_div(static_cast<uint32_t>(std::max(1, G)));
 }
 
 PlanOpts opts_from_env()
@@ -571,7 +573,12 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     p.tmem_cols = static_cast<uint32_t>(tmem_cols);
     p.acc_stride = static_cast<uint32_t>(tmem_cols / n_acc);
     p.acc_ring = dual ? 2u : static_cast<uint32_t>(n_acc);
-    for (size_t i = 0; i < phases.size(); ++i) p.phase[i] = phases[i];
+    for (size_t i = 0; i < phases.size(); ++i) {
+        p.phase[i] = phases[i];
+        p.div_tiles_w[i] = cdg_make_div(static_cast<uint32_t>(std::max(1, phases[i].tiles_w)));
+        p.div_tiles_h[i] = cdg_make_div(static_cast<uint32_t>(std::max(1, phases[i].tiles_h)));
+    }
+    p.div_tiles_n = cdg_make_div(static_cast<uint32_t>(std::max(1, tiles_n)));
     for (size_t i = 0; i < taps.size(); ++i) p.tap[i] = taps[i];
 
     h->smem = static_cast<size_t>(1024 + ring_bytes + staging + CDG_SMEM_TAIL + red_bytes);

@@ -37,6 +37,25 @@
 #define CDG_SMEM_RED (2 * 4 * 64 * 4)
 #define CDG_MAX_STAGES_TOTAL 10  // all ring stages together (their mbarriers live in the 384-byte area)
 
+// Division by a divisor fixed for the launch as a multiply-high, an add and a
+// shift (Granlund and Montgomery, "Division by invariant integers using
+// multiplication", PLDI 1994, the round-up method with N = 32): with
+// shr = ceil(log2 d) and mul = floor(2^32 (2^shr - d) / d) + 1,
+// n / d = (mulhi(n, mul) + n) >> shr for every 0 <= n < 2^31 and d >= 1.
+// The kernels' item bookkeeping divides by tile counts; as plain integer
+// divisions they cost the epilogue several hundred cycles per work item.
+struct CdgDiv {
+    uint32_t mul, shr;
+};
+
+static inline CdgDiv cdg_make_div(uint32_t d)
+{
+    uint32_t shr = 0;
+    while ((1ull << shr) < d) ++shr;
+    const unsigned long long m = ((1ull << 32) * ((1ull << shr) - d)) / d + 1ull;
+    return CdgDiv{static_cast<uint32_t>(m), shr};
+}
+
 // One phase sub-convolution of a (possibly strided) dgrad.  The dX pixels with
 // h = stride*i + ph, w = stride*j + pw (0 <= i < hph, 0 <= j < wph) form the
 // phase sub-grid; the filter taps whose contributions land on it are
@@ -124,6 +143,10 @@ struct CdgParams {  // CUtensorMap members carry their own (128-byte) alignment
     int withhold_stage;   // test only: >= 0 makes every per-tap/row loader skip the load (and its
                           // transaction count) of its stage with this sequence number, so the MMA
                           // warp's wait for it runs out; -1 in normal use
+    CdgDiv div_tiles_w[CDG_MAX_PHASES], div_tiles_h[CDG_MAX_PHASES];  // per phase: its box tiles along j and i
+    CdgDiv div_tiles_n;   // N tiles
+    CdgDiv div_il;        // interleaved phases (1 when none)
+    CdgDiv div_il_round;  // items per scheduling round (il_round; 1 when unset)
     CdgPhase phase[CDG_MAX_PHASES];
     CdgTap tap[CDG_MAX_TAPS];
 };

@@ -39,6 +39,12 @@
 
 namespace cdg {
 
+// n / d for 0 <= n < 2^31 with d's precomputed multiplier and shift (CdgDiv).
+__device__ __forceinline__ int fdiv(int n, CdgDiv d)
+{
+    return static_cast<int>((__umulhi(static_cast<uint32_t>(n), d.mul) + static_cast<uint32_t>(n)) >> d.shr);
+}
+
 // Walk over this CTA's work items g = start, start + step, ... as (phase,
 // index within the phase), phases read from the shared-memory copy.  The
 // first `il` phases (il >= 2, all with il_items items) are interleaved: the
@@ -51,25 +57,28 @@ namespace cdg {
 // follow one after another.
 struct ItemWalk {
     const CdgPhase *tab;
-    int nph, step, il, il_items, il_round;
+    int nph, step, il, il_items, il_round, per_round;
+    CdgDiv div_il, div_round;
     int g, phase, local;
     // items start, start + step, ...: one CTA's (step = gridDim.x) or one CTA
     // pair's (step = number of pairs) share of the work list
-    __device__ __forceinline__ ItemWalk(const CdgPhase *t, int n, int start, int stp, int il_, int il_items_,
-                                        int il_round_)
-        : tab(t), nph(n), step(stp), il(il_), il_items(il_items_), il_round(il_round_), g(start), phase(0), local(0)
+    __device__ __forceinline__ ItemWalk(const CdgPhase *t, const CdgParams &p, int start, int stp)
+        : tab(t), nph(p.nphases), step(stp), il(p.interleave), il_items(p.il_items), il_round(p.il_round),
+          per_round(0), div_il(p.div_il), div_round(p.div_il_round), g(start), phase(0), local(0)
     {
+        if (il > 0) per_round = fdiv(il_round, div_il);  // tiles of each phase per round
         settle();
     }
     __device__ __forceinline__ void settle()
     {
         if (il > 0 && g < il * il_items) {
-            const int r = g / il_round;
+            const int r = fdiv(g, div_round);
             const int pos = g - r * il_round;
-            const int a = pos / il;
+            const int a = fdiv(pos, div_il);
             const int b = pos - a * il;
-            phase = (b + r) % il;
-            local = r * (il_round / il) + a;
+            const int rr = r - fdiv(r, div_il) * il;  // r mod il
+            phase = b + rr >= il ? b + rr - il : b + rr;
+            local = r * per_round + a;
             return;
         }
         phase = il;
@@ -92,21 +101,22 @@ struct Sched {
     int start, step;
     int pair;   // 1: CTA pairs share each item (M tiles 2*t and 2*t + 1)
     int rank;   // rank in the pair (0 = leader, issues the MMAs)
-    __device__ __forceinline__ int m_tile(int local, int tiles_n) const
+    __device__ __forceinline__ int m_tile(int local, int tiles_n, CdgDiv div_tiles_n) const
     {
-        const int t = tiles_n == 1 ? local : local / tiles_n;
+        const int t = tiles_n == 1 ? local : fdiv(local, div_tiles_n);
         return pair ? 2 * t + rank : t;
     }
 };
 
-// Origin (j0, i0, n0) of 4-D box tile mt of a phase.
-__device__ __forceinline__ void box_origin(const CdgPhase &ph, int mt, int bw, int bh, int bn, int &j0, int &i0,
-                                           int &n0)
+// Origin (j0, i0, n0) of 4-D box tile mt of phase `phase` (tiles_w x tiles_h
+// boxes per image).
+__device__ __forceinline__ void box_origin(const CdgParams &p, const CdgPhase &ph, int phase, int mt, int bw, int bh,
+                                           int bn, int &j0, int &i0, int &n0)
 {
-    const int tj = mt % ph.tiles_w;
-    const int rest = mt / ph.tiles_w;
-    const int ti = rest % ph.tiles_h;
-    const int tn = rest / ph.tiles_h;
+    const int rest = fdiv(mt, p.div_tiles_w[phase]);
+    const int tj = mt - rest * ph.tiles_w;
+    const int tn = fdiv(rest, p.div_tiles_h[phase]);
+    const int ti = rest - tn * ph.tiles_h;
     j0 = tj * bw;
     i0 = ti * bh;
     n0 = tn * bn;
@@ -160,7 +170,7 @@ __device__ __forceinline__ void run_loader(const CdgParams &p, const Ring &R, co
     // GB300 this makes the 1x1 layers slower (the ring already covers the
     // latency), so plans leave it off unless asked.
     constexpr int kPrefetchStages = 8;
-    ItemWalk pw(tab, p.nphases, S.start, S.step, p.interleave, p.il_items, p.il_round);
+    ItemWalk pw(tab, p, S.start, S.step);
     int pkb = 0;
     auto pf_advance = [&]() {
         if (!pw.valid()) return;
@@ -173,15 +183,15 @@ __device__ __forceinline__ void run_loader(const CdgParams &p, const Ring &R, co
     if (prefetch)
         for (int i = 0; i < kPrefetchStages; ++i) pf_advance();
     bool ok = true;
-    for (ItemWalk w(tab, p.nphases, S.start, S.step, p.interleave, p.il_items, p.il_round); ok && w.valid(); w.next()) {
+    for (ItemWalk w(tab, p, S.start, S.step); ok && w.valid(); w.next()) {
         const CdgPhase &ph = tab[w.phase];
         const int ntap = ph.tap_count;
         if (ntap == 0) continue;
-        const int tq = tiles_n == 1 ? w.local : w.local / tiles_n;
+        const int tq = tiles_n == 1 ? w.local : fdiv(w.local, p.div_tiles_n);
         const int nt = w.local - tq * tiles_n;
-        const int mt = S.m_tile(w.local, tiles_n);
+        const int mt = S.m_tile(w.local, tiles_n, p.div_tiles_n);
         int j0 = 0, i0 = 0, n0 = 0;
-        if (!flat) box_origin(ph, mt, bw, bh, bn, j0, i0, n0);
+        if (!flat) box_origin(p, ph, w.phase, mt, bw, bh, bn, j0, i0, n0);
         // a pair splits the N tile's weight rows: this CTA loads its half
         const int c0 = nt * BN + (PAIR ? S.rank * (BN / 2) : 0);
         const int m0 = mt * m_step;
@@ -196,7 +206,7 @@ __device__ __forceinline__ void run_loader(const CdgParams &p, const Ring &R, co
                         break;
                     }
                     if (prefetch && leader && pw.valid() && tab[pw.phase].tap_count > 0)
-                        tma_prefetch_2d(mapA, pkb * CDG_BK, S.m_tile(pw.local, tiles_n) * m_step);
+                        tma_prefetch_2d(mapA, pkb * CDG_BK, S.m_tile(pw.local, tiles_n, p.div_tiles_n) * m_step);
                     // (test only) a withheld stage gets neither its copies nor
                     // their byte count, and is not recorded for the abort drain:
                     // its full barrier never completes, so the consumer's
@@ -286,7 +296,7 @@ __device__ __forceinline__ void run_loader_halo(const CdgParams &p, const Ring &
     // into L2 the halo box kPrefetchBoxes (tile, K block) steps ahead of the
     // one it loads
     constexpr int kPrefetchBoxes = 4;
-    ItemWalk pw(tab, p.nphases, S.start, S.step, p.interleave, p.il_items, p.il_round);
+    ItemWalk pw(tab, p, S.start, S.step);
     int pkb = 0;
     auto pf_advance = [&]() {
         if (!pw.valid()) return;
@@ -317,14 +327,14 @@ __device__ __forceinline__ void run_loader_halo(const CdgParams &p, const Ring &
     }
     uint32_t n_item = 0;             // items with taps so far (two MMA warps: item n is warp n % 2's)
     uint32_t wpar[2] = {0u, 0u};     // two MMA warps: parity bit per stage of each warp's full barriers
-    for (ItemWalk w(tab, p.nphases, S.start, S.step, p.interleave, p.il_items, p.il_round); ok && w.valid(); w.next()) {
+    for (ItemWalk w(tab, p, S.start, S.step); ok && w.valid(); w.next()) {
         const CdgPhase &ph = tab[w.phase];
         const int ntap = ph.tap_count;
         if (ntap == 0) continue;
-        const int mt = S.m_tile(w.local, tiles_n);
-        const int nt = w.local - (tiles_n == 1 ? w.local : w.local / tiles_n) * tiles_n;
+        const int mt = S.m_tile(w.local, tiles_n, p.div_tiles_n);
+        const int nt = w.local - (tiles_n == 1 ? w.local : fdiv(w.local, p.div_tiles_n)) * tiles_n;
         int j0, i0, n0;
-        box_origin(ph, mt, wt, bh, 1, j0, i0, n0);
+        box_origin(p, ph, w.phase, mt, wt, bh, 1, j0, i0, n0);
         const int c0 = nt * BN;
         const uint32_t wj = DUALH ? (n_item & 1u) : 0u;
         ++n_item;
@@ -351,7 +361,7 @@ __device__ __forceinline__ void run_loader_halo(const CdgParams &p, const Ring &
                     if (p.prefetch && pw.valid() && tab[pw.phase].tap_count > 0) {
                         const CdgPhase &pph = tab[pw.phase];
                         int pj, pi, pn;
-                        box_origin(pph, S.m_tile(pw.local, tiles_n), wt, bh, 1, pj, pi, pn);
+                        box_origin(p, pph, pw.phase, S.m_tile(pw.local, tiles_n, p.div_tiles_n), wt, bh, 1, pj, pi, pn);
                         tma_prefetch_4d(mapA, pkb * CDG_BK, pj + pph.ds_min, pi + pph.dr_min, pn);
                     }
                 }
@@ -450,7 +460,7 @@ __device__ __forceinline__ void run_mma_halo(const CdgParams &p, const Ring &R, 
     bool b_ready = false;  // full barrier of the current weight stage already seen complete
     const bool res = p.b_res != 0;
     if (res && !wait_bar(R.full0 + 8u * as, 0, ctl)) ok = false;  // resident weights landed
-    for (ItemWalk w(tab, p.nphases, S.start, S.step, p.interleave, p.il_items, p.il_round); ok && w.valid(); w.next()) {
+    for (ItemWalk w(tab, p, S.start, S.step); ok && w.valid(); w.next()) {
         const CdgPhase &ph = tab[w.phase];
         const int ntap = ph.tap_count;
         if (ntap == 0) continue;
@@ -565,7 +575,7 @@ __device__ __forceinline__ void run_mma(const CdgParams &p, const Ring &R, const
     uint32_t acc_count = 0;
     bool ok = true;
     bool ready = false;  // full barrier of `stage` already seen complete
-    for (ItemWalk w(tab, p.nphases, S.start, S.step, p.interleave, p.il_items, p.il_round); ok && w.valid(); w.next()) {
+    for (ItemWalk w(tab, p, S.start, S.step); ok && w.valid(); w.next()) {
         const int ntap = tab[w.phase].tap_count;
         if (ntap == 0) continue;
         const uint32_t acc = acc_count & 1u;
@@ -697,14 +707,14 @@ __device__ __forceinline__ void gate_issue(const CdgParams &p, const GateCursor 
                                            uint32_t bar)
 {
     const CdgPhase &ph = gc.w.tab[gc.w.phase];
-    const int mt = S.m_tile(gc.w.local, p.tiles_n);
-    const int nt = gc.w.local - (p.tiles_n == 1 ? gc.w.local : gc.w.local / p.tiles_n) * p.tiles_n;
+    const int mt = S.m_tile(gc.w.local, p.tiles_n, p.div_tiles_n);
+    const int nt = gc.w.local - (p.tiles_n == 1 ? gc.w.local : fdiv(gc.w.local, p.div_tiles_n)) * p.tiles_n;
     const int x0 = p.mask_bits ? (p.tiles_n == 1 ? 0 : nt * (p.BN / 8)) : nt * p.BN + gc.cc;
     const uint64_t map = reinterpret_cast<uint64_t>(&p.tmG[gc.w.phase]);
     if (!PREFETCH) mbar_arrive_expect_tx(bar, p.gate_tx);
     if (p.d_mode == CDG_D_BOX4) {
         int j0, i0, n0;
-        box_origin(ph, mt, max(p.box_w, 1), max(p.box_h, 1), max(p.box_n, 1), j0, i0, n0);
+        box_origin(p, ph, gc.w.phase, mt, max(p.box_w, 1), max(p.box_h, 1), max(p.box_n, 1), j0, i0, n0);
         if (PREFETCH)
             tma_prefetch_4d(map, x0, j0, i0, n0);
         else
@@ -900,7 +910,7 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
     // so one warp issuing them all would pace the epilogue); every epilogue
     // thread walks the cursor in step.  (Four chunks of lookahead, six
     // buffers, measured slower on GB300: the operand ring loses a stage.)
-    GateCursor gc{ItemWalk(tab, p.nphases, S.start, S.step, p.interleave, p.il_items, p.il_round), 0};
+    GateCursor gc{ItemWalk(tab, p, S.start, S.step), 0};
     const int gstep = mask_bits ? BN : CH;
     const uint32_t gring = mask_bits ? R.gate0 : R.out0;
     const uint32_t gslot = mask_bits ? static_cast<uint32_t>(CDG_GATE_SLOT) : 128u * 128u;
@@ -909,7 +919,7 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
     uint32_t gated_items = 0;
     // the prefetch cursor runs ahead of gc by the loads' lookahead plus
     // kGatePrefetch* loads; its issues rotate over the warps like the loads'
-    GateCursor pf{ItemWalk(tab, p.nphases, S.start, S.step, p.interleave, p.il_items, p.il_round), 0};
+    GateCursor pf{ItemWalk(tab, p, S.start, S.step), 0};
     uint32_t pf_issued = 0;
     auto gate_prefetch = [&]() {
         if (!p.prefetch || !pf.valid()) return;
@@ -949,10 +959,10 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
         for (int j = 0; j < ahead; ++j) gate_ahead();
     }
     bool ok = true;
-    for (ItemWalk w(tab, p.nphases, S.start, S.step, p.interleave, p.il_items, p.il_round); w.valid(); w.next(), ++item_index) {
+    for (ItemWalk w(tab, p, S.start, S.step); w.valid(); w.next(), ++item_index) {
         const CdgPhase &ph = tab[w.phase];
-        const int mt = S.m_tile(w.local, tiles_n);
-        const int nt = w.local - (tiles_n == 1 ? w.local : w.local / tiles_n) * tiles_n;
+        const int mt = S.m_tile(w.local, tiles_n, p.div_tiles_n);
+        const int nt = w.local - (tiles_n == 1 ? w.local : fdiv(w.local, p.div_tiles_n)) * tiles_n;
         const int c_begin = nt * BN;
         const int c_end = min(C, c_begin + BN);
         const uint64_t mapD = reinterpret_cast<uint64_t>(&p.tmD[w.phase]);
@@ -970,7 +980,7 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
                 zero_ready = true;
             }
             int j0, i0, n0;
-            box_origin(ph, mt, ph.zbw, ph.zbh, 1, j0, i0, n0);
+            box_origin(p, ph, w.phase, mt, ph.zbw, ph.zbh, 1, j0, i0, n0);
             const int nchunks = (c_end - c_begin + CH - 1) / CH;
             if (elected)
                 for (int q = ew; q < nchunks; q += 4) {
@@ -989,7 +999,7 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
         }
         // tile origin in the store map's coordinates
         int j0 = 0, i0 = 0, n0 = 0;
-        if (d_mode == CDG_D_BOX4) box_origin(ph, mt, bw, bh, bn, j0, i0, n0);
+        if (d_mode == CDG_D_BOX4) box_origin(p, ph, w.phase, mt, bw, bh, bn, j0, i0, n0);
         // does this thread's tile row hold a dX pixel of the item?  (rows past
         // the sub-grid's edges, halo padding rows and the tail of the last
         // tile are computed but never stored; the sums must skip them too)
@@ -1462,7 +1472,7 @@ __device__ __forceinline__ void run_mma_fused(const CdgParams &p, const Ring &R,
         __syncwarp();
         return true;
     };
-    for (ItemWalk w(tab, p.nphases, S.start, S.step, p.interleave, p.il_items, p.il_round); ok && w.valid(); w.next()) {
+    for (ItemWalk w(tab, p, S.start, S.step); ok && w.valid(); w.next()) {
         const CdgPhase &ph = tab[w.phase];
         const int ntap = ph.tap_count;
         const uint32_t acc = n & 1u;
@@ -1541,9 +1551,9 @@ __device__ __forceinline__ void run_epilogue_fused(const CdgParams &p, const Rin
     const Ctl gate_ctl{&gate_no_abort, ctl.status, ctl.limit};
     // the gate tile of the next item is loaded into the one gate buffer as
     // soon as every thread has read the current one (issued by warp 0)
-    ItemWalk nx(tab, p.nphases, S.start, S.step, p.interleave, p.il_items, p.il_round);
+    ItemWalk nx(tab, p, S.start, S.step);
     // and the tile two items beyond that is prefetched into L2 meanwhile
-    ItemWalk px(tab, p.nphases, S.start, S.step, p.interleave, p.il_items, p.il_round);
+    ItemWalk px(tab, p, S.start, S.step);
     px.next();
     px.next();
     uint32_t g_issued = 0, g_used = 0;
@@ -1552,11 +1562,11 @@ __device__ __forceinline__ void run_epilogue_fused(const CdgParams &p, const Rin
         ++g_issued;
         if (ew == 0 && elected) {
             int j0, i0, n0;
-            box_origin(tab[nx.phase], S.m_tile(nx.local, 1), p.halo_wt, p.halo_bh, 1, j0, i0, n0);
+            box_origin(p, tab[nx.phase], nx.phase, S.m_tile(nx.local, 1, p.div_tiles_n), p.halo_wt, p.halo_bh, 1, j0, i0, n0);
             mbar_arrive_expect_tx(B.gate_full, p.gate_tx);
             tma_load_4d(x2_smem, mapGate, B.gate_full, 0, j0, i0, n0);
             if (p.prefetch && px.valid()) {
-                box_origin(tab[px.phase], S.m_tile(px.local, 1), p.halo_wt, p.halo_bh, 1, j0, i0, n0);
+                box_origin(p, tab[px.phase], px.phase, S.m_tile(px.local, 1, p.div_tiles_n), p.halo_wt, p.halo_bh, 1, j0, i0, n0);
                 tma_prefetch_4d(mapGate, 0, j0, i0, n0);
             }
         }
@@ -1614,10 +1624,10 @@ __device__ __forceinline__ void run_epilogue_fused(const CdgParams &p, const Rin
     uint32_t n = 0;
     int pj0 = 0, pi0 = 0, pn0 = 0;  // the previous item's tile origin
     bool ok = true;
-    for (ItemWalk w(tab, p.nphases, S.start, S.step, p.interleave, p.il_items, p.il_round); w.valid(); w.next(), ++n) {
+    for (ItemWalk w(tab, p, S.start, S.step); w.valid(); w.next(), ++n) {
         const CdgPhase &ph = tab[w.phase];
         int j0, i0, n0;
-        box_origin(ph, S.m_tile(w.local, 1), p.halo_wt, p.halo_bh, 1, j0, i0, n0);
+        box_origin(p, ph, w.phase, S.m_tile(w.local, 1, p.div_tiles_n), p.halo_wt, p.halo_bh, 1, j0, i0, n0);
         // ---- g = gate(GEMM 1): accumulator -> registers -> tensor memory (GEMM 2's A)
         bool okw = wait_bar(B.acc1_full0 + 8u * (n & 1u), (n >> 1) & 1u, ctl);
         okw = okw && wait_bar(B.a2_empty0 + 8u * (n & 1u), ((n >> 1) & 1u) ^ 1u, ctl);
