@@ -432,10 +432,12 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
 
     // ---- CTA pairs: two CTAs (a cluster) share each 256-row tile through the
     // 2-SM MMA, each holding its 128 rows of dY and half of the weight tile.
-    // Measured on GB300 over the ResNet-50 layers: pairs win (4-8 %) for
-    // 256-channel N tiles whose tiles run at least 9 pipeline stages, and lose
-    // elsewhere (short tiles couple two SMs' epilogues and rings); 192-channel
-    // tiles (below) behave alike.
+    // Measured on GB300 over the ResNet-50 layers: pairs win for 256-channel
+    // N tiles whose tiles run at least 4 pipeline stages (1x1 1024 -> 512 at
+    // 14x14, 8 stages: 51.4 -> 43.5 us; 512 -> 256 at 28x28, 4 stages: 61.7 ->
+    // 58.5 us), and lose with 1 or 2 (1x1 512 -> 128 at 28x28: 46.2 -> 49.1
+    // us: the short tiles couple two SMs' epilogues); 192-channel tiles
+    // (below) behave alike.
     int tap_phases = 0, tap_sum = 0;
     for (const CdgPhase &f : phases)
         if (f.tap_count > 0) {
@@ -443,7 +445,7 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
             tap_sum += f.tap_count;
         }
     const double stages_per_tile = tap_phases ? double(tap_sum) / tap_phases * ceil_div(K, CDG_BK) : 0.0;
-    bool pair = halo ? halo_pair : (BN >= 192 && num_sms >= 2 && stages_per_tile >= 9.0);
+    bool pair = halo ? halo_pair : (BN >= 192 && num_sms >= 2 && stages_per_tile >= 4.0);
     if (opt.pair == 0) pair = false;
     if (opt.pair == 1) pair = halo ? halo_pair : (BN >= 128 && num_sms >= 2);
 
