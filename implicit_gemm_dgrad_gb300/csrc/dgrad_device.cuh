@@ -1080,6 +1080,16 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
                         mbar_arrive(R.acc_empty0 + 8u * acc);
                 }
             }
+            // 16-bit output gated by the saved activation: this row's eight
+            // activation pieces, all read before any output piece is written
+            // over them (volatile shared-memory reads and writes interleaved
+            // piece by piece would pay the read latency eight times a chunk)
+            uint32_t xwa[(MASK && OSZ == 2) ? 8 : 1][4];
+            if (MASK && OSZ == 2 && !mask_bits && srow >= 0) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    ld_shared_v4(buf + srow_off + ((static_cast<uint32_t>(q) ^ sw) << 4), xwa[q % ((MASK && OSZ == 2) ? 8 : 1)]);
+            }
 #pragma unroll
             for (int q = 0; q < 8; ++q) {  // 16-byte pieces of this row
                 constexpr int PER = 16 / OSZ;  // values per piece
@@ -1092,9 +1102,8 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
                 if (MASK && srow >= 0) {
                     if (mask_bits) {
                         gate_mask<PER>(v, gw[(PER * q) >> 5] >> ((PER * q) & 31));
-                    } else if (OSZ == 2) {  // x piece q sits where output piece q goes
-                        uint32_t xw[4];
-                        ld_shared_v4(buf + srow_off + ((static_cast<uint32_t>(q) ^ sw) << 4), xw);
+                    } else if (OSZ == 2) {  // x piece q sat where output piece q goes
+                        const uint32_t *xw = xwa[q % ((MASK && OSZ == 2) ? 8 : 1)];
                         if (EPI != 0)
                             gate_x<IN_T, PER, ACT>(v, xw, xp);
                         else
