@@ -834,42 +834,16 @@ int launch_plan(cdg_handle_t h, const void *dY, const void *Wpacked, void *dX, c
     return CDG_OK;
 }
 
-// Scheduling rounds x tile width of the items with taps: the tensor time of
-// the longest CTA, in tile-width units (every item of a layer does the same
-// number of pipeline stages per channel of its tile).
-long long round_cost(const cdg_plan_st *h)
-{
-    const CdgParams &p = h->prm;
-    long long items = 0;
-    for (int i = 0; i < p.nphases; ++i)
-        if (p.phase[i].tap_count > 0) items += p.phase[i].items;
-    const long long G = std::max(1, p.pair ? h->grid / 2 : h->grid);
-    return (items + G - 1) / G * p.BN;
-}
-
 // The planner's N tile for C > 256 channels is 256 (or the multiple of 64 with
-// the least padding); when the last scheduling round of those tiles is
-// nearly empty, 192-channel tiles can fill the rounds better.  Measured on
-// GB300 for the ResNet-50 layers: the 1x1 512 -> 2048 channel layer at 7x7
-// (98 M tiles x 2 N tiles over 76 CTA pairs = 1.29 rounds) runs 31.9 ->
-// 27.0 us with 192-channel tiles (3 N tiles, 1.93 rounds); every other layer
-// runs slower with them.  So 192 is taken only when its rounds x width comes
-// out at least 10 % below the default's.
-int choose_plan_bn(int N, int H, int W, int C, int K, int R, int S, int stride, int pad, int dil, int dtype,
-                   int epilogue, int num_sms, const PlanOpts &opt)
+// the least padding).  192-channel tiles, which fill the last scheduling round
+// of the 1x1 512 -> 2048 channel layer at 7x7 better (147 pair items, 1.93
+// rounds, against 98, 1.29 rounds), measured faster once (31.9 -> 27.0 us)
+// but slower since the CTA pairs' accumulator hand-back got cheaper (29.5 us
+// with 256, 30.8 with 192), so the planner no longer picks them by itself:
+// CDG_BN=192 asks for them, and cdg_autotune times them.
+int choose_plan_bn(int, int, int, int, int, int, int, int, int, int, int, int, int, const PlanOpts &opt)
 {
-    if (opt.bn > 0 || C <= 256 || opt.max_bn != 256 || (epilogue & CDG_EPI_RELU_BWD_BITS)) return opt.bn;
-    cdg_handle_t a = nullptr, b = nullptr;
-    PlanOpts o192 = opt;
-    o192.bn = 192;
-    int bn = 0;
-    if (make_plan(N, H, W, C, K, R, S, stride, pad, dil, dtype, epilogue, num_sms, true, opt, &a) == CDG_OK &&
-        make_plan(N, H, W, C, K, R, S, stride, pad, dil, dtype, epilogue, num_sms, true, o192, &b) == CDG_OK &&
-        b->prm.BN == 192 && 10 * round_cost(b) <= 9 * round_cost(a))
-        bn = 192;
-    cdg_destroy(a);
-    cdg_destroy(b);
-    return bn;
+    return opt.bn;
 }
 
 }  // namespace

@@ -61,17 +61,17 @@ def test_wgrad_planner_sweep():
     assert planned > 150
 
 
-def test_192_channel_tiles_only_where_they_fill_the_rounds():
-    """For C > 256 the planner compares scheduling rounds x tile width of the
-    items with taps for 256- and 192-channel N tiles, and takes 192 only when
-    that saves at least 10 %: among the ResNet-50 layers, the 1x1 512 -> 2048
-    layer at 7x7 (98 M tiles x 2 N tiles over 76 CTA pairs = 1.29 rounds
-    against 147 pair items = 1.93 rounds)."""
+def test_no_192_channel_tiles_unless_asked(monkeypatch):
+    """For C > 256 the planner takes 256-channel N tiles (or the multiple of 64
+    with the least padding); 192-channel tiles only when asked (CDG_BN=192),
+    e.g. the 1x1 512 -> 2048 layer at 7x7 as 147 pair items instead of 98."""
     import implicit_gemm_dgrad_gb300 as cdg
     from implicit_gemm_dgrad_gb300.workloads import RESNET50_B256
     for L in RESNET50_B256:
         inf = cdg.plan_host(L.N, L.H, L.W, L.C, L.K, L.R, L.S, L.stride, L.pad, L.dil, L.dtype, num_sms=152).info()
+        assert inf["tile_n"] in (64, 128, 256), (L.name, inf["tile_n"])
         if L.name.startswith("L19"):
-            assert (inf["tile_n"], inf["cta_pair"], inf["work_items"]) == (192, 1, 147)
-        else:
-            assert inf["tile_n"] in (64, 128, 256), (L.name, inf["tile_n"])
+            assert (inf["tile_n"], inf["cta_pair"], inf["work_items"]) == (256, 1, 98)
+    monkeypatch.setenv("CDG_BN", "192")
+    inf = cdg.plan_host(256, 7, 7, 512, 2048, 1, 1, 1, 0, 1, "bf16", num_sms=152).info()
+    assert (inf["tile_n"], inf["cta_pair"], inf["work_items"]) == (192, 1, 147)
