@@ -131,7 +131,8 @@ struct Ring {
     uint32_t out0;         // first of the 16 KB output staging buffers (two; four when gated by the activation)
     uint32_t full0, empty0;
     uint32_t acc_full0, acc_empty0, drain;
-    uint32_t gfull0;       // gate loads: four mbarriers
+    uint32_t gfull0;       // gate loads: eight mbarriers
+    uint32_t gfree0;       // activation gate issued by a loader warp: eight "staging buffer free" mbarriers
     uint32_t gate0;        // packed-mask ring (four CDG_GATE_SLOT slots)
     uint32_t red0;         // per-channel sums: the warps' partials of one chunk, [sum][warp][64] fp32
 };
@@ -850,7 +851,7 @@ __device__ __forceinline__ void gate_mask(float *v, uint32_t bits)
 // enlarges another's unrolled per-element loop.
 template <int OUT_T, bool MASK, int IN_T, bool HALO, bool PAIR, bool DUAL, int EPI>
 __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, const CdgPhase *tab, Ctl ctl,
-                                             uint32_t tmem_base, Sched S)
+                                             uint32_t tmem_base, Sched S, volatile uint32_t *gate_used_sh)
 {
     constexpr int OSZ = OUT_T == CDG_T_F32 ? 4 : 2;
     constexpr int CH = 128 / OSZ;  // channels per 128-byte staging row
@@ -960,7 +961,12 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
         gc.next(gstep, BN);
         gate_prefetch();
     };
-    if (MASK) {
+    // Per-tap and row plans gated by the activation: loader warp 3 issues the
+    // activation tiles (run_gate_issuer), so no epilogue thread is held by a
+    // TMA issue; the epilogue only signals, on R.gfree0, each staging buffer
+    // that its store has finished reading.
+    const bool xg_ext = MASK && !HALO && !DUAL && !mask_bits;
+    if (MASK && !xg_ext) {
         const int ahead = mask_bits ? 3 : static_cast<int>(nbuf) - 2;
         // skip the prefetch cursor past the loads issued at once, then run it
         // kGatePrefetch* loads further
@@ -1046,7 +1052,11 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
             // the store of chunk k-2 (issued by warp (k-2) % 4) must be done
             // reading its buffer: with two buffers that is this chunk's, with
             // nbuf it is the one chunk k + nbuf - 2's gate goes into
-            if (k >= 2 && elected && static_cast<uint32_t>(ew) == ((k - 2) & 3u)) bulk_wait_group_read<0>();
+            if (k >= 2 && elected && static_cast<uint32_t>(ew) == ((k - 2) & 3u)) {
+                bulk_wait_group_read<0>();
+                // staging buffer (k - 2) % nbuf is free: gate load k - 2 + nbuf may land in it
+                if (xg_ext) mbar_arrive(R.gfree0 + 8u * ((k - 2u) & 7u));
+            }
             named_bar_sync(1, 128);
             uint32_t gw[2] = {0u, 0u};  // packed mask: the chunk's bits 0-31 and 32-63
             uint32_t xf[OSZ == 4 ? 16 : 1];  // fp32 output: the chunk's 32 activation values
@@ -1062,7 +1072,7 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
                     break;
                 }
                 ++g_used;
-                gate_ahead();  // chunk k + nbuf - 2 into the buffer store k - 2 has finished reading
+                if (!xg_ext) gate_ahead();  // chunk k + nbuf - 2 into the buffer store k - 2 has finished reading
                 if (OSZ == 4) {
                     // fp32 output: the activation tile holds 64-byte rows; read this
                     // row before any thread writes the wider output over the buffer
@@ -1202,6 +1212,7 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
         for (int c = ethread; c < C; c += CH)
             for (int k = 0; k < nsum; ++k) row_out[k * C + c] = ld_shared_f32(red_acc0 + 4u * static_cast<uint32_t>(k * C + c));
     }
+    if (xg_ext && ew == 0 && elected) *gate_used_sh = g_used;  // for the abort drain
     if (MASK && ew == 0 && elected && g_used != g_issued) {
         // aborted: let the gate loads still in flight land before the CTA exits
         volatile uint32_t no_abort = 0;
@@ -1214,6 +1225,31 @@ __device__ __forceinline__ void run_epilogue(const CdgParams &p, const Ring &R, 
         }
     }
     if (elected) bulk_wait_group_all();
+}
+
+// Gate issuer (per-tap and row plans gated by the saved activation): loader
+// warp 3 walks the chunk sequence of the epilogue and loads chunk n's
+// activation tile into staging buffer n % nbuf on gate barrier n % 8, once
+// the epilogue has signalled (R.gfree0, barrier (n - nbuf) % 8) that store
+// n - nbuf, the buffer's previous user, has finished reading it.  The count
+// of issued loads goes to *issued_sh for the abort drain.
+__device__ __forceinline__ void run_gate_issuer(const CdgParams &p, const Ring &R, const CdgPhase *tab, Ctl ctl,
+                                                Sched S, int ch, volatile uint32_t *issued_sh)
+{
+    const bool leader = elect_one_sync();
+    const uint32_t nbuf = static_cast<uint32_t>(p.gate_bufs);
+    GateCursor gc{ItemWalk(tab, p, S.start, S.step), 0};
+    uint32_t n = 0;
+    for (; gc.valid(); ++n) {
+        if (n >= nbuf) {
+            const uint32_t f = n - nbuf;
+            if (!wait_bar(R.gfree0 + 8u * (f & 7u), (f >> 3) & 1u, ctl)) break;
+        }
+        if (leader) gate_issue<false>(p, gc, S, R.out0 + (n % nbuf) * (128u * 128u), R.gfull0 + 8u * (n & 7u));
+        __syncwarp();
+        gc.next(ch, p.BN);
+    }
+    if (leader) *issued_sh = n;
 }
 
 // ------------------------------------------------------------------ kernel
@@ -1260,21 +1296,29 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_cons
     // and a shared barrier could then be waited on two phases ahead, whose
     // parity test would pass on the older phase.
     const int nfull = (HALO && DUAL) ? stages + p.a_stages : stages;
+    // per-tap and row kernels with a gate: eight more barriers, on which the
+    // epilogue frees staging buffers for the gate issuer (activation gate);
+    // such plans have at most eight stages, so all fits the 384-byte area
+    constexpr int kGfree = (MASK && !HALO && !DUAL) ? 8 : 0;
     R.full0 = bars;
     R.empty0 = bars + 8u * nfull;
     R.acc_full0 = bars + 8u * (nfull + stages);
     R.acc_empty0 = R.acc_full0 + 32u;
     R.drain = R.acc_full0 + 64u;
     R.gfull0 = R.acc_full0 + 80u;
+    R.gfree0 = R.gfull0 + 64u;
     R.red0 = bars + CDG_SMEM_TAIL;  // only plans with per-channel sums reserve it
     uint8_t *const tail = smem_raw + (bars - raw);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tail + 8 * (nfull + stages + 18));
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tail + 8 * (nfull + stages + 18 + kGfree));
     volatile uint32_t *abort_flag = tmem_slot + 1;
     volatile uint32_t *slot_parity = tmem_slot + 2;  // [nfull]: the planner keeps all of it within the tables' offset
+    volatile uint32_t *gate_counts = slot_parity + nfull;  // gate loads issued, consumed (activation gate issuer)
     CdgPhase *tab = reinterpret_cast<CdgPhase *>(tail + CDG_SMEM_TABLES);
     CdgTap *taps = reinterpret_cast<CdgTap *>(tab + CDG_MAX_PHASES);
-    static_assert(8 * (2 * CDG_MAX_STAGES_TOTAL + 18) + 8 + 4 * CDG_MAX_STAGES_TOTAL <= CDG_SMEM_TABLES,
+    static_assert(8 * (2 * CDG_MAX_STAGES_TOTAL + 18) + 8 + 4 * CDG_MAX_STAGES_TOTAL + 8 <= CDG_SMEM_TABLES,
                   "mbarrier area overflows");
+    // per-tap and row plans have at most eight stages (kMaxStages in the planner)
+    static_assert(8 * (2 * 8 + 18 + 8) + 8 + 4 * 8 + 8 <= CDG_SMEM_TABLES, "gate-issuer barriers overflow");
     static_assert(CDG_SMEM_TABLES + CDG_MAX_PHASES * sizeof(CdgPhase) + CDG_MAX_TAPS * sizeof(CdgTap) <=
                       CDG_SMEM_TAIL,
                   "phase and tap tables overflow the shared-memory tail");
@@ -1310,8 +1354,11 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_cons
         mbar_init(R.drain, 1);
         mbar_init(R.drain + 8u, 1);
         for (int g = 0; g < 8; ++g) mbar_init(R.gfull0 + 8u * g, 1);
+        for (int g = 0; g < kGfree; ++g) mbar_init(R.gfree0 + 8u * g, 1);
         *abort_flag = 0u;
         for (int s = 0; s < nfull; ++s) slot_parity[s] = 0u;
+        gate_counts[0] = 0u;
+        gate_counts[1] = 0u;
         fence_mbar_init();
     }
     // Everything above touches only shared memory and kernel parameters.  Global
@@ -1373,7 +1420,7 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_cons
                 wait_bar(Rj.drain, 0, Ctl{&no_abort, p.status, p.wait_limit_ns});
             }
         } else if (warp >= CDG_EPI_WARP0) {
-            run_epilogue<OUT_T, MASK, IN_T, HALO, PAIR, true, EPI>(p, R, tab, ctl, tmem_base, S);
+            run_epilogue<OUT_T, MASK, IN_T, HALO, PAIR, true, EPI>(p, R, tab, ctl, tmem_base, S, gate_counts + 1);
         } else {
             run_loader_halo<PAIR, true>(p, R, tab, taps, ctl, warp == 0 ? 0 : 1, elect_one_sync(), slot_parity, S);
         }
@@ -1382,7 +1429,7 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_cons
             const int j = warp >> 1;
             run_mma<false>(p, ring_of(j), tab, ctl, tmem_base + 2u * j * p.acc_stride, elect_one_sync(), sched_of(j));
         } else if (warp >= CDG_EPI_WARP0) {
-            run_epilogue<OUT_T, MASK, IN_T, false, false, true, EPI>(p, R, tab, ctl, tmem_base, S);
+            run_epilogue<OUT_T, MASK, IN_T, false, false, true, EPI>(p, R, tab, ctl, tmem_base, S, gate_counts + 1);
         } else {
             const int j = warp >> 1;  // warps 0 and 2
             run_loader<false>(p, ring_of(j), tab, taps, ctl, 0, 1, elect_one_sync(),
@@ -1400,15 +1447,29 @@ __global__ void __launch_bounds__(CDG_THREADS, 1) dgrad_kernel(const __grid_cons
             wait_bar(R.drain, 0, Ctl{&no_abort, p.status, p.wait_limit_ns});
         }
     } else if (warp >= CDG_EPI_WARP0) {
-        run_epilogue<OUT_T, MASK, IN_T, HALO, PAIR, false, EPI>(p, R, tab, ctl, tmem_base, S);
+        run_epilogue<OUT_T, MASK, IN_T, HALO, PAIR, false, EPI>(p, R, tab, ctl, tmem_base, S, gate_counts + 1);
     } else if (HALO) {
         run_loader_halo<PAIR>(p, R, tab, taps, ctl, warp == 0 ? 0 : warp - 1, elect_one_sync(), slot_parity, S);
+    } else if (kGfree && !p.mask_bits) {
+        // gated by the saved activation: warps 0 and 2 load the operands,
+        // warp 3 the activation tiles
+        if (warp == 3)
+            run_gate_issuer(p, R, tab, ctl, S, OUT_T == CDG_T_F32 ? 32 : 64, gate_counts);
+        else
+            run_loader<PAIR>(p, R, tab, taps, ctl, warp == 0 ? 0 : 1, 2, elect_one_sync(), slot_parity, S);
     } else {
         run_loader<PAIR>(p, R, tab, taps, ctl, warp == 0 ? 0 : warp - 1, CDG_LOADERS, elect_one_sync(), slot_parity,
                          S);
     }
 
     __syncthreads();
+    if (kGfree && !p.mask_bits && *abort_flag && threadIdx.x == 0) {
+        // activation tiles the issuer loaded and the epilogue never waited for
+        volatile uint32_t no_abort = 0;
+        const Ctl drain_ctl{&no_abort, p.status, p.wait_limit_ns};
+        for (uint32_t n = gate_counts[1]; n < gate_counts[0]; ++n)
+            wait_bar(R.gfull0 + 8u * (n & 7u), (n >> 3) & 1u, drain_ctl);
+    }
     if (*abort_flag && threadIdx.x == 0) {
         if (!PAIR || S.rank == 0) {
             drain_loads(R, nfull, p.status, p.wait_limit_ns, slot_parity);
