@@ -354,7 +354,14 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     const bool pair_ok = BN >= 64 && BN % 16 == 0 && num_sms >= 2;
     const bool pair_forced = halo_forced && opt.pair == 1 && pair_ok;
     const bool pair_auto = opt.halo != 0 && opt.pair != 0 && stride == 1 && BN >= 128 && pair_ok;
-    for (int attempt = pair_forced ? 1 : 0; attempt < 2 && !halo && !flat && opt.halo != 0; ++attempt) {
+    // Gated by the saved activation, plans with per-tap or row boxes let a
+    // loader warp issue the activation tiles (the kernels' gate issuer), and
+    // halo plans do not; measured on GB300 the x-gated 3x3 64 -> 64 layer runs
+    // 99.7 us with per-tap boxes (two MMA warps) against 110.9 with halo boxes,
+    // so such plans take halo boxes only when asked (CDG_HALO=1).
+    const bool xgate = h->mask && !h->mask_bits;
+    const bool halo_allowed = opt.halo != 0 && (!xgate || halo_forced);
+    for (int attempt = pair_forced ? 1 : 0; attempt < 2 && !halo && !flat && halo_allowed; ++attempt) {
         const bool pw = attempt == 1;  // this attempt holds half of the weight rows per CTA
         if (pw && !pair_forced && !pair_auto) break;
         const int b_rows = pw ? BN / 2 : BN;  // weight rows one CTA holds
@@ -480,7 +487,13 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     // (measured on GB300: ~350 cycles per 64-channel stage against ~200 of
     // tensor work); with two, the other warp's MMAs fill that gap.  Tiles of
     // fewer than four stages gain nothing (the epilogue dominates them).
-    bool dual = !halo && !pair && BN <= 128 && max_stages >= 4 && stages_per_tile >= 4.0;
+    // (gated by the activation, dual issue leaves no warp for the gate issuer:
+    // it pays only for long tiles, where one MMA warp's stage hand-offs are
+    // the bound; the x-gated 3x3 s2 128-channel layer runs 112.7 us with one
+    // MMA warp and the issuer against 141.2 with two, the 1x1 128 -> 512 layer
+    // with eight stages a tile 58.9 against 62.4, the 3x3 64-channel layer
+    // with nine stages a tile 140.9 against 99.7)
+    bool dual = !halo && !pair && BN <= 128 && max_stages >= 4 && stages_per_tile >= (xgate ? 9.0 : 4.0);
     // Halo boxes with resident weights: two MMA warps take alternate items
     // from the one halo ring, so that one warp's per-tile hand-offs (commits,
     // item bookkeeping, barrier waits: ~1,400 cycles a tile, measured with a

@@ -214,25 +214,30 @@ def test_halo_operand_mode_with_cta_pairs(L, reach, monkeypatch):
 # the warps) as for ResNet-50's 3x3 64-channel layer, six, two with CTA
 # pairs, four stride-2 phases under the ReLU gate, fp32 output.
 HALO_DUAL_CASES = [
-    (_case(8, 56, 56, 64, 64, 3, 3, 1, 1, 1, "bf16", idx=40), "6", {"a_mode": 3, "mma_warps": 2, "cta_pair": 0}),
-    (_case(16, 12, 12, 64, 64, 3, 3, 1, 1, 1, "bf16", idx=41), "2", {"a_mode": 3, "mma_warps": 2, "cta_pair": 0}),
-    (_case(8, 28, 28, 128, 128, 3, 3, 1, 1, 1, "bf16", idx=42), "6", {"a_mode": 3, "mma_warps": 2, "cta_pair": 1}),
-    (_case(8, 14, 14, 64, 64, 3, 3, 2, 1, 1, "bf16", relu=True, idx=43), "2", {"a_mode": 3, "mma_warps": 2}),
-    (_case(40, 9, 7, 64, 64, 3, 3, 1, 1, 1, "f16", out="f32", relu=True, idx=44), "6", {"a_mode": 3, "mma_warps": 2}),
+    (_case(8, 56, 56, 64, 64, 3, 3, 1, 1, 1, "bf16", idx=40), "CDG_MAX_GRID=6", {"a_mode": 3, "mma_warps": 2, "cta_pair": 0}),
+    (_case(16, 12, 12, 64, 64, 3, 3, 1, 1, 1, "bf16", idx=41), "CDG_MAX_GRID=2", {"a_mode": 3, "mma_warps": 2, "cta_pair": 0}),
+    (_case(8, 28, 28, 128, 128, 3, 3, 1, 1, 1, "bf16", idx=42), "CDG_MAX_GRID=6", {"a_mode": 3, "mma_warps": 2, "cta_pair": 1}),
+    # gated by the activation: halo boxes only when asked
+    (_case(8, 14, 14, 64, 64, 3, 3, 2, 1, 1, "bf16", relu=True, idx=43), "CDG_MAX_GRID=2 CDG_HALO=1", {"a_mode": 3, "mma_warps": 2}),
+    (_case(40, 9, 7, 64, 64, 3, 3, 1, 1, 1, "f16", out="f32", relu=True, idx=44), "CDG_MAX_GRID=6 CDG_HALO=1",
+     {"a_mode": 3, "mma_warps": 2}),
 ]
 
 
-@pytest.mark.parametrize("L,grid,reach", HALO_DUAL_CASES, ids=lambda v: v.name if isinstance(v, Layer) else None)
-def test_halo_dual_issue(L, grid, reach, monkeypatch):
+@pytest.mark.parametrize("L,env,reach", HALO_DUAL_CASES, ids=lambda v: v.name if isinstance(v, Layer) else None)
+def test_halo_dual_issue(L, env, reach, monkeypatch):
     """Halo boxes with resident weights and two MMA warps taking alternate
     items from the one halo ring give the oracle's result."""
     monkeypatch.setenv("CDG_DUAL", "1")
-    monkeypatch.setenv("CDG_MAX_GRID", grid)
+    for kv in env.split():
+        key, val = kv.split("=")
+        monkeypatch.setenv(key, val)
     run, _, _ = check_layer(L)
     info = run.plan.info()
     for k, v in reach.items():
         assert info[k] == v, (k, info)
-    assert info["grid"] <= int(grid) and info["work_items"] >= 4 * (info["grid"] // (2 if info["cta_pair"] else 1))
+    grid = int(dict(kv.split("=") for kv in env.split())["CDG_MAX_GRID"])
+    assert info["grid"] <= grid and info["work_items"] >= 4 * (info["grid"] // (2 if info["cta_pair"] else 1))
 
 
 def test_chained_launches_keep_stream_order():
@@ -375,7 +380,10 @@ GATE_CASES = [
     (_case(3, 13, 11, 200, 72, 1, 1, 1, 0, 1, "bf16", relu=True, idx=14), "", {"a_mode": 1}),  # rows, 8-ch tail chunk
     (_case(2, 14, 14, 64, 128, 1, 1, 2, 0, 1, "bf16", relu=True, idx=15), "", {"a_mode": 1}),  # rows, zero phases
     (_case(2, 13, 13, 64, 64, 1, 1, 2, 0, 1, "f16", relu=True, idx=16), "", {"a_mode": 0}),    # 4-D boxes, zero phases
-    (_case(2, 20, 20, 64, 64, 3, 3, 1, 1, 1, "bf16", relu=True, idx=17), "", {"a_mode": 3}),   # halo, resident weights
+    (_case(2, 20, 20, 64, 64, 3, 3, 1, 1, 1, "bf16", relu=True, idx=17), "CDG_HALO=1", {"a_mode": 3}),  # halo, resident weights
+    # the activation's tiles issued by loader warp 3, many chunks per CTA
+    (_case(4, 16, 16, 128, 64, 3, 3, 2, 1, 1, "bf16", relu=True, idx=24), "CDG_MAX_GRID=2", {"a_mode": 0, "mma_warps": 1}),
+    (_case(2, 14, 14, 256, 128, 1, 1, 1, 0, 1, "bf16", relu=True, idx=25), "CDG_MAX_GRID=2", {"a_mode": 1, "mma_warps": 1}),
     (_case(2, 12, 12, 128, 128, 3, 3, 1, 1, 1, "bf16", relu=True, idx=18), "CDG_HALO=1", {"a_mode": 2}),
     (_case(2, 12, 12, 128, 128, 3, 3, 1, 1, 1, "bf16", relu=True, idx=23), "CDG_HALO=1 CDG_PAIR=1",
      {"cta_pair": 1}),

@@ -97,7 +97,7 @@ EXACT = [
     (_case(3, 13, 11, 200, 72, 1, 1, 1, 0, 1, idx=0), 1, "x", "", {"a_mode": 1}),            # rows, C tail
     (_case(2, 14, 14, 64, 128, 1, 1, 2, 0, 1, idx=1), 1, "x", "", {"a_mode": 1}),            # whole rows, zero phases
     (_case(2, 13, 13, 64, 64, 1, 1, 2, 0, 1, "f16", idx=2), 1, "x", "", {"a_mode": 0}),      # boxes, zero phases
-    (_case(2, 20, 20, 64, 64, 3, 3, 1, 1, 1, relu=True, idx=3), 2, "x", "", {"a_mode": 3}),   # halo, resident
+    (_case(2, 20, 20, 64, 64, 3, 3, 1, 1, 1, relu=True, idx=3), 2, "x", "CDG_HALO=1", {"a_mode": 3}),  # halo, resident
     (_case(2, 12, 12, 128, 128, 3, 3, 1, 1, 1, relu=True, idx=4), 2, "x", "CDG_HALO=1", {"a_mode": 2}),
     (_case(2, 14, 14, 256, 256, 3, 3, 1, 1, 1, relu=True, idx=5), 2, "x", "", {"cta_pair": 1}),
     (_case(4, 16, 16, 128, 256, 3, 3, 2, 1, 1, relu=True, idx=6), 2, "x", "", {"mma_warps": 2}),

@@ -34,8 +34,8 @@ CASES = [
     # dY rows as a matrix (1x1), four K blocks per tile
     (Layer("to_1x1_rows", 4, 14, 14, 64, 256, 1, 1, 1, 0, 1, dtype="bf16", workload=12, index=2),
      "", 1, {"a_mode": 1}),
-    # strided phases and the gate from the saved activation, whose tiles the
-    # epilogue loads ahead and must let land before leaving
+    # strided phases and the gate from the saved activation, whose tiles loader
+    # warp 3 loads ahead; those in flight must land before the CTA leaves
     (Layer("to_3x3s2_c256_relu", 2, 14, 14, 256, 128, 3, 3, 2, 1, 1, dtype="bf16", relu=True, workload=12,
            index=3), "CDG_PAIR=0", 3, {"a_mode": 0, "cta_pair": 0}),
 ]
