@@ -345,15 +345,17 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     int hwb = 0, hwt = 0, hbh = 0, hhb = 0, hrows = 0, a_stages = 0, b_stages = 0, b_res_bytes = 0, halo_tg = 1;
     const bool halo_forced = opt.halo == 1;
     // Halo boxes with CTA pairs: each CTA of a pair holds its own tile's halo
-    // box and half of every weight tile, so twice the filter fits resident.
-    // Taken when both are asked for (CDG_HALO=1 CDG_PAIR=1), and by default
-    // for stride-1 layers whose filter is resident only as halves, with N
-    // tiles of at least 128 channels (measured on GB300, ResNet-50 3x3
-    // 128 -> 128 at 28x28: 45.6 us against 57.3 us with per-tap boxes; the
-    // 64-channel, strided and streamed-weight cases measured slower).
+    // box and half of every weight tile, so twice the filter fits resident,
+    // and each SM reads half of B per MMA.  Taken when both are asked for
+    // (CDG_HALO=1 CDG_PAIR=1; CDG_HALO=1 alone keeps single CTAs), and by
+    // default, tried first, for stride-1 layers whose filter is resident as
+    // halves (measured on GB300, ResNet-50
+    // 3x3 128 -> 128 at 28x28: 45.6 us against 57.3 us with per-tap boxes; 3x3
+    // 64 -> 64 at 56x56, both with two MMA warps: 53.4 us against 56.8 in
+    // single CTAs; the strided and streamed-weight cases measured slower).
     const bool pair_ok = BN >= 64 && BN % 16 == 0 && num_sms >= 2;
     const bool pair_forced = halo_forced && opt.pair == 1 && pair_ok;
-    const bool pair_auto = opt.halo != 0 && opt.pair != 0 && stride == 1 && BN >= 128 && pair_ok;
+    const bool pair_auto = !halo_forced && opt.halo != 0 && opt.pair != 0 && stride == 1 && pair_ok;
     // Gated by the saved activation, plans with per-tap or row boxes let a
     // loader warp issue the activation tiles (the kernels' gate issuer), and
     // halo plans do not; measured on GB300 the x-gated 3x3 64 -> 64 layer runs
@@ -361,9 +363,11 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     // so such plans take halo boxes only when asked (CDG_HALO=1).
     const bool xgate = h->mask && !h->mask_bits;
     const bool halo_allowed = opt.halo != 0 && (!xgate || halo_forced);
-    for (int attempt = pair_forced ? 1 : 0; attempt < 2 && !halo && !flat && halo_allowed; ++attempt) {
-        const bool pw = attempt == 1;  // this attempt holds half of the weight rows per CTA
-        if (pw && !pair_forced && !pair_auto) break;
+    // attempts: resident halves in CTA pairs first where pairs may be taken,
+    // then a single CTA (forced pairs: the pair attempt only)
+    const int n_attempts = pair_forced ? 1 : (pair_auto ? 2 : 1);
+    for (int attempt = 0; attempt < n_attempts && !halo && !flat && halo_allowed; ++attempt) {
+        const bool pw = pair_forced || (pair_auto && attempt == 0);  // half of the weight rows per CTA
         const int b_rows = pw ? BN / 2 : BN;  // weight rows one CTA holds
         int span_r = 0, span_s = 0, wt = 0, hmax = 0, maxtaps = 0;
         for (const CdgPhase &f : phases) {
@@ -410,7 +414,8 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
             bs = 1;  // one barrier: the resident weights have landed
             tg = 1;
         }
-        // streamed weights only when asked; by default pairs only with resident halves
+        // streamed weights only when asked (by default pairs only with resident
+        // halves; a single CTA falls back to streamed weights only when asked)
         const bool take = pw && !pair_forced ? res : (res || halo_forced);
         if (hb <= 256 && bs >= (res ? 1 : 2) && take) {
             halo = true;
@@ -1319,7 +1324,8 @@ int fused_make(int N, int H, int W, int C1, int C2, int K2, int R2, int S2, int 
     opt.halo = 1;
     opt.bn = 0;
     opt.gate_bufs = 4;  // the fused kernel lays out its own shared memory
-    opt.dual = 0;       // and issues its MMAs from one warp
+    opt.dual = 0;       // and issues its MMAs from one warp,
+    opt.pair = 0;       // in single CTAs
     cdg_handle_t g = nullptr;
     int rc = make_plan(N, H, W, C2, K2, R2, S2, 1, pad2, dil2, dtype, flags & gates, num_sms, host_only, opt, &g);
     if (rc != CDG_OK) return rc;

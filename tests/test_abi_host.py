@@ -169,16 +169,20 @@ def test_workload_plans():
 
 
 def test_halo_resident_weights_when_the_filter_fits(monkeypatch):
-    """A filter whose packed weights for the one N tile fit beside two halo
-    stages is kept resident with halo operand boxes (a_mode 3, the default).
-    A stride-1 filter that fits only as halves (N tile of 128 channels or
-    more) is kept resident by CTA pairs, half in each CTA.  Otherwise the
-    default is per-tap boxes (a_mode 0), with streamed halo weights only when
-    asked (a_mode 2).  CDG_HALO=0 turns halo mode off, and CDG_PAIR=0 the pairs."""
+    """A stride-1 filter whose packed weights fit resident as halves is kept
+    resident by CTA pairs, half in each CTA (a_mode 3, cta_pair 1, the
+    default); with pairs off, a filter that fits one CTA beside two halo
+    stages is kept resident there.  Otherwise the default is per-tap boxes
+    (a_mode 0), with streamed halo weights only when asked (a_mode 2).
+    CDG_HALO=0 turns halo mode off, and CDG_PAIR=0 the pairs."""
     monkeypatch.delenv("CDG_HALO", raising=False)
     monkeypatch.delenv("CDG_PAIR", raising=False)
     small = cdg.plan_host(256, 56, 56, 64, 64, 3, 3, 1, 1, 1, "bf16", num_sms=148).info()
-    assert small["a_mode"] == 3 and small["cta_pair"] == 0 and small["smem_bytes"] <= 232448
+    assert small["a_mode"] == 3 and small["cta_pair"] == 1 and small["smem_bytes"] <= 232448
+    monkeypatch.setenv("CDG_PAIR", "0")
+    small = cdg.plan_host(256, 56, 56, 64, 64, 3, 3, 1, 1, 1, "bf16", num_sms=148).info()
+    assert small["a_mode"] == 3 and small["cta_pair"] == 0
+    monkeypatch.delenv("CDG_PAIR")
     halves = cdg.plan_host(256, 28, 28, 128, 128, 3, 3, 1, 1, 1, "bf16", num_sms=148).info()
     assert halves["a_mode"] == 3 and halves["cta_pair"] == 1 and halves["smem_bytes"] <= 232448
     # strided, or too large even as halves: per-tap boxes
@@ -204,7 +208,9 @@ def test_grid_cap_and_dual_halo_option(monkeypatch):
     and at most six halo stages."""
     monkeypatch.setenv("CDG_MAX_GRID", "5")
     info = cdg.plan_host(256, 56, 56, 64, 64, 3, 3, 1, 1, 1, "bf16", num_sms=152).info()
-    assert info["grid"] == 5
+    assert info["cta_pair"] == 1 and info["grid"] == 4
+    info = cdg.plan_host(256, 56, 56, 64, 64, 1, 1, 1, 0, 1, "bf16", num_sms=152).info()
+    assert info["cta_pair"] == 0 and info["grid"] == 5
     info = cdg.plan_host(256, 28, 28, 128, 128, 3, 3, 1, 1, 1, "bf16", num_sms=152).info()
     assert info["cta_pair"] == 1 and info["grid"] == 4
     monkeypatch.setenv("CDG_MAX_GRID", "1")

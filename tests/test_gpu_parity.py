@@ -208,14 +208,19 @@ def test_halo_operand_mode_with_cta_pairs(L, reach, monkeypatch):
         assert info[k] == v, (k, info)
 
 
-# two MMA warps over the halo ring (opt-in: CDG_DUAL=1).  The grid is capped
+# two MMA warps over the halo ring (the planner's choice for halo plans with
+# resident weights; the test also sets CDG_DUAL=1).  The grid is capped
 # (CDG_MAX_GRID) so that every CTA walks many items and the halo ring wraps
 # around many times: three halo stages (odd, so a stage alternates between
-# the warps) as for ResNet-50's 3x3 64-channel layer, six, two with CTA
-# pairs, four stride-2 phases under the ReLU gate, fp32 output.
+# the warps) as in single CTAs of ResNet-50's 3x3 64-channel layer, six, CTA
+# pairs at 64 and 128 channels, four stride-2 phases under the ReLU gate,
+# fp32 output.
 HALO_DUAL_CASES = [
-    (_case(8, 56, 56, 64, 64, 3, 3, 1, 1, 1, "bf16", idx=40), "CDG_MAX_GRID=6", {"a_mode": 3, "mma_warps": 2, "cta_pair": 0}),
-    (_case(16, 12, 12, 64, 64, 3, 3, 1, 1, 1, "bf16", idx=41), "CDG_MAX_GRID=2", {"a_mode": 3, "mma_warps": 2, "cta_pair": 0}),
+    (_case(8, 56, 56, 64, 64, 3, 3, 1, 1, 1, "bf16", idx=40), "CDG_MAX_GRID=6 CDG_PAIR=0",
+     {"a_mode": 3, "mma_warps": 2, "cta_pair": 0}),
+    (_case(16, 12, 12, 64, 64, 3, 3, 1, 1, 1, "bf16", idx=41), "CDG_MAX_GRID=2 CDG_PAIR=0",
+     {"a_mode": 3, "mma_warps": 2, "cta_pair": 0}),
+    (_case(8, 56, 56, 64, 64, 3, 3, 1, 1, 1, "bf16", idx=45), "CDG_MAX_GRID=6", {"a_mode": 3, "mma_warps": 2, "cta_pair": 1}),
     (_case(8, 28, 28, 128, 128, 3, 3, 1, 1, 1, "bf16", idx=42), "CDG_MAX_GRID=6", {"a_mode": 3, "mma_warps": 2, "cta_pair": 1}),
     # gated by the activation: halo boxes only when asked
     (_case(8, 14, 14, 64, 64, 3, 3, 2, 1, 1, "bf16", relu=True, idx=43), "CDG_MAX_GRID=2 CDG_HALO=1", {"a_mode": 3, "mma_warps": 2}),
