@@ -445,7 +445,7 @@ class WgradInfo(ctypes.Structure):
     _fields_ = [("P", ctypes.c_int), ("Q", ctypes.c_int), ("tile_m", ctypes.c_int), ("tile_n", ctypes.c_int),
                 ("taps_per_item", ctypes.c_int), ("splits", ctypes.c_int), ("pos_box", ctypes.c_int * 3), ("blocks", ctypes.c_int),
                 ("stages", ctypes.c_int), ("work_items", ctypes.c_int), ("grid", ctypes.c_int),
-                ("smem_bytes", ctypes.c_int), ("tmem_cols", ctypes.c_int)]
+                ("smem_bytes", ctypes.c_int), ("tmem_cols", ctypes.c_int), ("x_major", ctypes.c_int)]
 
     def as_dict(self) -> dict:
         d = {name: getattr(self, name) for name, _ in self._fields_}

@@ -154,6 +154,23 @@ int make_wgrad_plan(int N, int H, int W, int C, int K, int R, int S, int stride,
         p.G = ceil_div(p.T, ng);
     }
     p.ngroups = ceil_div(p.T, p.G);
+    // x-major tiles when the dY channels fill at most half of a 128-row M
+    // tile, for 1x1 filters with at least two 64-channel slices of x to pair
+    // (measured on GB300: the 1x1 256 -> 64 layer at 56x56 99.3 -> 92.5 us).
+    // With taps paired along M every item reads its dY block again (the 3x3
+    // 64 -> 64 layer: five items a split against three tap groups), and that
+    // layer measured slower (113.0 -> 116.3 us), so filters with more taps
+    // keep the dY-channel tiles.
+    p.cslices = ceil_div(C, 64);
+    p.units = p.T * p.cslices;
+    p.xm = (K <= 64 && p.T == 1 && p.units >= 2) ? 1 : 0;
+    if (p.xm) {
+        p.BN = 64;
+        p.G = 1;
+        p.ngroups = 1;
+        p.tiles_m = ceil_div(p.units, 2);
+        p.tiles_n = 1;
+    }
     const int tiles = p.ngroups * p.tiles_m * p.tiles_n;
     int splits = splits_req;
     // default: as many splits as fit in one wave of work items
@@ -161,6 +178,8 @@ int make_wgrad_plan(int N, int H, int W, int C, int K, int R, int S, int stride,
     splits = std::max(1, std::min(splits, p.nblk));
     p.splits = splits;
     p.total_items = splits * tiles;
+    // A: two 8 KB slices (dY channels, or x-major: two units of x); B: the x
+    // slices of the item's taps (x-major: one dY slice)
     p.stage_bytes = static_cast<uint32_t>(2 * 64 * 128 + p.G * (p.BN / 64) * 64 * 128);
     p.stages = std::min(kMaxStages, (kMaxSmem - 1024 - CDG_SMEM_STAGING - CDG_SMEM_TAIL) / static_cast<int>(p.stage_bytes));
     const uint32_t ab = dtype == CDG_BF16 ? 1u : 0u;
@@ -189,6 +208,7 @@ int make_wgrad_plan(int N, int H, int W, int C, int K, int R, int S, int stride,
     std::memset(&inf, 0, sizeof inf);
     inf.P = P; inf.Q = Q;
     inf.tile_m = 128; inf.tile_n = p.BN;
+    inf.x_major = p.xm;
     inf.taps_per_item = p.G;
     inf.splits = splits;
     inf.pos_box[0] = p.qb; inf.pos_box[1] = p.pb; inf.pos_box[2] = p.nb;
@@ -250,6 +270,12 @@ int encode_wgrad_maps(cdg_wgrad_st *h, const void *dY, const void *x, void *ws)
         if (enc(&p.tmW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ws, dims, strides, wbox, ones,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return CDG_ERR_CUDA;
+        // x-major tiles: 32 dY channels x one tap x 64 x channels, rows of 256 bytes
+        const cuuint32_t xbox[4] = {64, 1, 32, 1};
+        if (p.xm && enc(&p.tmWx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ws, dims, strides, xbox, ones,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return CDG_ERR_CUDA;
     }
     h->cached_dY = dY;

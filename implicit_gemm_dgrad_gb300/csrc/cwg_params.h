@@ -18,6 +18,7 @@ struct CwgParams {
     CUtensorMap tmB[CDG_MAX_PHASES];   // x per phase (h mod stride, w mod stride): 4-D
                                        // {C, wph, hph, N} over the phase sub-grid, boxes {64, qb, pb, nb}
     CUtensorMap tmW;                   // workspace: 4-D {C, T, K, splits} fp32, boxes {32, 1, 128, 1}
+    CUtensorMap tmWx;                  // the same workspace, boxes {64, 1, 32, 1} (x-major tiles, below)
     int *status;
     int N, H, W, C, K, P, Q, stride;
     int T;                // filter taps R*S
@@ -35,6 +36,13 @@ struct CwgParams {
     uint32_t stage_bytes; // A (2 slices x 8 KB) + B (G*BN/64 slices x 8 KB)
     uint32_t tmem_cols;   // two accumulators
     uint32_t acc_stride;
+    // x-major tiles (K <= 64, where a 128-row tile of dY channels would leave
+    // half of its rows idle): M = two units of (tap t, 64-channel slice cs of
+    // x), unit u = t * cslices + cs, units 2m and 2m + 1 in M tile m; N = the
+    // dY channels (64, zero-filled past K); the accumulator holds dW^T rows
+    // (t, c), stored transposed through shared memory
+    int xm;
+    int cslices, units;   // x-major: 64-channel slices of x, and T * cslices
     int16_t tap_phase[CDG_MAX_TAPS];  // phase index (ph*stride + pw) of tap t
     int16_t tap_di[CDG_MAX_TAPS];     // row offset of tap t in its phase sub-grid: h = stride*(p + di) + ph
     int16_t tap_dj[CDG_MAX_TAPS];     // column offset: w = stride*(q + dj) + pw

@@ -826,17 +826,6 @@ __device__ __forceinline__ void warp_transpose_sum(float (&a)[N], int lane)
     }
 }
 
-__device__ __forceinline__ void st_shared_f32(uint32_t addr, float v)
-{
-    asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
-__device__ __forceinline__ float ld_shared_f32(uint32_t addr)
-{
-    float v;
-    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-    return v;
-}
-
 template <int PER>
 __device__ __forceinline__ void gate_mask(float *v, uint32_t bits)
 {

@@ -112,6 +112,21 @@ __device__ __forceinline__ void run_wg_loader(const CwgParams &p, const WgRing &
                     const uint32_t full = R.full0 + 8u * stage;
                     const uint32_t sa = R.s0 + static_cast<uint32_t>(stage) * p.stage_bytes;
                     mbar_arrive_expect_tx(full, tx);
+                    if (p.xm) {
+                        // x-major: A = x slices of units 2 mt and 2 mt + 1 (a unit
+                        // past the last loads a box wholly past the images: zeros,
+                        // never stored), B = the dY slice
+                        for (int hf = 0; hf < 2; ++hf) {
+                            const int u = 2 * it.mt + hf;
+                            const bool real = u < p.units;
+                            const int t = real ? u / p.cslices : p.T - 1;
+                            const int cs = real ? u - (u / p.cslices) * p.cslices : 0;
+                            const uint64_t mapB = reinterpret_cast<uint64_t>(&p.tmB[p.tap_phase[t]]);
+                            tma_load_4d(sa + static_cast<uint32_t>(hf) * kSlice, mapB, full, 64 * cs, q0 + p.tap_dj[t],
+                                        p0 + p.tap_di[t], real ? n0 : n0 + p.N);
+                        }
+                        tma_load_4d(sa + 2 * kSlice, mapA, full, 0, q0, p0, n0);
+                    } else {
                     tma_load_4d(sa, mapA, full, k0, q0, p0, n0);
                     tma_load_4d(sa + kSlice, mapA, full, k0 + 64, q0, p0, n0);
                     for (int u = 0; u < p.G; ++u) {
@@ -123,6 +138,7 @@ __device__ __forceinline__ void run_wg_loader(const CwgParams &p, const WgRing &
                         for (int j = 0; j < nbs; ++j)
                             tma_load_4d(sa + static_cast<uint32_t>((2 + u * nbs + j) * kSlice), mapB, full, c0 + 64 * j,
                                         q0 + p.tap_dj[t], p0 + p.tap_di[t], nz);
+                    }
                     }
                 }
                 __syncwarp();
@@ -193,6 +209,7 @@ __device__ __forceinline__ void run_wg_epilogue(const CwgParams &p, const WgRing
     const int row = quad * 32 + lane;
     const uint32_t srow_off = static_cast<uint32_t>(row) * 128u, sw = static_cast<uint32_t>(row & 7);
     const uint64_t mapW = reinterpret_cast<uint64_t>(&p.tmW);
+    const uint64_t mapWx = reinterpret_cast<uint64_t>(&p.tmWx);
     uint32_t acc_count = 0, chunk = 0;
     for (int g = blockIdx.x; g < p.total_items; g += gridDim.x) {
         const WgItem it(p, g);
@@ -214,6 +231,27 @@ __device__ __forceinline__ void run_wg_epilogue(const CwgParams &p, const WgRing
                 tc_fence_before();
                 __syncwarp();
                 if (elected) mbar_arrive(R.acc_empty0 + 8u * acc);
+            }
+            if (p.xm) {
+                // x-major: row = (unit 2 mt + row / 64, x channel row % 64), columns
+                // = dY channels cc .. cc + 31.  Transposed into [dY channel][x
+                // channel] rows of 256 bytes, one 8 KB half per unit: a warp
+                // writes one 128-byte run per dY channel.
+                const uint32_t dst = buf + static_cast<uint32_t>(row / 64) * 8192u + static_cast<uint32_t>(row % 64) * 4u;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) st_shared_f32(dst + static_cast<uint32_t>(j) * 256u, __uint_as_float(r[j]));
+                fence_proxy_async_smem();
+                named_bar_sync(1, 128);
+                if (cc < p.K && elected && static_cast<uint32_t>(ew) == (k & 3u)) {  // dY channels cc.. exist
+                    for (int hf = 0; hf < 2; ++hf) {
+                        const int u = 2 * it.mt + hf;
+                        if (u >= p.units) break;
+                        const int t = u / p.cslices, cs = u - (u / p.cslices) * p.cslices;
+                        tma_store_4d(mapWx, buf + static_cast<uint32_t>(hf) * 8192u, 64 * cs, t, cc, it.split);
+                    }
+                    bulk_commit_group();
+                }
+                continue;
             }
 #pragma unroll
             for (int q = 0; q < 8; ++q)

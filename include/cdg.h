@@ -435,6 +435,10 @@ typedef struct {
     int grid;             /* persistent CTAs                                      */
     int smem_bytes;       /* dynamic shared memory per CTA                        */
     int tmem_cols;        /* tensor-memory columns per CTA                        */
+    int x_major;          /* 1 (1x1 filters, K <= 64, C > 64): M tiles pair two   */
+                          /* 64-channel slices of x and N runs over the dY        */
+                          /* channels, so that no M row is idle; tile_m/tile_n    */
+                          /* then count x channels / dY channels                  */
 } cdg_wgrad_info_t;
 
 /*

@@ -371,7 +371,10 @@ def test_wgrad_plans(shape):
     assert 1 <= G and G * i["tile_n"] <= 256
     if -(-C // i["tile_n"]) > 1:
         assert G == 1
-    tiles = -(-(R * S) // G) * -(-K // 128) * -(-C // i["tile_n"])
+    if i["x_major"]:  # M tiles of two (tap, 64-channel slice of x) units, N = the dY channels
+        tiles = -(-(R * S * -(-C // 64)) // 2)
+    else:
+        tiles = -(-(R * S) // G) * -(-K // 128) * -(-C // i["tile_n"])
     assert i["work_items"] == i["splits"] * tiles
     assert i["work_items"] <= 148 or i["splits"] == 1
     assert p.workspace_bytes == i["splits"] * K * R * S * C * 4

@@ -26,6 +26,9 @@ CASES = [
     (64, 7, 7, 256, 128, 3, 3, 1, 1, 1, "bf16", "same", 0),
     (2, 14, 14, 256, 256, 1, 1, 2, 0, 1, "bf16", "same", 1),
     (2, 10, 9, 64, 64, 5, 1, 1, 2, 1, "bf16", "same", 0),   # taps in groups of 3 and 2
+    (2, 9, 8, 192, 40, 1, 1, 1, 0, 1, "bf16", "f32", 0),    # x-major: 3 slices of x, 40 dY channels
+    (3, 10, 10, 72, 32, 1, 1, 2, 0, 1, "f16", "same", 2),   # x-major: 2 slices, stride 2
+    (4, 12, 12, 256, 64, 1, 1, 1, 0, 1, "bf16", "same", 0), # x-major: the 1x1 256 -> 64 shape
 ]
 
 
@@ -91,7 +94,8 @@ def test_wgrad_splits_agree():
     assert_close(three, ref, odt, "three splits")
 
 
-FULL = ["L01_1x1_64-64_56", "L04_3x3_64_56", "L06_3x3s2_128_56-28", "L20_1x1_2048-512_7", "L21_3x3_512_7"]
+FULL = ["L01_1x1_64-64_56", "L03_1x1_256-64_56", "L04_3x3_64_56", "L06_3x3s2_128_56-28", "L20_1x1_2048-512_7",
+        "L21_3x3_512_7"]
 
 
 @pytest.mark.parametrize("name", FULL)

@@ -75,3 +75,21 @@ def test_no_192_channel_tiles_unless_asked(monkeypatch):
     monkeypatch.setenv("CDG_BN", "192")
     inf = cdg.plan_host(256, 7, 7, 512, 2048, 1, 1, 1, 0, 1, "bf16", num_sms=152).info()
     assert (inf["tile_n"], inf["cta_pair"], inf["work_items"]) == (192, 1, 147)
+
+
+def test_wgrad_x_major_rule():
+    """wgrad tiles are x-major exactly when the dY channels fill at most half
+    of a 128-row M tile (K <= 64), the filter is 1x1 and x has at least two
+    64-channel slices to pair; then N = 64 and M tiles = ceil(slices / 2)."""
+    for s in _shapes(300, seed=2029):
+        try:
+            w = cdg.wgrad_plan_host(*_args(s), out_f32=s["out_f32"], num_sms=SMS)
+        except cdg.CdgError:
+            continue
+        i = w.info()
+        units = s["R"] * s["S"] * -(-s["C"] // 64)
+        want = int(s["K"] <= 64 and s["R"] * s["S"] == 1 and units >= 2)
+        assert i["x_major"] == want, (s, i)
+        if want:
+            assert i["tile_n"] == 64 and i["taps_per_item"] == 1, (s, i)
+            assert i["work_items"] == i["splits"] * -(-units // 2), (s, i)
