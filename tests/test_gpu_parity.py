@@ -69,6 +69,7 @@ SWEEP = [
     _case(5, 3, 4, 16, 8, 3, 3, 1, 2, 1, "bf16"),           # dX smaller than the halo
     _case(1, 57, 3, 16, 16, 3, 1, 1, 1, 1, "f16"),          # tall and narrow
     _case(2, 16, 16, 8, 8, 7, 7, 2, 3, 1, "bf16", out="f32"),
+    _case(5, 14, 14, 64, 64, 1, 1, 2, 0, 1, "bf16"),  # three of four phases zero-filled, 7x7 sub-grids
 ]
 
 
