@@ -362,12 +362,26 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
     // 99.7 us with per-tap boxes (two MMA warps) against 110.9 with halo boxes,
     // so such plans take halo boxes only when asked (CDG_HALO=1).
     const bool xgate = h->mask && !h->mask_bits;
-    const bool halo_allowed = opt.halo != 0 && (!xgate || halo_forced);
+    // The exception: ReLU-gated stride-1 plans with 128-channel N tiles take
+    // halo boxes in CTA pairs, with weight halves resident or streamed
+    // (measured on GB300, x-gated 3x3 128 -> 128 at 28x28: 55.3 us against
+    // 65.1 with per-tap boxes and two MMA warps; at 64 channels 105.8 against
+    // 95.7, at 256 channels 52.9 against 52.2 (14x14) and 89.9 against 50.3
+    // (7x7)).  With GELU or SiLU backward, or the per-channel sums, the
+    // epilogue has the most work and issues the activation loads itself in a
+    // halo plan; those stay with per-tap boxes (the 28x28 layer: GELU 115.7
+    // against 131.1 us, SiLU 75.8 against 86.5, both sums 94 against 111).
+    const bool heavy_epi = (epilogue & (CDG_EPI_GELU_BWD | CDG_EPI_SILU_BWD | CDG_EPI_SUM | CDG_EPI_SUM_X)) != 0;
+    const bool xg_pair = xgate && !heavy_epi && !halo_forced && opt.halo != 0 && opt.pair != 0 && stride == 1 &&
+                         BN == 128 && pair_ok;
+    const bool halo_allowed = opt.halo != 0 && (!xgate || halo_forced || xg_pair);
     // attempts: resident halves in CTA pairs first where pairs may be taken,
-    // then a single CTA (forced pairs: the pair attempt only)
-    const int n_attempts = pair_forced ? 1 : (pair_auto ? 2 : 1);
+    // then a single CTA (forced pairs, and the gated pairs above: the pair
+    // attempt only)
+    const bool pair_only = pair_forced || xg_pair;
+    const int n_attempts = pair_only ? 1 : (pair_auto ? 2 : 1);
     for (int attempt = 0; attempt < n_attempts && !halo && !flat && halo_allowed; ++attempt) {
-        const bool pw = pair_forced || (pair_auto && attempt == 0);  // half of the weight rows per CTA
+        const bool pw = pair_only || (pair_auto && attempt == 0);  // half of the weight rows per CTA
         const int b_rows = pw ? BN / 2 : BN;  // weight rows one CTA holds
         int span_r = 0, span_s = 0, wt = 0, hmax = 0, maxtaps = 0;
         for (const CdgPhase &f : phases) {
@@ -416,7 +430,7 @@ int make_plan(int N, int H, int W, int C, int K, int R, int S, int stride, int p
         }
         // streamed weights only when asked (by default pairs only with resident
         // halves; a single CTA falls back to streamed weights only when asked)
-        const bool take = pw && !pair_forced ? res : (res || halo_forced);
+        const bool take = pw && !pair_only ? res : (res || halo_forced || xg_pair);
         if (hb <= 256 && bs >= (res ? 1 : 2) && take) {
             halo = true;
             halo_pair = pw;

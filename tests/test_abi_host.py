@@ -188,9 +188,19 @@ def test_halo_resident_weights_when_the_filter_fits(monkeypatch):
     # strided, or too large even as halves: per-tap boxes
     assert cdg.plan_host(256, 56, 56, 128, 128, 3, 3, 2, 1, 1, "bf16", num_sms=148).info()["a_mode"] == 0
     assert cdg.plan_host(256, 14, 14, 256, 256, 3, 3, 1, 1, 1, "bf16", num_sms=148).info()["a_mode"] == 0
-    # gated by the saved activation: four staging buffers leave no room for the halves
+    # gated by the saved activation: four staging buffers leave no room for the
+    # halves, so 128-channel tiles take halo pairs with streamed weight halves
+    # (one MMA warp); 64- and 256-channel tiles keep per-tap boxes
     gated = cdg.plan_host(256, 28, 28, 128, 128, 3, 3, 1, 1, 1, "bf16", relu=True, num_sms=148).info()
-    assert gated["a_mode"] == 0
+    assert (gated["a_mode"], gated["cta_pair"], gated["mma_warps"]) == (2, 1, 1)
+    for shape in [(256, 56, 56, 64, 64), (256, 14, 14, 256, 256), (256, 7, 7, 512, 512)]:
+        g = cdg.plan_host(*shape, 3, 3, 1, 1, 1, "bf16", relu=True, num_sms=148).info()
+        assert g["a_mode"] == 0, (shape, g)
+    g = cdg.plan_host(256, 28, 28, 128, 128, 3, 3, 1, 1, 1, "bf16", relu_bits=True, num_sms=148).info()
+    assert g["a_mode"] != 2  # the packed mask keeps the ungated rules
+    for kw in (dict(act="gelu"), dict(act="silu"), dict(sums=2)):  # heavier epilogues keep per-tap boxes
+        g = cdg.plan_host(256, 28, 28, 128, 128, 3, 3, 1, 1, 1, "bf16", relu=True, num_sms=148, **kw).info()
+        assert g["a_mode"] == 0, (kw, g)
     monkeypatch.setenv("CDG_PAIR", "0")
     assert cdg.plan_host(256, 28, 28, 128, 128, 3, 3, 1, 1, 1, "bf16", num_sms=148).info()["a_mode"] == 0
     monkeypatch.delenv("CDG_PAIR")

@@ -397,7 +397,21 @@ GATE_CASES = [
     (_case(4, 16, 16, 128, 256, 3, 3, 2, 1, 1, "bf16", relu=True, idx=20), "", {"mma_warps": 2}),
     (_case(2, 10, 10, 96, 48, 3, 3, 1, 1, 1, "f16", out="f32", relu=True, idx=21), "", {}),
     (_case(2, 9, 9, 64, 64, 1, 1, 1, 0, 1, "bf16", out="f32", relu=True, idx=22), "", {"a_mode": 1}),
+    # 128-channel stride-1 tiles gated by x: halo pairs, streamed weight halves
+    (_case(8, 14, 14, 128, 128, 3, 3, 1, 1, 1, "bf16", relu=True, idx=26), "CDG_MAX_GRID=4", {}),
 ]
+
+
+def test_gated_halo_pairs_by_default(monkeypatch):
+    """Gated by the saved activation, a stride-1 layer with 128-channel N
+    tiles runs halo boxes in CTA pairs with streamed weight halves (the
+    activation's staging buffers leave no room for resident halves), and
+    gives the oracle's result with several items per pair."""
+    monkeypatch.setenv("CDG_MAX_GRID", "4")
+    run, _, _ = check_layer(GATE_CASES[-1][0])
+    info = run.plan.info()
+    assert (info["a_mode"], info["cta_pair"], info["mma_warps"]) == (2, 1, 1), info
+    assert info["work_items"] >= 4 * (info["grid"] // 2)
 
 
 @pytest.mark.parametrize("gate", ["x", "bits"])
