@@ -402,13 +402,19 @@ GATE_CASES = [
 ]
 
 
-def test_gated_halo_pairs_by_default(monkeypatch):
+@pytest.mark.parametrize("L", [
+    GATE_CASES[-1][0],
+    _case(8, 14, 14, 128, 128, 3, 3, 1, 1, 1, "f16", out="f32", relu=True, idx=27),
+    _case(6, 15, 13, 128, 128, 3, 3, 1, 2, 2, "f16", relu=True, idx=28),  # dilation 2, ragged sub-grid
+], ids=lambda L: L.name)
+def test_gated_halo_pairs_by_default(L, monkeypatch):
     """Gated by the saved activation, a stride-1 layer with 128-channel N
     tiles runs halo boxes in CTA pairs with streamed weight halves (the
     activation's staging buffers leave no room for resident halves), and
-    gives the oracle's result with several items per pair."""
+    gives the oracle's result with several items per pair (fp16 and bf16,
+    16-bit and fp32 output, dilation 2)."""
     monkeypatch.setenv("CDG_MAX_GRID", "4")
-    run, _, _ = check_layer(GATE_CASES[-1][0])
+    run, _, _ = check_layer(L)
     info = run.plan.info()
     assert (info["a_mode"], info["cta_pair"], info["mma_warps"]) == (2, 1, 1), info
     assert info["work_items"] >= 4 * (info["grid"] // 2)
