@@ -35,7 +35,9 @@ the end-to-end uploads then include that input.
 --op wgrad times the weight gradient of the same 22 layers instead (per layer
 one split-K GEMM launch and one ordered-reduction launch; dY and the forward
 input resident), with per-layer tensor fractions; it prints its own JSON line
-(metric "wgrad TFLOP/s ...").
+(metric "wgrad TFLOP/s ...").  --op hbm measures the DRAM bandwidth of a
+write-only fill, a read-only sum and a copy (no dgrad), the ceilings the
+write-heavy layers run against.
 
 N > 1 (torchrun, one rank per GPU): every rank runs the full workload on its
 own GPU (replicas; dgrad has no exchange step), barrier + max over ranks.
@@ -774,6 +776,45 @@ def run_fused(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def run_hbm(args, rank, world, local_rank):
+    """DRAM bandwidth that the dgrad layers' byte mix can draw on: a
+    write-only fill, a read-only reduction and a 1:1 copy of 4 GiB buffers
+    (PyTorch's own kernels, no dgrad), each timed with CUDA events over
+    --steps launches after --warmup.  Layers whose bytes are mostly dX writes
+    are bounded by the fill's rate, not by the copy's."""
+    import torch
+    dev = torch.device("cuda", local_rank)
+    n = 4 << 30
+    a = torch.empty(n, dtype=torch.uint8, device=dev)
+    b = torch.empty(n, dtype=torch.uint8, device=dev)
+    a.fill_(1)
+    out = torch.empty((), dtype=torch.int64, device=dev)
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(args.steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / args.steps
+
+    av = a.view(torch.int64)
+    fill_ms = timed(lambda: b.fill_(7))
+    read_ms = timed(lambda: torch.sum(av, 0, dtype=torch.int64, out=out))
+    copy_ms = timed(lambda: b.copy_(a))
+    peaks = load_peaks()
+    rec = {"metric": "DRAM bandwidth: write-only fill, read-only sum, 1:1 copy (4 GiB each)", "unit": "GB/s",
+           "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "data": "synthetic",
+           "write_only_gbs": round(n / fill_ms / 1e6, 1), "read_only_gbs": round(n / read_ms / 1e6, 1),
+           "copy_gbs": round(2 * n / copy_ms / 1e6, 1), "measured_copy_peak_gbs": peaks["hbm_gbs"]}
+    if rank == 0:
+        print(json.dumps(rec), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -790,9 +831,10 @@ def main():
     ap.add_argument("--layers", default="", help="comma-separated layer names (default: all 22)")
     ap.add_argument("--autotune", type=int, default=0,
                     help="1: tune every layer's plan with cdg_autotune during set-up (untimed)")
-    ap.add_argument("--op", default="dgrad", choices=["dgrad", "wgrad", "fused"],
+    ap.add_argument("--op", default="dgrad", choices=["dgrad", "wgrad", "fused", "hbm"],
                     help="wgrad: time the weight gradient (split-K GEMM + ordered reduction) of the same layers; "
-                         "fused: time the back-to-back fused dgrad of ResNet-50 stage 1 alone")
+                         "fused: time the back-to-back fused dgrad of ResNet-50 stage 1 alone; "
+                         "hbm: DRAM bandwidth of a write-only fill, a read-only sum and a copy (no dgrad)")
     ap.add_argument("--gate", default="none", choices=["none", "x", "bits"],
                     help="fused ReLU-backward gate on every layer: none; x = the saved bf16 activation; "
                          "bits = its 1-bit packed mask (packed once at set-up, as a forward pass would store it)")
@@ -820,6 +862,9 @@ def main():
         return
     if args.op == "fused":
         run_fused(args, rank, world, local_rank)
+        return
+    if args.op == "hbm":
+        run_hbm(args, rank, world, local_rank)
         return
     dev = torch.device("cuda", local_rank)
     stream = torch.cuda.Stream(device=dev)
