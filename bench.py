@@ -26,7 +26,7 @@ resident in HBM.  Prints one JSON line:
                the fused ReLU-backward config, and each layer's weight prepack
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--gate none|x|bits] [--autotune 1] [--layers L01,...] [--op dgrad|wgrad|fused]
+                    [--gate none|x|bits] [--autotune 1] [--layers L01,...] [--op dgrad|wgrad|fused|hbm]
 
 --gate x|bits runs every layer with the fused ReLU-backward gate, reading the
 saved activation or its 1-bit packed mask; algorithmic bytes, the roofline and
