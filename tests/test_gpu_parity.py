@@ -70,6 +70,8 @@ SWEEP = [
     _case(1, 57, 3, 16, 16, 3, 1, 1, 1, 1, "f16"),          # tall and narrow
     _case(2, 16, 16, 8, 8, 7, 7, 2, 3, 1, "bf16", out="f32"),
     _case(5, 14, 14, 64, 64, 1, 1, 2, 0, 1, "bf16"),  # three of four phases zero-filled, 7x7 sub-grids
+    _case(1, 12, 20, 16, 16, 8, 16, 1, 4, 1, "bf16"),  # 128 taps, the most a filter may have
+    _case(2, 16, 24, 24, 16, 8, 16, 2, 4, 1, "f16"),   # 128 taps over four phases of 32
 ]
 
 
